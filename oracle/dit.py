@@ -1,0 +1,136 @@
+"""One DiT block stage of chunked autoregressive denoising, float64.
+
+Source: PhysisServe article (AREX feed, 2026-10-15), section on cutting the
+pipeline into "one block at one denoise step": each chunk starts from noise and
+runs several denoise steps; the next chunk does not wait for the previous one
+to finish, it reads the *noisy* KV that the earlier chunks left at the current
+step; a stage is one transformer block at one denoise step and the KV stays
+where it was produced.  Section on one GPU running several stages: tasks of
+different chunks on the same block are merged into one batch.
+
+Readings where the pages are silent (listed in the design notes):
+* Block (Wan/DiT style, adaLN): m = A[s] split into (shift1, scale1, gate1,
+  shift2, scale2, gate2), each of width D;
+  h  = x + gate1 * Attn(LN(x) (1 + scale1) + shift1)
+  x' = h + gate2 * (GELU_tanh(u W1) W2),  u = LN(h) (1 + scale2) + shift2.
+  Attention is full multi-head, no biases, RoPE (rotate-half, 1-D) on Q and K.
+* A[s] = SiLU(e(t_s)) Wmod + bmod with e(t) = SiLU(temb256(t) Wt1 + bt1) Wt2 + bt2,
+  t_s = s / S, shared by all blocks.
+* Ring: one ring of n_hist + 1 = 5 chunk slots per (stream, block, step);
+  chunk c lives in slot c mod 5.  Chunk c at step s attends to its own tokens
+  and to chunks c-1 .. c-n_hist (those >= 0) of the same stream at the same
+  step.  Token j of chunk c has RoPE position c * T_chunk + j.
+* A batched call first writes every chunk's own K/V into its slot, then runs
+  attention for every chunk.  Two chunks of one call may not share a
+  (stream, step, slot).
+"""
+import numpy as np
+
+from . import bf16
+from .ops import attention, gelu_tanh, layernorm, rope, silu, timestep_embedding
+
+
+def adaln_table(W, cfg):
+    """A[s] for s < S: float64 [S, 6D]."""
+    S, td = cfg["S"], cfg["t_dim"]
+    rows = []
+    for s in range(S):
+        e = silu(timestep_embedding(s / S, td) @ W["wt1"] + W["bt1"]) @ W["wt2"] + W["bt2"]
+        rows.append(silu(e) @ W["wmod"] + W["bmod"])
+    return np.stack(rows)
+
+
+def ring_slot(c: int, n_hist: int) -> int:
+    return c % (n_hist + 1)
+
+
+def history_chunks(c: int, n_hist: int) -> list:
+    """Earlier chunks visible to chunk c, oldest first."""
+    return [c - k for k in range(n_hist, 0, -1) if c - k >= 0]
+
+
+def positions(c: int, T: int) -> np.ndarray:
+    return c * T + np.arange(T)
+
+
+def _split6(a, D):
+    return [a[i * D:(i + 1) * D] for i in range(6)]
+
+
+def block_batch(xs, descs, ring, table, w, cfg):
+    """One DiT block for a batch of chunks.
+
+    xs[n, T, D] residual streams (fp32/fp64); descs: list of (stream, chunk, step);
+    ring: float64 [streams, S, n_hist+1, 2, T, D] for this block, modified in
+    place (own K/V written, bf16-rounded); table[S, 6D]; w: block weights
+    (float64).  Returns x'[n, T, D].
+    """
+    D, H, dh, T, nh = cfg["D"], cfg["H"], cfg["dh"], cfg["T_chunk"], cfg["n_hist"]
+    base, eps = cfg["rope_base"], cfg["eps"]
+    n = len(descs)
+    seen = set()
+    for (st, c, s) in descs:
+        key = (st, s, ring_slot(c, nh))
+        assert key not in seen, "two chunks of one call share a ring slot"
+        seen.add(key)
+    qs, mods = [], []
+    # phase 1: norm + modulation + QKV + RoPE; own K/V into the ring
+    for b, (st, c, s) in enumerate(descs):
+        sh1, sc1, g1, sh2, sc2, g2 = _split6(table[s], D)
+        mods.append((sh1, sc1, g1, sh2, sc2, g2))
+        u = layernorm(np.asarray(xs[b], np.float64), eps) * (1.0 + sc1) + sh1
+        pos = positions(c, T)
+        q = rope((u @ w["wq"]).reshape(T, H, dh), pos, base)
+        k = rope((u @ w["wk"]).reshape(T, H, dh), pos, base)
+        v = (u @ w["wv"]).reshape(T, H, dh)
+        ring[st, s, ring_slot(c, nh), 0] = bf16.round_rne(k.reshape(T, D))
+        ring[st, s, ring_slot(c, nh), 1] = bf16.round_rne(v.reshape(T, D))
+        qs.append(q)
+    # phase 2: attention over history + own, then the rest of the block
+    out = np.empty((n, T, D))
+    for b, (st, c, s) in enumerate(descs):
+        sh1, sc1, g1, sh2, sc2, g2 = mods[b]
+        chunks = history_chunks(c, nh) + [c]
+        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in chunks])
+        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in chunks])
+        o = attention(qs[b], K.reshape(-1, H, dh), V.reshape(-1, H, dh),
+                      1.0 / np.sqrt(dh)).reshape(T, D)
+        h = np.asarray(xs[b], np.float64) + g1 * (o @ w["wo"])
+        u2 = layernorm(h, eps) * (1.0 + sc2) + sh2
+        out[b] = h + g2 * (gelu_tanh(u2 @ w["w1"]) @ w["w2"])
+    return out
+
+
+def block_batch_rows(xs, descs, ring, table, w, cfg, rows):
+    """Same block, but only output rows ``rows`` (token indices) of every chunk.
+
+    K/V of every token are still computed (attention needs all of them); the
+    query-side work is done for the sampled rows only.  Returns x'[n, len(rows), D]
+    and updates ``ring`` like ``block_batch``.
+    """
+    D, H, dh, T, nh = cfg["D"], cfg["H"], cfg["dh"], cfg["T_chunk"], cfg["n_hist"]
+    base, eps = cfg["rope_base"], cfg["eps"]
+    rows = np.asarray(rows)
+    qs, mods = [], []
+    for b, (st, c, s) in enumerate(descs):
+        sh1, sc1, g1, sh2, sc2, g2 = _split6(table[s], D)
+        mods.append((sh1, sc1, g1, sh2, sc2, g2))
+        u = layernorm(np.asarray(xs[b], np.float64), eps) * (1.0 + sc1) + sh1
+        pos = positions(c, T)
+        k = rope((u @ w["wk"]).reshape(T, H, dh), pos, base)
+        v = (u @ w["wv"]).reshape(T, H, dh)
+        ring[st, s, ring_slot(c, nh), 0] = bf16.round_rne(k.reshape(T, D))
+        ring[st, s, ring_slot(c, nh), 1] = bf16.round_rne(v.reshape(T, D))
+        qs.append(rope((u[rows] @ w["wq"]).reshape(len(rows), H, dh), pos[rows], base))
+    out = np.empty((len(descs), len(rows), D))
+    for b, (st, c, s) in enumerate(descs):
+        sh1, sc1, g1, sh2, sc2, g2 = mods[b]
+        chunks = history_chunks(c, nh) + [c]
+        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in chunks])
+        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in chunks])
+        o = attention(qs[b], K.reshape(-1, H, dh), V.reshape(-1, H, dh),
+                      1.0 / np.sqrt(dh)).reshape(len(rows), D)
+        h = np.asarray(xs[b], np.float64)[rows] + g1 * (o @ w["wo"])
+        u2 = layernorm(h, eps) * (1.0 + sc2) + sh2
+        out[b] = h + g2 * (gelu_tanh(u2 @ w["w1"]) @ w["w2"])
+    return out

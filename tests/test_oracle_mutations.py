@@ -1,0 +1,106 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check a pin fails.
+
+Each mutation replaces one oracle function by a subtly wrong version (a wrong
+sign, a swapped pairing, a dropped term, an off-by-one) and runs the pin tests
+that should catch it.  A mutation no pin catches would mean the oracle is not
+pinned at that point.
+"""
+import numpy as np
+import pytest
+
+import oracle.ops as ops
+import oracle.dit as dit
+import oracle.pi0 as pi0
+import oracle.fold as fold
+import tests.test_oracle_pins as pins
+
+
+def _rope_wrong_sign(x, pos, base):
+    T, H, dh = x.shape
+    half = dh // 2
+    ang = ops.rope_angles(pos, dh, base)
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c + b * s, b * c - a * s], axis=-1)
+
+
+def _rope_interleaved(x, pos, base):
+    T, H, dh = x.shape
+    ang = ops.rope_angles(pos, dh, base)
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = b * c + a * s
+    return out
+
+
+def _attention_no_scale(q, k, v, scale):
+    return _orig_attention(q, k, v, 1.0)
+
+
+def _rmsnorm_var(x, eps):
+    return x / np.sqrt(np.var(x, axis=-1, keepdims=True) + eps)
+
+
+def _gelu_wrong_const(x):
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.0447 * x ** 3)))
+
+
+def _temb_swapped(t, d):
+    half = d // 2
+    w = 10000.0 ** (-np.arange(half, dtype=np.float64) / half)
+    a = 1000.0 * float(t) * w
+    return np.concatenate([np.cos(a), np.sin(a)])
+
+
+def _history_off_by_one(c, n_hist):
+    return [c - k for k in range(n_hist + 1, 0, -1) if c - k >= 0]
+
+
+def _fold_no_round(g, w):
+    return g[:, None] * w * (1 + 2.0 ** -7)
+
+
+def _times_wrong(cfg):
+    S = cfg["S"]
+    return [(s + 1) / S for s in range(S)]
+
+
+_orig_attention = ops.attention
+
+MUTATIONS = [
+    # (module, attribute, replacement, pins that must catch it)
+    ((ops, pi0, dit), "rope", _rope_wrong_sign, ["test_rope_hand_case", "test_rope_is_complex_rotation"]),
+    ((ops, pi0, dit), "rope", _rope_interleaved, ["test_rope_hand_case", "test_rope_is_complex_rotation"]),
+    ((ops, pi0, dit), "attention", _attention_no_scale, ["test_attention_brute_force"]),
+    ((ops, pi0), "rmsnorm", _rmsnorm_var, ["test_rmsnorm_closed_forms"]),
+    ((ops, pi0, dit), "gelu_tanh", _gelu_wrong_const, ["test_gelu_tanh_against_erf_gelu"]),
+    ((ops, pi0, dit, fold), "timestep_embedding", _temb_swapped, ["test_timestep_embedding_closed_forms"]),
+    ((dit,), "history_chunks", _history_off_by_one, ["test_ring_slot_matches_fifo_simulation"]),
+    ((fold, pi0), "fold_scale", _fold_no_round, ["test_rmsnorm_scale_fold_identity"]),
+    ((pi0,), "times", _times_wrong, ["test_time_grid"]),
+]
+
+
+def _run_pin(name):
+    fn = getattr(pins, name)
+    if name == "test_attention_brute_force":
+        fn(4, 1)
+    else:
+        fn()
+
+
+@pytest.mark.parametrize("mods,attr,repl,catchers", MUTATIONS,
+                         ids=[f"{m[1]}:{m[2].__name__}" for m in MUTATIONS])
+def test_mutation_is_caught(monkeypatch, mods, attr, repl, catchers):
+    for m in mods:
+        if hasattr(m, attr):
+            monkeypatch.setattr(m, attr, repl)
+    caught = False
+    for name in catchers:
+        try:
+            _run_pin(name)
+        except AssertionError:
+            caught = True
+    assert caught, f"mutation {repl.__name__} of {attr} not caught by {catchers}"

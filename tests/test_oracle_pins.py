@@ -1,0 +1,397 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU).
+
+Each test checks the oracle against something it does not compute itself: a
+library routine, a closed form, an invariant of the mathematics, brute force on
+tiny inputs, or a special case whose answer is known.  Together they are meant
+to catch a dropped term, a wrong sign or index, or a transposed operand
+anywhere in ``oracle/``.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from latency_transformer_block_gb300 import synth
+from oracle import bf16, dit, fold, ops, pi0
+
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------------------
+# bf16 storage
+# ----------------------------------------------------------------------------
+def test_bf16_round_matches_torch_conversion():
+    x = (RNG.standard_normal(200_000) * np.exp(RNG.uniform(-20, 20, 200_000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(bf16.round_rne(x.astype(np.float64)), ref)
+    ref_bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bf16.encode(x.astype(np.float64)), ref_bits)
+
+
+def test_bf16_ties_to_even_and_decode():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to the even mantissa (1.0)
+    assert bf16.round_rne(np.array([1 + 2.0 ** -8]))[0] == 1.0
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 (odd) and 1 + 2^-6 (even)
+    assert bf16.round_rne(np.array([1 + 3 * 2.0 ** -8]))[0] == 1 + 2.0 ** -6
+    assert bf16.round_rne(np.array([-(1 + 3 * 2.0 ** -8)]))[0] == -(1 + 2.0 ** -6)
+    bits = np.array([0x3F80, 0xC000, 0x3E80, 0x0000], dtype=np.uint16)
+    assert list(bf16.decode(bits)) == [1.0, -2.0, 0.25, 0.0]
+    assert bf16.ulp(np.array([1.0]))[0] == 2.0 ** -7
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+def _attention_loops(q, k, v, scale):
+    """Brute force with Python loops and math.exp."""
+    Tq, Hq, dh = q.shape
+    Tk, Hkv, _ = k.shape
+    group = Hq // Hkv
+    out = np.zeros((Tq, Hq, v.shape[2]))
+    for i in range(Tq):
+        for h in range(Hq):
+            j = h // group
+            s = [sum(q[i, h, d] * k[t, j, d] for d in range(dh)) * scale for t in range(Tk)]
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            z = sum(e)
+            for d in range(v.shape[2]):
+                out[i, h, d] = sum(e[t] * v[t, j, d] for t in range(Tk)) / z
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 1), (2, 2), (4, 2)])
+def test_attention_brute_force(Hq, Hkv):
+    q = RNG.standard_normal((5, Hq, 4))
+    k = RNG.standard_normal((7, Hkv, 4))
+    v = RNG.standard_normal((7, Hkv, 3))
+    got = ops.attention(q, k, v, 0.5)
+    assert np.allclose(got, _attention_loops(q, k, v, 0.5), rtol=1e-13, atol=1e-14)
+
+
+def test_attention_special_cases():
+    q = RNG.standard_normal((6, 2, 8))
+    v = RNG.standard_normal((9, 1, 8))
+    k_same = np.repeat(RNG.standard_normal((1, 1, 8)), 9, axis=0)
+    # all keys equal -> output is the mean of V
+    got = ops.attention(q, k_same, v, 0.3)
+    assert np.allclose(got, np.broadcast_to(v.mean(axis=0), got.shape), atol=1e-14)
+    # a single key -> output is that V row
+    got1 = ops.attention(q, k_same[:1], v[:1], 0.3)
+    assert np.allclose(got1, np.broadcast_to(v[0], got1.shape), atol=1e-15)
+    # adding one vector to every key shifts each query's scores by a constant
+    k = RNG.standard_normal((9, 1, 8))
+    delta = RNG.standard_normal((1, 1, 8)) * 3
+    assert np.allclose(ops.attention(q, k, v, 0.3), ops.attention(q, k + delta, v, 0.3),
+                       rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# norms
+# ----------------------------------------------------------------------------
+def test_rmsnorm_closed_forms():
+    eps = 1e-6
+    for c in (3.0, -0.5, 1e-4):
+        x = np.full((1, 16), c)
+        assert np.allclose(ops.rmsnorm(x, eps), c / np.sqrt(c * c + eps), rtol=1e-15)
+    x = RNG.standard_normal((4, 64))
+    y = ops.rmsnorm(x, 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-14)
+    assert np.allclose(ops.rmsnorm(7.0 * x, 0.0), y, rtol=1e-14)  # scale invariance
+    ms = np.mean(x * x, axis=-1)
+    y = ops.rmsnorm(x, eps)
+    assert np.allclose(np.mean(y * y, axis=-1), ms / (ms + eps), rtol=1e-13)
+
+
+def test_layernorm_closed_forms():
+    eps = 1e-6
+    x = RNG.standard_normal((5, 128)) * 3 + 2
+    y = ops.layernorm(x, eps)
+    var = x.var(axis=-1)
+    assert np.allclose(y.mean(axis=-1), 0.0, atol=1e-14)
+    assert np.allclose(y.var(axis=-1), var / (var + eps), rtol=1e-13)
+    assert np.allclose(ops.layernorm(x + 11.0, eps), y, rtol=1e-10, atol=1e-12)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (128,), eps=eps).numpy()
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# RoPE
+# ----------------------------------------------------------------------------
+def test_rope_hand_case():
+    # dh = 4: pairs (0, 2) with theta 1 and (1, 3) with theta 1e4**-0.5 = 0.01
+    x = np.zeros((1, 1, 4)); x[0, 0, 0] = 1.0
+    y = ops.rope(x, np.array([1]), 10000.0)
+    assert np.allclose(y[0, 0], [math.cos(1.0), 0.0, math.sin(1.0), 0.0], atol=1e-16)
+    x = np.zeros((1, 1, 4)); x[0, 0, 3] = 1.0
+    y = ops.rope(x, np.array([2]), 10000.0)
+    assert np.allclose(y[0, 0], [0.0, -math.sin(0.02), 0.0, math.cos(0.02)], atol=1e-16)
+
+
+def test_rope_is_complex_rotation():
+    dh, base = 64, 10000.0
+    x = RNG.standard_normal((9, 3, dh))
+    pos = RNG.integers(0, 200_000, 9)
+    z = x[..., : dh // 2] + 1j * x[..., dh // 2:]
+    theta = base ** (-np.arange(dh // 2) * 2.0 / dh)
+    zr = z * np.exp(1j * pos[:, None, None] * theta[None, None, :])
+    y = ops.rope(x, pos, base)
+    assert np.allclose(y[..., : dh // 2], zr.real, rtol=1e-11, atol=1e-11)
+    assert np.allclose(y[..., dh // 2:], zr.imag, rtol=1e-11, atol=1e-11)
+
+
+def test_rope_invariants():
+    dh = 32
+    q = RNG.standard_normal((1, 1, dh))
+    k = RNG.standard_normal((1, 1, dh))
+    assert np.array_equal(ops.rope(q, np.array([0]), 1e4), q)
+    assert np.isclose(np.linalg.norm(ops.rope(q, np.array([77]), 1e4)), np.linalg.norm(q))
+
+    def dot(m, n):
+        return float(np.sum(ops.rope(q, np.array([m]), 1e4) * ops.rope(k, np.array([n]), 1e4)))
+
+    assert np.isclose(dot(5, 3), dot(105, 103), rtol=1e-11)
+    assert np.isclose(dot(0, 9), dot(600, 609), rtol=1e-11)
+
+
+# ----------------------------------------------------------------------------
+# activations and timestep embedding
+# ----------------------------------------------------------------------------
+def test_gelu_tanh_against_erf_gelu():
+    x = np.linspace(-8, 8, 20001)
+    erf_gelu = 0.5 * x * (1 + np.array([math.erf(v / math.sqrt(2)) for v in x]))
+    dev = np.max(np.abs(ops.gelu_tanh(x) - erf_gelu))
+    assert dev < 5e-4  # the tanh form's known max deviation is about 4.7e-4 (|x| ~ 2.1)
+    assert ops.gelu_tanh(np.array([0.0]))[0] == 0.0
+    assert np.isclose(ops.gelu_tanh(np.array([12.0]))[0], 12.0)
+    assert abs(ops.gelu_tanh(np.array([-12.0]))[0]) < 1e-12
+    tg = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    assert np.allclose(ops.gelu_tanh(x), tg, rtol=1e-12, atol=1e-13)
+
+
+def test_silu_library():
+    x = np.linspace(-30, 30, 1001)
+    assert np.allclose(ops.silu(x), torch.nn.functional.silu(torch.from_numpy(x)).numpy(),
+                       rtol=1e-13, atol=1e-15)
+
+
+def test_timestep_embedding_closed_forms():
+    e0 = ops.timestep_embedding(0.0, 8)
+    assert np.array_equal(e0, [0, 0, 0, 0, 1, 1, 1, 1])
+    e = ops.timestep_embedding(0.25, 8)
+    w = 10000.0 ** (-np.arange(4) / 4)
+    assert np.isclose(e[0], math.sin(250.0))           # lowest index: frequency 1
+    assert np.isclose(e[3], math.sin(250.0 * w[3]))
+    assert np.isclose(e[7], math.cos(250.0 * w[3]))
+    assert np.allclose(e[:4] ** 2 + e[4:] ** 2, 1.0)
+
+
+# ----------------------------------------------------------------------------
+# folds (section 4 of the reading note)
+# ----------------------------------------------------------------------------
+def _tiny_cfg():
+    return synth.config("tiny", D=32, Hq=2, Hkv=1, dh=16, F=48, T_prefix=8, T_q=6, act_dim=4)
+
+
+def _tiny_pi0(seed=3):
+    cfg = _tiny_cfg()
+    wb = synth.pi0_weights(cfg, seed)
+    ib = synth.pi0_inputs(cfg, seed)
+    return cfg, wb, ib
+
+
+def test_rmsnorm_scale_fold_identity():
+    cfg, wb, ib = _tiny_pi0()
+    blk = pi0.decode_tree(wb["blocks"][0])
+    kv = bf16.decode(ib["kv"][0])
+    x = RNG.standard_normal((cfg["T_q"], cfg["D"]))
+    pos = cfg["T_prefix"] + np.arange(cfg["T_q"])
+    Tp = cfg["T_prefix"]
+    unfused, _, _ = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, blk, cfg)
+    exact = dict(blk)
+    one = np.ones(cfg["D"])
+    exact.update(g_attn=one, g_ffn=one,
+                 wq=fold.fold_scale_exact(blk["g_attn"], blk["wq"]),
+                 wk=fold.fold_scale_exact(blk["g_attn"], blk["wk"]),
+                 wv=fold.fold_scale_exact(blk["g_attn"], blk["wv"]),
+                 wg=fold.fold_scale_exact(blk["g_ffn"], blk["wg"]),
+                 wu=fold.fold_scale_exact(blk["g_ffn"], blk["wu"]))
+    folded, _, _ = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, exact, cfg)
+    # the cache write rounds K/V to bf16 and both sides see the same rounding
+    # unless a value sits on a tie; compare on the residual stream
+    assert np.allclose(folded, unfused, rtol=1e-12, atol=1e-12)
+    # the stored fold is the exact product rounded once to bf16
+    st = fold.fold_scale(blk["g_attn"], blk["wq"])
+    ex = fold.fold_scale_exact(blk["g_attn"], blk["wq"])
+    assert np.all(np.abs(st - ex) <= 2.0 ** -8 * np.abs(ex))
+    assert np.array_equal(st, bf16.round_rne(ex))
+
+
+def test_merged_qkv_equals_separate():
+    cfg, wb, _ = _tiny_pi0()
+    w = pi0.method_block(pi0.decode_tree(wb["blocks"][0]))
+    x = RNG.standard_normal((cfg["T_q"], cfg["D"]))
+    q, k, v = pi0.qkv(x, w, cfg)
+    xn = ops.rmsnorm(x, cfg["eps"])
+    assert np.allclose(q.reshape(len(x), -1), xn @ w["wq"], rtol=1e-14, atol=1e-15)
+    assert np.allclose(k.reshape(len(x), -1), xn @ w["wk"], rtol=1e-14, atol=1e-15)
+    assert np.allclose(v.reshape(len(x), -1), xn @ w["wv"], rtol=1e-14, atol=1e-15)
+
+
+def test_time_embedding_fold():
+    cfg, wb, ib = _tiny_pi0()
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    w_fold, table = pi0.fold_tables(wb, cfg)
+    x = np.asarray(ib["noise"], np.float64)
+    for s, t in enumerate(pi0.times(cfg)):
+        a = pi0.embed(x, t, W, cfg["D"])
+        b = pi0.embed_folded(x, s, w_fold, table, W)
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# Euler integration and block wiring
+# ----------------------------------------------------------------------------
+def test_time_grid():
+    assert pi0.times(synth.config("pi0_ae")) == [s / 10 for s in range(10)]
+
+
+def test_constant_velocity_field_integrates_exactly():
+    """W_out = 0, b_out = c  =>  v = c at every step  =>  x_S = x_0 + S dt c = x_0 + c."""
+    cfg, wb, ib = _tiny_pi0()
+    cfg = dict(cfg, S=5)
+    wb = dict(wb)
+    wb["w_out"] = np.zeros_like(wb["w_out"])
+    c = bf16.round_rne(RNG.standard_normal(cfg["act_dim"]))
+    wb["b_out"] = bf16.encode(c)
+    x, _ = pi0.denoise(ib["noise"], ib["state"], ib["kv"], wb, cfg)
+    assert np.allclose(x, ib["noise"] + c[None, :], rtol=0, atol=1e-14)
+
+
+def test_linear_velocity_euler_closed_form():
+    """x_{s+1} = x_s + dt (a x_s + c) has x_S = (1+a dt)^S x0 + c dt sum_k (1+a dt)^k."""
+    a, c, S = -0.7, 0.3, 10
+    dt = 1.0 / S
+    x0 = RNG.standard_normal(5)
+    x = x0.copy()
+    for _ in range(S):
+        x = x + dt * (a * x + c)
+    r = 1 + a * dt
+    assert np.allclose(x, r ** S * x0 + c * dt * sum(r ** k for k in range(S)), rtol=1e-14)
+
+
+def test_block_identity_and_wiring():
+    cfg, wb, ib = _tiny_pi0()
+    blk = pi0.decode_tree(wb["blocks"][0])
+    Tp, T = cfg["T_prefix"], cfg["T_q"]
+    kv = bf16.decode(ib["kv"][0])
+    x = RNG.standard_normal((T, cfg["D"]))
+    pos = Tp + np.arange(T)
+    zero = dict(blk, wo=np.zeros_like(blk["wo"]), wd=np.zeros_like(blk["wd"]))
+    y, k_own, v_own = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, zero, cfg)
+    assert np.array_equal(y, x)
+    # q = 0 -> uniform attention over [prefix | own]: o = mean of all V rows
+    unif = dict(blk, wq=np.zeros_like(blk["wq"]), wd=np.zeros_like(blk["wd"]))
+    y, k_own, v_own = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, unif, cfg)
+    vmean = np.concatenate([kv[1, :Tp], v_own]).mean(axis=0)            # [Hkv*dh]
+    o = np.tile(vmean, cfg["Hq"] // cfg["Hkv"])                          # every q head
+    assert np.allclose(y, x + o[None, :] @ blk["wo"], rtol=1e-12, atol=1e-13)
+    # own V is the bf16 of the projected (un-rotated) values
+    xn = ops.rmsnorm(x, cfg["eps"]) * blk["g_attn"]
+    assert np.array_equal(v_own, bf16.round_rne(xn @ blk["wv"]))
+    # with attention removed the FFN sees the *normed* residual (pre-norm)
+    noatt = dict(blk, wo=np.zeros_like(blk["wo"]))
+    y, _, _ = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, noatt, cfg)
+    hn = ops.rmsnorm(x, cfg["eps"]) * blk["g_ffn"]
+    ffn = (ops.gelu_tanh(hn @ blk["wg"]) * (hn @ blk["wu"])) @ blk["wd"]
+    assert np.allclose(y, x + ffn, rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_last_layer_skip_leaves_kv_unchanged():
+    cfg = synth.config("prefill", D=32, Hq=2, Hkv=1, dh=16, F=48, L=3, T_prefix=8,
+                       T_q=4, patch_dim=12)
+    wb = synth.prefill_weights(cfg, 5)
+    pe = synth.prefill_inputs(cfg, 2, 5)["patch_emb"]
+    a = pi0.prefill(pe, wb, cfg, skip_last=True)
+    b = pi0.prefill(pe, wb, cfg, skip_last=False)
+    assert np.array_equal(a, b)
+    assert not np.any(a[:, :, :, cfg["T_prefix"]:])   # own-token slots untouched
+    # batch elements are independent
+    a1 = pi0.prefill(pe[1:2], wb, cfg)
+    assert np.array_equal(a[:, 1:2], a1)
+
+
+# ----------------------------------------------------------------------------
+# DiT stage: ring, batching, adaLN wiring
+# ----------------------------------------------------------------------------
+def test_ring_slot_matches_fifo_simulation():
+    nh = 4
+    slots = [None] * (nh + 1)      # slot -> chunk living there
+    where = {}
+    for c in range(40):
+        if c >= nh + 1:            # the chunk that leaves the window frees its slot
+            free = where.pop(c - nh - 1)
+        else:
+            free = slots.index(None)
+        slots[free] = c
+        where[c] = free
+        assert free == dit.ring_slot(c, nh)
+        visible = sorted(ch for ch in slots if ch is not None and ch != c)
+        assert visible == dit.history_chunks(c, nh)
+    assert list(dit.positions(3, 1560)[[0, -1]]) == [4680, 6239]
+
+
+def _tiny_dit(seed=2):
+    cfg = synth.config("dit_1p3b", D=32, H=2, dh=16, F=40, L=1, T_chunk=6, t_dim=16)
+    wb = synth.dit_weights(cfg, seed)
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    w = pi0.decode_tree(wb["blocks"][0])
+    table = dit.adaln_table(W, cfg)
+    ring = bf16.decode(synth.dit_ring(cfg, seed, streams=2))[:, 0]
+    return cfg, w, W, table, ring
+
+
+def test_dit_batch_equals_separate_calls():
+    cfg, w, _, table, ring = _tiny_dit()
+    descs = [(0, 9, 0), (0, 8, 1), (0, 7, 2), (1, 2, 3)]
+    xs = synth.dit_latents(cfg, len(descs), 4)
+    r_batch = ring.copy()
+    out = dit.block_batch(xs, descs, r_batch, table, w, cfg)
+    r_sep = ring.copy()
+    for b, d in enumerate(descs):
+        ob = dit.block_batch(xs[b:b + 1], [d], r_sep, table, w, cfg)
+        assert np.array_equal(ob[0], out[b])
+    assert np.array_equal(r_sep, r_batch)
+    rows = [0, 3, 5]
+    r_rows = ring.copy()
+    part = dit.block_batch_rows(xs, descs, r_rows, table, w, cfg, rows)
+    assert np.allclose(part, out[:, rows], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(r_rows, r_batch)
+
+
+def test_dit_zero_gates_is_identity_and_history_set():
+    cfg, w, W, table, ring = _tiny_dit()
+    D = cfg["D"]
+    W0 = dict(W, wmod=np.zeros_like(W["wmod"]))
+    bm = RNG.standard_normal(6 * D)
+    bm[2 * D:3 * D] = 0.0          # gate1
+    bm[5 * D:6 * D] = 0.0          # gate2
+    W0["bmod"] = bm
+    t0 = dit.adaln_table(W0, cfg)
+    assert np.allclose(t0, bm[None, :])
+    xs = synth.dit_latents(cfg, 1, 8)
+    out = dit.block_batch(xs, [(0, 6, 1)], ring.copy(), t0, w, cfg)
+    assert np.array_equal(out[0], xs[0].astype(np.float64))
+    # q = 0 -> uniform attention: o = mean of V over history chunks + own chunk
+    bm2 = RNG.standard_normal(6 * D) * 0.1
+    t2 = np.broadcast_to(bm2, (cfg["S"], 6 * D)).copy()
+    wz = dict(w, wq=np.zeros_like(w["wq"]), w2=np.zeros_like(w["w2"]))
+    for c in (0, 2, 9):
+        r = ring.copy()
+        out = dit.block_batch(xs, [(0, c, 1)], r, t2, wz, cfg)
+        chunks = [cc for cc in range(c - 4, c + 1) if cc >= 0]
+        V = np.concatenate([r[0, 1, cc % 5, 1] for cc in chunks])
+        o = V.mean(axis=0)
+        expect = xs[0] + bm2[2 * D:3 * D] * (o[None, :] @ w["wo"])
+        assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
