@@ -1,0 +1,342 @@
+"""Benchmark of the pi0 action-expert denoise chunk (18 blocks x 10 Euler steps,
+64 query tokens over a 512-token prefix KV) on one GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one lat_denoise_chunk (the whole hot path: state token, 10 x
+[embedding, 18 x block, head + Euler]).  The metric is milliseconds per
+denoised chunk (lower is better); microseconds per block and tokens/s are
+reported alongside.  Every step streams all 623 MB of folded block weights
+from HBM (L2 is 129 MB), so no flush is needed between steps.
+
+--impl reference times the CPU oracle (float64 numpy) on the same workload on
+the host cores; under torchrun only rank 0 runs it.
+Multi-GPU: replicas only (one independent chunk per GPU per step, no
+collective on the data path); value = whole-job chunks per step time.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "pi0_ae"
+PAGES_AE_MS = 11.001   # pages' action-expert time, 2 views, RTX 4090 (context)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def aggregate(elapsed_ms, units_per_rank, world, reduce_max):
+    """Whole-job numbers: max time over ranks, units summed over ranks."""
+    t = reduce_max(elapsed_ms)
+    return t, units_per_rank * world
+
+
+def algorithmic_bytes(cfg):
+    """Bytes per block-step and per chunk (weights read once + KV read once)."""
+    D, F, Hq, Hkv, dh, L, S = cfg["D"], cfg["F"], cfg["Hq"], cfg["Hkv"], cfg["dh"], cfg["L"], cfg["S"]
+    Tkv = cfg["T_prefix"] + cfg["T_q"]
+    w_block = 2 * (D * (Hq + 2 * Hkv) * dh + Hq * dh * D + D * 2 * F + F * D)
+    kv_block = 2 * 2 * Tkv * Hkv * dh
+    A = cfg["act_dim"]
+    per_step_extra = 2 * D * D + 4 * (A * D + D * A)          # W2 (bf16), W' and W_out (fp32)
+    return w_block, kv_block, L * S * (w_block + kv_block) + S * per_step_extra
+
+
+def macs(cfg):
+    D, F, Hq, Hkv, dh, L, S, T = cfg["D"], cfg["F"], cfg["Hq"], cfg["Hkv"], cfg["dh"], cfg["L"], cfg["S"], cfg["T_q"]
+    Tkv = cfg["T_prefix"] + T
+    per_block = T * (D * (Hq + 2 * Hkv) * dh + Hq * dh * D + D * 2 * F + F * D) + 2 * T * Hq * Tkv * dh
+    return per_block, per_block * L * S
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def cpu_baseline(cfg, wb, ib):
+    """The oracle as it stands, one full denoised chunk on the host cores."""
+    from oracle import pi0
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    blocks = [pi0.method_block(pi0.decode_tree(b)) for b in wb["blocks"]]
+    t0 = time.perf_counter()
+    pi0.denoise(ib["noise"], ib["state"], ib["kv"], wb, cfg, blocks=blocks)
+    ms = (time.perf_counter() - t0) * 1e3
+    return {"value": round(ms, 3), "unit": "ms", "cores": cores, "kind": "oracle",
+            "sample": "one full chunk (18 blocks x 10 steps), float64 numpy, weights pre-decoded"}
+
+
+def run_reference(args):
+    rank, _, world = dist_info()
+    if rank != 0:
+        return
+    from latency_transformer_block_gb300 import synth
+    from oracle import pi0
+    cfg = synth.config(WORKLOAD)
+    wb = synth.pi0_weights(cfg, 0)
+    ib = synth.pi0_inputs(cfg, 0)
+    # one step = one block at one denoise step (a bounded sample); scaled to a chunk
+    blk = pi0.method_block(pi0.decode_tree(wb["blocks"][0]))
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    from oracle import bf16
+    kv = bf16.decode(ib["kv"][0])
+    Tp, Tq = cfg["T_prefix"], cfg["T_q"]
+    pos = Tp + np.arange(Tq)
+    x = ib["noise"].astype(np.float64)
+    st = pi0.state_token(ib["state"].astype(np.float64), W)
+    h = np.vstack([st[None, :], pi0.embed(x, 0.0, W, cfg["D"])])
+
+    def one():
+        pi0.block(h, kv[0, :Tp], kv[1, :Tp], pos, blk, cfg)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    per_block = (time.perf_counter() - t0) * 1e3 / args.steps
+    t1 = time.perf_counter()
+    for _ in range(3):
+        pi0.embed(x, 0.0, W, cfg["D"])
+        pi0.head(h[1:], W, cfg["eps"])
+    per_embed_head = (time.perf_counter() - t1) * 1e3 / 3
+    value = per_block * cfg["L"] * cfg["S"] + per_embed_head * cfg["S"]
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    line = {
+        "impl": "reference", "metric": "ms per denoised chunk", "value": round(value, 3), "unit": "ms",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) bf16 weights)",
+        "config": {"workload": WORKLOAD, "blocks": cfg["L"], "steps": cfg["S"], "tokens": cfg["T_q"],
+                   "prefix_kv": cfg["T_prefix"], "us_per_block": round(per_block * 1e3, 1)},
+        "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} timed block-steps (block 0, step 0) + embedding/head, "
+                                   f"scaled x{cfg['L'] * cfg['S']} to one chunk"},
+        "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, local_rank, world = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from latency_transformer_block_gb300 import build as B
+    B.build()
+    from latency_transformer_block_gb300 import synth
+    from latency_transformer_block_gb300.models import Pi0ActionExpert
+
+    cfg = synth.config(WORKLOAD)
+    wb = synth.pi0_weights(cfg, 0)
+    ib = synth.pi0_inputs(cfg, 0)
+    m = Pi0ActionExpert(cfg, wb, device=dev)
+    kv = m.kv_from_bits(ib["kv"])
+    state = torch.from_numpy(ib["state"]).to(dev)
+    noise = torch.from_numpy(ib["noise"]).to(dev)
+    x = noise.clone()
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        x.copy_(noise, non_blocking=True)
+        m.denoise(kv, state, x, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    m.ctx.sync()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def reduce_max(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    m.ctx.sync()
+    elapsed = e0.elapsed_time(e1)
+    t_max, chunks = aggregate(elapsed, args.steps, world, reduce_max)
+    ms_per_step = t_max / args.steps
+    value = ms_per_step / world if world > 1 else ms_per_step   # whole-job time per chunk
+
+    # --- end to end through the C ABI with host buffers (pinned), copies timed ---
+    h_noise = torch.from_numpy(ib["noise"]).pin_memory()
+    h_state = torch.from_numpy(ib["state"]).pin_memory()
+    h_out = torch.empty_like(h_noise).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x.copy_(h_noise, non_blocking=True)
+            state.copy_(h_state, non_blocking=True)
+            m.denoise(kv, state, x, stream)
+            h_out.copy_(x, non_blocking=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        ee0, ee1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ee0.record(stream)
+        for _ in range(args.steps):
+            x.copy_(h_noise, non_blocking=True)
+            state.copy_(h_state, non_blocking=True)
+            m.denoise(kv, state, x, stream)
+            h_out.copy_(x, non_blocking=True)
+        ee1.record(stream)
+        stream.synchronize()
+        host_ms = (time.perf_counter() - t0) * 1e3
+    e2e_ms = reduce_max(max(ee0.elapsed_time(ee1), host_ms)) / args.steps
+
+    # --- dominant kernel alone: the weight-streaming GEMM, gate/up projection ---
+    peak_gbs, peak_tf, peak_src = measured_peaks()
+    F, D = cfg["F"], cfg["D"]
+    kernels = {}
+    names = {0: ("qkv", D * (cfg["Hq"] + 2 * cfg["Hkv"]) * cfg["dh"]), 1: ("o", cfg["Hq"] * cfg["dh"] * D),
+             2: ("gate_up", D * 2 * F), 3: ("down", F * D)}
+    reps = 50
+    with torch.cuda.stream(stream):
+        for which, (nm, nw) in names.items():
+            m.ctx.debug_gemm(which, 0, 5, stream)
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for l in range(reps):
+                m.ctx.debug_gemm(which, l % cfg["L"], 1, stream)
+            k1.record(stream)
+            stream.synchronize()
+            us = k0.elapsed_time(k1) * 1e3 / reps
+            kernels[nm] = {"us": round(us, 2), "weight_bytes": 2 * nw, "gbs": round(2 * nw / us / 1e3, 1)}
+    m.ctx.sync()
+    dom = kernels["gate_up"]
+    w_block, kv_block, bytes_chunk = algorithmic_bytes(cfg)
+    mac_block, mac_chunk = macs(cfg)
+    path_gbs = bytes_chunk / (ms_per_step * 1e-3) / 1e9
+    nsplit = (cfg["T_prefix"] + cfg["T_q"] + 63) // 64
+    launches_per_chunk = 1 + cfg["S"] * (3 + cfg["L"] * (6 + (1 if nsplit > 1 else 0)))
+
+    line = {
+        "metric": "ms per denoised chunk", "value": round(value, 4), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": round(value / PAGES_AE_MS, 4), "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs and prefix KV, N(0,0.02) bf16 weights)",
+        "config": {"workload": WORKLOAD, "blocks": cfg["L"], "steps": cfg["S"], "tokens": cfg["T_q"],
+                   "prefix_kv": cfg["T_prefix"], "width": cfg["D"], "ffn": cfg["F"],
+                   "us_per_block": round(ms_per_step * 1e3 / (cfg["L"] * cfg["S"]), 3),
+                   "tokens_per_s": round(cfg["T_q"] * 1e3 / ms_per_step, 1),
+                   "l2": "inputs larger than L2: 623 MB of block weights streamed per step",
+                   "path_roofline_ms": round(bytes_chunk / (peak_gbs * 1e9) * 1e3, 4),
+                   "path_hbm_gbs": round(path_gbs, 1), "path_frac": round(path_gbs / peak_gbs, 4),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "skinny_gemm (gate/up projection, 64 tokens x 1024 -> 8192)",
+                     "achieved": dom["gbs"], "peak": peak_gbs, "unit": "GB/s",
+                     "frac": round(dom["gbs"] / peak_gbs, 4), "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (burst copy)", "kernels": kernels},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_ms, 4), "unit": "ms",
+                "h2d_bytes_per_step": int(h_noise.numel() * 4 + h_state.numel() * 4),
+                "d2h_bytes_per_step": int(h_out.numel() * 4)},
+        "gpu_launches": launches_per_chunk * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, wb, ib)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

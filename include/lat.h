@@ -1,0 +1,230 @@
+/*
+ * lat.h -- C ABI of the low-latency transformer-block library (GB300, sm_103a).
+ *
+ * The hot path: a small chunk of query tokens runs through a stack of
+ * transformer blocks, attending to a cached prefix / history KV, and the stack
+ * is repeated over a fixed number of flow-matching (Euler) denoise steps.  Two
+ * model families take this path:
+ *
+ *  - LAT_PI0_ACTION_EXPERT: the pi0 action expert ("Running VLAs at Real-time
+ *    Speed", reading note on arXiv 2510.26742, section 2 and Fig. 4): 63 action
+ *    tokens + 1 state token over a per-layer prefix KV of 512 vision tokens,
+ *    18 blocks x 10 Euler steps.  RMSNorm with its scale folded into the next
+ *    weight (section 4.1), folded action/time embedding with a precomputed time
+ *    table (section 4.2), merged QKV with RoPE (section 4.3), gated FFN
+ *    (section 5).
+ *  - LAT_PI0_PREFIX: the prefix model whose per-layer K/V is that cache; the
+ *    last layer stops after K and V (section 4.3).
+ *  - LAT_DIT: one DiT block stage of chunked autoregressive denoising
+ *    (PhysisServe article, sections on pipelining by "one block at one denoise
+ *    step" and on batching chunks of one block): a chunk attends to its own
+ *    tokens and to the noisy KV that the previous chunks left at the same
+ *    denoise step; LayerNorm + adaLN shift/scale/gate, GELU-tanh FFN.
+ *
+ * Conventions for every call
+ *  - Pointers named "device" are CUDA device pointers owned by the caller; the
+ *    library borrows them for the duration of the work it enqueues.  Pointers
+ *    named "host" are read before the call returns.
+ *  - All device pointers must be 16-byte aligned (LAT_ERR_ALIGN otherwise).
+ *  - bf16 = IEEE bfloat16 bit patterns; fp32 = IEEE float.
+ *  - Weight matrices passed to lat_create use the math convention y = x W:
+ *    bf16 [K_in][N_out], row-major.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously; argument errors are detected on the host
+ *    and returned before anything is enqueued.  A device-side wait that gives
+ *    up (bounded spin) records LAT_ERR_TIMEOUT in the context; it is returned
+ *    by lat_sync() and by the next call on that context.
+ *  - No call allocates device memory except lat_create (weights, tables,
+ *    workspace) and the first lat_denoise_chunk on a new set of buffer
+ *    addresses (graph instantiation).
+ *  - A context is not thread-safe: calls on one context must be serialised by
+ *    the caller and enqueued on one stream at a time.
+ */
+#ifndef LAT_H
+#define LAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LAT_OK = 0,
+  LAT_ERR_ARG = 1,        /* null pointer, index out of range, bad enum          */
+  LAT_ERR_SHAPE = 2,      /* a size the kernels do not support                   */
+  LAT_ERR_ALIGN = 3,      /* a device pointer not 16-byte aligned                */
+  LAT_ERR_CUDA = 4,       /* a CUDA runtime/driver call failed (see lat_last_error) */
+  LAT_ERR_OOM = 5,        /* device allocation failed in lat_create              */
+  LAT_ERR_TIMEOUT = 6,    /* a bounded device-side wait gave up                  */
+  LAT_ERR_STATE = 7,      /* call not valid for this context kind / state        */
+  LAT_ERR_UNSUPPORTED = 8 /* no kernel for this device (needs sm_103)            */
+} lat_status;
+
+typedef enum {
+  LAT_PI0_ACTION_EXPERT = 0,
+  LAT_PI0_PREFIX = 1,
+  LAT_DIT = 2
+} lat_model_kind;
+
+/* Model shape.  Fields not used by a kind must be 0. */
+typedef struct {
+  int kind;        /* lat_model_kind                                              */
+  int D;           /* residual width                                             */
+  int Hq, Hkv, dh; /* query heads, KV heads, head dim (DiT: Hq == Hkv)           */
+  int F;           /* FFN width                                                   */
+  int L;           /* blocks                                                      */
+  int S;           /* denoise steps (action expert, DiT)                          */
+  int T_prefix;    /* pi0: prefix tokens in the cache                             */
+  int T_q;         /* pi0: query tokens (state + actions); DiT: tokens per chunk  */
+  int act_dim;     /* action expert: action/state width                          */
+  int n_hist;      /* DiT: history chunks visible to a chunk (ring = n_hist+1)    */
+  int t_dim;       /* DiT: sinusoidal timestep width of the adaLN MLP             */
+  int patch_dim;   /* prefix: patch-embedding width                               */
+  int max_batch;   /* prefix: max B; DiT: max chunks per lat_block_forward call   */
+  int n_streams;   /* DiT: number of independent rings in the kv buffer           */
+  float rope_base; /* RoPE base (10000)                                           */
+  float eps;       /* norm epsilon (1e-6)                                         */
+} lat_model_desc;
+
+/* One block's weights (device, bf16, [K_in][N_out] row-major; vectors [D]). */
+typedef struct {
+  const void *g_attn;  /* pi0: RMSNorm scale before attention [D]               */
+  const void *wq;      /* [D][Hq*dh]                                             */
+  const void *wk;      /* [D][Hkv*dh]                                            */
+  const void *wv;      /* [D][Hkv*dh]                                            */
+  const void *wo;      /* [Hq*dh][D]                                             */
+  const void *g_ffn;   /* pi0: RMSNorm scale before the FFN [D]                  */
+  const void *wg;      /* pi0: gate projection [D][F]                            */
+  const void *wu;      /* pi0: up projection [D][F]                              */
+  const void *wd;      /* pi0: down projection [F][D]                            */
+  const void *w1;      /* DiT: FFN in [D][F]                                     */
+  const void *w2;      /* DiT: FFN out [F][D]                                    */
+} lat_block_weights;
+
+typedef struct {
+  const lat_block_weights *blocks; /* host array of L                              */
+  /* action expert: action/time embedding, state token and head                  */
+  const void *w_in, *b_in;         /* [act_dim][D], [D]                           */
+  const void *w1, *b1;             /* [2D][D] (rows 0..D-1: action emb, D..: time emb), [D] */
+  const void *w2, *b2;             /* [D][D], [D]                                 */
+  const void *w_state, *b_state;   /* [act_dim][D], [D]                           */
+  const void *g_final;             /* [D]                                         */
+  const void *w_out, *b_out;       /* [D][act_dim], [act_dim]                     */
+  /* prefix: patch projection                                                     */
+  const void *w_patch, *b_patch;   /* [patch_dim][D], [D]                         */
+  /* DiT: timestep MLP producing the adaLN table                                   */
+  const void *wt1, *bt1;           /* [t_dim][D], [D]                             */
+  const void *wt2, *bt2;           /* [D][D], [D]                                 */
+  const void *wmod, *bmod;         /* [D][6D], [6D]                               */
+} lat_weights;
+
+/* One chunk of a DiT batch. */
+typedef struct {
+  int stream;  /* ring index, 0 <= stream < n_streams                             */
+  int chunk;   /* chunk index c >= 0 (RoPE position of token j: c*T_q + j)        */
+  int step;    /* denoise step 0 <= step < S                                      */
+} lat_chunk_desc;
+
+typedef struct lat_ctx lat_ctx;
+
+/*
+ * lat_create -- fold and copy the weights, build the tables, allocate workspace.
+ *
+ * Offline transforms ("Running VLAs at Real-time Speed", section 4):
+ *  - RMSNorm scale fold (4.1): diag(g) W for the QKV and gate/up projections,
+ *    stored as bf16 (one rounding of the exact product); the head's
+ *    diag(g_final) W_out is stored in fp32.
+ *  - Action/time fold (4.2): W' = W_in W1[0:D] (fp32 [act_dim][D]) and the time
+ *    table T[s] = temb(t_s) W1[D:2D] + b_in W1[0:D] + b1 (fp32 [S][D]).
+ *  - Merged QKV (4.3): one [Wq|Wk|Wv] projection.
+ *  - DiT: adaLN table A[s] = SiLU(e(t_s)) Wmod + bmod (fp32 [S][6D]),
+ *    e(t) = SiLU(temb_t_dim(t) Wt1 + bt1) Wt2 + bt2.
+ * The default schedule is t_s = s/S, dt = 1/S.  The caller's weight buffers are
+ * not referenced after lat_create returns.  Synchronous.
+ * Errors: LAT_ERR_ARG / LAT_ERR_SHAPE for descriptors the kernels do not cover,
+ * LAT_ERR_OOM, LAT_ERR_CUDA, LAT_ERR_UNSUPPORTED (no sm_103 device).
+ */
+lat_status lat_create(const lat_model_desc *desc, const lat_weights *w, lat_ctx **out);
+
+/*
+ * lat_set_schedule -- replace the denoise time grid: t (host, S+1 values,
+ * t[0] < t[1] < ... < t[S]).  Step s evaluates the model at t[s] and moves x by
+ * (t[s+1] - t[s]) * v.  Rebuilds the time table / adaLN table (section 4.2: a
+ * schedule change needs the precomputed table recomputed).  Synchronous.
+ */
+lat_status lat_set_schedule(lat_ctx *ctx, const float *t, int n);
+
+/*
+ * lat_prefill_kv -- LAT_PI0_PREFIX: per-layer K/V of the prefix tokens.
+ *  patch_emb: device bf16 [B][T_prefix][patch_dim], 1 <= B <= max_batch.
+ *  kv:        device bf16 [L][B][2][T_prefix + T_q][Hkv*dh]; slots
+ *             0..T_prefix-1 of plane 0 (K, after RoPE at positions 0..) and
+ *             plane 1 (V) are written; slots >= T_prefix are not touched.
+ * The last layer computes only its K and V.
+ */
+lat_status lat_prefill_kv(lat_ctx *ctx, const void *patch_emb, int B, void *kv, void *stream);
+
+/*
+ * lat_block_forward -- one block, in place on the residual stream.
+ *  LAT_PI0_ACTION_EXPERT / LAT_PI0_PREFIX (chunks = NULL, n = 1):
+ *    x:  device fp32 [T_q][D] (action expert) -- query tokens at positions
+ *        T_prefix + j;
+ *    kv: device bf16 [2][T_prefix + T_q][Hkv*dh] of this layer; own K/V are
+ *        written to slots T_prefix.. and attention runs over all slots.
+ *  LAT_DIT:
+ *    x:  device fp32 [n][T_q][D], one chunk per chunks[i] (host array, n <= max_batch);
+ *    kv: device bf16 rings [n_streams][L][S][n_hist+1][2][T_q][D]; chunk c at
+ *        step s writes its K/V into slot c mod (n_hist+1) of ring
+ *        (stream, layer, s), then attends to that slot and to the slots of
+ *        chunks c-1..c-n_hist (those >= 0).  Two chunks of one call may not
+ *        share (stream, step, slot): LAT_ERR_ARG.
+ */
+lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_desc *chunks,
+                             int n, void *kv, void *stream);
+
+/*
+ * lat_denoise_chunk -- LAT_PI0_ACTION_EXPERT: the full S-step x L-block loop.
+ *  kv:    device bf16 [L][2][T_prefix + T_q][Hkv*dh] (slots >= T_prefix are
+ *         overwritten with the query tokens' K/V at every step);
+ *  state: device fp32 [act_dim];
+ *  x:     device fp32 [T_q - 1][act_dim]: the initial noise in, the actions out
+ *         (x <- x + dt * v after every step).
+ * The first call for a given (kv, state, x, stream) captures the whole loop in
+ * a CUDA graph; later calls replay it.  New addresses re-capture.
+ */
+lat_status lat_denoise_chunk(lat_ctx *ctx, void *kv, const float *state, float *x, void *stream);
+
+/*
+ * lat_debug_indices -- the integer maps the kernels use, computed by the same
+ * device code: for chunk i (DiT) ring slot slot_out[i] and RoPE position of its
+ * first token pos_out[i]; for the pi0 kinds (chunks = NULL, n = T_q) the cache
+ * slot and position of query token i.  Host output arrays of n ints.
+ * Synchronous; allocates and frees small temporary device buffers.
+ */
+lat_status lat_debug_indices(lat_ctx *ctx, const lat_chunk_desc *chunks, int n, int *slot_out,
+                             int *pos_out);
+
+/*
+ * lat_debug_gemm -- measurement hook for the action expert: enqueue `reps`
+ * back-to-back launches of one streamed projection of block `layer`
+ * (which: 0 = merged QKV, 1 = attention output, 2 = gate/up, 3 = down) on the
+ * context's own workspace, then clear the accumulators it touched.  Used to
+ * time the weight-streaming kernel alone with events on `stream`.
+ */
+lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *stream);
+
+/* Wait for all work of the context and report a recorded device-side error. */
+lat_status lat_sync(lat_ctx *ctx);
+
+/* Human-readable name of a status; message of the last failure on this thread. */
+const char *lat_status_str(lat_status s);
+const char *lat_last_error(void);
+
+void lat_destroy(lat_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAT_H */

@@ -1,0 +1,250 @@
+// Chunk-over-cached-KV attention: softmax(Q K^T / sqrt(dh)) V, no mask, with
+// grouped KV heads (Hkv = 1 is the pi0 multi-query case: all query heads read
+// the one cached head).  "Running VLAs at Real-time Speed" (reading note,
+// section 5) keeps a library attention here; this is a hand-written one.
+//
+// Each CTA runs 4 warps x 16 query rows of one query head against a range of
+// 64-key blocks with an online softmax (running max / sum per row, rescaling
+// the output accumulator).  Q (fp32) and P (fp32) enter the warp-level bf16
+// tensor-core MMA as three-term splits, K and V are the cache's bf16 values,
+// accumulation is fp32, so the only roundings are fp32 ones.  With several key
+// ranges (flash-decoding) each CTA writes its partial (max, sum, unnormalised
+// output) and a combine kernel merges them.
+#pragma once
+#include "common.cuh"
+
+namespace lat {
+
+struct AttnArgs {
+  const float* q;            // fp32 [T_q][q_ld], head h at column h*dh
+  int q_ld;
+  const __nv_bfloat16* k;    // bf16 keys [T_kv][kv_ld], kv head j at column j*dh
+  const __nv_bfloat16* v;
+  int kv_ld;
+  int T_q, T_kv, Hq, Hkv;
+  float scale_log2;          // log2(e) / sqrt(dh)
+  int n_split;               // key ranges
+  float* out;                // n_split == 1: fp32 [T_q][out_ld] (head h at h*dh)
+  int out_ld;
+  float* part_m;             // n_split > 1: [n_split][Hq][T_q]
+  float* part_l;
+  float* part_o;             // [n_split][Hq][T_q][dh]
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Split a pair of fp32 values into three packed bf16x2 words.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  Split3 a = split3(x), b = split3(y);
+  hi = pack_bf16(a.hi, b.hi);
+  mid = pack_bf16(a.mid, b.mid);
+  lo = pack_bf16(a.lo, b.lo);
+}
+
+template <int DH>
+__global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
+  constexpr int KB = 64;          // keys per block
+  constexpr int LD = DH + 8;      // padded smem row (bf16): conflict-free ldmatrix
+  constexpr int NT = DH / 8;      // output n-tiles
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* sV = sK + KB * LD;
+
+  const int h = blockIdx.x;
+  const int qt = blockIdx.y;
+  const int split = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int kvh = h / (a.Hq / a.Hkv);
+  const int nkb = (a.T_kv + KB - 1) / KB;
+  const int kb0 = split * nkb / a.n_split, kb1 = (split + 1) * nkb / a.n_split;
+
+  const int r0 = qt * 64 + warp * 16 + g;   // this thread's two query rows: r0, r0 + 8
+  const int r1 = r0 + 8;
+  const bool v0 = r0 < a.T_q, v1 = r1 < a.T_q;
+  const float* q0 = a.q + (size_t)(v0 ? r0 : 0) * a.q_ld + h * DH;
+  const float* q1 = a.q + (size_t)(v1 ? r1 : 0) * a.q_ld + h * DH;
+
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
+
+  for (int kb = kb0; kb < kb1; ++kb) {
+    // ---- stage K and V blocks (zero-filled past T_kv) ----
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
+      const int row = idx / (DH / 8), c8 = idx % (DH / 8);
+      const int key = kb * KB + row;
+      uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (key < a.T_kv) {
+        kk = *reinterpret_cast<const uint4*>(a.k + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+        vv = *reinterpret_cast<const uint4*>(a.v + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+      }
+      *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
+      *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
+    }
+    __syncthreads();
+
+    // ---- S = Q K^T for 16 rows x 64 keys (8 n-tiles) ----
+    float s[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll 1
+    for (int ks = 0; ks < DH / 16; ++ks) {
+      const int c = ks * 16 + 2 * tq;
+      float2 x00 = v0 ? *reinterpret_cast<const float2*>(q0 + c) : make_float2(0.f, 0.f);
+      float2 x10 = v1 ? *reinterpret_cast<const float2*>(q1 + c) : make_float2(0.f, 0.f);
+      float2 x01 = v0 ? *reinterpret_cast<const float2*>(q0 + c + 8) : make_float2(0.f, 0.f);
+      float2 x11 = v1 ? *reinterpret_cast<const float2*>(q1 + c + 8) : make_float2(0.f, 0.f);
+      uint32_t ah[4], am[4], al[4];
+      split_pair(x00.x, x00.y, ah[0], am[0], al[0]);
+      split_pair(x10.x, x10.y, ah[1], am[1], al[1]);
+      split_pair(x01.x, x01.y, ah[2], am[2], al[2]);
+      split_pair(x11.x, x11.y, ah[3], am[3], al[3]);
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {
+        // matrices: keys jp*16 + (0..7 | 8..15), d ks*16 + (0..7 | 8..7)
+        const int mi = lane >> 3, rr = lane & 7;
+        const int key = jp * 16 + ((mi >> 1) << 3) + rr;
+        const int col = ks * 16 + ((mi & 1) << 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+        mma_16816(s[2 * jp], ah, b0, b1);
+        mma_16816(s[2 * jp], am, b0, b1);
+        mma_16816(s[2 * jp], al, b0, b1);
+        mma_16816(s[2 * jp + 1], ah, b2, b3);
+        mma_16816(s[2 * jp + 1], am, b2, b3);
+        mma_16816(s[2 * jp + 1], al, b2, b3);
+      }
+    }
+
+    // ---- online softmax (base 2) ----
+    float mx0 = m0, mx1 = m1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int key = kb * KB + j * 8 + 2 * tq;
+      s[j][0] = (key < a.T_kv) ? s[j][0] * a.scale_log2 : -INFINITY;
+      s[j][1] = (key + 1 < a.T_kv) ? s[j][1] * a.scale_log2 : -INFINITY;
+      s[j][2] = (key < a.T_kv) ? s[j][2] * a.scale_log2 : -INFINITY;
+      s[j][3] = (key + 1 < a.T_kv) ? s[j][3] * a.scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float al0 = exp2f(m0 - mx0), al1 = exp2f(m1 - mx1);
+    m0 = mx0;
+    m1 = mx1;
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      s[j][0] = exp2f(s[j][0] - mx0);
+      s[j][1] = exp2f(s[j][1] - mx0);
+      s[j][2] = exp2f(s[j][2] - mx1);
+      s[j][3] = exp2f(s[j][3] - mx1);
+      sum0 += s[j][0] + s[j][1];
+      sum1 += s[j][2] + s[j][3];
+    }
+    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
+    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
+    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 1);
+    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 2);
+    l0 = l0 * al0 + sum0;
+    l1 = l1 * al1 + sum1;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al0;
+      o[j][2] *= al1;
+      o[j][3] *= al1;
+    }
+
+    // ---- O += P V ----
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t ph[4], pm[4], pl[4];
+      split_pair(s[2 * kk][0], s[2 * kk][1], ph[0], pm[0], pl[0]);
+      split_pair(s[2 * kk][2], s[2 * kk][3], ph[1], pm[1], pl[1]);
+      split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pm[2], pl[2]);
+      split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pm[3], pl[3]);
+#pragma unroll
+      for (int jp = 0; jp < NT / 2; ++jp) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int key = kk * 16 + ((mi & 1) << 3) + rr;
+        const int col = jp * 16 + ((mi >> 1) << 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+        mma_16816(o[2 * jp], ph, b0, b1);
+        mma_16816(o[2 * jp], pm, b0, b1);
+        mma_16816(o[2 * jp], pl, b0, b1);
+        mma_16816(o[2 * jp + 1], ph, b2, b3);
+        mma_16816(o[2 * jp + 1], pm, b2, b3);
+        mma_16816(o[2 * jp + 1], pl, b2, b3);
+      }
+    }
+  }
+
+  // ---- write out ----
+  if (a.n_split == 1) {
+    const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f, i1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int c = h * DH + j * 8 + 2 * tq;
+      if (v0) *reinterpret_cast<float2*>(a.out + (size_t)r0 * a.out_ld + c) = make_float2(o[j][0] * i0, o[j][1] * i0);
+      if (v1) *reinterpret_cast<float2*>(a.out + (size_t)r1 * a.out_ld + c) = make_float2(o[j][2] * i1, o[j][3] * i1);
+    }
+  } else {
+    const size_t base = ((size_t)split * a.Hq + h) * a.T_q;
+    if (tq == 0) {
+      if (v0) { a.part_m[base + r0] = m0; a.part_l[base + r0] = l0; }
+      if (v1) { a.part_m[base + r1] = m1; a.part_l[base + r1] = l1; }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int c = j * 8 + 2 * tq;
+      if (v0) *reinterpret_cast<float2*>(a.part_o + (base + r0) * DH + c) = make_float2(o[j][0], o[j][1]);
+      if (v1) *reinterpret_cast<float2*>(a.part_o + (base + r1) * DH + c) = make_float2(o[j][2], o[j][3]);
+    }
+  }
+}
+
+// Merge key-range partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// Grid (T_q, Hq), blockDim = dh.
+__global__ void attention_combine_kernel(AttnArgs a, int dh) {
+  const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.part_m[((size_t)s * a.Hq + h) * a.T_q + t]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < a.n_split; ++s) {
+    const size_t i = ((size_t)s * a.Hq + h) * a.T_q + t;
+    const float w = (a.part_m[i] == -INFINITY) ? 0.f : exp2f(a.part_m[i] - M);
+    L += w * a.part_l[i];
+    acc += w * a.part_o[i * dh + d];
+  }
+  a.out[(size_t)t * a.out_ld + h * dh + d] = acc / L;
+}
+
+}  // namespace lat

@@ -1,0 +1,672 @@
+// C ABI of the low-latency transformer-block library (declared in include/lat.h).
+//
+// Host side: argument validation, offline folds, tensor maps, workspace, the
+// per-block kernel sequence and the CUDA-graph capture of the denoise loop
+// ("Running VLAs at Real-time Speed", reading note, section 3: CUDA Graph
+// replay of a fixed kernel sequence with fixed buffers).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/lat.h"
+#include "attention.cuh"
+#include "common.cuh"
+#include "skinny_gemm.cuh"
+#include "small_kernels.cuh"
+
+using namespace lat;
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+static thread_local std::string g_last_error;
+
+static lat_status fail(lat_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                        \
+  do {                                                                                        \
+    cudaError_t e_ = (expr);                                                                  \
+    if (e_ != cudaSuccess)                                                                    \
+      return fail(e_ == cudaErrorMemoryAllocation ? LAT_ERR_OOM : LAT_ERR_CUDA, "%s: %s (%s:%d)", \
+                  #expr, cudaGetErrorString(e_), __FILE__, __LINE__);                         \
+  } while (0)
+
+#define LAT_TRY(expr)              \
+  do {                             \
+    lat_status s_ = (expr);        \
+    if (s_ != LAT_OK) return s_;   \
+  } while (0)
+
+static inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// tensor maps (driver entry point fetched through the runtime)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static lat_status get_encode(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  if (!cached) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || !p) return fail(LAT_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cached = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = cached;
+  return LAT_OK;
+}
+
+// K-major bf16 matrix [rows][K] -> tiles of 128 rows x 64 K, 128-byte swizzle.
+static lat_status make_kmajor_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  EncodeTiledFn enc;
+  LAT_TRY(get_encode(&enc));
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LAT_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return LAT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// context
+// ---------------------------------------------------------------------------
+struct GemmPlan {
+  int w_row0_per_layer;  // rows of one layer inside the stacked tensor
+  int N_out, K, splits;
+};
+
+struct lat_ctx {
+  lat_model_desc d{};
+  int num_sms = 0;
+  std::vector<void*> allocs;
+
+  // streamed block weights, K-major bf16, stacked over layers
+  bf16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr, *w2 = nullptr;
+  CUtensorMap map_qkv, map_o, map_gu, map_d, map_w2;
+  int nqkv = 0;
+  GemmPlan g_qkv{}, g_o{}, g_gu{}, g_d{}, g_w2{};
+
+  // action-expert tables (fp32)
+  float *wfold = nullptr, *ttab = nullptr, *b2 = nullptr, *wout = nullptr, *bout = nullptr, *dt = nullptr;
+  bf16 *w_state = nullptr, *b_state = nullptr, *w1_keep = nullptr, *b1_keep = nullptr, *w_in_keep = nullptr,
+       *b_in_keep = nullptr;
+  float* cos_t = nullptr;
+  float* sin_t = nullptr;
+
+  // workspace
+  float *xres = nullptr, *qkv_acc = nullptr, *gu_acc = nullptr, *q = nullptr, *o = nullptr, *r1 = nullptr,
+        *r2 = nullptr, *z = nullptr, *pm = nullptr, *pl = nullptr, *po = nullptr, *state_emb = nullptr,
+        *temb = nullptr;
+  int attn_split = 1;
+  DevErr* err = nullptr;
+
+  // captured denoise loop
+  cudaGraphExec_t gexec = nullptr;
+  void* g_kv = nullptr;
+  const float* g_state = nullptr;
+  float* g_x = nullptr;
+  void* g_stream = nullptr;
+
+  template <class T>
+  lat_status alloc(T** p, size_t count) {
+    void* v = nullptr;
+    cudaError_t e = cudaMalloc(&v, count * sizeof(T) + 16);
+    if (e != cudaSuccess) return fail(LAT_ERR_OOM, "cudaMalloc(%zu): %s", count * sizeof(T), cudaGetErrorString(e));
+    allocs.push_back(v);
+    *p = reinterpret_cast<T*>(v);
+    return LAT_OK;
+  }
+  ~lat_ctx() {
+    if (gexec) cudaGraphExecDestroy(gexec);
+    for (void* p : allocs) cudaFree(p);
+  }
+};
+
+static constexpr int kStages = 4;
+
+static lat_status launch_check(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch %s: %s", what, cudaGetErrorString(e));
+  return LAT_OK;
+}
+
+static GemmPlan plan_gemm(int N_out, int K, int num_sms) {
+  GemmPlan p;
+  p.w_row0_per_layer = N_out;
+  p.N_out = N_out;
+  p.K = K;
+  const int m_tiles = N_out / 128, kb = K / 64;
+  int s = num_sms / m_tiles;
+  if (s < 1) s = 1;
+  if (s > kb) s = kb;
+  p.splits = s;
+  return p;
+}
+
+static lat_status enqueue_skinny(const lat_ctx* c, const CUtensorMap& map, const GemmPlan& g, int layer,
+                                 SkinnyArgs a, cudaStream_t st) {
+  a.w_row0 = layer * g.w_row0_per_layer;
+  a.N_out = g.N_out;
+  a.K = g.K;
+  a.splits = g.splits;
+  a.err = c->err;
+  const int grid = (g.N_out / 128) * g.splits;
+  skinny_gemm_kernel<kStages><<<grid, 192, skinny_smem_bytes(kStages), st>>>(map, a);
+  return launch_check("skinny_gemm");
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+static lat_status check_desc(const lat_model_desc* d) {
+  if (!d) return fail(LAT_ERR_ARG, "desc is NULL");
+  if (d->kind != LAT_PI0_ACTION_EXPERT)
+    return fail(LAT_ERR_UNSUPPORTED, "model kind %d not built into this library", d->kind);
+  if (d->D <= 0 || d->D % 128) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 128");
+  if (d->Hq <= 0 || d->Hkv <= 0 || d->Hq % d->Hkv) return fail(LAT_ERR_SHAPE, "Hq must be a multiple of Hkv");
+  if (d->dh != 64 && d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 64, 128 or 256");
+  if (((d->Hq + 2 * d->Hkv) * d->dh) % 128) return fail(LAT_ERR_SHAPE, "(Hq + 2 Hkv) dh must be a multiple of 128");
+  if ((d->Hq * d->dh) % 64) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 64");
+  if (d->F <= 0 || d->F % 64) return fail(LAT_ERR_SHAPE, "F must be a positive multiple of 64");
+  if (d->L <= 0 || d->S <= 0) return fail(LAT_ERR_SHAPE, "L and S must be positive");
+  if (d->T_q < 2 || d->T_q > 64) return fail(LAT_ERR_SHAPE, "T_q must be in [2, 64]");
+  if (d->T_prefix < 0) return fail(LAT_ERR_SHAPE, "T_prefix must be >= 0");
+  if (d->act_dim <= 0) return fail(LAT_ERR_SHAPE, "act_dim must be positive");
+  if (!(d->eps > 0.f) || !(d->rope_base > 1.f)) return fail(LAT_ERR_ARG, "eps / rope_base out of range");
+  return LAT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// offline folds
+// ---------------------------------------------------------------------------
+static lat_status fold_t(const void* W, const void* g, bf16* out, int K, int N) {
+  if (!W || !aligned16(W)) return fail(LAT_ERR_ALIGN, "weight pointer NULL or not 16-byte aligned");
+  dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+  fold_transpose_kernel<<<grid, block>>>(reinterpret_cast<const bf16*>(W), reinterpret_cast<const bf16*>(g), out,
+                                         K, N);
+  return launch_check("fold_transpose");
+}
+
+static lat_status small_gemm(const void* A, bool a_bf16, int lda, const void* B, bool b_bf16, int ldb,
+                             const void* bias, bool bias_bf16, float* C, int ldc, int M, int N, int K, int act,
+                             cudaStream_t st = 0) {
+  SmallGemmArgs a{A, a_bf16, lda, B, b_bf16, ldb, bias, bias_bf16, C, ldc, M, N, K, act};
+  dim3 grid((N + 127) / 128, M);
+  small_gemm_kernel<<<grid, 128, 0, st>>>(a);
+  return launch_check("small_gemm");
+}
+
+static void timestep_embedding_host(double t, int d, std::vector<float>& out) {
+  const int half = d / 2;
+  out.resize(d);
+  for (int i = 0; i < half; ++i) {
+    const double w = std::pow(10000.0, -(double)i / half);
+    out[i] = (float)std::sin(1000.0 * t * w);
+    out[half + i] = (float)std::cos(1000.0 * t * w);
+  }
+}
+
+static lat_status build_schedule(lat_ctx* c, const std::vector<double>& t) {
+  const lat_model_desc& d = c->d;
+  // time table T[s] = temb(t_s) W1[D:2D] + b_in W1[0:D] + b1, and dt[s]
+  std::vector<float> emb((size_t)d.S * d.D), tmp;
+  for (int s = 0; s < d.S; ++s) {
+    timestep_embedding_host(t[s], d.D, tmp);
+    std::memcpy(&emb[(size_t)s * d.D], tmp.data(), d.D * sizeof(float));
+  }
+  std::vector<float> dts(d.S);
+  for (int s = 0; s < d.S; ++s) dts[s] = (float)(t[s + 1] - t[s]);
+  CUDA_TRY(cudaMemcpy(c->temb, emb.data(), emb.size() * sizeof(float), cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->dt, dts.data(), dts.size() * sizeof(float), cudaMemcpyHostToDevice));
+  // bias row c0 = b_in W1[0:D] + b1  (into ttab row 0 temporarily via z scratch)
+  float* c0 = c->z;  // [D] scratch
+  LAT_TRY(small_gemm(c->b_in_keep, true, d.D, c->w1_keep, true, d.D, c->b1_keep, true, c0, d.D, 1, d.D, d.D, 0));
+  // T[s] = temb(t_s) W1_t + c0
+  LAT_TRY(small_gemm(c->temb, false, d.D, c->w1_keep + (size_t)d.D * d.D, true, d.D, c0, false, c->ttab, d.D, d.S,
+                     d.D, d.D, 0));
+  CUDA_TRY(cudaDeviceSynchronize());
+  return LAT_OK;
+}
+
+static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, F = d.F, L = d.L, A = d.act_dim;
+  const int qd = d.Hq * d.dh, kvd = d.Hkv * d.dh;
+  c->nqkv = (d.Hq + 2 * d.Hkv) * d.dh;
+  if (!w || !w->blocks) return fail(LAT_ERR_ARG, "weights / blocks NULL");
+  const void* vecs[] = {w->w_in, w->b_in, w->w1, w->b1, w->w2, w->b2, w->w_state, w->b_state, w->g_final, w->w_out,
+                        w->b_out};
+  for (const void* p : vecs)
+    if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "embedding/head weight NULL or not 16-byte aligned");
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    const void* bp[] = {b.g_attn, b.wq, b.wk, b.wv, b.wo, b.g_ffn, b.wg, b.wu, b.wd};
+    for (const void* p : bp)
+      if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "block %d weight NULL or not 16-byte aligned", l);
+  }
+  // --- streamed weights: fold + transpose to K-major, stacked over layers ---
+  LAT_TRY(c->alloc(&c->wqkv, (size_t)L * c->nqkv * D));
+  LAT_TRY(c->alloc(&c->wo, (size_t)L * D * qd));
+  LAT_TRY(c->alloc(&c->wgu, (size_t)L * 2 * F * D));
+  LAT_TRY(c->alloc(&c->wd, (size_t)L * D * F));
+  LAT_TRY(c->alloc(&c->w2, (size_t)D * D));
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    bf16* q0 = c->wqkv + (size_t)l * c->nqkv * D;
+    LAT_TRY(fold_t(b.wq, b.g_attn, q0, D, qd));
+    LAT_TRY(fold_t(b.wk, b.g_attn, q0 + (size_t)qd * D, D, kvd));
+    LAT_TRY(fold_t(b.wv, b.g_attn, q0 + (size_t)(qd + kvd) * D, D, kvd));
+    LAT_TRY(fold_t(b.wo, nullptr, c->wo + (size_t)l * D * qd, qd, D));
+    bf16* gu0 = c->wgu + (size_t)l * 2 * F * D;
+    LAT_TRY(fold_t(b.wg, b.g_ffn, gu0, D, F));
+    LAT_TRY(fold_t(b.wu, b.g_ffn, gu0 + (size_t)F * D, D, F));
+    LAT_TRY(fold_t(b.wd, nullptr, c->wd + (size_t)l * D * F, F, D));
+  }
+  LAT_TRY(fold_t(w->w2, nullptr, c->w2, D, D));
+  LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * c->nqkv, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, qd, 128));
+  LAT_TRY(make_kmajor_map(&c->map_gu, c->wgu, L * 2 * F, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_d, c->wd, L * D, F, 128));
+  LAT_TRY(make_kmajor_map(&c->map_w2, c->w2, D, D, 128));
+  c->g_qkv = plan_gemm(c->nqkv, D, c->num_sms);
+  c->g_o = plan_gemm(D, qd, c->num_sms);
+  c->g_gu = plan_gemm(2 * F, D, c->num_sms);
+  c->g_d = plan_gemm(D, F, c->num_sms);
+  c->g_w2 = plan_gemm(D, D, c->num_sms);
+
+  // --- embedding / head (fp32 folds) ---
+  LAT_TRY(c->alloc(&c->w_in_keep, (size_t)A * D));
+  LAT_TRY(c->alloc(&c->b_in_keep, (size_t)D));
+  LAT_TRY(c->alloc(&c->w1_keep, (size_t)2 * D * D));
+  LAT_TRY(c->alloc(&c->b1_keep, (size_t)D));
+  LAT_TRY(c->alloc(&c->w_state, (size_t)A * D));
+  LAT_TRY(c->alloc(&c->b_state, (size_t)D));
+  CUDA_TRY(cudaMemcpy(c->w_in_keep, w->w_in, (size_t)A * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->b_in_keep, w->b_in, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->w1_keep, w->w1, (size_t)2 * D * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->b1_keep, w->b1, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->w_state, w->w_state, (size_t)A * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->b_state, w->b_state, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+  LAT_TRY(c->alloc(&c->wfold, (size_t)A * D));
+  LAT_TRY(c->alloc(&c->ttab, (size_t)d.S * D));
+  LAT_TRY(c->alloc(&c->temb, (size_t)d.S * D));
+  LAT_TRY(c->alloc(&c->dt, (size_t)d.S));
+  LAT_TRY(c->alloc(&c->b2, (size_t)D));
+  LAT_TRY(c->alloc(&c->wout, (size_t)D * A));
+  LAT_TRY(c->alloc(&c->bout, (size_t)A));
+  // W' = W_in W1[0:D]
+  LAT_TRY(small_gemm(w->w_in, true, D, w->w1, true, D, nullptr, false, c->wfold, D, A, D, D, 0));
+  bf16_to_f32_kernel<<<(D + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->b2), c->b2, D);
+  LAT_TRY(launch_check("b2"));
+  bf16_to_f32_kernel<<<(A + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->b_out), c->bout, A);
+  LAT_TRY(launch_check("bout"));
+  scale_rows_f32_kernel<<<(D * A + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->w_out),
+                                                       reinterpret_cast<const bf16*>(w->g_final), c->wout, D, A);
+  LAT_TRY(launch_check("wout"));
+
+  // --- RoPE tables for the query positions (float64 -> fp32) ---
+  const int half = d.dh / 2;
+  std::vector<float> ct((size_t)d.T_q * half), stt((size_t)d.T_q * half);
+  for (int t = 0; t < d.T_q; ++t)
+    for (int i = 0; i < half; ++i) {
+      const double theta = std::pow((double)d.rope_base, -2.0 * i / d.dh);
+      const double ang = (double)query_pos(d.T_prefix, t) * theta;
+      ct[(size_t)t * half + i] = (float)std::cos(ang);
+      stt[(size_t)t * half + i] = (float)std::sin(ang);
+    }
+  LAT_TRY(c->alloc(&c->cos_t, ct.size()));
+  LAT_TRY(c->alloc(&c->sin_t, stt.size()));
+  CUDA_TRY(cudaMemcpy(c->cos_t, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->sin_t, stt.data(), stt.size() * 4, cudaMemcpyHostToDevice));
+
+  // --- workspace ---
+  const int T = d.T_q;
+  const int T_kv = d.T_prefix + d.T_q;
+  const int nkb = (T_kv + 63) / 64;
+  c->attn_split = nkb;
+  LAT_TRY(c->alloc(&c->xres, (size_t)T * D));
+  LAT_TRY(c->alloc(&c->qkv_acc, (size_t)T * c->nqkv));
+  LAT_TRY(c->alloc(&c->gu_acc, (size_t)T * 2 * F));
+  LAT_TRY(c->alloc(&c->q, (size_t)T * qd));
+  LAT_TRY(c->alloc(&c->o, (size_t)T * qd));
+  LAT_TRY(c->alloc(&c->r1, (size_t)T));
+  LAT_TRY(c->alloc(&c->r2, (size_t)T));
+  LAT_TRY(c->alloc(&c->z, (size_t)T * D));
+  LAT_TRY(c->alloc(&c->pm, (size_t)c->attn_split * d.Hq * T));
+  LAT_TRY(c->alloc(&c->pl, (size_t)c->attn_split * d.Hq * T));
+  LAT_TRY(c->alloc(&c->po, (size_t)c->attn_split * d.Hq * T * d.dh));
+  LAT_TRY(c->alloc(&c->state_emb, (size_t)D));
+  LAT_TRY(c->alloc(&c->err, 1));
+  CUDA_TRY(cudaMemset(c->qkv_acc, 0, (size_t)T * c->nqkv * 4));
+  CUDA_TRY(cudaMemset(c->gu_acc, 0, (size_t)T * 2 * F * 4));
+  CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
+
+  std::vector<double> t(d.S + 1);
+  for (int s = 0; s <= d.S; ++s) t[s] = (double)s / d.S;
+  LAT_TRY(build_schedule(c, t));
+  CUDA_TRY(cudaDeviceSynchronize());
+  return LAT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// one pi0 block on the residual stream xres [T_q][D]; kv_layer = [2][T_kv][kvd]
+// ---------------------------------------------------------------------------
+static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_layer, cudaStream_t st) {
+  const lat_model_desc& d = c->d;
+  const int T = d.T_q, D = d.D, F = d.F;
+  const int qd = d.Hq * d.dh, kvd = d.Hkv * d.dh;
+  const int T_kv = d.T_prefix + d.T_q;
+  bf16* kc = kv_layer;
+  bf16* vc = kv_layer + (size_t)T_kv * kvd;
+  // 1. merged QKV projection of x (RMS factor r1 computed alongside)
+  {
+    SkinnyArgs a{};
+    a.src = xres; a.src_ld = D; a.mode = B_PLAIN; a.n_tok = T;
+    a.out = c->qkv_acc; a.out_ld = c->nqkv;
+    a.stat_src = xres; a.stat_len = D; a.stat_out = c->r1; a.eps = d.eps;
+    LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, l, a, st));
+  }
+  // 2. row scale + RoPE + K/V into the cache + q; clears qkv_acc and gu_acc
+  {
+    QkvEpiArgs a{c->qkv_acc, c->nqkv, c->r1, c->cos_t, c->sin_t, c->q, kc, vc, kvd, d.T_prefix,
+                 d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F};
+    qkv_epilogue_kernel<<<T, 256, 0, st>>>(a);
+    LAT_TRY(launch_check("qkv_epilogue"));
+  }
+  // 3. attention over [prefix | own] (key ranges) + combine
+  {
+    AttnArgs a{};
+    a.q = c->q; a.q_ld = qd; a.k = kc; a.v = vc; a.kv_ld = kvd;
+    a.T_q = T; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+    a.n_split = c->attn_split;
+    a.out = c->o; a.out_ld = qd; a.part_m = c->pm; a.part_l = c->pl; a.part_o = c->po;
+    dim3 grid(d.Hq, (T + 63) / 64, a.n_split);
+    const int smem = 2 * 64 * (d.dh + 8) * 2;
+    if (d.dh == 64) attention_kernel<64><<<grid, 128, smem, st>>>(a);
+    else if (d.dh == 128) attention_kernel<128><<<grid, 128, smem, st>>>(a);
+    else attention_kernel<256><<<grid, 128, smem, st>>>(a);
+    LAT_TRY(launch_check("attention"));
+    if (a.n_split > 1) {
+      attention_combine_kernel<<<dim3(T, d.Hq), d.dh, 0, st>>>(a, d.dh);
+      LAT_TRY(launch_check("attention_combine"));
+    }
+  }
+  // 4. x += o Wo
+  {
+    SkinnyArgs a{};
+    a.src = c->o; a.src_ld = qd; a.mode = B_PLAIN; a.n_tok = T;
+    a.out = xres; a.out_ld = D;
+    LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, l, a, st));
+  }
+  // 5. gate/up projection of x (RMS factor r2 alongside)
+  {
+    SkinnyArgs a{};
+    a.src = xres; a.src_ld = D; a.mode = B_PLAIN; a.n_tok = T;
+    a.out = c->gu_acc; a.out_ld = 2 * F;
+    a.stat_src = xres; a.stat_len = D; a.stat_out = c->r2; a.eps = d.eps;
+    LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, l, a, st));
+  }
+  // 6. x += (GELU(r2 g) * (r2 u)) Wd
+  {
+    SkinnyArgs a{};
+    a.src = c->gu_acc; a.src_ld = 2 * F; a.src2_off = F; a.row_scale = c->r2; a.mode = B_GEGLU; a.n_tok = T;
+    a.out = xres; a.out_ld = D;
+    LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, l, a, st));
+  }
+  return LAT_OK;
+}
+
+static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, float* x, cudaStream_t st) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, T = d.T_q, A = d.act_dim;
+  const int T_kv = d.T_prefix + d.T_q;
+  const size_t layer_elems = (size_t)2 * T_kv * d.Hkv * d.dh;
+  // state token (once per chunk)
+  LAT_TRY(small_gemm(state, false, A, c->w_state, true, D, c->b_state, true, c->state_emb, D, 1, D, A, 0, st));
+  for (int s = 0; s < d.S; ++s) {
+    EmbedArgs e{x, c->wfold, c->ttab, c->b2, c->state_emb, c->z, c->xres, D, A, T, s};
+    embed_prologue_kernel<<<dim3((D + 255) / 256, T), 256, 0, st>>>(e);
+    LAT_TRY(launch_check("embed_prologue"));
+    {
+      SkinnyArgs a{};
+      a.src = c->z; a.src_ld = D; a.mode = B_SILU; a.n_tok = T - 1;
+      a.out = c->xres + D; a.out_ld = D;
+      LAT_TRY(enqueue_skinny(c, c->map_w2, c->g_w2, 0, a, st));
+    }
+    for (int l = 0; l < d.L; ++l) LAT_TRY(enqueue_pi0_block(c, l, c->xres, kv + (size_t)l * layer_elems, st));
+    HeadArgs h{c->xres, c->wout, c->bout, x, c->dt, s, D, A, d.eps};
+    head_euler_kernel<<<T - 1, 256, 0, st>>>(h);
+    LAT_TRY(launch_check("head_euler"));
+  }
+  return LAT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* lat_status_str(lat_status s) {
+  switch (s) {
+    case LAT_OK: return "LAT_OK";
+    case LAT_ERR_ARG: return "LAT_ERR_ARG";
+    case LAT_ERR_SHAPE: return "LAT_ERR_SHAPE";
+    case LAT_ERR_ALIGN: return "LAT_ERR_ALIGN";
+    case LAT_ERR_CUDA: return "LAT_ERR_CUDA";
+    case LAT_ERR_OOM: return "LAT_ERR_OOM";
+    case LAT_ERR_TIMEOUT: return "LAT_ERR_TIMEOUT";
+    case LAT_ERR_STATE: return "LAT_ERR_STATE";
+    case LAT_ERR_UNSUPPORTED: return "LAT_ERR_UNSUPPORTED";
+  }
+  return "LAT_ERR_?";
+}
+
+const char* lat_last_error(void) { return g_last_error.c_str(); }
+
+lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx** out) {
+  if (!out) return fail(LAT_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  LAT_TRY(check_desc(desc));
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(LAT_ERR_UNSUPPORTED, "needs an sm_103 device, found sm_%d%d", prop.major, prop.minor);
+  lat_ctx* c = new lat_ctx();
+  c->d = *desc;
+  c->num_sms = prop.multiProcessorCount;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(skinny_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         skinny_smem_bytes(kStages));
+    cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 72 * 2);
+    cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 136 * 2);
+    cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 264 * 2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      delete c;
+      return fail(LAT_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    }
+    attr_done = true;
+  }
+  lat_status s = create_pi0(c, w);
+  if (s != LAT_OK) {
+    std::string msg = g_last_error;
+    cudaDeviceSynchronize();
+    delete c;
+    g_last_error = msg;
+    return s;
+  }
+  *out = c;
+  return LAT_OK;
+}
+
+lat_status lat_set_schedule(lat_ctx* c, const float* t, int n) {
+  if (!c || !t) return fail(LAT_ERR_ARG, "NULL argument");
+  if (n != c->d.S + 1) return fail(LAT_ERR_SHAPE, "schedule needs S + 1 = %d values", c->d.S + 1);
+  for (int i = 0; i < c->d.S; ++i)
+    if (!(t[i + 1] > t[i])) return fail(LAT_ERR_ARG, "schedule must be increasing");
+  std::vector<double> tt(t, t + n);
+  CUDA_TRY(cudaDeviceSynchronize());
+  return build_schedule(c, tt);
+}
+
+lat_status lat_prefill_kv(lat_ctx* c, const void* patch_emb, int B, void* kv, void* stream) {
+  (void)patch_emb; (void)B; (void)kv; (void)stream;
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  return fail(LAT_ERR_STATE, "lat_prefill_kv needs a LAT_PI0_PREFIX context");
+}
+
+static lat_status check_dev_err(lat_ctx* c) {
+  DevErr e{};
+  CUDA_TRY(cudaMemcpy(&e, c->err, sizeof(e), cudaMemcpyDeviceToHost));
+  if (e.code) return fail(LAT_ERR_TIMEOUT, "device wait gave up (code %u, site %u)", e.code, e.where);
+  return LAT_OK;
+}
+
+lat_status lat_block_forward(lat_ctx* c, int layer, float* x, const lat_chunk_desc* chunks, int n, void* kv,
+                             void* stream) {
+  if (!c || !x || !kv) return fail(LAT_ERR_ARG, "NULL argument");
+  if (layer < 0 || layer >= c->d.L) return fail(LAT_ERR_ARG, "layer %d out of range", layer);
+  if (!aligned16(x) || !aligned16(kv)) return fail(LAT_ERR_ALIGN, "x / kv not 16-byte aligned");
+  if (c->d.kind == LAT_PI0_ACTION_EXPERT) {
+    if (chunks != nullptr || n != 1) return fail(LAT_ERR_ARG, "pi0 block: chunks must be NULL and n == 1");
+    return enqueue_pi0_block(c, layer, x, reinterpret_cast<bf16*>(kv), reinterpret_cast<cudaStream_t>(stream));
+  }
+  return fail(LAT_ERR_STATE, "unsupported context kind");
+}
+
+lat_status lat_denoise_chunk(lat_ctx* c, void* kv, const float* state, float* x, void* stream) {
+  if (!c || !kv || !state || !x) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "lat_denoise_chunk needs an action-expert context");
+  if (!aligned16(kv) || !aligned16(state) || !aligned16(x)) return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!c->gexec || c->g_kv != kv || c->g_state != state || c->g_x != x || c->g_stream != stream) {
+    if (c->gexec) {
+      cudaGraphExecDestroy(c->gexec);
+      c->gexec = nullptr;
+    }
+    cudaStream_t cap = st;
+    bool own = false;
+    if (cap == nullptr) {  // the legacy stream cannot be captured: capture on a private one
+      CUDA_TRY(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+      own = true;
+    }
+    CUDA_TRY(cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal));
+    lat_status s = enqueue_denoise(c, reinterpret_cast<bf16*>(kv), state, x, cap);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cap, &g);
+    if (own) cudaStreamDestroy(cap);
+    if (s != LAT_OK) {
+      if (g) cudaGraphDestroy(g);
+      return s;
+    }
+    if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&c->gexec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    c->g_kv = kv;
+    c->g_state = state;
+    c->g_x = x;
+    c->g_stream = stream;
+  }
+  CUDA_TRY(cudaGraphLaunch(c->gexec, st));
+  return LAT_OK;
+}
+
+lat_status lat_debug_indices(lat_ctx* c, const lat_chunk_desc* chunks, int n, int* slot_out, int* pos_out) {
+  if (!c || !slot_out || !pos_out || n <= 0) return fail(LAT_ERR_ARG, "bad argument");
+  std::vector<int> ch(n, 0);
+  if (c->d.kind == LAT_DIT) {
+    if (!chunks) return fail(LAT_ERR_ARG, "chunks NULL");
+    for (int i = 0; i < n; ++i) {
+      if (chunks[i].chunk < 0) return fail(LAT_ERR_ARG, "negative chunk index");
+      ch[i] = chunks[i].chunk;
+    }
+  } else if (n > c->d.T_q) {
+    return fail(LAT_ERR_ARG, "n > T_q");
+  }
+  int *dch = nullptr, *ds = nullptr, *dp = nullptr;
+  CUDA_TRY(cudaMalloc(&dch, n * sizeof(int)));
+  CUDA_TRY(cudaMalloc(&ds, n * sizeof(int)));
+  CUDA_TRY(cudaMalloc(&dp, n * sizeof(int)));
+  cudaMemcpy(dch, ch.data(), n * sizeof(int), cudaMemcpyHostToDevice);
+  debug_indices_kernel<<<(n + 127) / 128, 128>>>(dch, n, c->d.kind, c->d.T_prefix, c->d.T_q, c->d.n_hist, ds, dp);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpy(slot_out, ds, n * sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(pos_out, dp, n * sizeof(int), cudaMemcpyDeviceToHost);
+  cudaFree(dch);
+  cudaFree(ds);
+  cudaFree(dp);
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "debug_indices: %s", cudaGetErrorString(e));
+  return LAT_OK;
+}
+
+lat_status lat_debug_gemm(lat_ctx* c, int which, int layer, int reps, void* stream) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "needs an action-expert context");
+  if (which < 0 || which > 3 || layer < 0 || layer >= c->d.L || reps < 0) return fail(LAT_ERR_ARG, "bad argument");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const lat_model_desc& d = c->d;
+  const int T = d.T_q, D = d.D, F = d.F, qd = d.Hq * d.dh;
+  for (int r = 0; r < reps; ++r) {
+    SkinnyArgs a{};
+    a.n_tok = T;
+    a.mode = B_PLAIN;
+    if (which == 0) {
+      a.src = c->xres; a.src_ld = D; a.out = c->qkv_acc; a.out_ld = c->nqkv;
+      LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, layer, a, st));
+    } else if (which == 1) {
+      a.src = c->o; a.src_ld = qd; a.out = c->xres; a.out_ld = D;
+      LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, layer, a, st));
+    } else if (which == 2) {
+      a.src = c->xres; a.src_ld = D; a.out = c->gu_acc; a.out_ld = 2 * F;
+      LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, layer, a, st));
+    } else {
+      a.src = c->gu_acc; a.src_ld = 2 * F; a.src2_off = F; a.row_scale = c->r2; a.mode = B_GEGLU;
+      a.out = c->xres; a.out_ld = D;
+      LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, layer, a, st));
+    }
+  }
+  CUDA_TRY(cudaMemsetAsync(c->qkv_acc, 0, (size_t)T * c->nqkv * 4, st));
+  CUDA_TRY(cudaMemsetAsync(c->gu_acc, 0, (size_t)T * 2 * F * 4, st));
+  return LAT_OK;
+}
+
+lat_status lat_sync(lat_ctx* c) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  CUDA_TRY(cudaDeviceSynchronize());
+  return check_dev_err(c);
+}
+
+void lat_destroy(lat_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  delete c;
+}
+
+}  // extern "C"

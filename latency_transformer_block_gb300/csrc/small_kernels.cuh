@@ -1,0 +1,242 @@
+// Small kernels of the action-expert path and the offline folds.
+#pragma once
+#include "common.cuh"
+
+namespace lat {
+
+// The integer maps used by the kernels, exposed for exact checks.
+//  pi0: query token t lives in cache slot T_prefix + t and has RoPE position
+//       T_prefix + t (the prefix occupies slots / positions 0..T_prefix-1).
+//  DiT: chunk c lives in ring slot c mod (n_hist + 1); its token j has RoPE
+//       position c * T_chunk + j.
+__host__ __device__ __forceinline__ int query_slot(int T_prefix, int t) { return T_prefix + t; }
+__host__ __device__ __forceinline__ int query_pos(int T_prefix, int t) { return T_prefix + t; }
+__host__ __device__ __forceinline__ int ring_slot_of(int chunk, int n_hist) { return chunk % (n_hist + 1); }
+__host__ __device__ __forceinline__ long long chunk_pos0(int chunk, int T) { return (long long)chunk * T; }
+
+
+// ---------------------------------------------------------------------------
+// QKV epilogue (runs once the split-K sums are complete):
+//   y = r1[t] * acc[t]              (RMS row factor applied after the GEMM)
+//   q = RoPE(y_q), k = RoPE(y_k), v = y_v
+//   q -> fp32 q buffer; k, v -> bf16 into the cache at slot (slot0 + t)
+// then zero the consumed accumulator row and the FFN accumulator row.
+// Rotate-half RoPE with cos/sin tables [T_q][dh/2] (fp32, from float64).
+// Grid T_q, blockDim 256.
+// ---------------------------------------------------------------------------
+struct QkvEpiArgs {
+  float* acc;                // fp32 [T_q][nqkv] (zeroed after reading)
+  int nqkv;
+  const float* r1;           // [T_q]
+  const float* cos_t;        // [T_q][dh/2]
+  const float* sin_t;
+  float* q;                  // fp32 [T_q][Hq*dh]
+  __nv_bfloat16* k_cache;    // plane K of this layer, row stride kv_ld
+  __nv_bfloat16* v_cache;
+  int kv_ld;
+  int slot0;
+  int Hq, Hkv, dh;
+  float* zero2;              // optional: second buffer row to clear, [T_q][zero2_ld]
+  int zero2_ld;
+};
+
+__global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
+  const int t = blockIdx.x;
+  const int half = a.dh / 2;
+  const float r = a.r1[t];
+  float* row = a.acc + (size_t)t * a.nqkv;
+  const float* ct = a.cos_t + (size_t)t * half;
+  const float* st = a.sin_t + (size_t)t * half;
+  const int nq_pairs = a.Hq * half, nk_pairs = a.Hkv * half;
+  for (int p = threadIdx.x; p < nq_pairs + nk_pairs; p += blockDim.x) {
+    const bool isq = p < nq_pairs;
+    const int pp = isq ? p : p - nq_pairs;
+    const int head = pp / half, i = pp % half;
+    const int base = (isq ? 0 : a.Hq * a.dh) + head * a.dh;
+    const float x0 = r * row[base + i], x1 = r * row[base + i + half];
+    const float c = ct[i], s = st[i];
+    const float y0 = x0 * c - x1 * s, y1 = x1 * c + x0 * s;
+    if (isq) {
+      a.q[(size_t)t * a.Hq * a.dh + head * a.dh + i] = y0;
+      a.q[(size_t)t * a.Hq * a.dh + head * a.dh + i + half] = y1;
+    } else {
+      __nv_bfloat16* kr = a.k_cache + (size_t)query_slot(a.slot0, t) * a.kv_ld + head * a.dh;
+      kr[i] = __float2bfloat16_rn(y0);
+      kr[i + half] = __float2bfloat16_rn(y1);
+    }
+  }
+  const int vbase = (a.Hq + a.Hkv) * a.dh;
+  for (int j = threadIdx.x; j < a.Hkv * a.dh; j += blockDim.x)
+    a.v_cache[(size_t)query_slot(a.slot0, t) * a.kv_ld + j] = __float2bfloat16_rn(r * row[vbase + j]);
+  __syncthreads();
+  for (int j = threadIdx.x; j < a.nqkv; j += blockDim.x) row[j] = 0.f;
+  if (a.zero2)
+    for (int j = threadIdx.x; j < a.zero2_ld; j += blockDim.x) a.zero2[(size_t)t * a.zero2_ld + j] = 0.f;
+}
+
+// ---------------------------------------------------------------------------
+// Embedding prologue of one denoise step (folded form, section 4.2 of the note):
+//   z[t][n]      = sum_a x[t][a] W'[a][n] + T[s][n]      (t < T_q - 1)
+//   xres[0][n]   = state token (precomputed for the chunk)
+//   xres[1+t][n] = b2[n]   (the W2 GEMM accumulates SiLU(z) W2 on top)
+// Grid (ceil(D/256), T_q), blockDim 256; row blockIdx.y == T_q - 1 writes the state row.
+// ---------------------------------------------------------------------------
+struct EmbedArgs {
+  const float* x;        // actions fp32 [T_q-1][A]
+  const float* wfold;    // fp32 [A][D]
+  const float* ttab;     // fp32 [S][D]
+  const float* b2;       // fp32 [D]
+  const float* state_emb;  // fp32 [D]
+  float* z;              // fp32 [T_q-1][D]
+  float* xres;           // fp32 [T_q][D]
+  int D, A, T_q, step;
+};
+
+__global__ void embed_prologue_kernel(EmbedArgs a) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  const int t = blockIdx.y;
+  if (n >= a.D) return;
+  if (t == a.T_q - 1) {
+    a.xres[n] = a.state_emb[n];
+    return;
+  }
+  float acc = a.ttab[(size_t)a.step * a.D + n];
+  const float* xr = a.x + (size_t)t * a.A;
+  for (int j = 0; j < a.A; ++j) acc = fmaf(xr[j], a.wfold[(size_t)j * a.D + n], acc);
+  a.z[(size_t)t * a.D + n] = acc;
+  a.xres[(size_t)(1 + t) * a.D + n] = a.b2[n];
+}
+
+// ---------------------------------------------------------------------------
+// Head + Euler update: for action row t (residual row 1 + t)
+//   v[t][a] = r * sum_n h[1+t][n] W'out[n][a] + b_out[a],  r = RMS factor
+//   x[t][a] += dt * v[t][a]
+// W'out = diag(g_final) W_out in fp32.  Grid T_q - 1, blockDim 256.
+// ---------------------------------------------------------------------------
+struct HeadArgs {
+  const float* xres;     // [T_q][D]
+  const float* wout;     // fp32 [D][A]
+  const float* bout;     // fp32 [A]
+  float* x;              // [T_q-1][A]
+  const float* dt;       // device scalar table [S]
+  int step, D, A;
+  float eps;
+};
+
+__global__ void head_euler_kernel(HeadArgs a) {
+  const int t = blockIdx.x;
+  const float* h = a.xres + (size_t)(1 + t) * a.D;
+  __shared__ float red[8][33];
+  __shared__ float rs;
+  // RMS factor
+  float ss = 0.f;
+  for (int n = threadIdx.x; n < a.D; n += blockDim.x) ss += h[n] * h[n];
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp][32] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][32];
+    rs = rsqrtf(s / a.D + a.eps);
+  }
+  __syncthreads();
+  // A outputs: thread (warp w, lane l) accumulates column l over rows n = w, w+8, ...
+  for (int a0 = 0; a0 < a.A; a0 += 32) {
+    const int col = a0 + lane;
+    float acc = 0.f;
+    if (col < a.A)
+      for (int n = warp; n < a.D; n += (int)(blockDim.x >> 5)) acc = fmaf(h[n], a.wout[(size_t)n * a.A + col], acc);
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && col < a.A) {
+      float s = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][lane];
+      const float v = rs * s + a.bout[col];
+      a.x[(size_t)t * a.A + col] += a.dt[a.step] * v;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Offline folds
+// ---------------------------------------------------------------------------
+// out[n][k] = bf16( g[k] * W[k][n] )  -- transpose to K-major with the RMSNorm
+// scale folded (g may be null: plain transpose).  W: bf16 [K][N] row-major;
+// out row stride = K.  32 x 32 tiles, blockDim (32, 8).
+__global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, __nv_bfloat16* out, int K,
+                                      int N) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int k = k0 + i, n = n0 + threadIdx.x;
+    float v = 0.f;
+    if (k < K && n < N) {
+      v = __bfloat162float(W[(size_t)k * N + n]);
+      if (g) v *= __bfloat162float(g[k]);   // exact in fp32: 8 x 8 significant bits
+    }
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int n = n0 + i, k = k0 + threadIdx.x;
+    if (n < N && k < K) out[(size_t)n * K + k] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+  }
+}
+
+// Generic small fp32 GEMM for the offline tables (CUDA cores, fp32 accumulate):
+//   C[m][n] = act( sum_k A[m][k] B[k][n] + bias[n] )
+// A, B, bias each either bf16 or fp32 (flags).  act: 0 none, 1 SiLU.
+struct SmallGemmArgs {
+  const void* A; int a_bf16; int lda;
+  const void* B; int b_bf16; int ldb;
+  const void* bias; int bias_bf16;
+  float* C; int ldc;
+  int M, N, K, act;
+};
+
+__device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
+  return is_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
+                 : reinterpret_cast<const float*>(p)[i];
+}
+
+__global__ void small_gemm_kernel(SmallGemmArgs a) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  const int m = blockIdx.y;
+  if (n >= a.N) return;
+  float acc = 0.f;
+  for (int k = 0; k < a.K; ++k)
+    acc = fmaf(ld_any(a.A, a.a_bf16, (size_t)m * a.lda + k), ld_any(a.B, a.b_bf16, (size_t)k * a.ldb + n), acc);
+  if (a.bias) acc += ld_any(a.bias, a.bias_bf16, n);
+  if (a.act == 1) acc = silu(acc);
+  a.C[(size_t)m * a.ldc + n] = acc;
+}
+
+// out[k][n] = g[k] * W[k][n] in fp32 (head fold; exact).
+__global__ void scale_rows_f32_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, float* out, int K, int N) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)K * N) return;
+  const int k = (int)(i / N);
+  out[i] = __bfloat162float(W[i]) * __bfloat162float(g[k]);
+}
+
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* in, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __bfloat162float(in[i]);
+}
+
+__global__ void debug_indices_kernel(const int* chunks, int n, int kind, int T_prefix, int T_q, int n_hist,
+                                     int* slot_out, int* pos_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  if (kind == 2) {
+    slot_out[i] = ring_slot_of(chunks[i], n_hist);
+    pos_out[i] = (int)chunk_pos0(chunks[i], T_q);
+  } else {
+    slot_out[i] = query_slot(T_prefix, i);
+    pos_out[i] = query_pos(T_prefix, i);
+  }
+}
+
+}  // namespace lat

@@ -1,0 +1,80 @@
+"""Model wrappers: upload seeded weights to the GPU and create a lat context.
+
+PyTorch is used only to hold device memory and streams; all arithmetic of the
+path runs in liblat.so.
+"""
+import numpy as np
+import torch
+
+from . import lat
+
+
+def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    """Upload bf16 bit patterns (uint16) as a torch bfloat16 tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def desc_from_config(cfg: dict, kind: int, max_batch: int = 1, n_streams: int = 1) -> lat.ModelDesc:
+    d = lat.ModelDesc()
+    d.kind = kind
+    d.D = cfg["D"]
+    if cfg["kind"] == "dit":
+        d.Hq = d.Hkv = cfg["H"]
+    else:
+        d.Hq, d.Hkv = cfg["Hq"], cfg["Hkv"]
+    d.dh, d.F, d.L = cfg["dh"], cfg["F"], cfg["L"]
+    d.S = cfg.get("S", 0)
+    d.T_prefix = cfg.get("T_prefix", 0) if cfg["kind"] != "dit" else 0
+    d.T_q = cfg["T_chunk"] if cfg["kind"] == "dit" else cfg["T_q"]
+    d.act_dim = cfg.get("act_dim", 0)
+    d.n_hist = cfg.get("n_hist", 0)
+    d.t_dim = cfg.get("t_dim", 0)
+    d.patch_dim = cfg.get("patch_dim", 0)
+    d.max_batch = max_batch
+    d.n_streams = n_streams
+    d.rope_base = cfg["rope_base"]
+    d.eps = cfg["eps"]
+    return d
+
+
+class Pi0ActionExpert:
+    """The pi0 action expert behind lat_denoise_chunk / lat_block_forward."""
+
+    def __init__(self, cfg: dict, weight_bits: dict, device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        keep = []
+
+        def up(x):
+            t = _dev_bf16(x, self.device)
+            keep.append(t)
+            return lat.ptr(t)
+
+        L = cfg["L"]
+        blocks = (lat.BlockWeights * L)()
+        for l, b in enumerate(weight_bits["blocks"]):
+            for k in ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "wg", "wu", "wd"):
+                setattr(blocks[l], k, up(b[k]))
+        w = lat.Weights()
+        w.blocks = blocks
+        for k in ("w_in", "b_in", "w1", "b1", "w2", "b2", "w_state", "b_state", "g_final", "w_out", "b_out"):
+            setattr(w, k, up(weight_bits[k]))
+        self._blocks = blocks
+        self.ctx = lat.Context(desc_from_config(cfg, lat.LAT_PI0_ACTION_EXPERT), w)
+        torch.cuda.synchronize()
+        del keep  # the library folded its own copies
+
+    def kv_from_bits(self, kv_bits: np.ndarray) -> torch.Tensor:
+        return _dev_bf16(kv_bits, self.device)
+
+    def denoise(self, kv: torch.Tensor, state: torch.Tensor, x: torch.Tensor, stream=None):
+        self.ctx.denoise_chunk(kv, state, x, stream)
+
+    def block(self, layer: int, x: torch.Tensor, kv_layer: torch.Tensor, stream=None):
+        self.ctx.block_forward(layer, x, kv_layer, None, stream)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """bf16 torch tensor -> uint16 bit patterns (host)."""
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)

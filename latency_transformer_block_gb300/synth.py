@@ -200,6 +200,11 @@ def pi0_inputs(cfg: dict, seed: int = 0) -> dict:
     }
 
 
+def residual_stream(cfg: dict, seed: int = 0, std: float = 0.5, tag: str = "xres") -> np.ndarray:
+    """A residual-stream input for one block, N(0, std^2) fp32 [T_q][D]."""
+    return normal_f32(seed, tag, (cfg["T_q"], cfg["D"]), std)
+
+
 def prefill_weights(cfg: dict, seed: int = 0) -> dict:
     D, P = cfg["D"], cfg["patch_dim"]
     w = WEIGHT_STD

@@ -24,6 +24,13 @@ def round_rne(x: np.ndarray) -> np.ndarray:
     treated specially.
     """
     x = np.asarray(x, dtype=np.float64)
+    x32 = x.astype(np.float32)
+    if np.array_equal(x32.astype(np.float64), x):
+        # exactly a float32 (e.g. a product of two bf16 values): round the
+        # 32-bit pattern, adding half an ulp of bf16 plus the tie-to-even bit
+        u = x32.view(np.uint32)
+        u = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) & np.uint32(0xFFFF0000)
+        return u.view(np.float32).astype(np.float64)
     m, e = np.frexp(x)
     return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
 

@@ -29,6 +29,18 @@ def test_bf16_round_matches_torch_conversion():
     assert np.array_equal(bf16.encode(x.astype(np.float64)), ref_bits)
 
 
+def test_bf16_round_paths_agree():
+    # values that are exact float32 take the bit path, others the frexp path;
+    # adding 2^-40 relative moves a value off float32 without crossing a bf16
+    # rounding boundary (except exact ties, which the offset breaks upward)
+    x = (RNG.standard_normal(100_000) * np.exp(RNG.uniform(-10, 10, 100_000))).astype(np.float32)
+    x = x.astype(np.float64)
+    a = bf16.round_rne(x)
+    b = bf16.round_rne(x * (1 + 2.0 ** -40))
+    tie = np.abs(x - a) == 0.5 * bf16.ulp(a)
+    assert np.array_equal(a[~tie], b[~tie])
+
+
 def test_bf16_ties_to_even_and_decode():
     # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to the even mantissa (1.0)
     assert bf16.round_rne(np.array([1 + 2.0 ** -8]))[0] == 1.0
