@@ -208,12 +208,15 @@ lat_status lat_debug_indices(lat_ctx *ctx, const lat_chunk_desc *chunks, int n, 
 
 /*
  * lat_debug_gemm -- measurement hook for the action expert: enqueue `reps`
- * back-to-back launches of one streamed projection of block `layer`
- * (which: 0 = merged QKV, 1 = attention output, 2 = gate/up, 3 = down) on the
- * context's own workspace, then clear the accumulators it touched.  Used to
- * time the weight-streaming kernel alone with events on `stream`.
+ * back-to-back launches of one streamed projection (which: 0 = merged QKV,
+ * 1 = attention output, 2 = gate/up, 3 = down) of blocks layer, layer+1, ...
+ * (mod L, so successive launches stream different weights from HBM) on the
+ * context's own workspace.  Used to time the weight-streaming kernel alone with
+ * events on `stream`.  The workspace accumulators are left dirty: call
+ * lat_debug_clear before the next lat_denoise_chunk / lat_block_forward.
  */
 lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *stream);
+lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 
 /* Wait for all work of the context and report a recorded device-side error. */
 lat_status lat_sync(lat_ctx *ctx);

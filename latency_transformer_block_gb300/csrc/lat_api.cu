@@ -634,26 +634,34 @@ lat_status lat_debug_gemm(lat_ctx* c, int which, int layer, int reps, void* stre
   const lat_model_desc& d = c->d;
   const int T = d.T_q, D = d.D, F = d.F, qd = d.Hq * d.dh;
   for (int r = 0; r < reps; ++r) {
+    const int l = (layer + r) % d.L;   // successive launches read different layers' weights (HBM, not L2)
     SkinnyArgs a{};
     a.n_tok = T;
     a.mode = B_PLAIN;
     if (which == 0) {
       a.src = c->xres; a.src_ld = D; a.out = c->qkv_acc; a.out_ld = c->nqkv;
-      LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, layer, a, st));
+      LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, l, a, st));
     } else if (which == 1) {
       a.src = c->o; a.src_ld = qd; a.out = c->xres; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, layer, a, st));
+      LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, l, a, st));
     } else if (which == 2) {
       a.src = c->xres; a.src_ld = D; a.out = c->gu_acc; a.out_ld = 2 * F;
-      LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, layer, a, st));
+      LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, l, a, st));
     } else {
       a.src = c->gu_acc; a.src_ld = 2 * F; a.src2_off = F; a.row_scale = c->r2; a.mode = B_GEGLU;
       a.out = c->xres; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, layer, a, st));
+      LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, l, a, st));
     }
   }
-  CUDA_TRY(cudaMemsetAsync(c->qkv_acc, 0, (size_t)T * c->nqkv * 4, st));
-  CUDA_TRY(cudaMemsetAsync(c->gu_acc, 0, (size_t)T * 2 * F * 4, st));
+  return LAT_OK;
+}
+
+lat_status lat_debug_clear(lat_ctx* c, void* stream) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const lat_model_desc& d = c->d;
+  CUDA_TRY(cudaMemsetAsync(c->qkv_acc, 0, (size_t)d.T_q * c->nqkv * 4, st));
+  CUDA_TRY(cudaMemsetAsync(c->gu_acc, 0, (size_t)d.T_q * 2 * d.F * 4, st));
   return LAT_OK;
 }
 

@@ -73,6 +73,8 @@ def lib():
         L.lat_debug_indices.restype = st
         L.lat_debug_gemm.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
         L.lat_debug_gemm.restype = st
+        L.lat_debug_clear.argtypes = [_P, _P]
+        L.lat_debug_clear.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -140,6 +142,9 @@ class Context:
 
     def debug_gemm(self, which, layer, reps, stream=None):
         check(lib().lat_debug_gemm(self.handle, which, layer, reps, stream_ptr(stream)))
+
+    def debug_clear(self, stream=None):
+        check(lib().lat_debug_clear(self.handle, stream_ptr(stream)))
 
     def sync(self):
         check(lib().lat_sync(self.handle))

@@ -27,3 +27,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every parity comparison of the session to $LAT_PARITY_REPORT (if set)."""
+    path = os.environ.get("LAT_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from tests.parity import REPORT
+    except Exception:
+        return
+    with open(path, "w") as f:
+        for what, val, bound in REPORT:
+            f.write(f"{what}\t{val:.4e}\t{bound:.1e}\n")

@@ -12,7 +12,7 @@ import torch
 from latency_transformer_block_gb300 import lat, synth
 from latency_transformer_block_gb300.models import Pi0ActionExpert, bits_of
 from oracle import bf16, pi0
-from tests.parity import BLOCK_TOL, FINAL_TOL, assert_bf16_close, assert_rel
+from tests.parity import BLOCK_TOL, FINAL_TOL, assert_bf16_close, assert_rel, assert_scale_rel
 
 pytestmark = pytest.mark.gpu
 
@@ -75,9 +75,11 @@ def test_denoise_parity(name, over):
     Tp = cfg["T_prefix"]
     got_kv = bits_of(kv)
     assert np.array_equal(got_kv[:, :, :Tp], ib["kv"][:, :, :Tp])
-    # own slots hold the last step's K/V; after S steps small differences in x may
-    # move a few more values across a rounding boundary
-    assert_bf16_close(got_kv[:, :, Tp:], ref_kv[:, :, Tp:], f"{name} final own KV", max_ulp=2, min_exact=0.95)
+    # own slots hold the last step's K/V, bf16 values that sit at the end of the
+    # whole chain; near the 1e-3 floor one bf16 ulp alone is up to 0.8 %, so they
+    # are held to the final tolerance relative to their RMS (scale-relative)
+    assert_scale_rel(bf16.decode(got_kv[:, :, Tp:]), bf16.decode(ref_kv[:, :, Tp:]), FINAL_TOL,
+                     f"{name} final own KV")
 
 
 def test_constant_velocity_field_is_exact():
