@@ -218,6 +218,20 @@ lat_status lat_debug_indices(lat_ctx *ctx, const lat_chunk_desc *chunks, int n, 
 lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *stream);
 lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 
+/*
+ * lat_debug_attention -- the chunk attention of an action-expert context
+ * alone (kernel-level parity and timing): out = softmax(q k^T / sqrt(dh)) v,
+ * no mask, query head h reading KV head h / (Hq / Hkv), using the context's
+ * head layout and its workspace for the key-range partials.
+ *  q:   device fp32 [T_q][Hq*dh] (RoPE already applied);
+ *  k,v: device bf16 [T_kv][Hkv*dh];
+ *  out: device fp32 [T_q][Hq*dh].
+ * 1 <= T_q <= the context's T_q, 1 <= T_kv <= T_prefix + T_q of the context.
+ * Reuses the context's workspace: not concurrent with other calls on it.
+ */
+lat_status lat_debug_attention(lat_ctx *ctx, const float *q, const void *k, const void *v, float *out, int T_q,
+                               int T_kv, void *stream);
+
 /* Wait for all work of the context and report a recorded device-side error. */
 lat_status lat_sync(lat_ctx *ctx);
 

@@ -60,7 +60,7 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint3
 }
 
 template <int DH>
-__global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
+static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
   constexpr int KB = 64;          // keys per block
   constexpr int LD = DH + 8;      // padded smem row (bf16): conflict-free ldmatrix
   constexpr int NT = DH / 8;      // output n-tiles
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
       split_pair(x11.x, x11.y, ah[3], am[3], al[3]);
 #pragma unroll
       for (int jp = 0; jp < 4; ++jp) {
-        // matrices: keys jp*16 + (0..7 | 8..15), d ks*16 + (0..7 | 8..7)
+        // matrices: keys jp*16 + (0..7 | 8..15), d ks*16 + (0..7 | 8..15)
         const int mi = lane >> 3, rr = lane & 7;
         const int key = jp * 16 + ((mi >> 1) << 3) + rr;
         const int col = ks * 16 + ((mi & 1) << 3);
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
 
 // Merge key-range partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // Grid (T_q, Hq), blockDim = dh.
-__global__ void attention_combine_kernel(AttnArgs a, int dh) {
+static __global__ void attention_combine_kernel(AttnArgs a, int dh) {
   const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   float M = -INFINITY;
   for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.part_m[((size_t)s * a.Hq + h) * a.T_q + t]);
@@ -245,6 +245,28 @@ __global__ void attention_combine_kernel(AttnArgs a, int dh) {
     acc += w * a.part_o[i * dh + d];
   }
   a.out[(size_t)t * a.out_ld + h * dh + d] = acc / L;
+}
+
+// Launch the attention (and the combine when there are several key ranges).
+// The kernels need more than 48 KB of dynamic shared memory for dh = 256:
+// call set_attention_smem_limits() once per device first.
+static inline cudaError_t set_attention_smem_limits() {
+  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 72 * 2);
+  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 136 * 2);
+  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 264 * 2);
+  return cudaGetLastError();
+}
+
+static inline cudaError_t launch_chunk_attention(const AttnArgs& a, int dh, cudaStream_t st) {
+  dim3 grid(a.Hq, (a.T_q + 63) / 64, a.n_split);
+  const int smem = 2 * 64 * (dh + 8) * 2;
+  if (dh == 64) attention_kernel<64><<<grid, 128, smem, st>>>(a);
+  else if (dh == 128) attention_kernel<128><<<grid, 128, smem, st>>>(a);
+  else attention_kernel<256><<<grid, 128, smem, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_split == 1) return e;
+  attention_combine_kernel<<<dim3(a.T_q, a.Hq), dh, 0, st>>>(a, dh);
+  return cudaGetLastError();
 }
 
 }  // namespace lat

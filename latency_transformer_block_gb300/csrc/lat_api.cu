@@ -28,6 +28,11 @@ typedef __nv_bfloat16 bf16;
 // ---------------------------------------------------------------------------
 static thread_local std::string g_last_error;
 
+lat_status lat_internal_fail(lat_status s, const char* msg) {
+  g_last_error = msg;
+  return s;
+}
+
 static lat_status fail(lat_status s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -371,6 +376,23 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
 }
 
 // ---------------------------------------------------------------------------
+// chunk attention: key-range partials (n_split > 1) merged by the combine kernel
+// ---------------------------------------------------------------------------
+static lat_status enqueue_attention(const lat_model_desc& d, const float* q, int q_ld, const bf16* k, const bf16* v,
+                                    int kv_ld, int T_q, int T_kv, int n_split, float* out, int out_ld, float* pm,
+                                    float* pl, float* po, cudaStream_t st) {
+  AttnArgs a{};
+  a.q = q; a.q_ld = q_ld; a.k = k; a.v = v; a.kv_ld = kv_ld;
+  a.T_q = T_q; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+  a.n_split = n_split;
+  a.out = out; a.out_ld = out_ld; a.part_m = pm; a.part_l = pl; a.part_o = po;
+  cudaError_t e = launch_chunk_attention(a, d.dh, st);
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch attention: %s", cudaGetErrorString(e));
+  return LAT_OK;
+}
+
+// ---------------------------------------------------------------------------
 // one pi0 block on the residual stream xres [T_q][D]; kv_layer = [2][T_kv][kvd]
 // ---------------------------------------------------------------------------
 static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_layer, cudaStream_t st) {
@@ -396,24 +418,7 @@ static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_lay
     LAT_TRY(launch_check("qkv_epilogue"));
   }
   // 3. attention over [prefix | own] (key ranges) + combine
-  {
-    AttnArgs a{};
-    a.q = c->q; a.q_ld = qd; a.k = kc; a.v = vc; a.kv_ld = kvd;
-    a.T_q = T; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
-    a.n_split = c->attn_split;
-    a.out = c->o; a.out_ld = qd; a.part_m = c->pm; a.part_l = c->pl; a.part_o = c->po;
-    dim3 grid(d.Hq, (T + 63) / 64, a.n_split);
-    const int smem = 2 * 64 * (d.dh + 8) * 2;
-    if (d.dh == 64) attention_kernel<64><<<grid, 128, smem, st>>>(a);
-    else if (d.dh == 128) attention_kernel<128><<<grid, 128, smem, st>>>(a);
-    else attention_kernel<256><<<grid, 128, smem, st>>>(a);
-    LAT_TRY(launch_check("attention"));
-    if (a.n_split > 1) {
-      attention_combine_kernel<<<dim3(T, d.Hq), d.dh, 0, st>>>(a, d.dh);
-      LAT_TRY(launch_check("attention_combine"));
-    }
-  }
+  LAT_TRY(enqueue_attention(d, c->q, qd, kc, vc, kvd, T, T_kv, c->attn_split, c->o, qd, c->pm, c->pl, c->po, st));
   // 4. x += o Wo
   {
     SkinnyArgs a{};
@@ -503,9 +508,7 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
   if (!attr_done) {
     cudaFuncSetAttribute(skinny_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          skinny_smem_bytes(kStages));
-    cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 72 * 2);
-    cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 136 * 2);
-    cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 264 * 2);
+    set_attention_smem_limits();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       delete c;
@@ -654,6 +657,21 @@ lat_status lat_debug_gemm(lat_ctx* c, int which, int layer, int reps, void* stre
     }
   }
   return LAT_OK;
+}
+
+lat_status lat_debug_attention(lat_ctx* c, const float* q, const void* k, const void* v, float* out, int T_q,
+                               int T_kv, void* stream) {
+  if (!c || !q || !k || !v || !out) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "needs an action-expert context");
+  const lat_model_desc& d = c->d;
+  if (T_q < 1 || T_q > d.T_q || T_kv < 1 || T_kv > d.T_prefix + d.T_q)
+    return fail(LAT_ERR_SHAPE, "T_q / T_kv out of the context's range");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  const int n_split = (T_kv + 63) / 64;
+  return enqueue_attention(d, q, d.Hq * d.dh, reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v),
+                           d.Hkv * d.dh, T_q, T_kv, n_split, out, d.Hq * d.dh, c->pm, c->pl, c->po,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 lat_status lat_debug_clear(lat_ctx* c, void* stream) {

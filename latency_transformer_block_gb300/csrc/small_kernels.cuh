@@ -40,7 +40,7 @@ struct QkvEpiArgs {
   int zero2_ld;
 };
 
-__global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
+static __global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
   const int t = blockIdx.x;
   const int half = a.dh / 2;
   const float r = a.r1[t];
@@ -92,7 +92,7 @@ struct EmbedArgs {
   int D, A, T_q, step;
 };
 
-__global__ void embed_prologue_kernel(EmbedArgs a) {
+static __global__ void embed_prologue_kernel(EmbedArgs a) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int t = blockIdx.y;
   if (n >= a.D) return;
@@ -123,7 +123,7 @@ struct HeadArgs {
   float eps;
 };
 
-__global__ void head_euler_kernel(HeadArgs a) {
+static __global__ void head_euler_kernel(HeadArgs a) {
   const int t = blockIdx.x;
   const float* h = a.xres + (size_t)(1 + t) * a.D;
   __shared__ float red[8][33];
@@ -165,7 +165,7 @@ __global__ void head_euler_kernel(HeadArgs a) {
 // out[n][k] = bf16( g[k] * W[k][n] )  -- transpose to K-major with the RMSNorm
 // scale folded (g may be null: plain transpose).  W: bf16 [K][N] row-major;
 // out row stride = K.  32 x 32 tiles, blockDim (32, 8).
-__global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, __nv_bfloat16* out, int K,
+static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, __nv_bfloat16* out, int K,
                                       int N) {
   __shared__ float tile[32][33];
   const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
@@ -201,7 +201,7 @@ __device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
                  : reinterpret_cast<const float*>(p)[i];
 }
 
-__global__ void small_gemm_kernel(SmallGemmArgs a) {
+static __global__ void small_gemm_kernel(SmallGemmArgs a) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int m = blockIdx.y;
   if (n >= a.N) return;
@@ -214,19 +214,19 @@ __global__ void small_gemm_kernel(SmallGemmArgs a) {
 }
 
 // out[k][n] = g[k] * W[k][n] in fp32 (head fold; exact).
-__global__ void scale_rows_f32_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, float* out, int K, int N) {
+static __global__ void scale_rows_f32_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, float* out, int K, int N) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)K * N) return;
   const int k = (int)(i / N);
   out[i] = __bfloat162float(W[i]) * __bfloat162float(g[k]);
 }
 
-__global__ void bf16_to_f32_kernel(const __nv_bfloat16* in, float* out, int n) {
+static __global__ void bf16_to_f32_kernel(const __nv_bfloat16* in, float* out, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) out[i] = __bfloat162float(in[i]);
 }
 
-__global__ void debug_indices_kernel(const int* chunks, int n, int kind, int T_prefix, int T_q, int n_hist,
+static __global__ void debug_indices_kernel(const int* chunks, int n, int kind, int T_prefix, int T_q, int n_hist,
                                      int* slot_out, int* pos_out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;

@@ -73,6 +73,8 @@ def lib():
         L.lat_debug_indices.restype = st
         L.lat_debug_gemm.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
         L.lat_debug_gemm.restype = st
+        L.lat_debug_attention.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P]
+        L.lat_debug_attention.restype = st
         L.lat_debug_clear.argtypes = [_P, _P]
         L.lat_debug_clear.restype = st
         L.lat_sync.argtypes = [_P]
@@ -142,6 +144,10 @@ class Context:
 
     def debug_gemm(self, which, layer, reps, stream=None):
         check(lib().lat_debug_gemm(self.handle, which, layer, reps, stream_ptr(stream)))
+
+    def debug_attention(self, q, k, v, out, T_q, T_kv, stream=None):
+        check(lib().lat_debug_attention(self.handle, ptr(q), ptr(k), ptr(v), ptr(out), T_q, T_kv,
+                                        stream_ptr(stream)))
 
     def debug_clear(self, stream=None):
         check(lib().lat_debug_clear(self.handle, stream_ptr(stream)))

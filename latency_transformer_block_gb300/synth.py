@@ -205,6 +205,15 @@ def residual_stream(cfg: dict, seed: int = 0, std: float = 0.5, tag: str = "xres
     return normal_f32(seed, tag, (cfg["T_q"], cfg["D"]), std)
 
 
+def attention_inputs(T_q, T_kv, Hq, Hkv, dh, seed=0, q_std=0.6):
+    """q fp32 [T_q][Hq*dh] ~ N(0, q_std^2); k, v bf16 [T_kv][Hkv*dh] ~ N(0,1)."""
+    return {
+        "q": normal_f32(seed, "attn_q", (T_q, Hq * dh), q_std),
+        "k": normal_bf16(seed, "attn_k", (T_kv, Hkv * dh)),
+        "v": normal_bf16(seed, "attn_v", (T_kv, Hkv * dh)),
+    }
+
+
 def prefill_weights(cfg: dict, seed: int = 0) -> dict:
     D, P = cfg["D"], cfg["patch_dim"]
     w = WEIGHT_STD

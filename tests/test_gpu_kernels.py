@@ -1,0 +1,44 @@
+"""Kernel-level GPU parity: single kernels of the path against the oracle's
+matching piece (through the C ABI's measurement hooks)."""
+import numpy as np
+import pytest
+import torch
+
+from latency_transformer_block_gb300 import synth
+from latency_transformer_block_gb300.models import Pi0ActionExpert, _dev_bf16
+from oracle import bf16, ops
+from tests.parity import BLOCK_TOL, assert_rel
+
+pytestmark = pytest.mark.gpu
+
+_CTX = {}
+
+
+def _ctx(name):
+    if name not in _CTX:
+        cfg = synth.config(name)
+        _CTX[name] = (cfg, Pi0ActionExpert(cfg, synth.pi0_weights(cfg, 0)))
+    return _CTX[name]
+
+
+def run_attention(m, cfg, T_q, T_kv, seed):
+    Hq, Hkv, dh = cfg["Hq"], cfg["Hkv"], cfg["dh"]
+    a = synth.attention_inputs(T_q, T_kv, Hq, Hkv, dh, seed)
+    q = torch.from_numpy(a["q"]).cuda()
+    k = _dev_bf16(a["k"], "cuda")
+    v = _dev_bf16(a["v"], "cuda")
+    out = torch.full((T_q, Hq * dh), float("nan"), device="cuda")
+    m.ctx.debug_attention(q, k, v, out, T_q, T_kv)
+    m.ctx.sync()
+    ref = ops.attention(a["q"].astype(np.float64).reshape(T_q, Hq, dh),
+                        bf16.decode(a["k"]).reshape(T_kv, Hkv, dh),
+                        bf16.decode(a["v"]).reshape(T_kv, Hkv, dh), 1.0 / np.sqrt(dh))
+    return out.cpu().numpy(), ref.reshape(T_q, Hq * dh)
+
+
+@pytest.mark.parametrize("name,T_q,T_kv", [("tiny", 64, 192), ("pi0_ae", 64, 576), ("pi0_ae", 37, 100),
+                                           ("pi0_ae", 5, 1), ("tiny", 1, 129)])
+def test_attention_kernel(name, T_q, T_kv):
+    cfg, m = _ctx(name)
+    got, ref = run_attention(m, cfg, T_q, T_kv, seed=T_q * 1000 + T_kv)
+    assert_rel(got, ref, BLOCK_TOL, f"attention {name} {T_q}x{T_kv}")
