@@ -232,6 +232,35 @@ lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 lat_status lat_debug_attention(lat_ctx *ctx, const float *q, const void *k, const void *v, float *out, int T_q,
                                int T_kv, void *stream);
 
+/*
+ * lat_chunk_attention_noalloc -- the chunk attention for callers that cannot
+ * allocate device memory.  (No counterpart on the pages: it is a packaging of
+ * the attention step for such callers.)
+ *
+ * Who needs it: code that owns every byte of device memory itself -- an
+ * inference engine with its own memory pool, or a real-time control loop that
+ * forbids allocation once it runs -- can neither call cudaMalloc nor create a
+ * context (lat_create allocates weights and workspace).  This call needs no
+ * context and allocates nothing: the key-range partials it merges live in one
+ * static device array of 4 MiB (1048576 floats) inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ *
+ *  out = softmax(q k^T / sqrt(dh)) v per query head, no mask, query head h
+ *  reading KV head h / (Hq / Hkv).
+ *  q:   device fp32 [T_q][Hq*dh];  k, v: device bf16 [T_kv][Hkv*dh];
+ *  out: device fp32 [T_q][Hq*dh].  dh in {64, 128, 256}.
+ * Limit: Hq * T_q * (dh + 2) <= 1048576 (one key range of partials), else
+ * LAT_ERR_SHAPE; larger T_kv only means fewer, longer key ranges.
+ * The first call on a device (with that device current) looks up the array's
+ * device address and sets the kernels' shared-memory limit; make that first
+ * call before any stream capture.  Every call shares the one array: calls that
+ * overlap on the GPU (different streams, or different host threads) race on
+ * it and must be serialised by the caller.  Nothing in it needs clearing: a
+ * call writes every partial it reads.
+ */
+lat_status lat_chunk_attention_noalloc(const float *q, const void *k, const void *v, float *out, int T_q,
+                                       int T_kv, int Hq, int Hkv, int dh, void *stream);
+
 /* Wait for all work of the context and report a recorded device-side error. */
 lat_status lat_sync(lat_ctx *ctx);
 

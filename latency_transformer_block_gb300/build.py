@@ -11,7 +11,7 @@ OUT = os.path.join(HERE, "liblat.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 # translation units (compiled in parallel, then linked)
-SOURCES = ["lat_api.cu"]
+SOURCES = ["lat_api.cu", "noalloc.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -1,0 +1,107 @@
+// lat_chunk_attention_noalloc: the chunk attention for callers that cannot
+// allocate device memory.
+//
+// The attention splits the keys into ranges and merges per-range partial
+// results (running max, running sum, unnormalised output), which needs scratch
+// memory.  lat_create's context keeps that scratch in its cudaMalloc'd
+// workspace; this entry point instead uses one file-scope device array, so it
+// needs no context and calls no allocator at all.  It is for code that owns
+// every device byte itself (an engine with its own memory pool, or a real-time
+// loop that forbids allocation once it runs) and therefore can neither call
+// cudaMalloc nor let a library do it for them.
+//
+// The array is part of the library image: every GPU that loads liblat.so holds
+// it (4 MiB) until the process exits.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/lat.h"
+#include "attention.cuh"
+
+lat_status lat_internal_fail(lat_status s, const char* msg);
+
+namespace {
+
+constexpr int kNoAllocScratchFloats = 1 << 20;   // 4 MiB of fp32 partials
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+// Device address of g_noalloc_scratch, per device.  In host code the symbol
+// name is only a host-side stand-in; a kernel must be given the address that
+// cudaGetSymbolAddress returns with the device current.
+float* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_setup_mu;
+
+lat_status setup_device(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return lat_internal_fail(LAT_ERR_CUDA, "cudaGetSymbolAddress(noalloc scratch) failed");
+    e = lat::set_attention_smem_limits();
+    if (e != cudaSuccess) return lat_internal_fail(LAT_ERR_CUDA, "cudaFuncSetAttribute(attention) failed");
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return LAT_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" lat_status lat_chunk_attention_noalloc(const float* q, const void* k, const void* v, float* out,
+                                                  int T_q, int T_kv, int Hq, int Hkv, int dh, void* stream) {
+  if (!q || !k || !v || !out) return lat_internal_fail(LAT_ERR_ARG, "NULL argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return lat_internal_fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  if (T_q < 1 || T_kv < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv)
+    return lat_internal_fail(LAT_ERR_SHAPE, "need T_q, T_kv, Hq, Hkv >= 1 and Hq a multiple of Hkv");
+  if (dh != 64 && dh != 128 && dh != 256) return lat_internal_fail(LAT_ERR_SHAPE, "dh must be 64, 128 or 256");
+  // one key range needs Hq * T_q * (dh + 2) floats of partials (output, max, sum)
+  const long long per_split = (long long)Hq * T_q * (dh + 2);
+  if (per_split > kNoAllocScratchFloats)
+    return lat_internal_fail(LAT_ERR_SHAPE,
+                             "Hq * T_q * (dh + 2) exceeds the static scratch (1048576 floats, 4 MiB)");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return lat_internal_fail(LAT_ERR_CUDA, "no usable current device");
+  float* scratch = nullptr;
+  lat_status s = setup_device(dev, &scratch);
+  if (s != LAT_OK) return s;
+
+  const int nkb = (T_kv + 63) / 64;
+  int n_split = (int)(kNoAllocScratchFloats / per_split);
+  if (n_split > nkb) n_split = nkb;
+  if (n_split < 1) n_split = 1;
+
+  lat::AttnArgs a{};
+  a.q = q;
+  a.q_ld = Hq * dh;
+  a.k = reinterpret_cast<const __nv_bfloat16*>(k);
+  a.v = reinterpret_cast<const __nv_bfloat16*>(v);
+  a.kv_ld = Hkv * dh;
+  a.T_q = T_q;
+  a.T_kv = T_kv;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)dh));
+  a.n_split = n_split;
+  a.out = out;
+  a.out_ld = Hq * dh;
+  // partials: [n_split][Hq][T_q] max, then sum, then [n_split][Hq][T_q][dh]
+  // output.  Every element the merge reads is written by this call first, so
+  // nothing needs clearing between calls.
+  const size_t nrow = (size_t)n_split * Hq * T_q;
+  a.part_m = scratch;
+  a.part_l = scratch + nrow;
+  a.part_o = scratch + 2 * nrow;
+  cudaError_t e = lat::launch_chunk_attention(a, dh, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return lat_internal_fail(LAT_ERR_CUDA, cudaGetErrorString(e));
+  return LAT_OK;
+}

@@ -75,6 +75,8 @@ def lib():
         L.lat_debug_gemm.restype = st
         L.lat_debug_attention.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P]
         L.lat_debug_attention.restype = st
+        L.lat_chunk_attention_noalloc.argtypes = [_P, _P, _P, _P] + [ctypes.c_int] * 5 + [_P]
+        L.lat_chunk_attention_noalloc.restype = st
         L.lat_debug_clear.argtypes = [_P, _P]
         L.lat_debug_clear.restype = st
         L.lat_sync.argtypes = [_P]
@@ -101,6 +103,12 @@ def ptr(t):
 
 def stream_ptr(stream):
     return None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+
+
+def chunk_attention_noalloc(q, k, v, out, T_q, T_kv, Hq, Hkv, dh, stream=None):
+    """Context-free chunk attention whose scratch is the library's static array."""
+    check(lib().lat_chunk_attention_noalloc(ptr(q), ptr(k), ptr(v), ptr(out), T_q, T_kv, Hq, Hkv, dh,
+                                            stream_ptr(stream)))
 
 
 class Context:
