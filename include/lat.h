@@ -219,6 +219,19 @@ lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *st
 lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 
 /*
+ * lat_debug_dense_gemm -- one dense projection of a LAT_PI0_PREFIX or LAT_DIT
+ * context alone (kernel-level parity and timing):
+ *   out[m][n] = sum_t sum_k act[m][t*K + k] * W[n][k]
+ * for the folded K-major weight W of block `layer` (which: 0 = merged QKV,
+ * 1 = attention output, 2 = FFN in (prefix: gate/up interleaved in tiles of 64
+ * gate + 64 up rows), 3 = FFN out).
+ *  act: device bf16 [M][terms*K] (terms bf16 planes of one activation);
+ *  out: device fp32 [M][N].  1 <= M <= the context's workspace rows, terms 1..3.
+ */
+lat_status lat_debug_dense_gemm(lat_ctx *ctx, int which, int layer, const void *act, int M, int terms,
+                                float *out, void *stream);
+
+/*
  * lat_debug_attention -- the chunk attention of an action-expert context
  * alone (kernel-level parity and timing): out = softmax(q k^T / sqrt(dh)) v,
  * no mask, query head h reading KV head h / (Hq / Hkv), using the context's

@@ -6,10 +6,11 @@
 // Each CTA runs 4 warps x 16 query rows of one query head against a range of
 // 64-key blocks with an online softmax (running max / sum per row, rescaling
 // the output accumulator).  Q (fp32) and P (fp32) enter the warp-level bf16
-// tensor-core MMA as three-term splits, K and V are the cache's bf16 values,
-// accumulation is fp32, so the only roundings are fp32 ones.  With several key
-// ranges (flash-decoding) each CTA writes its partial (max, sum, unnormalised
-// output) and a combine kernel merges them.
+// tensor-core MMA as three-term splits; cached K and V are bf16 values; the
+// block's own keys (index >= own0) come in fp32 as computed and are split into
+// two bf16 planes (hi, lo) in shared memory; accumulation is fp32.  With
+// several key ranges (flash-decoding) each CTA writes its partial (max, sum,
+// unnormalised output) and a combine kernel merges them.
 #pragma once
 #include "common.cuh"
 
@@ -29,7 +30,28 @@ struct AttnArgs {
   float* part_m;             // n_split > 1: [n_split][Hq][T_q]
   float* part_l;
   float* part_o;             // [n_split][Hq][T_q][dh]
+  const float* k_own;        // fp32 keys own0.. [T_kv - own0][own_ld] (null: none)
+  const float* v_own;
+  int own0;
+  int own_ld;
 };
+
+// 8 fp32 values -> 8 bf16 hi and 8 bf16 lo (two-term split)
+__device__ __forceinline__ void split8_to(const float* src, uint4& hi, uint4& lo) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 b = *reinterpret_cast<const float4*>(src + 4);
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+    h[e] = pack_bf16(h0, h1);
+    l[e] = pack_bf16(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
+                     __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -65,8 +87,8 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
   constexpr int LD = DH + 8;      // padded smem row (bf16): conflict-free ldmatrix
   constexpr int NT = DH / 8;      // output n-tiles
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  __nv_bfloat16* sV = sK + KB * LD;
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [2 planes][KB][LD]
+  __nv_bfloat16* sV = sK + 2 * KB * LD;
 
   const int h = blockIdx.x;
   const int qt = blockIdx.y;
@@ -89,20 +111,33 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
+  const uint32_t LO = (uint32_t)(KB * LD * 2);   // byte offset of the lo plane
 
   for (int kb = kb0; kb < kb1; ++kb) {
-    // ---- stage K and V blocks (zero-filled past T_kv) ----
+    // ---- stage K and V blocks (zero-filled past T_kv); own keys as hi + lo ----
+    const bool has_lo = a.k_own != nullptr && (kb + 1) * KB > a.own0 && a.own0 < a.T_kv;
     __syncthreads();
     for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
       const int row = idx / (DH / 8), c8 = idx % (DH / 8);
       const int key = kb * KB + row;
-      uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4 kk = z, vv = z, kl = z, vl = z;
       if (key < a.T_kv) {
-        kk = *reinterpret_cast<const uint4*>(a.k + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
-        vv = *reinterpret_cast<const uint4*>(a.v + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+        if (a.k_own != nullptr && key >= a.own0) {
+          const size_t o = (size_t)(key - a.own0) * a.own_ld + kvh * DH + c8 * 8;
+          split8_to(a.k_own + o, kk, kl);
+          split8_to(a.v_own + o, vv, vl);
+        } else {
+          kk = *reinterpret_cast<const uint4*>(a.k + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+          vv = *reinterpret_cast<const uint4*>(a.v + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+        }
       }
       *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
       *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
+      if (has_lo) {
+        *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
+        *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
+      }
     }
     __syncthreads();
 
@@ -136,6 +171,13 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
         mma_16816(s[2 * jp + 1], ah, b2, b3);
         mma_16816(s[2 * jp + 1], am, b2, b3);
         mma_16816(s[2 * jp + 1], al, b2, b3);
+        if (has_lo) {
+          ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+          mma_16816(s[2 * jp], ah, b0, b1);
+          mma_16816(s[2 * jp], am, b0, b1);
+          mma_16816(s[2 * jp + 1], ah, b2, b3);
+          mma_16816(s[2 * jp + 1], am, b2, b3);
+        }
       }
     }
 
@@ -203,6 +245,13 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
         mma_16816(o[2 * jp + 1], ph, b2, b3);
         mma_16816(o[2 * jp + 1], pm, b2, b3);
         mma_16816(o[2 * jp + 1], pl, b2, b3);
+        if (has_lo) {
+          ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+          mma_16816(o[2 * jp], ph, b0, b1);
+          mma_16816(o[2 * jp], pm, b0, b1);
+          mma_16816(o[2 * jp + 1], ph, b2, b3);
+          mma_16816(o[2 * jp + 1], pm, b2, b3);
+        }
       }
     }
   }
@@ -247,19 +296,250 @@ static __global__ void attention_combine_kernel(AttnArgs a, int dh) {
   a.out[(size_t)t * a.out_ld + h * dh + d] = acc / L;
 }
 
+
+// ---------------------------------------------------------------------------
+// Segmented attention for the dense path.  Group b (a DiT chunk or a prefill
+// batch element) has T_rows query rows starting at row b * T_rows of q and up
+// to kMaxSeg key segments (ring slots of the noisy history plus its own slot,
+// or the prefix cache); keys of a segment are rows 0..n-1 of k/v with stride
+// kv_ld.  Q and P enter the MMA as TERMS-term bf16 splits; fp32 segments (the
+// group's own keys as computed) as two bf16 planes.  The output of row r, head
+// h, dim d goes to the three planes out[r][t*ldh + h*DH + d] (hi, mid, lo of the
+// fp32 value) -- the split activation of the output projection.
+// Grid (Hq, ceil(T_rows / 64), groups).
+// ---------------------------------------------------------------------------
+constexpr int kMaxSeg = 5;
+
+struct AttnSeg {
+  const __nv_bfloat16* k;    // bf16 keys (cache), or
+  const __nv_bfloat16* v;
+  const float* k32;          // fp32 keys as computed (own chunk): split into hi + lo
+  const float* v32;
+  int n;
+};
+
+struct SegGroup {
+  int nseg;
+  AttnSeg seg[kMaxSeg];
+};
+
+struct SegAttnArgs {
+  const float* q;            // fp32 [groups * T_rows][q_ld]
+  int q_ld;
+  int T_rows;
+  int Hq, Hkv, kv_ld;
+  float scale_log2;
+  __nv_bfloat16* out;        // [groups * T_rows][3 * ldh]
+  int ldh;
+  SegGroup grp[16];
+};
+
+template <int DH, int TERMS>
+static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_constant__ SegAttnArgs a) {
+  constexpr int KB = 64;
+  constexpr int LD = DH + 8;
+  constexpr int NT = DH / 8;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [2 planes][KB][LD]
+  __nv_bfloat16* sV = sK + 2 * KB * LD;
+  const uint32_t LO = (uint32_t)(KB * LD * 2);
+  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int kvh = h / (a.Hq / a.Hkv);
+  const int rl0 = qt * 64 + warp * 16 + g, rl1 = rl0 + 8;     // rows within the group
+  const bool v0 = rl0 < a.T_rows, v1 = rl1 < a.T_rows;
+  const size_t row0 = (size_t)b * a.T_rows + (v0 ? rl0 : 0), row1 = (size_t)b * a.T_rows + (v1 ? rl1 : 0);
+  const float* q0 = a.q + row0 * a.q_ld + h * DH;
+  const float* q1 = a.q + row1 * a.q_ld + h * DH;
+
+  // this warp's Q fragments, split once: [k-step][term][4]
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
+  const SegGroup& G = a.grp[b];
+
+  for (int si = 0; si < G.nseg; ++si) {
+    const AttnSeg sg = G.seg[si];
+    const bool f32 = sg.k32 != nullptr;
+    const int nkb = (sg.n + KB - 1) / KB;
+    for (int kb = 0; kb < nkb; ++kb) {
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
+        const int row = idx / (DH / 8), c8 = idx % (DH / 8);
+        const int key = kb * KB + row;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        uint4 kk = z, vv = z, kl = z, vl = z;
+        if (key < sg.n) {
+          const size_t o = (size_t)key * a.kv_ld + kvh * DH + c8 * 8;
+          if (f32) {
+            split8_to(sg.k32 + o, kk, kl);
+            split8_to(sg.v32 + o, vv, vl);
+          } else {
+            kk = *reinterpret_cast<const uint4*>(sg.k + o);
+            vv = *reinterpret_cast<const uint4*>(sg.v + o);
+          }
+        }
+        *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
+        *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
+        if (f32) {
+          *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
+          *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
+        }
+      }
+      __syncthreads();
+      float s[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll 2
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        const int c = ks * 16 + 2 * tq;
+        const float2 x00 = *reinterpret_cast<const float2*>(q0 + c);
+        const float2 x10 = *reinterpret_cast<const float2*>(q1 + c);
+        const float2 x01 = *reinterpret_cast<const float2*>(q0 + c + 8);
+        const float2 x11 = *reinterpret_cast<const float2*>(q1 + c + 8);
+        uint32_t af[3][4];
+        split_pair(x00.x, x00.y, af[0][0], af[1][0], af[2][0]);
+        split_pair(x10.x, x10.y, af[0][1], af[1][1], af[2][1]);
+        split_pair(x01.x, x01.y, af[0][2], af[1][2], af[2][2]);
+        split_pair(x11.x, x11.y, af[0][3], af[1][3], af[2][3]);
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int key = jp * 16 + ((mi >> 1) << 3) + rr;
+          const int col = ks * 16 + ((mi & 1) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+#pragma unroll
+          for (int t = 0; t < TERMS; ++t) {
+            mma_16816(s[2 * jp], af[t], b0, b1);
+            mma_16816(s[2 * jp + 1], af[t], b2, b3);
+          }
+          if (f32) {
+            ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+#pragma unroll
+            for (int t = 0; t < TERMS - 1; ++t) {
+              mma_16816(s[2 * jp], af[t], b0, b1);
+              mma_16816(s[2 * jp + 1], af[t], b2, b3);
+            }
+          }
+        }
+      }
+      float mx0 = m0, mx1 = m1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int key = kb * KB + j * 8 + 2 * tq;
+        s[j][0] = (key < sg.n) ? s[j][0] * a.scale_log2 : -INFINITY;
+        s[j][1] = (key + 1 < sg.n) ? s[j][1] * a.scale_log2 : -INFINITY;
+        s[j][2] = (key < sg.n) ? s[j][2] * a.scale_log2 : -INFINITY;
+        s[j][3] = (key + 1 < sg.n) ? s[j][3] * a.scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float al0 = exp2f(m0 - mx0), al1 = exp2f(m1 - mx1);
+      m0 = mx0;
+      m1 = mx1;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s[j][0] = exp2f(s[j][0] - mx0);
+        s[j][1] = exp2f(s[j][1] - mx0);
+        s[j][2] = exp2f(s[j][2] - mx1);
+        s[j][3] = exp2f(s[j][3] - mx1);
+        sum0 += s[j][0] + s[j][1];
+        sum1 += s[j][2] + s[j][3];
+      }
+      sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
+      sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
+      sum1 += __shfl_xor_sync(0xffffffffu, sum1, 1);
+      sum1 += __shfl_xor_sync(0xffffffffu, sum1, 2);
+      l0 = l0 * al0 + sum0;
+      l1 = l1 * al1 + sum1;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        o[j][0] *= al0;
+        o[j][1] *= al0;
+        o[j][2] *= al1;
+        o[j][3] *= al1;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t pf[3][4];
+        split_pair(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0], pf[2][0]);
+        split_pair(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1], pf[2][1]);
+        split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], pf[0][2], pf[1][2], pf[2][2]);
+        split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], pf[0][3], pf[1][3], pf[2][3]);
+#pragma unroll
+        for (int jp = 0; jp < NT / 2; ++jp) {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int key = kk * 16 + ((mi & 1) << 3) + rr;
+          const int col = jp * 16 + ((mi >> 1) << 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+#pragma unroll
+          for (int t = 0; t < TERMS; ++t) {
+            mma_16816(o[2 * jp], pf[t], b0, b1);
+            mma_16816(o[2 * jp + 1], pf[t], b2, b3);
+          }
+          if (f32) {
+            ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+#pragma unroll
+            for (int t = 0; t < TERMS - 1; ++t) {
+              mma_16816(o[2 * jp], pf[t], b0, b1);
+              mma_16816(o[2 * jp + 1], pf[t], b2, b3);
+            }
+          }
+        }
+      }
+    }
+  }
+  const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f, i1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c = h * DH + j * 8 + 2 * tq;
+    if (v0) {
+      uint32_t hh, mm, ll;
+      split_pair(o[j][0] * i0, o[j][1] * i0, hh, mm, ll);
+      __nv_bfloat16* p = a.out + row0 * 3 * a.ldh + c;
+      *reinterpret_cast<uint32_t*>(p) = hh;
+      *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
+      *reinterpret_cast<uint32_t*>(p + 2 * a.ldh) = ll;
+    }
+    if (v1) {
+      uint32_t hh, mm, ll;
+      split_pair(o[j][2] * i1, o[j][3] * i1, hh, mm, ll);
+      __nv_bfloat16* p = a.out + row1 * 3 * a.ldh + c;
+      *reinterpret_cast<uint32_t*>(p) = hh;
+      *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
+      *reinterpret_cast<uint32_t*>(p + 2 * a.ldh) = ll;
+    }
+  }
+}
+
 // Launch the attention (and the combine when there are several key ranges).
 // The kernels need more than 48 KB of dynamic shared memory for dh = 256:
 // call set_attention_smem_limits() once per device first.
+// K and V tiles, two planes each, rows padded to dh + 8
+static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2; }
+
 static inline cudaError_t set_attention_smem_limits() {
-  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 72 * 2);
-  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 136 * 2);
-  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * 64 * 264 * 2);
+  cudaFuncSetAttribute(attention_seg_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
+  cudaFuncSetAttribute(attention_seg_kernel<256, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
+  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(64));
+  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
+  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
   return cudaGetLastError();
 }
 
 static inline cudaError_t launch_chunk_attention(const AttnArgs& a, int dh, cudaStream_t st) {
   dim3 grid(a.Hq, (a.T_q + 63) / 64, a.n_split);
-  const int smem = 2 * 64 * (dh + 8) * 2;
+  const int smem = attn_smem_bytes(dh);
   if (dh == 64) attention_kernel<64><<<grid, 128, smem, st>>>(a);
   else if (dh == 128) attention_kernel<128><<<grid, 128, smem, st>>>(a);
   else attention_kernel<256><<<grid, 128, smem, st>>>(a);

@@ -17,6 +17,8 @@
 #include "../../include/lat.h"
 #include "attention.cuh"
 #include "common.cuh"
+#include "dense_gemm.cuh"
+#include "dense_kernels.cuh"
 #include "skinny_gemm.cuh"
 #include "small_kernels.cuh"
 
@@ -127,6 +129,18 @@ struct lat_ctx {
   int attn_split = 1;
   DevErr* err = nullptr;
 
+  // dense path (prefix prefill, DiT)
+  bf16 *wup = nullptr, *wdown = nullptr, *wpatch = nullptr;
+  CUtensorMap map_up, map_down, map_patch;
+  float *bpatch = nullptr, *adaln = nullptr, *cos_j = nullptr, *sin_j = nullptr, *qkvbuf = nullptr,
+        *qbuf = nullptr;
+  double* theta = nullptr;
+  float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32)
+  bf16 *act2 = nullptr, *act2f = nullptr;
+  CUtensorMap map_act_d, map_act_o, map_act_f;
+  int m_max = 0;
+  bf16 *wt1 = nullptr, *bt1 = nullptr, *wt2 = nullptr, *bt2 = nullptr, *wmod = nullptr, *bmod = nullptr;
+
   // captured denoise loop
   cudaGraphExec_t gexec = nullptr;
   void* g_kv = nullptr;
@@ -187,30 +201,53 @@ static lat_status enqueue_skinny(const lat_ctx* c, const CUtensorMap& map, const
 // ---------------------------------------------------------------------------
 static lat_status check_desc(const lat_model_desc* d) {
   if (!d) return fail(LAT_ERR_ARG, "desc is NULL");
-  if (d->kind != LAT_PI0_ACTION_EXPERT)
+  if (d->kind != LAT_PI0_ACTION_EXPERT && d->kind != LAT_PI0_PREFIX && d->kind != LAT_DIT)
     return fail(LAT_ERR_UNSUPPORTED, "model kind %d not built into this library", d->kind);
-  if (d->D <= 0 || d->D % 128) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 128");
   if (d->Hq <= 0 || d->Hkv <= 0 || d->Hq % d->Hkv) return fail(LAT_ERR_SHAPE, "Hq must be a multiple of Hkv");
-  if (d->dh != 64 && d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 64, 128 or 256");
-  if (((d->Hq + 2 * d->Hkv) * d->dh) % 128) return fail(LAT_ERR_SHAPE, "(Hq + 2 Hkv) dh must be a multiple of 128");
-  if ((d->Hq * d->dh) % 64) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 64");
-  if (d->F <= 0 || d->F % 64) return fail(LAT_ERR_SHAPE, "F must be a positive multiple of 64");
-  if (d->L <= 0 || d->S <= 0) return fail(LAT_ERR_SHAPE, "L and S must be positive");
-  if (d->T_q < 2 || d->T_q > 64) return fail(LAT_ERR_SHAPE, "T_q must be in [2, 64]");
-  if (d->T_prefix < 0) return fail(LAT_ERR_SHAPE, "T_prefix must be >= 0");
-  if (d->act_dim <= 0) return fail(LAT_ERR_SHAPE, "act_dim must be positive");
+  if (d->L <= 0) return fail(LAT_ERR_SHAPE, "L must be positive");
   if (!(d->eps > 0.f) || !(d->rope_base > 1.f)) return fail(LAT_ERR_ARG, "eps / rope_base out of range");
+  if (d->F <= 0) return fail(LAT_ERR_SHAPE, "F must be positive");
+  if (d->kind == LAT_PI0_ACTION_EXPERT) {
+    if (d->D <= 0 || d->D % 128) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 128");
+    if (d->dh != 64 && d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 64, 128 or 256");
+    if (((d->Hq + 2 * d->Hkv) * d->dh) % 128) return fail(LAT_ERR_SHAPE, "(Hq + 2 Hkv) dh must be a multiple of 128");
+    if ((d->Hq * d->dh) % 64) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 64");
+    if (d->F % 64) return fail(LAT_ERR_SHAPE, "F must be a multiple of 64");
+    if (d->S <= 0) return fail(LAT_ERR_SHAPE, "S must be positive");
+    if (d->T_q < 2 || d->T_q > 64) return fail(LAT_ERR_SHAPE, "T_q must be in [2, 64]");
+    if (d->T_prefix < 0) return fail(LAT_ERR_SHAPE, "T_prefix must be >= 0");
+    if (d->act_dim <= 0) return fail(LAT_ERR_SHAPE, "act_dim must be positive");
+    return LAT_OK;
+  }
+  // dense kinds: 128 x 128 x 64 tiles
+  if (d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 128 or 256 for the dense path");
+  if (d->D <= 0 || d->D % 256) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 256");
+  if ((d->Hq * d->dh) % 256) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 256");
+  if (d->max_batch < 1 || d->max_batch > kMaxChunks) return fail(LAT_ERR_SHAPE, "max_batch must be in [1, 16]");
+  if (d->kind == LAT_PI0_PREFIX) {
+    if (((d->Hq + 2 * d->Hkv) * d->dh) % 256 || (2 * d->Hkv * d->dh) % 256)
+      return fail(LAT_ERR_SHAPE, "QKV and KV widths must be multiples of 256");
+    if (d->F % 128) return fail(LAT_ERR_SHAPE, "F must be a multiple of 128");
+    if (d->patch_dim <= 0 || d->patch_dim % 64) return fail(LAT_ERR_SHAPE, "patch_dim must be a multiple of 64");
+    if (d->T_prefix < 1 || d->T_q < 0) return fail(LAT_ERR_SHAPE, "T_prefix must be >= 1");
+    return LAT_OK;
+  }
+  if (d->Hq != d->Hkv || d->Hq * d->dh != d->D) return fail(LAT_ERR_SHAPE, "DiT: Hq == Hkv and Hq dh == D");
+  if (d->F % 256) return fail(LAT_ERR_SHAPE, "F must be a multiple of 256");
+  if (d->S <= 0 || d->T_q < 1 || d->n_hist < 0 || d->n_streams < 1 || d->t_dim <= 0 || d->t_dim % 2)
+    return fail(LAT_ERR_SHAPE, "DiT: S, T_q, n_streams, t_dim must be positive (t_dim even), n_hist >= 0");
+  if (d->n_hist + 1 > kMaxSeg) return fail(LAT_ERR_SHAPE, "n_hist must be <= 4");
   return LAT_OK;
 }
 
 // ---------------------------------------------------------------------------
 // offline folds
 // ---------------------------------------------------------------------------
-static lat_status fold_t(const void* W, const void* g, bf16* out, int K, int N) {
+static lat_status fold_t(const void* W, const void* g, bf16* out, int K, int N, int il = 0, int il_off = 0) {
   if (!W || !aligned16(W)) return fail(LAT_ERR_ALIGN, "weight pointer NULL or not 16-byte aligned");
   dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
   fold_transpose_kernel<<<grid, block>>>(reinterpret_cast<const bf16*>(W), reinterpret_cast<const bf16*>(g), out,
-                                         K, N);
+                                         K, N, il, il_off);
   return launch_check("fold_transpose");
 }
 
@@ -363,6 +400,8 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(c->alloc(&c->pl, (size_t)c->attn_split * d.Hq * T));
   LAT_TRY(c->alloc(&c->po, (size_t)c->attn_split * d.Hq * T * d.dh));
   LAT_TRY(c->alloc(&c->state_emb, (size_t)D));
+  LAT_TRY(c->alloc(&c->kown, (size_t)T * d.Hkv * d.dh));
+  LAT_TRY(c->alloc(&c->vown, (size_t)T * d.Hkv * d.dh));
   LAT_TRY(c->alloc(&c->err, 1));
   CUDA_TRY(cudaMemset(c->qkv_acc, 0, (size_t)T * c->nqkv * 4));
   CUDA_TRY(cudaMemset(c->gu_acc, 0, (size_t)T * 2 * F * 4));
@@ -380,8 +419,10 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
 // ---------------------------------------------------------------------------
 static lat_status enqueue_attention(const lat_model_desc& d, const float* q, int q_ld, const bf16* k, const bf16* v,
                                     int kv_ld, int T_q, int T_kv, int n_split, float* out, int out_ld, float* pm,
-                                    float* pl, float* po, cudaStream_t st) {
+                                    float* pl, float* po, cudaStream_t st, const float* k_own = nullptr,
+                                    const float* v_own = nullptr, int own0 = 0) {
   AttnArgs a{};
+  a.k_own = k_own; a.v_own = v_own; a.own0 = k_own ? own0 : T_kv; a.own_ld = kv_ld;
   a.q = q; a.q_ld = q_ld; a.k = k; a.v = v; a.kv_ld = kv_ld;
   a.T_q = T_q; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
@@ -413,12 +454,13 @@ static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_lay
   // 2. row scale + RoPE + K/V into the cache + q; clears qkv_acc and gu_acc
   {
     QkvEpiArgs a{c->qkv_acc, c->nqkv, c->r1, c->cos_t, c->sin_t, c->q, kc, vc, kvd, d.T_prefix,
-                 d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F};
+                 d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F, c->kown, c->vown};
     qkv_epilogue_kernel<<<T, 256, 0, st>>>(a);
     LAT_TRY(launch_check("qkv_epilogue"));
   }
   // 3. attention over [prefix | own] (key ranges) + combine
-  LAT_TRY(enqueue_attention(d, c->q, qd, kc, vc, kvd, T, T_kv, c->attn_split, c->o, qd, c->pm, c->pl, c->po, st));
+  LAT_TRY(enqueue_attention(d, c->q, qd, kc, vc, kvd, T, T_kv, c->attn_split, c->o, qd, c->pm, c->pl, c->po, st,
+                            c->kown, c->vown, d.T_prefix));
   // 4. x += o Wo
   {
     SkinnyArgs a{};
@@ -469,6 +511,353 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
   return LAT_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// dense path: prefix prefill and DiT stage
+// ---------------------------------------------------------------------------
+static constexpr int kDStages = 6;
+// bf16 planes of every dense activation: three terms carry the fp32 value
+static constexpr int kActTerms = 3;
+
+static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, const CUtensorMap& wmap, DenseArgs a,
+                                cudaStream_t st) {
+  a.err = c->err;
+  const int grid = ((a.M + 127) / 128) * (a.N / 128);
+  dense_gemm_kernel<kDStages><<<grid, 192, dense_smem_bytes(kDStages), st>>>(amap, wmap, a);
+  return launch_check("dense_gemm");
+}
+
+// tensor map of a row-major bf16 activation [rows][cols] read in 128 x 64 tiles
+static lat_status make_act_map(CUtensorMap* map, const void* base, int rows, int cols) {
+  return make_kmajor_map(map, base, rows, cols, 128);
+}
+
+static lat_status build_rope_tables(lat_ctx* c, int T) {
+  const lat_model_desc& d = c->d;
+  const int half = d.dh / 2;
+  std::vector<float> ct((size_t)T * half), stt((size_t)T * half);
+  std::vector<double> th(half);
+  for (int i = 0; i < half; ++i) th[i] = std::pow((double)d.rope_base, -2.0 * i / d.dh);
+  for (int t = 0; t < T; ++t)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)t * th[i];
+      ct[(size_t)t * half + i] = (float)std::cos(ang);
+      stt[(size_t)t * half + i] = (float)std::sin(ang);
+    }
+  LAT_TRY(c->alloc(&c->cos_j, ct.size()));
+  LAT_TRY(c->alloc(&c->sin_j, stt.size()));
+  LAT_TRY(c->alloc(&c->theta, th.size()));
+  CUDA_TRY(cudaMemcpy(c->cos_j, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->sin_j, stt.data(), stt.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->theta, th.data(), th.size() * 8, cudaMemcpyHostToDevice));
+  return LAT_OK;
+}
+
+static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
+  const lat_model_desc& d = c->d;
+  const int qd = d.Hq * d.dh;
+  c->m_max = d.max_batch * rows_per_group;
+  const int wact = d.D > qd ? d.D : qd;
+  LAT_TRY(c->alloc(&c->act2, (size_t)c->m_max * kActTerms * wact));
+  LAT_TRY(c->alloc(&c->act2f, (size_t)c->m_max * kActTerms * d.F));
+  LAT_TRY(c->alloc(&c->qkvbuf, (size_t)c->m_max * c->nqkv));
+  LAT_TRY(c->alloc(&c->qbuf, (size_t)c->m_max * qd));
+  LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
+  LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
+  LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, kActTerms * d.D));
+  LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, kActTerms * qd));
+  LAT_TRY(make_act_map(&c->map_act_f, c->act2f, c->m_max, kActTerms * d.F));
+  LAT_TRY(c->alloc(&c->err, 1));
+  CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
+  return LAT_OK;
+}
+
+static lat_status create_prefix(lat_ctx* c, const lat_weights* w) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, F = d.F, L = d.L;
+  const int qd = d.Hq * d.dh, kvd = d.Hkv * d.dh;
+  c->nqkv = qd + 2 * kvd;
+  if (!w || !w->blocks) return fail(LAT_ERR_ARG, "weights / blocks NULL");
+  if (!w->w_patch || !w->b_patch || !aligned16(w->w_patch) || !aligned16(w->b_patch))
+    return fail(LAT_ERR_ALIGN, "patch weights NULL or not 16-byte aligned");
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    const void* bp[] = {b.g_attn, b.wq, b.wk, b.wv, b.wo, b.g_ffn, b.wg, b.wu, b.wd};
+    for (const void* p : bp)
+      if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "block %d weight NULL or not 16-byte aligned", l);
+  }
+  LAT_TRY(c->alloc(&c->wqkv, (size_t)L * c->nqkv * D));
+  LAT_TRY(c->alloc(&c->wo, (size_t)L * D * qd));
+  LAT_TRY(c->alloc(&c->wup, (size_t)L * 2 * F * D));
+  LAT_TRY(c->alloc(&c->wdown, (size_t)L * D * F));
+  LAT_TRY(c->alloc(&c->wpatch, (size_t)D * d.patch_dim));
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    bf16* q0 = c->wqkv + (size_t)l * c->nqkv * D;
+    LAT_TRY(fold_t(b.wq, b.g_attn, q0, D, qd));
+    LAT_TRY(fold_t(b.wk, b.g_attn, q0 + (size_t)qd * D, D, kvd));
+    LAT_TRY(fold_t(b.wv, b.g_attn, q0 + (size_t)(qd + kvd) * D, D, kvd));
+    LAT_TRY(fold_t(b.wo, nullptr, c->wo + (size_t)l * D * qd, qd, D));
+    bf16* gu0 = c->wup + (size_t)l * 2 * F * D;   // tiles of [64 gate | 64 up] rows
+    LAT_TRY(fold_t(b.wg, b.g_ffn, gu0, D, F, 64, 0));
+    LAT_TRY(fold_t(b.wu, b.g_ffn, gu0, D, F, 64, 64));
+    LAT_TRY(fold_t(b.wd, nullptr, c->wdown + (size_t)l * D * F, F, D));
+  }
+  LAT_TRY(fold_t(w->w_patch, nullptr, c->wpatch, d.patch_dim, D));
+  LAT_TRY(c->alloc(&c->bpatch, (size_t)D));
+  bf16_to_f32_kernel<<<(D + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->b_patch), c->bpatch, D);
+  LAT_TRY(launch_check("bpatch"));
+  LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * c->nqkv, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, qd, 128));
+  LAT_TRY(make_kmajor_map(&c->map_up, c->wup, L * 2 * F, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_down, c->wdown, L * D, F, 128));
+  LAT_TRY(make_kmajor_map(&c->map_patch, c->wpatch, D, d.patch_dim, 128));
+  LAT_TRY(c->alloc(&c->xres, (size_t)d.max_batch * d.T_prefix * D));
+  LAT_TRY(alloc_dense_workspace(c, d.T_prefix));
+  LAT_TRY(build_rope_tables(c, d.T_prefix));
+  CUDA_TRY(cudaDeviceSynchronize());
+  return LAT_OK;
+}
+
+static lat_status build_adaln(lat_ctx* c, const std::vector<double>& t) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, S = d.S, td = d.t_dim;
+  std::vector<float> emb((size_t)S * td), tmp;
+  for (int s = 0; s < S; ++s) {
+    timestep_embedding_host(t[s], td, tmp);
+    std::memcpy(&emb[(size_t)s * td], tmp.data(), td * sizeof(float));
+  }
+  float *e0 = nullptr, *e1 = nullptr, *e2 = nullptr;
+  CUDA_TRY(cudaMalloc(&e0, (size_t)S * td * 4));
+  CUDA_TRY(cudaMalloc(&e1, (size_t)S * D * 4));
+  CUDA_TRY(cudaMalloc(&e2, (size_t)S * D * 4));
+  cudaMemcpy(e0, emb.data(), emb.size() * 4, cudaMemcpyHostToDevice);
+  // e(t) = SiLU(temb Wt1 + bt1) Wt2 + bt2 ; A = SiLU(e) Wmod + bmod
+  lat_status st = small_gemm(e0, false, td, c->wt1, true, D, c->bt1, true, e1, D, S, D, td, 1);
+  if (st == LAT_OK) st = small_gemm(e1, false, D, c->wt2, true, D, c->bt2, true, e2, D, S, D, D, 1);
+  if (st == LAT_OK) st = small_gemm(e2, false, D, c->wmod, true, 6 * D, c->bmod, true, c->adaln, 6 * D, S, 6 * D, D, 0);
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaFree(e0);
+  cudaFree(e1);
+  cudaFree(e2);
+  if (st != LAT_OK) return st;
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "adaLN table: %s", cudaGetErrorString(e));
+  return LAT_OK;
+}
+
+static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, F = d.F, L = d.L;
+  c->nqkv = 3 * D;
+  if (!w || !w->blocks) return fail(LAT_ERR_ARG, "weights / blocks NULL");
+  const void* vecs[] = {w->wt1, w->bt1, w->wt2, w->bt2, w->wmod, w->bmod};
+  for (const void* p : vecs)
+    if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "timestep MLP weight NULL or not 16-byte aligned");
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    const void* bp[] = {b.wq, b.wk, b.wv, b.wo, b.w1, b.w2};
+    for (const void* p : bp)
+      if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "block %d weight NULL or not 16-byte aligned", l);
+  }
+  LAT_TRY(c->alloc(&c->wqkv, (size_t)L * 3 * D * D));
+  LAT_TRY(c->alloc(&c->wo, (size_t)L * D * D));
+  LAT_TRY(c->alloc(&c->wup, (size_t)L * F * D));
+  LAT_TRY(c->alloc(&c->wdown, (size_t)L * D * F));
+  for (int l = 0; l < L; ++l) {
+    const lat_block_weights& b = w->blocks[l];
+    bf16* q0 = c->wqkv + (size_t)l * 3 * D * D;
+    LAT_TRY(fold_t(b.wq, nullptr, q0, D, D));
+    LAT_TRY(fold_t(b.wk, nullptr, q0 + (size_t)D * D, D, D));
+    LAT_TRY(fold_t(b.wv, nullptr, q0 + (size_t)2 * D * D, D, D));
+    LAT_TRY(fold_t(b.wo, nullptr, c->wo + (size_t)l * D * D, D, D));
+    LAT_TRY(fold_t(b.w1, nullptr, c->wup + (size_t)l * F * D, D, F));
+    LAT_TRY(fold_t(b.w2, nullptr, c->wdown + (size_t)l * D * F, F, D));
+  }
+  LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * 3 * D, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_up, c->wup, L * F, D, 128));
+  LAT_TRY(make_kmajor_map(&c->map_down, c->wdown, L * D, F, 128));
+  // timestep MLP weights are kept for schedule changes
+  const int td = d.t_dim;
+  LAT_TRY(c->alloc(&c->wt1, (size_t)td * D));
+  LAT_TRY(c->alloc(&c->bt1, (size_t)D));
+  LAT_TRY(c->alloc(&c->wt2, (size_t)D * D));
+  LAT_TRY(c->alloc(&c->bt2, (size_t)D));
+  LAT_TRY(c->alloc(&c->wmod, (size_t)D * 6 * D));
+  LAT_TRY(c->alloc(&c->bmod, (size_t)6 * D));
+  CUDA_TRY(cudaMemcpy(c->wt1, w->wt1, (size_t)td * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->bt1, w->bt1, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->wt2, w->wt2, (size_t)D * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->bt2, w->bt2, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->wmod, w->wmod, (size_t)D * 6 * D * 2, cudaMemcpyDeviceToDevice));
+  CUDA_TRY(cudaMemcpy(c->bmod, w->bmod, (size_t)6 * D * 2, cudaMemcpyDeviceToDevice));
+  LAT_TRY(c->alloc(&c->adaln, (size_t)d.S * 6 * D));
+  std::vector<double> t(d.S + 1);
+  for (int s = 0; s <= d.S; ++s) t[s] = (double)s / d.S;
+  LAT_TRY(build_adaln(c, t));
+  LAT_TRY(alloc_dense_workspace(c, d.T_q));
+  LAT_TRY(build_rope_tables(c, d.T_q));
+  CUDA_TRY(cudaDeviceSynchronize());
+  return LAT_OK;
+}
+
+static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, int groups, cudaStream_t st) {
+  const int dh = c->d.dh;
+  dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups);
+  const int smem = attn_smem_bytes(dh);
+  if (dh == 128) attention_seg_kernel<128, 3><<<grid, 128, smem, st>>>(a);
+  else attention_seg_kernel<256, 3><<<grid, 128, smem, st>>>(a);
+  return launch_check("attention_seg");
+}
+
+static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, cudaStream_t st) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, F = d.F, L = d.L, T = d.T_prefix, M = B * T;
+  const int qd = d.Hq * d.dh, kvd = d.Hkv * d.dh, T_kv = d.T_prefix + d.T_q;
+  CUtensorMap pmap;
+  LAT_TRY(make_act_map(&pmap, pe, M, d.patch_dim));
+  {  // patch projection
+    DenseArgs a{};
+    a.M = M; a.N = D; a.K = d.patch_dim; a.terms = 1; a.w_row0 = 0; a.epi = E_STORE;
+    a.out = c->xres; a.ldo = D; a.bias = c->bpatch;
+    LAT_TRY(enqueue_dense(c, pmap, c->map_patch, a, st));
+  }
+  for (int l = 0; l < L; ++l) {
+    const bool last = (l == L - 1);
+    NormArgs na{};
+    na.x = c->xres; na.D = D; na.mode = NORM_RMS; na.eps = d.eps; na.act2 = c->act2;
+    norm_split_kernel<<<M, 256, 0, st>>>(na);
+    LAT_TRY(launch_check("norm_split"));
+    {
+      DenseArgs a{};
+      a.M = M; a.K = D; a.terms = kActTerms; a.epi = E_STORE; a.out = c->qkvbuf;
+      if (last) { a.N = 2 * kvd; a.w_row0 = l * c->nqkv + qd; a.ldo = 2 * kvd; }
+      else { a.N = c->nqkv; a.w_row0 = l * c->nqkv; a.ldo = c->nqkv; }
+      LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_qkv, a, st));
+    }
+    RopeKvArgs ra{};
+    ra.qkv = c->qkvbuf; ra.ld_qkv = last ? 2 * kvd : c->nqkv; ra.q_cols = last ? 0 : qd; ra.kv_cols = kvd;
+    ra.dh = d.dh; ra.T = T; ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta;
+    ra.q_out = c->qbuf; ra.kv_ld = kvd; ra.k32 = c->kown; ra.v32 = c->vown;
+    SegAttnArgs sa{};
+    for (int b = 0; b < B; ++b) {
+      bf16* kb = kv + (((size_t)l * B + b) * 2 + 0) * T_kv * kvd;
+      ra.pos0[b] = 0;
+      ra.kdst[b] = kb;
+      ra.vdst[b] = kb + (size_t)T_kv * kvd;
+      sa.grp[b].nseg = 1;   // the prefix tokens attend to their own K/V as computed
+      sa.grp[b].seg[0] = AttnSeg{nullptr, nullptr, c->kown + (size_t)b * T * kvd, c->vown + (size_t)b * T * kvd, T};
+    }
+    rope_kv_kernel<<<M, 128, 0, st>>>(ra);
+    LAT_TRY(launch_check("rope_kv"));
+    if (last) break;   // the last layer only needs its K and V
+    sa.q = c->qbuf; sa.q_ld = qd; sa.T_rows = T; sa.Hq = d.Hq; sa.Hkv = d.Hkv; sa.kv_ld = kvd;
+    sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+    sa.out = c->act2; sa.ldh = qd;
+    LAT_TRY(enqueue_attention_seg(c, sa, B, st));
+    {
+      DenseArgs a{};
+      a.M = M; a.N = D; a.K = qd; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
+      LAT_TRY(enqueue_dense(c, c->map_act_o, c->map_o, a, st));
+    }
+    norm_split_kernel<<<M, 256, 0, st>>>(na);
+    LAT_TRY(launch_check("norm_split"));
+    {
+      DenseArgs a{};
+      a.M = M; a.N = 2 * F; a.K = D; a.terms = kActTerms; a.w_row0 = l * 2 * F; a.epi = E_GEGLU_SPLIT;
+      a.act2 = c->act2f; a.ldh = F;
+      LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_up, a, st));
+    }
+    {
+      DenseArgs a{};
+      a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
+      LAT_TRY(enqueue_dense(c, c->map_act_f, c->map_down, a, st));
+    }
+  }
+  return LAT_OK;
+}
+
+static bf16* ring_ptr(const lat_ctx* c, bf16* kv, int stream, int layer, int step, int slot, int plane) {
+  const lat_model_desc& d = c->d;
+  const size_t R = d.n_hist + 1;
+  const size_t idx = ((((size_t)stream * d.L + layer) * d.S + step) * R + slot) * 2 + plane;
+  return kv + idx * d.T_q * d.D;
+}
+
+static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk_desc* ch, int n, bf16* kv,
+                                    cudaStream_t st) {
+  const lat_model_desc& d = c->d;
+  const int D = d.D, F = d.F, T = d.T_q, M = n * T;
+  NormArgs na{};
+  na.x = x; na.D = D; na.mode = NORM_LN_MOD; na.eps = d.eps; na.table = c->adaln; na.rows_per_chunk = T;
+  na.act2 = c->act2;
+  for (int b = 0; b < n; ++b) {
+    na.shift_off[b] = ch[b].step * 6 * D + 0 * D;
+    na.scale_off[b] = ch[b].step * 6 * D + 1 * D;
+  }
+  norm_split_kernel<<<M, 256, 0, st>>>(na);
+  LAT_TRY(launch_check("norm_split"));
+  {
+    DenseArgs a{};
+    a.M = M; a.N = 3 * D; a.K = D; a.terms = kActTerms; a.w_row0 = l * 3 * D; a.epi = E_STORE; a.out = c->qkvbuf;
+    a.ldo = 3 * D;
+    LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_qkv, a, st));
+  }
+  RopeKvArgs ra{};
+  ra.qkv = c->qkvbuf; ra.ld_qkv = 3 * D; ra.q_cols = D; ra.kv_cols = D; ra.dh = d.dh; ra.T = T;
+  ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta; ra.q_out = c->qbuf; ra.kv_ld = D;
+  ra.k32 = c->kown; ra.v32 = c->vown;
+  SegAttnArgs sa{};
+  for (int b = 0; b < n; ++b) {
+    const int cb = ch[b].chunk, sb = ch[b].step, stb = ch[b].stream;
+    ra.pos0[b] = chunk_pos0(cb, T);
+    ra.kdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 0);
+    ra.vdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 1);
+    int ns = 0;
+    for (int k = d.n_hist; k >= 1; --k) {       // history, oldest first
+      const int cc = cb - k;
+      if (cc < 0) continue;
+      sa.grp[b].seg[ns++] = AttnSeg{ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 0),
+                                    ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 1), nullptr, nullptr, T};
+    }
+    // own keys as computed (fp32); the ring slot holds their bf16 copy for later chunks
+    sa.grp[b].seg[ns++] = AttnSeg{nullptr, nullptr, c->kown + (size_t)b * T * D, c->vown + (size_t)b * T * D, T};
+    sa.grp[b].nseg = ns;
+  }
+  rope_kv_kernel<<<M, 128, 0, st>>>(ra);
+  LAT_TRY(launch_check("rope_kv"));
+  sa.q = c->qbuf; sa.q_ld = D; sa.T_rows = T; sa.Hq = d.Hq; sa.Hkv = d.Hkv; sa.kv_ld = D;
+  sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+  sa.out = c->act2; sa.ldh = D;
+  LAT_TRY(enqueue_attention_seg(c, sa, n, st));
+  {
+    DenseArgs a{};
+    a.M = M; a.N = D; a.K = D; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
+    a.gate = c->adaln; a.rows_per_chunk = T;
+    for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 2 * D;
+    LAT_TRY(enqueue_dense(c, c->map_act_o, c->map_o, a, st));
+  }
+  for (int b = 0; b < n; ++b) {
+    na.shift_off[b] = ch[b].step * 6 * D + 3 * D;
+    na.scale_off[b] = ch[b].step * 6 * D + 4 * D;
+  }
+  norm_split_kernel<<<M, 256, 0, st>>>(na);
+  LAT_TRY(launch_check("norm_split"));
+  {
+    DenseArgs a{};
+    a.M = M; a.N = F; a.K = D; a.terms = kActTerms; a.w_row0 = l * F; a.epi = E_GELU_SPLIT; a.act2 = c->act2f; a.ldh = F;
+    LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_up, a, st));
+  }
+  {
+    DenseArgs a{};
+    a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
+    a.gate = c->adaln; a.rows_per_chunk = T;
+    for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 5 * D;
+    LAT_TRY(enqueue_dense(c, c->map_act_f, c->map_down, a, st));
+  }
+  return LAT_OK;
+}
+
 // ---------------------------------------------------------------------------
 // ABI
 // ---------------------------------------------------------------------------
@@ -509,6 +898,8 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     cudaFuncSetAttribute(skinny_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          skinny_smem_bytes(kStages));
     set_attention_smem_limits();
+    cudaFuncSetAttribute(dense_gemm_kernel<kDStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         dense_smem_bytes(kDStages));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       delete c;
@@ -516,7 +907,9 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     }
     attr_done = true;
   }
-  lat_status s = create_pi0(c, w);
+  lat_status s = desc->kind == LAT_PI0_ACTION_EXPERT ? create_pi0(c, w)
+                 : desc->kind == LAT_PI0_PREFIX        ? create_prefix(c, w)
+                                                       : create_dit(c, w);
   if (s != LAT_OK) {
     std::string msg = g_last_error;
     cudaDeviceSynchronize();
@@ -535,13 +928,18 @@ lat_status lat_set_schedule(lat_ctx* c, const float* t, int n) {
     if (!(t[i + 1] > t[i])) return fail(LAT_ERR_ARG, "schedule must be increasing");
   std::vector<double> tt(t, t + n);
   CUDA_TRY(cudaDeviceSynchronize());
+  if (c->d.kind == LAT_DIT) return build_adaln(c, tt);
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "the prefix model has no schedule");
   return build_schedule(c, tt);
 }
 
 lat_status lat_prefill_kv(lat_ctx* c, const void* patch_emb, int B, void* kv, void* stream) {
-  (void)patch_emb; (void)B; (void)kv; (void)stream;
-  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
-  return fail(LAT_ERR_STATE, "lat_prefill_kv needs a LAT_PI0_PREFIX context");
+  if (!c || !patch_emb || !kv) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_PI0_PREFIX) return fail(LAT_ERR_STATE, "lat_prefill_kv needs a LAT_PI0_PREFIX context");
+  if (B < 1 || B > c->d.max_batch) return fail(LAT_ERR_SHAPE, "B = %d outside [1, max_batch = %d]", B, c->d.max_batch);
+  if (!aligned16(patch_emb) || !aligned16(kv)) return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  return enqueue_prefill(c, reinterpret_cast<const bf16*>(patch_emb), B, reinterpret_cast<bf16*>(kv),
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 static lat_status check_dev_err(lat_ctx* c) {
@@ -560,7 +958,19 @@ lat_status lat_block_forward(lat_ctx* c, int layer, float* x, const lat_chunk_de
     if (chunks != nullptr || n != 1) return fail(LAT_ERR_ARG, "pi0 block: chunks must be NULL and n == 1");
     return enqueue_pi0_block(c, layer, x, reinterpret_cast<bf16*>(kv), reinterpret_cast<cudaStream_t>(stream));
   }
-  return fail(LAT_ERR_STATE, "unsupported context kind");
+  if (c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "lat_block_forward: the prefix model runs via lat_prefill_kv");
+  if (!chunks || n < 1 || n > c->d.max_batch) return fail(LAT_ERR_ARG, "DiT block: need 1 <= n <= max_batch chunks");
+  for (int i = 0; i < n; ++i) {
+    const lat_chunk_desc& a = chunks[i];
+    if (a.chunk < 0 || a.step < 0 || a.step >= c->d.S || a.stream < 0 || a.stream >= c->d.n_streams)
+      return fail(LAT_ERR_ARG, "chunk %d: index out of range", i);
+    if ((long long)a.chunk * c->d.T_q > 0x7fffffffLL) return fail(LAT_ERR_ARG, "chunk %d: position overflow", i);
+    for (int j = 0; j < i; ++j)
+      if (chunks[j].stream == a.stream && chunks[j].step == a.step &&
+          ring_slot_of(chunks[j].chunk, c->d.n_hist) == ring_slot_of(a.chunk, c->d.n_hist))
+        return fail(LAT_ERR_ARG, "chunks %d and %d share a ring slot", j, i);
+  }
+  return enqueue_dit_block(c, layer, x, chunks, n, reinterpret_cast<bf16*>(kv), reinterpret_cast<cudaStream_t>(stream));
 }
 
 lat_status lat_denoise_chunk(lat_ctx* c, void* kv, const float* state, float* x, void* stream) {
@@ -672,6 +1082,27 @@ lat_status lat_debug_attention(lat_ctx* c, const float* q, const void* k, const 
   return enqueue_attention(d, q, d.Hq * d.dh, reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v),
                            d.Hkv * d.dh, T_q, T_kv, n_split, out, d.Hq * d.dh, c->pm, c->pl, c->po,
                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+lat_status lat_debug_dense_gemm(lat_ctx* c, int which, int layer, const void* act, int M, int terms, float* out,
+                                void* stream) {
+  if (!c || !act || !out) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_PI0_PREFIX && c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "needs a dense context");
+  const lat_model_desc& d = c->d;
+  if (which < 0 || which > 3 || layer < 0 || layer >= d.L || M < 1 || M > c->m_max || terms < 1 || terms > 3)
+    return fail(LAT_ERR_ARG, "bad argument");
+  if (!aligned16(act) || !aligned16(out)) return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  const int qd = d.Hq * d.dh;
+  const int ffn_rows = d.kind == LAT_PI0_PREFIX ? 2 * d.F : d.F;
+  const int N[4] = {c->nqkv, d.D, ffn_rows, d.D};
+  const int K[4] = {d.D, qd, d.D, d.F};
+  const CUtensorMap* wm[4] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down};
+  CUtensorMap amap;
+  LAT_TRY(make_act_map(&amap, act, M, terms * K[which]));
+  DenseArgs a{};
+  a.M = M; a.N = N[which]; a.K = K[which]; a.terms = terms; a.w_row0 = layer * N[which];
+  a.epi = E_STORE; a.out = out; a.ldo = N[which];
+  return enqueue_dense(c, amap, *wm[which], a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lat_status lat_debug_clear(lat_ctx* c, void* stream) {

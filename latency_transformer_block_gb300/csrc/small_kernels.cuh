@@ -38,6 +38,8 @@ struct QkvEpiArgs {
   int Hq, Hkv, dh;
   float* zero2;              // optional: second buffer row to clear, [T_q][zero2_ld]
   int zero2_ld;
+  float* k32;                // fp32 own K (after RoPE) and V as computed, [T_q][Hkv*dh]
+  float* v32;
 };
 
 static __global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
@@ -63,11 +65,17 @@ static __global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
       __nv_bfloat16* kr = a.k_cache + (size_t)query_slot(a.slot0, t) * a.kv_ld + head * a.dh;
       kr[i] = __float2bfloat16_rn(y0);
       kr[i + half] = __float2bfloat16_rn(y1);
+      float* k32 = a.k32 + (size_t)t * a.Hkv * a.dh + head * a.dh;
+      k32[i] = y0;
+      k32[i + half] = y1;
     }
   }
   const int vbase = (a.Hq + a.Hkv) * a.dh;
-  for (int j = threadIdx.x; j < a.Hkv * a.dh; j += blockDim.x)
-    a.v_cache[(size_t)query_slot(a.slot0, t) * a.kv_ld + j] = __float2bfloat16_rn(r * row[vbase + j]);
+  for (int j = threadIdx.x; j < a.Hkv * a.dh; j += blockDim.x) {
+    const float y = r * row[vbase + j];
+    a.v_cache[(size_t)query_slot(a.slot0, t) * a.kv_ld + j] = __float2bfloat16_rn(y);
+    a.v32[(size_t)t * a.Hkv * a.dh + j] = y;
+  }
   __syncthreads();
   for (int j = threadIdx.x; j < a.nqkv; j += blockDim.x) row[j] = 0.f;
   if (a.zero2)
@@ -162,11 +170,13 @@ static __global__ void head_euler_kernel(HeadArgs a) {
 // ---------------------------------------------------------------------------
 // Offline folds
 // ---------------------------------------------------------------------------
-// out[n][k] = bf16( g[k] * W[k][n] )  -- transpose to K-major with the RMSNorm
-// scale folded (g may be null: plain transpose).  W: bf16 [K][N] row-major;
-// out row stride = K.  32 x 32 tiles, blockDim (32, 8).
-static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, __nv_bfloat16* out, int K,
-                                      int N) {
+// out[orow(n)][k] = bf16( g[k] * W[k][n] )  -- transpose to K-major with the
+// RMSNorm scale folded (g may be null: plain transpose).  W: bf16 [K][N]
+// row-major; out row stride = K.  With il > 0 the output rows interleave blocks
+// of il rows: orow(n) = (n / il) * 2 il + il_off + n mod il (gate and up
+// projections share 2*il-row tiles).  32 x 32 tiles, blockDim (32, 8).
+static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, __nv_bfloat16* out,
+                                             int K, int N, int il, int il_off) {
   __shared__ float tile[32][33];
   const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -181,7 +191,10 @@ static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int n = n0 + i, k = k0 + threadIdx.x;
-    if (n < N && k < K) out[(size_t)n * K + k] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+    if (n < N && k < K) {
+      const size_t orow = il > 0 ? (size_t)(n / il) * 2 * il + il_off + n % il : (size_t)n;
+      out[orow * K + k] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+    }
   }
 }
 

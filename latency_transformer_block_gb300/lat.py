@@ -77,6 +77,8 @@ def lib():
         L.lat_debug_attention.restype = st
         L.lat_chunk_attention_noalloc.argtypes = [_P, _P, _P, _P] + [ctypes.c_int] * 5 + [_P]
         L.lat_chunk_attention_noalloc.restype = st
+        L.lat_debug_dense_gemm.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P, _P]
+        L.lat_debug_dense_gemm.restype = st
         L.lat_debug_clear.argtypes = [_P, _P]
         L.lat_debug_clear.restype = st
         L.lat_sync.argtypes = [_P]
@@ -156,6 +158,10 @@ class Context:
     def debug_attention(self, q, k, v, out, T_q, T_kv, stream=None):
         check(lib().lat_debug_attention(self.handle, ptr(q), ptr(k), ptr(v), ptr(out), T_q, T_kv,
                                         stream_ptr(stream)))
+
+    def debug_dense_gemm(self, which, layer, act, M, terms, out, stream=None):
+        check(lib().lat_debug_dense_gemm(self.handle, which, layer, ptr(act), M, terms, ptr(out),
+                                         stream_ptr(stream)))
 
     def debug_clear(self, stream=None):
         check(lib().lat_debug_clear(self.handle, stream_ptr(stream)))

@@ -78,3 +78,68 @@ class Pi0ActionExpert:
 def bits_of(t: torch.Tensor) -> np.ndarray:
     """bf16 torch tensor -> uint16 bit patterns (host)."""
     return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class _Uploader:
+    def __init__(self, device):
+        self.device = device
+        self.keep = []
+
+    def __call__(self, bits):
+        t = _dev_bf16(bits, self.device)
+        self.keep.append(t)
+        return lat.ptr(t)
+
+
+class Pi0Prefix:
+    """The prefix model behind lat_prefill_kv (per-layer K/V of the vision tokens)."""
+
+    def __init__(self, cfg: dict, weight_bits: dict, max_batch: int = 1, device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        up = _Uploader(self.device)
+        blocks = (lat.BlockWeights * cfg["L"])()
+        for l, b in enumerate(weight_bits["blocks"]):
+            for k in ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "wg", "wu", "wd"):
+                setattr(blocks[l], k, up(b[k]))
+        w = lat.Weights()
+        w.blocks = blocks
+        w.w_patch = up(weight_bits["w_patch"])
+        w.b_patch = up(weight_bits["b_patch"])
+        self._blocks = blocks
+        self.ctx = lat.Context(desc_from_config(cfg, lat.LAT_PI0_PREFIX, max_batch=max_batch), w)
+        torch.cuda.synchronize()
+
+    def new_kv(self, B):
+        c = self.cfg
+        return torch.zeros((c["L"], B, 2, c["T_prefix"] + c["T_q"], c["Hkv"] * c["dh"]),
+                           dtype=torch.bfloat16, device=self.device)
+
+    def prefill(self, patch_emb: torch.Tensor, kv: torch.Tensor, stream=None):
+        self.ctx.prefill_kv(patch_emb, patch_emb.shape[0], kv, stream)
+
+
+class DitStage:
+    """One DiT stage (L blocks) behind lat_block_forward."""
+
+    def __init__(self, cfg: dict, weight_bits: dict, max_batch: int = 4, n_streams: int = 1, device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        up = _Uploader(self.device)
+        L = len(weight_bits["blocks"])
+        blocks = (lat.BlockWeights * L)()
+        for l, b in enumerate(weight_bits["blocks"]):
+            for k in ("wq", "wk", "wv", "wo", "w1", "w2"):
+                setattr(blocks[l], k, up(b[k]))
+        w = lat.Weights()
+        w.blocks = blocks
+        for k in ("wt1", "bt1", "wt2", "bt2", "wmod", "bmod"):
+            setattr(w, k, up(weight_bits[k]))
+        self._blocks = blocks
+        cfg = dict(cfg, L=L)
+        self.cfg = cfg
+        self.ctx = lat.Context(desc_from_config(cfg, lat.LAT_DIT, max_batch=max_batch, n_streams=n_streams), w)
+        torch.cuda.synchronize()
+
+    def block(self, layer, x: torch.Tensor, chunks, ring: torch.Tensor, stream=None):
+        self.ctx.block_forward(layer, x, ring, chunks=chunks, stream=stream)

@@ -20,9 +20,10 @@ Readings where the pages are silent (listed in the design notes):
   chunk c lives in slot c mod 5.  Chunk c at step s attends to its own tokens
   and to chunks c-1 .. c-n_hist (those >= 0) of the same stream at the same
   step.  Token j of chunk c has RoPE position c * T_chunk + j.
-* A batched call first writes every chunk's own K/V into its slot, then runs
-  attention for every chunk.  Two chunks of one call may not share a
-  (stream, step, slot).
+* A batched call first writes every chunk's own K/V into its slot (bf16, the
+  ring's format), then runs attention for every chunk.  A chunk's history keys
+  are the ring's bf16 values; its own keys enter its attention as computed.
+  Two chunks of one call may not share a (stream, step, slot).
 """
 import numpy as np
 
@@ -73,7 +74,7 @@ def block_batch(xs, descs, ring, table, w, cfg):
         key = (st, s, ring_slot(c, nh))
         assert key not in seen, "two chunks of one call share a ring slot"
         seen.add(key)
-    qs, mods = [], []
+    qs, mods, own = [], [], []
     # phase 1: norm + modulation + QKV + RoPE; own K/V into the ring
     for b, (st, c, s) in enumerate(descs):
         sh1, sc1, g1, sh2, sc2, g2 = _split6(table[s], D)
@@ -86,13 +87,14 @@ def block_batch(xs, descs, ring, table, w, cfg):
         ring[st, s, ring_slot(c, nh), 0] = bf16.round_rne(k.reshape(T, D))
         ring[st, s, ring_slot(c, nh), 1] = bf16.round_rne(v.reshape(T, D))
         qs.append(q)
+        own.append((k.reshape(T, D), v.reshape(T, D)))
     # phase 2: attention over history + own, then the rest of the block
     out = np.empty((n, T, D))
     for b, (st, c, s) in enumerate(descs):
         sh1, sc1, g1, sh2, sc2, g2 = mods[b]
-        chunks = history_chunks(c, nh) + [c]
-        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in chunks])
-        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in chunks])
+        hist = history_chunks(c, nh)
+        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in hist] + [own[b][0]])
+        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in hist] + [own[b][1]])
         o = attention(qs[b], K.reshape(-1, H, dh), V.reshape(-1, H, dh),
                       1.0 / np.sqrt(dh)).reshape(T, D)
         h = np.asarray(xs[b], np.float64) + g1 * (o @ w["wo"])
@@ -111,7 +113,7 @@ def block_batch_rows(xs, descs, ring, table, w, cfg, rows):
     D, H, dh, T, nh = cfg["D"], cfg["H"], cfg["dh"], cfg["T_chunk"], cfg["n_hist"]
     base, eps = cfg["rope_base"], cfg["eps"]
     rows = np.asarray(rows)
-    qs, mods = [], []
+    qs, mods, own = [], [], []
     for b, (st, c, s) in enumerate(descs):
         sh1, sc1, g1, sh2, sc2, g2 = _split6(table[s], D)
         mods.append((sh1, sc1, g1, sh2, sc2, g2))
@@ -121,13 +123,14 @@ def block_batch_rows(xs, descs, ring, table, w, cfg, rows):
         v = (u @ w["wv"]).reshape(T, H, dh)
         ring[st, s, ring_slot(c, nh), 0] = bf16.round_rne(k.reshape(T, D))
         ring[st, s, ring_slot(c, nh), 1] = bf16.round_rne(v.reshape(T, D))
+        own.append((k.reshape(T, D), v.reshape(T, D)))
         qs.append(rope((u[rows] @ w["wq"]).reshape(len(rows), H, dh), pos[rows], base))
     out = np.empty((len(descs), len(rows), D))
     for b, (st, c, s) in enumerate(descs):
         sh1, sc1, g1, sh2, sc2, g2 = mods[b]
-        chunks = history_chunks(c, nh) + [c]
-        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in chunks])
-        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in chunks])
+        hist = history_chunks(c, nh)
+        K = np.concatenate([ring[st, s, ring_slot(cc, nh), 0] for cc in hist] + [own[b][0]])
+        V = np.concatenate([ring[st, s, ring_slot(cc, nh), 1] for cc in hist] + [own[b][1]])
         o = attention(qs[b], K.reshape(-1, H, dh), V.reshape(-1, H, dh),
                       1.0 / np.sqrt(dh)).reshape(len(rows), D)
         h = np.asarray(xs[b], np.float64)[rows] + g1 * (o @ w["wo"])

@@ -12,8 +12,9 @@ Readings where the pages are silent (listed in the design notes):
   FFN(u) = (GELU_tanh(u Wg) * (u Wu)) Wd, no biases inside blocks.
 * Attention is bidirectional over [prefix cache | own 64 tokens], multi-query
   (all q heads share the single KV head).  K is stored after RoPE.  The own
-  tokens' K and V are written into cache slots T_prefix .. T_prefix+63 and read
-  back from there, so attention sees them in the cache's bf16 format.
+  tokens' K and V are written into cache slots T_prefix .. T_prefix+63 in the
+  cache's bf16 format for later readers; the block's own attention uses them as
+  computed (the prefix keys are the cache's bf16 values).
 * Positions: prefix token i -> i; query token j (j = 0 is the state token) ->
   T_prefix + j.
 * Time grid t_s = s / S, dt = 1 / S; x_{s+1} = x_s + dt * v(x_s, t_s).
@@ -76,7 +77,8 @@ def block(x, k_prefix, v_prefix, pos, w, cfg, kv_only=False):
 
     x[T, D] residual stream; k_prefix/v_prefix[Tp, Hkv*dh] cached (post-RoPE);
     pos[T] positions of the own tokens.  Returns (x', k_own, v_own), k_own and
-    v_own being the bf16 values written to the cache (post-RoPE K).
+    v_own being the bf16 values written to the cache (post-RoPE K); the
+    attention inside the block uses the unrounded own K and V.
     """
     T = x.shape[0]
     Hq, Hkv, dh = cfg["Hq"], cfg["Hkv"], cfg["dh"]
@@ -84,12 +86,14 @@ def block(x, k_prefix, v_prefix, pos, w, cfg, kv_only=False):
     q, k, v = qkv(x, w, cfg)
     q = rope(q, pos, base)
     k = rope(k, pos, base)
-    k_own = bf16.round_rne(k.reshape(T, Hkv * dh))
-    v_own = bf16.round_rne(v.reshape(T, Hkv * dh))
+    k = k.reshape(T, Hkv * dh)
+    v = v.reshape(T, Hkv * dh)
+    k_own = bf16.round_rne(k)          # what the cache stores
+    v_own = bf16.round_rne(v)
     if kv_only:
         return None, k_own, v_own
-    K = np.concatenate([k_prefix, k_own]).reshape(-1, Hkv, dh)
-    V = np.concatenate([v_prefix, v_own]).reshape(-1, Hkv, dh)
+    K = np.concatenate([k_prefix, k]).reshape(-1, Hkv, dh)
+    V = np.concatenate([v_prefix, v]).reshape(-1, Hkv, dh)
     o = attention(q, K, V, 1.0 / np.sqrt(dh)).reshape(T, Hq * dh)
     h = x + o @ w["wo"]
     hn = rmsnorm(h, cfg["eps"]) * w["g_ffn"]

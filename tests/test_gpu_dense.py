@@ -1,0 +1,150 @@
+"""GPU parity of the dense path (prefix prefill and DiT stage) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from latency_transformer_block_gb300 import lat, synth
+from latency_transformer_block_gb300.models import DitStage, Pi0Prefix, _dev_bf16, bits_of
+from oracle import bf16, dit, pi0
+from tests.parity import BLOCK_TOL, FINAL_TOL, assert_bf16_close, assert_rel
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------------------
+# prefix prefill
+# ----------------------------------------------------------------------------
+def _prefill(cfg, B, seed=0, max_batch=None, model=None):
+    wb = synth.prefill_weights(cfg, seed)
+    pe = synth.prefill_inputs(cfg, B, seed)["patch_emb"]
+    m = model or Pi0Prefix(cfg, wb, max_batch=max_batch or B)
+    kv = m.new_kv(B)
+    m.prefill(_dev_bf16(pe, "cuda"), kv)
+    m.ctx.sync()
+    return wb, pe, bits_of(kv), m
+
+
+SMALL_PREFIX = dict(D=512, Hq=2, Hkv=1, dh=256, F=1024, L=3, T_prefix=100, T_q=8, patch_dim=192)
+
+
+def test_prefill_small_parity():
+    cfg = synth.config("prefill", **SMALL_PREFIX)
+    wb, pe, got, _ = _prefill(cfg, 2)
+    ref = pi0.prefill(pe, wb, cfg)
+    Tp = cfg["T_prefix"]
+    # layer 0: one block from exact inputs -> cache values within one bf16 ulp
+    assert_bf16_close(got[0, :, :, :Tp], ref[0, :, :, :Tp], "prefill layer 0 KV")
+    assert_rel(bf16.decode(got[:, :, :, :Tp]), bf16.decode(ref[:, :, :, :Tp]), FINAL_TOL, "prefill KV all layers")
+    assert not np.any(got[:, :, :, Tp:]), "own-token slots must stay untouched"
+
+
+def test_prefill_full_b1_and_batch_independence():
+    cfg = synth.config("prefill")
+    wb = synth.prefill_weights(cfg, 0)
+    m = Pi0Prefix(cfg, wb, max_batch=8)
+    pe8 = synth.prefill_inputs(cfg, 8, 0)["patch_emb"]
+    kv8 = m.new_kv(8)
+    m.prefill(_dev_bf16(pe8, "cuda"), kv8)
+    kv1 = m.new_kv(1)
+    m.prefill(_dev_bf16(pe8[3:4], "cuda"), kv1)
+    m.ctx.sync()
+    got8, got1 = bits_of(kv8), bits_of(kv1)
+    # batch elements are independent and row-wise identical work: bit-exact
+    assert np.array_equal(got8[:, 3:4], got1)
+    ref = pi0.prefill(pe8[3:4], wb, cfg)
+    Tp = cfg["T_prefix"]
+    assert_bf16_close(got1[0, :, :, :Tp], ref[0, :, :, :Tp], "prefill full layer 0 KV")
+    assert_rel(bf16.decode(got1[:, :, :, :Tp]), bf16.decode(ref[:, :, :, :Tp]), FINAL_TOL, "prefill full KV")
+
+
+# ----------------------------------------------------------------------------
+# DiT stage
+# ----------------------------------------------------------------------------
+def _dit_case(cfg, descs, seed=0, streams=1, layer=0, rows=None):
+    wb = synth.dit_weights(cfg, seed)
+    n = len(descs)
+    m = DitStage(cfg, wb, max_batch=n, n_streams=streams)
+    ring_bits = synth.dit_ring(cfg, seed, streams=streams, layers=cfg["L"])
+    xs = synth.dit_latents(cfg, n, seed)
+    x = torch.from_numpy(xs).cuda()
+    ring = _dev_bf16(ring_bits, "cuda")
+    m.block(layer, x, descs, ring)
+    m.ctx.sync()
+    got_x, got_ring = x.cpu().numpy(), bits_of(ring)
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    table = dit.adaln_table(W, cfg)
+    w = pi0.decode_tree(wb["blocks"][layer])
+    r = bf16.decode(ring_bits[:, layer])
+    if rows is None:
+        ref_x = dit.block_batch(xs, descs, r, table, w, cfg)
+    else:
+        ref_x = dit.block_batch_rows(xs, descs, r, table, w, cfg, rows)
+        got_x = got_x[:, rows]
+    return got_x, ref_x, got_ring[:, layer], bf16.encode(r), ring_bits[:, layer]
+
+
+SMALL_DIT = dict(D=256, H=2, dh=128, F=512, L=2, T_chunk=100, t_dim=64)
+
+
+@pytest.mark.parametrize("descs,streams,layer", [
+    ([(0, 7, 0), (0, 6, 1), (0, 5, 2), (0, 4, 3)], 1, 1),     # steady state, 4 chunks at steps 0..3
+    ([(0, 0, 0), (1, 2, 0), (1, 9, 3)], 2, 0),                 # first chunk (no history), two streams
+    ([(0, 3, 2)], 1, 0),                                       # single chunk, partial history
+])
+def test_dit_small_parity(descs, streams, layer):
+    cfg = synth.config("dit_1p3b", **SMALL_DIT)
+    got_x, ref_x, got_ring, ref_ring, ring_in = _dit_case(cfg, descs, streams=streams, layer=layer)
+    assert_rel(got_x, ref_x, BLOCK_TOL, "dit small block residual")
+    nh = cfg["n_hist"]
+    for (st, c, s) in descs:
+        slot = c % (nh + 1)
+        assert_bf16_close(got_ring[st, s, slot], ref_ring[st, s, slot], f"dit own KV chunk {c}")
+    # every other slot is untouched
+    touched = {(st, s, c % (nh + 1)) for (st, c, s) in descs}
+    for st in range(streams):
+        for s in range(cfg["S"]):
+            for sl in range(nh + 1):
+                if (st, s, sl) not in touched:
+                    assert np.array_equal(got_ring[st, s, sl], ring_in[st, s, sl])
+
+
+def test_dit_1p3b_full_block_sampled_rows():
+    cfg = synth.config("dit_1p3b", L=1)
+    descs = synth.dit_chunk_descs(cfg, 4)
+    rows = np.r_[0:8, 700:708, 1530:1560]          # includes the ragged last tile
+    got_x, ref_x, got_ring, ref_ring, _ = _dit_case(cfg, descs, rows=rows)
+    assert_rel(got_x, ref_x, BLOCK_TOL, "dit 1.3B block residual (sampled rows)")
+    for (st, c, s) in descs:
+        sl = c % 5
+        assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 1.3B own KV chunk {c}")
+
+
+def test_dit_14b_block_batch8_sampled_rows():
+    cfg = synth.config("dit_14b")
+    descs = synth.dit_chunk_descs(cfg, 8)
+    rows = np.r_[0:4, 777:781, 1556:1560]
+    got_x, ref_x, got_ring, ref_ring, _ = _dit_case(cfg, descs, streams=2, rows=rows)
+    assert_rel(got_x, ref_x, BLOCK_TOL, "dit 14B block residual (sampled rows)")
+    for (st, c, s) in descs:
+        sl = c % 5
+        assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 14B own KV chunk {c}")
+
+
+def test_dit_indices_and_errors():
+    cfg = synth.config("dit_1p3b", **SMALL_DIT)
+    wb = synth.dit_weights(cfg, 0)
+    m = DitStage(cfg, wb, max_batch=4, n_streams=2)
+    chunks = [(0, c, 0) for c in range(13)] + [(1, 123456, 2)]
+    slots, pos = m.ctx.debug_indices(chunks=chunks)
+    assert slots == [dit.ring_slot(c, cfg["n_hist"]) for (_, c, _) in chunks]
+    assert pos == [int(dit.positions(c, cfg["T_chunk"])[0]) for (_, c, _) in chunks]
+    ring = torch.zeros(1, device="cuda", dtype=torch.bfloat16)
+    x = torch.zeros(16, device="cuda")
+    for bad in ([(0, 5, 0), (0, 10, 0)],       # same stream, step and slot
+                [(0, 5, 4)],                    # step out of range
+                [(2, 5, 0)],                    # stream out of range
+                [(0, -1, 0)],
+                [(0, c, 0) for c in range(5)]):  # more than max_batch
+        with pytest.raises(lat.LatError) as e:
+            m.block(0, x, bad, ring)
+        assert e.value.code == 1

@@ -303,15 +303,17 @@ def test_block_identity_and_wiring():
     zero = dict(blk, wo=np.zeros_like(blk["wo"]), wd=np.zeros_like(blk["wd"]))
     y, k_own, v_own = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, zero, cfg)
     assert np.array_equal(y, x)
-    # q = 0 -> uniform attention over [prefix | own]: o = mean of all V rows
+    # q = 0 -> uniform attention over [prefix | own]: o = mean of all V rows,
+    # the prefix from the cache, the own rows as computed
     unif = dict(blk, wq=np.zeros_like(blk["wq"]), wd=np.zeros_like(blk["wd"]))
     y, k_own, v_own = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, unif, cfg)
-    vmean = np.concatenate([kv[1, :Tp], v_own]).mean(axis=0)            # [Hkv*dh]
+    xn = ops.rmsnorm(x, cfg["eps"]) * blk["g_attn"]
+    v_exact = xn @ blk["wv"]
+    vmean = np.concatenate([kv[1, :Tp], v_exact]).mean(axis=0)          # [Hkv*dh]
     o = np.tile(vmean, cfg["Hq"] // cfg["Hkv"])                          # every q head
     assert np.allclose(y, x + o[None, :] @ blk["wo"], rtol=1e-12, atol=1e-13)
-    # own V is the bf16 of the projected (un-rotated) values
-    xn = ops.rmsnorm(x, cfg["eps"]) * blk["g_attn"]
-    assert np.array_equal(v_own, bf16.round_rne(xn @ blk["wv"]))
+    # the cache receives the bf16 of the projected (un-rotated) values
+    assert np.array_equal(v_own, bf16.round_rne(v_exact))
     # with attention removed the FFN sees the *normed* residual (pre-norm)
     noatt = dict(blk, wo=np.zeros_like(blk["wo"]))
     y, _, _ = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, noatt, cfg)
@@ -399,11 +401,14 @@ def test_dit_zero_gates_is_identity_and_history_set():
     bm2 = RNG.standard_normal(6 * D) * 0.1
     t2 = np.broadcast_to(bm2, (cfg["S"], 6 * D)).copy()
     wz = dict(w, wq=np.zeros_like(w["wq"]), w2=np.zeros_like(w["w2"]))
+    u = ops.layernorm(xs[0].astype(np.float64), cfg["eps"]) * (1 + bm2[D:2 * D]) + bm2[:D]
+    v_own = u @ w["wv"]
     for c in (0, 2, 9):
         r = ring.copy()
         out = dit.block_batch(xs, [(0, c, 1)], r, t2, wz, cfg)
-        chunks = [cc for cc in range(c - 4, c + 1) if cc >= 0]
-        V = np.concatenate([r[0, 1, cc % 5, 1] for cc in chunks])
+        hist = [cc for cc in range(c - 4, c) if cc >= 0]
+        V = np.concatenate([r[0, 1, cc % 5, 1] for cc in hist] + [v_own])
+        assert np.array_equal(r[0, 1, c % 5, 1], bf16.round_rne(v_own))
         o = V.mean(axis=0)
         expect = xs[0] + bm2[2 * D:3 * D] * (o[None, :] @ w["wo"])
         assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
