@@ -34,6 +34,7 @@ struct AttnArgs {
   const float* v_own;
   int own0;
   int own_ld;
+  int force_partials;        // write partials even with one key range (combine follows)
 };
 
 // 8 fp32 values -> 8 bf16 hi and 8 bf16 lo (two-term split)
@@ -73,6 +74,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
+// 16-byte async copy global -> shared; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Split a pair of fp32 values into three packed bf16x2 words.
 __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
   Split3 a = split3(x), b = split3(y);
@@ -83,12 +91,16 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint3
 
 template <int DH>
 static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int KB = 64;          // keys per block
   constexpr int LD = DH + 8;      // padded smem row (bf16): conflict-free ldmatrix
   constexpr int NT = DH / 8;      // output n-tiles
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [2 planes][KB][LD]
   __nv_bfloat16* sV = sK + 2 * KB * LD;
+  float* sQ = reinterpret_cast<float*>(sV + 2 * KB * LD);            // [64 rows][DH + 4]
+  constexpr int QLD = DH + 4;
 
   const int h = blockIdx.x;
   const int qt = blockIdx.y;
@@ -102,8 +114,15 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
   const int r0 = qt * 64 + warp * 16 + g;   // this thread's two query rows: r0, r0 + 8
   const int r1 = r0 + 8;
   const bool v0 = r0 < a.T_q, v1 = r1 < a.T_q;
-  const float* q0 = a.q + (size_t)(v0 ? r0 : 0) * a.q_ld + h * DH;
-  const float* q1 = a.q + (size_t)(v1 ? r1 : 0) * a.q_ld + h * DH;
+  // stage this CTA's 64 query rows of head h (zero rows past T_q)
+  for (int idx = threadIdx.x; idx < 64 * (DH / 4); idx += 128) {
+    const int row = idx / (DH / 4), c4 = idx % (DH / 4);
+    const int qr = qt * 64 + row;
+    cp_async16(sQ + row * QLD + c4 * 4, a.q + (size_t)(qr < a.T_q ? qr : 0) * a.q_ld + h * DH + c4 * 4,
+               qr < a.T_q ? 16 : 0);
+  }
+  const float* q0 = sQ + (warp * 16 + g) * QLD;
+  const float* q1 = q0 + 8 * QLD;
 
   float o[NT][4];
 #pragma unroll
@@ -120,38 +139,41 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
     for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
       const int row = idx / (DH / 8), c8 = idx % (DH / 8);
       const int key = kb * KB + row;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 kk = z, vv = z, kl = z, vl = z;
-      if (key < a.T_kv) {
-        if (a.k_own != nullptr && key >= a.own0) {
-          const size_t o = (size_t)(key - a.own0) * a.own_ld + kvh * DH + c8 * 8;
-          split8_to(a.k_own + o, kk, kl);
-          split8_to(a.v_own + o, vv, vl);
-        } else {
-          kk = *reinterpret_cast<const uint4*>(a.k + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
-          vv = *reinterpret_cast<const uint4*>(a.v + (size_t)key * a.kv_ld + kvh * DH + c8 * 8);
+      const bool own = a.k_own != nullptr && key >= a.own0 && key < a.T_kv;
+      if (!own) {   // cache keys (and zero fill past T_kv) by async copy
+        const bool in = key < a.T_kv;
+        const size_t o = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
+        cp_async16(sK + row * LD + c8 * 8, a.k + o, in ? 16 : 0);
+        cp_async16(sV + row * LD + c8 * 8, a.v + o, in ? 16 : 0);
+        if (has_lo) {
+          *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
         }
-      }
-      *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
-      *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
-      if (has_lo) {
+      } else {      // own keys as computed: hi and lo planes
+        const size_t o = (size_t)(key - a.own0) * a.own_ld + kvh * DH + c8 * 8;
+        uint4 kk, kl, vv, vl;
+        split8_to(a.k_own + o, kk, kl);
+        split8_to(a.v_own + o, vv, vl);
+        *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
+        *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
         *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
         *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
       }
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // ---- S = Q K^T for 16 rows x 64 keys (8 n-tiles) ----
     float s[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll 1
+#pragma unroll 2
     for (int ks = 0; ks < DH / 16; ++ks) {
       const int c = ks * 16 + 2 * tq;
-      float2 x00 = v0 ? *reinterpret_cast<const float2*>(q0 + c) : make_float2(0.f, 0.f);
-      float2 x10 = v1 ? *reinterpret_cast<const float2*>(q1 + c) : make_float2(0.f, 0.f);
-      float2 x01 = v0 ? *reinterpret_cast<const float2*>(q0 + c + 8) : make_float2(0.f, 0.f);
-      float2 x11 = v1 ? *reinterpret_cast<const float2*>(q1 + c + 8) : make_float2(0.f, 0.f);
+      const float2 x00 = *reinterpret_cast<const float2*>(q0 + c);
+      const float2 x10 = *reinterpret_cast<const float2*>(q1 + c);
+      const float2 x01 = *reinterpret_cast<const float2*>(q0 + c + 8);
+      const float2 x11 = *reinterpret_cast<const float2*>(q1 + c + 8);
       uint32_t ah[4], am[4], al[4];
       split_pair(x00.x, x00.y, ah[0], am[0], al[0]);
       split_pair(x10.x, x10.y, ah[1], am[1], al[1]);
@@ -257,7 +279,7 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
   }
 
   // ---- write out ----
-  if (a.n_split == 1) {
+  if (a.n_split == 1 && !a.force_partials) {
     const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f, i1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -281,19 +303,44 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
 }
 
 // Merge key-range partials: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-// Grid (T_q, Hq), blockDim = dh.
-static __global__ void attention_combine_kernel(AttnArgs a, int dh) {
+// Grid (T_q, Hq), blockDim = dh.  With planes != null the result is written as
+// the three bf16 planes [3][64][Hq*dh] of the output projection's activation.
+static __global__ void attention_combine_kernel(AttnArgs a, int dh, __nv_bfloat16* planes) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  constexpr int MAXS = 32;
+  float mv[MAXS], lv[MAXS], ov[MAXS];
   float M = -INFINITY;
-  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.part_m[((size_t)s * a.Hq + h) * a.T_q + t]);
-  float L = 0.f, acc = 0.f;
-  for (int s = 0; s < a.n_split; ++s) {
-    const size_t i = ((size_t)s * a.Hq + h) * a.T_q + t;
-    const float w = (a.part_m[i] == -INFINITY) ? 0.f : exp2f(a.part_m[i] - M);
-    L += w * a.part_l[i];
-    acc += w * a.part_o[i * dh + d];
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < a.n_split) {
+      const size_t i = ((size_t)s * a.Hq + h) * a.T_q + t;
+      mv[s] = a.part_m[i];
+      lv[s] = a.part_l[i];
+      ov[s] = a.part_o[i * dh + d];
+      M = fmaxf(M, mv[s]);
+    }
   }
-  a.out[(size_t)t * a.out_ld + h * dh + d] = acc / L;
+  float L = 0.f, acc = 0.f;
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < a.n_split) {
+      const float w = (mv[s] == -INFINITY) ? 0.f : exp2f(mv[s] - M);
+      L += w * lv[s];
+      acc += w * ov[s];
+    }
+  }
+  const float o = acc / L;
+  if (planes) {
+    const int K = a.Hq * dh, c = h * dh + d;
+    const Split3 s3 = split3(o);
+    planes[(size_t)t * K + c] = s3.hi;
+    planes[(size_t)(64 + t) * K + c] = s3.mid;
+    planes[(size_t)(128 + t) * K + c] = s3.lo;
+  } else {
+    a.out[(size_t)t * a.out_ld + h * dh + d] = o;
+  }
 }
 
 
@@ -525,8 +572,9 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
 // Launch the attention (and the combine when there are several key ranges).
 // The kernels need more than 48 KB of dynamic shared memory for dh = 256:
 // call set_attention_smem_limits() once per device first.
-// K and V tiles, two planes each, rows padded to dh + 8
-static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2; }
+// K and V tiles, two planes each, rows padded to dh + 8; plus the fp32 Q tile
+// of the chunk kernel (rows padded to dh + 4)
+static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2 + 64 * (dh + 4) * 4; }
 
 static inline cudaError_t set_attention_smem_limits() {
   cudaFuncSetAttribute(attention_seg_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
@@ -545,7 +593,7 @@ static inline cudaError_t launch_chunk_attention(const AttnArgs& a, int dh, cuda
   else attention_kernel<256><<<grid, 128, smem, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
-  attention_combine_kernel<<<dim3(a.T_q, a.Hq), dh, 0, st>>>(a, dh);
+  attention_combine_kernel<<<dim3(a.T_q, a.Hq), dh, 0, st>>>(a, dh, nullptr);
   return cudaGetLastError();
 }
 

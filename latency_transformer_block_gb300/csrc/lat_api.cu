@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <utility>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -123,6 +124,8 @@ struct lat_ctx {
   float* sin_t = nullptr;
 
   // workspace
+  bf16 *planes_x = nullptr, *planes_o = nullptr, *planes_h = nullptr;   // [3][64][K] activation planes
+  CUtensorMap bmap_x, bmap_o, bmap_h;
   float *xres = nullptr, *qkv_acc = nullptr, *gu_acc = nullptr, *q = nullptr, *o = nullptr, *r1 = nullptr,
         *r2 = nullptr, *z = nullptr, *pm = nullptr, *pl = nullptr, *po = nullptr, *state_emb = nullptr,
         *temb = nullptr;
@@ -164,6 +167,7 @@ struct lat_ctx {
 };
 
 static constexpr int kStages = 4;
+static constexpr int kMaxKeySplits = 32;   // partials the combine kernel merges
 
 static lat_status launch_check(const char* what) {
   cudaError_t e = cudaGetLastError();
@@ -184,16 +188,54 @@ static GemmPlan plan_gemm(int N_out, int K, int num_sms) {
   return p;
 }
 
-static lat_status enqueue_skinny(const lat_ctx* c, const CUtensorMap& map, const GemmPlan& g, int layer,
-                                 SkinnyArgs a, cudaStream_t st) {
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream finishes; it orders itself with
+// griddepcontrol.wait before touching that kernel's results.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#define PDL_TRY(what, expr)                                                              \
+  do {                                                                                   \
+    cudaError_t e_ = (expr);                                                             \
+    if (e_ != cudaSuccess) return fail(LAT_ERR_CUDA, "launch %s: %s", what, cudaGetErrorString(e_)); \
+  } while (0)
+
+static lat_status enqueue_skinny(const lat_ctx* c, const CUtensorMap& map, const CUtensorMap& bmap,
+                                 const GemmPlan& g, int layer, SkinnyArgs a, cudaStream_t st) {
   a.w_row0 = layer * g.w_row0_per_layer;
   a.N_out = g.N_out;
   a.K = g.K;
   a.splits = g.splits;
   a.err = c->err;
   const int grid = (g.N_out / 128) * g.splits;
-  skinny_gemm_kernel<kStages><<<grid, 192, skinny_smem_bytes(kStages), st>>>(map, a);
-  return launch_check("skinny_gemm");
+  PDL_TRY("skinny_gemm", launch_pdl(skinny_gemm_kernel<kStages>, dim3(grid), dim3(192),
+                                    (size_t)skinny_smem_bytes(kStages), st, map, bmap, a));
+  return LAT_OK;
+}
+
+static lat_status enqueue_prep(const float* src, int ld, int K, int n_tok, int mode, int off, const float* row_scale,
+                               bf16* planes, float* stat_out, float eps, cudaStream_t st) {
+  PrepArgs a{src, ld, K, mode, off, row_scale, planes, stat_out, eps};
+  PDL_TRY("prep_planes", launch_pdl(prep_planes_kernel, dim3((K + 255) / 256, n_tok), dim3(256), 0, st, a));
+  return LAT_OK;
+}
+
+// planes [3 * 64][K] bf16 read by TMA in 192 x 64 boxes
+static lat_status make_planes_map(CUtensorMap* map, const void* base, int K) {
+  return make_kmajor_map(map, base, 192, K, 192);
 }
 
 // ---------------------------------------------------------------------------
@@ -387,7 +429,7 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   const int T = d.T_q;
   const int T_kv = d.T_prefix + d.T_q;
   const int nkb = (T_kv + 63) / 64;
-  c->attn_split = nkb;
+  c->attn_split = nkb < kMaxKeySplits ? nkb : kMaxKeySplits;
   LAT_TRY(c->alloc(&c->xres, (size_t)T * D));
   LAT_TRY(c->alloc(&c->qkv_acc, (size_t)T * c->nqkv));
   LAT_TRY(c->alloc(&c->gu_acc, (size_t)T * 2 * F));
@@ -400,6 +442,15 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(c->alloc(&c->pl, (size_t)c->attn_split * d.Hq * T));
   LAT_TRY(c->alloc(&c->po, (size_t)c->attn_split * d.Hq * T * d.dh));
   LAT_TRY(c->alloc(&c->state_emb, (size_t)D));
+  LAT_TRY(c->alloc(&c->planes_x, (size_t)192 * D));
+  LAT_TRY(c->alloc(&c->planes_o, (size_t)192 * qd));
+  LAT_TRY(c->alloc(&c->planes_h, (size_t)192 * F));
+  CUDA_TRY(cudaMemset(c->planes_x, 0, (size_t)192 * D * 2));
+  CUDA_TRY(cudaMemset(c->planes_o, 0, (size_t)192 * qd * 2));
+  CUDA_TRY(cudaMemset(c->planes_h, 0, (size_t)192 * F * 2));
+  LAT_TRY(make_planes_map(&c->bmap_x, c->planes_x, D));
+  LAT_TRY(make_planes_map(&c->bmap_o, c->planes_o, qd));
+  LAT_TRY(make_planes_map(&c->bmap_h, c->planes_h, F));
   LAT_TRY(c->alloc(&c->kown, (size_t)T * d.Hkv * d.dh));
   LAT_TRY(c->alloc(&c->vown, (size_t)T * d.Hkv * d.dh));
   LAT_TRY(c->alloc(&c->err, 1));
@@ -443,45 +494,56 @@ static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_lay
   const int T_kv = d.T_prefix + d.T_q;
   bf16* kc = kv_layer;
   bf16* vc = kv_layer + (size_t)T_kv * kvd;
-  // 1. merged QKV projection of x (RMS factor r1 computed alongside)
+  // 1. planes of x + RMS factor r1; merged QKV projection
+  LAT_TRY(enqueue_prep(xres, D, D, T, PREP_PLAIN, 0, nullptr, c->planes_x, c->r1, d.eps, st));
   {
     SkinnyArgs a{};
-    a.src = xres; a.src_ld = D; a.mode = B_PLAIN; a.n_tok = T;
-    a.out = c->qkv_acc; a.out_ld = c->nqkv;
-    a.stat_src = xres; a.stat_len = D; a.stat_out = c->r1; a.eps = d.eps;
-    LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, l, a, st));
+    a.n_tok = T; a.out = c->qkv_acc; a.out_ld = c->nqkv;
+    LAT_TRY(enqueue_skinny(c, c->map_qkv, c->bmap_x, c->g_qkv, l, a, st));
   }
   // 2. row scale + RoPE + K/V into the cache + q; clears qkv_acc and gu_acc
   {
     QkvEpiArgs a{c->qkv_acc, c->nqkv, c->r1, c->cos_t, c->sin_t, c->q, kc, vc, kvd, d.T_prefix,
                  d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F, c->kown, c->vown};
-    qkv_epilogue_kernel<<<T, 256, 0, st>>>(a);
-    LAT_TRY(launch_check("qkv_epilogue"));
+    PDL_TRY("qkv_epilogue", launch_pdl(qkv_epilogue_kernel, dim3(T), dim3(256), 0, st, a));
   }
-  // 3. attention over [prefix | own] (key ranges) + combine
-  LAT_TRY(enqueue_attention(d, c->q, qd, kc, vc, kvd, T, T_kv, c->attn_split, c->o, qd, c->pm, c->pl, c->po, st,
-                            c->kown, c->vown, d.T_prefix));
+  // 3. attention over [prefix | own] (key ranges) + combine into the O planes
+  {
+    AttnArgs a{};
+    a.q = c->q; a.q_ld = qd; a.k = kc; a.v = vc; a.kv_ld = kvd;
+    a.T_q = T; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+    a.n_split = c->attn_split;
+    a.out = c->o; a.out_ld = qd; a.part_m = c->pm; a.part_l = c->pl; a.part_o = c->po;
+    a.k_own = c->kown; a.v_own = c->vown; a.own0 = d.T_prefix; a.own_ld = kvd;
+    a.force_partials = 1;
+    const dim3 grid(d.Hq, (T + 63) / 64, a.n_split);
+    const size_t smem = attn_smem_bytes(d.dh);
+    if (d.dh == 64) PDL_TRY("attention", launch_pdl(attention_kernel<64>, grid, dim3(128), smem, st, a));
+    else if (d.dh == 128) PDL_TRY("attention", launch_pdl(attention_kernel<128>, grid, dim3(128), smem, st, a));
+    else PDL_TRY("attention", launch_pdl(attention_kernel<256>, grid, dim3(128), smem, st, a));
+    PDL_TRY("attention_combine", launch_pdl(attention_combine_kernel, dim3(T, d.Hq), dim3(d.dh), 0, st, a, d.dh,
+                                            c->planes_o));
+  }
   // 4. x += o Wo
   {
     SkinnyArgs a{};
-    a.src = c->o; a.src_ld = qd; a.mode = B_PLAIN; a.n_tok = T;
-    a.out = xres; a.out_ld = D;
-    LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, l, a, st));
+    a.n_tok = T; a.out = xres; a.out_ld = D;
+    LAT_TRY(enqueue_skinny(c, c->map_o, c->bmap_o, c->g_o, l, a, st));
   }
-  // 5. gate/up projection of x (RMS factor r2 alongside)
+  // 5. planes of x + RMS factor r2; gate/up projection
+  LAT_TRY(enqueue_prep(xres, D, D, T, PREP_PLAIN, 0, nullptr, c->planes_x, c->r2, d.eps, st));
   {
     SkinnyArgs a{};
-    a.src = xres; a.src_ld = D; a.mode = B_PLAIN; a.n_tok = T;
-    a.out = c->gu_acc; a.out_ld = 2 * F;
-    a.stat_src = xres; a.stat_len = D; a.stat_out = c->r2; a.eps = d.eps;
-    LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, l, a, st));
+    a.n_tok = T; a.out = c->gu_acc; a.out_ld = 2 * F;
+    LAT_TRY(enqueue_skinny(c, c->map_gu, c->bmap_x, c->g_gu, l, a, st));
   }
-  // 6. x += (GELU(r2 g) * (r2 u)) Wd
+  // 6. planes of GELU(r2 g) * (r2 u); x += h Wd
+  LAT_TRY(enqueue_prep(c->gu_acc, 2 * F, F, T, PREP_GEGLU, F, c->r2, c->planes_h, nullptr, d.eps, st));
   {
     SkinnyArgs a{};
-    a.src = c->gu_acc; a.src_ld = 2 * F; a.src2_off = F; a.row_scale = c->r2; a.mode = B_GEGLU; a.n_tok = T;
-    a.out = xres; a.out_ld = D;
-    LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, l, a, st));
+    a.n_tok = T; a.out = xres; a.out_ld = D;
+    LAT_TRY(enqueue_skinny(c, c->map_d, c->bmap_h, c->g_d, l, a, st));
   }
   return LAT_OK;
 }
@@ -494,19 +556,16 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
   // state token (once per chunk)
   LAT_TRY(small_gemm(state, false, A, c->w_state, true, D, c->b_state, true, c->state_emb, D, 1, D, A, 0, st));
   for (int s = 0; s < d.S; ++s) {
-    EmbedArgs e{x, c->wfold, c->ttab, c->b2, c->state_emb, c->z, c->xres, D, A, T, s};
-    embed_prologue_kernel<<<dim3((D + 255) / 256, T), 256, 0, st>>>(e);
-    LAT_TRY(launch_check("embed_prologue"));
+    EmbedArgs e{x, c->wfold, c->ttab, c->b2, c->state_emb, c->planes_x, c->xres, D, A, T, s};
+    PDL_TRY("embed_prologue", launch_pdl(embed_prologue_kernel, dim3((D + 255) / 256, T), dim3(256), 0, st, e));
     {
       SkinnyArgs a{};
-      a.src = c->z; a.src_ld = D; a.mode = B_SILU; a.n_tok = T - 1;
-      a.out = c->xres + D; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_w2, c->g_w2, 0, a, st));
+      a.n_tok = T - 1; a.out = c->xres + D; a.out_ld = D;
+      LAT_TRY(enqueue_skinny(c, c->map_w2, c->bmap_x, c->g_w2, 0, a, st));
     }
     for (int l = 0; l < d.L; ++l) LAT_TRY(enqueue_pi0_block(c, l, c->xres, kv + (size_t)l * layer_elems, st));
     HeadArgs h{c->xres, c->wout, c->bout, x, c->dt, s, D, A, d.eps};
-    head_euler_kernel<<<T - 1, 256, 0, st>>>(h);
-    LAT_TRY(launch_check("head_euler"));
+    PDL_TRY("head_euler", launch_pdl(head_euler_kernel, dim3(T - 1), dim3(256), 0, st, h));
   }
   return LAT_OK;
 }
@@ -1050,22 +1109,21 @@ lat_status lat_debug_gemm(lat_ctx* c, int which, int layer, int reps, void* stre
     const int l = (layer + r) % d.L;   // successive launches read different layers' weights (HBM, not L2)
     SkinnyArgs a{};
     a.n_tok = T;
-    a.mode = B_PLAIN;
     if (which == 0) {
-      a.src = c->xres; a.src_ld = D; a.out = c->qkv_acc; a.out_ld = c->nqkv;
-      LAT_TRY(enqueue_skinny(c, c->map_qkv, c->g_qkv, l, a, st));
+      a.out = c->qkv_acc; a.out_ld = c->nqkv;
+      LAT_TRY(enqueue_skinny(c, c->map_qkv, c->bmap_x, c->g_qkv, l, a, st));
     } else if (which == 1) {
-      a.src = c->o; a.src_ld = qd; a.out = c->xres; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_o, c->g_o, l, a, st));
-    } else if (which == 2) {
-      a.src = c->xres; a.src_ld = D; a.out = c->gu_acc; a.out_ld = 2 * F;
-      LAT_TRY(enqueue_skinny(c, c->map_gu, c->g_gu, l, a, st));
-    } else {
-      a.src = c->gu_acc; a.src_ld = 2 * F; a.src2_off = F; a.row_scale = c->r2; a.mode = B_GEGLU;
       a.out = c->xres; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_d, c->g_d, l, a, st));
+      LAT_TRY(enqueue_skinny(c, c->map_o, c->bmap_o, c->g_o, l, a, st));
+    } else if (which == 2) {
+      a.out = c->gu_acc; a.out_ld = 2 * F;
+      LAT_TRY(enqueue_skinny(c, c->map_gu, c->bmap_x, c->g_gu, l, a, st));
+    } else {
+      a.out = c->xres; a.out_ld = D;
+      LAT_TRY(enqueue_skinny(c, c->map_d, c->bmap_h, c->g_d, l, a, st));
     }
   }
+  (void)qd;
   return LAT_OK;
 }
 
@@ -1078,7 +1136,8 @@ lat_status lat_debug_attention(lat_ctx* c, const float* q, const void* k, const 
     return fail(LAT_ERR_SHAPE, "T_q / T_kv out of the context's range");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
-  const int n_split = (T_kv + 63) / 64;
+  const int nkb = (T_kv + 63) / 64;
+  const int n_split = nkb < kMaxKeySplits ? nkb : kMaxKeySplits;
   return enqueue_attention(d, q, d.Hq * d.dh, reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v),
                            d.Hkv * d.dh, T_q, T_kv, n_split, out, d.Hq * d.dh, c->pm, c->pl, c->po,
                            reinterpret_cast<cudaStream_t>(stream));

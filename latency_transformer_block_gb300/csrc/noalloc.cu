@@ -78,6 +78,7 @@ extern "C" lat_status lat_chunk_attention_noalloc(const float* q, const void* k,
   const int nkb = (T_kv + 63) / 64;
   int n_split = (int)(kNoAllocScratchFloats / per_split);
   if (n_split > nkb) n_split = nkb;
+  if (n_split > 32) n_split = 32;   // partials the combine kernel merges
   if (n_split < 1) n_split = 1;
 
   lat::AttnArgs a{};

@@ -43,6 +43,8 @@ struct QkvEpiArgs {
 };
 
 static __global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int half = a.dh / 2;
   const float r = a.r1[t];
@@ -85,6 +87,7 @@ static __global__ void qkv_epilogue_kernel(QkvEpiArgs a) {
 // ---------------------------------------------------------------------------
 // Embedding prologue of one denoise step (folded form, section 4.2 of the note):
 //   z[t][n]      = sum_a x[t][a] W'[a][n] + T[s][n]      (t < T_q - 1)
+//   planes       = three bf16 planes of SiLU(z) (the W2 GEMM's activation)
 //   xres[0][n]   = state token (precomputed for the chunk)
 //   xres[1+t][n] = b2[n]   (the W2 GEMM accumulates SiLU(z) W2 on top)
 // Grid (ceil(D/256), T_q), blockDim 256; row blockIdx.y == T_q - 1 writes the state row.
@@ -95,12 +98,14 @@ struct EmbedArgs {
   const float* ttab;     // fp32 [S][D]
   const float* b2;       // fp32 [D]
   const float* state_emb;  // fp32 [D]
-  float* z;              // fp32 [T_q-1][D]
+  __nv_bfloat16* planes; // [3][64][D]
   float* xres;           // fp32 [T_q][D]
   int D, A, T_q, step;
 };
 
 static __global__ void embed_prologue_kernel(EmbedArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int t = blockIdx.y;
   if (n >= a.D) return;
@@ -111,7 +116,10 @@ static __global__ void embed_prologue_kernel(EmbedArgs a) {
   float acc = a.ttab[(size_t)a.step * a.D + n];
   const float* xr = a.x + (size_t)t * a.A;
   for (int j = 0; j < a.A; ++j) acc = fmaf(xr[j], a.wfold[(size_t)j * a.D + n], acc);
-  a.z[(size_t)t * a.D + n] = acc;
+  const Split3 s3 = split3(silu(acc));
+  a.planes[(size_t)t * a.D + n] = s3.hi;
+  a.planes[(size_t)(64 + t) * a.D + n] = s3.mid;
+  a.planes[(size_t)(128 + t) * a.D + n] = s3.lo;
   a.xres[(size_t)(1 + t) * a.D + n] = a.b2[n];
 }
 
@@ -132,6 +140,8 @@ struct HeadArgs {
 };
 
 static __global__ void head_euler_kernel(HeadArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const float* h = a.xres + (size_t)(1 + t) * a.D;
   __shared__ float red[8][33];
@@ -215,6 +225,8 @@ __device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
 }
 
 static __global__ void small_gemm_kernel(SmallGemmArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int m = blockIdx.y;
   if (n >= a.N) return;
