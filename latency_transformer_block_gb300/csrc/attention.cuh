@@ -89,40 +89,75 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint3
   lo = pack_bf16(a.lo, b.lo);
 }
 
+// Split a pair of fp32 values into two packed bf16x2 words (hi, lo): the pair
+// is carried to about 2^-17 relative.
+__device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
+  hi = pack_bf16(hx, hy);
+  lo = pack_bf16(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
+}
+
+// Keys per block of the chunk attention (and per key range when every range
+// holds one block).
+constexpr int kAttnKB = 32;
+__host__ __device__ constexpr int attn_key_blocks(int T_kv) { return (T_kv + kAttnKB - 1) / kAttnKB; }
+
+// Eight warps per CTA: warp w takes query rows (w & 3) * 16 .. +15 of the CTA's
+// 64 and half (w >> 2) of the head dimension.  Scores are summed over the two
+// halves through shared memory, so both warps of a row tile hold the same S and
+// the same P; each accumulates the output columns of its half.
+//   S = (q_hi + q_lo) k              cached keys (bf16 values)
+//   S = (q_hi + q_lo) k_hi + q_hi k_lo   own keys (fp32 as computed, two planes)
+//   O += (p_hi + p_lo) v  /  (p_hi + p_lo) v_hi + p_hi v_lo
+// The dropped products (q_lo k_lo, p_lo v_lo) are below 2^-16 of the kept ones.
 template <int DH>
-static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
+static __global__ void __launch_bounds__(256) attention_kernel(AttnArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int KB = 64;          // keys per block
+  constexpr int KB = kAttnKB;
   constexpr int LD = DH + 8;      // padded smem row (bf16): conflict-free ldmatrix
-  constexpr int NT = DH / 8;      // output n-tiles
+  constexpr int HD = DH / 2;      // dims per warp
+  constexpr int KS = HD / 16;     // k-steps of S per warp
+  constexpr int NT = HD / 8;      // output n-tiles per warp
+  constexpr int SLD = KB + 2;     // partial-score row (fp32)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [2 planes][KB][LD]
   __nv_bfloat16* sV = sK + 2 * KB * LD;
-  float* sQ = reinterpret_cast<float*>(sV + 2 * KB * LD);            // [64 rows][DH + 4]
-  constexpr int QLD = DH + 4;
+  float* sS = reinterpret_cast<float*>(sV + 2 * KB * LD);            // [8 warps][16][SLD]
 
   const int h = blockIdx.x;
   const int qt = blockIdx.y;
   const int split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
+  const int rt = warp & 3, half = warp >> 2;
+  const int d0 = half * HD;
   const int kvh = h / (a.Hq / a.Hkv);
-  const int nkb = (a.T_kv + KB - 1) / KB;
+  const int nkb = attn_key_blocks(a.T_kv);
   const int kb0 = split * nkb / a.n_split, kb1 = (split + 1) * nkb / a.n_split;
 
-  const int r0 = qt * 64 + warp * 16 + g;   // this thread's two query rows: r0, r0 + 8
+  const int r0 = qt * 64 + rt * 16 + g;   // this thread's two query rows: r0, r0 + 8
   const int r1 = r0 + 8;
   const bool v0 = r0 < a.T_q, v1 = r1 < a.T_q;
-  // stage this CTA's 64 query rows of head h (zero rows past T_q)
-  for (int idx = threadIdx.x; idx < 64 * (DH / 4); idx += 128) {
-    const int row = idx / (DH / 4), c4 = idx % (DH / 4);
-    const int qr = qt * 64 + row;
-    cp_async16(sQ + row * QLD + c4 * 4, a.q + (size_t)(qr < a.T_q ? qr : 0) * a.q_ld + h * DH + c4 * 4,
-               qr < a.T_q ? 16 : 0);
+
+  // Q fragments of this warp's rows and dims, split once (rows past T_q are 0)
+  uint32_t qh[KS][4], ql[KS][4];
+  {
+    const float* q0 = a.q + (size_t)(v0 ? r0 : 0) * a.q_ld + h * DH + d0 + 2 * tq;
+    const float* q1 = a.q + (size_t)(v1 ? r1 : 0) * a.q_ld + h * DH + d0 + 2 * tq;
+    float2 x[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      x[ks][0] = v0 ? *reinterpret_cast<const float2*>(q0 + ks * 16) : make_float2(0.f, 0.f);
+      x[ks][1] = v1 ? *reinterpret_cast<const float2*>(q1 + ks * 16) : make_float2(0.f, 0.f);
+      x[ks][2] = v0 ? *reinterpret_cast<const float2*>(q0 + ks * 16 + 8) : make_float2(0.f, 0.f);
+      x[ks][3] = v1 ? *reinterpret_cast<const float2*>(q1 + ks * 16 + 8) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_pair2(x[ks][e].x, x[ks][e].y, qh[ks][e], ql[ks][e]);
   }
-  const float* q0 = sQ + (warp * 16 + g) * QLD;
-  const float* q1 = q0 + 8 * QLD;
 
   float o[NT][4];
 #pragma unroll
@@ -131,82 +166,98 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
 
   const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV);
   const uint32_t LO = (uint32_t)(KB * LD * 2);   // byte offset of the lo plane
+  float* myS = sS + warp * 16 * SLD;
+  const float* peerS = sS + (warp ^ 4) * 16 * SLD;
 
   for (int kb = kb0; kb < kb1; ++kb) {
     // ---- stage K and V blocks (zero-filled past T_kv); own keys as hi + lo ----
     const bool has_lo = a.k_own != nullptr && (kb + 1) * KB > a.own0 && a.own0 < a.T_kv;
     __syncthreads();
-    for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
+    for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 256) {
       const int row = idx / (DH / 8), c8 = idx % (DH / 8);
       const int key = kb * KB + row;
       const bool own = a.k_own != nullptr && key >= a.own0 && key < a.T_kv;
       if (!own) {   // cache keys (and zero fill past T_kv) by async copy
         const bool in = key < a.T_kv;
-        const size_t o = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
-        cp_async16(sK + row * LD + c8 * 8, a.k + o, in ? 16 : 0);
-        cp_async16(sV + row * LD + c8 * 8, a.v + o, in ? 16 : 0);
+        const size_t off = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
+        cp_async16(sK + row * LD + c8 * 8, a.k + off, in ? 16 : 0);
+        cp_async16(sV + row * LD + c8 * 8, a.v + off, in ? 16 : 0);
         if (has_lo) {
           *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
         }
       } else {      // own keys as computed: hi and lo planes
-        const size_t o = (size_t)(key - a.own0) * a.own_ld + kvh * DH + c8 * 8;
+        const size_t off = (size_t)(key - a.own0) * a.own_ld + kvh * DH + c8 * 8;
         uint4 kk, kl, vv, vl;
-        split8_to(a.k_own + o, kk, kl);
-        split8_to(a.v_own + o, vv, vl);
+        split8_to(a.k_own + off, kk, kl);
+        split8_to(a.v_own + off, vv, vl);
         *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
-        *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
         *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
+        *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
         *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
       }
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- S = Q K^T for 16 rows x 64 keys (8 n-tiles) ----
-    float s[8][4];
+    // ---- partial S over this warp's dims: 16 rows x 32 keys (4 n-tiles) ----
+    float sa[4][4], sb[4][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll 2
-    for (int ks = 0; ks < DH / 16; ++ks) {
-      const int c = ks * 16 + 2 * tq;
-      const float2 x00 = *reinterpret_cast<const float2*>(q0 + c);
-      const float2 x10 = *reinterpret_cast<const float2*>(q1 + c);
-      const float2 x01 = *reinterpret_cast<const float2*>(q0 + c + 8);
-      const float2 x11 = *reinterpret_cast<const float2*>(q1 + c + 8);
-      uint32_t ah[4], am[4], al[4];
-      split_pair(x00.x, x00.y, ah[0], am[0], al[0]);
-      split_pair(x10.x, x10.y, ah[1], am[1], al[1]);
-      split_pair(x01.x, x01.y, ah[2], am[2], al[2]);
-      split_pair(x11.x, x11.y, ah[3], am[3], al[3]);
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        // matrices: keys jp*16 + (0..7 | 8..15), d ks*16 + (0..7 | 8..15)
-        const int mi = lane >> 3, rr = lane & 7;
+      for (int e = 0; e < 4; ++e) sa[j][e] = sb[j][e] = 0.f;
+    const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b[4][2];
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {
         const int key = jp * 16 + ((mi >> 1) << 3) + rr;
-        const int col = ks * 16 + ((mi & 1) << 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-        mma_16816(s[2 * jp], ah, b0, b1);
-        mma_16816(s[2 * jp], am, b0, b1);
-        mma_16816(s[2 * jp], al, b0, b1);
-        mma_16816(s[2 * jp + 1], ah, b2, b3);
-        mma_16816(s[2 * jp + 1], am, b2, b3);
-        mma_16816(s[2 * jp + 1], al, b2, b3);
-        if (has_lo) {
-          ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-          mma_16816(s[2 * jp], ah, b0, b1);
-          mma_16816(s[2 * jp], am, b0, b1);
-          mma_16816(s[2 * jp + 1], ah, b2, b3);
-          mma_16816(s[2 * jp + 1], am, b2, b3);
-        }
+        const int col = d0 + ks * 16 + ((mi & 1) << 3);
+        ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                b[2 * jp + 1][1]);
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_16816(sa[j], qh[ks], b[j][0], b[j][1]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_16816(sb[j], ql[ks], b[j][0], b[j][1]);
+      if (has_lo) {
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          const int key = jp * 16 + ((mi >> 1) << 3) + rr;
+          const int col = d0 + ks * 16 + ((mi & 1) << 3);
+          ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                  b[2 * jp + 1][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_16816(sb[j], qh[ks], b[j][0], b[j][1]);
+      }
+    }
+    // ---- exchange partial scores with the warp of the other half ----
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = j * 8 + 2 * tq;
+      *reinterpret_cast<float2*>(myS + g * SLD + c) = make_float2(sa[j][0] + sb[j][0], sa[j][1] + sb[j][1]);
+      *reinterpret_cast<float2*>(myS + (g + 8) * SLD + c) = make_float2(sa[j][2] + sb[j][2], sa[j][3] + sb[j][3]);
+    }
+    __syncthreads();
+    float s[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = j * 8 + 2 * tq;
+      const float2 p0 = *reinterpret_cast<const float2*>(peerS + g * SLD + c);
+      const float2 p1 = *reinterpret_cast<const float2*>(peerS + (g + 8) * SLD + c);
+      // a + b == b + a: both warps of the pair get bit-identical scores
+      s[j][0] = (sa[j][0] + sb[j][0]) + p0.x;
+      s[j][1] = (sa[j][1] + sb[j][1]) + p0.y;
+      s[j][2] = (sa[j][2] + sb[j][2]) + p1.x;
+      s[j][3] = (sa[j][3] + sb[j][3]) + p1.y;
     }
 
     // ---- online softmax (base 2) ----
     float mx0 = m0, mx1 = m1;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       const int key = kb * KB + j * 8 + 2 * tq;
       s[j][0] = (key < a.T_kv) ? s[j][0] * a.scale_log2 : -INFINITY;
       s[j][1] = (key + 1 < a.T_kv) ? s[j][1] * a.scale_log2 : -INFINITY;
@@ -224,7 +275,7 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
     m1 = mx1;
     float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       s[j][0] = exp2f(s[j][0] - mx0);
       s[j][1] = exp2f(s[j][1] - mx0);
       s[j][2] = exp2f(s[j][2] - mx1);
@@ -246,34 +297,35 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
       o[j][3] *= al1;
     }
 
-    // ---- O += P V ----
+    // ---- O += P V over this warp's output columns ----
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t ph[4], pm[4], pl[4];
-      split_pair(s[2 * kk][0], s[2 * kk][1], ph[0], pm[0], pl[0]);
-      split_pair(s[2 * kk][2], s[2 * kk][3], ph[1], pm[1], pl[1]);
-      split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pm[2], pl[2]);
-      split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pm[3], pl[3]);
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t ph[4], pl[4];
+      split_pair2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+      split_pair2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+      split_pair2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+      split_pair2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+      const int key = kk * 16 + ((mi & 1) << 3) + rr;
+      uint32_t b[NT][2];
 #pragma unroll
       for (int jp = 0; jp < NT / 2; ++jp) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int key = kk * 16 + ((mi & 1) << 3) + rr;
-        const int col = jp * 16 + ((mi >> 1) << 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-        mma_16816(o[2 * jp], ph, b0, b1);
-        mma_16816(o[2 * jp], pm, b0, b1);
-        mma_16816(o[2 * jp], pl, b0, b1);
-        mma_16816(o[2 * jp + 1], ph, b2, b3);
-        mma_16816(o[2 * jp + 1], pm, b2, b3);
-        mma_16816(o[2 * jp + 1], pl, b2, b3);
-        if (has_lo) {
-          ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-          mma_16816(o[2 * jp], ph, b0, b1);
-          mma_16816(o[2 * jp], pm, b0, b1);
-          mma_16816(o[2 * jp + 1], ph, b2, b3);
-          mma_16816(o[2 * jp + 1], pm, b2, b3);
+        const int col = d0 + jp * 16 + ((mi >> 1) << 3);
+        ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                  b[2 * jp + 1][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_16816(o[j], ph, b[j][0], b[j][1]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_16816(o[j], pl, b[j][0], b[j][1]);
+      if (has_lo) {
+#pragma unroll
+        for (int jp = 0; jp < NT / 2; ++jp) {
+          const int col = d0 + jp * 16 + ((mi >> 1) << 3);
+          ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                    b[2 * jp + 1][1]);
         }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_16816(o[j], ph, b[j][0], b[j][1]);
       }
     }
   }
@@ -283,19 +335,19 @@ static __global__ void __launch_bounds__(128) attention_kernel(AttnArgs a) {
     const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f, i1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const int c = h * DH + j * 8 + 2 * tq;
+      const int c = h * DH + d0 + j * 8 + 2 * tq;
       if (v0) *reinterpret_cast<float2*>(a.out + (size_t)r0 * a.out_ld + c) = make_float2(o[j][0] * i0, o[j][1] * i0);
       if (v1) *reinterpret_cast<float2*>(a.out + (size_t)r1 * a.out_ld + c) = make_float2(o[j][2] * i1, o[j][3] * i1);
     }
   } else {
     const size_t base = ((size_t)split * a.Hq + h) * a.T_q;
-    if (tq == 0) {
+    if (tq == 0 && half == 0) {
       if (v0) { a.part_m[base + r0] = m0; a.part_l[base + r0] = l0; }
       if (v1) { a.part_m[base + r1] = m1; a.part_l[base + r1] = l1; }
     }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const int c = j * 8 + 2 * tq;
+      const int c = d0 + j * 8 + 2 * tq;
       if (v0) *reinterpret_cast<float2*>(a.part_o + (base + r0) * DH + c) = make_float2(o[j][0], o[j][1]);
       if (v1) *reinterpret_cast<float2*>(a.part_o + (base + r1) * DH + c) = make_float2(o[j][2], o[j][3]);
     }
@@ -575,22 +627,24 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
 // K and V tiles, two planes each, rows padded to dh + 8; plus the fp32 Q tile
 // of the chunk kernel (rows padded to dh + 4)
 static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2 + 64 * (dh + 4) * 4; }
+// chunk attention: K and V blocks in two planes each, plus the partial scores
+static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
 static inline cudaError_t set_attention_smem_limits() {
   cudaFuncSetAttribute(attention_seg_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
   cudaFuncSetAttribute(attention_seg_kernel<256, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
-  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(64));
-  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
-  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
+  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(64));
+  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(128));
+  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(256));
   return cudaGetLastError();
 }
 
 static inline cudaError_t launch_chunk_attention(const AttnArgs& a, int dh, cudaStream_t st) {
   dim3 grid(a.Hq, (a.T_q + 63) / 64, a.n_split);
-  const int smem = attn_smem_bytes(dh);
-  if (dh == 64) attention_kernel<64><<<grid, 128, smem, st>>>(a);
-  else if (dh == 128) attention_kernel<128><<<grid, 128, smem, st>>>(a);
-  else attention_kernel<256><<<grid, 128, smem, st>>>(a);
+  const int smem = chunk_attn_smem_bytes(dh);
+  if (dh == 64) attention_kernel<64><<<grid, 256, smem, st>>>(a);
+  else if (dh == 128) attention_kernel<128><<<grid, 256, smem, st>>>(a);
+  else attention_kernel<256><<<grid, 256, smem, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_split == 1) return e;
   attention_combine_kernel<<<dim3(a.T_q, a.Hq), dh, 0, st>>>(a, dh, nullptr);

@@ -428,7 +428,7 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   // --- workspace ---
   const int T = d.T_q;
   const int T_kv = d.T_prefix + d.T_q;
-  const int nkb = (T_kv + 63) / 64;
+  const int nkb = attn_key_blocks(T_kv);
   c->attn_split = nkb < kMaxKeySplits ? nkb : kMaxKeySplits;
   LAT_TRY(c->alloc(&c->xres, (size_t)T * D));
   LAT_TRY(c->alloc(&c->qkv_acc, (size_t)T * c->nqkv));
@@ -518,10 +518,10 @@ static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_lay
     a.k_own = c->kown; a.v_own = c->vown; a.own0 = d.T_prefix; a.own_ld = kvd;
     a.force_partials = 1;
     const dim3 grid(d.Hq, (T + 63) / 64, a.n_split);
-    const size_t smem = attn_smem_bytes(d.dh);
-    if (d.dh == 64) PDL_TRY("attention", launch_pdl(attention_kernel<64>, grid, dim3(128), smem, st, a));
-    else if (d.dh == 128) PDL_TRY("attention", launch_pdl(attention_kernel<128>, grid, dim3(128), smem, st, a));
-    else PDL_TRY("attention", launch_pdl(attention_kernel<256>, grid, dim3(128), smem, st, a));
+    const size_t smem = chunk_attn_smem_bytes(d.dh);
+    if (d.dh == 64) PDL_TRY("attention", launch_pdl(attention_kernel<64>, grid, dim3(256), smem, st, a));
+    else if (d.dh == 128) PDL_TRY("attention", launch_pdl(attention_kernel<128>, grid, dim3(256), smem, st, a));
+    else PDL_TRY("attention", launch_pdl(attention_kernel<256>, grid, dim3(256), smem, st, a));
     PDL_TRY("attention_combine", launch_pdl(attention_combine_kernel, dim3(T, d.Hq), dim3(d.dh), 0, st, a, d.dh,
                                             c->planes_o));
   }
@@ -1136,7 +1136,7 @@ lat_status lat_debug_attention(lat_ctx* c, const float* q, const void* k, const 
     return fail(LAT_ERR_SHAPE, "T_q / T_kv out of the context's range");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
-  const int nkb = (T_kv + 63) / 64;
+  const int nkb = attn_key_blocks(T_kv);
   const int n_split = nkb < kMaxKeySplits ? nkb : kMaxKeySplits;
   return enqueue_attention(d, q, d.Hq * d.dh, reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v),
                            d.Hkv * d.dh, T_q, T_kv, n_split, out, d.Hq * d.dh, c->pm, c->pl, c->po,

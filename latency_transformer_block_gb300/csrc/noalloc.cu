@@ -75,7 +75,7 @@ extern "C" lat_status lat_chunk_attention_noalloc(const float* q, const void* k,
   lat_status s = setup_device(dev, &scratch);
   if (s != LAT_OK) return s;
 
-  const int nkb = (T_kv + 63) / 64;
+  const int nkb = lat::attn_key_blocks(T_kv);
   int n_split = (int)(kNoAllocScratchFloats / per_split);
   if (n_split > nkb) n_split = nkb;
   if (n_split > 32) n_split = 32;   // partials the combine kernel merges
