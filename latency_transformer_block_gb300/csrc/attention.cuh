@@ -362,28 +362,34 @@ static __global__ void attention_combine_kernel(AttnArgs a, int dh, __nv_bfloat1
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   constexpr int MAXS = 32;
-  float mv[MAXS], lv[MAXS], ov[MAXS];
-  float M = -INFINITY;
+  __shared__ float sw[MAXS];
+  __shared__ float sL;
+  // every partial's output value is requested before any is used
+  float ov[MAXS];
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
-    if (s < a.n_split) {
-      const size_t i = ((size_t)s * a.Hq + h) * a.T_q + t;
-      mv[s] = a.part_m[i];
-      lv[s] = a.part_l[i];
-      ov[s] = a.part_o[i * dh + d];
-      M = fmaxf(M, mv[s]);
-    }
+    const int sc = s < a.n_split ? s : 0;
+    ov[s] = __ldcg(a.part_o + (((size_t)sc * a.Hq + h) * a.T_q + t) * dh + d);
   }
-  float L = 0.f, acc = 0.f;
+  if (d < 32) {   // weights 2^(m_s - M) of the key ranges, and L
+    const bool in = d < a.n_split;
+    const size_t i = ((size_t)(in ? d : 0) * a.Hq + h) * a.T_q + t;
+    const float mv = in ? __ldcg(a.part_m + i) : -INFINITY;
+    const float lv = in ? __ldcg(a.part_l + i) : 0.f;
+    float M = mv;
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (mv == -INFINITY) ? 0.f : exp2f(mv - M);
+    float L = w * lv;
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    sw[d] = w;
+    if (d == 0) sL = L;
+  }
+  __syncthreads();
+  float acc = 0.f;
 #pragma unroll
-  for (int s = 0; s < MAXS; ++s) {
-    if (s < a.n_split) {
-      const float w = (mv[s] == -INFINITY) ? 0.f : exp2f(mv[s] - M);
-      L += w * lv[s];
-      acc += w * ov[s];
-    }
-  }
-  const float o = acc / L;
+  for (int s = 0; s < MAXS; ++s)
+    if (s < a.n_split) acc += sw[s] * ov[s];
+  const float o = acc / sL;
   if (planes) {
     const int K = a.Hq * dh, c = h * dh + d;
     const Split3 s3 = split3(o);

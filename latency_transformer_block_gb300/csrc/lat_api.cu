@@ -505,7 +505,8 @@ static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_lay
   {
     QkvEpiArgs a{c->qkv_acc, c->nqkv, c->r1, c->cos_t, c->sin_t, c->q, kc, vc, kvd, d.T_prefix,
                  d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F, c->kown, c->vown};
-    PDL_TRY("qkv_epilogue", launch_pdl(qkv_epilogue_kernel, dim3(T), dim3(256), 0, st, a));
+    PDL_TRY("qkv_epilogue", launch_pdl(qkv_epilogue_kernel, dim3(T, (qkv_epi_items(d.Hq, d.Hkv, d.dh) + 127) / 128),
+                                          dim3(128), 0, st, a));
   }
   // 3. attention over [prefix | own] (key ranges) + combine into the O planes
   {
