@@ -219,6 +219,20 @@ lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *st
 lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 
 /*
+ * lat_debug_trace -- measurement hook for the action expert's persistent step
+ * kernel: with buf != NULL (device, caller-owned, 8-byte aligned, at least
+ * num_SMs * L * 64 entries) later launches record %globaltimer nanoseconds at
+ * the phase boundaries of every block, buf[(layer * grid + cta) * 64 + event]
+ * (events 0..12: block start, after each phase and each grid barrier;
+ * 16 + 4 g .. 19 + 4 g for projection g: first activation tile in, operand
+ * built, accumulator ready, epilogue issued).  Each launch overwrites the
+ * entries of its layers.  buf = NULL turns recording off.  Drops the captured
+ * denoise graph (the next lat_denoise_chunk re-captures).  LAT_ERR_SHAPE if the
+ * buffer is too small.
+ */
+lat_status lat_debug_trace(lat_ctx *ctx, unsigned long long *buf, long long n);
+
+/*
  * lat_debug_dense_gemm -- one dense projection of a LAT_PI0_PREFIX or LAT_DIT
  * context alone (kernel-level parity and timing):
  *   out[m][n] = sum_t sum_k act[m][t*K + k] * W[n][k]

@@ -38,18 +38,15 @@ struct AttnArgs {
 };
 
 // 8 fp32 values -> 8 bf16 hi and 8 bf16 lo (two-term split)
+__device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo);
 __device__ __forceinline__ void split8_to(const float* src, uint4& hi, uint4& lo) {
   const float4 a = *reinterpret_cast<const float4*>(src);
   const float4 b = *reinterpret_cast<const float4*>(src + 4);
-  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t h[4], l[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-    h[e] = pack_bf16(h0, h1);
-    l[e] = pack_bf16(__float2bfloat16_rn(v[2 * e] - __bfloat162float(h0)),
-                     __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1)));
-  }
+  split_pair2(a.x, a.y, h[0], l[0]);
+  split_pair2(a.z, a.w, h[1], l[1]);
+  split_pair2(b.x, b.y, h[2], l[2]);
+  split_pair2(b.z, b.w, h[3], l[3]);
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -81,20 +78,45 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Split a pair of fp32 values into three packed bf16x2 words.
+// Round a pair of fp32 values to bf16 (nearest even) in one packed conversion.
+__device__ __forceinline__ uint32_t rn_pair(float x, float y, float& bx, float& by) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 f = __bfloat1622float2(h);
+  bx = f.x;
+  by = f.y;
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Split a pair of fp32 values into three packed bf16x2 words (each term the
+// nearest bf16 of what is left).
 __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-  Split3 a = split3(x), b = split3(y);
-  hi = pack_bf16(a.hi, b.hi);
-  mid = pack_bf16(a.mid, b.mid);
-  lo = pack_bf16(a.lo, b.lo);
+  float hx, hy, mx, my, lx, ly;
+  hi = rn_pair(x, y, hx, hy);
+  const float rx = x - hx, ry = y - hy;
+  mid = rn_pair(rx, ry, mx, my);
+  lo = rn_pair(rx - mx, ry - my, lx, ly);
 }
 
 // Split a pair of fp32 values into two packed bf16x2 words (hi, lo): the pair
 // is carried to about 2^-17 relative.
 __device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
-  hi = pack_bf16(hx, hy);
-  lo = pack_bf16(__float2bfloat16_rn(x - __bfloat162float(hx)), __float2bfloat16_rn(y - __bfloat162float(hy)));
+  float hx, hy, lx, ly;
+  hi = rn_pair(x, y, hx, hy);
+  lo = rn_pair(x - hx, y - hy, lx, ly);
+}
+
+// Exact three-term split of a pair of fp32 values by truncation: hi keeps the
+// top 8 significant bits of x, mid the top 8 of what is left, and the rest
+// (at most 8 significant bits) is lo, so x = hi + mid + lo exactly and no
+// conversion instruction is needed (bf16 is the upper half of fp32).
+__device__ __forceinline__ void split_pair_exact(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const uint32_t hx = __float_as_uint(x) & 0xffff0000u, hy = __float_as_uint(y) & 0xffff0000u;
+  const float rx = x - __uint_as_float(hx), ry = y - __uint_as_float(hy);
+  const uint32_t mx = __float_as_uint(rx) & 0xffff0000u, my = __float_as_uint(ry) & 0xffff0000u;
+  const float qx = rx - __uint_as_float(mx), qy = ry - __uint_as_float(my);
+  hi = __byte_perm(hx, hy, 0x7632);
+  mid = __byte_perm(mx, my, 0x7632);
+  lo = __byte_perm(__float_as_uint(qx), __float_as_uint(qy), 0x7632);
 }
 
 // Keys per block of the chunk attention (and per key range when every range

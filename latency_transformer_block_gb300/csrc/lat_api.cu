@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "dense_gemm.cuh"
 #include "dense_kernels.cuh"
+#include "pi0_step.cuh"
 #include "skinny_gemm.cuh"
 #include "small_kernels.cuh"
 
@@ -97,6 +98,21 @@ static lat_status make_kmajor_map(CUtensorMap* map, const void* base, int rows, 
   return LAT_OK;
 }
 
+// fp32 row-major activation [rows][cols] -> tiles of 64 rows x 64 columns, no swizzle.
+static lat_status make_f32_map(CUtensorMap* map, const void* base, int rows, int cols) {
+  EncodeTiledFn enc;
+  LAT_TRY(get_encode(&enc));
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LAT_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
+  return LAT_OK;
+}
+
 // ---------------------------------------------------------------------------
 // context
 // ---------------------------------------------------------------------------
@@ -131,6 +147,12 @@ struct lat_ctx {
         *temb = nullptr;
   int attn_split = 1;
   DevErr* err = nullptr;
+
+  // persistent step kernel: arguments, fp32 activation maps, zero-at-entry block
+  MkArgs mk{};
+  CUtensorMap amap_x;
+  void* mk_zero = nullptr;
+  size_t mk_zero_bytes = 0;
 
   // dense path (prefix prefill, DiT)
   bf16 *wup = nullptr, *wdown = nullptr, *wpatch = nullptr;
@@ -223,13 +245,6 @@ static lat_status enqueue_skinny(const lat_ctx* c, const CUtensorMap& map, const
   const int grid = (g.N_out / 128) * g.splits;
   PDL_TRY("skinny_gemm", launch_pdl(skinny_gemm_kernel<kStages>, dim3(grid), dim3(192),
                                     (size_t)skinny_smem_bytes(kStages), st, map, bmap, a));
-  return LAT_OK;
-}
-
-static lat_status enqueue_prep(const float* src, int ld, int K, int n_tok, int mode, int off, const float* row_scale,
-                               bf16* planes, float* stat_out, float eps, cudaStream_t st) {
-  PrepArgs a{src, ld, K, mode, off, row_scale, planes, stat_out, eps};
-  PDL_TRY("prep_planes", launch_pdl(prep_planes_kernel, dim3((K + 255) / 256, n_tok), dim3(256), 0, st, a));
   return LAT_OK;
 }
 
@@ -424,19 +439,38 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(c->alloc(&c->sin_t, stt.size()));
   CUDA_TRY(cudaMemcpy(c->cos_t, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice));
   CUDA_TRY(cudaMemcpy(c->sin_t, stt.data(), stt.size() * 4, cudaMemcpyHostToDevice));
+  // the same angles in the step kernel's q-fragment order: [warp][dh / 64][4][lane]
+  // x {cos i, cos i+1, sin i, sin i+1}, warp = row tile (w & 3) x dim half (w >> 2)
+  {
+    const int ksh = d.dh / 64, q4 = d.dh / 4;
+    std::vector<float> rf((size_t)8 * ksh * 4 * 32 * 4, 0.f);
+    for (int w = 0; w < 8; ++w)
+      for (int ks = 0; ks < ksh; ++ks)
+        for (int e = 0; e < 4; ++e)
+          for (int ln = 0; ln < 32; ++ln) {
+            const int row = (w & 3) * 16 + (ln >> 2) + (e & 1) * 8;
+            const int i = (w >> 2) * q4 + ks * 16 + 2 * (ln & 3) + (e >> 1) * 8;
+            if (row >= d.T_q) continue;
+            float* o = &rf[((((size_t)w * ksh + ks) * 4 + e) * 32 + ln) * 4];
+            o[0] = ct[(size_t)row * half + i];
+            o[1] = ct[(size_t)row * half + i + 1];
+            o[2] = stt[(size_t)row * half + i];
+            o[3] = stt[(size_t)row * half + i + 1];
+          }
+    float* dev = nullptr;
+    LAT_TRY(c->alloc(&dev, rf.size()));
+    CUDA_TRY(cudaMemcpy(dev, rf.data(), rf.size() * 4, cudaMemcpyHostToDevice));
+    c->mk.rope_frag = reinterpret_cast<const float4*>(dev);
+  }
 
   // --- workspace ---
   const int T = d.T_q;
   const int T_kv = d.T_prefix + d.T_q;
   const int nkb = attn_key_blocks(T_kv);
   c->attn_split = nkb < kMaxKeySplits ? nkb : kMaxKeySplits;
-  LAT_TRY(c->alloc(&c->xres, (size_t)T * D));
+  LAT_TRY(c->alloc(&c->xres, (size_t)64 * D));   // 64 rows: the step kernel reads 64 x 64 tiles
   LAT_TRY(c->alloc(&c->qkv_acc, (size_t)T * c->nqkv));
   LAT_TRY(c->alloc(&c->gu_acc, (size_t)T * 2 * F));
-  LAT_TRY(c->alloc(&c->q, (size_t)T * qd));
-  LAT_TRY(c->alloc(&c->o, (size_t)T * qd));
-  LAT_TRY(c->alloc(&c->r1, (size_t)T));
-  LAT_TRY(c->alloc(&c->r2, (size_t)T));
   LAT_TRY(c->alloc(&c->z, (size_t)T * D));
   LAT_TRY(c->alloc(&c->pm, (size_t)c->attn_split * d.Hq * T));
   LAT_TRY(c->alloc(&c->pl, (size_t)c->attn_split * d.Hq * T));
@@ -451,12 +485,70 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(make_planes_map(&c->bmap_x, c->planes_x, D));
   LAT_TRY(make_planes_map(&c->bmap_o, c->planes_o, qd));
   LAT_TRY(make_planes_map(&c->bmap_h, c->planes_h, F));
-  LAT_TRY(c->alloc(&c->kown, (size_t)T * d.Hkv * d.dh));
-  LAT_TRY(c->alloc(&c->vown, (size_t)T * d.Hkv * d.dh));
   LAT_TRY(c->alloc(&c->err, 1));
   CUDA_TRY(cudaMemset(c->qkv_acc, 0, (size_t)T * c->nqkv * 4));
   CUDA_TRY(cudaMemset(c->gu_acc, 0, (size_t)T * 2 * F * 4));
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
+  CUDA_TRY(cudaMemset(c->xres, 0, (size_t)64 * D * 4));
+
+  // --- persistent step kernel: [barrier counter | sums of squares | gate/up sums],
+  //     cleared before every launch; key-block partials; maps; plans ---
+  {
+    const size_t bar_b = 256, ss_b = (size_t)L * 128 * 4;
+    c->mk_zero_bytes = bar_b + ss_b;
+    uint8_t* z = nullptr;
+    LAT_TRY(c->alloc(&z, c->mk_zero_bytes));
+    CUDA_TRY(cudaMemset(z, 0, c->mk_zero_bytes));
+    c->mk_zero = z;
+    MkArgs& m = c->mk;
+    m.bar = reinterpret_cast<unsigned*>(z);
+    m.ss = reinterpret_cast<float*>(z + bar_b);
+    float* gu = nullptr;   // one slab of gate/up partial sums per K range
+    LAT_TRY(c->alloc(&gu, (size_t)c->g_gu.splits * 64 * 2 * F));
+    m.gu = gu;
+    float* qp = nullptr;   // one slab of QKV partial sums per K range
+    LAT_TRY(c->alloc(&qp, (size_t)c->g_qkv.splits * 64 * c->nqkv));
+    bf16 *qpl = nullptr, *kvo = nullptr;
+    LAT_TRY(c->alloc(&qpl, (size_t)2 * 64 * qd));
+    LAT_TRY(c->alloc(&kvo, (size_t)4 * 64 * kvd));
+    CUDA_TRY(cudaMemset(qpl, 0, (size_t)2 * 64 * qd * 2));
+    CUDA_TRY(cudaMemset(kvo, 0, (size_t)4 * 64 * kvd * 2));
+    m.q_planes = qpl;
+    m.kv_own = kvo;
+    float *pm = nullptr, *pl = nullptr, *po = nullptr;
+    LAT_TRY(c->alloc(&pm, (size_t)nkb * d.Hq * T));
+    LAT_TRY(c->alloc(&pl, (size_t)nkb * d.Hq * T));
+    LAT_TRY(c->alloc(&po, (size_t)nkb * d.Hq * 64 * d.dh));   // fragment order covers 64 rows
+    m.part_m = pm;
+    m.part_l = pl;
+    m.part_o = po;
+    m.x = c->xres;
+    m.qkv = qp;
+    m.o_planes = c->planes_o;
+    m.h_planes = c->planes_h;
+    m.cos_t = c->cos_t;
+    m.sin_t = c->sin_t;
+    m.err = c->err;
+    m.D = D;
+    m.F = F;
+    m.Hq = d.Hq;
+    m.Hkv = d.Hkv;
+    m.T_q = T;
+    m.T_prefix = d.T_prefix;
+    m.T_kv = T_kv;
+    m.nqkv = c->nqkv;
+    m.eps = d.eps;
+    m.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
+    const GemmPlan* gp[4] = {&c->g_qkv, &c->g_o, &c->g_gu, &c->g_d};
+    for (int i = 0; i < 4; ++i) {
+      m.g[i].MT = gp[i]->N_out / 128;
+      m.g[i].KT = gp[i]->K / 64;
+      m.g[i].splits = gp[i]->splits;
+      m.g[i].N = gp[i]->N_out;
+      if (m.g[i].MT * m.g[i].splits > c->num_sms) return fail(LAT_ERR_SHAPE, "projection plan exceeds the grid");
+    }
+    LAT_TRY(make_f32_map(&c->amap_x, c->xres, 64, D));
+  }
 
   std::vector<double> t(d.S + 1);
   for (int s = 0; s <= d.S; ++s) t[s] = (double)s / d.S;
@@ -485,67 +577,37 @@ static lat_status enqueue_attention(const lat_model_desc& d, const float* q, int
 }
 
 // ---------------------------------------------------------------------------
-// one pi0 block on the residual stream xres [T_q][D]; kv_layer = [2][T_kv][kvd]
+// layers [l0, l1) of one denoise step on ctx->xres, one persistent launch
+// (cooperative: every CTA is resident, which the grid barriers need)
 // ---------------------------------------------------------------------------
-static lat_status enqueue_pi0_block(lat_ctx* c, int l, float* xres, bf16* kv_layer, cudaStream_t st) {
-  const lat_model_desc& d = c->d;
-  const int T = d.T_q, D = d.D, F = d.F;
-  const int qd = d.Hq * d.dh, kvd = d.Hkv * d.dh;
-  const int T_kv = d.T_prefix + d.T_q;
-  bf16* kc = kv_layer;
-  bf16* vc = kv_layer + (size_t)T_kv * kvd;
-  // 1. planes of x + RMS factor r1; merged QKV projection
-  LAT_TRY(enqueue_prep(xres, D, D, T, PREP_PLAIN, 0, nullptr, c->planes_x, c->r1, d.eps, st));
-  {
-    SkinnyArgs a{};
-    a.n_tok = T; a.out = c->qkv_acc; a.out_ld = c->nqkv;
-    LAT_TRY(enqueue_skinny(c, c->map_qkv, c->bmap_x, c->g_qkv, l, a, st));
-  }
-  // 2. row scale + RoPE + K/V into the cache + q; clears qkv_acc and gu_acc
-  {
-    QkvEpiArgs a{c->qkv_acc, c->nqkv, c->r1, c->cos_t, c->sin_t, c->q, kc, vc, kvd, d.T_prefix,
-                 d.Hq, d.Hkv, d.dh, c->gu_acc, 2 * F, c->kown, c->vown};
-    PDL_TRY("qkv_epilogue", launch_pdl(qkv_epilogue_kernel, dim3(T, (qkv_epi_items(d.Hq, d.Hkv, d.dh) + 127) / 128),
-                                          dim3(128), 0, st, a));
-  }
-  // 3. attention over [prefix | own] (key ranges) + combine into the O planes
-  {
-    AttnArgs a{};
-    a.q = c->q; a.q_ld = qd; a.k = kc; a.v = vc; a.kv_ld = kvd;
-    a.T_q = T; a.T_kv = T_kv; a.Hq = d.Hq; a.Hkv = d.Hkv;
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
-    a.n_split = c->attn_split;
-    a.out = c->o; a.out_ld = qd; a.part_m = c->pm; a.part_l = c->pl; a.part_o = c->po;
-    a.k_own = c->kown; a.v_own = c->vown; a.own0 = d.T_prefix; a.own_ld = kvd;
-    a.force_partials = 1;
-    const dim3 grid(d.Hq, (T + 63) / 64, a.n_split);
-    const size_t smem = chunk_attn_smem_bytes(d.dh);
-    if (d.dh == 64) PDL_TRY("attention", launch_pdl(attention_kernel<64>, grid, dim3(256), smem, st, a));
-    else if (d.dh == 128) PDL_TRY("attention", launch_pdl(attention_kernel<128>, grid, dim3(256), smem, st, a));
-    else PDL_TRY("attention", launch_pdl(attention_kernel<256>, grid, dim3(256), smem, st, a));
-    PDL_TRY("attention_combine", launch_pdl(attention_combine_kernel, dim3(T, d.Hq), dim3(d.dh), 0, st, a, d.dh,
-                                            c->planes_o));
-  }
-  // 4. x += o Wo
-  {
-    SkinnyArgs a{};
-    a.n_tok = T; a.out = xres; a.out_ld = D;
-    LAT_TRY(enqueue_skinny(c, c->map_o, c->bmap_o, c->g_o, l, a, st));
-  }
-  // 5. planes of x + RMS factor r2; gate/up projection
-  LAT_TRY(enqueue_prep(xres, D, D, T, PREP_PLAIN, 0, nullptr, c->planes_x, c->r2, d.eps, st));
-  {
-    SkinnyArgs a{};
-    a.n_tok = T; a.out = c->gu_acc; a.out_ld = 2 * F;
-    LAT_TRY(enqueue_skinny(c, c->map_gu, c->bmap_x, c->g_gu, l, a, st));
-  }
-  // 6. planes of GELU(r2 g) * (r2 u); x += h Wd
-  LAT_TRY(enqueue_prep(c->gu_acc, 2 * F, F, T, PREP_GEGLU, F, c->r2, c->planes_h, nullptr, d.eps, st));
-  {
-    SkinnyArgs a{};
-    a.n_tok = T; a.out = xres; a.out_ld = D;
-    LAT_TRY(enqueue_skinny(c, c->map_d, c->bmap_h, c->g_d, l, a, st));
-  }
+static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long long kv_stride, cudaStream_t st) {
+  CUDA_TRY(cudaMemsetAsync(c->mk_zero, 0, c->mk_zero_bytes, st));
+  MkArgs a = c->mk;
+  a.l0 = l0;
+  a.l1 = l1;
+  a.kv = kv;
+  a.kv_stride = kv_stride;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c->num_sms);
+  cfg.blockDim = dim3(kMkThreads);
+  cfg.dynamicSmemBytes = mk_smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (c->d.dh == 64)
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+                           c->bmap_o, c->bmap_h, a);
+  else if (c->d.dh == 128)
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<128>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+                           c->bmap_o, c->bmap_h, a);
+  else
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<256>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+                           c->bmap_o, c->bmap_h, a);
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch pi0_step: %s", cudaGetErrorString(e));
   return LAT_OK;
 }
 
@@ -564,7 +626,7 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
       a.n_tok = T - 1; a.out = c->xres + D; a.out_ld = D;
       LAT_TRY(enqueue_skinny(c, c->map_w2, c->bmap_x, c->g_w2, 0, a, st));
     }
-    for (int l = 0; l < d.L; ++l) LAT_TRY(enqueue_pi0_block(c, l, c->xres, kv + (size_t)l * layer_elems, st));
+    LAT_TRY(enqueue_pi0_step(c, 0, d.L, kv, (long long)layer_elems, st));
     HeadArgs h{c->xres, c->wout, c->bout, x, c->dt, s, D, A, d.eps};
     PDL_TRY("head_euler", launch_pdl(head_euler_kernel, dim3(T - 1), dim3(256), 0, st, h));
   }
@@ -960,6 +1022,9 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     set_attention_smem_limits();
     cudaFuncSetAttribute(dense_gemm_kernel<kDStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          dense_smem_bytes(kDStages));
+    cudaFuncSetAttribute(pi0_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
+    cudaFuncSetAttribute(pi0_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
+    cudaFuncSetAttribute(pi0_step_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       delete c;
@@ -1016,7 +1081,12 @@ lat_status lat_block_forward(lat_ctx* c, int layer, float* x, const lat_chunk_de
   if (!aligned16(x) || !aligned16(kv)) return fail(LAT_ERR_ALIGN, "x / kv not 16-byte aligned");
   if (c->d.kind == LAT_PI0_ACTION_EXPERT) {
     if (chunks != nullptr || n != 1) return fail(LAT_ERR_ARG, "pi0 block: chunks must be NULL and n == 1");
-    return enqueue_pi0_block(c, layer, x, reinterpret_cast<bf16*>(kv), reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t xb = (size_t)c->d.T_q * c->d.D * 4;
+    CUDA_TRY(cudaMemcpyAsync(c->xres, x, xb, cudaMemcpyDeviceToDevice, st));
+    LAT_TRY(enqueue_pi0_step(c, layer, layer + 1, reinterpret_cast<bf16*>(kv), 0, st));
+    CUDA_TRY(cudaMemcpyAsync(x, c->xres, xb, cudaMemcpyDeviceToDevice, st));
+    return LAT_OK;
   }
   if (c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "lat_block_forward: the prefix model runs via lat_prefill_kv");
   if (!chunks || n < 1 || n > c->d.max_batch) return fail(LAT_ERR_ARG, "DiT block: need 1 <= n <= max_batch chunks");
@@ -1163,6 +1233,19 @@ lat_status lat_debug_dense_gemm(lat_ctx* c, int which, int layer, const void* ac
   a.M = M; a.N = N[which]; a.K = K[which]; a.terms = terms; a.w_row0 = layer * N[which];
   a.epi = E_STORE; a.out = out; a.ldo = N[which];
   return enqueue_dense(c, amap, *wm[which], a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lat_status lat_debug_trace(lat_ctx* c, unsigned long long* buf, long long n) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "trace: action-expert contexts only");
+  if (buf && n < (long long)c->num_sms * c->d.L * 64) return fail(LAT_ERR_SHAPE, "trace buffer too small");
+  if (buf && (reinterpret_cast<uintptr_t>(buf) & 7u)) return fail(LAT_ERR_ALIGN, "trace buffer not 8-byte aligned");
+  c->mk.trace = buf;
+  if (c->gexec) {   // the captured graph holds the old arguments
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  return LAT_OK;
 }
 
 lat_status lat_debug_clear(lat_ctx* c, void* stream) {

@@ -1,0 +1,1030 @@
+// Persistent kernel for the pi0 action expert: all blocks of one denoise step
+// in one launch.
+//
+// "Running VLAs at Real-time Speed" (reading note, sections 3 and 6) puts the
+// action expert's time into launch gaps and into streaming every block's
+// weights once per step; the TileRT page describes a persistent engine that
+// keeps weight loads running while compute waits on its dependencies.  Here one
+// CTA per SM lives for the whole step:
+//
+//  * warp 0 streams this CTA's share of every block's weights (128 x 64 bf16
+//    tiles, TMA, 128-byte swizzle) through a ring of shared-memory slots.  The
+//    weights do not depend on activations, so the stream runs ahead across
+//    phase boundaries and is throttled only by the ring.
+//  * warp 1 issues tcgen05 MMAs (M = 128 weight rows, N = 192 = three bf16
+//    planes x 64 tokens, fp32 accumulator in TMEM, two buffers).
+//  * warps 4..11 ("math") do everything that depends on activations: they load
+//    fp32 activation tiles by TMA, split them into three bf16 planes in the
+//    MMA's swizzled layout, run the split-K epilogue (fp32 atomics into the
+//    output), the attention and the combine of key-range partials.
+//
+// Per block seven phases, separated by a grid barrier (bounded spin):
+//   1 QKV projection of x (sums of squares of x on the side)
+//   2 attention: per (head, 32-key block); q and own k/v come from the raw
+//     projection sums with the RMS factor and RoPE applied on load; own k/v
+//     go to the cache as bf16
+//   3 combine of the key-block partials into the exact bf16 planes of o;
+//     clears the QKV accumulator
+//   4 x += o Wo (operand planes by TMA)
+//   5 gate/up projection of x (sums of squares of x on the side)
+//   6 h = GELU(r g) * (r u) once per element, into exact bf16 planes; clears
+//     the gate/up accumulator
+//   7 x += h Wd (operand planes by TMA)
+// The RMSNorm scales are folded into the weights; the per-token factor
+// r = rsqrt(mean(x^2) + eps) multiplies the projection sums (the projection is
+// linear in its input), as in the pages' fold (section 4.1).
+#pragma once
+#include "attention.cuh"
+#include "common.cuh"
+#include "skinny_gemm.cuh"
+
+namespace lat {
+
+constexpr int kMkThreads = 384;                 // 12 warps
+constexpr int kMkNW = 6;                        // weight ring slots
+constexpr int kMkNB = 2;                        // activation-plane ring slots
+constexpr int kMkNS = 4;                        // fp32 staging tiles (16 KB each)
+constexpr int kMkWBytes = 128 * 64 * 2;         // one weight tile
+constexpr int kMkBBytes = 192 * 64 * 2;         // one activation tile, three planes
+constexpr int kMkTile32 = 64 * 64 * 4;          // one fp32 64 x 64 activation tile
+constexpr int kMkRegion = kMkNB * kMkBBytes + kMkNS * kMkTile32;   // also the attention's tiles
+constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 2 * kMkNS + 3;
+
+__host__ __device__ constexpr int mk_smem_bytes() { return 1024 + kMkNW * kMkWBytes + kMkRegion + 8 * kMkBars + 16; }
+
+// attention tiles: K hi, V hi, K lo, V lo ([32 keys][dh + 8] bf16 each), the
+// exchanged scores [8][16][34] fp32; the q planes [2][64][dh + 8] bf16 overlay
+// everything after the two hi planes (they are consumed before it is needed)
+template <int DH>
+__host__ __device__ constexpr int mk_attn_smem() {
+  return 4 * kAttnKB * (DH + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4;
+}
+template <int DH>
+__host__ __device__ constexpr int mk_attn_q_end() {
+  return 2 * kAttnKB * (DH + 8) * 2 + 2 * 64 * (DH + 8) * 2;
+}
+static_assert(mk_attn_smem<256>() <= kMkRegion && mk_attn_q_end<256>() <= kMkRegion,
+              "attention tiles must fit in the activation region");
+
+// One projection: MT tiles of 128 output rows, KT tiles of 64 inputs, K split
+// into `splits` ranges; CTA b < MT * splits takes m-tile b % MT and K range
+// b / MT.  N = rows of one layer's matrix in the stacked weight tensor.
+struct MkGemm {
+  int MT, KT, splits, N;
+};
+
+struct MkArgs {
+  MkGemm g[4];              // 0 QKV, 1 O, 2 gate/up, 3 down
+  int l0, l1;               // layers [l0, l1) of this launch
+  int D, F, Hq, Hkv, T_q, T_prefix, T_kv, nqkv;
+  float eps, scale_log2;
+  float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
+  float* qkv;               // fp32 [splits][64][nqkv] QKV partial sums, one slab per K range
+  float* gu;                // fp32 [splits][64][2F] gate/up partial sums, one slab per K range
+  __nv_bfloat16* o_planes;  // [3][64][Hq dh] attention output as exact bf16 planes (rows >= T_q stay 0)
+  __nv_bfloat16* h_planes;  // [3][64][F] GeGLU output as exact bf16 planes (rows >= T_q stay 0)
+  __nv_bfloat16* q_planes;  // [2][64][Hq dh] q after RoPE, two-term bf16 (hi, lo)
+  __nv_bfloat16* kv_own;    // [k hi, k lo, v hi, v lo][64][Hkv dh] own keys / values, two-term bf16
+  float* ss;                // fp32 [L][2][64] sums of squares of x (0 at entry)
+  float* part_m;            // [n_kb][Hq][T_q]
+  float* part_l;
+  float* part_o;            // [n_kb][Hq][8 warps][dh / 16 n-tiles][32 lanes] x float4
+  const float* cos_t;       // [T_q][dh / 2] RoPE tables of the query positions
+  const float* sin_t;
+  const float4* rope_frag;  // the same angles in the attention's q-fragment order:
+                            // [8 warps][dh / 32 k-steps][4][32 lanes] x {cos i, cos i+1, sin i, sin i+1}
+  __nv_bfloat16* kv;        // cache of layer l0: [2][T_kv][Hkv dh]
+  long long kv_stride;      // elements from one layer's cache to the next
+  unsigned* bar;            // grid barrier counter (0 at entry)
+  DevErr* err;
+  unsigned long long* trace;   // null, or [layers][grid][64] phase timestamps (ns): 0..14 block
+                               // start and the ends of each phase / barrier, 16..18 attention,
+                               // 20 + 4 g .. 23 + 4 g projection g
+};
+
+struct MkRange {
+  int m, k0, k1;
+  bool active;
+};
+
+__device__ __forceinline__ MkRange mk_range(const MkGemm& g, int b) {
+  MkRange r;
+  r.active = b < g.MT * g.splits;
+  r.m = b % g.MT;
+  const int s = b / g.MT;
+  r.k0 = s * g.KT / g.splits;
+  r.k1 = (s + 1) * g.KT / g.splits;
+  return r;
+}
+
+__device__ __forceinline__ bool mk_aborted(DevErr* e) { return *reinterpret_cast<volatile unsigned*>(&e->code) != 0; }
+
+// Bounded mbarrier wait that also gives up as soon as any CTA has recorded an
+// error: after a failure every wait returns at once and the kernel runs to its
+// end with meaningless results (the host reports the error).
+__device__ __forceinline__ bool mk_wait(uint64_t* bar, uint32_t parity, DevErr* err, unsigned where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (int i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63) {
+      if (mk_aborted(err)) return false;
+      if (clock64() - t0 > kSpinBudget) {
+        record_error(err, 1u, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mk_mark(unsigned long long* tr, int ev) {
+  if (tr) tr[ev] = global_ns();
+}
+
+__device__ __forceinline__ float2 ldcg2(const float* p) { return __ldcg(reinterpret_cast<const float2*>(p)); }
+
+// 8 fp32 values (registers) -> 8 bf16 hi and 8 bf16 lo (two-term split)
+__device__ __forceinline__ void split8_regs(const float (&v)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) split_pair2(v[2 * e], v[2 * e + 1], h[e], l[e]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Grid barrier among the math warps of all CTAs (barrier n waits for n * grid
+// arrivals).  Generic-proxy writes before it become visible to TMA reads after it.
+__device__ __forceinline__ void mk_grid_sync(unsigned* ctr, unsigned target, DevErr* err, int mt) {
+  fence_proxy_async_global();
+  named_sync(1, 256);
+  if (mt == 0) {
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
+    const long long t0 = clock64();
+    for (int i = 0;; ++i) {
+      if (ld_acquire_u32(ctr) >= target) break;
+      if ((i & 15) == 15) {
+        if (mk_aborted(err)) break;
+        if (clock64() - t0 > kSpinBudget) {
+          record_error(err, 2u, 900);
+          break;
+        }
+      }
+    }
+    fence_proxy_async_global();
+  }
+  named_sync(1, 256);
+}
+
+// Shared state of the math warps.
+struct MkMath {
+  uint8_t* sB;
+  uint8_t* sS;
+  uint64_t* bfull;
+  uint64_t* bempty;
+  uint64_t* sfull;
+  uint64_t* sempty;
+  uint64_t* accfull;
+  uint64_t* go;
+  uint32_t tmem;
+  uint32_t bt, gc;
+  uint32_t sph;    // bit i: parity of the next completion of sfull[i]
+  int mt;
+};
+
+// Math side of one projection: fp32 activation tiles (staged by the loader) ->
+// exact bf16 planes for the MMA, or nothing when the loader brings the planes
+// themselves; then the split-K epilogue.  `stats` (CTAs of m-tile 0) receives
+// the per-token sums of squares of the activation.
+// `slab` > 0: each K range stores its partial sums into its own slab of `out`
+// (plain stores, summed by the consumer) instead of adding them atomically.
+__device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool staged, float* stats, float* out,
+                                             int ld, size_t slab, int T_q, DevErr* err, unsigned long long* tr) {
+  const MkRange r = mk_range(g, blockIdx.x);
+  if (!r.active) return;
+  const int nk = r.k1 - r.k0;
+  const int mw = s.mt >> 5, lane = s.mt & 31;
+  if (!staged) {   // the loader brings this projection's operand planes by TMA
+    s.bt += nk;
+    if (tr) tr[0] = tr[1] = global_ns();
+  }
+  // conversion layout: per k-tile each thread takes two rows, 8 columns of each
+  // (cols 4p..4p+3 and 32+4p..+3); rows ordered so a warp's 8-byte stores of
+  // one pass touch both halves of the 128-byte swizzled rows (conflict-free)
+  const int rq = lane >> 3, p = lane & 7;
+  int rows[2];
+  float sq[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    rows[i] = mw * 8 + i + (rq & 1) * 4 + (rq >> 1) * 2;
+    sq[i] = 0.f;
+  }
+  const bool do_stats = stats != nullptr && r.m == 0;
+  for (int j = 0; j < (staged ? nk : 0); ++j) {
+    const int bi = j % kMkNS;
+    const uint32_t b = s.bt % kMkNB;
+    mk_wait(&s.sfull[bi], (s.sph >> bi) & 1u, err, 30);
+    s.sph ^= 1u << bi;
+    if (j == 0) mk_mark(tr, 0);
+    mk_wait(&s.bempty[b], ((s.bt / kMkNB) & 1) ^ 1, err, 31);
+    const float* src = reinterpret_cast<const float*>(s.sS + bi * kMkTile32);
+    uint8_t* dst = s.sB + b * kMkBBytes;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = rows[i];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int col = hh * 32 + 4 * p;
+        const float4 v = *reinterpret_cast<const float4*>(src + t * 64 + col);
+        if (do_stats) sq[i] += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+        uint32_t h0, m0, l0, h1, m1, l1;
+        split_pair_exact(v.x, v.y, h0, m0, l0);
+        split_pair_exact(v.z, v.w, h1, m1, l1);
+        const uint32_t off = (uint32_t)(t * 128 + ((((col >> 3) ^ t) & 7) << 4) + ((p & 1) << 3));
+        *reinterpret_cast<uint2*>(dst + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(m0, m1);
+        *reinterpret_cast<uint2*>(dst + 16384 + off) = make_uint2(l0, l1);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&s.sempty[bi]);   // this warp is done with the staging tile
+      mbar_arrive(&s.bfull[b]);     // and its rows of the operand are written
+    }
+    ++s.bt;
+  }
+  if (do_stats) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float v = sq[i];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      if (p == 0) atomicAdd(stats + rows[i], v);
+    }
+  }
+  // epilogue: warp (4 + mw) reads TMEM lanes 32 (mw % 4) .. +31 = output rows,
+  // tokens 32 (mw / 4) .. +31 of each plane; the planes are summed hi + mid + lo
+  if (staged) mk_mark(tr, 1);
+  mk_wait(s.accfull, s.gc & 1, err, 32);
+  mk_mark(tr, 2);
+  tc_fence_after();
+  const uint32_t acc = s.tmem + (s.gc & 1) * 256;
+  ++s.gc;
+  const int q = mw & 3, ch = mw >> 2;
+  const int f = r.m * 128 + q * 32 + lane;
+  const uint32_t tb = acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
+  float v[32], w[32];
+  tmem_ld32(tb, v);
+  tmem_ld32(tb + 64, w);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += w[j];
+  tmem_ld32(tb + 128, w);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] += w[j];
+  tc_fence_before();
+  if (slab) {
+    float* o = out + (size_t)(blockIdx.x / g.MT) * slab;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (ch * 32 + j < T_q) __stcg(o + (size_t)(ch * 32 + j) * ld + f, v[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (ch * 32 + j < T_q) atomicAdd(out + (size_t)(ch * 32 + j) * ld + f, v[j]);
+  }
+  mk_mark(tr, 3);
+}
+
+// Phase 2: q, own k and own v of the block, once per element: the sum of the
+// QKV partial slabs times r = rsqrt(mean(x^2) + eps), RoPE (rotate-half pairs
+// (i, i + dh/2)) on q and k, then two-term bf16 splits: q -> q_planes, own k/v
+// -> kv_own planes; the bf16 cache copy of own k/v (nearest) goes to the cache
+// slots T_prefix + t.  Item = 4 RoPE pairs of one q/k head or 4 values of v.
+template <int DH>
+__device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int splits, const float* ss1, __nv_bfloat16* kc,
+                                                __nv_bfloat16* vc, float invD, int mt) {
+  constexpr int HD = DH / 2;
+  const int nh = a.Hq + a.Hkv, kvd = a.Hkv * DH, qd = a.Hq * DH;
+  const int rot_per_t = nh * (HD / 4), v_per_t = a.Hkv * (DH / 4);
+  const int n_rot = a.T_q * rot_per_t, n_all = n_rot + a.T_q * v_per_t;
+  const size_t slab = (size_t)64 * a.nqkv;
+  const size_t qpl = (size_t)64 * qd, kpl = (size_t)64 * kvd;
+  for (int it = blockIdx.x * 256 + mt; it < n_all; it += gridDim.x * 256) {
+    if (it < n_rot) {
+      const int t = it / rot_per_t, rem = it % rot_per_t;
+      const int hd = rem / (HD / 4), i = (rem % (HD / 4)) * 4;
+      const float* p0 = a.qkv + (size_t)t * a.nqkv + hd * DH + i;
+      float4 x0 = __ldcg(reinterpret_cast<const float4*>(p0));
+      float4 x1 = __ldcg(reinterpret_cast<const float4*>(p0 + HD));
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 y0 = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab));
+        const float4 y1 = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab + HD));
+        x0.x += y0.x; x0.y += y0.y; x0.z += y0.z; x0.w += y0.w;
+        x1.x += y1.x; x1.y += y1.y; x1.z += y1.z; x1.w += y1.w;
+      }
+      const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
+      const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)t * HD + i));
+      const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)t * HD + i));
+      const float a0[4] = {rv * x0.x, rv * x0.y, rv * x0.z, rv * x0.w};
+      const float a1[4] = {rv * x1.x, rv * x1.y, rv * x1.z, rv * x1.w};
+      const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+      float y0[4], y1[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y0[e] = a0[e] * cc[e] - a1[e] * ss[e];
+        y1[e] = a1[e] * cc[e] + a0[e] * ss[e];
+      }
+      uint32_t h0[2], l0[2], h1[2], l1[2];
+      split_pair2(y0[0], y0[1], h0[0], l0[0]);
+      split_pair2(y0[2], y0[3], h0[1], l0[1]);
+      split_pair2(y1[0], y1[1], h1[0], l1[0]);
+      split_pair2(y1[2], y1[3], h1[1], l1[1]);
+      if (hd < a.Hq) {
+        uint2* q = reinterpret_cast<uint2*>(a.q_planes + (size_t)t * qd + hd * DH + i);
+        q[0] = make_uint2(h0[0], h0[1]);
+        q[HD / 4] = make_uint2(h1[0], h1[1]);
+        q[qpl / 4] = make_uint2(l0[0], l0[1]);
+        q[qpl / 4 + HD / 4] = make_uint2(l1[0], l1[1]);
+      } else {
+        const int kh = hd - a.Hq;
+        uint2* k = reinterpret_cast<uint2*>(a.kv_own + (size_t)t * kvd + kh * DH + i);
+        k[0] = make_uint2(h0[0], h0[1]);
+        k[HD / 4] = make_uint2(h1[0], h1[1]);
+        k[kpl / 4] = make_uint2(l0[0], l0[1]);
+        k[kpl / 4 + HD / 4] = make_uint2(l1[0], l1[1]);
+        float tx, ty;
+        uint2* ck = reinterpret_cast<uint2*>(kc + (size_t)(a.T_prefix + t) * kvd + kh * DH + i);
+        ck[0] = make_uint2(rn_pair(y0[0], y0[1], tx, ty), rn_pair(y0[2], y0[3], tx, ty));
+        ck[HD / 4] = make_uint2(rn_pair(y1[0], y1[1], tx, ty), rn_pair(y1[2], y1[3], tx, ty));
+      }
+    } else {
+      const int iv = it - n_rot;
+      const int t = iv / v_per_t, j = (iv % v_per_t) * 4;
+      const float* p0 = a.qkv + (size_t)t * a.nqkv + nh * DH + j;
+      float4 x = __ldcg(reinterpret_cast<const float4*>(p0));
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 y = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab));
+        x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+      }
+      const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
+      x.x *= rv; x.y *= rv; x.z *= rv; x.w *= rv;
+      uint32_t hh[2], ll[2];
+      split_pair2(x.x, x.y, hh[0], ll[0]);
+      split_pair2(x.z, x.w, hh[1], ll[1]);
+      uint2* v = reinterpret_cast<uint2*>(a.kv_own + 2 * kpl + (size_t)t * kvd + j);
+      v[0] = make_uint2(hh[0], hh[1]);
+      v[kpl / 4] = make_uint2(ll[0], ll[1]);
+      float tx, ty;
+      *reinterpret_cast<uint2*>(vc + (size_t)(a.T_prefix + t) * kvd + j) =
+          make_uint2(rn_pair(x.x, x.y, tx, ty), rn_pair(x.z, x.w, tx, ty));
+    }
+  }
+}
+
+// Phase 3: attention of the chunk over [cache | own], one (head, 32-key block)
+// per unit, partial (max, sum, unnormalised output) per unit.  Same arithmetic
+// as attention_kernel (two-term q and p, own keys as computed in two planes);
+// warp half h owns head dims [h dh/4, +dh/4) and [dh/2 + h dh/4, +dh/4).  q and
+// the own keys arrive as planes from phase 2, cache keys from the cache.
+template <int DH>
+__device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc, __nv_bfloat16* vc, uint8_t* sR,
+                                             int mt, unsigned long long* tr) {
+  constexpr int KB = kAttnKB;
+  constexpr int LD = DH + 8;
+  constexpr int HD = DH / 2;
+  constexpr int KS = HD / 16;
+  constexpr int NT = HD / 8;
+  constexpr int SLD = KB + 2;
+  constexpr int Q4 = DH / 4;
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sR);       // hi plane; lo plane at + 2 KB LD
+  __nv_bfloat16* sV = sK + KB * LD;
+  float* sS = reinterpret_cast<float*>(sK + 4 * KB * LD);
+  __nv_bfloat16* sQ = sK + 2 * KB * LD;                            // q hi plane; lo plane at + 64 LD
+  const int warp = mt >> 5, lane = mt & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int rt = warp & 3, half = warp >> 2;
+  const int nkb = attn_key_blocks(a.T_kv);
+  const int units = a.Hq * nkb;
+  const int kvd = a.Hkv * DH, group = a.Hq / a.Hkv, qd = a.Hq * DH;
+  const int own0 = a.T_prefix;
+  const int r0 = rt * 16 + g, r1 = r0 + 8;
+  const bool v0 = r0 < a.T_q, v1 = r1 < a.T_q;
+  const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV), sQa = smem_u32(sQ);
+  const uint32_t LO = (uint32_t)(2 * KB * LD * 2);
+  const size_t kpl = (size_t)64 * kvd, qpl = (size_t)64 * qd;
+  float* myS = sS + warp * 16 * SLD;
+  const float* peerS = sS + (warp ^ 4) * 16 * SLD;
+  const int mi = lane >> 3, rr = lane & 7;
+
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int h = u / nkb, kb = u % nkb, kvh = h / group;
+    const bool has_lo = (kb + 1) * KB > own0 && own0 < a.T_kv;
+    named_sync(3, 256);   // the previous unit is done with the tiles
+    // ---- async copies: hi planes of the key block (cache or own), q planes ----
+    for (int idx = mt; idx < KB * (DH / 8); idx += 256) {
+      const int row = idx / (DH / 8), c8 = idx % (DH / 8);
+      const int key = kb * KB + row;
+      const bool own = key >= own0 && key < a.T_kv;
+      const bool in = key < a.T_kv;
+      const __nv_bfloat16* ks;
+      const __nv_bfloat16* vs;
+      if (own) {
+        const size_t off = (size_t)(key - own0) * kvd + kvh * DH + c8 * 8;
+        ks = a.kv_own + off;
+        vs = a.kv_own + 2 * kpl + off;
+      } else {
+        const size_t off = (size_t)(in ? key : 0) * kvd + kvh * DH + c8 * 8;
+        ks = kc + off;
+        vs = vc + off;
+      }
+      cp_async16(sK + row * LD + c8 * 8, ks, in ? 16 : 0);
+      cp_async16(sV + row * LD + c8 * 8, vs, in ? 16 : 0);
+    }
+    for (int idx = mt; idx < 2 * 64 * (DH / 8); idx += 256) {
+      const int pr = idx / (DH / 8), c8 = idx % (DH / 8);   // plane-row: plane pr / 64, row pr % 64
+      const int row = pr & 63;
+      const bool in = row < a.T_q;
+      const __nv_bfloat16* src = a.q_planes + (pr >> 6) * qpl + (size_t)(in ? row : 0) * qd + h * DH + c8 * 8;
+      cp_async16(sQ + pr * LD + c8 * 8, src, in ? 16 : 0);
+    }
+    cp_async_wait_all();
+    named_sync(3, 256);
+    // ---- q fragments by ldmatrix: rows rt*16.., this warp's dims ----
+    uint32_t qh[KS][4], ql[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int db = (ks < KS / 2) ? half * Q4 + ks * 16 : HD + half * Q4 + (ks - KS / 2) * 16;
+      const uint32_t ad = sQa + (uint32_t)((rt * 16 + (lane & 15)) * LD + db + ((lane >> 4) << 3)) * 2u;
+      ldsm_x4(ad, qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3]);
+      ldsm_x4(ad + (uint32_t)(64 * LD * 2), ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3]);
+    }
+    named_sync(3, 256);   // the q tiles are consumed: their bytes hold the lo planes and scores next
+    mk_mark(tr, 17);
+    // ---- lo planes: own keys from phase 2, zero for cache keys ----
+    if (has_lo) {
+      for (int idx = mt; idx < KB * (DH / 8); idx += 256) {
+        const int row = idx / (DH / 8), c8 = idx % (DH / 8);
+        const int key = kb * KB + row;
+        if (key >= own0 && key < a.T_kv) {
+          const size_t off = (size_t)(key - own0) * kvd + kvh * DH + c8 * 8;
+          cp_async16(sK + 2 * KB * LD + row * LD + c8 * 8, a.kv_own + kpl + off, 16);
+          cp_async16(sV + 2 * KB * LD + row * LD + c8 * 8, a.kv_own + 3 * kpl + off, 16);
+        } else {
+          *reinterpret_cast<uint4*>(sK + 2 * KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sV + 2 * KB * LD + row * LD + c8 * 8) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      cp_async_wait_all();
+    }
+    named_sync(3, 256);
+    mk_mark(tr, 18);
+
+    // ---- partial scores over this warp's dims: 16 rows x 32 keys ----
+    float sa[4][4], sb[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[j][e] = sb[j][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int db = (ks < KS / 2) ? half * Q4 + ks * 16 : HD + half * Q4 + (ks - KS / 2) * 16;
+      uint32_t b[4][2];
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {
+        const int key = jp * 16 + ((mi >> 1) << 3) + rr;
+        const int col = db + ((mi & 1) << 3);
+        ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                b[2 * jp + 1][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_16816(sa[j], qh[ks], b[j][0], b[j][1]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_16816(sb[j], ql[ks], b[j][0], b[j][1]);
+      if (has_lo) {
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          const int key = jp * 16 + ((mi >> 1) << 3) + rr;
+          const int col = db + ((mi & 1) << 3);
+          ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                  b[2 * jp + 1][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma_16816(sb[j], qh[ks], b[j][0], b[j][1]);
+      }
+    }
+    // ---- exchange partial scores with the other half ----
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = j * 8 + 2 * tq;
+      *reinterpret_cast<float2*>(myS + g * SLD + c) = make_float2(sa[j][0] + sb[j][0], sa[j][1] + sb[j][1]);
+      *reinterpret_cast<float2*>(myS + (g + 8) * SLD + c) = make_float2(sa[j][2] + sb[j][2], sa[j][3] + sb[j][3]);
+    }
+    named_sync(3, 256);
+    float s[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = j * 8 + 2 * tq;
+      const float2 p0 = *reinterpret_cast<const float2*>(peerS + g * SLD + c);
+      const float2 p1 = *reinterpret_cast<const float2*>(peerS + (g + 8) * SLD + c);
+      s[j][0] = (sa[j][0] + sb[j][0]) + p0.x;
+      s[j][1] = (sa[j][1] + sb[j][1]) + p0.y;
+      s[j][2] = (sa[j][2] + sb[j][2]) + p1.x;
+      s[j][3] = (sa[j][3] + sb[j][3]) + p1.y;
+    }
+    // ---- softmax of this key block (base 2) ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int key = kb * KB + j * 8 + 2 * tq;
+      s[j][0] = (key < a.T_kv) ? s[j][0] * a.scale_log2 : -INFINITY;
+      s[j][1] = (key + 1 < a.T_kv) ? s[j][1] * a.scale_log2 : -INFINITY;
+      s[j][2] = (key < a.T_kv) ? s[j][2] * a.scale_log2 : -INFINITY;
+      s[j][3] = (key + 1 < a.T_kv) ? s[j][3] * a.scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s[j][0] = exp2f(s[j][0] - mx0);
+      s[j][1] = exp2f(s[j][1] - mx0);
+      s[j][2] = exp2f(s[j][2] - mx1);
+      s[j][3] = exp2f(s[j][3] - mx1);
+      sum0 += s[j][0] + s[j][1];
+      sum1 += s[j][2] + s[j][3];
+    }
+    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 1);
+    sum0 += __shfl_xor_sync(0xffffffffu, sum0, 2);
+    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 1);
+    sum1 += __shfl_xor_sync(0xffffffffu, sum1, 2);
+
+    // ---- O = P V over this warp's output dims ----
+    float o[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t ph[4], pl[4];
+      split_pair2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+      split_pair2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+      split_pair2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+      split_pair2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+      const int key = kk * 16 + ((mi & 1) << 3) + rr;
+      uint32_t b[NT][2];
+#pragma unroll
+      for (int jp = 0; jp < NT / 2; ++jp) {
+        const int j8 = 2 * jp;
+        const int col = ((j8 < NT / 2) ? half * Q4 + j8 * 8 : HD + half * Q4 + (j8 - NT / 2) * 8) + ((mi >> 1) << 3);
+        ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                  b[2 * jp + 1][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_16816(o[j], ph, b[j][0], b[j][1]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_16816(o[j], pl, b[j][0], b[j][1]);
+      if (has_lo) {
+#pragma unroll
+        for (int jp = 0; jp < NT / 2; ++jp) {
+          const int j8 = 2 * jp;
+          const int col =
+              ((j8 < NT / 2) ? half * Q4 + j8 * 8 : HD + half * Q4 + (j8 - NT / 2) * 8) + ((mi >> 1) << 3);
+          ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b[2 * jp][0], b[2 * jp][1], b[2 * jp + 1][0],
+                    b[2 * jp + 1][1]);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_16816(o[j], ph, b[j][0], b[j][1]);
+      }
+    }
+
+    mk_mark(tr, 19);
+    // ---- partials of this key block: (max, sum) per row; the unnormalised
+    //      output in fragment order, [warp][n-tile][lane] x float4 (rows r0 | r1) ----
+    const size_t base = ((size_t)kb * a.Hq + h) * a.T_q;
+    if (tq == 0 && half == 0) {
+      if (v0) { a.part_m[base + r0] = mx0; a.part_l[base + r0] = sum0; }
+      if (v1) { a.part_m[base + r1] = mx1; a.part_l[base + r1] = sum1; }
+    }
+    float4* po = reinterpret_cast<float4*>(a.part_o) + (((size_t)kb * a.Hq + h) * 8 + warp) * NT * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) __stcg(po + j * 32, make_float4(o[j][0], o[j][1], o[j][2], o[j][3]));
+  }
+  fence_proxy_async_smem();   // the tiles' bytes are reused by TMA in the next phase
+}
+
+// Phase 4: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s per (token,
+// head), written as the exact bf16 planes of the output projection's operand.  Work comes in
+// chunks of 256 fragments (the attention's output order); for the <= 2 (head,
+// warp) groups of a chunk the per-row weights 2^(m_s - M) / L go to shared
+// memory first, then each thread merges one fragment over all key blocks.
+template <int DH>
+__device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw) {
+  constexpr int HD = DH / 2, NT = HD / 8, Q4 = DH / 4;
+  constexpr int PER_HW = NT * 32;   // fragments of one (head, warp)
+  const int nkb = attn_key_blocks(a.T_kv);
+  const int qd = a.Hq * DH;
+  const int items = a.Hq * 8 * PER_HW;
+  const size_t ml_stride = (size_t)a.Hq * a.T_q;
+  const size_t o_stride = (size_t)a.Hq * 8 * PER_HW;
+  const size_t pl = (size_t)64 * qd;   // one plane
+  for (int c0 = blockIdx.x * 256; c0 < items; c0 += gridDim.x * 256) {
+    const int g0 = c0 / PER_HW;
+    // pass 1: weights of the rows of groups g0, g0 + 1 (16 rows each): thread
+    // (row mt / 8, lane-group part mt % 8) takes key blocks part, part + 8, ...
+    {
+      const int row = mt >> 3, part = mt & 7;
+      const int gg = g0 + (row >> 4), rr = row & 15;
+      const int h = gg / 8, t = (gg % 8 & 3) * 16 + rr;
+      const bool valid = h < a.Hq && t < a.T_q;
+      const size_t i0 = (size_t)(valid ? h : 0) * a.T_q + (valid ? t : 0);
+      constexpr int MAXP = 4;   // key blocks per thread held in registers (n_kb <= 32)
+      float mv[MAXP], lv[MAXP];
+#pragma unroll
+      for (int e = 0; e < MAXP; ++e) {
+        const int kb = part + 8 * e;
+        const bool in = valid && kb < nkb;
+        mv[e] = in ? __ldcg(a.part_m + (size_t)kb * ml_stride + i0) : -INFINITY;
+        lv[e] = in ? __ldcg(a.part_l + (size_t)kb * ml_stride + i0) : 0.f;
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < MAXP; ++e) M = fmaxf(M, mv[e]);
+      for (int kb = part + 8 * MAXP; kb < nkb; kb += 8)   // longer caches
+        if (valid) M = fmaxf(M, __ldcg(a.part_m + (size_t)kb * ml_stride + i0));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+      float wv[MAXP], L = 0.f;
+#pragma unroll
+      for (int e = 0; e < MAXP; ++e) {
+        wv[e] = (mv[e] == -INFINITY) ? 0.f : exp2f(mv[e] - M);
+        L += wv[e] * lv[e];
+      }
+      for (int kb = part + 8 * MAXP; kb < nkb; kb += 8)
+        if (valid) {
+          const float m = __ldcg(a.part_m + (size_t)kb * ml_stride + i0);
+          L += exp2f(m - M) * __ldcg(a.part_l + (size_t)kb * ml_stride + i0);
+        }
+      L += __shfl_xor_sync(0xffffffffu, L, 1);
+      L += __shfl_xor_sync(0xffffffffu, L, 2);
+      L += __shfl_xor_sync(0xffffffffu, L, 4);
+      const float il = valid ? 1.f / L : 0.f;
+#pragma unroll
+      for (int e = 0; e < MAXP; ++e)
+        if (part + 8 * e < nkb) sw[row * nkb + part + 8 * e] = wv[e] * il;
+      for (int kb = part + 8 * MAXP; kb < nkb; kb += 8)
+        sw[row * nkb + kb] = valid ? exp2f(__ldcg(a.part_m + (size_t)kb * ml_stride + i0) - M) * il : 0.f;
+    }
+    named_sync(3, 256);
+    // pass 2: one fragment per thread
+    const int it = c0 + mt;
+    if (it < items) {
+      const int lane = it & 31, j = (it >> 5) % NT, gg = it / PER_HW;
+      const int h = gg / 8, w = gg % 8;
+      const int rt = w & 3, half = w >> 2, g = lane >> 2, tq = lane & 3;
+      const int r0 = rt * 16 + g, r1 = r0 + 8;
+      const int c = ((j < NT / 2) ? half * Q4 + j * 8 : HD + half * Q4 + (j - NT / 2) * 8) + 2 * tq;
+      const float* w0 = sw + ((gg - g0) * 16 + g) * nkb;
+      const float* w1 = w0 + 8 * nkb;
+      const float4* po = reinterpret_cast<const float4*>(a.part_o) + it;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < nkb; s0 += 16) {
+        float4 ov[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          ov[e] = (s0 + e < nkb) ? __ldcg(po + (size_t)(s0 + e) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          if (s0 + e < nkb) {
+            const float a0 = w0[s0 + e], a1 = w1[s0 + e];
+            acc.x += a0 * ov[e].x;
+            acc.y += a0 * ov[e].y;
+            acc.z += a1 * ov[e].z;
+            acc.w += a1 * ov[e].w;
+          }
+        }
+      }
+      uint32_t hi, mid, lo;
+      const size_t col = (size_t)h * DH + c;
+      if (r0 < a.T_q) {
+        split_pair_exact(acc.x, acc.y, hi, mid, lo);
+        uint32_t* d = reinterpret_cast<uint32_t*>(a.o_planes + (size_t)r0 * qd + col);
+        d[0] = hi;
+        d[pl / 2] = mid;
+        d[pl] = lo;
+      }
+      if (r1 < a.T_q) {
+        split_pair_exact(acc.z, acc.w, hi, mid, lo);
+        uint32_t* d = reinterpret_cast<uint32_t*>(a.o_planes + (size_t)r1 * qd + col);
+        d[0] = hi;
+        d[pl / 2] = mid;
+        d[pl] = lo;
+      }
+    }
+    named_sync(3, 256);   // sw is reused by the next chunk
+  }
+  fence_proxy_async_smem();   // sw's bytes are reused by TMA in the next phase
+}
+
+// Phase 7: h = GELU(r g) * (r u) for every token and FFN column, once, as the
+// exact bf16 planes of the down projection's operand; g and u are the sums of
+// the gate/up partial slabs.  r = rsqrt(mean(x^2) + eps) of the FFN input.
+__device__ __forceinline__ void mk_geglu_planes(const MkArgs& a, int splits, const float* ss2, float invD, int mt) {
+  const int F = a.F;
+  const int n4 = a.T_q * F / 4;
+  const size_t pl = (size_t)64 * F, slab = (size_t)64 * 2 * F;
+  for (int i = blockIdx.x * 256 + mt; i < n4; i += gridDim.x * 256) {
+    const int t = (i * 4) / F, j = (i * 4) % F;
+    const float rv = rsqrtf(__ldcg(ss2 + t) * invD + a.eps);
+    const float* gp = a.gu + (size_t)t * 2 * F + j;
+    float4 g = __ldcg(reinterpret_cast<const float4*>(gp));
+    float4 u = __ldcg(reinterpret_cast<const float4*>(gp + F));
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 g2 = __ldcg(reinterpret_cast<const float4*>(gp + sp * slab));
+      const float4 u2 = __ldcg(reinterpret_cast<const float4*>(gp + sp * slab + F));
+      g.x += g2.x; g.y += g2.y; g.z += g2.z; g.w += g2.w;
+      u.x += u2.x; u.y += u2.y; u.z += u2.z; u.w += u2.w;
+    }
+    const float h0 = gelu_tanh_fast(rv * g.x) * (rv * u.x), h1 = gelu_tanh_fast(rv * g.y) * (rv * u.y);
+    const float h2 = gelu_tanh_fast(rv * g.z) * (rv * u.z), h3 = gelu_tanh_fast(rv * g.w) * (rv * u.w);
+    uint32_t a0, b0, c0, a1, b1, c1;
+    split_pair_exact(h0, h1, a0, b0, c0);
+    split_pair_exact(h2, h3, a1, b1, c1);
+    uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + j);
+    d[0] = make_uint2(a0, a1);
+    d[pl / 4] = make_uint2(b0, b1);
+    d[pl / 2] = make_uint2(c0, c1);
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kMkThreads, 1)
+    pi0_step_kernel(const __grid_constant__ CUtensorMap w_qkv, const __grid_constant__ CUtensorMap w_o,
+                    const __grid_constant__ CUtensorMap w_gu, const __grid_constant__ CUtensorMap w_d,
+                    const __grid_constant__ CUtensorMap act_x, const __grid_constant__ CUtensorMap act_op,
+                    const __grid_constant__ CUtensorMap act_hp, const MkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sW = smem;
+  uint8_t* sR = smem + kMkNW * kMkWBytes;
+  uint8_t* sB = sR;
+  uint8_t* sS = sR + kMkNB * kMkBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kMkRegion);
+  uint64_t* wfull = bars;                  // weight tile landed
+  uint64_t* wempty = wfull + kMkNW;        // weight slot free (MMA done)
+  uint64_t* bfull = wempty + kMkNW;        // operand tile built by the math warps (8 arrivals)
+  uint64_t* bfullt = bfull + kMkNB;        // operand tile landed by TMA (O and down projections)
+  uint64_t* bempty = bfullt + kMkNB;       // operand slot free (MMA done)
+  uint64_t* sfull = bempty + kMkNB;        // staging tile landed
+  uint64_t* sempty = sfull + kMkNS;        // staging tile read by all math warps (8 arrivals)
+  uint64_t* accfull = sempty + kMkNS;      // accumulator complete
+  uint64_t* mdone = accfull + 1;           // every MMA complete (teardown)
+  uint64_t* go = mdone + 1;                // grid barrier passed before a projection phase
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(go + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMkNW; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], 1);
+    }
+    for (int i = 0; i < kMkNB; ++i) {
+      mbar_init(&bfull[i], 8);
+      mbar_init(&bfullt[i], 1);
+      mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < kMkNS; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 8);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(mdone, 1);
+    mbar_init(go, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    if (warp == 0 && lane == 0) {
+      // ---------------- weight stream ----------------
+      tma_prefetch_desc(&w_qkv);
+      tma_prefetch_desc(&w_o);
+      tma_prefetch_desc(&w_gu);
+      tma_prefetch_desc(&w_d);
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t wt = 0;
+      bool ok = true;
+      for (int l = a.l0; l < a.l1 && ok; ++l)
+        for (int gi = 0; gi < 4 && ok; ++gi) {
+          const MkRange r = mk_range(a.g[gi], blockIdx.x);
+          if (!r.active) continue;
+          const CUtensorMap* map = gi == 0 ? &w_qkv : gi == 1 ? &w_o : gi == 2 ? &w_gu : &w_d;
+          const int row = l * a.g[gi].N + r.m * 128;
+          for (int k = r.k0; k < r.k1; ++k) {
+            const uint32_t s = wt % kMkNW;
+            if (!mk_wait(&wempty[s], ((wt / kMkNW) & 1) ^ 1, a.err, 20)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&wfull[s], kMkWBytes);
+            tma_load_2d(sW + s * kMkWBytes, map, &wfull[s], k * 64, row, pol);
+            ++wt;
+          }
+        }
+      // never leave a copy in flight into this CTA's shared memory
+      for (uint32_t i = wt > (uint32_t)kMkNW ? wt - kMkNW : 0; i < wt; ++i)
+        mbar_wait(&wfull[i % kMkNW], (i / kMkNW) & 1, nullptr, 0);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issue ----------------
+      const uint32_t idesc = idesc_bf16_f32(128, 192);
+      uint32_t wt = 0, bt = 0, gc = 0, pf = 0, pt = 0;   // pf / pt: per-slot parities of bfull / bfullt
+      bool ok = true;
+      for (int l = a.l0; l < a.l1 && ok; ++l)
+        for (int gi = 0; gi < 4 && ok; ++gi) {
+          const MkRange r = mk_range(a.g[gi], blockIdx.x);
+          if (!r.active) continue;
+          const uint32_t acc = tmem + (gc & 1) * 256;
+          for (int k = r.k0; k < r.k1; ++k) {
+            const uint32_t b = bt % kMkNB, s = wt % kMkNW;
+            const bool tma_b = gi == 1 || gi == 3;
+            uint64_t* bf = tma_b ? &bfullt[b] : &bfull[b];
+            const uint32_t par = ((tma_b ? pt : pf) >> b) & 1u;
+            if (!mk_wait(bf, par, a.err, 21) || !mk_wait(&wfull[s], (wt / kMkNW) & 1, a.err, 22)) {
+              ok = false;
+              break;
+            }
+            if (tma_b) pt ^= 1u << b;
+            else pf ^= 1u << b;
+            tc_fence_after();
+            const uint32_t wa = smem_u32(sW + s * kMkWBytes), ba = smem_u32(sB + b * kMkBBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(acc, desc_k_sw128(wa + kk * 32), desc_k_sw128(ba + kk * 32), idesc,
+                          (k != r.k0 || kk != 0) ? 1u : 0u);
+            mma_commit(&wempty[s]);
+            mma_commit(&bempty[b]);
+            ++wt;
+            ++bt;
+          }
+          if (!ok) break;
+          mma_commit(accfull);
+          ++gc;
+        }
+      mma_commit(mdone);   // every MMA of this CTA has completed before TMEM is freed
+      mbar_wait(mdone, 0, nullptr, 0);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------- activation loader ----------------
+      // after each grid barrier that opens a projection phase: fp32 activation
+      // tiles into the staging slots (refilled as the math warps release them),
+      // or, for the output projection, the operand planes straight into the
+      // operand slots
+      tma_prefetch_desc(&act_x);
+      tma_prefetch_desc(&act_op);
+      tma_prefetch_desc(&act_hp);
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t bt = 0, gop = 0;
+      uint32_t sfill[kMkNS] = {};   // copies issued into each staging tile so far
+      uint32_t bout = 0;            // operand copies issued, by slot (bit)
+      uint32_t pt = 0;              // per-slot parity of bfullt
+      bool ok = true;
+      for (int l = a.l0; l < a.l1 && ok; ++l)
+        for (int gi = 0; gi < 4 && ok; ++gi) {
+          if (!mk_wait(go, gop & 1, a.err, 40)) {
+            ok = false;
+            break;
+          }
+          ++gop;
+          fence_proxy_async_global();
+          fence_proxy_async_smem();
+          const MkRange r = mk_range(a.g[gi], blockIdx.x);
+          if (!r.active) continue;
+          const int nk = r.k1 - r.k0;
+          if (gi == 1 || gi == 3) {   // operand planes straight into the operand slots
+            const CUtensorMap* map = gi == 1 ? &act_op : &act_hp;
+            for (int j = 0; j < nk; ++j) {
+              const uint32_t b = bt % kMkNB;
+              if (!mk_wait(&bempty[b], ((bt / kMkNB) & 1) ^ 1, a.err, 41)) {
+                ok = false;
+                break;
+              }
+              fence_proxy_async_smem();
+              mbar_arrive_expect_tx(&bfullt[b], kMkBBytes);
+              tma_load_2d(sB + b * kMkBBytes, map, &bfullt[b], (r.k0 + j) * 64, 0, pol);
+              bout |= 1u << b;
+              pt ^= 1u << b;
+              ++bt;
+            }
+          } else {                    // fp32 tiles of x into the staging slots
+            for (int j = 0; j < nk; ++j) {
+              const int bi = j % kMkNS;
+              if (sfill[bi] > 0 && !mk_wait(&sempty[bi], (sfill[bi] - 1) & 1, a.err, 42)) {
+                ok = false;
+                break;
+              }
+              fence_proxy_async_smem();   // the math warps' reads of the tile precede the copy
+              mbar_arrive_expect_tx(&sfull[bi], kMkTile32);
+              tma_load_2d(sS + bi * kMkTile32, &act_x, &sfull[bi], (r.k0 + j) * 64, 0, pol);
+              ++sfill[bi];
+            }
+            bt += nk;
+          }
+        }
+      // never leave a copy in flight: the last fill of every staging tile and
+      // every operand copy have landed
+      for (int i = 0; i < kMkNS; ++i)
+        if (sfill[i] > 0) mbar_wait(&sfull[i], (sfill[i] - 1) & 1, nullptr, 0);
+      for (int i = 0; i < kMkNB; ++i)
+        if ((bout >> i) & 1u) mbar_wait(&bfullt[i], ((pt >> i) & 1u) ^ 1u, nullptr, 0);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    // ---------------- math warps ----------------
+    MkMath s;
+    s.sB = sB;
+    s.sS = sS;
+    s.bfull = bfull;
+    s.bempty = bempty;
+    s.sfull = sfull;
+    s.sempty = sempty;
+    s.accfull = accfull;
+    s.go = go;
+    s.tmem = tmem;
+    s.bt = s.gc = 0;
+    s.sph = 0;
+    s.mt = threadIdx.x - 128;
+    const int mt = s.mt;
+    const unsigned G = gridDim.x;
+    unsigned nbar = 0;
+    const float invD = 1.f / (float)a.D;
+    const int kvd = a.Hkv * DH;
+    for (int l = a.l0; l < a.l1; ++l) {
+      float* ss1 = a.ss + (size_t)l * 128;
+      float* ss2 = ss1 + 64;
+      __nv_bfloat16* kc = a.kv + (size_t)(l - a.l0) * a.kv_stride;
+      __nv_bfloat16* vc = kc + (size_t)a.T_kv * kvd;
+      unsigned long long* tr =
+          (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * gridDim.x + blockIdx.x) * 64 : nullptr;
+      mk_mark(tr, 0);
+      // phases: 0 QKV, 1 q / own k, v, 2 attention, 3 combine, 4 O, 5 gate/up,
+      // 6 GeGLU planes, 7 down; a grid barrier before each (the first one of a
+      // launch has none)
+      for (int ph = 0; ph < 8; ++ph) {
+        if (ph > 0 || l > a.l0) mk_grid_sync(a.bar, ++nbar * G, a.err, mt);
+        const bool proj = ph == 0 || ph == 4 || ph == 5 || ph == 7;
+        if (proj && mt == 0) mbar_arrive(go);   // the loader may fetch this phase's operand
+        mk_mark(tr, 2 * ph + 1);
+        if (ph == 1) {
+          mk_qkv_finalize<DH>(a, a.g[0].splits, ss1, kc, vc, invD, mt);
+        } else if (ph == 2) {
+          mk_attention<DH>(a, kc, vc, sR, mt, tr);
+        } else if (ph == 3) {
+          mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR));
+        } else if (ph == 6) {
+          mk_geglu_planes(a, a.g[2].splits, ss2, invD, mt);
+        } else {
+          const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
+          float* out = ph == 0 ? a.qkv : ph == 5 ? a.gu : a.x;
+          const int ld = ph == 0 ? a.nqkv : ph == 5 ? 2 * a.F : a.D;
+          float* stats = ph == 0 ? ss1 : ph == 5 ? ss2 : nullptr;
+          const size_t slab = ph == 0 ? (size_t)64 * a.nqkv : ph == 5 ? (size_t)64 * 2 * a.F : 0;
+          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5, stats, out, ld, slab, a.T_q, a.err,
+                       tr ? tr + 20 + 4 * gi : nullptr);
+        }
+        mk_mark(tr, 2 * ph + 2);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace lat

@@ -10,10 +10,12 @@
 //  * A operand = a 128 x 64 tile of the K-major weight matrix, moved by TMA
 //    (128-byte swizzle) through a ring of STAGES shared-memory slots with an
 //    L2 evict-first hint (weights are read once per step).
-//  * B operand = the activation, prepared once per GEMM by a separate prep
-//    kernel as three bf16 planes (hi, mid, lo: 24 significant bits) stacked as
-//    192 K-major rows [3][64 tokens][K]; its 192 x 64 tile of the same K range
-//    arrives by TMA in the same stage.
+//  * B operand = the activation, written by the kernel that produces it as
+//    three bf16 planes (hi, mid, lo: 24 significant bits) stacked as 192
+//    K-major rows [3][64 tokens][K]; its 192 x 64 tile of the same K range
+//    arrives by TMA in the same stage.  (The action expert's blocks run in the
+//    persistent step kernel; this kernel serves the embedding projection and
+//    the standalone weight-streaming measurement.)
 //  * One tcgen05.mma per 16-wide K step: M = 128 features, N = 192, fp32
 //    accumulator in TMEM.  The epilogue adds the three terms of each token and
 //    reduces split-K partial sums with fp32 atomics.
@@ -168,31 +170,6 @@ __global__ void __launch_bounds__(192, 1) skinny_gemm_kernel(const __grid_consta
   }
 }
 
-// ---------------------------------------------------------------------------
-// Activation preparation: three bf16 planes of a [<=64][K] fp32 activation,
-// planes[t * 64 + row][k] (t = hi, mid, lo), rows beyond n_tok never written
-// (kept zero).  Modes:
-//   PREP_PLAIN: a = src[row][k]                      (+ optional RMS statistics)
-//   PREP_GEGLU: a = GELU(r g) * (r u), g = src[row][k], u = src[row][off + k],
-//               r = row_scale[row]
-//   PREP_SILU:  a = SiLU(src[row][k])
-// Grid (ceil(K / 256), n_tok), blockDim 256; with stats, CTAs of grid column 0
-// also write stat_out[row] = rsqrt(mean(src[row]^2) + eps) over K.
-// ---------------------------------------------------------------------------
-enum PrepMode : int { PREP_PLAIN = 0, PREP_GEGLU = 1, PREP_SILU = 2 };
-
-struct PrepArgs {
-  const float* src;
-  int ld;
-  int K;
-  int mode;
-  int off;
-  const float* row_scale;
-  __nv_bfloat16* planes;   // [3 * 64][K]
-  float* stat_out;
-  float eps;
-};
-
 // tanh from the exponential (no cancellation concern here: the callers use
 // 1 + tanh), accurate to a few fp32 ulps of 1
 __device__ __forceinline__ float gelu_tanh_fast(float x) {
@@ -201,39 +178,6 @@ __device__ __forceinline__ float gelu_tanh_fast(float x) {
   const float e = __expf(2.f * y);
   const float t = 1.f - 2.f / (1.f + e);
   return 0.5f * x * (1.f + t);
-}
-
-static __global__ void __launch_bounds__(256) prep_planes_kernel(PrepArgs a) {
-  griddep_launch();
-  griddep_wait();
-  const int row = blockIdx.y;
-  const int k = blockIdx.x * 256 + threadIdx.x;
-  const float* sr = a.src + (size_t)row * a.ld;
-  if (a.stat_out && blockIdx.x == 0) {
-    __shared__ float red[8];
-    float ss = 0.f;
-    for (int j = threadIdx.x; j < a.K; j += 256) ss += sr[j] * sr[j];
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float s = 0.f;
-      for (int w = 0; w < 8; ++w) s += red[w];
-      a.stat_out[row] = rsqrtf(s / a.K + a.eps);
-    }
-  }
-  if (k >= a.K) return;
-  float v = sr[k];
-  if (a.mode == PREP_GEGLU) {
-    const float r = a.row_scale[row];
-    v = gelu_tanh_fast(r * v) * (r * sr[a.off + k]);
-  } else if (a.mode == PREP_SILU) {
-    v = silu(v);
-  }
-  const Split3 t = split3(v);
-  a.planes[(size_t)row * a.K + k] = t.hi;
-  a.planes[(size_t)(64 + row) * a.K + k] = t.mid;
-  a.planes[(size_t)(128 + row) * a.K + k] = t.lo;
 }
 
 }  // namespace lat

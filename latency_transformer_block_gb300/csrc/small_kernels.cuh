@@ -15,104 +15,6 @@ __host__ __device__ __forceinline__ int ring_slot_of(int chunk, int n_hist) { re
 __host__ __device__ __forceinline__ long long chunk_pos0(int chunk, int T) { return (long long)chunk * T; }
 
 
-// ---------------------------------------------------------------------------
-// QKV epilogue (runs once the split-K sums are complete):
-//   y = r1[t] * acc[t]              (RMS row factor applied after the GEMM)
-//   q = RoPE(y_q), k = RoPE(y_k), v = y_v
-//   q -> fp32 q buffer; k, v -> bf16 into the cache at slot (slot0 + t)
-// then zero the consumed accumulator row and the FFN accumulator row.
-// Rotate-half RoPE with cos/sin tables [T_q][dh/2] (fp32, from float64).
-// ---------------------------------------------------------------------------
-struct QkvEpiArgs {
-  float* acc;                // fp32 [T_q][nqkv] (zeroed after reading)
-  int nqkv;
-  const float* r1;           // [T_q]
-  const float* cos_t;        // [T_q][dh/2]
-  const float* sin_t;
-  float* q;                  // fp32 [T_q][Hq*dh]
-  __nv_bfloat16* k_cache;    // plane K of this layer, row stride kv_ld
-  __nv_bfloat16* v_cache;
-  int kv_ld;
-  int slot0;
-  int Hq, Hkv, dh;
-  float* zero2;              // optional: second buffer row to clear, [T_q][zero2_ld]
-  int zero2_ld;
-  float* k32;                // fp32 own K (after RoPE) and V as computed, [T_q][Hkv*dh]
-  float* v32;
-};
-
-// Work items of one row: groups of 4 rotate-half pairs of the q heads, then of
-// the k heads, then groups of 4 v values; each thread takes one item, loads
-// it, zeroes what it read, and writes its results.  Grid (T_q, ceil(items /
-// 128)), blockDim 128; dh / 2 is a multiple of 4.
-__host__ __device__ __forceinline__ int qkv_epi_items(int Hq, int Hkv, int dh) {
-  return (Hq + Hkv) * (dh / 8) + Hkv * (dh / 4);
-}
-
-static __global__ void __launch_bounds__(128) qkv_epilogue_kernel(QkvEpiArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int t = blockIdx.x;
-  const int half = a.dh / 2, g4 = half / 4;
-  const int n_rot = (a.Hq + a.Hkv) * g4;
-  const int item = blockIdx.y * 128 + threadIdx.x;
-  float* row = a.acc + (size_t)t * a.nqkv;
-  if (item < n_rot) {
-    const bool isq = item < a.Hq * g4;
-    const int it = isq ? item : item - a.Hq * g4;
-    const int head = it / g4, i = (it % g4) * 4;
-    const int base = (isq ? 0 : a.Hq * a.dh) + head * a.dh;
-    const float r = a.r1[t];
-    float4* p0 = reinterpret_cast<float4*>(row + base + i);
-    float4* p1 = reinterpret_cast<float4*>(row + base + i + half);
-    const float4 x0 = __ldcg(p0), x1 = __ldcg(p1);
-    const float4 c = *reinterpret_cast<const float4*>(a.cos_t + (size_t)t * half + i);
-    const float4 sn = *reinterpret_cast<const float4*>(a.sin_t + (size_t)t * half + i);
-    __stcg(p0, make_float4(0.f, 0.f, 0.f, 0.f));
-    __stcg(p1, make_float4(0.f, 0.f, 0.f, 0.f));
-    const float a0[4] = {r * x0.x, r * x0.y, r * x0.z, r * x0.w};
-    const float a1[4] = {r * x1.x, r * x1.y, r * x1.z, r * x1.w};
-    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
-    float y0[4], y1[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      y0[e] = a0[e] * cc[e] - a1[e] * ss[e];
-      y1[e] = a1[e] * cc[e] + a0[e] * ss[e];
-    }
-    if (isq) {
-      float* q = a.q + (size_t)t * a.Hq * a.dh + head * a.dh + i;
-      *reinterpret_cast<float4*>(q) = make_float4(y0[0], y0[1], y0[2], y0[3]);
-      *reinterpret_cast<float4*>(q + half) = make_float4(y1[0], y1[1], y1[2], y1[3]);
-    } else {
-      __nv_bfloat16* kr = a.k_cache + (size_t)query_slot(a.slot0, t) * a.kv_ld + head * a.dh + i;
-      *reinterpret_cast<uint2*>(kr) = make_uint2(pack_bf16(__float2bfloat16_rn(y0[0]), __float2bfloat16_rn(y0[1])),
-                                                 pack_bf16(__float2bfloat16_rn(y0[2]), __float2bfloat16_rn(y0[3])));
-      *reinterpret_cast<uint2*>(kr + half) =
-          make_uint2(pack_bf16(__float2bfloat16_rn(y1[0]), __float2bfloat16_rn(y1[1])),
-                     pack_bf16(__float2bfloat16_rn(y1[2]), __float2bfloat16_rn(y1[3])));
-      float* k32 = a.k32 + (size_t)t * a.Hkv * a.dh + head * a.dh + i;
-      *reinterpret_cast<float4*>(k32) = make_float4(y0[0], y0[1], y0[2], y0[3]);
-      *reinterpret_cast<float4*>(k32 + half) = make_float4(y1[0], y1[1], y1[2], y1[3]);
-    }
-  } else if (item < qkv_epi_items(a.Hq, a.Hkv, a.dh)) {
-    const int j = (item - n_rot) * 4;
-    const float r = a.r1[t];
-    float4* p = reinterpret_cast<float4*>(row + (a.Hq + a.Hkv) * a.dh + j);
-    const float4 x = __ldcg(p);
-    __stcg(p, make_float4(0.f, 0.f, 0.f, 0.f));
-    const float y[4] = {r * x.x, r * x.y, r * x.z, r * x.w};
-    __nv_bfloat16* vr = a.v_cache + (size_t)query_slot(a.slot0, t) * a.kv_ld + j;
-    *reinterpret_cast<uint2*>(vr) = make_uint2(pack_bf16(__float2bfloat16_rn(y[0]), __float2bfloat16_rn(y[1])),
-                                               pack_bf16(__float2bfloat16_rn(y[2]), __float2bfloat16_rn(y[3])));
-    *reinterpret_cast<float4*>(a.v32 + (size_t)t * a.Hkv * a.dh + j) = make_float4(y[0], y[1], y[2], y[3]);
-  }
-  if (a.zero2) {   // this CTA's share of the row of the second buffer
-    const int per = (a.zero2_ld / 4 + gridDim.y - 1) / gridDim.y;
-    float4* z = reinterpret_cast<float4*>(a.zero2 + (size_t)t * a.zero2_ld);
-    for (int k = blockIdx.y * per + threadIdx.x; k < min(a.zero2_ld / 4, (int)(blockIdx.y + 1) * per); k += 128)
-      z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Embedding prologue of one denoise step (folded form, section 4.2 of the note):

@@ -81,6 +81,8 @@ def lib():
         L.lat_debug_dense_gemm.restype = st
         L.lat_debug_clear.argtypes = [_P, _P]
         L.lat_debug_clear.restype = st
+        L.lat_debug_trace.argtypes = [_P, _P, ctypes.c_longlong]
+        L.lat_debug_trace.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -165,6 +167,11 @@ class Context:
 
     def debug_clear(self, stream=None):
         check(lib().lat_debug_clear(self.handle, stream_ptr(stream)))
+
+    def debug_trace(self, buf=None):
+        """Record phase timestamps of the step kernel into `buf` (int64 device tensor), or stop (None)."""
+        check(lib().lat_debug_trace(self.handle, ptr(buf) if buf is not None else None,
+                                    buf.numel() if buf is not None else 0))
 
     def sync(self):
         check(lib().lat_sync(self.handle))
