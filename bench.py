@@ -28,6 +28,9 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD = "pi0_ae"
 PAGES_AE_MS = 11.001   # pages' action-expert time, 2 views, RTX 4090 (context)
+# DRAM bytes (read + write) of one step-kernel launch from the ncu capture in
+# profiles/pi0_step_kernel_pi0_ae.md; None when the kernel changed since then
+STEP_TRAFFIC = None
 
 
 def parse():
@@ -37,7 +40,21 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD] + list(DENSE_WORKLOADS),
+                   help="pi0_ae (default: the headline line) or one dense configuration")
     return p.parse_args()
+
+
+# dense configurations (parity cases of the dense path; timed on request):
+# name -> (config, batch, metric, unit)
+DENSE_WORKLOADS = {
+    "prefill_b1": ("prefill", 1, "ms per prefix prefill", "ms"),
+    "prefill_b8": ("prefill", 8, "ms per prefix prefill", "ms"),
+    "dit_1p3b": ("dit_1p3b", 4, "ms per denoised chunk", "ms"),
+    "dit_14b_n1": ("dit_14b", 1, "us per block", "us"),
+    "dit_14b_n4": ("dit_14b", 4, "us per block", "us"),
+    "dit_14b_n8": ("dit_14b", 8, "us per block", "us"),
+}
 
 
 def dist_info():
@@ -272,31 +289,27 @@ def run_ours(args):
         host_ms = (time.perf_counter() - t0) * 1e3
     e2e_ms = reduce_max(max(ee0.elapsed_time(ee1), host_ms)) / args.steps
 
-    # --- dominant kernel alone: the weight-streaming GEMM, gate/up projection ---
+    # --- dominant kernel alone: the persistent step kernel (all blocks of one
+    #     denoise step), timed back to back with events on its stream ---
     peak_gbs, peak_tf, peak_src = measured_peaks()
-    F, D = cfg["F"], cfg["D"]
-    kernels = {}
-    names = {0: ("qkv", D * (cfg["Hq"] + 2 * cfg["Hkv"]) * cfg["dh"]), 1: ("o", cfg["Hq"] * cfg["dh"] * D),
-             2: ("gate_up", D * 2 * F), 3: ("down", F * D)}
-    reps = 3 * cfg["L"]
-    with torch.cuda.stream(stream):
-        for which, (nm, nw) in names.items():
-            m.ctx.debug_gemm(which, 0, 5, stream)
-            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            k0.record(stream)
-            m.ctx.debug_gemm(which, 0, reps, stream)
-            k1.record(stream)
-            stream.synchronize()
-            us = k0.elapsed_time(k1) * 1e3 / reps
-            kernels[nm] = {"us": round(us, 2), "weight_bytes": 2 * nw, "gbs": round(2 * nw / us / 1e3, 1)}
-        m.ctx.debug_clear(stream)
-    m.ctx.sync()
-    dom = kernels["gate_up"]
     w_block, kv_block, bytes_chunk = algorithmic_bytes(cfg)
     mac_block, mac_chunk = macs(cfg)
+    step_bytes = cfg["L"] * (w_block + kv_block)       # weights + KV read once per block
+    reps = 20
+    with torch.cuda.stream(stream):
+        m.ctx.debug_step(kv, 3, stream)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        m.ctx.debug_step(kv, reps, stream)
+        k1.record(stream)
+        stream.synchronize()
+    m.ctx.sync()
+    step_us = k0.elapsed_time(k1) * 1e3 / reps
+    step_gbs = step_bytes / step_us / 1e3
     path_gbs = bytes_chunk / (ms_per_step * 1e-3) / 1e9
-    nsplit = (cfg["T_prefix"] + cfg["T_q"] + 63) // 64
-    launches_per_chunk = 1 + cfg["S"] * (3 + cfg["L"] * (6 + (1 if nsplit > 1 else 0)))
+    # our kernels per chunk: state token, then per denoise step embedding
+    # prologue, W2 projection, the step kernel and head + Euler
+    launches_per_chunk = 1 + cfg["S"] * 4
 
     line = {
         "metric": "ms per denoised chunk", "value": round(value, 4), "unit": "ms", "n_gpus": world,
@@ -312,10 +325,11 @@ def run_ours(args):
                    "path_roofline_ms": round(bytes_chunk / (peak_gbs * 1e9) * 1e3, 4),
                    "path_hbm_gbs": round(path_gbs, 1), "path_frac": round(path_gbs / peak_gbs, 4),
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "skinny_gemm (gate/up projection, 64 tokens x 1024 -> 8192)",
-                     "achieved": dom["gbs"], "peak": peak_gbs, "unit": "GB/s",
-                     "frac": round(dom["gbs"] / peak_gbs, 4), "traffic": None,
-                     "peak_source": f"{peak_src} hbm_gbs (burst copy)", "kernels": kernels},
+        "roofline": {"bound": "hbm", "kernel": "pi0_step_kernel (18 blocks of one denoise step, one launch)",
+                     "achieved": round(step_gbs, 1), "peak": peak_gbs, "unit": "GB/s",
+                     "frac": round(step_gbs / peak_gbs, 4), "traffic": STEP_TRAFFIC,
+                     "algorithmic_bytes": step_bytes, "us_per_launch": round(step_us, 2),
+                     "peak_source": f"{peak_src} hbm_gbs (burst copy)"},
         "clocks": clk,
         "e2e": {"value": round(e2e_ms, 4), "unit": "ms",
                 "h2d_bytes_per_step": int(h_noise.numel() * 4 + h_state.numel() * 4),
@@ -330,10 +344,133 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def dense_flops(cfg, nb, descs=None):
+    """Useful FLOPs of one step of a dense workload (2 per multiply-add): the
+    method's projections and its dense attention; for the prefix model the last
+    layer computes K and V only."""
+    D, F, Hq, Hkv, dh, L = cfg["D"], cfg["F"], cfg["Hq"], cfg.get("Hkv", cfg["Hq"]), cfg["dh"], cfg["L"]
+    if cfg["kind"] == "prefill":
+        tok = nb * cfg["T_prefix"]
+        qd, kvd = Hq * dh, Hkv * dh
+        proj = D * (qd + 2 * kvd) + qd * D + D * 2 * F + F * D
+        attn = 2 * nb * Hq * cfg["T_prefix"] * cfg["T_prefix"] * dh
+        macs = tok * cfg["patch_dim"] * D + (L - 1) * (tok * proj + attn) + tok * D * 2 * kvd
+        return 2 * macs
+    T, nh = cfg["T_chunk"], cfg["n_hist"]
+    per_chunk_proj = T * (D * 3 * D + D * D + D * F + F * D)
+    macs = 0
+    for (_, c, _) in descs:
+        macs += per_chunk_proj + 2 * T * T * (1 + min(c, nh)) * D
+    return 2 * macs * L
+
+
+def run_dense(args):
+    import torch
+    rank, local_rank, world = dist_info()
+    if rank != 0:
+        return
+    name, nb, metric, unit = DENSE_WORKLOADS[args.workload]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from latency_transformer_block_gb300 import build as B
+    B.build()
+    from latency_transformer_block_gb300 import synth
+    from latency_transformer_block_gb300.models import DitStage, Pi0Prefix
+
+    cfg = synth.config(name)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    stream = torch.cuda.Stream(dev)
+    if cfg["kind"] == "prefill":
+        m = Pi0Prefix(cfg, synth.prefill_weights(cfg, 0), max_batch=nb, device=dev)
+        pe = torch.randn(nb, cfg["T_prefix"], cfg["patch_dim"], generator=gen, device=dev).to(torch.bfloat16)
+        kv = m.new_kv(nb)
+        flops = dense_flops(cfg, nb)
+        rows = nb * cfg["T_prefix"]
+        ffn_n, ffn_k = 2 * cfg["F"], cfg["D"]
+
+        def step():
+            m.prefill(pe, kv, stream)
+        blocks = cfg["L"]
+    else:
+        descs = synth.dit_chunk_descs(cfg, nb)
+        streams = (nb + cfg["S"] - 1) // cfg["S"]
+        m = DitStage(cfg, synth.dit_weights(cfg, 0), max_batch=nb, n_streams=streams, device=dev)
+        ring = torch.randn(streams, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
+                           generator=gen, device=dev).to(torch.bfloat16)
+        x = torch.randn(nb, cfg["T_chunk"], cfg["D"], generator=gen, device=dev)
+        cfg["Hkv"] = cfg["H"]
+        cfg["Hq"] = cfg["H"]
+        flops = dense_flops(cfg, nb, descs)
+        rows = nb * cfg["T_chunk"]
+        ffn_n, ffn_k = cfg["F"], cfg["D"]
+
+        def step():
+            for l in range(cfg["L"]):
+                m.block(l, x, descs, ring, stream)
+        blocks = cfg["L"]
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    m.ctx.sync()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    m.ctx.sync()
+    ms = e0.elapsed_time(e1) / args.steps
+    peak_gbs, peak_tf, peak_src = measured_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    # dominant kernel alone: the dense tcgen05 GEMM on the FFN-in projection,
+    # three bf16 planes of the activation (the executed tensor work is 3x useful)
+    act = torch.randn(rows, 3 * ffn_k, generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty(rows, ffn_n, device=dev, dtype=torch.float32)
+    reps = 10
+    with torch.cuda.stream(stream):
+        m.ctx.debug_dense_gemm(2, 0, act, rows, 3, out, stream)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(reps):
+            m.ctx.debug_dense_gemm(2, 0, act, rows, 3, out, stream)
+        k1.record(stream)
+    stream.synchronize()
+    m.ctx.sync()
+    g_us = k0.elapsed_time(k1) * 1e3 / reps
+    g_useful = 2.0 * rows * ffn_n * ffn_k / (g_us * 1e-6) / 1e12
+    value = ms if unit == "ms" else ms * 1e3 / blocks
+    line = {
+        "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs and history, N(0,0.02) bf16 weights)",
+        "config": {"workload": args.workload, "batch": nb, "blocks": blocks,
+                   "us_per_block": round(ms * 1e3 / blocks, 2), "useful_tflop_per_step": round(flops / 1e12, 3),
+                   "path_tflops": round(tflops, 1), "path_frac": round(tflops / peak_tf, 4),
+                   "l2": "inputs larger than L2 (weights and KV streamed per step)"},
+        "roofline": {"bound": "tensor", "kernel": "dense_gemm_kernel (FFN-in projection, M = %d, three planes)" % rows,
+                     "achieved": round(g_useful, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(g_useful / peak_tf, 4), "executed_frac": round(3 * g_useful / peak_tf, 4),
+                     "traffic": None, "us_per_launch": round(g_us, 1),
+                     "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS)"},
+        "clocks": clk, "e2e": None, "gpu_launches": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != WORKLOAD:
+        run_dense(args)
     else:
         run_ours(args)
 

@@ -219,6 +219,17 @@ lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *st
 lat_status lat_debug_clear(lat_ctx *ctx, void *stream);
 
 /*
+ * lat_debug_step -- measurement hook for the action expert: enqueue `reps`
+ * launches of the persistent step kernel (all L blocks of one denoise step,
+ * each launch preceded by the clear of its barrier counter and statistics) on
+ * the context's own residual stream, with the caller's cache `kv` (device,
+ * [L][2][T_prefix + T_q][Hkv dh] bf16; own-token slots are overwritten).  Used
+ * to time the kernel alone with events on `stream`; the residual stream is left
+ * with meaningless values (the next lat_denoise_chunk overwrites it).
+ */
+lat_status lat_debug_step(lat_ctx *ctx, void *kv, int reps, void *stream);
+
+/*
  * lat_debug_trace -- measurement hook for the action expert's persistent step
  * kernel: with buf != NULL (device, caller-owned, 8-byte aligned, at least
  * num_SMs * L * 64 entries) later launches record %globaltimer nanoseconds at

@@ -265,7 +265,7 @@ static lat_status check_desc(const lat_model_desc* d) {
   if (!(d->eps > 0.f) || !(d->rope_base > 1.f)) return fail(LAT_ERR_ARG, "eps / rope_base out of range");
   if (d->F <= 0) return fail(LAT_ERR_SHAPE, "F must be positive");
   if (d->kind == LAT_PI0_ACTION_EXPERT) {
-    if (d->D <= 0 || d->D % 128) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 128");
+    if (d->D <= 0 || d->D % 128 || d->D > 8192) return fail(LAT_ERR_SHAPE, "D must be a multiple of 128 in [128, 8192]");
     if (d->dh != 64 && d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 64, 128 or 256");
     if (((d->Hq + 2 * d->Hkv) * d->dh) % 128) return fail(LAT_ERR_SHAPE, "(Hq + 2 Hkv) dh must be a multiple of 128");
     if ((d->Hq * d->dh) % 64) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 64");
@@ -628,7 +628,7 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
     }
     LAT_TRY(enqueue_pi0_step(c, 0, d.L, kv, (long long)layer_elems, st));
     HeadArgs h{c->xres, c->wout, c->bout, x, c->dt, s, D, A, d.eps};
-    PDL_TRY("head_euler", launch_pdl(head_euler_kernel, dim3(T - 1), dim3(256), 0, st, h));
+    PDL_TRY("head_euler", launch_pdl(head_euler_kernel, dim3(T - 1), dim3(256), (size_t)D * 4, st, h));
   }
   return LAT_OK;
 }
@@ -1233,6 +1233,18 @@ lat_status lat_debug_dense_gemm(lat_ctx* c, int which, int layer, const void* ac
   a.M = M; a.N = N[which]; a.K = K[which]; a.terms = terms; a.w_row0 = layer * N[which];
   a.epi = E_STORE; a.out = out; a.ldo = N[which];
   return enqueue_dense(c, amap, *wm[which], a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lat_status lat_debug_step(lat_ctx* c, void* kv, int reps, void* stream) {
+  if (!c || !kv) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "step kernel: action-expert contexts only");
+  if (reps < 1) return fail(LAT_ERR_ARG, "reps must be positive");
+  if (!aligned16(kv)) return fail(LAT_ERR_ALIGN, "kv not 16-byte aligned");
+  const size_t layer_elems = (size_t)2 * (c->d.T_prefix + c->d.T_q) * c->d.Hkv * c->d.dh;
+  for (int r = 0; r < reps; ++r)
+    LAT_TRY(enqueue_pi0_step(c, 0, c->d.L, reinterpret_cast<bf16*>(kv), (long long)layer_elems,
+                             reinterpret_cast<cudaStream_t>(stream)));
+  return LAT_OK;
 }
 
 lat_status lat_debug_trace(lat_ctx* c, unsigned long long* buf, long long n) {

@@ -59,7 +59,8 @@ static __global__ void embed_prologue_kernel(EmbedArgs a) {
 // Head + Euler update: for action row t (residual row 1 + t)
 //   v[t][a] = r * sum_n h[1+t][n] W'out[n][a] + b_out[a],  r = RMS factor
 //   x[t][a] += dt * v[t][a]
-// W'out = diag(g_final) W_out in fp32.  Grid T_q - 1, blockDim 256.
+// W'out = diag(g_final) W_out in fp32.  Grid T_q - 1, blockDim 256, dynamic
+// shared memory D floats (the row).
 // ---------------------------------------------------------------------------
 struct HeadArgs {
   const float* xres;     // [T_q][D]
@@ -71,37 +72,56 @@ struct HeadArgs {
   float eps;
 };
 
-static __global__ void head_euler_kernel(HeadArgs a) {
+static __global__ void __launch_bounds__(256) head_euler_kernel(HeadArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const float* h = a.xres + (size_t)(1 + t) * a.D;
+  extern __shared__ float sh[];   // the row h [D]
   __shared__ float red[8][33];
   __shared__ float rs;
-  // RMS factor
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < a.D; n += blockDim.x) ss += h[n] * h[n];
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // RMS factor (and the row into shared memory)
+  float ss = 0.f;
+  for (int n = threadIdx.x; n < a.D; n += 256) {
+    const float v = h[n];
+    sh[n] = v;
+    ss += v * v;
+  }
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[warp][32] = ss;
   __syncthreads();
   if (threadIdx.x == 0) {
     float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][32];
+    for (int w = 0; w < 8; ++w) s += red[w][32];
     rs = rsqrtf(s / a.D + a.eps);
   }
   __syncthreads();
-  // A outputs: thread (warp w, lane l) accumulates column l over rows n = w, w+8, ...
+  // A outputs: thread (warp w, lane l) accumulates column l over rows n = w,
+  // w + 8, ...; 16 rows per pass with their weight loads in flight together
   for (int a0 = 0; a0 < a.A; a0 += 32) {
     const int col = a0 + lane;
     float acc = 0.f;
-    if (col < a.A)
-      for (int n = warp; n < a.D; n += (int)(blockDim.x >> 5)) acc = fmaf(h[n], a.wout[(size_t)n * a.A + col], acc);
+    if (col < a.A) {
+      for (int n0 = warp; n0 < a.D; n0 += 8 * 16) {
+        float wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = n0 + 8 * i;
+          wv[i] = n < a.D ? __ldg(a.wout + (size_t)n * a.A + col) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = n0 + 8 * i;
+          if (n < a.D) acc = fmaf(sh[n], wv[i], acc);
+        }
+      }
+    }
     red[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && col < a.A) {
       float s = 0.f;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][lane];
+      for (int w = 0; w < 8; ++w) s += red[w][lane];
       const float v = rs * s + a.bout[col];
       a.x[(size_t)t * a.A + col] += a.dt[a.step] * v;
     }

@@ -81,6 +81,8 @@ def lib():
         L.lat_debug_dense_gemm.restype = st
         L.lat_debug_clear.argtypes = [_P, _P]
         L.lat_debug_clear.restype = st
+        L.lat_debug_step.argtypes = [_P, _P, ctypes.c_int, _P]
+        L.lat_debug_step.restype = st
         L.lat_debug_trace.argtypes = [_P, _P, ctypes.c_longlong]
         L.lat_debug_trace.restype = st
         L.lat_sync.argtypes = [_P]
@@ -167,6 +169,9 @@ class Context:
 
     def debug_clear(self, stream=None):
         check(lib().lat_debug_clear(self.handle, stream_ptr(stream)))
+
+    def debug_step(self, kv, reps, stream=None):
+        check(lib().lat_debug_step(self.handle, ptr(kv), reps, stream_ptr(stream)))
 
     def debug_trace(self, buf=None):
         """Record phase timestamps of the step kernel into `buf` (int64 device tensor), or stop (None)."""
