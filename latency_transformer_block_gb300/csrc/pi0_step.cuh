@@ -309,6 +309,26 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool st
   mk_mark(tr, 3);
 }
 
+// Sum of `n` partial slabs (slab elements apart) of 4 consecutive floats, in
+// slab order; the loads of up to 8 slabs are in flight together.
+__device__ __forceinline__ float4 sum_slabs(const float* p, size_t slab, int n) {
+  float4 y[8];
+#pragma unroll
+  for (int sp = 0; sp < 8; ++sp)
+    y[sp] = sp < n ? __ldcg(reinterpret_cast<const float4*>(p + sp * slab)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 x = y[0];
+#pragma unroll
+  for (int sp = 1; sp < 8; ++sp)
+    if (sp < n) {
+      x.x += y[sp].x; x.y += y[sp].y; x.z += y[sp].z; x.w += y[sp].w;
+    }
+  for (int sp = 8; sp < n; ++sp) {
+    const float4 z = __ldcg(reinterpret_cast<const float4*>(p + sp * slab));
+    x.x += z.x; x.y += z.y; x.z += z.z; x.w += z.w;
+  }
+  return x;
+}
+
 // Phase 2: q, own k and own v of the block, once per element: the sum of the
 // QKV partial slabs times r = rsqrt(mean(x^2) + eps), RoPE (rotate-half pairs
 // (i, i + dh/2)) on q and k, then two-term bf16 splits: q -> q_planes, own k/v
@@ -328,14 +348,7 @@ __device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int splits, con
       const int t = it / rot_per_t, rem = it % rot_per_t;
       const int hd = rem / (HD / 4), i = (rem % (HD / 4)) * 4;
       const float* p0 = a.qkv + (size_t)t * a.nqkv + hd * DH + i;
-      float4 x0 = __ldcg(reinterpret_cast<const float4*>(p0));
-      float4 x1 = __ldcg(reinterpret_cast<const float4*>(p0 + HD));
-      for (int sp = 1; sp < splits; ++sp) {
-        const float4 y0 = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab));
-        const float4 y1 = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab + HD));
-        x0.x += y0.x; x0.y += y0.y; x0.z += y0.z; x0.w += y0.w;
-        x1.x += y1.x; x1.y += y1.y; x1.z += y1.z; x1.w += y1.w;
-      }
+      const float4 x0 = sum_slabs(p0, slab, splits), x1 = sum_slabs(p0 + HD, slab, splits);
       const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
       const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)t * HD + i));
       const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)t * HD + i));
@@ -375,11 +388,7 @@ __device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int splits, con
       const int iv = it - n_rot;
       const int t = iv / v_per_t, j = (iv % v_per_t) * 4;
       const float* p0 = a.qkv + (size_t)t * a.nqkv + nh * DH + j;
-      float4 x = __ldcg(reinterpret_cast<const float4*>(p0));
-      for (int sp = 1; sp < splits; ++sp) {
-        const float4 y = __ldcg(reinterpret_cast<const float4*>(p0 + sp * slab));
-        x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-      }
+      float4 x = sum_slabs(p0, slab, splits);
       const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
       x.x *= rv; x.y *= rv; x.z *= rv; x.w *= rv;
       uint32_t hh[2], ll[2];
@@ -635,7 +644,7 @@ __device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc,
 // warp) groups of a chunk the per-row weights 2^(m_s - M) / L go to shared
 // memory first, then each thread merges one fragment over all key blocks.
 template <int DH>
-__device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw) {
+__device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, unsigned long long* tr) {
   constexpr int HD = DH / 2, NT = HD / 8, Q4 = DH / 4;
   constexpr int PER_HW = NT * 32;   // fragments of one (head, warp)
   const int nkb = attn_key_blocks(a.T_kv);
@@ -693,6 +702,7 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw) {
         sw[row * nkb + kb] = valid ? exp2f(__ldcg(a.part_m + (size_t)kb * ml_stride + i0) - M) * il : 0.f;
     }
     named_sync(3, 256);
+    mk_mark(tr, 36);
     // pass 2: one fragment per thread
     const int it = c0 + mt;
     if (it < items) {
@@ -739,6 +749,7 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw) {
       }
     }
     named_sync(3, 256);   // sw is reused by the next chunk
+    mk_mark(tr, 37);
   }
   fence_proxy_async_smem();   // sw's bytes are reused by TMA in the next phase
 }
@@ -754,14 +765,7 @@ __device__ __forceinline__ void mk_geglu_planes(const MkArgs& a, int splits, con
     const int t = (i * 4) / F, j = (i * 4) % F;
     const float rv = rsqrtf(__ldcg(ss2 + t) * invD + a.eps);
     const float* gp = a.gu + (size_t)t * 2 * F + j;
-    float4 g = __ldcg(reinterpret_cast<const float4*>(gp));
-    float4 u = __ldcg(reinterpret_cast<const float4*>(gp + F));
-    for (int sp = 1; sp < splits; ++sp) {
-      const float4 g2 = __ldcg(reinterpret_cast<const float4*>(gp + sp * slab));
-      const float4 u2 = __ldcg(reinterpret_cast<const float4*>(gp + sp * slab + F));
-      g.x += g2.x; g.y += g2.y; g.z += g2.z; g.w += g2.w;
-      u.x += u2.x; u.y += u2.y; u.z += u2.z; u.w += u2.w;
-    }
+    const float4 g = sum_slabs(gp, slab, splits), u = sum_slabs(gp + F, slab, splits);
     const float h0 = gelu_tanh_fast(rv * g.x) * (rv * u.x), h1 = gelu_tanh_fast(rv * g.y) * (rv * u.y);
     const float h2 = gelu_tanh_fast(rv * g.z) * (rv * u.z), h3 = gelu_tanh_fast(rv * g.w) * (rv * u.w);
     uint32_t a0, b0, c0, a1, b1, c1;
@@ -1003,7 +1007,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         } else if (ph == 2) {
           mk_attention<DH>(a, kc, vc, sR, mt, tr);
         } else if (ph == 3) {
-          mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR));
+          mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR), tr);
         } else if (ph == 6) {
           mk_geglu_planes(a, a.g[2].splits, ss2, invD, mt);
         } else {
