@@ -234,9 +234,10 @@ lat_status lat_debug_step(lat_ctx *ctx, void *kv, int reps, void *stream);
  * kernel: with buf != NULL (device, caller-owned, 8-byte aligned, at least
  * num_SMs * L * 64 entries) later launches record %globaltimer nanoseconds at
  * the phase boundaries of every block, buf[(layer * grid + cta) * 64 + event]
- * (events 0..12: block start, after each phase and each grid barrier;
- * 16 + 4 g .. 19 + 4 g for projection g: first activation tile in, operand
- * built, accumulator ready, epilogue issued).  Each launch overwrites the
+ * (event 0: block start; 2p + 1 / 2p + 2: phase p = 0..7 begins (after its grid
+ * barrier) / ends; 17..19 inside the attention phase; 20 + 4 g .. 23 + 4 g for
+ * projection g: first activation tile in, operand built, accumulator ready,
+ * epilogue issued; 36, 37 inside the combine).  Each launch overwrites the
  * entries of its layers.  buf = NULL turns recording off.  Drops the captured
  * denoise graph (the next lat_denoise_chunk re-captures).  LAT_ERR_SHAPE if the
  * buffer is too small.
