@@ -480,7 +480,26 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   const float* q0 = a.q + row0 * a.q_ld + h * DH;
   const float* q1 = a.q + row1 * a.q_ld + h * DH;
 
-  // this warp's Q fragments, split once: [k-step][term][4]
+  // Q fragments as exact three-term splits: for dh <= 128 split once into
+  // registers [k-step][term][4]; for larger dh re-read per k-step
+  constexpr bool QREG = DH <= 128;
+  constexpr int KSQ = QREG ? DH / 16 : 1;
+  uint32_t qf[KSQ][3][4];
+  auto q_frag = [&](int ks, uint32_t (&af)[3][4]) {
+    const int c = ks * 16 + 2 * tq;
+    const float2 x00 = v0 ? *reinterpret_cast<const float2*>(q0 + c) : make_float2(0.f, 0.f);
+    const float2 x10 = v1 ? *reinterpret_cast<const float2*>(q1 + c) : make_float2(0.f, 0.f);
+    const float2 x01 = v0 ? *reinterpret_cast<const float2*>(q0 + c + 8) : make_float2(0.f, 0.f);
+    const float2 x11 = v1 ? *reinterpret_cast<const float2*>(q1 + c + 8) : make_float2(0.f, 0.f);
+    split_pair_exact(x00.x, x00.y, af[0][0], af[1][0], af[2][0]);
+    split_pair_exact(x10.x, x10.y, af[0][1], af[1][1], af[2][1]);
+    split_pair_exact(x01.x, x01.y, af[0][2], af[1][2], af[2][2]);
+    split_pair_exact(x11.x, x11.y, af[0][3], af[1][3], af[2][3]);
+  };
+  if constexpr (QREG) {
+#pragma unroll
+    for (int ks = 0; ks < KSQ; ++ks) q_frag(ks, qf[ks]);
+  }
   float o[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -497,41 +516,34 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
         const int row = idx / (DH / 8), c8 = idx % (DH / 8);
         const int key = kb * KB + row;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        uint4 kk = z, vv = z, kl = z, vl = z;
-        if (key < sg.n) {
-          const size_t o = (size_t)key * a.kv_ld + kvh * DH + c8 * 8;
-          if (f32) {
+        const bool in = key < sg.n;
+        const size_t o = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
+        if (f32) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          uint4 kk = z, vv = z, kl = z, vl = z;
+          if (in) {
             split8_to(sg.k32 + o, kk, kl);
             split8_to(sg.v32 + o, vv, vl);
-          } else {
-            kk = *reinterpret_cast<const uint4*>(sg.k + o);
-            vv = *reinterpret_cast<const uint4*>(sg.v + o);
           }
-        }
-        *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
-        *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
-        if (f32) {
+          *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
+          *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
           *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
           *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
+        } else {   // cache keys: async copies (zero fill past the segment)
+          cp_async16(sK + row * LD + c8 * 8, sg.k + o, in ? 16 : 0);
+          cp_async16(sV + row * LD + c8 * 8, sg.v + o, in ? 16 : 0);
         }
       }
+      cp_async_wait_all();
       __syncthreads();
       float s[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll 2
+#pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
-        const int c = ks * 16 + 2 * tq;
-        const float2 x00 = *reinterpret_cast<const float2*>(q0 + c);
-        const float2 x10 = *reinterpret_cast<const float2*>(q1 + c);
-        const float2 x01 = *reinterpret_cast<const float2*>(q0 + c + 8);
-        const float2 x11 = *reinterpret_cast<const float2*>(q1 + c + 8);
-        uint32_t af[3][4];
-        split_pair(x00.x, x00.y, af[0][0], af[1][0], af[2][0]);
-        split_pair(x10.x, x10.y, af[0][1], af[1][1], af[2][1]);
-        split_pair(x01.x, x01.y, af[0][2], af[1][2], af[2][2]);
-        split_pair(x11.x, x11.y, af[0][3], af[1][3], af[2][3]);
+        uint32_t afl[3][4];
+        if constexpr (!QREG) q_frag(ks, afl);
+        const uint32_t (&af)[3][4] = QREG ? qf[QREG ? ks : 0] : afl;
 #pragma unroll
         for (int jp = 0; jp < 4; ++jp) {
           const int mi = lane >> 3, rr = lane & 7;
@@ -598,10 +610,10 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t pf[3][4];
-        split_pair(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0], pf[2][0]);
-        split_pair(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1], pf[2][1]);
-        split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], pf[0][2], pf[1][2], pf[2][2]);
-        split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], pf[0][3], pf[1][3], pf[2][3]);
+        split_pair_exact(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0], pf[2][0]);
+        split_pair_exact(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1], pf[2][1]);
+        split_pair_exact(s[2 * kk + 1][0], s[2 * kk + 1][1], pf[0][2], pf[1][2], pf[2][2]);
+        split_pair_exact(s[2 * kk + 1][2], s[2 * kk + 1][3], pf[0][3], pf[1][3], pf[2][3]);
 #pragma unroll
         for (int jp = 0; jp < NT / 2; ++jp) {
           const int mi = lane >> 3, rr = lane & 7;
@@ -632,7 +644,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
     const int c = h * DH + j * 8 + 2 * tq;
     if (v0) {
       uint32_t hh, mm, ll;
-      split_pair(o[j][0] * i0, o[j][1] * i0, hh, mm, ll);
+      split_pair_exact(o[j][0] * i0, o[j][1] * i0, hh, mm, ll);
       __nv_bfloat16* p = a.out + row0 * 3 * a.ldh + c;
       *reinterpret_cast<uint32_t*>(p) = hh;
       *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
@@ -640,7 +652,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
     }
     if (v1) {
       uint32_t hh, mm, ll;
-      split_pair(o[j][2] * i1, o[j][3] * i1, hh, mm, ll);
+      split_pair_exact(o[j][2] * i1, o[j][3] * i1, hh, mm, ll);
       __nv_bfloat16* p = a.out + row1 * 3 * a.ldh + c;
       *reinterpret_cast<uint32_t*>(p) = hh;
       *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
