@@ -217,6 +217,20 @@ __device__ __forceinline__ Split3 split3(float a) {
   return s;
 }
 
+// Exact three-term split of a pair of fp32 values by truncation: hi keeps the
+// top 8 significant bits of x, mid the top 8 of what is left, and the rest
+// (at most 8 significant bits) is lo, so x = hi + mid + lo exactly and no
+// conversion instruction is needed (bf16 is the upper half of fp32).
+__device__ __forceinline__ void split_pair_exact(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const uint32_t hx = __float_as_uint(x) & 0xffff0000u, hy = __float_as_uint(y) & 0xffff0000u;
+  const float rx = x - __uint_as_float(hx), ry = y - __uint_as_float(hy);
+  const uint32_t mx = __float_as_uint(rx) & 0xffff0000u, my = __float_as_uint(ry) & 0xffff0000u;
+  const float qx = rx - __uint_as_float(mx), qy = ry - __uint_as_float(my);
+  hi = __byte_perm(hx, hy, 0x7632);
+  mid = __byte_perm(mx, my, 0x7632);
+  lo = __byte_perm(__float_as_uint(qx), __float_as_uint(qy), 0x7632);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 a, __nv_bfloat16 b) {
   return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }

@@ -637,14 +637,15 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
 // ---------------------------------------------------------------------------
 // dense path: prefix prefill and DiT stage
 // ---------------------------------------------------------------------------
-static constexpr int kDStages = 6;
+static constexpr int kDStages = 3;
 // bf16 planes of every dense activation: three terms carry the fp32 value
 static constexpr int kActTerms = 3;
 
 static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, const CUtensorMap& wmap, DenseArgs a,
                                 cudaStream_t st) {
   a.err = c->err;
-  const int grid = ((a.M + 127) / 128) * (a.N / 128);
+  const int tiles = ((a.M + 127) / 128) * (a.N / 128);
+  const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
   dense_gemm_kernel<kDStages><<<grid, 192, dense_smem_bytes(kDStages), st>>>(amap, wmap, a);
   return launch_check("dense_gemm");
 }
