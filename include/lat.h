@@ -240,7 +240,10 @@ lat_status lat_debug_step(lat_ctx *ctx, void *kv, int reps, void *stream);
  * epilogue issued; 36, 37 inside the combine).  Each launch overwrites the
  * entries of its layers.  buf = NULL turns recording off.  Drops the captured
  * denoise graph (the next lat_denoise_chunk re-captures).  LAT_ERR_SHAPE if the
- * buffer is too small.
+ * buffer is too small.  For a LAT_DIT context (dh = 128) later block calls record
+ * the tensor-core attention of CTA (0, 0, 0) instead: buf[(role * 32 + block) * 8
+ * + event] for the first 32 key blocks (role 0 MMA issue, 1 a row thread, 2 a
+ * loader thread), at least 768 entries.
  */
 lat_status lat_debug_trace(lat_ctx *ctx, unsigned long long *buf, long long n);
 

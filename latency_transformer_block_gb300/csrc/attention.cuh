@@ -444,6 +444,7 @@ struct SegAttnArgs {
   float scale_log2;
   __nv_bfloat16* out;        // [groups * T_rows][3 * ldh]
   int ldh;
+  unsigned long long* trace; // null, or per-block timestamps of CTA (0, 0, 0) (tensor-core kernel)
   SegGroup grp[16];
 };
 

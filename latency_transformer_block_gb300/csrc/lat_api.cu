@@ -17,6 +17,7 @@
 
 #include "../../include/lat.h"
 #include "attention.cuh"
+#include "attention_tc.cuh"
 #include "common.cuh"
 #include "dense_gemm.cuh"
 #include "dense_kernels.cuh"
@@ -165,6 +166,8 @@ struct lat_ctx {
   CUtensorMap map_act_d, map_act_o, map_act_f;
   int m_max = 0;
   bf16 *wt1 = nullptr, *bt1 = nullptr, *wt2 = nullptr, *bt2 = nullptr, *wmod = nullptr, *bmod = nullptr;
+
+  unsigned long long* attn_trace = nullptr;   // DiT: timestamps of the attention (measurement hook)
 
   // captured denoise loop
   cudaGraphExec_t gexec = nullptr;
@@ -826,10 +829,13 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
 
 static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, int groups, cudaStream_t st) {
   const int dh = c->d.dh;
+  if (dh == 128) {   // tensor-core attention: one CTA per (head, group, 128 rows)
+    dim3 grid(c->d.Hq, (a.T_rows + 127) / 128, groups);
+    attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, c->err);
+    return launch_check("attention_tc");
+  }
   dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups);
-  const int smem = attn_smem_bytes(dh);
-  if (dh == 128) attention_seg_kernel<128, 3><<<grid, 128, smem, st>>>(a);
-  else attention_seg_kernel<256, 3><<<grid, 128, smem, st>>>(a);
+  attention_seg_kernel<256, 3><<<grid, 128, attn_smem_bytes(dh), st>>>(a);
   return launch_check("attention_seg");
 }
 
@@ -952,6 +958,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   sa.q = c->qbuf; sa.q_ld = D; sa.T_rows = T; sa.Hq = d.Hq; sa.Hkv = d.Hkv; sa.kv_ld = D;
   sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
   sa.out = c->act2; sa.ldh = D;
+  sa.trace = c->attn_trace;
   LAT_TRY(enqueue_attention_seg(c, sa, n, st));
   {
     DenseArgs a{};
@@ -1023,6 +1030,7 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     set_attention_smem_limits();
     cudaFuncSetAttribute(dense_gemm_kernel<kDStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          dense_smem_bytes(kDStages));
+    cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_tc_smem_bytes());
     cudaFuncSetAttribute(pi0_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
     cudaFuncSetAttribute(pi0_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
     cudaFuncSetAttribute(pi0_step_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
@@ -1250,7 +1258,12 @@ lat_status lat_debug_step(lat_ctx* c, void* kv, int reps, void* stream) {
 
 lat_status lat_debug_trace(lat_ctx* c, unsigned long long* buf, long long n) {
   if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
-  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "trace: action-expert contexts only");
+  if (c->d.kind == LAT_DIT) {   // the tensor-core attention of the DiT block: 3 x 32 x 8 entries
+    if (buf && n < 3 * 32 * 8) return fail(LAT_ERR_SHAPE, "trace buffer too small");
+    c->attn_trace = buf;
+    return LAT_OK;
+  }
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "trace: action-expert and DiT contexts only");
   if (buf && n < (long long)c->num_sms * c->d.L * 64) return fail(LAT_ERR_SHAPE, "trace buffer too small");
   if (buf && (reinterpret_cast<uintptr_t>(buf) & 7u)) return fail(LAT_ERR_ALIGN, "trace buffer not 8-byte aligned");
   c->mk.trace = buf;
