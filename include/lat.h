@@ -254,8 +254,9 @@ lat_status lat_debug_trace(lat_ctx *ctx, unsigned long long *buf, long long n);
  * for the folded K-major weight W of block `layer` (which: 0 = merged QKV,
  * 1 = attention output, 2 = FFN in (prefix: gate/up interleaved in tiles of 64
  * gate + 64 up rows), 3 = FFN out).
- *  act: device bf16 [M][terms*K] (terms bf16 planes of one activation);
- *  out: device fp32 [M][N].  1 <= M <= the context's workspace rows, terms 1..3.
+ *  act: device fp16 [M][terms*K] (terms fp16 planes of one activation);
+ *  out: device fp32 [M][N].  1 <= M <= the context's workspace rows, terms 1..2.
+ *  W is held as fp16 = 2^s W (exact) and the result scaled back by 2^-s.
  */
 lat_status lat_debug_dense_gemm(lat_ctx *ctx, int which, int layer, const void *act, int M, int terms,
                                 float *out, void *stream);

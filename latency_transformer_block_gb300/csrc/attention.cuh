@@ -38,7 +38,6 @@ struct AttnArgs {
 };
 
 // 8 fp32 values -> 8 bf16 hi and 8 bf16 lo (two-term split)
-__device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo);
 __device__ __forceinline__ void split8_to(const float* src, uint4& hi, uint4& lo) {
   const float4 a = *reinterpret_cast<const float4*>(src);
   const float4 b = *reinterpret_cast<const float4*>(src + 4);
@@ -77,33 +76,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Round a pair of fp32 values to bf16 (nearest even) in one packed conversion.
-__device__ __forceinline__ uint32_t rn_pair(float x, float y, float& bx, float& by) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  const float2 f = __bfloat1622float2(h);
-  bx = f.x;
-  by = f.y;
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Split a pair of fp32 values into three packed bf16x2 words (each term the
-// nearest bf16 of what is left).
-__device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-  float hx, hy, mx, my, lx, ly;
-  hi = rn_pair(x, y, hx, hy);
-  const float rx = x - hx, ry = y - hy;
-  mid = rn_pair(rx, ry, mx, my);
-  lo = rn_pair(rx - mx, ry - my, lx, ly);
-}
-
-// Split a pair of fp32 values into two packed bf16x2 words (hi, lo): the pair
-// is carried to about 2^-17 relative.
-__device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo) {
-  float hx, hy, lx, ly;
-  hi = rn_pair(x, y, hx, hy);
-  lo = rn_pair(x - hx, y - hy, lx, ly);
-}
 
 // Keys per block of the chunk attention (and per key range when every range
 // holds one block).
@@ -417,7 +389,7 @@ static __global__ void attention_combine_kernel(AttnArgs a, int dh, __nv_bfloat1
 // or the prefix cache); keys of a segment are rows 0..n-1 of k/v with stride
 // kv_ld.  Q and P enter the MMA as TERMS-term bf16 splits; fp32 segments (the
 // group's own keys as computed) as two bf16 planes.  The output of row r, head
-// h, dim d goes to the three planes out[r][t*ldh + h*DH + d] (hi, mid, lo of the
+// h, dim d goes to the two fp16 planes out[r][t*ldh + h*DH + d] (hi, lo of the
 // fp32 value) -- the split activation of the output projection.
 // Grid (Hq, ceil(T_rows / 64), groups).
 // ---------------------------------------------------------------------------
@@ -442,7 +414,7 @@ struct SegAttnArgs {
   int T_rows;
   int Hq, Hkv, kv_ld;
   float scale_log2;
-  __nv_bfloat16* out;        // [groups * T_rows][3 * ldh]
+  __half* out;               // fp16 planes [groups * T_rows][kActTerms * ldh]
   int ldh;
   unsigned long long* trace; // null, or per-block timestamps of CTA (0, 0, 0) (tensor-core kernel)
   SegGroup grp[16];
@@ -630,20 +602,18 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   for (int j = 0; j < NT; ++j) {
     const int c = h * DH + j * 8 + 2 * tq;
     if (v0) {
-      uint32_t hh, mm, ll;
-      split_pair_exact(o[j][0] * i0, o[j][1] * i0, hh, mm, ll);
-      __nv_bfloat16* p = a.out + row0 * 3 * a.ldh + c;
+      uint32_t hh, ll;
+      split_pair_h2(o[j][0] * i0, o[j][1] * i0, hh, ll);
+      __half* p = a.out + row0 * kActTerms * a.ldh + c;
       *reinterpret_cast<uint32_t*>(p) = hh;
-      *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
-      *reinterpret_cast<uint32_t*>(p + 2 * a.ldh) = ll;
+      *reinterpret_cast<uint32_t*>(p + a.ldh) = ll;
     }
     if (v1) {
-      uint32_t hh, mm, ll;
-      split_pair_exact(o[j][2] * i1, o[j][3] * i1, hh, mm, ll);
-      __nv_bfloat16* p = a.out + row1 * 3 * a.ldh + c;
+      uint32_t hh, ll;
+      split_pair_h2(o[j][2] * i1, o[j][3] * i1, hh, ll);
+      __half* p = a.out + row1 * kActTerms * a.ldh + c;
       *reinterpret_cast<uint32_t*>(p) = hh;
-      *reinterpret_cast<uint32_t*>(p + a.ldh) = mm;
-      *reinterpret_cast<uint32_t*>(p + 2 * a.ldh) = ll;
+      *reinterpret_cast<uint32_t*>(p + a.ldh) = ll;
     }
   }
 }
@@ -658,7 +628,6 @@ static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2 + 64 * 
 static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
 static inline cudaError_t set_attention_smem_limits() {
-  cudaFuncSetAttribute(attention_seg_kernel<128, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(128));
   cudaFuncSetAttribute(attention_seg_kernel<256, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
   cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(64));
   cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(128));

@@ -398,18 +398,10 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     const float lt = l + xl[(half ^ 1) * 128 + r];
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
     if (rg < a.T_rows) {
-      __nv_bfloat16* dst = a.out + ((size_t)b * a.T_rows + rg) * 3 * a.ldh + h * DH + half * 64;
+      // the two fp16 planes of the output projection's activation
 #pragma unroll
-      for (int i = 0; i < 64; i += 8) {
-        uint4 hv, mv, lv;
-        split_pair_exact(o[i] * inv, o[i + 1] * inv, hv.x, mv.x, lv.x);
-        split_pair_exact(o[i + 2] * inv, o[i + 3] * inv, hv.y, mv.y, lv.y);
-        split_pair_exact(o[i + 4] * inv, o[i + 5] * inv, hv.z, mv.z, lv.z);
-        split_pair_exact(o[i + 6] * inv, o[i + 7] * inv, hv.w, mv.w, lv.w);
-        *reinterpret_cast<uint4*>(dst + i) = hv;
-        *reinterpret_cast<uint4*>(dst + a.ldh + i) = mv;
-        *reinterpret_cast<uint4*>(dst + 2 * a.ldh + i) = lv;
-      }
+      for (int i = 0; i < 64; ++i) o[i] *= inv;
+      store_planes<64>(a.out + ((size_t)b * a.T_rows + rg) * kActTerms * a.ldh + h * DH + half * 64, a.ldh, o);
     }
   }
   tc_fence_before();

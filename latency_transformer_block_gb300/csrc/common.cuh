@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -158,6 +159,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// the same with fp16 A and B (format fields 0)
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 64 bf16
 // (128 B), 8-row groups of 1024 B (stride byte offset), version 1 (sm_100+),
@@ -177,6 +182,20 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t smem_addr) {
 // rows hold 64 bf16: 16-byte chunk index (k / 8) XOR (r mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
   return (uint32_t)(r * 128 + ((((k >> 3) ^ (r & 7)) & 7) << 4) + ((k & 7) << 1));
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread.
@@ -229,6 +248,57 @@ __device__ __forceinline__ void split_pair_exact(float x, float y, uint32_t& hi,
   hi = __byte_perm(hx, hy, 0x7632);
   mid = __byte_perm(mx, my, 0x7632);
   lo = __byte_perm(__float_as_uint(qx), __float_as_uint(qy), 0x7632);
+}
+
+// Round a pair of fp32 values to bf16 (nearest even) in one packed conversion.
+__device__ __forceinline__ uint32_t rn_pair(float x, float y, float& bx, float& by) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 f = __bfloat1622float2(h);
+  bx = f.x;
+  by = f.y;
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two-term split of a pair of fp32 values into packed bf16x2 words: hi is the
+// nearest bf16 of x, lo the nearest bf16 of x - hi (exact in fp32), so hi + lo
+// carries x to 16 significant bits (|x - hi - lo| <= 2^-17 |x|).
+__device__ __forceinline__ void split_pair2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  float hx, hy, lx, ly;
+  hi = rn_pair(x, y, hx, hy);
+  lo = rn_pair(x - hx, y - hy, lx, ly);
+}
+
+
+// Two-term fp16 split of a pair of fp32 values into packed half2 words: hi is
+// the nearest fp16 of x, lo the nearest fp16 of x - hi (exact in fp32), so
+// |x - hi - lo| <= max(2^-22 |x|, 2^-25) for |x| < 65504 (the second bound
+// where lo falls below fp16's normal range).
+__device__ __forceinline__ void split_pair_h2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x, y);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x - f.x, y - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Activations of the dense path (prefix prefill, DiT stage) enter the tensor
+// cores as two fp16 planes (hi + lo, 22 significant bits) against the folded
+// bf16 weights held as fp16 scaled by a power of two (an exact conversion):
+// two MMAs per product instead of the three of an exact bf16 split, at the
+// precision of fp32 inputs to within a few units of 2^-22.
+constexpr int kActTerms = 2;
+
+// n values -> the two fp16 planes (hi at dst, lo at dst + plane), n a multiple of 8
+template <int N>
+__device__ __forceinline__ void store_planes(__half* dst, size_t plane, const float* v) {
+#pragma unroll
+  for (int j = 0; j < N; j += 8) {
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_pair_h2(v[j + 2 * e], v[j + 2 * e + 1], wh[e], wl[e]);
+    *reinterpret_cast<uint4*>(dst + j) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    *reinterpret_cast<uint4*>(dst + plane + j) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 a, __nv_bfloat16 b) {

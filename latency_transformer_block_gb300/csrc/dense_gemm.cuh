@@ -33,8 +33,8 @@ enum DenseEpi : int {
   E_STORE = 0,        // out[m][n] = acc (+ bias[n])
   E_RESID = 1,        // out[m][n] += acc
   E_RESID_GATE = 2,   // out[m][n] += gate[chunk(m)][n] * acc
-  E_GELU_SPLIT = 3,   // act planes <- exact split of GELU_tanh(acc)
-  E_GEGLU_SPLIT = 4,  // tile = [64 gate | 64 up] -> act planes <- exact split of GELU(g) * u
+  E_GELU_SPLIT = 3,   // act planes <- split of GELU_tanh(acc)
+  E_GEGLU_SPLIT = 4,  // tile = [64 gate | 64 up] -> act planes <- split of GELU(g) * u
 };
 
 constexpr int kMaxChunks = 16;
@@ -42,7 +42,9 @@ constexpr int kChunkMMA = 32;   // MMAs (of K = 16) per TMEM accumulation chunk,
 
 struct DenseArgs {
   int M, N, K;           // K = reduction length of one term
-  int terms;             // planes in A (1, 2 or 3)
+  int terms;             // planes in A (1..PLANES)
+  int f16;               // operands fp16 (activation planes, scaled fp16 weights) instead of bf16
+  float out_scale;       // acc *= out_scale before the epilogue (2^-s of weights held as 2^s W)
   int w_row0;            // first weight row of this matrix in the stacked tensor
   int epi;
   float* out;            // fp32 [M][ldo] (E_STORE / E_RESID / E_RESID_GATE)
@@ -52,84 +54,120 @@ struct DenseArgs {
   const float* gate;
   int gate_off[kMaxChunks];
   int rows_per_chunk;
-  // E_*_SPLIT: bf16 planes [M][3 * ldh] (hi at column c, mid at ldh + c, lo at 2 ldh + c)
-  __nv_bfloat16* act2;
+  // E_*_SPLIT: fp16 planes [M][kActTerms * ldh] (hi of column c at c, lo at ldh + c)
+  __half* act2;
   int ldh;
   DevErr* err;
 };
 
 constexpr int kDA = 128 * 64 * 2;   // A tile bytes (one plane)
 constexpr int kDB = 128 * 64 * 2;   // B tile bytes
-constexpr int kDSlot = 3 * kDA + kDB;   // one slot: up to three planes of A + B
+// one pipeline slot: up to PLANES activation tiles + one weight tile
+__host__ __device__ constexpr int dense_slot_bytes(int planes) { return planes * kDA + kDB; }
 
-__host__ __device__ constexpr int dense_smem_bytes(int stages) {
-  return 1024 + stages * kDSlot + 8 * (2 * stages + 4) + 16;
+__host__ __device__ constexpr int dense_smem_bytes(int stages, int planes) {
+  return 1024 + stages * dense_slot_bytes(planes) + 4 * 32 * 64 * 4 + 8 * (2 * stages + 4) + 16;
 }
 
-// 8 values -> three planes of 8 bf16 (hi, mid, lo: the exact split of the fp32 value)
-__device__ __forceinline__ void store_split3(__nv_bfloat16* hi, int plane, const float* v) {
-  uint32_t wh[4], wm[4], wl[4];
+// Epilogue staging: each of the four epilogue warps passes its 32 rows through
+// an 8 KB buffer [32 rows][16 float4] in shared memory, float4 chunk c of row r
+// at position c ^ (r & 15) (conflict-free both for a lane writing its own row
+// and for 16 lanes reading one row), so that global reads and writes run along
+// rows (a lane holding a whole row would touch 32 rows per warp access).
+constexpr int kDStageBytes = 4 * 32 * 64 * 4;
+constexpr int kEpiU = 4;   // row pairs per pass of the staged epilogue
+
+__device__ __forceinline__ void stage_put(float4* st, int lane, const float* v, float scale) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) split_pair_exact(v[2 * e], v[2 * e + 1], wh[e], wm[e], wl[e]);
-  *reinterpret_cast<uint4*>(hi) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-  *reinterpret_cast<uint4*>(hi + plane) = make_uint4(wm[0], wm[1], wm[2], wm[3]);
-  *reinterpret_cast<uint4*>(hi + 2 * plane) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  for (int c = 0; c < 16; ++c)
+    st[lane * 16 + (c ^ (lane & 15))] =
+        make_float4(v[4 * c] * scale, v[4 * c + 1] * scale, v[4 * c + 2] * scale, v[4 * c + 3] * scale);
 }
 
-// Epilogue of one tile row: 128 accumulated columns of token `row`, feature
-// tile tn.
-__device__ __forceinline__ void dense_epilogue(const DenseArgs& a, const float (&acc)[128], int row, int tn) {
-  if (a.epi == E_GEGLU_SPLIT) {
-    // columns 0..63 gate, 64..127 up of features tn*64 + j
-    __nv_bfloat16* hi = a.act2 + (size_t)row * 3 * a.ldh + tn * 64;
+// One staged 64-column half of the warp's rows row0 .. row0 + 31: output
+// columns n0 .. n0 + 63 (feature columns of the split planes for the
+// E_*_SPLIT epilogues).  Lane l takes float4 chunk l & 15 of rows 2i + (l >> 4);
+// the loads of 8 rows are issued before their stores.
+__device__ __forceinline__ void epi_half(const DenseArgs& a, const float4* st, int row0, int n0, int lane) {
+  const int c = lane & 15, rsub = lane >> 4;
+  const int col = n0 + 4 * c;
+  float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.epi == E_STORE && a.bias) bias = *reinterpret_cast<const float4*>(a.bias + col);
+#pragma unroll 1
+  for (int i0 = 0; i0 < 32; i0 += 2 * kEpiU) {
+    float4 x[kEpiU], g[kEpiU];
 #pragma unroll
-    for (int j = 0; j < 64; j += 8) {
-      float h[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = gelu_tanh(acc[j + e]) * acc[64 + j + e];
-      store_split3(hi + j, a.ldh, h);
+    for (int u = 0; u < kEpiU; ++u) {
+      const int row = row0 + i0 + 2 * u + rsub;
+      x[u] = g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row < a.M && (a.epi == E_RESID || a.epi == E_RESID_GATE))
+        x[u] = *reinterpret_cast<const float4*>(a.out + (size_t)row * a.ldo + col);
+      if (row < a.M && a.epi == E_RESID_GATE)
+        g[u] = *reinterpret_cast<const float4*>(a.gate + a.gate_off[row / a.rows_per_chunk] + col);
     }
-  } else if (a.epi == E_GELU_SPLIT) {
-    __nv_bfloat16* hi = a.act2 + (size_t)row * 3 * a.ldh + tn * 128;
 #pragma unroll
-    for (int j = 0; j < 128; j += 8) {
-      float h[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = gelu_tanh(acc[j + e]);
-      store_split3(hi + j, a.ldh, h);
-    }
-  } else {
-    const int n0 = tn * 128;
-    float* o = a.out + (size_t)row * a.ldo + n0;
-    const float* gate = (a.epi == E_RESID_GATE) ? a.gate + a.gate_off[row / a.rows_per_chunk] + n0 : nullptr;
-#pragma unroll
-    for (int j = 0; j < 128; j += 4) {
-      float4 r = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-      if (a.epi == E_STORE) {
-        if (a.bias) {
-          const float4 b = *reinterpret_cast<const float4*>(a.bias + n0 + j);
-          r.x += b.x; r.y += b.y; r.z += b.z; r.w += b.w;
+    for (int u = 0; u < kEpiU; ++u) {
+      const int r0 = i0 + 2 * u + rsub, row = row0 + r0;
+      if (row >= a.M) continue;
+      float4 r = st[r0 * 16 + (c ^ (r0 & 15))];
+      if (a.epi == E_GELU_SPLIT || a.epi == E_GEGLU_SPLIT) {
+        if (a.epi == E_GELU_SPLIT) {
+          r.x = gelu_tanh(r.x); r.y = gelu_tanh(r.y); r.z = gelu_tanh(r.z); r.w = gelu_tanh(r.w);
         }
-      } else {
-        const float4 x = *reinterpret_cast<const float4*>(o + j);
-        if (a.epi == E_RESID_GATE) {
-          const float4 gg = *reinterpret_cast<const float4*>(gate + j);
-          r.x = x.x + gg.x * r.x; r.y = x.y + gg.y * r.y; r.z = x.z + gg.z * r.z; r.w = x.w + gg.w * r.w;
-        } else {
-          r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
-        }
+        uint2 hv, lv;
+        split_pair_h2(r.x, r.y, hv.x, lv.x);
+        split_pair_h2(r.z, r.w, hv.y, lv.y);
+        __half* hp = a.act2 + (size_t)row * kActTerms * a.ldh + col;
+        *reinterpret_cast<uint2*>(hp) = hv;
+        *reinterpret_cast<uint2*>(hp + a.ldh) = lv;
+        continue;
       }
-      *reinterpret_cast<float4*>(o + j) = r;
+      if (a.epi == E_STORE) {
+        r.x += bias.x; r.y += bias.y; r.z += bias.z; r.w += bias.w;
+      } else if (a.epi == E_RESID_GATE) {
+        r.x = x[u].x + g[u].x * r.x; r.y = x[u].y + g[u].y * r.y;
+        r.z = x[u].z + g[u].z * r.z; r.w = x[u].w + g[u].w * r.w;
+      } else {
+        r.x += x[u].x; r.y += x[u].y; r.z += x[u].z; r.w += x[u].w;
+      }
+      *reinterpret_cast<float4*>(a.out + (size_t)row * a.ldo + col) = r;
     }
   }
 }
 
-template <int STAGES>
+// Epilogue of one tile for the warp's 32 rows (lane l holds the 128
+// accumulated columns of row row0 + l), feature tile tn; the accumulators are
+// scaled by a.out_scale (a power of two: exact) on the way.  All lanes take part.
+__device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[128], int row0, int tn, float4* st,
+                                               int lane) {
+  if (a.epi == E_GEGLU_SPLIT) {
+    // columns 0..63 gate, 64..127 up of features tn*64 + j
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = gelu_tanh(acc[j] * a.out_scale) * (acc[64 + j] * a.out_scale);
+    stage_put(st, lane, acc, 1.f);
+    __syncwarp();
+    epi_half(a, st, row0, tn * 64, lane);
+    __syncwarp();
+    return;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    stage_put(st, lane, acc + 64 * h, a.out_scale);
+    __syncwarp();
+    epi_half(a, st, row0, tn * 128 + 64 * h, lane);
+    __syncwarp();
+  }
+}
+
+template <int STAGES, int PLANES>
 __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
-                                                            const __grid_constant__ CUtensorMap wmap, DenseArgs a) {
+                                                            const __grid_constant__ CUtensorMap wmap,
+                                                            const __grid_constant__ DenseArgs a) {
+  constexpr int kSlot = dense_slot_bytes(PLANES);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kDSlot);
+  float4* stage = reinterpret_cast<float4*>(smem + STAGES * kSlot);   // epilogue staging, 8 KB per warp
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kSlot + kDStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;    // [2]
@@ -180,11 +218,11 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, a.err, 20)) { ok = false; break; }
-          uint8_t* slot = smem + s * kDSlot;
+          uint8_t* slot = smem + s * kSlot;
           mbar_arrive_expect_tx(&full[s], a.terms * kDA + kDB);
           for (int t = 0; t < a.terms; ++t)
             tma_load_2d(slot + t * kDA, &amap, &full[s], t * a.K + i * 64, tm * 128, pol_a);
-          tma_load_2d(slot + 3 * kDA, &wmap, &full[s], i * 64, a.w_row0 + tn * 128, pol_w);
+          tma_load_2d(slot + PLANES * kDA, &wmap, &full[s], i * 64, a.w_row0 + tn * 128, pol_w);
         }
       }
       for (uint32_t i = (it > (uint32_t)STAGES ? it - STAGES : 0); i < it; ++i)
@@ -192,7 +230,7 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      const uint32_t idesc = a.f16 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
       bool ok = true;
       uint32_t it = 0, gch = 0;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -208,7 +246,7 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
             const uint32_t ph = (it / STAGES) & 1;
             if (!mbar_wait(&full[s], ph, a.err, 22)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * kDSlot), bb = sa + 3 * kDA;
+            const uint32_t sa = smem_u32(smem + s * kSlot), bb = sa + PLANES * kDA;
             for (int t = 0; t < a.terms; ++t) {
               const uint32_t aa = sa + t * kDA;
 #pragma unroll
@@ -224,31 +262,32 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
     }
   } else {
     const int quad = warp & 3;
+    float4* st = stage + quad * 32 * 16;
     uint32_t gch = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int tm = tile / n_tiles, tn = tile % n_tiles;
-      const int row = tm * 128 + quad * 32 + lane;
-      const bool valid = row < a.M;
+      const int row0 = tm * 128 + quad * 32;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
       for (int ch = 0; ch < nchunk; ++ch, ++gch) {
         const int buf = gch & 1;
-        if (!mbar_wait(&acc_full[buf], (gch >> 1) & 1, a.err, 23)) { ok = false; break; }
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (gch >> 1) & 1, a.err, 23))) { ok = false; break; }
         tc_fence_after();
         const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 128);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tb + c * 32, v);
+        for (int c = 0; c < 8; ++c) {
+          float v[16];
+          tmem_ld16(tb + c * 16, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] += v[j];
+          for (int j = 0; j < 16; ++j) acc[c * 16 + j] += v[j];
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
-      if (ok && valid) dense_epilogue(a, acc, row, tn);
+      if (ok) dense_epilogue(a, acc, row0, tn, st, lane);
     }
   }
   tc_fence_before();

@@ -6,10 +6,10 @@
 namespace lat {
 
 // ---------------------------------------------------------------------------
-// Norm prologue with the three-term split of the next GEMM's activation:
+// Norm prologue with the split of the next GEMM's activation into two fp16 planes:
 //   RMS:    u = x * rsqrt(mean(x^2) + eps)              (scale g folded into W)
 //   LN_MOD: u = LN(x) * (1 + scale_b) + shift_b          (adaLN of chunk b)
-//   act[m][c], act[m][D + c], act[m][2D + c] = hi, mid, lo of u
+//   act[m][c] = fp16(u), act[m][D + c] = fp16(u - act[m][c])
 // One CTA of 256 threads per row.
 // ---------------------------------------------------------------------------
 enum NormMode : int { NORM_RMS = 0, NORM_LN_MOD = 1 };
@@ -23,7 +23,7 @@ struct NormArgs {
   int shift_off[kMaxChunks];  // LN_MOD: table offset of chunk b's shift row
   int scale_off[kMaxChunks];
   int rows_per_chunk;
-  __nv_bfloat16* act2;     // [M][3D]
+  __half* act2;            // [M][kActTerms * D]
 };
 
 static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
@@ -69,14 +69,13 @@ static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
     sh = a.table + a.shift_off[b];
     sc = a.table + a.scale_off[b];
   }
-  __nv_bfloat16* hi = a.act2 + (size_t)m * 3 * a.D;
+  __half* hi = a.act2 + (size_t)m * kActTerms * a.D;
   for (int c = threadIdx.x; c < a.D; c += 256) {
     float u = (xr[c] - mu) * rs;
     if (a.mode == NORM_LN_MOD) u = u * (1.f + sc[c]) + sh[c];
-    const Split3 t = split3(u);
-    hi[c] = t.hi;
-    hi[a.D + c] = t.mid;
-    hi[2 * a.D + c] = t.lo;
+    const __half h = __float2half_rn(u);
+    hi[c] = h;
+    hi[a.D + c] = __float2half_rn(u - __half2float(h));
   }
 }
 

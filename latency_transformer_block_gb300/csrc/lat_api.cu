@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <utility>
 #include <cstdarg>
@@ -162,7 +163,10 @@ struct lat_ctx {
         *qbuf = nullptr;
   double* theta = nullptr;
   float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32)
-  bf16 *act2 = nullptr, *act2f = nullptr;
+  __half *act2 = nullptr, *act2f = nullptr;   // fp16 activation planes [M][kActTerms * K]
+  // the four block projections (merged QKV, output, FFN in, FFN out) of the dense
+  // path are held as fp16 = 2^s x folded bf16 weight; wscale = 2^-s per matrix
+  float wscale[4] = {1.f, 1.f, 1.f, 1.f};
   CUtensorMap map_act_d, map_act_o, map_act_f;
   int m_max = 0;
   bf16 *wt1 = nullptr, *bt1 = nullptr, *wt2 = nullptr, *bt2 = nullptr, *wmod = nullptr, *bmod = nullptr;
@@ -309,6 +313,34 @@ static lat_status fold_t(const void* W, const void* g, bf16* out, int K, int N, 
   fold_transpose_kernel<<<grid, block>>>(reinterpret_cast<const bf16*>(W), reinterpret_cast<const bf16*>(g), out,
                                          K, N, il, il_off);
   return launch_check("fold_transpose");
+}
+
+// Hold a folded bf16 weight (n values) as fp16 = 2^s w in place, s chosen so
+// that max |w| 2^s lies in [2^14, 2^15): the conversion is exact except for
+// values below 2^(-14-s), which keep fp16's subnormal spacing (an absolute
+// error <= 2^(-25-s), ~1e-13 for N(0, 0.02) weights).  *inv = 2^-s.
+static lat_status to_f16_scaled(bf16* w, size_t n, float* inv) {
+  unsigned* dmax = nullptr;
+  CUDA_TRY(cudaMalloc(&dmax, sizeof(unsigned)));
+  unsigned hm = 0;
+  cudaError_t e = cudaMemset(dmax, 0, sizeof(unsigned));
+  if (e == cudaSuccess) {
+    absmax_bf16_kernel<<<1024, 256>>>(w, n, dmax);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpy(&hm, dmax, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  cudaFree(dmax);
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "weight scan: %s", cudaGetErrorString(e));
+  float m;
+  std::memcpy(&m, &hm, sizeof(float));
+  if (!std::isfinite(m)) return fail(LAT_ERR_ARG, "non-finite weight");
+  int ex = 0;
+  if (m > 0.f) std::frexp(m, &ex);          // m < 2^ex
+  const int s = m > 0.f ? std::min(15 - ex, 100) : 0;
+  *inv = std::ldexp(1.f, -s);
+  const size_t blocks = std::min<size_t>((n + 255) / 256, 65536);
+  bf16_to_f16_scaled_kernel<<<(unsigned)blocks, 256>>>(reinterpret_cast<uint16_t*>(w), n, std::ldexp(1.f, s));
+  return launch_check("to_f16_scaled");
 }
 
 static lat_status small_gemm(const void* A, bool a_bf16, int lda, const void* B, bool b_bf16, int ldb,
@@ -640,16 +672,22 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
 // ---------------------------------------------------------------------------
 // dense path: prefix prefill and DiT stage
 // ---------------------------------------------------------------------------
-static constexpr int kDStages = 3;
-// bf16 planes of every dense activation: three terms carry the fp32 value
-static constexpr int kActTerms = 3;
+// four pipeline slots of two activation planes + one weight tile (48 KB each)
+static constexpr int kDStages = 4;
 
-static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, const CUtensorMap& wmap, DenseArgs a,
-                                cudaStream_t st) {
+// weight of a dense projection: the four fp16 block projections, or the bf16
+// patch embedding (prefix prefill, one plain bf16 activation plane)
+enum WSel : int { W_QKV = 0, W_O = 1, W_UP = 2, W_DOWN = 3, W_PATCH = 4 };
+
+static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int wsel, DenseArgs a, cudaStream_t st) {
+  const CUtensorMap* wm[5] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down, &c->map_patch};
   a.err = c->err;
+  a.f16 = wsel != W_PATCH;
+  a.out_scale = wsel != W_PATCH ? c->wscale[wsel] : 1.f;
   const int tiles = ((a.M + 127) / 128) * (a.N / 128);
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
-  dense_gemm_kernel<kDStages><<<grid, 192, dense_smem_bytes(kDStages), st>>>(amap, wmap, a);
+  dense_gemm_kernel<kDStages, kActTerms><<<grid, 192, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel],
+                                                                                                   a);
   return launch_check("dense_gemm");
 }
 
@@ -683,16 +721,17 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
   const lat_model_desc& d = c->d;
   const int qd = d.Hq * d.dh;
   c->m_max = d.max_batch * rows_per_group;
+  const int terms = kActTerms;
   const int wact = d.D > qd ? d.D : qd;
-  LAT_TRY(c->alloc(&c->act2, (size_t)c->m_max * kActTerms * wact));
-  LAT_TRY(c->alloc(&c->act2f, (size_t)c->m_max * kActTerms * d.F));
+  LAT_TRY(c->alloc(&c->act2, (size_t)c->m_max * terms * wact));
+  LAT_TRY(c->alloc(&c->act2f, (size_t)c->m_max * terms * d.F));
   LAT_TRY(c->alloc(&c->qkvbuf, (size_t)c->m_max * c->nqkv));
   LAT_TRY(c->alloc(&c->qbuf, (size_t)c->m_max * qd));
   LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
   LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
-  LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, kActTerms * d.D));
-  LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, kActTerms * qd));
-  LAT_TRY(make_act_map(&c->map_act_f, c->act2f, c->m_max, kActTerms * d.F));
+  LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, terms * d.D));
+  LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, terms * qd));
+  LAT_TRY(make_act_map(&c->map_act_f, c->act2f, c->m_max, terms * d.F));
   LAT_TRY(c->alloc(&c->err, 1));
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
   return LAT_OK;
@@ -729,6 +768,10 @@ static lat_status create_prefix(lat_ctx* c, const lat_weights* w) {
     LAT_TRY(fold_t(b.wu, b.g_ffn, gu0, D, F, 64, 64));
     LAT_TRY(fold_t(b.wd, nullptr, c->wdown + (size_t)l * D * F, F, D));
   }
+  LAT_TRY(to_f16_scaled(c->wqkv, (size_t)L * c->nqkv * D, &c->wscale[W_QKV]));
+  LAT_TRY(to_f16_scaled(c->wo, (size_t)L * D * qd, &c->wscale[W_O]));
+  LAT_TRY(to_f16_scaled(c->wup, (size_t)L * 2 * F * D, &c->wscale[W_UP]));
+  LAT_TRY(to_f16_scaled(c->wdown, (size_t)L * D * F, &c->wscale[W_DOWN]));
   LAT_TRY(fold_t(w->w_patch, nullptr, c->wpatch, d.patch_dim, D));
   LAT_TRY(c->alloc(&c->bpatch, (size_t)D));
   bf16_to_f32_kernel<<<(D + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->b_patch), c->bpatch, D);
@@ -799,6 +842,10 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
     LAT_TRY(fold_t(b.w1, nullptr, c->wup + (size_t)l * F * D, D, F));
     LAT_TRY(fold_t(b.w2, nullptr, c->wdown + (size_t)l * D * F, F, D));
   }
+  LAT_TRY(to_f16_scaled(c->wqkv, (size_t)L * 3 * D * D, &c->wscale[W_QKV]));
+  LAT_TRY(to_f16_scaled(c->wo, (size_t)L * D * D, &c->wscale[W_O]));
+  LAT_TRY(to_f16_scaled(c->wup, (size_t)L * F * D, &c->wscale[W_UP]));
+  LAT_TRY(to_f16_scaled(c->wdown, (size_t)L * D * F, &c->wscale[W_DOWN]));
   LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * 3 * D, D, 128));
   LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, D, 128));
   LAT_TRY(make_kmajor_map(&c->map_up, c->wup, L * F, D, 128));
@@ -834,6 +881,7 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
     attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, c->err);
     return launch_check("attention_tc");
   }
+  if (dh != 256) return fail(LAT_ERR_SHAPE, "dense-path attention: dh 128 or 256");
   dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups);
   attention_seg_kernel<256, 3><<<grid, 128, attn_smem_bytes(dh), st>>>(a);
   return launch_check("attention_seg");
@@ -849,7 +897,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     DenseArgs a{};
     a.M = M; a.N = D; a.K = d.patch_dim; a.terms = 1; a.w_row0 = 0; a.epi = E_STORE;
     a.out = c->xres; a.ldo = D; a.bias = c->bpatch;
-    LAT_TRY(enqueue_dense(c, pmap, c->map_patch, a, st));
+    LAT_TRY(enqueue_dense(c, pmap, W_PATCH, a, st));
   }
   for (int l = 0; l < L; ++l) {
     const bool last = (l == L - 1);
@@ -862,7 +910,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
       a.M = M; a.K = D; a.terms = kActTerms; a.epi = E_STORE; a.out = c->qkvbuf;
       if (last) { a.N = 2 * kvd; a.w_row0 = l * c->nqkv + qd; a.ldo = 2 * kvd; }
       else { a.N = c->nqkv; a.w_row0 = l * c->nqkv; a.ldo = c->nqkv; }
-      LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_qkv, a, st));
+      LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, a, st));
     }
     RopeKvArgs ra{};
     ra.qkv = c->qkvbuf; ra.ld_qkv = last ? 2 * kvd : c->nqkv; ra.q_cols = last ? 0 : qd; ra.kv_cols = kvd;
@@ -887,7 +935,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     {
       DenseArgs a{};
       a.M = M; a.N = D; a.K = qd; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
-      LAT_TRY(enqueue_dense(c, c->map_act_o, c->map_o, a, st));
+      LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
     }
     norm_split_kernel<<<M, 256, 0, st>>>(na);
     LAT_TRY(launch_check("norm_split"));
@@ -895,12 +943,12 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
       DenseArgs a{};
       a.M = M; a.N = 2 * F; a.K = D; a.terms = kActTerms; a.w_row0 = l * 2 * F; a.epi = E_GEGLU_SPLIT;
       a.act2 = c->act2f; a.ldh = F;
-      LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_up, a, st));
+      LAT_TRY(enqueue_dense(c, c->map_act_d, W_UP, a, st));
     }
     {
       DenseArgs a{};
       a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
-      LAT_TRY(enqueue_dense(c, c->map_act_f, c->map_down, a, st));
+      LAT_TRY(enqueue_dense(c, c->map_act_f, W_DOWN, a, st));
     }
   }
   return LAT_OK;
@@ -930,7 +978,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     DenseArgs a{};
     a.M = M; a.N = 3 * D; a.K = D; a.terms = kActTerms; a.w_row0 = l * 3 * D; a.epi = E_STORE; a.out = c->qkvbuf;
     a.ldo = 3 * D;
-    LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_qkv, a, st));
+    LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, a, st));
   }
   RopeKvArgs ra{};
   ra.qkv = c->qkvbuf; ra.ld_qkv = 3 * D; ra.q_cols = D; ra.kv_cols = D; ra.dh = d.dh; ra.T = T;
@@ -965,7 +1013,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     a.M = M; a.N = D; a.K = D; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
     a.gate = c->adaln; a.rows_per_chunk = T;
     for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 2 * D;
-    LAT_TRY(enqueue_dense(c, c->map_act_o, c->map_o, a, st));
+    LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
   }
   for (int b = 0; b < n; ++b) {
     na.shift_off[b] = ch[b].step * 6 * D + 3 * D;
@@ -976,14 +1024,14 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   {
     DenseArgs a{};
     a.M = M; a.N = F; a.K = D; a.terms = kActTerms; a.w_row0 = l * F; a.epi = E_GELU_SPLIT; a.act2 = c->act2f; a.ldh = F;
-    LAT_TRY(enqueue_dense(c, c->map_act_d, c->map_up, a, st));
+    LAT_TRY(enqueue_dense(c, c->map_act_d, W_UP, a, st));
   }
   {
     DenseArgs a{};
     a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
     a.gate = c->adaln; a.rows_per_chunk = T;
     for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 5 * D;
-    LAT_TRY(enqueue_dense(c, c->map_act_f, c->map_down, a, st));
+    LAT_TRY(enqueue_dense(c, c->map_act_f, W_DOWN, a, st));
   }
   return LAT_OK;
 }
@@ -1028,8 +1076,8 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     cudaFuncSetAttribute(skinny_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          skinny_smem_bytes(kStages));
     set_attention_smem_limits();
-    cudaFuncSetAttribute(dense_gemm_kernel<kDStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         dense_smem_bytes(kDStages));
+    cudaFuncSetAttribute(dense_gemm_kernel<kDStages, kActTerms>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         dense_smem_bytes(kDStages, kActTerms));
     cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_tc_smem_bytes());
     cudaFuncSetAttribute(pi0_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
     cudaFuncSetAttribute(pi0_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
@@ -1228,20 +1276,19 @@ lat_status lat_debug_dense_gemm(lat_ctx* c, int which, int layer, const void* ac
   if (!c || !act || !out) return fail(LAT_ERR_ARG, "NULL argument");
   if (c->d.kind != LAT_PI0_PREFIX && c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "needs a dense context");
   const lat_model_desc& d = c->d;
-  if (which < 0 || which > 3 || layer < 0 || layer >= d.L || M < 1 || M > c->m_max || terms < 1 || terms > 3)
+  if (which < 0 || which > 3 || layer < 0 || layer >= d.L || M < 1 || M > c->m_max || terms < 1 || terms > kActTerms)
     return fail(LAT_ERR_ARG, "bad argument");
   if (!aligned16(act) || !aligned16(out)) return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
   const int qd = d.Hq * d.dh;
   const int ffn_rows = d.kind == LAT_PI0_PREFIX ? 2 * d.F : d.F;
   const int N[4] = {c->nqkv, d.D, ffn_rows, d.D};
   const int K[4] = {d.D, qd, d.D, d.F};
-  const CUtensorMap* wm[4] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down};
   CUtensorMap amap;
   LAT_TRY(make_act_map(&amap, act, M, terms * K[which]));
   DenseArgs a{};
   a.M = M; a.N = N[which]; a.K = K[which]; a.terms = terms; a.w_row0 = layer * N[which];
   a.epi = E_STORE; a.out = out; a.ldo = N[which];
-  return enqueue_dense(c, amap, *wm[which], a, reinterpret_cast<cudaStream_t>(stream));
+  return enqueue_dense(c, amap, which, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lat_status lat_debug_step(lat_ctx* c, void* kv, int reps, void* stream) {

@@ -160,6 +160,24 @@ static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_
   }
 }
 
+// max |w| over n bf16 values into *out (as fp32 bits: non-negative floats
+// order like their bit patterns).  *out must start at 0.
+static __global__ void absmax_bf16_kernel(const __nv_bfloat16* w, size_t n, unsigned* out) {
+  float m = 0.f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(__bfloat162float(w[i])));
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));
+}
+
+// In place: bf16 bit patterns w -> fp16 bit patterns of w * scale (scale a power of two).
+static __global__ void bf16_to_f16_scaled_kernel(uint16_t* w, size_t n, float scale) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = __bfloat162float(__ushort_as_bfloat16(w[i])) * scale;
+    w[i] = __half_as_ushort(__float2half_rn(v));
+  }
+}
+
 // Generic small fp32 GEMM for the offline tables (CUDA cores, fp32 accumulate):
 //   C[m][n] = act( sum_k A[m][k] B[k][n] + bias[n] )
 // A, B, bias each either bf16 or fp32 (flags).  act: 0 none, 1 SiLU.
