@@ -2,28 +2,30 @@
 //
 //   acc[m][n] = sum_k A[m][k] W[n][k]
 //
-// A is an activation stored as `terms` bf16 planes side by side ([M][terms*K],
-// plane t holding the t-th term of the fp32 value's split, so sum_t A_t = A to
-// 8 * terms significant bits); the K loop runs over terms*K and reuses the
-// weight tile of column k mod K for every plane.  Products of bf16 pairs are
-// exact on the tensor cores and accumulate in fp32 in TMEM.
+// A is an activation stored as `terms` 16-bit planes side by side
+// ([M][terms*K]): for the block projections two fp16 planes (hi, lo: 22
+// significant bits of the fp32 value) against the weight held as fp16 =
+// 2^s W (exact), for the patch embedding one plain bf16 plane; the K loop runs
+// over terms*K and reuses the weight tile of column k mod K for every plane.
+// Products are exact on the tensor cores and accumulate in fp32 in TMEM.
 //
-// Tile 128 (tokens) x 128 (features) x 64, both operands moved by TMA with a
+// Tile 128 (tokens) x 256 (features) x 64, both operands moved by TMA with a
 // 128-byte swizzle through STAGES slots; a slot holds one weight tile and the
 // `terms` activation tiles of the same K range, so each weight tile crosses
-// from L2 once (per-SM L2 bandwidth, ~120 GB/s, is what bounds this GEMM);
-// one tcgen05.mma (M=128, N=128, K=16) per 16-wide K step and plane; warp 0
-// issues TMA, warp 1 MMAs, warps 2..5 accumulate and run the fused epilogue
-// (bias, residual, per-chunk gate, GELU / GeGLU followed by the split of the
-// next GEMM's activation).
+// from L2 once.  One tcgen05.mma (M=128, N=256, K=16) per 16-wide K step and
+// plane: on this hardware an M=128 MMA takes the same ~152 cycles for N = 64,
+// 128 or 256, so only N = 256 runs the tensor core at its rate.  Warp 0 issues
+// TMA, warp 1 MMAs, warps 4..11 accumulate and run the fused epilogue (bias,
+// residual, per-chunk gate, GELU / GeGLU followed by the split of the next
+// GEMM's activation).
 //
 // Accumulation in two levels: the tensor core sums one chunk of at most 32
-// MMAs (8 / terms K-blocks of all planes) into a TMEM accumulator; the epilogue warps add each
-// finished chunk into fp32 registers (round to nearest) while the tensor core
-// fills the other TMEM accumulator.  Measured on this hardware, an fp32 TMEM
-// accumulator run over thousands of MMAs drifts by about one unit of its last
-// place per MMA in one direction (K = 13824 x 2 terms gave 2e-4 relative
-// error); chunks of 32 MMAs bound that drift to ~4e-6.
+// MMAs (8 / terms K-blocks of all planes) into a TMEM accumulator; the
+// epilogue warps add each finished chunk into fp32 registers (round to
+// nearest) while the tensor core fills the other TMEM accumulator.  Measured
+// on this hardware, an fp32 TMEM accumulator run over thousands of MMAs drifts
+// by about one unit of its last place per MMA in one direction (K = 13824 x 2
+// terms gave 2e-4 relative error); chunks of 32 MMAs bound that drift to ~4e-6.
 #pragma once
 #include "common.cuh"
 
@@ -60,45 +62,51 @@ struct DenseArgs {
   DevErr* err;
 };
 
-constexpr int kDA = 128 * 64 * 2;   // A tile bytes (one plane)
-constexpr int kDB = 128 * 64 * 2;   // B tile bytes
+constexpr int kDA = 128 * 64 * 2;   // A tile bytes (one plane, 128 tokens x 64)
+constexpr int kDB = 256 * 64 * 2;   // B tile bytes (256 weight rows x 64)
 // one pipeline slot: up to PLANES activation tiles + one weight tile
 __host__ __device__ constexpr int dense_slot_bytes(int planes) { return planes * kDA + kDB; }
 
-__host__ __device__ constexpr int dense_smem_bytes(int stages, int planes) {
-  return 1024 + stages * dense_slot_bytes(planes) + 4 * 32 * 64 * 4 + 8 * (2 * stages + 4) + 16;
-}
+// Epilogue: eight warps; warp 4 + e reads TMEM lanes 32 (e % 4) .. + 31 (the
+// rows of its quadrant) and columns 128 (e / 4) .. + 127 of the 256-wide
+// accumulator.  Each passes its 32 rows x 128 columns through a 4 KB buffer
+// [32 rows][8 float4] in four 32-column quarters, float4 chunk c of row r at
+// position c ^ (r & 7) (conflict-free both for a lane writing its own row and
+// for 8 lanes reading one row), so that global reads and writes run along rows
+// (a lane holding a whole row would touch 32 rows per warp access).
+constexpr int kDEpiWarps = 8;
+constexpr int kDThreads = 128 + 32 * kDEpiWarps;        // warpgroup 0: TMA, MMA; 1-2: epilogue
+constexpr int kDStageBytes = kDEpiWarps * 32 * 32 * 4;   // 32 KB
+// registers per thread after setmaxnreg: producer warpgroup / epilogue warpgroups
+// (128 x 56 + 256 x 224 = 64512 = 384 x 168, the registers given at launch)
+constexpr int kDRegsProd = 56, kDRegsEpi = 224;
 
-// Epilogue staging: each of the four epilogue warps passes its 32 rows through
-// an 8 KB buffer [32 rows][16 float4] in shared memory, float4 chunk c of row r
-// at position c ^ (r & 15) (conflict-free both for a lane writing its own row
-// and for 16 lanes reading one row), so that global reads and writes run along
-// rows (a lane holding a whole row would touch 32 rows per warp access).
-constexpr int kDStageBytes = 4 * 32 * 64 * 4;
-constexpr int kEpiU = 4;   // row pairs per pass of the staged epilogue
+__host__ __device__ constexpr int dense_smem_bytes(int stages, int planes) {
+  return 1024 + stages * dense_slot_bytes(planes) + kDStageBytes + 8 * (2 * stages + 4) + 16;
+}
 
 __device__ __forceinline__ void stage_put(float4* st, int lane, const float* v, float scale) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c)
-    st[lane * 16 + (c ^ (lane & 15))] =
+  for (int c = 0; c < 8; ++c)
+    st[lane * 8 + (c ^ (lane & 7))] =
         make_float4(v[4 * c] * scale, v[4 * c + 1] * scale, v[4 * c + 2] * scale, v[4 * c + 3] * scale);
 }
 
-// One staged 64-column half of the warp's rows row0 .. row0 + 31: output
-// columns n0 .. n0 + 63 (feature columns of the split planes for the
-// E_*_SPLIT epilogues).  Lane l takes float4 chunk l & 15 of rows 2i + (l >> 4);
+// One staged 32-column quarter of the warp's rows row0 .. row0 + 31: output
+// columns n0 .. n0 + 31 (feature columns of the split planes for the
+// E_*_SPLIT epilogues).  Lane l takes float4 chunk l & 7 of rows 4i + (l >> 3);
 // the loads of 8 rows are issued before their stores.
-__device__ __forceinline__ void epi_half(const DenseArgs& a, const float4* st, int row0, int n0, int lane) {
-  const int c = lane & 15, rsub = lane >> 4;
+__device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st, int row0, int n0, int lane) {
+  const int c = lane & 7, rsub = lane >> 3;
   const int col = n0 + 4 * c;
   float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
   if (a.epi == E_STORE && a.bias) bias = *reinterpret_cast<const float4*>(a.bias + col);
 #pragma unroll 1
-  for (int i0 = 0; i0 < 32; i0 += 2 * kEpiU) {
-    float4 x[kEpiU], g[kEpiU];
+  for (int i0 = 0; i0 < 32; i0 += 8) {
+    float4 x[2], g[2];
 #pragma unroll
-    for (int u = 0; u < kEpiU; ++u) {
-      const int row = row0 + i0 + 2 * u + rsub;
+    for (int u = 0; u < 2; ++u) {
+      const int row = row0 + i0 + 4 * u + rsub;
       x[u] = g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (row < a.M && (a.epi == E_RESID || a.epi == E_RESID_GATE))
         x[u] = *reinterpret_cast<const float4*>(a.out + (size_t)row * a.ldo + col);
@@ -106,10 +114,10 @@ __device__ __forceinline__ void epi_half(const DenseArgs& a, const float4* st, i
         g[u] = *reinterpret_cast<const float4*>(a.gate + a.gate_off[row / a.rows_per_chunk] + col);
     }
 #pragma unroll
-    for (int u = 0; u < kEpiU; ++u) {
-      const int r0 = i0 + 2 * u + rsub, row = row0 + r0;
+    for (int u = 0; u < 2; ++u) {
+      const int r0 = i0 + 4 * u + rsub, row = row0 + r0;
       if (row >= a.M) continue;
-      float4 r = st[r0 * 16 + (c ^ (r0 & 15))];
+      float4 r = st[r0 * 8 + (c ^ (r0 & 7))];
       if (a.epi == E_GELU_SPLIT || a.epi == E_GEGLU_SPLIT) {
         if (a.epi == E_GELU_SPLIT) {
           r.x = gelu_tanh(r.x); r.y = gelu_tanh(r.y); r.z = gelu_tanh(r.z); r.w = gelu_tanh(r.w);
@@ -136,46 +144,50 @@ __device__ __forceinline__ void epi_half(const DenseArgs& a, const float4* st, i
 }
 
 // Epilogue of one tile for the warp's 32 rows (lane l holds the 128
-// accumulated columns of row row0 + l), feature tile tn; the accumulators are
-// scaled by a.out_scale (a power of two: exact) on the way.  All lanes take part.
-__device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[128], int row0, int tn, float4* st,
-                                               int lane) {
+// accumulated columns of row row0 + l): output columns n0 .. n0 + 127, or for
+// the gate/up tile of E_GEGLU_SPLIT ([64 gate | 64 up] of features f0 ..
+// f0 + 63) those features.  The accumulators are scaled by a.out_scale (a
+// power of two: exact) on the way.  All lanes take part.
+__device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[128], int row0, int n0, int f0,
+                                               float4* st, int lane) {
   if (a.epi == E_GEGLU_SPLIT) {
-    // columns 0..63 gate, 64..127 up of features tn*64 + j
 #pragma unroll
     for (int j = 0; j < 64; ++j) acc[j] = gelu_tanh(acc[j] * a.out_scale) * (acc[64 + j] * a.out_scale);
-    stage_put(st, lane, acc, 1.f);
-    __syncwarp();
-    epi_half(a, st, row0, tn * 64, lane);
-    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      stage_put(st, lane, acc + 32 * q, 1.f);
+      __syncwarp();
+      epi_quarter(a, st, row0, f0 + 32 * q, lane);
+      __syncwarp();
+    }
     return;
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    stage_put(st, lane, acc + 64 * h, a.out_scale);
+  for (int q = 0; q < 4; ++q) {
+    stage_put(st, lane, acc + 32 * q, a.out_scale);
     __syncwarp();
-    epi_half(a, st, row0, tn * 128 + 64 * h, lane);
+    epi_quarter(a, st, row0, n0 + 32 * q, lane);
     __syncwarp();
   }
 }
 
 template <int STAGES, int PLANES>
-__global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
-                                                            const __grid_constant__ CUtensorMap wmap,
-                                                            const __grid_constant__ DenseArgs a) {
+__global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                  const __grid_constant__ CUtensorMap wmap,
+                                                                  const __grid_constant__ DenseArgs a) {
   constexpr int kSlot = dense_slot_bytes(PLANES);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float4* stage = reinterpret_cast<float4*>(smem + STAGES * kSlot);   // epilogue staging, 8 KB per warp
+  float4* stage = reinterpret_cast<float4*>(smem + STAGES * kSlot);   // epilogue staging, 4 KB per warp
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kSlot + kDStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
-  uint64_t* acc_full = bars + 2 * STAGES;    // [2]
+  uint64_t* acc_full = bars + 2 * STAGES;       // [2]
   uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = a.N / 128;
+  const int n_tiles = a.N / 256;
   const int tiles = ((a.M + 127) / 128) * n_tiles;
   const int nkb = a.K / 64;                                   // K-blocks of one plane
   const int chunk_kb = kChunkMMA / (4 * a.terms);             // K-blocks per accumulation chunk
@@ -188,12 +200,12 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
-    mbar_init(&acc_empty[0], 128);
-    mbar_init(&acc_empty[1], 128);
+    mbar_init(&acc_empty[0], 32 * kDEpiWarps);
+    mbar_init(&acc_empty[1], 32 * kDEpiWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);   // two 256-column accumulators
     tmem_relinquish();
   }
   tc_fence_before();
@@ -204,8 +216,9 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
   // persistent: CTA b takes tiles b, b + grid, ...; the slot ring and the two
   // accumulators carry on across tiles, so a tile's epilogue overlaps the next
   // tile's MMAs (counters it / gch run over all tiles of the CTA)
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDRegsProd));
+    if (warp == 0 && lane == 0) {
       tma_prefetch_desc(&amap);
       tma_prefetch_desc(&wmap);
       const uint64_t pol_w = l2_policy_evict_last();   // weight tiles are re-read by every m-tile
@@ -222,15 +235,15 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
           mbar_arrive_expect_tx(&full[s], a.terms * kDA + kDB);
           for (int t = 0; t < a.terms; ++t)
             tma_load_2d(slot + t * kDA, &amap, &full[s], t * a.K + i * 64, tm * 128, pol_a);
-          tma_load_2d(slot + PLANES * kDA, &wmap, &full[s], i * 64, a.w_row0 + tn * 128, pol_w);
+          // the weight tile's 256 rows in two 128-row boxes (contiguous in the swizzled layout)
+          tma_load_2d(slot + PLANES * kDA, &wmap, &full[s], i * 64, a.w_row0 + tn * 256, pol_w);
+          tma_load_2d(slot + PLANES * kDA + kDB / 2, &wmap, &full[s], i * 64, a.w_row0 + tn * 256 + 128, pol_w);
         }
       }
       for (uint32_t i = (it > (uint32_t)STAGES ? it - STAGES : 0); i < it; ++i)
         mbar_wait(&full[i % STAGES], (i / STAGES) & 1, a.err, 21);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = a.f16 ? idesc_f16_f32(128, 128) : idesc_bf16_f32(128, 128);
+    } else if (warp == 1 && lane == 0) {
+      const uint32_t idesc = a.f16 ? idesc_f16_f32(128, 256) : idesc_bf16_f32(128, 256);
       bool ok = true;
       uint32_t it = 0, gch = 0;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -239,7 +252,7 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
           // the epilogue has drained this accumulator (use gch - 2)
           if (!mbar_wait(&acc_empty[buf], ((gch >> 1) & 1) ^ 1, a.err, 24)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(buf * 128);
+          const uint32_t d = tmem + (uint32_t)(buf * 256);
           const int i0 = ch * chunk_kb, i1 = min(nkb, i0 + chunk_kb);
           for (int i = i0; i < i1; ++i, ++it) {
             const int s = it % STAGES;
@@ -261,8 +274,10 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
       }
     }
   } else {
-    const int quad = warp & 3;
-    float4* st = stage + quad * 32 * 16;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDRegsEpi));
+    const int ew = warp - 4;
+    const int quad = warp & 3, hc = ew >> 2;   // TMEM lane quadrant, column half
+    float4* st = stage + ew * 32 * 8;
     uint32_t gch = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
         // warp-uniform outcome: the TMEM loads below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (gch >> 1) & 1, a.err, 23))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 128);
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + hc * 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           float v[16];
@@ -287,14 +302,14 @@ __global__ void __launch_bounds__(192, 1) dense_gemm_kernel(const __grid_constan
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
-      if (ok) dense_epilogue(a, acc, row0, tn, st, lane);
+      if (ok) dense_epilogue(a, acc, row0, tn * 256 + hc * 128, tn * 128 + hc * 64, st, lane);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 

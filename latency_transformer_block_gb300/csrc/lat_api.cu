@@ -283,7 +283,7 @@ static lat_status check_desc(const lat_model_desc* d) {
     if (d->act_dim <= 0) return fail(LAT_ERR_SHAPE, "act_dim must be positive");
     return LAT_OK;
   }
-  // dense kinds: 128 x 128 x 64 tiles
+  // dense kinds: 128 x 256 x 64 tiles (every projection width a multiple of 256)
   if (d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 128 or 256 for the dense path");
   if (d->D <= 0 || d->D % 256) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 256");
   if ((d->Hq * d->dh) % 256) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 256");
@@ -672,8 +672,8 @@ static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, floa
 // ---------------------------------------------------------------------------
 // dense path: prefix prefill and DiT stage
 // ---------------------------------------------------------------------------
-// four pipeline slots of two activation planes + one weight tile (48 KB each)
-static constexpr int kDStages = 4;
+// three pipeline slots of two activation planes + one 256-row weight tile (64 KB each)
+static constexpr int kDStages = 3;
 
 // weight of a dense projection: the four fp16 block projections, or the bf16
 // patch embedding (prefix prefill, one plain bf16 activation plane)
@@ -684,10 +684,11 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
   a.err = c->err;
   a.f16 = wsel != W_PATCH;
   a.out_scale = wsel != W_PATCH ? c->wscale[wsel] : 1.f;
-  const int tiles = ((a.M + 127) / 128) * (a.N / 128);
+  if (a.N % 256 || a.K % 64 || a.terms < 1 || a.terms > kActTerms) return fail(LAT_ERR_SHAPE, "dense GEMM shape");
+  const int tiles = ((a.M + 127) / 128) * (a.N / 256);
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
-  dense_gemm_kernel<kDStages, kActTerms><<<grid, 192, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel],
-                                                                                                   a);
+  dense_gemm_kernel<kDStages, kActTerms>
+      <<<grid, kDThreads, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel], a);
   return launch_check("dense_gemm");
 }
 
