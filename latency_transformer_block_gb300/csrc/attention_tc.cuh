@@ -1,21 +1,36 @@
 // Segmented attention on the 5th-generation tensor cores (tcgen05, TMEM) for
 // the dense path's MHA with dh = 128 (the DiT stage): a chunk of query rows
 // attends to its noisy history segments (bf16 ring slots) and to its own keys
-// as computed (fp32, two bf16 planes).  Same inputs, outputs and arithmetic
-// as attention_seg_kernel (exact three-term q and P, own keys in two planes,
-// online softmax in base 2, fp32 accumulation), with the products on tcgen05:
+// as computed (fp32).  Online softmax in base 2, fp32 accumulation; the
+// operands enter the tensor cores in fp16:
 //
-//   S  = sum_t Q_t K^T          M = 128 query rows, N = 64 keys, K = 128 dims
-//   O += sum_t P_t V            M = 128 query rows, N = 128 dims, K = 64 keys
-//                               (V as an MN-major operand: dims contiguous, as stored)
+//   q, P       two fp16 planes (hi = fp16(x), lo = fp16(x - hi): 22 bits)
+//   cached K/V the ring's bf16 values converted to fp16 (exact for
+//              2^-14 <= |x| < 65504; below, fp16's subnormal spacing 2^-24)
+//   own K/V    two fp16 planes of the fp32 values
 //
-// One CTA = one (head, group, 128-row tile).  Warp 0 (lane 0) issues the MMAs;
-// warps 1..3 load each key block (K and V by cp.async into the swizzled layout,
-// own keys split into two planes); warps 4..11 hold the rows:
-// warp w reads TMEM lanes 32 (w % 4).., half (w - 4) / 4 of the keys of S and
-// of the columns of O.  The product of one key block lands in TMEM and is
-// added to the running output in fp32 registers, so no TMEM accumulation chain
-// is longer than 20 MMAs.
+//   S  = (Q_hi + Q_lo) K^T  (+ Q_hi K_lo^T for own keys)
+//   O  = (P_hi + P_lo) V    (+ P_hi V_lo for own keys)
+//
+// The dropped cross terms (Q_lo K_lo, P_lo V_lo) are below 2^-22 of the kept
+// ones.  One CTA = one (head, 128-row query tile, group).  Keys run in blocks:
+// 128 cached keys (history segments concatenated, N = 128 for S) or 64 own
+// keys (hi and lo planes in the same buffers).  On this hardware an M = 128
+// MMA costs the same ~152 cycles for N up to 256, so wide blocks matter.
+//
+// Roles: warp 0 (lane 0) issues the MMAs in the order S(0), S(1), PV(0),
+// S(2), PV(1), ... so the tensor core computes S(j+1) while the row warps run
+// the softmax of block j; warps 1..3 load K and V of each block into one of
+// two buffers each (converting to fp16 on the way); warps 4..11 hold the rows:
+// warp w reads TMEM lanes 32 (w % 4) .. + 31, half (w - 4) / 4 of each block's
+// keys and of the output columns.
+//
+// TMEM (512 columns): S of block j in columns 128 (j % 2) ..; the row warps
+// write P of the block back over its own S columns as packed fp16 (per
+// 32-key chunk: 16 columns of P_hi, then 16 of P_lo) and the PV MMA reads it
+// there as its A operand.  The product of one key block, P V, lands in
+// columns 256 + 128 (j % 2) .. and is added to the running output in fp32
+// registers, so no TMEM accumulation chain is longer than 24 MMAs.
 #pragma once
 #include "attention.cuh"
 #include "common.cuh"
@@ -24,18 +39,23 @@
 namespace lat {
 
 constexpr int kTcThreads = 384;
-constexpr int kTcKB = 64;                       // keys per block
-constexpr int kTcQT = 16384;                    // one [128 rows][64] bf16 tile
-constexpr int kTcKT = 8192;                     // one [64 keys][64] bf16 tile
-// shared memory: Q [3 terms][2 k-tiles], K [hi, lo][2 k-tiles], V^T [hi, lo],
-// P [3 terms], row exchange, barriers
+constexpr int kTcKB = 128;                      // cached keys per block
+constexpr int kTcKBO = 64;                      // own keys per block
+constexpr int kTcQT = 16384;                    // one [128 rows][64] 16-bit tile
+constexpr int kTcBuf = 32768;                   // one K or V buffer
+// shared memory: Q [2 planes][2 k-tiles], K [2 buffers], V [2 buffers], row
+// exchange [2 parities][2 halves][128 rows] fp32, barriers
 constexpr int kTcOffQ = 0;
-constexpr int kTcOffK = kTcOffQ + 6 * kTcQT;    // 96 KB
-constexpr int kTcOffV = kTcOffK + 4 * kTcKT;    // +32 KB
-constexpr int kTcOffP = kTcOffV + 2 * kTcQT;    // +32 KB
-constexpr int kTcOffX = kTcOffP + 3 * kTcQT;    // +48 KB
-constexpr int kTcOffBar = kTcOffX + 4 * 128 * 4;   // exchange: [2 parities][2 halves][128 rows]
-constexpr int kTcSmem = 1024 + kTcOffBar + 16 * 8 + 16;
+constexpr int kTcOffK = kTcOffQ + 4 * kTcQT;    // 64 KB
+constexpr int kTcOffV = kTcOffK + 2 * kTcBuf;   // +64 KB
+constexpr int kTcOffX = kTcOffV + 2 * kTcBuf;   // +64 KB
+constexpr int kTcOffBar = kTcOffX + 4 * 128 * 4;
+constexpr int kTcNBar = 24;
+constexpr int kTcOffTab = kTcOffBar + kTcNBar * 8;   // TcSegTab
+constexpr int kTcSmem = 1024 + kTcOffTab + 128 + 16;
+// registers per thread after setmaxnreg: MMA/loader warpgroup, row warpgroups
+// (128 x 104 + 256 x 192 = 62464 <= 384 x 168 = 64512, the registers given at launch)
+constexpr int kTcRegsLoad = 104, kTcRegsRow = 192;
 
 __host__ __device__ constexpr int attn_tc_smem_bytes() { return kTcSmem; }
 
@@ -53,9 +73,47 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t l
   return d;
 }
 
-// byte offset of element (row r, column c < 64) in a K-major 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)(r * 128 + ((((c >> 3) ^ r) & 7) << 4) + ((c & 7) << 1));
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M = 128 lanes x K = 16) read from
+// TMEM, 16-bit elements packed two per 32-bit column.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 bit, 32 consecutive columns per thread, then wait for the store.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 8 bf16 (one uint4) -> 8 fp16
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  auto cv = [](uint32_t w) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
+}
+
+// 8 fp32 -> fp16 hi (8) and lo (8)
+__device__ __forceinline__ void f32x8_to_h2planes(const float4 a, const float4 b, uint4& hi, uint4& lo) {
+  split_pair_h2(a.x, a.y, hi.x, lo.x);
+  split_pair_h2(a.z, a.w, hi.y, lo.y);
+  split_pair_h2(b.x, b.y, hi.z, lo.z);
+  split_pair_h2(b.z, b.w, hi.w, lo.w);
 }
 
 // Bounded wait that also returns at once after any recorded error, so a
@@ -84,63 +142,122 @@ __device__ __forceinline__ void tc_mark(unsigned long long* tr, int role, int j,
   }
 }
 
-// key block j of a group -> (segment, block within the segment)
-__device__ __forceinline__ void tc_block(const SegGroup& G, int j, int& si, int& kb) {
-  si = 0;
-  kb = j;
-  while (si < G.nseg - 1) {
-    const int nb = (G.seg[si].n + kTcKB - 1) / kTcKB;
-    if (kb < nb) break;
-    kb -= nb;
-    ++si;
-  }
-}
+// The key blocks of a group: each cached segment (those without k16) cut
+// into blocks of kTcKB keys, then the own keys (the segment with k16: fp16
+// hi/lo planes) in blocks of kTcKBO.  A block never spans two segments, so
+// each K or V block is one or two TMA boxes.  The per-segment table lives in
+// shared memory (filled by one thread).
+struct TcSegTab {
+  int krow[kMaxSeg];       // first ring row of cached segment s, K plane
+  int vrow[kMaxSeg];       // ... V plane
+  int n[kMaxSeg];          // its keys
+  int blk0[kMaxSeg + 1];   // its first block
+  int own_row;             // first row of the own keys in the own-plane buffer
+};
 
+struct TcKeys {
+  int nseg_c;              // cached segments
+  int own_seg;             // index of the own segment (-1: none)
+  int n_o;                 // own keys
+  int nb_c, nblk;          // cached blocks, all blocks
+  // tab: filled when not null (one thread)
+  __device__ void init(const SegAttnArgs& a, const SegGroup& G, TcSegTab* tab) {
+    nseg_c = 0;
+    n_o = 0;
+    own_seg = -1;
+    nb_c = 0;
+    for (int s = 0; s < G.nseg; ++s) {
+      if (G.seg[s].k16) {
+        own_seg = s;
+        n_o = G.seg[s].n;
+        if (tab) tab->own_row = (int)((G.seg[s].k16 - a.own16) / (4 * (size_t)a.kv_ld));
+      } else {
+        if (tab) {
+          tab->krow[nseg_c] = (int)((G.seg[s].k - a.ring) / (size_t)a.kv_ld);
+          tab->vrow[nseg_c] = (int)((G.seg[s].v - a.ring) / (size_t)a.kv_ld);
+          tab->n[nseg_c] = G.seg[s].n;
+          tab->blk0[nseg_c] = nb_c;
+        }
+        ++nseg_c;
+        nb_c += (G.seg[s].n + kTcKB - 1) / kTcKB;
+      }
+    }
+    if (tab) tab->blk0[nseg_c] = nb_c;
+    nblk = nb_c + (n_o + kTcKBO - 1) / kTcKBO;
+  }
+  __device__ bool own(int j) const { return j >= nb_c; }
+  // cached block j: its segment, first key within the segment and valid keys
+  __device__ void cached(const TcSegTab* tab, int j, int& s, int& k0, int& nv) const {
+    s = 0;
+    while (s + 1 < nseg_c && j >= tab->blk0[s + 1]) ++s;
+    k0 = (j - tab->blk0[s]) * kTcKB;
+    nv = min(kTcKB, tab->n[s] - k0);
+  }
+  // valid keys of block j
+  __device__ int valid(const TcSegTab* tab, int j) const {
+    if (own(j)) return min(kTcKBO, n_o - (j - nb_c) * kTcKBO);
+    int s, k0, nv;
+    cached(tab, j, s, k0, nv);
+    return nv;
+  }
+};
+
+// ring_map: the KV ring as rows of kv_ld bf16 (box 64 x 128, 128-byte swizzle);
+// own_map: the own fp16 planes as rows of 4 kv_ld, [K hi | K lo | V hi | V lo]
+// (box 64 x 64, same swizzle).
 static __global__ void __launch_bounds__(kTcThreads, 1)
-    attention_tc_kernel(const __grid_constant__ SegAttnArgs a, DevErr* err) {
+    attention_tc_kernel(const __grid_constant__ SegAttnArgs a, const __grid_constant__ CUtensorMap ring_map,
+                        const __grid_constant__ CUtensorMap own_map, DevErr* err) {
   constexpr int DH = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm + kTcOffQ;
-  uint8_t* sK = sm + kTcOffK;   // [hi k-tile 0, hi k-tile 1, lo k-tile 0, lo k-tile 1]
-  uint8_t* sV = sm + kTcOffV;   // V [hi, lo] x [2 halves of 64 dims][64 keys][64 dims]
-  uint8_t* sP = sm + kTcOffP;   // [3 terms][128 rows][64 keys]
+  uint8_t* sQ = sm + kTcOffQ;   // [plane][k-tile] of [128 rows][64 dims], K-major, swizzled
+  uint8_t* sK = sm + kTcOffK;   // buffer: cached [k-tile][128 keys][64]; own hi [k-tile][64 keys][64], lo at +16 KB
+  uint8_t* sV = sm + kTcOffV;   // buffer: cached [64-dim half][128 keys][64]; own hi [half][64 keys][64], lo at +16 KB
   float* sX = reinterpret_cast<float*>(sm + kTcOffX);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kTcOffBar);
-  uint64_t* q_full = bar + 0;   // Q planes built (256 arrivals)
-  uint64_t* k_full = bar + 1;   // K block loaded (96)
-  uint64_t* v_full = bar + 2;   // V block loaded (96)
-  uint64_t* k_free = bar + 3;   // S MMAs done with K (commit)
-  uint64_t* v_free = bar + 4;   // PV MMAs done with V and P (commit)
-  uint64_t* s_full = bar + 5;   // S in TMEM (commit)
-  uint64_t* s_free = bar + 6;   // S read by the row warps (256)
-  uint64_t* p_full = bar + 7;   // P written, previous O read (256)
-  uint64_t* o_full = bar + 8;   // O of the block in TMEM (commit)
-  uint64_t* mdone = bar + 9;    // every MMA complete (teardown)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 10);
+  uint64_t* q_full = bar + 0;    // Q planes built (256 arrivals)
+  uint64_t* k_full = bar + 1;    // [2] K block loaded (64: warps 1, 2)
+  uint64_t* k_free = bar + 3;    // [2] S MMAs done with the K buffer (commit)
+  uint64_t* v_full = bar + 5;    // [2] V block loaded (32: warp 3)
+  uint64_t* v_free = bar + 7;    // [2] PV MMAs done with the V buffer (commit)
+  uint64_t* s_full = bar + 9;    // [2] S in TMEM (commit)
+  uint64_t* p_full = bar + 11;   // [2] P written over S (256)
+  uint64_t* o_full = bar + 13;   // [2] P V of the block in TMEM (commit)
+  uint64_t* o_free = bar + 15;   // [2] P V read by the row warps (256)
+  uint64_t* mdone = bar + 17;    // every MMA complete (teardown)
+  uint64_t* kt_full = bar + 18;  // [2] TMA of the K block landed (1 + bytes)
+  uint64_t* vt_full = bar + 20;  // [2] TMA of the V block landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 22);
+  TcSegTab* tab = reinterpret_cast<TcSegTab*>(sm + kTcOffTab);
 
   const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = h / (a.Hq / a.Hkv);
   const SegGroup& G = a.grp[b];
-  int nblk = 0;
-  for (int si = 0; si < G.nseg; ++si) nblk += (G.seg[si].n + kTcKB - 1) / kTcKB;
+  TcKeys kk;
+  kk.init(a, G, threadIdx.x == 0 ? tab : nullptr);
+  const int nblk = kk.nblk;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 256);
-    mbar_init(k_full, 96);
-    mbar_init(v_full, 96);
-    mbar_init(k_free, 1);
-    mbar_init(v_free, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
-    mbar_init(p_full, 256);
-    mbar_init(o_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 64);
+      mbar_init(&k_free[i], 1);
+      mbar_init(&v_full[i], 32);
+      mbar_init(&v_free[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 256);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 256);
+      mbar_init(&kt_full[i], 1);
+      mbar_init(&vt_full[i], 1);
+    }
     mbar_init(mdone, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 256);   // S at columns [0, 64), O of a block at [128, 256)
+    tmem_alloc(tmem_slot, 512);   // S/P [2 x 128], P V [2 x 128]
     tmem_relinquish();
   }
   tc_fence_before();
@@ -148,166 +265,177 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- MMA issue: S(0), then per block PV(j), S(j + 1) ----------------
-      const uint32_t idS = idesc_bf16_f32(128, kTcKB), idO = idesc_bf16_f32(128, DH) | (1u << 16);   // B MN-major
-      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
-      bool ok = tc_wait(q_full, 0, err, 60);
-      auto issue_s = [&](int j) {
-        int si, kb;
-        tc_block(G, j, si, kb);
-        const bool own = G.seg[si].k32 != nullptr;
-        if (!tc_wait(k_full, j & 1, err, 61)) return false;
-        tc_mark(a.trace, 0, j, 0);
-        if (j > 0 && !tc_wait(s_free, (j - 1) & 1, err, 62)) return false;
-        tc_mark(a.trace, 0, j, 1);
-        tc_fence_after();
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcRegsLoad));
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------- MMA issue: S(0), S(1), PV(0), S(2), PV(1), ... ----------------
+        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
+        const uint32_t idO = idesc_f16_f32(128, DH) | (1u << 16);   // B (V) MN-major
+        auto issue_s = [&](int j) -> bool {
+          const int bf = j & 1;
+          if (!tc_wait(&k_full[bf], (j >> 1) & 1, err, 61)) return false;
+          tc_mark(a.trace, 0, j, 0);
+          tc_fence_after();
+          const bool own = kk.own(j);
+          const uint32_t kb = ka + (uint32_t)(bf * kTcBuf);
+          const uint32_t kts = own ? 8192u : 16384u;   // k-tile stride: keys x 128 B
+          const uint32_t idS = idesc_f16_f32(128, own ? kTcKBO : kTcKB);
+          const uint32_t d = tmem + (uint32_t)(bf * 128);
 #pragma unroll
-        for (int ks = 0; ks < DH / 16; ++ks) {
-          const int kt = ks >> 2;
-          const uint32_t off = (uint32_t)((ks & 3) * 32);
-#pragma unroll
-          for (int t = 0; t < 3; ++t)
-            mma_bf16_ss(tmem, desc_k_sw128(qa + (t * 2 + kt) * kTcQT + off), desc_k_sw128(ka + kt * kTcKT + off), idS,
-                        (ks | t) != 0 ? 1u : 0u);
-          if (own)
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              mma_bf16_ss(tmem, desc_k_sw128(qa + (t * 2 + kt) * kTcQT + off),
-                          desc_k_sw128(ka + (2 + kt) * kTcKT + off), idS, 1u);
+          for (int s = 0; s < DH / 16; ++s) {   // dims 16 s .. 16 s + 15
+            const uint32_t kt = (uint32_t)(s >> 2), off = (uint32_t)((s & 3) * 32);
+            const uint64_t bk = desc_k_sw128(kb + kt * kts + off);
+            mma_bf16_ss(d, desc_k_sw128(qa + kt * kTcQT + off), bk, idS, s != 0 ? 1u : 0u);   // Q_hi K
+            mma_bf16_ss(d, desc_k_sw128(qa + (2 + kt) * kTcQT + off), bk, idS, 1u);          // Q_lo K
+            if (own)                                                                          // Q_hi K_lo
+              mma_bf16_ss(d, desc_k_sw128(qa + kt * kTcQT + off), desc_k_sw128(kb + 16384u + kt * kts + off), idS,
+                          1u);
+          }
+          mma_commit(&k_free[bf]);
+          mma_commit(&s_full[bf]);
+          return true;
+        };
+        auto issue_pv = [&](int j) -> bool {
+          const int bf = j & 1;
+          const uint32_t par = (uint32_t)(j >> 1) & 1u;
+          if (!tc_wait(&p_full[bf], par, err, 62) || !tc_wait(&v_full[bf], par, err, 63)) return false;
+          if (j >= 2 && !tc_wait(&o_free[bf], par ^ 1u, err, 64)) return false;
+          tc_mark(a.trace, 0, j, 1);
+          tc_fence_after();
+          const bool own = kk.own(j);
+          const int nk = own ? kTcKBO : kTcKB;
+          const uint32_t vb = va + (uint32_t)(bf * kTcBuf);
+          const uint32_t lbo = own ? 8192u : 16384u;   // bytes between the two 64-dim halves of V
+          const uint32_t ps = tmem + (uint32_t)(bf * 128);
+          const uint32_t d = tmem + 256u + (uint32_t)(bf * 128);
+          for (int i = 0; i < nk / 16; ++i) {   // keys 16 i .. 16 i + 15
+            const uint32_t ph = ps + (uint32_t)(32 * (i >> 1) + 8 * (i & 1));   // P_hi; P_lo at + 16
+            const uint64_t bv = desc_mn_sw128(vb + (uint32_t)i * 2048u, lbo, 1024);
+            mma_f16_ts(d, ph, bv, idO, i != 0 ? 1u : 0u);   // P_hi V
+            mma_f16_ts(d, ph + 16u, bv, idO, 1u);           // P_lo V
+            if (own)                                         // P_hi V_lo
+              mma_f16_ts(d, ph, desc_mn_sw128(vb + 16384u + (uint32_t)i * 2048u, lbo, 1024), idO, 1u);
+          }
+          mma_commit(&v_free[bf]);
+          mma_commit(&o_full[bf]);
+          return true;
+        };
+        bool ok = tc_wait(q_full, 0, err, 60);
+        for (int j = 0; j <= nblk && ok; ++j) {
+          if (j < nblk) ok = issue_s(j);
+          if (ok && j >= 1) ok = issue_pv(j - 1);
         }
-        mma_commit(k_free);
-        mma_commit(s_full);
-        tc_mark(a.trace, 0, j, 2);
-        return true;
-      };
-      if (ok && nblk > 0) ok = issue_s(0);
+        mma_commit(mdone);
+        mbar_wait(mdone, 0, nullptr, 0);
+      }
+    } else {
+      // ---------------- loaders: K (warps 1, 2) and V (warp 3) of each block ----------------
+      // One thread of the group moves the block by TMA (cached: two 128-row
+      // boxes of bf16 ring rows; own: two 64-row boxes of each fp16 plane) into
+      // the swizzled operand layout; then every thread of the group converts
+      // its chunks of a cached block from bf16 to fp16 in place and zeroes the
+      // rows past the block's valid keys (whatever the neighbouring rows hold).
+      const bool isv = warp == 3;
+      const int tid = isv ? lane : threadIdx.x - 32, nthr = isv ? 32 : 64;
+      uint8_t* const base = isv ? sV : sK;
+      uint64_t* const full = isv ? v_full : k_full;
+      uint64_t* const tfull = isv ? vt_full : kt_full;
+      uint64_t* const freed = isv ? v_free : k_free;
+      if (tid == 0) {
+        tma_prefetch_desc(&ring_map);
+        tma_prefetch_desc(&own_map);
+      }
+      const uint64_t pol = l2_policy_evict_last();   // every query tile of the head re-reads the block
+      bool ok = true;
       for (int j = 0; j < nblk && ok; ++j) {
-        int si, kb;
-        tc_block(G, j, si, kb);
-        const bool own = G.seg[si].k32 != nullptr;
-        if (!tc_wait(p_full, j & 1, err, 63)) {
+        const int bf = j & 1;
+        const uint32_t par = (uint32_t)(j >> 1) & 1u;
+        if (j >= 2 && !tc_wait(&freed[bf], par ^ 1u, err, isv ? 66 : 65)) {
           ok = false;
           break;
         }
-        tc_mark(a.trace, 0, j, 3);
-        if (!tc_wait(v_full, j & 1, err, 64)) {
-          ok = false;
-          break;
-        }
-        tc_mark(a.trace, 0, j, 4);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTcKB / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk * 32);
-          const uint32_t voff = (uint32_t)(kk * 2048);   // 16 keys = two 8-key atoms
-#pragma unroll
-          for (int t = 0; t < 3; ++t)
-            mma_bf16_ss(tmem + 128, desc_k_sw128(pa + t * kTcQT + off), desc_mn_sw128(va + voff, kTcKT, 1024), idO,
-                        (kk | t) != 0 ? 1u : 0u);
-          if (own)
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-              mma_bf16_ss(tmem + 128, desc_k_sw128(pa + t * kTcQT + off),
-                          desc_mn_sw128(va + kTcQT + voff, kTcKT, 1024), idO, 1u);
-        }
-        mma_commit(v_free);
-        mma_commit(o_full);
-        // S of the next block: its K was loaded while the rows ran block j
-        if (j + 1 < nblk && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-      }
-      mma_commit(mdone);
-      mbar_wait(mdone, 0, nullptr, 0);
-    }
-  } else if (warp < 4) {
-    // ---------------- loaders: K and V of each key block ----------------
-    const int lt = threadIdx.x - 32;
-    bool ok = true;
-    for (int j = 0; j < nblk && ok; ++j) {
-      int si, kb;
-      tc_block(G, j, si, kb);
-      const AttnSeg sg = G.seg[si];
-      const bool own = sg.k32 != nullptr;
-      const int k0 = kb * kTcKB;
-      if (j > 0 && !tc_wait(k_free, (j - 1) & 1, err, 65)) {
-        ok = false;
-        break;
-      }
-      if (lt == 0) tc_mark(a.trace, 2, j, 0);
-      fence_proxy_async_smem();
-      for (int it = lt; it < kTcKB * (DH / 8); it += 96) {
-        const int r = it >> 4, c = it & 15;       // key row, 8-dim chunk
-        const int key = k0 + r;
-        const bool in = key < sg.n;
-        const size_t off = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c * 8;
-        uint8_t* dst = sK + (c >> 3) * kTcKT + r * 128 + ((((c & 7) ^ r) & 7) << 4);
+        if (tid == 0) tc_mark(a.trace, 2, j, isv ? 2 : 0);
+        uint8_t* dst = base + bf * kTcBuf;
+        const bool own = kk.own(j);
+        int nv;
+        if (tid == 0) fence_proxy_async_smem();
         if (!own) {
-          cp_async16(dst, sg.k + off, in ? 16 : 0);
+          int s, k0;
+          kk.cached(tab, j, s, k0, nv);
+          if (tid == 0) {
+            const int row = (isv ? tab->vrow[s] : tab->krow[s]) + k0;
+            mbar_arrive_expect_tx(&tfull[bf], kTcBuf);
+            tma_load_2d(dst, &ring_map, &tfull[bf], kvh * DH, row, pol);
+            tma_load_2d(dst + 16384, &ring_map, &tfull[bf], kvh * DH + 64, row, pol);
+          }
         } else {
-          uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
-          if (in) split8_to(sg.k32 + off, hi, lo);
-          *reinterpret_cast<uint4*>(dst) = hi;
-          *reinterpret_cast<uint4*>(dst + 2 * kTcKT) = lo;
+          const int k0 = (j - kk.nb_c) * kTcKBO;
+          nv = min(kTcKBO, kk.n_o - k0);
+          if (tid == 0) {
+            // own-plane rows: [K hi | K lo | V hi | V lo], kv_ld columns each
+            const int row = tab->own_row + k0, xh = (isv ? 2 * a.kv_ld : 0) + kvh * DH, xl = xh + a.kv_ld;
+            mbar_arrive_expect_tx(&tfull[bf], kTcBuf);
+            tma_load_2d(dst, &own_map, &tfull[bf], xh, row, pol);
+            tma_load_2d(dst + 8192, &own_map, &tfull[bf], xh + 64, row, pol);
+            tma_load_2d(dst + 16384, &own_map, &tfull[bf], xl, row, pol);
+            tma_load_2d(dst + 16384 + 8192, &own_map, &tfull[bf], xl + 64, row, pol);
+          }
         }
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      if (lt == 0) tc_mark(a.trace, 2, j, 1);
-      mbar_arrive(k_full);
-      if (j > 0 && !tc_wait(v_free, (j - 1) & 1, err, 66)) {
-        ok = false;
-        break;
-      }
-      if (lt == 0) tc_mark(a.trace, 2, j, 2);
-      fence_proxy_async_smem();
-      for (int it = lt; it < kTcKB * (DH / 8); it += 96) {
-        const int r = it >> 4, c = it & 15;       // key row, 8-dim chunk
-        const int key = k0 + r;
-        const bool in = key < sg.n;
-        const size_t off = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c * 8;
-        uint8_t* dst = sV + (c >> 3) * kTcKT + r * 128 + ((((c & 7) ^ r) & 7) << 4);
-        if (!own) {
-          cp_async16(dst, sg.v + off, in ? 16 : 0);
-        } else {
-          uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
-          if (in) split8_to(sg.v32 + off, hi, lo);
-          *reinterpret_cast<uint4*>(dst) = hi;
-          *reinterpret_cast<uint4*>(dst + kTcQT) = lo;
+        if (!tc_wait(&tfull[bf], par, err, isv ? 70 : 69)) {
+          ok = false;
+          break;
         }
+        if (!own) {   // 2048 chunks, a multiple of 8 x nthr: 8 shared-memory loads in flight
+          for (int i0 = tid; i0 < kTcKB * 16; i0 += 8 * nthr) {
+            uint4 v[8];
+            int off[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int it = i0 + u * nthr, r = it >> 4, c = it & 15;
+              off[u] = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+              v[u] = *reinterpret_cast<const uint4*>(dst + off[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int r = (i0 + u * nthr) >> 4;
+              *reinterpret_cast<uint4*>(dst + off[u]) = r < nv ? bf16x8_to_f16x8(v[u]) : make_uint4(0, 0, 0, 0);
+            }
+          }
+        } else if (nv < kTcKBO) {
+          for (int it = tid; it < kTcKBO * 16; it += nthr) {
+            const int r = it >> 4, c = it & 15;
+            if (r < nv) continue;
+            const int off = (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dst + 16384 + off) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        if (tid == 0) tc_mark(a.trace, 2, j, isv ? 3 : 1);
+        mbar_arrive(&full[bf]);
       }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      if (lt == 0) tc_mark(a.trace, 2, j, 3);
-      mbar_arrive(v_full);
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcRegsRow));
     // ---------------- row warps ----------------
     const int st = threadIdx.x - 128;
-    const int qd = warp & 3, half = (warp - 4) >> 2;
-    const int r = qd * 32 + lane;                    // row of the tile = TMEM lane
+    const int quad = warp & 3, half = (warp - 4) >> 2;
+    const int r = quad * 32 + lane;                  // row of the tile = TMEM lane
     const int rg = qt * 128 + r;                     // row within the group
-    // Q planes (exact three-term split) for the tile's 128 rows
+    // Q planes (fp16 hi, lo) for the tile's 128 rows
     for (int it = st; it < 128 * (DH / 8); it += 256) {
       const int rr = it >> 4, c = it & 15;
       const int rq = qt * 128 + rr;
-      uint4 hv = make_uint4(0, 0, 0, 0), mv = hv, lv = hv;
+      uint4 hv = make_uint4(0, 0, 0, 0), lv = hv;
       if (rq < a.T_rows) {
         const float* src = a.q + ((size_t)b * a.T_rows + rq) * a.q_ld + h * DH + c * 8;
-        const float4 x0 = *reinterpret_cast<const float4*>(src);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-        split_pair_exact(x0.x, x0.y, hv.x, mv.x, lv.x);
-        split_pair_exact(x0.z, x0.w, hv.y, mv.y, lv.y);
-        split_pair_exact(x1.x, x1.y, hv.z, mv.z, lv.z);
-        split_pair_exact(x1.z, x1.w, hv.w, mv.w, lv.w);
+        f32x8_to_h2planes(__ldg(reinterpret_cast<const float4*>(src)), __ldg(reinterpret_cast<const float4*>(src + 4)),
+                          hv, lv);
       }
-      const uint32_t o = (uint32_t)((c >> 3) * kTcQT + rr * 128 + ((((c & 7) ^ rr) & 7) << 4));
+      const int o = (c >> 3) * kTcQT + rr * 128 + (((c & 7) ^ (rr & 7)) << 4);
       *reinterpret_cast<uint4*>(sQ + o) = hv;
-      *reinterpret_cast<uint4*>(sQ + 2 * kTcQT + o) = mv;
-      *reinterpret_cast<uint4*>(sQ + 4 * kTcQT + o) = lv;
+      *reinterpret_cast<uint4*>(sQ + 2 * kTcQT + o) = lv;
     }
     fence_proxy_async_smem();
     mbar_arrive(q_full);
@@ -316,81 +444,76 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int i = 0; i < 64; ++i) o[i] = 0.f;
     float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
-    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-    for (int j = 0; j < nblk; ++j) {
-      int si, kb;
-      tc_block(G, j, si, kb);
-      const int n = G.seg[si].n, k0 = kb * kTcKB;
-      tc_wait(s_full, j & 1, err, 67);
-      if (st == 0) tc_mark(a.trace, 1, j, 0);
-      tc_fence_after();
-      float sv[32];
-      tmem_ld32(trow + (uint32_t)(half * 32), sv);
-      tc_fence_before();
-      mbar_arrive(s_free);
-      float mloc = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sv[i] = (k0 + half * 32 + i < n) ? sv[i] * a.scale_log2 : -INFINITY;
-        mloc = fmaxf(mloc, sv[i]);
-      }
-      float* xb = sX + (j & 1) * 256;
-      xb[half * 128 + r] = mloc;
-      named_sync(4, 256);
-      if (st == 0) tc_mark(a.trace, 1, j, 1);
-      const float mnew = fmaxf(m, fmaxf(mloc, xb[(half ^ 1) * 128 + r]));
-      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mnew);
-      float lsum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sv[i] = exp2f(sv[i] - mnew);
-        lsum += sv[i];
-      }
-      l = l * alpha + lsum;
-      m = mnew;
-      if (j > 0) {   // O of block j - 1 into the running output (frees P and the O columns)
-        tc_wait(o_full, (j - 1) & 1, err, 68);
-        if (st == 0) tc_mark(a.trace, 1, j, 2);
-        tc_fence_after();
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          float t[32];
-          tmem_ld32(trow + 128u + (uint32_t)(half * 64 + c2 * 32), t);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = o[c2 * 32 + i] * alpha_prev + t[i];
-        }
-      }
-      alpha_prev = alpha;
-      // P of this block: exact three-term split, keys half*32 .. +31 of row r
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint4 hv, mv, lv;
-        split_pair_exact(sv[8 * c4 + 0], sv[8 * c4 + 1], hv.x, mv.x, lv.x);
-        split_pair_exact(sv[8 * c4 + 2], sv[8 * c4 + 3], hv.y, mv.y, lv.y);
-        split_pair_exact(sv[8 * c4 + 4], sv[8 * c4 + 5], hv.z, mv.z, lv.z);
-        split_pair_exact(sv[8 * c4 + 6], sv[8 * c4 + 7], hv.w, mv.w, lv.w);
-        const uint32_t off = (uint32_t)(r * 128 + ((((half * 4 + c4) ^ r) & 7) << 4));
-        *reinterpret_cast<uint4*>(sP + off) = hv;
-        *reinterpret_cast<uint4*>(sP + kTcQT + off) = mv;
-        *reinterpret_cast<uint4*>(sP + 2 * kTcQT + off) = lv;
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      if (st == 0) tc_mark(a.trace, 1, j, 3);
-      mbar_arrive(p_full);
-    }
-    if (nblk > 0) {
-      tc_wait(o_full, (nblk - 1) & 1, err, 69);
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    // P V of block jb into the running output (then the columns are free again)
+    auto add_o = [&](int jb) {
+      const int bf = jb & 1;
+      tc_wait(&o_full[bf], (uint32_t)(jb >> 1) & 1u, err, 68);
       tc_fence_after();
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         float t[32];
-        tmem_ld32(trow + 128u + (uint32_t)(half * 64 + c2 * 32), t);
+        tmem_ld32(trow + 256u + (uint32_t)(bf * 128 + half * 64 + c2 * 32), t);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = o[c2 * 32 + i] * alpha_prev + t[i];
       }
       tc_fence_before();
+      mbar_arrive(&o_free[bf]);
+    };
+    for (int j = 0; j < nblk; ++j) {
+      const int bf = j & 1;
+      const bool own = kk.own(j);
+      const int nh = (own ? kTcKBO : kTcKB) / 2;     // keys of this thread's half
+      const int k0 = half * nh, nv = kk.valid(tab, j);
+      tc_wait(&s_full[bf], (uint32_t)(j >> 1) & 1u, err, 67);
+      if (st == 0) tc_mark(a.trace, 1, j, 0);
+      tc_fence_after();
+      const uint32_t sb = trow + (uint32_t)(bf * 128 + k0);   // S (then P) columns of my keys
+      float s[2][32];
+      tmem_ld32(sb, s[0]);
+      if (!own) tmem_ld32(sb + 32u, s[1]);
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + ch * 32 + i;
+          s[ch][i] = (ch * 32 + i < nh && key < nv) ? s[ch][i] * a.scale_log2 : -INFINITY;
+          mloc = fmaxf(mloc, s[ch][i]);
+        }
+      float* xb = sX + (j & 1) * 256;
+      xb[half * 128 + r] = mloc;
+      named_sync(4, 256);
+      const float mnew = fmaxf(m, fmaxf(mloc, xb[(half ^ 1) * 128 + r]));
+      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mnew);
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[ch][i] = exp2f(s[ch][i] - mnew);
+          lsum += s[ch][i];
+        }
+      l = l * alpha + lsum;
+      m = mnew;
+      if (st == 0) tc_mark(a.trace, 1, j, 1);
+      // P over the S columns: per 32-key chunk 16 columns of P_hi, 16 of P_lo
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        if (ch == 1 && own) break;
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split_pair_h2(s[ch][2 * e], s[ch][2 * e + 1], w[e], w[16 + e]);
+        tmem_st32(sb + (uint32_t)(ch * 32), w);
+      }
+      tc_fence_before();
+      mbar_arrive(&p_full[bf]);
+      if (st == 0) tc_mark(a.trace, 1, j, 2);
+      if (j > 0) add_o(j - 1);
+      if (st == 0) tc_mark(a.trace, 1, j, 3);
+      alpha_prev = alpha;
     }
+    if (nblk > 0) add_o(nblk - 1);
     // the row's sum over both halves of the keys
     float* xl = sX + (nblk & 1) * 256;
     xl[half * 128 + r] = l;
@@ -398,9 +521,9 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     const float lt = l + xl[(half ^ 1) * 128 + r];
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
     if (rg < a.T_rows) {
-      // the two fp16 planes of the output projection's activation
 #pragma unroll
       for (int i = 0; i < 64; ++i) o[i] *= inv;
+      // the two fp16 planes of the output projection's activation
       store_planes<64>(a.out + ((size_t)b * a.T_rows + rg) * kActTerms * a.ldh + h * DH + half * 64, a.ldh, o);
     }
   }
@@ -408,7 +531,7 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 

@@ -103,8 +103,11 @@ struct RopeKvArgs {
   __nv_bfloat16* kdst[kMaxChunks];
   __nv_bfloat16* vdst[kMaxChunks];
   int kv_ld;                // row stride of kdst / vdst (elements)
-  float* k32;               // fp32 K (after RoPE) and V as computed, [M][kv_cols]
+  float* k32;               // fp32 K (after RoPE) and V as computed, [M][kv_cols], or
   float* v32;
+  __half* k16;              // the same as two fp16 planes (hi at column c, lo at kv_cols + c)
+  __half* v16;              // of rows ld16 apart
+  int ld16;
 };
 
 static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
@@ -143,15 +146,31 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
       __nv_bfloat16* kr = a.kdst[b] + (size_t)j * a.kv_ld + (col - a.q_cols);
       kr[0] = __float2bfloat16_rn(y0);
       kr[half] = __float2bfloat16_rn(y1);
-      float* k32 = a.k32 + (size_t)m * a.kv_cols + (col - a.q_cols);
-      k32[0] = y0;
-      k32[half] = y1;
+      if (a.k16) {
+        __half* k16 = a.k16 + (size_t)m * a.ld16 + (col - a.q_cols);
+        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+        k16[0] = h0;
+        k16[half] = h1;
+        k16[a.kv_cols] = __float2half_rn(y0 - __half2float(h0));
+        k16[a.kv_cols + half] = __float2half_rn(y1 - __half2float(h1));
+      } else {
+        float* k32 = a.k32 + (size_t)m * a.kv_cols + (col - a.q_cols);
+        k32[0] = y0;
+        k32[half] = y1;
+      }
     }
   }
   const float* vr = row + a.q_cols + a.kv_cols;
   for (int c = threadIdx.x; c < a.kv_cols; c += blockDim.x) {
     a.vdst[b][(size_t)j * a.kv_ld + c] = __float2bfloat16_rn(vr[c]);
-    a.v32[(size_t)m * a.kv_cols + c] = vr[c];
+    if (a.v16) {
+      __half* v16 = a.v16 + (size_t)m * a.ld16 + c;
+      const __half h = __float2half_rn(vr[c]);
+      v16[0] = h;
+      v16[a.kv_cols] = __float2half_rn(vr[c] - __half2float(h));
+    } else {
+      a.v32[(size_t)m * a.kv_cols + c] = vr[c];
+    }
   }
 }
 

@@ -162,7 +162,8 @@ struct lat_ctx {
   float *bpatch = nullptr, *adaln = nullptr, *cos_j = nullptr, *sin_j = nullptr, *qkvbuf = nullptr,
         *qbuf = nullptr;
   double* theta = nullptr;
-  float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32)
+  float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32; prefix prefill)
+  __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
   __half *act2 = nullptr, *act2f = nullptr;   // fp16 activation planes [M][kActTerms * K]
   // the four block projections (merged QKV, output, FFN in, FFN out) of the dense
   // path are held as fp16 = 2^s x folded bf16 weight; wscale = 2^-s per matrix
@@ -728,8 +729,12 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
   LAT_TRY(c->alloc(&c->act2f, (size_t)c->m_max * terms * d.F));
   LAT_TRY(c->alloc(&c->qkvbuf, (size_t)c->m_max * c->nqkv));
   LAT_TRY(c->alloc(&c->qbuf, (size_t)c->m_max * qd));
-  LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
-  LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
+  if (d.kind == LAT_DIT) {
+    LAT_TRY(c->alloc(&c->kvown16, (size_t)c->m_max * 4 * d.Hkv * d.dh));
+  } else {
+    LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
+    LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
+  }
   LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, terms * d.D));
   LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, terms * qd));
   LAT_TRY(make_act_map(&c->map_act_f, c->act2f, c->m_max, terms * d.F));
@@ -878,8 +883,15 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
 static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, int groups, cudaStream_t st) {
   const int dh = c->d.dh;
   if (dh == 128) {   // tensor-core attention: one CTA per (head, group, 128 rows)
-    dim3 grid(c->d.Hq, (a.T_rows + 127) / 128, groups);
-    attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, c->err);
+    const lat_model_desc& d = c->d;
+    if (!a.ring || !a.own16 || !aligned16(a.ring)) return fail(LAT_ERR_ALIGN, "KV ring NULL or not 16-byte aligned");
+    const size_t ring_rows = (size_t)d.n_streams * d.L * d.S * (d.n_hist + 1) * 2 * d.T_q;
+    if (ring_rows > 0x7fffffffu) return fail(LAT_ERR_SHAPE, "KV ring too large for one tensor map");
+    CUtensorMap ring_map, own_map;
+    LAT_TRY(make_kmajor_map(&ring_map, a.ring, (int)ring_rows, a.kv_ld, 128));
+    LAT_TRY(make_kmajor_map(&own_map, a.own16, c->m_max, 4 * a.kv_ld, 64));
+    dim3 grid(d.Hq, (a.T_rows + 127) / 128, groups);
+    attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, ring_map, own_map, c->err);
     return launch_check("attention_tc");
   }
   if (dh != 256) return fail(LAT_ERR_SHAPE, "dense-path attention: dh 128 or 256");
@@ -984,7 +996,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   RopeKvArgs ra{};
   ra.qkv = c->qkvbuf; ra.ld_qkv = 3 * D; ra.q_cols = D; ra.kv_cols = D; ra.dh = d.dh; ra.T = T;
   ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta; ra.q_out = c->qbuf; ra.kv_ld = D;
-  ra.k32 = c->kown; ra.v32 = c->vown;
+  ra.k16 = c->kvown16; ra.v16 = c->kvown16 + 2 * D; ra.ld16 = 4 * D;
   SegAttnArgs sa{};
   for (int b = 0; b < n; ++b) {
     const int cb = ch[b].chunk, sb = ch[b].step, stb = ch[b].stream;
@@ -998,8 +1010,9 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
       sa.grp[b].seg[ns++] = AttnSeg{ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 0),
                                     ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 1), nullptr, nullptr, T};
     }
-    // own keys as computed (fp32); the ring slot holds their bf16 copy for later chunks
-    sa.grp[b].seg[ns++] = AttnSeg{nullptr, nullptr, c->kown + (size_t)b * T * D, c->vown + (size_t)b * T * D, T};
+    // own keys as computed (fp16 hi/lo planes of the fp32 values); the ring slot holds their bf16 copy
+    const __half* own = c->kvown16 + (size_t)b * T * 4 * D;
+    sa.grp[b].seg[ns++] = AttnSeg{nullptr, nullptr, nullptr, nullptr, T, own, own + 2 * D};
     sa.grp[b].nseg = ns;
   }
   rope_kv_kernel<<<M, 128, 0, st>>>(ra);
@@ -1008,6 +1021,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
   sa.out = c->act2; sa.ldh = D;
   sa.trace = c->attn_trace;
+  sa.ring = kv; sa.own16 = c->kvown16;
   LAT_TRY(enqueue_attention_seg(c, sa, n, st));
   {
     DenseArgs a{};
