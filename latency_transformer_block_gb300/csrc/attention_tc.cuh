@@ -13,17 +13,20 @@
 //   O  = (P_hi + P_lo) V    (+ P_hi V_lo for own keys)
 //
 // The dropped cross terms (Q_lo K_lo, P_lo V_lo) are below 2^-22 of the kept
-// ones.  One CTA = one (head, 128-row query tile, group).  Keys run in blocks:
+// ones.  One CTA = one (128-row query tile, head, group).  Keys run in blocks:
 // 128 cached keys (history segments concatenated, N = 128 for S) or 64 own
 // keys (hi and lo planes in the same buffers).  On this hardware an M = 128
 // MMA costs the same ~152 cycles for N up to 256, so wide blocks matter.
 //
 // Roles: warp 0 (lane 0) issues the MMAs in the order S(0), S(1), PV(0),
 // S(2), PV(1), ... so the tensor core computes S(j+1) while the row warps run
-// the softmax of block j; warps 1..3 load K and V of each block into one of
-// two buffers each (converting to fp16 on the way); warps 4..11 hold the rows:
-// warp w reads TMEM lanes 32 (w % 4) .. + 31, half (w - 4) / 4 of each block's
-// keys and of the output columns.
+// the softmax of block j; warp 1 (lane 0) moves K and V of each block by TMA
+// into one of two buffers each; warps 4..11 hold the rows: warp w reads TMEM
+// lanes 32 (w % 4) .. + 31, half (w - 4) / 4 of each block's keys and of the
+// output columns.  The row warps also turn each landed cached K/V block from
+// bf16 into fp16 in shared memory (8 chunks of 8 values per thread) and zero
+// the rows past its valid keys: K(j+1) before the softmax of block j, V(j)
+// right after writing its P.
 //
 // TMEM (512 columns): S of block j in columns 128 (j % 2) ..; the row warps
 // write P of the block back over its own S columns as packed fp16 (per
@@ -53,9 +56,9 @@ constexpr int kTcOffBar = kTcOffX + 4 * 128 * 4;
 constexpr int kTcNBar = 24;
 constexpr int kTcOffTab = kTcOffBar + kTcNBar * 8;   // TcSegTab
 constexpr int kTcSmem = 1024 + kTcOffTab + 128 + 16;
-// registers per thread after setmaxnreg: MMA/loader warpgroup, row warpgroups
-// (128 x 104 + 256 x 192 = 62464 <= 384 x 168 = 64512, the registers given at launch)
-constexpr int kTcRegsLoad = 104, kTcRegsRow = 192;
+// registers per thread after setmaxnreg: MMA/TMA warpgroup, row warpgroups
+// (128 x 56 + 256 x 224 = 64512 = 384 x 168, the registers given at launch)
+constexpr int kTcRegsLoad = 56, kTcRegsRow = 224;
 
 __host__ __device__ constexpr int attn_tc_smem_bytes() { return kTcSmem; }
 
@@ -217,9 +220,9 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   float* sX = reinterpret_cast<float*>(sm + kTcOffX);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kTcOffBar);
   uint64_t* q_full = bar + 0;    // Q planes built (256 arrivals)
-  uint64_t* k_full = bar + 1;    // [2] K block loaded (64: warps 1, 2)
+  uint64_t* k_full = bar + 1;    // [2] K block in fp16 (256: row warps)
   uint64_t* k_free = bar + 3;    // [2] S MMAs done with the K buffer (commit)
-  uint64_t* v_full = bar + 5;    // [2] V block loaded (32: warp 3)
+  uint64_t* v_full = bar + 5;    // [2] V block in fp16 (256)
   uint64_t* v_free = bar + 7;    // [2] PV MMAs done with the V buffer (commit)
   uint64_t* s_full = bar + 9;    // [2] S in TMEM (commit)
   uint64_t* p_full = bar + 11;   // [2] P written over S (256)
@@ -231,7 +234,8 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 22);
   TcSegTab* tab = reinterpret_cast<TcSegTab*>(sm + kTcOffTab);
 
-  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  // query tile fastest: the tiles of one head run together and share its K/V in L2
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = h / (a.Hq / a.Hkv);
   const SegGroup& G = a.grp[b];
@@ -242,9 +246,9 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 256);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 64);
+      mbar_init(&k_full[i], 256);
       mbar_init(&k_free[i], 1);
-      mbar_init(&v_full[i], 32);
+      mbar_init(&v_full[i], 256);
       mbar_init(&v_free[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 256);
@@ -329,91 +333,48 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(mdone);
         mbar_wait(mdone, 0, nullptr, 0);
       }
-    } else {
-      // ---------------- loaders: K (warps 1, 2) and V (warp 3) of each block ----------------
-      // One thread of the group moves the block by TMA (cached: two 128-row
-      // boxes of bf16 ring rows; own: two 64-row boxes of each fp16 plane) into
-      // the swizzled operand layout; then every thread of the group converts
-      // its chunks of a cached block from bf16 to fp16 in place and zeroes the
-      // rows past the block's valid keys (whatever the neighbouring rows hold).
-      const bool isv = warp == 3;
-      const int tid = isv ? lane : threadIdx.x - 32, nthr = isv ? 32 : 64;
-      uint8_t* const base = isv ? sV : sK;
-      uint64_t* const full = isv ? v_full : k_full;
-      uint64_t* const tfull = isv ? vt_full : kt_full;
-      uint64_t* const freed = isv ? v_free : k_free;
-      if (tid == 0) {
-        tma_prefetch_desc(&ring_map);
-        tma_prefetch_desc(&own_map);
-      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- TMA: K and V of each block ----------------
+      // cached: two 128-row boxes of bf16 ring rows; own: two 64-row boxes of
+      // each fp16 plane, into the swizzled operand layout
+      tma_prefetch_desc(&ring_map);
+      tma_prefetch_desc(&own_map);
       const uint64_t pol = l2_policy_evict_last();   // every query tile of the head re-reads the block
       bool ok = true;
       for (int j = 0; j < nblk && ok; ++j) {
         const int bf = j & 1;
         const uint32_t par = (uint32_t)(j >> 1) & 1u;
-        if (j >= 2 && !tc_wait(&freed[bf], par ^ 1u, err, isv ? 66 : 65)) {
-          ok = false;
-          break;
-        }
-        if (tid == 0) tc_mark(a.trace, 2, j, isv ? 2 : 0);
-        uint8_t* dst = base + bf * kTcBuf;
-        const bool own = kk.own(j);
-        int nv;
-        if (tid == 0) fence_proxy_async_smem();
-        if (!own) {
-          int s, k0;
-          kk.cached(tab, j, s, k0, nv);
-          if (tid == 0) {
-            const int row = (isv ? tab->vrow[s] : tab->krow[s]) + k0;
-            mbar_arrive_expect_tx(&tfull[bf], kTcBuf);
-            tma_load_2d(dst, &ring_map, &tfull[bf], kvh * DH, row, pol);
-            tma_load_2d(dst + 16384, &ring_map, &tfull[bf], kvh * DH + 64, row, pol);
+        for (int isv = 0; isv < 2 && ok; ++isv) {
+          if (j >= 2 && !tc_wait(isv ? &v_free[bf] : &k_free[bf], par ^ 1u, err, isv ? 66 : 65)) {
+            ok = false;
+            break;
           }
-        } else {
-          const int k0 = (j - kk.nb_c) * kTcKBO;
-          nv = min(kTcKBO, kk.n_o - k0);
-          if (tid == 0) {
+          tc_mark(a.trace, 2, j, isv ? 2 : 0);
+          uint8_t* dst = (isv ? sV : sK) + bf * kTcBuf;
+          uint64_t* tb = isv ? &vt_full[bf] : &kt_full[bf];
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(tb, kTcBuf);
+          if (!kk.own(j)) {
+            int sgi, k0, nv;
+            kk.cached(tab, j, sgi, k0, nv);
+            const int row = (isv ? tab->vrow[sgi] : tab->krow[sgi]) + k0;
+            tma_load_2d(dst, &ring_map, tb, kvh * DH, row, pol);
+            tma_load_2d(dst + 16384, &ring_map, tb, kvh * DH + 64, row, pol);
+          } else {
             // own-plane rows: [K hi | K lo | V hi | V lo], kv_ld columns each
-            const int row = tab->own_row + k0, xh = (isv ? 2 * a.kv_ld : 0) + kvh * DH, xl = xh + a.kv_ld;
-            mbar_arrive_expect_tx(&tfull[bf], kTcBuf);
-            tma_load_2d(dst, &own_map, &tfull[bf], xh, row, pol);
-            tma_load_2d(dst + 8192, &own_map, &tfull[bf], xh + 64, row, pol);
-            tma_load_2d(dst + 16384, &own_map, &tfull[bf], xl, row, pol);
-            tma_load_2d(dst + 16384 + 8192, &own_map, &tfull[bf], xl + 64, row, pol);
+            const int row = tab->own_row + (j - kk.nb_c) * kTcKBO;
+            const int xh = (isv ? 2 * a.kv_ld : 0) + kvh * DH, xl = xh + a.kv_ld;
+            tma_load_2d(dst, &own_map, tb, xh, row, pol);
+            tma_load_2d(dst + 8192, &own_map, tb, xh + 64, row, pol);
+            tma_load_2d(dst + 16384, &own_map, tb, xl, row, pol);
+            tma_load_2d(dst + 16384 + 8192, &own_map, tb, xl + 64, row, pol);
           }
         }
-        if (!tc_wait(&tfull[bf], par, err, isv ? 70 : 69)) {
-          ok = false;
-          break;
-        }
-        if (!own) {   // 2048 chunks, a multiple of 8 x nthr: 8 shared-memory loads in flight
-          for (int i0 = tid; i0 < kTcKB * 16; i0 += 8 * nthr) {
-            uint4 v[8];
-            int off[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int it = i0 + u * nthr, r = it >> 4, c = it & 15;
-              off[u] = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-              v[u] = *reinterpret_cast<const uint4*>(dst + off[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int r = (i0 + u * nthr) >> 4;
-              *reinterpret_cast<uint4*>(dst + off[u]) = r < nv ? bf16x8_to_f16x8(v[u]) : make_uint4(0, 0, 0, 0);
-            }
-          }
-        } else if (nv < kTcKBO) {
-          for (int it = tid; it < kTcKBO * 16; it += nthr) {
-            const int r = it >> 4, c = it & 15;
-            if (r < nv) continue;
-            const int off = (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(dst + 16384 + off) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
-        if (tid == 0) tc_mark(a.trace, 2, j, isv ? 3 : 1);
-        mbar_arrive(&full[bf]);
+      }
+      // never leave a copy in flight into this CTA's shared memory
+      for (int j = (nblk > 2 ? nblk - 2 : 0); j < nblk; ++j) {
+        tc_wait(&kt_full[j & 1], (uint32_t)(j >> 1) & 1u, err, 71);
+        tc_wait(&vt_full[j & 1], (uint32_t)(j >> 1) & 1u, err, 72);
       }
     }
   } else {
@@ -440,6 +401,41 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(q_full);
 
+    // a landed K or V block: cached -> fp16 in place (8 chunks per thread, loads
+    // first), rows past the valid keys zeroed; own -> only the zeroing
+    auto prep = [&](int j, bool isv) {
+      const int bf = j & 1;
+      tc_wait(isv ? &vt_full[bf] : &kt_full[bf], (uint32_t)(j >> 1) & 1u, err, isv ? 70 : 69);
+      uint8_t* dst = (isv ? sV : sK) + bf * kTcBuf;
+      const int nv = kk.valid(tab, j);
+      if (!kk.own(j)) {
+        uint4 v[8];
+        int off[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int it = st + 256 * u, r = it >> 4, c = it & 15;
+          off[u] = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          v[u] = *reinterpret_cast<const uint4*>(dst + off[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int r = (st + 256 * u) >> 4;
+          *reinterpret_cast<uint4*>(dst + off[u]) = r < nv ? bf16x8_to_f16x8(v[u]) : make_uint4(0, 0, 0, 0);
+        }
+      } else if (nv < kTcKBO) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int it = st + 256 * u, r = it >> 4, c = it & 15;
+          if (r < nv) continue;
+          const int off = (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dst + 16384 + off) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(isv ? &v_full[bf] : &k_full[bf]);
+    };
+
     float o[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) o[i] = 0.f;
@@ -460,9 +456,11 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&o_free[bf]);
     };
+    if (nblk > 0) prep(0, false);
     for (int j = 0; j < nblk; ++j) {
       const int bf = j & 1;
       const bool own = kk.own(j);
+      if (j + 1 < nblk) prep(j + 1, false);   // K of the next block: its S overlaps this softmax
       const int nh = (own ? kTcKBO : kTcKB) / 2;     // keys of this thread's half
       const int k0 = half * nh, nv = kk.valid(tab, j);
       tc_wait(&s_full[bf], (uint32_t)(j >> 1) & 1u, err, 67);
@@ -508,6 +506,7 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&p_full[bf]);
+      prep(j, true);   // V of this block
       if (st == 0) tc_mark(a.trace, 1, j, 2);
       if (j > 0) add_o(j - 1);
       if (st == 0) tc_mark(a.trace, 1, j, 3);

@@ -882,7 +882,7 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
 
 static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, int groups, cudaStream_t st) {
   const int dh = c->d.dh;
-  if (dh == 128) {   // tensor-core attention: one CTA per (head, group, 128 rows)
+  if (dh == 128) {   // tensor-core attention: one CTA per (128 rows, head, group)
     const lat_model_desc& d = c->d;
     if (!a.ring || !a.own16 || !aligned16(a.ring)) return fail(LAT_ERR_ALIGN, "KV ring NULL or not 16-byte aligned");
     const size_t ring_rows = (size_t)d.n_streams * d.L * d.S * (d.n_hist + 1) * 2 * d.T_q;
@@ -890,7 +890,7 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
     CUtensorMap ring_map, own_map;
     LAT_TRY(make_kmajor_map(&ring_map, a.ring, (int)ring_rows, a.kv_ld, 128));
     LAT_TRY(make_kmajor_map(&own_map, a.own16, c->m_max, 4 * a.kv_ld, 64));
-    dim3 grid(d.Hq, (a.T_rows + 127) / 128, groups);
+    dim3 grid((a.T_rows + 127) / 128, d.Hq, groups);
     attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, ring_map, own_map, c->err);
     return launch_check("attention_tc");
   }
