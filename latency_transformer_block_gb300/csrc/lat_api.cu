@@ -414,9 +414,11 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     LAT_TRY(fold_t(b.wk, b.g_attn, q0 + (size_t)qd * D, D, kvd));
     LAT_TRY(fold_t(b.wv, b.g_attn, q0 + (size_t)(qd + kvd) * D, D, kvd));
     LAT_TRY(fold_t(b.wo, nullptr, c->wo + (size_t)l * D * qd, qd, D));
+    // gate/up rows interleaved in 128-row tiles: 64 gate rows, then the 64 up
+    // rows of the same FFN columns (one tile holds both inputs of its GeGLU)
     bf16* gu0 = c->wgu + (size_t)l * 2 * F * D;
-    LAT_TRY(fold_t(b.wg, b.g_ffn, gu0, D, F));
-    LAT_TRY(fold_t(b.wu, b.g_ffn, gu0 + (size_t)F * D, D, F));
+    LAT_TRY(fold_t(b.wg, b.g_ffn, gu0, D, F, 64, 0));
+    LAT_TRY(fold_t(b.wu, b.g_ffn, gu0, D, F, 64, 64));
     LAT_TRY(fold_t(b.wd, nullptr, c->wd + (size_t)l * D * F, F, D));
   }
   LAT_TRY(fold_t(w->w2, nullptr, c->w2, D, D));
@@ -527,23 +529,25 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
   CUDA_TRY(cudaMemset(c->xres, 0, (size_t)64 * D * 4));
 
-  // --- persistent step kernel: [barrier counter | sums of squares | gate/up sums],
-  //     cleared before every launch; key-block partials; maps; plans ---
+  // --- persistent step kernel: [barrier counter, group counters | sums of squares |
+  //     QKV sums], cleared before every launch; key-block partials; maps; plans ---
   {
-    const size_t bar_b = 256, ss_b = (size_t)L * 128 * 4;
-    c->mk_zero_bytes = bar_b + ss_b;
+    const size_t bar_b = 128 + 4 * (size_t)kCntWords, ss_b = (size_t)L * 128 * 4, qkv_b = (size_t)64 * c->nqkv * 4;
+    const size_t gu_b = (size_t)64 * 2 * F * 4;
+    static_assert((128 + 4 * kCntWords) % 16 == 0, "counter block keeps the sums 16-byte aligned");
+    if (c->nqkv / std::max(d.dh, 128) > 32) return fail(LAT_ERR_SHAPE, "at most 32 QKV head groups");
+    if (2 * F / 128 > 192) return fail(LAT_ERR_SHAPE, "F must be <= 12288");
+    c->mk_zero_bytes = bar_b + ss_b + qkv_b + gu_b;
     uint8_t* z = nullptr;
     LAT_TRY(c->alloc(&z, c->mk_zero_bytes));
     CUDA_TRY(cudaMemset(z, 0, c->mk_zero_bytes));
     c->mk_zero = z;
     MkArgs& m = c->mk;
     m.bar = reinterpret_cast<unsigned*>(z);
+    m.grp_cnt = m.bar + 32;
     m.ss = reinterpret_cast<float*>(z + bar_b);
-    float* gu = nullptr;   // one slab of gate/up partial sums per K range
-    LAT_TRY(c->alloc(&gu, (size_t)c->g_gu.splits * 64 * 2 * F));
-    m.gu = gu;
-    float* qp = nullptr;   // one slab of QKV partial sums per K range
-    LAT_TRY(c->alloc(&qp, (size_t)c->g_qkv.splits * 64 * c->nqkv));
+    m.qkv = reinterpret_cast<float*>(z + bar_b + ss_b);
+    m.gu = reinterpret_cast<float*>(z + bar_b + ss_b + qkv_b);
     bf16 *qpl = nullptr, *kvo = nullptr;
     LAT_TRY(c->alloc(&qpl, (size_t)2 * 64 * qd));
     LAT_TRY(c->alloc(&kvo, (size_t)4 * 64 * kvd));
@@ -559,7 +563,6 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     m.part_l = pl;
     m.part_o = po;
     m.x = c->xres;
-    m.qkv = qp;
     m.o_planes = c->planes_o;
     m.h_planes = c->planes_h;
     m.cos_t = c->cos_t;

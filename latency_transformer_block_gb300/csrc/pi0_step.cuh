@@ -13,23 +13,26 @@
 //    phase boundaries and is throttled only by the ring.
 //  * warp 1 issues tcgen05 MMAs (M = 128 weight rows, N = 192 = three bf16
 //    planes x 64 tokens, fp32 accumulator in TMEM, two buffers).
-//  * warps 4..11 ("math") do everything that depends on activations: they load
-//    fp32 activation tiles by TMA, split them into three bf16 planes in the
-//    MMA's swizzled layout, run the split-K epilogue (fp32 atomics into the
-//    output), the attention and the combine of key-range partials.
+//  * warps 4..11 ("math") do everything that depends on activations: they
+//    split fp32 activation tiles (staged by warp 2's TMA) into three bf16
+//    planes in the MMA's swizzled layout, run the split-K epilogues (vector
+//    reductions into fp32 sums at L2), the attention and the combine of
+//    key-range partials.
 //
-// Per block seven phases, separated by a grid barrier (bounded spin):
-//   1 QKV projection of x (sums of squares of x on the side)
-//   2 attention: per (head, 32-key block); q and own k/v come from the raw
-//     projection sums with the RMS factor and RoPE applied on load; own k/v
-//     go to the cache as bf16
+// Per block six phases, separated by a grid barrier (bounded spin):
+//   1 QKV projection of x (sums of squares of x on the side); the CTAs of
+//     each head group (its m-tiles, all K ranges) then wait for one another
+//     on a group counter and finalize the group's q / own k, v: RMS factor,
+//     RoPE, two-term bf16 planes, own k / v to the cache as bf16
+//   2 attention: per (head, 32-key block), partial (max, sum, output)
 //   3 combine of the key-block partials into the exact bf16 planes of o;
-//     clears the QKV accumulator
+//     clears the QKV sums for the next block
 //   4 x += o Wo (operand planes by TMA)
-//   5 gate/up projection of x (sums of squares of x on the side)
-//   6 h = GELU(r g) * (r u) once per element, into exact bf16 planes; clears
-//     the gate/up accumulator
-//   7 x += h Wd (operand planes by TMA)
+//   5 gate/up projection of x (gate and up rows of the same 64 FFN columns
+//     in one 128-row tile; sums of squares on the side); the CTAs of each
+//     tile wait for one another and write h = GELU(r g) * (r u) as exact
+//     bf16 planes
+//   6 x += h Wd (operand planes by TMA); clears the gate/up sums
 // The RMSNorm scales are folded into the weights; the per-token factor
 // r = rsqrt(mean(x^2) + eps) multiplies the projection sums (the projection is
 // linear in its input), as in the pages' fold (section 4.1).
@@ -79,8 +82,11 @@ struct MkArgs {
   int D, F, Hq, Hkv, T_q, T_prefix, T_kv, nqkv;
   float eps, scale_log2;
   float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
-  float* qkv;               // fp32 [splits][64][nqkv] QKV partial sums, one slab per K range
-  float* gu;                // fp32 [splits][64][2F] gate/up partial sums, one slab per K range
+  float* qkv;               // fp32 [64][nqkv] QKV sums (vector reductions of every K range; 0 at entry,
+                            // cleared again in the GeGLU phase for the next block)
+  float* gu;                // fp32 [64][2F] gate/up sums in weight-row order (each 128-row tile = 64 gate
+                            // rows, then the 64 up rows of the same FFN columns); 0 at entry, cleared
+                            // again in the down phase for the next block
   __nv_bfloat16* o_planes;  // [3][64][Hq dh] attention output as exact bf16 planes (rows >= T_q stay 0)
   __nv_bfloat16* h_planes;  // [3][64][F] GeGLU output as exact bf16 planes (rows >= T_q stay 0)
   __nv_bfloat16* q_planes;  // [2][64][Hq dh] q after RoPE, two-term bf16 (hi, lo)
@@ -96,6 +102,7 @@ struct MkArgs {
   __nv_bfloat16* kv;        // cache of layer l0: [2][T_kv][Hkv dh]
   long long kv_stride;      // elements from one layer's cache to the next
   unsigned* bar;            // grid barrier counter (0 at entry)
+  unsigned* grp_cnt;        // dataflow counters, kCntWords words (0 at entry)
   DevErr* err;
   unsigned long long* trace;   // null, or [layers][grid][64] phase timestamps (ns): 0..14 block
                                // start and the ends of each phase / barrier, 16..18 attention,
@@ -155,6 +162,30 @@ __device__ __forceinline__ void mk_mark(unsigned long long* tr, int ev) {
 
 __device__ __forceinline__ float2 ldcg2(const float* p) { return __ldcg(reinterpret_cast<const float2*>(p)); }
 
+// 4 x 4 transpose among the lanes k = lane % 4 of each lane quad: on entry
+// lane k holds row k (a0..a3), on exit it holds column k.  Two exchange rounds
+// (partner lane k ^ 1, then k ^ 2), two shuffles each.
+__device__ __forceinline__ void quad_transpose(float& a0, float& a1, float& a2, float& a3, int k) {
+  const bool c = k & 1, d = (k >> 1) & 1;
+  const float x0 = __shfl_xor_sync(0xffffffffu, c ? a0 : a1, 1);
+  const float x1 = __shfl_xor_sync(0xffffffffu, c ? a2 : a3, 1);
+  if (c) { a0 = x0; a2 = x1; } else { a1 = x0; a3 = x1; }
+  const float y0 = __shfl_xor_sync(0xffffffffu, d ? a0 : a2, 2);
+  const float y1 = __shfl_xor_sync(0xffffffffu, d ? a1 : a3, 2);
+  if (d) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
+}
+
+// n4 float4 of p = 0, spread over the grid's math threads
+__device__ __forceinline__ void mk_zero_f4(float* p, int n4, int mt) {
+  float4* z = reinterpret_cast<float4*>(p);
+  for (int i = blockIdx.x * 256 + mt; i < n4; i += gridDim.x * 256) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
+}
+
+// p[0..3] += (a, b, c, d): one vector reduction at L2 (p 16-byte aligned)
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // 8 fp32 values (registers) -> 8 bf16 hi and 8 bf16 lo (two-term split)
 __device__ __forceinline__ void split8_regs(const float (&v)[8], uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
@@ -208,10 +239,9 @@ struct MkMath {
 // exact bf16 planes for the MMA, or nothing when the loader brings the planes
 // themselves; then the split-K epilogue.  `stats` (CTAs of m-tile 0) receives
 // the per-token sums of squares of the activation.
-// `slab` > 0: each K range stores its partial sums into its own slab of `out`
-// (plain stores, summed by the consumer) instead of adding them atomically.
+// Every K range adds its partial sums into `out` (vector reductions at L2).
 __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool staged, float* stats, float* out,
-                                             int ld, size_t slab, int T_q, DevErr* err, unsigned long long* tr) {
+                                             int ld, int T_q, DevErr* err, unsigned long long* tr) {
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
   const int nk = r.k1 - r.k0;
@@ -296,112 +326,142 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool st
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] += w[j];
   tc_fence_before();
-  if (slab) {
-    float* o = out + (size_t)(blockIdx.x / g.MT) * slab;
+  // each lane quad transposes 4 tokens x its 4 outputs, so a lane adds 4
+  // consecutive outputs of one token: one vector reduction
+  const int k4 = lane & 3;
+  const int fb = f - k4;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (ch * 32 + j < T_q) __stcg(o + (size_t)(ch * 32 + j) * ld + f, v[j]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (ch * 32 + j < T_q) atomicAdd(out + (size_t)(ch * 32 + j) * ld + f, v[j]);
+  for (int j0 = 0; j0 < 32; j0 += 4) {
+    float a0 = v[j0], a1 = v[j0 + 1], a2 = v[j0 + 2], a3 = v[j0 + 3];
+    quad_transpose(a0, a1, a2, a3, k4);
+    const int t = ch * 32 + j0 + k4;
+    if (t < T_q) red_add_v4(out + (size_t)t * ld + fb, a0, a1, a2, a3);
   }
   mk_mark(tr, 3);
 }
 
-// Sum of `n` partial slabs (slab elements apart) of 4 consecutive floats, in
-// slab order; the loads of up to 8 slabs are in flight together.
-__device__ __forceinline__ float4 sum_slabs(const float* p, size_t slab, int n) {
-  float4 y[8];
-#pragma unroll
-  for (int sp = 0; sp < 8; ++sp)
-    y[sp] = sp < n ? __ldcg(reinterpret_cast<const float4*>(p + sp * slab)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 x = y[0];
-#pragma unroll
-  for (int sp = 1; sp < 8; ++sp)
-    if (sp < n) {
-      x.x += y[sp].x; x.y += y[sp].y; x.z += y[sp].z; x.w += y[sp].w;
-    }
-  for (int sp = 8; sp < n; ++sp) {
-    const float4 z = __ldcg(reinterpret_cast<const float4*>(p + sp * slab));
-    x.x += z.x; x.y += z.y; x.z += z.z; x.w += z.w;
-  }
-  return x;
-}
-
-// Phase 2: q, own k and own v of the block, once per element: the sum of the
-// QKV partial slabs times r = rsqrt(mean(x^2) + eps), RoPE (rotate-half pairs
-// (i, i + dh/2)) on q and k, then two-term bf16 splits: q -> q_planes, own k/v
-// -> kv_own planes; the bf16 cache copy of own k/v (nearest) goes to the cache
-// slots T_prefix + t.  Item = 4 RoPE pairs of one q/k head or 4 values of v.
+// q, own k and own v of one head group, from the finished QKV sums: every CTA
+// of the projection adds its K range into a.qkv (vector reductions); the CTA
+// that completes a group (all K ranges of its m-tiles) runs this for the
+// group's heads.  r = rsqrt(mean(x^2) + eps), RoPE (rotate-half pairs
+// (i, i + dh/2)) on q and k heads, two-term bf16 splits into q_planes /
+// kv_own, and the bf16 cache copy (nearest) of own k / v at slots T_prefix + t.
 template <int DH>
-__device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int splits, const float* ss1, __nv_bfloat16* kc,
-                                                __nv_bfloat16* vc, float invD, int mt) {
+__device__ __forceinline__ void mk_qkv_finalize_group(const MkArgs& a, int h0, int nhd, int part, int parts,
+                                                      const float* ss1, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                                                      float invD, int mt) {
   constexpr int HD = DH / 2;
   const int nh = a.Hq + a.Hkv, kvd = a.Hkv * DH, qd = a.Hq * DH;
-  const int rot_per_t = nh * (HD / 4), v_per_t = a.Hkv * (DH / 4);
-  const int n_rot = a.T_q * rot_per_t, n_all = n_rot + a.T_q * v_per_t;
-  const size_t slab = (size_t)64 * a.nqkv;
   const size_t qpl = (size_t)64 * qd, kpl = (size_t)64 * kvd;
-  for (int it = blockIdx.x * 256 + mt; it < n_all; it += gridDim.x * 256) {
-    if (it < n_rot) {
-      const int t = it / rot_per_t, rem = it % rot_per_t;
-      const int hd = rem / (HD / 4), i = (rem % (HD / 4)) * 4;
-      const float* p0 = a.qkv + (size_t)t * a.nqkv + hd * DH + i;
-      const float4 x0 = sum_slabs(p0, slab, splits), x1 = sum_slabs(p0 + HD, slab, splits);
-      const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
-      const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)t * HD + i));
-      const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)t * HD + i));
-      const float a0[4] = {rv * x0.x, rv * x0.y, rv * x0.z, rv * x0.w};
-      const float a1[4] = {rv * x1.x, rv * x1.y, rv * x1.z, rv * x1.w};
-      const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
-      float y0[4], y1[4];
+  for (int hd = h0; hd < h0 + nhd; ++hd) {
+    if (hd < nh) {   // q or k head: 4 RoPE pairs per item
+      const int n = a.T_q * (HD / 4);
+      for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
+        const int t = it / (HD / 4), i = (it % (HD / 4)) * 4;
+        const float* p0 = a.qkv + (size_t)t * a.nqkv + hd * DH + i;
+        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p0));
+        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(p0 + HD));
+        const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
+        const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)t * HD + i));
+        const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)t * HD + i));
+        const float a0[4] = {rv * x0.x, rv * x0.y, rv * x0.z, rv * x0.w};
+        const float a1[4] = {rv * x1.x, rv * x1.y, rv * x1.z, rv * x1.w};
+        const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+        float y0[4], y1[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        y0[e] = a0[e] * cc[e] - a1[e] * ss[e];
-        y1[e] = a1[e] * cc[e] + a0[e] * ss[e];
+        for (int e = 0; e < 4; ++e) {
+          y0[e] = a0[e] * cc[e] - a1[e] * ss[e];
+          y1[e] = a1[e] * cc[e] + a0[e] * ss[e];
+        }
+        uint32_t h0w[2], l0w[2], h1w[2], l1w[2];
+        split_pair2(y0[0], y0[1], h0w[0], l0w[0]);
+        split_pair2(y0[2], y0[3], h0w[1], l0w[1]);
+        split_pair2(y1[0], y1[1], h1w[0], l1w[0]);
+        split_pair2(y1[2], y1[3], h1w[1], l1w[1]);
+        if (hd < a.Hq) {
+          uint2* q = reinterpret_cast<uint2*>(a.q_planes + (size_t)t * qd + hd * DH + i);
+          q[0] = make_uint2(h0w[0], h0w[1]);
+          q[HD / 4] = make_uint2(h1w[0], h1w[1]);
+          q[qpl / 4] = make_uint2(l0w[0], l0w[1]);
+          q[qpl / 4 + HD / 4] = make_uint2(l1w[0], l1w[1]);
+        } else {
+          const int kh = hd - a.Hq;
+          uint2* k = reinterpret_cast<uint2*>(a.kv_own + (size_t)t * kvd + kh * DH + i);
+          k[0] = make_uint2(h0w[0], h0w[1]);
+          k[HD / 4] = make_uint2(h1w[0], h1w[1]);
+          k[kpl / 4] = make_uint2(l0w[0], l0w[1]);
+          k[kpl / 4 + HD / 4] = make_uint2(l1w[0], l1w[1]);
+          float tx, ty;
+          uint2* ck = reinterpret_cast<uint2*>(kc + (size_t)(a.T_prefix + t) * kvd + kh * DH + i);
+          ck[0] = make_uint2(rn_pair(y0[0], y0[1], tx, ty), rn_pair(y0[2], y0[3], tx, ty));
+          ck[HD / 4] = make_uint2(rn_pair(y1[0], y1[1], tx, ty), rn_pair(y1[2], y1[3], tx, ty));
+        }
       }
-      uint32_t h0[2], l0[2], h1[2], l1[2];
-      split_pair2(y0[0], y0[1], h0[0], l0[0]);
-      split_pair2(y0[2], y0[3], h0[1], l0[1]);
-      split_pair2(y1[0], y1[1], h1[0], l1[0]);
-      split_pair2(y1[2], y1[3], h1[1], l1[1]);
-      if (hd < a.Hq) {
-        uint2* q = reinterpret_cast<uint2*>(a.q_planes + (size_t)t * qd + hd * DH + i);
-        q[0] = make_uint2(h0[0], h0[1]);
-        q[HD / 4] = make_uint2(h1[0], h1[1]);
-        q[qpl / 4] = make_uint2(l0[0], l0[1]);
-        q[qpl / 4 + HD / 4] = make_uint2(l1[0], l1[1]);
-      } else {
-        const int kh = hd - a.Hq;
-        uint2* k = reinterpret_cast<uint2*>(a.kv_own + (size_t)t * kvd + kh * DH + i);
-        k[0] = make_uint2(h0[0], h0[1]);
-        k[HD / 4] = make_uint2(h1[0], h1[1]);
-        k[kpl / 4] = make_uint2(l0[0], l0[1]);
-        k[kpl / 4 + HD / 4] = make_uint2(l1[0], l1[1]);
+    } else {   // v head: 4 values per item
+      const int n = a.T_q * (DH / 4), j0 = (hd - nh) * DH;
+      for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
+        const int t = it / (DH / 4), j = j0 + (it % (DH / 4)) * 4;
+        float4 x = __ldcg(reinterpret_cast<const float4*>(a.qkv + (size_t)t * a.nqkv + nh * DH + j));
+        const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
+        x.x *= rv; x.y *= rv; x.z *= rv; x.w *= rv;
+        uint32_t hh[2], ll[2];
+        split_pair2(x.x, x.y, hh[0], ll[0]);
+        split_pair2(x.z, x.w, hh[1], ll[1]);
+        uint2* v = reinterpret_cast<uint2*>(a.kv_own + 2 * kpl + (size_t)t * kvd + j);
+        v[0] = make_uint2(hh[0], hh[1]);
+        v[kpl / 4] = make_uint2(ll[0], ll[1]);
         float tx, ty;
-        uint2* ck = reinterpret_cast<uint2*>(kc + (size_t)(a.T_prefix + t) * kvd + kh * DH + i);
-        ck[0] = make_uint2(rn_pair(y0[0], y0[1], tx, ty), rn_pair(y0[2], y0[3], tx, ty));
-        ck[HD / 4] = make_uint2(rn_pair(y1[0], y1[1], tx, ty), rn_pair(y1[2], y1[3], tx, ty));
+        *reinterpret_cast<uint2*>(vc + (size_t)(a.T_prefix + t) * kvd + j) =
+            make_uint2(rn_pair(x.x, x.y, tx, ty), rn_pair(x.z, x.w, tx, ty));
       }
-    } else {
-      const int iv = it - n_rot;
-      const int t = iv / v_per_t, j = (iv % v_per_t) * 4;
-      const float* p0 = a.qkv + (size_t)t * a.nqkv + nh * DH + j;
-      float4 x = sum_slabs(p0, slab, splits);
-      const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
-      x.x *= rv; x.y *= rv; x.z *= rv; x.w *= rv;
-      uint32_t hh[2], ll[2];
-      split_pair2(x.x, x.y, hh[0], ll[0]);
-      split_pair2(x.z, x.w, hh[1], ll[1]);
-      uint2* v = reinterpret_cast<uint2*>(a.kv_own + 2 * kpl + (size_t)t * kvd + j);
-      v[0] = make_uint2(hh[0], hh[1]);
-      v[kpl / 4] = make_uint2(ll[0], ll[1]);
-      float tx, ty;
-      *reinterpret_cast<uint2*>(vc + (size_t)(a.T_prefix + t) * kvd + j) =
-          make_uint2(rn_pair(x.x, x.y, tx, ty), rn_pair(x.z, x.w, tx, ty));
     }
   }
+}
+
+// Counters after the grid barrier word (MkArgs::grp_cnt), 0 at launch entry;
+// each grows by one group's arrivals per block.
+constexpr int kCntQkvArr = 0;      // [32] QKV head groups: CTAs past their epilogue
+constexpr int kCntGuArr = 32;      // [192] gate/up tiles: CTAs past their epilogue
+constexpr int kCntWords = 224;
+
+// Count this CTA into group counter `cnt`, then wait until the group has all
+// `target` arrivals and group counter `cnt0` too (the group whose CTAs add the
+// sums of squares of x).  Bounded: gives up (error recorded) after the spin
+// budget or when another CTA has failed.  The counters grow by one group's
+// arrivals per block and start at 0 with each launch.
+__device__ __forceinline__ void mk_group_wait(unsigned* cnt, const unsigned* cnt0, unsigned target, DevErr* err,
+                                              unsigned where, int mt) {
+  __threadfence();   // this thread's reductions are performed before the arrival
+  named_sync(2, 256);
+  if (mt == 0) {
+    atomicAdd(cnt, 1u);
+    const long long t0 = clock64();
+    for (int i = 0; ld_acquire_u32(cnt) < target || ld_acquire_u32(cnt0) < target; ++i)
+      if ((i & 15) == 15 && (mk_aborted(err) || clock64() - t0 > kSpinBudget)) {
+        if (!mk_aborted(err)) record_error(err, 2u, where);
+        break;
+      }
+    __threadfence();
+  }
+  named_sync(2, 256);
+}
+
+// After the QKV epilogue: every CTA of a head group (the m-tiles of whole
+// heads, all K ranges) waits for the group, then finalizes its share of the
+// group's heads.  `lr` = block index within the launch.
+template <int DH>
+__device__ __forceinline__ void mk_qkv_arrive(const MkArgs& a, int lr, const float* ss1, __nv_bfloat16* kc,
+                                              __nv_bfloat16* vc, float invD, int mt) {
+  const MkGemm& g = a.g[0];
+  const MkRange r = mk_range(g, blockIdx.x);
+  if (!r.active) return;
+  constexpr int MPG = DH >= 128 ? DH / 128 : 1;   // m-tiles per group
+  constexpr int HPG = DH >= 128 ? 1 : 128 / DH;   // heads per group
+  const int grp = r.m / MPG;
+  const int per = MPG * g.splits;
+  const int part = (r.m % MPG) * g.splits + (int)blockIdx.x / g.MT;
+  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, a.grp_cnt + kCntQkvArr, (unsigned)((lr + 1) * per), a.err, 901, mt);
+  mk_qkv_finalize_group<DH>(a, grp * HPG, HPG, part, per, ss1, kc, vc, invD, mt);
 }
 
 // Phase 3: attention of the chunk over [cache | own], one (head, 32-key block)
@@ -443,26 +503,32 @@ __device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc,
     const int h = u / nkb, kb = u % nkb, kvh = h / group;
     const bool has_lo = (kb + 1) * KB > own0 && own0 < a.T_kv;
     named_sync(3, 256);   // the previous unit is done with the tiles
-    // ---- async copies: hi planes of the key block (cache or own), q planes ----
-    for (int idx = mt; idx < KB * (DH / 8); idx += 256) {
-      const int row = idx / (DH / 8), c8 = idx % (DH / 8);
-      const int key = kb * KB + row;
-      const bool own = key >= own0 && key < a.T_kv;
-      const bool in = key < a.T_kv;
-      const __nv_bfloat16* ks;
-      const __nv_bfloat16* vs;
-      if (own) {
-        const size_t off = (size_t)(key - own0) * kvd + kvh * DH + c8 * 8;
-        ks = a.kv_own + off;
-        vs = a.kv_own + 2 * kpl + off;
-      } else {
-        const size_t off = (size_t)(in ? key : 0) * kvd + kvh * DH + c8 * 8;
-        ks = kc + off;
-        vs = vc + off;
+    // ---- async copies: hi planes of the key block (cache keys, then own
+    //      keys), q planes ----
+    auto kv_copies = [&](bool own_pass) {
+      for (int idx = mt; idx < KB * (DH / 8); idx += 256) {
+        const int row = idx / (DH / 8), c8 = idx % (DH / 8);
+        const int key = kb * KB + row;
+        const bool own = key >= own0 && key < a.T_kv;
+        const bool in = key < a.T_kv;
+        if (own != own_pass) continue;
+        const __nv_bfloat16* ks;
+        const __nv_bfloat16* vs;
+        if (own) {
+          const size_t off = (size_t)(key - own0) * kvd + kvh * DH + c8 * 8;
+          ks = a.kv_own + off;
+          vs = a.kv_own + 2 * kpl + off;
+        } else {
+          const size_t off = (size_t)(in ? key : 0) * kvd + kvh * DH + c8 * 8;
+          ks = kc + off;
+          vs = vc + off;
+        }
+        cp_async16(sK + row * LD + c8 * 8, ks, in ? 16 : 0);
+        cp_async16(sV + row * LD + c8 * 8, vs, in ? 16 : 0);
       }
-      cp_async16(sK + row * LD + c8 * 8, ks, in ? 16 : 0);
-      cp_async16(sV + row * LD + c8 * 8, vs, in ? 16 : 0);
-    }
+    };
+    kv_copies(false);
+    if (has_lo) kv_copies(true);
     for (int idx = mt; idx < 2 * 64 * (DH / 8); idx += 256) {
       const int pr = idx / (DH / 8), c8 = idx % (DH / 8);   // plane-row: plane pr / 64, row pr % 64
       const int row = pr & 63;
@@ -655,6 +721,16 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
   const size_t pl = (size_t)64 * qd;   // one plane
   for (int c0 = blockIdx.x * 256; c0 < items; c0 += gridDim.x * 256) {
     const int g0 = c0 / PER_HW;
+    // this thread's fragment of every key block, loaded before the weights so
+    // that both passes wait on one L2 round trip (up to kCombPre key blocks)
+    constexpr int kCombPre = 24;
+    const int it = c0 + mt;
+    const bool has_it = it < items;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o) + (has_it ? it : 0);
+    float4 ov[kCombPre];
+#pragma unroll
+    for (int e = 0; e < kCombPre; ++e)
+      ov[e] = (has_it && e < nkb) ? __ldcg(po + (size_t)e * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     // pass 1: weights of the rows of groups g0, g0 + 1 (16 rows each): thread
     // (row mt / 8, lane-group part mt % 8) takes key blocks part, part + 8, ...
     {
@@ -704,8 +780,7 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
     named_sync(3, 256);
     mk_mark(tr, 36);
     // pass 2: one fragment per thread
-    const int it = c0 + mt;
-    if (it < items) {
+    if (has_it) {
       const int lane = it & 31, j = (it >> 5) % NT, gg = it / PER_HW;
       const int h = gg / 8, w = gg % 8;
       const int rt = w & 3, half = w >> 2, g = lane >> 2, tq = lane & 3;
@@ -713,23 +788,24 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
       const int c = ((j < NT / 2) ? half * Q4 + j * 8 : HD + half * Q4 + (j - NT / 2) * 8) + 2 * tq;
       const float* w0 = sw + ((gg - g0) * 16 + g) * nkb;
       const float* w1 = w0 + 8 * nkb;
-      const float4* po = reinterpret_cast<const float4*>(a.part_o) + it;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < nkb; s0 += 16) {
-        float4 ov[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          ov[e] = (s0 + e < nkb) ? __ldcg(po + (size_t)(s0 + e) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          if (s0 + e < nkb) {
-            const float a0 = w0[s0 + e], a1 = w1[s0 + e];
-            acc.x += a0 * ov[e].x;
-            acc.y += a0 * ov[e].y;
-            acc.z += a1 * ov[e].z;
-            acc.w += a1 * ov[e].w;
-          }
+      for (int e = 0; e < kCombPre; ++e) {
+        if (e < nkb) {
+          const float a0 = w0[e], a1 = w1[e];
+          acc.x += a0 * ov[e].x;
+          acc.y += a0 * ov[e].y;
+          acc.z += a1 * ov[e].z;
+          acc.w += a1 * ov[e].w;
         }
+      }
+      for (int e = kCombPre; e < nkb; ++e) {   // longer caches
+        const float4 z = __ldcg(po + (size_t)e * o_stride);
+        const float a0 = w0[e], a1 = w1[e];
+        acc.x += a0 * z.x;
+        acc.y += a0 * z.y;
+        acc.z += a1 * z.z;
+        acc.w += a1 * z.w;
       }
       uint32_t hi, mid, lo;
       const size_t col = (size_t)h * DH + c;
@@ -754,28 +830,41 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
   fence_proxy_async_smem();   // sw's bytes are reused by TMA in the next phase
 }
 
-// Phase 7: h = GELU(r g) * (r u) for every token and FFN column, once, as the
-// exact bf16 planes of the down projection's operand; g and u are the sums of
-// the gate/up partial slabs.  r = rsqrt(mean(x^2) + eps) of the FFN input.
-__device__ __forceinline__ void mk_geglu_planes(const MkArgs& a, int splits, const float* ss2, float invD, int mt) {
+// h = GELU(r g) * (r u) for the 64 FFN columns of gate/up tile m and every
+// token, as the exact bf16 planes of the down projection's operand; g and u
+// are the finished gate/up sums, r = rsqrt(mean(x^2) + eps) of the FFN input.
+__device__ __forceinline__ void mk_geglu_tile(const MkArgs& a, int m, int part, int parts, const float* ss2,
+                                              float invD, int mt) {
   const int F = a.F;
-  const int n4 = a.T_q * F / 4;
-  const size_t pl = (size_t)64 * F, slab = (size_t)64 * 2 * F;
-  for (int i = blockIdx.x * 256 + mt; i < n4; i += gridDim.x * 256) {
-    const int t = (i * 4) / F, j = (i * 4) % F;
+  const size_t pl = (size_t)64 * F;
+  const int n = a.T_q * 16;
+  for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
+    const int t = it >> 4, i = (it & 15) * 4;
+    const float* gp = a.gu + (size_t)t * 2 * F + m * 128 + i;
+    const float4 g = __ldcg(reinterpret_cast<const float4*>(gp));
+    const float4 u = __ldcg(reinterpret_cast<const float4*>(gp + 64));
     const float rv = rsqrtf(__ldcg(ss2 + t) * invD + a.eps);
-    const float* gp = a.gu + (size_t)t * 2 * F + j;
-    const float4 g = sum_slabs(gp, slab, splits), u = sum_slabs(gp + F, slab, splits);
     const float h0 = gelu_tanh_fast(rv * g.x) * (rv * u.x), h1 = gelu_tanh_fast(rv * g.y) * (rv * u.y);
     const float h2 = gelu_tanh_fast(rv * g.z) * (rv * u.z), h3 = gelu_tanh_fast(rv * g.w) * (rv * u.w);
     uint32_t a0, b0, c0, a1, b1, c1;
     split_pair_exact(h0, h1, a0, b0, c0);
     split_pair_exact(h2, h3, a1, b1, c1);
-    uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + j);
+    uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + m * 64 + i);
     d[0] = make_uint2(a0, a1);
     d[pl / 4] = make_uint2(b0, b1);
     d[pl / 2] = make_uint2(c0, c1);
   }
+}
+
+// After the gate/up epilogue: every CTA of a tile (all K ranges) waits for
+// the tile, then writes its share of the tile's GeGLU planes.
+__device__ __forceinline__ void mk_gu_arrive(const MkArgs& a, int lr, const float* ss2, float invD, int mt) {
+  const MkGemm& g = a.g[2];
+  const MkRange r = mk_range(g, blockIdx.x);
+  if (!r.active) return;
+  unsigned* cnt = a.grp_cnt + kCntGuArr;
+  mk_group_wait(cnt + r.m, cnt, (unsigned)((lr + 1) * g.splits), a.err, 902, mt);
+  mk_geglu_tile(a, r.m, (int)blockIdx.x / g.MT, g.splits, ss2, invD, mt);
 }
 
 template <int DH>
@@ -994,30 +1083,36 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       unsigned long long* tr =
           (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * gridDim.x + blockIdx.x) * 64 : nullptr;
       mk_mark(tr, 0);
-      // phases: 0 QKV, 1 q / own k, v, 2 attention, 3 combine, 4 O, 5 gate/up,
-      // 6 GeGLU planes, 7 down; a grid barrier before each (the first one of a
-      // launch has none)
+      // phases: 0 QKV (+ q / own k, v), 2 attention, 3 combine, 4 O, 5 gate/up
+      // (+ GeGLU planes), 7 down; a grid barrier before each (the first one of
+      // a launch has none).  Indices 1 and 6 (former separate finalize phases)
+      // are skipped so trace slots keep their meaning.
+      const int lr = l - a.l0;
       for (int ph = 0; ph < 8; ++ph) {
+        if (ph == 1 || ph == 6) continue;   // finalized inside the QKV and gate/up phases
         if (ph > 0 || l > a.l0) mk_grid_sync(a.bar, ++nbar * G, a.err, mt);
         const bool proj = ph == 0 || ph == 4 || ph == 5 || ph == 7;
         if (proj && mt == 0) mbar_arrive(go);   // the loader may fetch this phase's operand
         mk_mark(tr, 2 * ph + 1);
-        if (ph == 1) {
-          mk_qkv_finalize<DH>(a, a.g[0].splits, ss1, kc, vc, invD, mt);
-        } else if (ph == 2) {
+        if (ph == 2) {
           mk_attention<DH>(a, kc, vc, sR, mt, tr);
         } else if (ph == 3) {
           mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR), tr);
-        } else if (ph == 6) {
-          mk_geglu_planes(a, a.g[2].splits, ss2, invD, mt);
+          // the QKV sums of the next block start from zero (every finalizer of
+          // this block is done before the barrier that opened phase 2)
+          mk_zero_f4(a.qkv, 16 * a.nqkv, mt);
         } else {
           const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
           float* out = ph == 0 ? a.qkv : ph == 5 ? a.gu : a.x;
           const int ld = ph == 0 ? a.nqkv : ph == 5 ? 2 * a.F : a.D;
           float* stats = ph == 0 ? ss1 : ph == 5 ? ss2 : nullptr;
-          const size_t slab = ph == 0 ? (size_t)64 * a.nqkv : ph == 5 ? (size_t)64 * 2 * a.F : 0;
-          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5, stats, out, ld, slab, a.T_q, a.err,
+          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5, stats, out, ld, a.T_q, a.err,
                        tr ? tr + 20 + 4 * gi : nullptr);
+          if (ph == 0) mk_qkv_arrive<DH>(a, lr, ss1, kc, vc, invD, mt);
+          if (ph == 5) mk_gu_arrive(a, lr, ss2, invD, mt);
+          // the gate/up sums of the next block start from zero (every GeGLU
+          // tile of this block was written before the barrier that opened phase 7)
+          if (ph == 7) mk_zero_f4(a.gu, 32 * a.F, mt);
         }
         mk_mark(tr, 2 * ph + 2);
       }
