@@ -396,13 +396,15 @@ static __global__ void attention_combine_kernel(AttnArgs a, int dh, __nv_bfloat1
 constexpr int kMaxSeg = 5;
 
 struct AttnSeg {
-  const __nv_bfloat16* k;    // bf16 keys (cache), or
+  const __nv_bfloat16* k;    // bf16 keys (cache; tensor-core kernel: their fp16 copy kh / vh), or
   const __nv_bfloat16* v;
   const float* k32;          // fp32 keys as computed (own chunk): split into hi + lo, or
   const float* v32;
   int n;
   const __half* k16;         // the same as two fp16 planes per key row (hi at column c,
   const __half* v16;         // lo at kv_ld + c; row stride 4 kv_ld): tensor-core kernel
+  const __half* kh;          // cached keys / values converted to fp16 (rows of kv_ld),
+  const __half* vh;          //   read by the tensor-core kernel
 };
 
 struct SegGroup {
@@ -419,8 +421,9 @@ struct SegAttnArgs {
   __half* out;               // fp16 planes [groups * T_rows][kActTerms * ldh]
   int ldh;
   unsigned long long* trace; // null, or per-block timestamps of CTA (0, 0, 0) (tensor-core kernel)
-  const __nv_bfloat16* ring; // tensor-core kernel: base of the KV ring (cached segments are rows of it)
-  const __half* own16;       //   and of the own fp16 planes
+  const __half* hist16;      // tensor-core kernel: base of the fp16 history copy (kh / vh are rows of it),
+  int hist_rows;             //   its rows,
+  const __half* own16;       //   and the base of the own fp16 planes
   SegGroup grp[16];
 };
 

@@ -7,6 +7,8 @@
 //   q, P       two fp16 planes (hi = fp16(x), lo = fp16(x - hi): 22 bits)
 //   cached K/V the ring's bf16 values converted to fp16 (exact for
 //              2^-14 <= |x| < 65504; below, fp16's subnormal spacing 2^-24)
+//              once per call by hist_to_f16_kernel, into a copy that every
+//              query tile and head then reads by TMA
 //   own K/V    two fp16 planes of the fp32 values
 //
 //   S  = (Q_hi + Q_lo) K^T  (+ Q_hi K_lo^T for own keys)
@@ -23,10 +25,11 @@
 // the softmax of block j; warp 1 (lane 0) moves K and V of each block by TMA
 // into one of two buffers each; warps 4..11 hold the rows: warp w reads TMEM
 // lanes 32 (w % 4) .. + 31, half (w - 4) / 4 of each block's keys and of the
-// output columns.  The row warps also turn each landed cached K/V block from
-// bf16 into fp16 in shared memory (8 chunks of 8 values per thread) and zero
-// the rows past its valid keys: K(j+1) before the softmax of block j, V(j)
-// right after writing its P.
+// output columns.  The row warps also release each landed K/V block to the
+// MMA warp, zeroing the rows past the valid keys of a partial own block
+// first (cached blocks need nothing: scores past the valid keys are masked,
+// and the rows after them in the fp16 copy are finite): K(j+1) before the
+// softmax of block j, V(j) right after writing its P.
 //
 // TMEM (512 columns): S of block j in columns 128 (j % 2) ..; the row warps
 // write P of the block back over its own S columns as packed fp16 (per
@@ -176,8 +179,8 @@ struct TcKeys {
         if (tab) tab->own_row = (int)((G.seg[s].k16 - a.own16) / (4 * (size_t)a.kv_ld));
       } else {
         if (tab) {
-          tab->krow[nseg_c] = (int)((G.seg[s].k - a.ring) / (size_t)a.kv_ld);
-          tab->vrow[nseg_c] = (int)((G.seg[s].v - a.ring) / (size_t)a.kv_ld);
+          tab->krow[nseg_c] = (int)((G.seg[s].kh - a.hist16) / (size_t)a.kv_ld);
+          tab->vrow[nseg_c] = (int)((G.seg[s].vh - a.hist16) / (size_t)a.kv_ld);
           tab->n[nseg_c] = G.seg[s].n;
           tab->blk0[nseg_c] = nb_c;
         }
@@ -205,7 +208,7 @@ struct TcKeys {
   }
 };
 
-// ring_map: the KV ring as rows of kv_ld bf16 (box 64 x 128, 128-byte swizzle);
+// ring_map: the fp16 history copy as rows of kv_ld (box 64 x 128, 128-byte swizzle);
 // own_map: the own fp16 planes as rows of 4 kv_ld, [K hi | K lo | V hi | V lo]
 // (box 64 x 64, same swizzle).
 static __global__ void __launch_bounds__(kTcThreads, 1)
@@ -335,7 +338,7 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- TMA: K and V of each block ----------------
-      // cached: two 128-row boxes of bf16 ring rows; own: two 64-row boxes of
+      // cached: two 128-row boxes of fp16 history rows; own: two 64-row boxes of
       // each fp16 plane, into the swizzled operand layout
       tma_prefetch_desc(&ring_map);
       tma_prefetch_desc(&own_map);
@@ -401,28 +404,14 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(q_full);
 
-    // a landed K or V block: cached -> fp16 in place (8 chunks per thread, loads
-    // first), rows past the valid keys zeroed; own -> only the zeroing
+    // a landed K or V block: own blocks get the rows past their valid keys
+    // zeroed (the own planes after a group's keys may hold anything)
     auto prep = [&](int j, bool isv) {
       const int bf = j & 1;
       tc_wait(isv ? &vt_full[bf] : &kt_full[bf], (uint32_t)(j >> 1) & 1u, err, isv ? 70 : 69);
       uint8_t* dst = (isv ? sV : sK) + bf * kTcBuf;
       const int nv = kk.valid(tab, j);
-      if (!kk.own(j)) {
-        uint4 v[8];
-        int off[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int it = st + 256 * u, r = it >> 4, c = it & 15;
-          off[u] = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          v[u] = *reinterpret_cast<const uint4*>(dst + off[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int r = (st + 256 * u) >> 4;
-          *reinterpret_cast<uint4*>(dst + off[u]) = r < nv ? bf16x8_to_f16x8(v[u]) : make_uint4(0, 0, 0, 0);
-        }
-      } else if (nv < kTcKBO) {
+      if (kk.own(j) && nv < kTcKBO) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int it = st + 256 * u, r = it >> 4, c = it & 15;
@@ -531,6 +520,26 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// The history K/V segments of one call (bf16 ring rows) -> their fp16 copy,
+// planes of `rows` x `cols`; the same conversion per value as bf16x8_to_f16x8.
+constexpr int kMaxHistPlanes = 128;
+struct HistCvtArgs {
+  const __nv_bfloat16* src[kMaxHistPlanes];
+  __half* dst[kMaxHistPlanes];
+  int planes, rows, cols;
+};
+
+static __global__ void __launch_bounds__(256) hist_to_f16_kernel(const __grid_constant__ HistCvtArgs a) {
+  const size_t per = (size_t)a.rows * a.cols / 8;   // 8-value chunks per plane
+  const size_t n = per * a.planes;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+    const int p = (int)(i / per);
+    const size_t j = i - (size_t)p * per;
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(a.src[p]) + j);
+    reinterpret_cast<uint4*>(a.dst[p])[j] = bf16x8_to_f16x8(v);
   }
 }
 

@@ -164,6 +164,8 @@ struct lat_ctx {
   double* theta = nullptr;
   float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32; prefix prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
+  __half* hist16 = nullptr;    // fp16 copy of one call's history K/V planes, [planes][T_q][D] (DiT)
+  int hist_rows = 0;
   __half *act2 = nullptr, *act2f = nullptr;   // fp16 activation planes [M][kActTerms * K]
   // the four block projections (merged QKV, output, FFN in, FFN out) of the dense
   // path are held as fp16 = 2^s x folded bf16 weight; wscale = 2^-s per matrix
@@ -734,6 +736,12 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
   LAT_TRY(c->alloc(&c->qbuf, (size_t)c->m_max * qd));
   if (d.kind == LAT_DIT) {
     LAT_TRY(c->alloc(&c->kvown16, (size_t)c->m_max * 4 * d.Hkv * d.dh));
+    const int planes = std::max(1, 2 * d.max_batch * d.n_hist);
+    if (planes > kMaxHistPlanes) return fail(LAT_ERR_SHAPE, "max_batch x n_hist must be <= %d", kMaxHistPlanes / 2);
+    if ((size_t)planes * d.T_q > 0x7fffffffu) return fail(LAT_ERR_SHAPE, "history copy too large for one tensor map");
+    c->hist_rows = planes * d.T_q;
+    LAT_TRY(c->alloc(&c->hist16, (size_t)c->hist_rows * d.D));
+    CUDA_TRY(cudaMemset(c->hist16, 0, (size_t)c->hist_rows * d.D * 2));   // rows never written stay finite
   } else {
     LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
     LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
@@ -887,11 +895,9 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
   const int dh = c->d.dh;
   if (dh == 128) {   // tensor-core attention: one CTA per (128 rows, head, group)
     const lat_model_desc& d = c->d;
-    if (!a.ring || !a.own16 || !aligned16(a.ring)) return fail(LAT_ERR_ALIGN, "KV ring NULL or not 16-byte aligned");
-    const size_t ring_rows = (size_t)d.n_streams * d.L * d.S * (d.n_hist + 1) * 2 * d.T_q;
-    if (ring_rows > 0x7fffffffu) return fail(LAT_ERR_SHAPE, "KV ring too large for one tensor map");
+    if (!a.hist16 || !a.own16) return fail(LAT_ERR_STATE, "tensor-core attention needs the fp16 history copy");
     CUtensorMap ring_map, own_map;
-    LAT_TRY(make_kmajor_map(&ring_map, a.ring, (int)ring_rows, a.kv_ld, 128));
+    LAT_TRY(make_kmajor_map(&ring_map, a.hist16, a.hist_rows, a.kv_ld, 128));
     LAT_TRY(make_kmajor_map(&own_map, a.own16, c->m_max, 4 * a.kv_ld, 64));
     dim3 grid((a.T_rows + 127) / 128, d.Hq, groups);
     attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, ring_map, own_map, c->err);
@@ -1001,6 +1007,9 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta; ra.q_out = c->qbuf; ra.kv_ld = D;
   ra.k16 = c->kvown16; ra.v16 = c->kvown16 + 2 * D; ra.ld16 = 4 * D;
   SegAttnArgs sa{};
+  HistCvtArgs hc{};   // every distinct history segment of the call, once, into the fp16 copy
+  hc.rows = T;
+  hc.cols = D;
   for (int b = 0; b < n; ++b) {
     const int cb = ch[b].chunk, sb = ch[b].step, stb = ch[b].stream;
     ra.pos0[b] = chunk_pos0(cb, T);
@@ -1010,8 +1019,22 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     for (int k = d.n_hist; k >= 1; --k) {       // history, oldest first
       const int cc = cb - k;
       if (cc < 0) continue;
-      sa.grp[b].seg[ns++] = AttnSeg{ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 0),
-                                    ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 1), nullptr, nullptr, T};
+      const bf16* hk = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 0);
+      const bf16* hv = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 1);
+      int p = 0;
+      while (p < hc.planes && hc.src[p] != hk) p += 2;
+      if (p == hc.planes) {
+        if (p + 2 > kMaxHistPlanes || (p + 2) * T > c->hist_rows) return fail(LAT_ERR_SHAPE, "history copy overflow");
+        hc.src[p] = hk;
+        hc.src[p + 1] = hv;
+        hc.dst[p] = c->hist16 + (size_t)p * T * D;
+        hc.dst[p + 1] = c->hist16 + (size_t)(p + 1) * T * D;
+        hc.planes = p + 2;
+      }
+      AttnSeg sg{hk, hv, nullptr, nullptr, T};
+      sg.kh = hc.dst[p];
+      sg.vh = hc.dst[p + 1];
+      sa.grp[b].seg[ns++] = sg;
     }
     // own keys as computed (fp16 hi/lo planes of the fp32 values); the ring slot holds their bf16 copy
     const __half* own = c->kvown16 + (size_t)b * T * 4 * D;
@@ -1020,11 +1043,17 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   }
   rope_kv_kernel<<<M, 128, 0, st>>>(ra);
   LAT_TRY(launch_check("rope_kv"));
+  if (hc.planes > 0) {   // after rope_kv: a chunk of this call may be another's history
+    const size_t chunks = (size_t)hc.planes * T * D / 8;
+    const unsigned grid = (unsigned)std::min<size_t>((chunks + 255) / 256, (size_t)c->num_sms * 8);
+    hist_to_f16_kernel<<<grid, 256, 0, st>>>(hc);
+    LAT_TRY(launch_check("hist_to_f16"));
+  }
   sa.q = c->qbuf; sa.q_ld = D; sa.T_rows = T; sa.Hq = d.Hq; sa.Hkv = d.Hkv; sa.kv_ld = D;
   sa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
   sa.out = c->act2; sa.ldh = D;
   sa.trace = c->attn_trace;
-  sa.ring = kv; sa.own16 = c->kvown16;
+  sa.hist16 = c->hist16; sa.hist_rows = c->hist_rows; sa.own16 = c->kvown16;
   LAT_TRY(enqueue_attention_seg(c, sa, n, st));
   {
     DenseArgs a{};
