@@ -62,6 +62,20 @@ struct DenseArgs {
   DevErr* err;
 };
 
+// Tile order: groups of kDGroupM m-tiles, m fastest within a group and the
+// group's n-tiles in turn.  A wave of CTAs then covers a block of about
+// kDGroupM m-tiles x (grid / kDGroupM) n-tiles: each weight tile crosses from
+// HBM once per group (its kDGroupM readers run together) and the group's
+// activation rows stay in L2 while the group sweeps the n-tiles.
+constexpr int kDGroupM = 8;
+__device__ __forceinline__ void dense_tile(int t, int m_tiles, int n_tiles, int& tm, int& tn) {
+  const int grp = t / (kDGroupM * n_tiles);
+  const int m0 = grp * kDGroupM, gm = min(kDGroupM, m_tiles - m0);
+  const int r = t - grp * kDGroupM * n_tiles;
+  tm = m0 + r % gm;
+  tn = r / gm;
+}
+
 constexpr int kDA = 128 * 64 * 2;   // A tile bytes (one plane, 128 tokens x 64)
 constexpr int kDB = 256 * 64 * 2;   // B tile bytes (256 weight rows x 64)
 // one pipeline slot: up to PLANES activation tiles + one weight tile
@@ -187,8 +201,8 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = a.N / 256;
-  const int tiles = ((a.M + 127) / 128) * n_tiles;
+  const int n_tiles = a.N / 256, m_tiles = (a.M + 127) / 128;
+  const int tiles = m_tiles * n_tiles;
   const int nkb = a.K / 64;                                   // K-blocks of one plane
   const int chunk_kb = kChunkMMA / (4 * a.terms);             // K-blocks per accumulation chunk
   const int nchunk = (nkb + chunk_kb - 1) / chunk_kb;
@@ -226,7 +240,8 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        const int tm = tile / n_tiles, tn = tile % n_tiles;
+        int tm, tn;
+        dense_tile(tile, m_tiles, n_tiles, tm, tn);
         for (int i = 0; i < nkb; ++i, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -281,7 +296,8 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
     uint32_t gch = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      const int tm = tile / n_tiles, tn = tile % n_tiles;
+      int tm, tn;
+      dense_tile(tile, m_tiles, n_tiles, tm, tn);
       const int row0 = tm * 128 + quad * 32;
       float acc[128];
 #pragma unroll
