@@ -52,13 +52,15 @@ CONFIGS = {
     # chunked AR-diffusion DiT stage, 1.3B class: 30 blocks, width 1536,
     # 12 heads x 128, GELU-tanh FFN 8960, chunk 1560 over 4 history chunks,
     # 4 denoise steps, 4 chunks (one per step) batched per block.
+    # Latent tokens of 64 channels enter / leave the stage through linear
+    # projections (lat_dim; the interleaved-schedule interval).
     "dit_1p3b": dict(kind="dit", D=1536, H=12, dh=128, F=8960, L=30, S=4,
                      T_chunk=1560, n_hist=4, t_dim=256, rope_base=10000.0,
-                     eps=1e-6, batches=(4,)),
+                     eps=1e-6, batches=(4,), lat_dim=64),
     # one 14B-class DiT block: width 5120, 40 heads x 128, FFN 13824.
     "dit_14b": dict(kind="dit", D=5120, H=40, dh=128, F=13824, L=1, S=4,
                     T_chunk=1560, n_hist=4, t_dim=256, rope_base=10000.0,
-                    eps=1e-6, batches=(1, 4, 8)),
+                    eps=1e-6, batches=(1, 4, 8), lat_dim=64),
 }
 
 WEIGHT_STD = 0.02
@@ -255,6 +257,11 @@ def dit_weights(cfg: dict, seed: int = 0, layers=None) -> dict:
         "bt2": normal_bf16(seed, "bt2", (D,), w),
         "wmod": normal_bf16(seed, "wmod", (D, 6 * D), w),
         "bmod": normal_bf16(seed, "bmod", (6 * D,), w),
+        # latent in / out projections of the stage (lat_dim channels)
+        "w_in": normal_bf16(seed, "dit.w_in", (cfg["lat_dim"], D), w),
+        "b_in": normal_bf16(seed, "dit.b_in", (D,), w),
+        "w_out": normal_bf16(seed, "dit.w_out", (D, cfg["lat_dim"]), w),
+        "b_out": normal_bf16(seed, "dit.b_out", (cfg["lat_dim"],), w),
     }
 
 
@@ -273,6 +280,11 @@ def dit_ring(cfg: dict, seed: int = 0, streams: int = 1, layers: int = 1,
 def dit_latents(cfg: dict, n: int, seed: int = 0, tag: str = "x") -> np.ndarray:
     """Residual-stream latents of n chunks, N(0,1) fp32: [n][T_chunk][D]."""
     return normal_f32(seed, tag, (n, cfg["T_chunk"], cfg["D"]))
+
+
+def dit_noise(cfg: dict, n: int, seed: int = 0, tag: str = "noise") -> np.ndarray:
+    """Starting latents of n chunks, N(0,1) fp32: [n][T_chunk][lat_dim]."""
+    return normal_f32(seed, tag, (n, cfg["T_chunk"], cfg["lat_dim"]))
 
 
 def dit_chunk_descs(cfg: dict, n: int, first_chunk: int = 7) -> list:

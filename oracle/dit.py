@@ -24,6 +24,14 @@ Readings where the pages are silent (listed in the design notes):
   ring's format), then runs attention for every chunk.  A chunk's history keys
   are the ring's bf16 values; its own keys enter its attention as computed.
   Two chunks of one call may not share a (stream, step, slot).
+* Latent in/out and the denoise step (silent on the pages; the survey's
+  reading): a chunk's latent z [T, A] enters the stage as x = z W_in + b_in, the
+  L blocks run at its step s, v = x W_out + b_out, and z <- z + dt v with
+  dt = 1 / S (the same grid t_s = s / S as the adaLN table).
+* Interleaved schedule (the article's steady state of one stream: the chunks
+  in flight sit at different denoise steps and run through every block as one
+  batch): interval i admits chunk i at step 0 and advances every chunk in
+  flight by one step; chunk c leaves after interval c + S - 1.
 """
 import numpy as np
 
@@ -137,3 +145,58 @@ def block_batch_rows(xs, descs, ring, table, w, cfg, rows):
         u2 = layernorm(h, eps) * (1.0 + sc2) + sh2
         out[b] = h + g2 * (gelu_tanh(u2 @ w["w1"]) @ w["w2"])
     return out
+
+
+def stage_interval(lats, descs, rings, table, W, cfg):
+    """One interval: chunk b of the batch (stream, chunk, step) = descs[b] runs
+    x = z W_in + b_in, all L blocks at its step, v = x W_out + b_out and the
+    Euler update z + dt v.
+
+    lats: list of [T, A] latents; rings: float64 [streams, L, S, n_hist+1, 2, T, D]
+    (modified in place, one ring per block as in ``block_batch``); table: the
+    adaLN table [S, 6D]; W: weights with "blocks", "w_in", "b_in", "w_out", "b_out".
+    Returns the updated latents.
+    """
+    dt = 1.0 / cfg["S"]
+    xs = np.stack([np.asarray(z, np.float64) @ W["w_in"] + W["b_in"] for z in lats])
+    for l, wl in enumerate(W["blocks"]):
+        xs = block_batch(xs, descs, rings[:, l], table, wl, cfg)
+    return [np.asarray(lats[b], np.float64) + dt * (xs[b] @ W["w_out"] + W["b_out"])
+            for b in range(len(descs))]
+
+
+def interval_descs(i: int, n_chunks: int, S: int, stream: int = 0) -> list:
+    """Chunks in flight during interval i of one stream, as (stream, chunk, step):
+    chunk c is at step i - c; ordered by chunk slot c mod S."""
+    chunks = [c for c in range(max(0, i - S + 1), min(i, n_chunks - 1) + 1)]
+    return sorted(((stream, c, i - c) for c in chunks), key=lambda d: d[1] % S)
+
+
+def pipeline(noises, rings, table, W, cfg, stream=0):
+    """Interleaved schedule over a stream of chunks; returns their final latents
+    in chunk order (chunk c is done after interval c + S - 1)."""
+    S, n = cfg["S"], len(noises)
+    live = {}
+    done = [None] * n
+    for i in range(n + S - 1):
+        if i < n:
+            live[i] = np.asarray(noises[i], np.float64)
+        descs = interval_descs(i, n, S, stream)
+        new = stage_interval([live[c] for (_, c, _) in descs], descs, rings, table, W, cfg)
+        for (_, c, _), z in zip(descs, new):
+            live[c] = z
+        if i - (S - 1) >= 0:
+            done[i - (S - 1)] = live.pop(i - (S - 1))
+    return done
+
+
+def sequential(noises, rings, table, W, cfg, stream=0):
+    """The plain order: every step of chunk c before chunk c + 1."""
+    out = []
+    for c, z in enumerate(noises):
+        z = np.asarray(z, np.float64)
+        for s in range(cfg["S"]):
+            z = stage_interval([z], [(stream, c, s)], rings, table, W, cfg)[0]
+        out.append(z)
+    return out
+

@@ -67,6 +67,11 @@ def _times_wrong(cfg):
     return [(s + 1) / S for s in range(S)]
 
 
+def _descs_step_off_by_one(i, n_chunks, S, stream=0):
+    chunks = [c for c in range(max(0, i - S + 1), min(i, n_chunks - 1) + 1)]
+    return sorted(((stream, c, min(S - 1, i - c + 1)) for c in chunks), key=lambda d: d[1] % S)
+
+
 _orig_attention = ops.attention
 
 MUTATIONS = [
@@ -80,6 +85,8 @@ MUTATIONS = [
     ((dit,), "history_chunks", _history_off_by_one, ["test_ring_slot_matches_fifo_simulation"]),
     ((fold, pi0), "fold_scale", _fold_no_round, ["test_rmsnorm_scale_fold_identity"]),
     ((pi0,), "times", _times_wrong, ["test_time_grid"]),
+    ((dit,), "interval_descs", _descs_step_off_by_one,
+     ["test_dit_interleaved_schedule", "test_dit_pipeline_equals_sequential"]),
 ]
 
 
