@@ -29,8 +29,9 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "pi0_ae"
 PAGES_AE_MS = 11.001   # pages' action-expert time, 2 views, RTX 4090 (context)
 # DRAM bytes (read + write) of one step-kernel launch from the ncu capture in
-# profiles/pi0_step_kernel_pi0_ae.md; None when the kernel changed since then
-STEP_TRAFFIC = None
+# profiles/pi0_step_kernel_pi0_ae.md (639.82 MB read + 4.22 MB written); set to
+# None whenever the kernel changes after that capture
+STEP_TRAFFIC = 644036864
 
 
 def parse():
@@ -51,6 +52,10 @@ DENSE_WORKLOADS = {
     "prefill_b1": ("prefill", 1, "ms per prefix prefill", "ms"),
     "prefill_b8": ("prefill", 8, "ms per prefix prefill", "ms"),
     "dit_1p3b": ("dit_1p3b", 4, "ms per denoised chunk", "ms"),
+    # steady state of the interleaved schedule through lat_dit_pipeline_push: one
+    # push admits a chunk, runs latent in/out + 30 blocks for the 4 chunks in
+    # flight (steps 0..3) and completes one chunk
+    "dit_1p3b_pipeline": ("dit_1p3b", 4, "ms per denoised chunk", "ms"),
     "dit_14b_n1": ("dit_14b", 1, "us per block", "us"),
     "dit_14b_n4": ("dit_14b", 4, "us per block", "us"),
     "dit_14b_n8": ("dit_14b", 8, "us per block", "us"),
@@ -391,6 +396,24 @@ def run_dense(args):
 
         def step():
             m.prefill(pe, kv, stream)
+        blocks = cfg["L"]
+    elif args.workload.endswith("_pipeline"):
+        m = DitStage(cfg, synth.dit_weights(cfg, 0), max_batch=nb, n_streams=1, device=dev)
+        ring = torch.randn(1, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
+                           generator=gen, device=dev).to(torch.bfloat16)
+        noise = torch.randn(cfg["T_chunk"], cfg["lat_dim"], generator=gen, device=dev)
+        done = torch.empty_like(noise)
+        cfg["Hkv"] = cfg["H"]
+        cfg["Hq"] = cfg["H"]
+        descs = synth.dit_chunk_descs(cfg, nb, first_chunk=nb + 3)
+        rows = nb * cfg["T_chunk"]
+        flops = dense_flops(cfg, nb, descs) + 2 * 2.0 * rows * cfg["lat_dim"] * cfg["D"]
+        ffn_n, ffn_k = cfg["F"], cfg["D"]
+        for _ in range(cfg["S"] - 1):   # fill the pipeline: from here on every push completes a chunk
+            m.push(ring, 0, noise, done, stream)
+
+        def step():
+            m.push(ring, 0, noise, done, stream)
         blocks = cfg["L"]
     else:
         descs = synth.dit_chunk_descs(cfg, nb)

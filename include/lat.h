@@ -78,7 +78,8 @@ typedef struct {
   int S;           /* denoise steps (action expert, DiT)                          */
   int T_prefix;    /* pi0: prefix tokens in the cache                             */
   int T_q;         /* pi0: query tokens (state + actions); DiT: tokens per chunk  */
-  int act_dim;     /* action expert: action/state width                          */
+  int act_dim;     /* action expert: action/state width; DiT: latent channels of */
+                   /* the stage's latent in/out projections (0 = none)            */
   int n_hist;      /* DiT: history chunks visible to a chunk (ring = n_hist+1)    */
   int t_dim;       /* DiT: sinusoidal timestep width of the adaLN MLP             */
   int patch_dim;   /* prefix: patch-embedding width                               */
@@ -112,6 +113,8 @@ typedef struct {
   const void *w_state, *b_state;   /* [act_dim][D], [D]                           */
   const void *g_final;             /* [D]                                         */
   const void *w_out, *b_out;       /* [D][act_dim], [act_dim]                     */
+  /* DiT with act_dim > 0: w_in, b_in and w_out, b_out are the stage's latent in- */
+  /* and out-projections (same shapes as above); the other fields above are unused */
   /* prefix: patch projection                                                     */
   const void *w_patch, *b_patch;   /* [patch_dim][D], [D]                         */
   /* DiT: timestep MLP producing the adaLN table                                   */
@@ -195,6 +198,48 @@ lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_
  * a CUDA graph; later calls replay it.  New addresses re-capture.
  */
 lat_status lat_denoise_chunk(lat_ctx *ctx, void *kv, const float *state, float *x, void *stream);
+
+/*
+ * lat_dit_interval -- LAT_DIT with latent I/O (act_dim > 0): one interval of
+ * the interleaved stage schedule of chunked autoregressive denoising
+ * (PhysisServe article: chunks at different denoise steps share the stage as
+ * one batch per block; a chunk reads the noisy KV that earlier chunks left at
+ * the same step).  Every chunk b of the batch, at its own step s_b, runs
+ *   x = z W_in + b_in,  the L blocks (lat_block_forward's math, all chunks
+ *   batched per block),  v = x W_out + b_out,  z <- z + dt[s_b] v
+ * with dt[s] = t_{s+1} - t_s of the context's schedule.
+ *  lat:    device fp32 [n][T_q][act_dim], the chunks' latents z, updated in place;
+ *  chunks: host [n], 1 <= n <= max_batch, the same rules as lat_block_forward
+ *          (no two chunks share (stream, step, ring slot): LAT_ERR_ARG);
+ *  kv:     the rings, as for lat_block_forward (every block's ring is written).
+ * Errors: LAT_ERR_STATE without latent I/O weights; LAT_ERR_ARG / LAT_ERR_ALIGN
+ * for bad arguments, detected before anything is enqueued.
+ */
+lat_status lat_dit_interval(lat_ctx *ctx, void *kv, float *lat, const lat_chunk_desc *chunks, int n,
+                            void *stream);
+
+/*
+ * lat_dit_pipeline_push -- the scheduler of one stream's steady state (same
+ * article): admit a new chunk and run one interval over every chunk in flight.
+ * The context keeps, per stream, the latents of the chunks in flight (at most
+ * S, one per denoise step) and the index of the next chunk.  A push
+ *  - with noise != NULL admits chunk c = (chunks admitted so far) at step 0,
+ *    its latent copied from noise (device fp32 [T_q][act_dim]);
+ *  - runs lat_dit_interval on the chunks in flight (chunk c' at the number of
+ *    intervals it has been through), then
+ *  - if a chunk has completed its S steps: copies its latent to done (device
+ *    fp32 [T_q][act_dim], may be NULL) and stores its index in *done_chunk
+ *    (host), else *done_chunk = -1.
+ * A push with noise == NULL only advances (drains) the chunks in flight.  In the
+ * steady state a push admits chunk c and completes chunk c - S + 1.  Requires
+ * S <= max_batch.  Asynchronous like every call; *done_chunk is known on return.
+ */
+lat_status lat_dit_pipeline_push(lat_ctx *ctx, void *kv, int stream_id, const float *noise, float *done,
+                                 int *done_chunk, void *stream);
+
+/* lat_dit_pipeline_reset -- forget the chunks in flight of one stream and start
+ * its chunk count at 0 again (host state only). */
+lat_status lat_dit_pipeline_reset(lat_ctx *ctx, int stream_id);
 
 /*
  * lat_debug_indices -- the integer maps the kernels use, computed by the same

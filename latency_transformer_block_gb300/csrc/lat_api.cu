@@ -176,6 +176,13 @@ struct lat_ctx {
 
   unsigned long long* attn_trace = nullptr;   // DiT: timestamps of the attention (measurement hook)
 
+  // DiT latent I/O (act_dim > 0) and the interleaved schedule
+  bf16 *wlin = nullptr, *blin = nullptr, *wlout = nullptr, *blout = nullptr;   // [A][D], [D], [D][A], [A]
+  float *dit_x = nullptr, *dit_z = nullptr, *dit_v = nullptr;   // [m_max][D], [m_max][A], [m_max][A]
+  float* pipe_lat = nullptr;                   // [n_streams][S][T_q][A]: latents in flight, slot c mod S
+  std::vector<int> pipe_next, pipe_done;       // per stream: chunks admitted / completed so far
+  std::vector<int> pipe_step;                  // [n_streams][S]: steps done by the chunk in each slot
+
   // captured denoise loop
   cudaGraphExec_t gexec = nullptr;
   void* g_kv = nullptr;
@@ -304,6 +311,7 @@ static lat_status check_desc(const lat_model_desc* d) {
   if (d->S <= 0 || d->T_q < 1 || d->n_hist < 0 || d->n_streams < 1 || d->t_dim <= 0 || d->t_dim % 2)
     return fail(LAT_ERR_SHAPE, "DiT: S, T_q, n_streams, t_dim must be positive (t_dim even), n_hist >= 0");
   if (d->n_hist + 1 > kMaxSeg) return fail(LAT_ERR_SHAPE, "n_hist must be <= 4");
+  if (d->act_dim < 0) return fail(LAT_ERR_SHAPE, "DiT: act_dim (latent channels) must be >= 0");
   return LAT_OK;
 }
 
@@ -828,6 +836,9 @@ static lat_status build_adaln(lat_ctx* c, const std::vector<double>& t) {
   cudaFree(e2);
   if (st != LAT_OK) return st;
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "adaLN table: %s", cudaGetErrorString(e));
+  std::vector<float> dts(S);   // Euler step sizes of the latent update
+  for (int s = 0; s < S; ++s) dts[s] = (float)(t[s + 1] - t[s]);
+  CUDA_TRY(cudaMemcpy(c->dt, dts.data(), dts.size() * sizeof(float), cudaMemcpyHostToDevice));
   return LAT_OK;
 }
 
@@ -882,10 +893,32 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
   CUDA_TRY(cudaMemcpy(c->wmod, w->wmod, (size_t)D * 6 * D * 2, cudaMemcpyDeviceToDevice));
   CUDA_TRY(cudaMemcpy(c->bmod, w->bmod, (size_t)6 * D * 2, cudaMemcpyDeviceToDevice));
   LAT_TRY(c->alloc(&c->adaln, (size_t)d.S * 6 * D));
+  LAT_TRY(c->alloc(&c->dt, (size_t)d.S));
   std::vector<double> t(d.S + 1);
   for (int s = 0; s <= d.S; ++s) t[s] = (double)s / d.S;
   LAT_TRY(build_adaln(c, t));
   LAT_TRY(alloc_dense_workspace(c, d.T_q));
+  if (d.act_dim > 0) {   // latent in/out projections (kept as bf16 [K][N]) and the schedule's state
+    const int A = d.act_dim;
+    const void* io[] = {w->w_in, w->b_in, w->w_out, w->b_out};
+    for (const void* p : io)
+      if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "latent in/out weight NULL or not 16-byte aligned");
+    LAT_TRY(c->alloc(&c->wlin, (size_t)A * D));
+    LAT_TRY(c->alloc(&c->blin, (size_t)D));
+    LAT_TRY(c->alloc(&c->wlout, (size_t)D * A));
+    LAT_TRY(c->alloc(&c->blout, (size_t)A));
+    CUDA_TRY(cudaMemcpy(c->wlin, w->w_in, (size_t)A * D * 2, cudaMemcpyDeviceToDevice));
+    CUDA_TRY(cudaMemcpy(c->blin, w->b_in, (size_t)D * 2, cudaMemcpyDeviceToDevice));
+    CUDA_TRY(cudaMemcpy(c->wlout, w->w_out, (size_t)D * A * 2, cudaMemcpyDeviceToDevice));
+    CUDA_TRY(cudaMemcpy(c->blout, w->b_out, (size_t)A * 2, cudaMemcpyDeviceToDevice));
+    LAT_TRY(c->alloc(&c->dit_x, (size_t)c->m_max * D));
+    LAT_TRY(c->alloc(&c->dit_z, (size_t)c->m_max * A));
+    LAT_TRY(c->alloc(&c->dit_v, (size_t)c->m_max * A));
+    LAT_TRY(c->alloc(&c->pipe_lat, (size_t)d.n_streams * d.S * d.T_q * A));
+    c->pipe_next.assign(d.n_streams, 0);
+    c->pipe_done.assign(d.n_streams, 0);
+    c->pipe_step.assign((size_t)d.n_streams * d.S, 0);
+  }
   LAT_TRY(build_rope_tables(c, d.T_q));
   CUDA_TRY(cudaDeviceSynchronize());
   return LAT_OK;
@@ -1083,6 +1116,38 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   return LAT_OK;
 }
 
+// One interval of the interleaved stage schedule for n chunks whose latents
+// sit at the device addresses lat[b] (gathered into one buffer for the
+// projections): x = z W_in + b_in, the L blocks, v = x W_out + b_out,
+// z += dt[step] v, scattered back.
+static lat_status enqueue_dit_interval(lat_ctx* c, bf16* kv, float* const* lat, const lat_chunk_desc* ch, int n,
+                                       cudaStream_t st) {
+  const lat_model_desc& d = c->d;
+  const int T = d.T_q, A = d.act_dim, D = d.D, M = n * T;
+  const size_t zb = (size_t)T * A * 4;
+  for (int b = 0; b < n; ++b)
+    if (lat[b] != c->dit_z + (size_t)b * T * A)
+      CUDA_TRY(cudaMemcpyAsync(c->dit_z + (size_t)b * T * A, lat[b], zb, cudaMemcpyDeviceToDevice, st));
+  LAT_TRY(small_gemm(c->dit_z, false, A, c->wlin, true, D, c->blin, true, c->dit_x, D, M, D, A, 0, st));
+  for (int l = 0; l < d.L; ++l) LAT_TRY(enqueue_dit_block(c, l, c->dit_x, ch, n, kv, st));
+  LAT_TRY(small_gemm(c->dit_x, false, D, c->wlout, true, A, c->blout, true, c->dit_v, A, M, A, D, 0, st));
+  DitEulerArgs e{};
+  e.z = c->dit_z;
+  e.v = c->dit_v;
+  e.dt = c->dt;
+  for (int b = 0; b < n; ++b) e.step[b] = ch[b].step;
+  e.T = T;
+  e.A = A;
+  e.n = n;
+  const size_t total = (size_t)M * A;
+  dit_euler_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(e);
+  LAT_TRY(launch_check("dit_euler"));
+  for (int b = 0; b < n; ++b)
+    if (lat[b] != c->dit_z + (size_t)b * T * A)
+      CUDA_TRY(cudaMemcpyAsync(lat[b], c->dit_z + (size_t)b * T * A, zb, cudaMemcpyDeviceToDevice, st));
+  return LAT_OK;
+}
+
 // ---------------------------------------------------------------------------
 // ABI
 // ---------------------------------------------------------------------------
@@ -1178,6 +1243,23 @@ static lat_status check_dev_err(lat_ctx* c) {
   return LAT_OK;
 }
 
+// A DiT batch: 1 <= n <= max_batch chunks with indices in range, no two
+// sharing (stream, step, ring slot).
+static lat_status check_chunks(const lat_ctx* c, const lat_chunk_desc* chunks, int n) {
+  if (!chunks || n < 1 || n > c->d.max_batch) return fail(LAT_ERR_ARG, "DiT: need 1 <= n <= max_batch chunks");
+  for (int i = 0; i < n; ++i) {
+    const lat_chunk_desc& a = chunks[i];
+    if (a.chunk < 0 || a.step < 0 || a.step >= c->d.S || a.stream < 0 || a.stream >= c->d.n_streams)
+      return fail(LAT_ERR_ARG, "chunk %d: index out of range", i);
+    if ((long long)a.chunk * c->d.T_q > 0x7fffffffLL) return fail(LAT_ERR_ARG, "chunk %d: position overflow", i);
+    for (int j = 0; j < i; ++j)
+      if (chunks[j].stream == a.stream && chunks[j].step == a.step &&
+          ring_slot_of(chunks[j].chunk, c->d.n_hist) == ring_slot_of(a.chunk, c->d.n_hist))
+        return fail(LAT_ERR_ARG, "chunks %d and %d share a ring slot", j, i);
+  }
+  return LAT_OK;
+}
+
 lat_status lat_block_forward(lat_ctx* c, int layer, float* x, const lat_chunk_desc* chunks, int n, void* kv,
                              void* stream) {
   if (!c || !x || !kv) return fail(LAT_ERR_ARG, "NULL argument");
@@ -1193,17 +1275,7 @@ lat_status lat_block_forward(lat_ctx* c, int layer, float* x, const lat_chunk_de
     return LAT_OK;
   }
   if (c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "lat_block_forward: the prefix model runs via lat_prefill_kv");
-  if (!chunks || n < 1 || n > c->d.max_batch) return fail(LAT_ERR_ARG, "DiT block: need 1 <= n <= max_batch chunks");
-  for (int i = 0; i < n; ++i) {
-    const lat_chunk_desc& a = chunks[i];
-    if (a.chunk < 0 || a.step < 0 || a.step >= c->d.S || a.stream < 0 || a.stream >= c->d.n_streams)
-      return fail(LAT_ERR_ARG, "chunk %d: index out of range", i);
-    if ((long long)a.chunk * c->d.T_q > 0x7fffffffLL) return fail(LAT_ERR_ARG, "chunk %d: position overflow", i);
-    for (int j = 0; j < i; ++j)
-      if (chunks[j].stream == a.stream && chunks[j].step == a.step &&
-          ring_slot_of(chunks[j].chunk, c->d.n_hist) == ring_slot_of(a.chunk, c->d.n_hist))
-        return fail(LAT_ERR_ARG, "chunks %d and %d share a ring slot", j, i);
-  }
+  LAT_TRY(check_chunks(c, chunks, n));
   return enqueue_dit_block(c, layer, x, chunks, n, reinterpret_cast<bf16*>(kv), reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -1242,6 +1314,73 @@ lat_status lat_denoise_chunk(lat_ctx* c, void* kv, const float* state, float* x,
     c->g_stream = stream;
   }
   CUDA_TRY(cudaGraphLaunch(c->gexec, st));
+  return LAT_OK;
+}
+
+static lat_status check_latent_io(const lat_ctx* c) {
+  if (c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "needs a LAT_DIT context");
+  if (c->d.act_dim <= 0 || !c->wlin) return fail(LAT_ERR_STATE, "the DiT context has no latent in/out projections");
+  return LAT_OK;
+}
+
+lat_status lat_dit_interval(lat_ctx* c, void* kv, float* lat, const lat_chunk_desc* chunks, int n, void* stream) {
+  if (!c || !kv || !lat) return fail(LAT_ERR_ARG, "NULL argument");
+  LAT_TRY(check_latent_io(c));
+  if (!aligned16(kv) || !aligned16(lat)) return fail(LAT_ERR_ALIGN, "kv / lat not 16-byte aligned");
+  LAT_TRY(check_chunks(c, chunks, n));
+  float* ptrs[kMaxChunks];
+  for (int b = 0; b < n; ++b) ptrs[b] = lat + (size_t)b * c->d.T_q * c->d.act_dim;
+  return enqueue_dit_interval(c, reinterpret_cast<bf16*>(kv), ptrs, chunks, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lat_status lat_dit_pipeline_push(lat_ctx* c, void* kv, int sid, const float* noise, float* done, int* done_chunk,
+                                 void* stream) {
+  if (!c || !kv || !done_chunk) return fail(LAT_ERR_ARG, "NULL argument");
+  *done_chunk = -1;
+  LAT_TRY(check_latent_io(c));
+  const lat_model_desc& d = c->d;
+  if (sid < 0 || sid >= d.n_streams) return fail(LAT_ERR_ARG, "stream_id %d out of range", sid);
+  if (d.S > d.max_batch) return fail(LAT_ERR_SHAPE, "the schedule needs S <= max_batch");
+  if (!aligned16(kv) || (noise && !aligned16(noise)) || (done && !aligned16(done)))
+    return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int S = d.S, T = d.T_q, A = d.act_dim;
+  int& next = c->pipe_next[sid];
+  int& fin = c->pipe_done[sid];
+  int* steps = &c->pipe_step[(size_t)sid * S];
+  auto slot = [&](int ch) { return c->pipe_lat + ((size_t)sid * S + ch % S) * T * A; };
+  if (noise) {
+    if ((long long)next * T > 0x7fffffffLL) return fail(LAT_ERR_ARG, "chunk position overflow: reset the stream");
+    CUDA_TRY(cudaMemcpyAsync(slot(next), noise, (size_t)T * A * 4, cudaMemcpyDeviceToDevice, st));
+    steps[next % S] = 0;
+    ++next;
+  }
+  const int n = next - fin;   // chunks in flight, fin .. next - 1
+  if (n == 0) return LAT_OK;
+  lat_chunk_desc ch[kMaxChunks];
+  float* ptrs[kMaxChunks];
+  for (int b = 0; b < n; ++b) {
+    const int cc = fin + b;
+    ch[b] = lat_chunk_desc{sid, cc, steps[cc % S]};
+    ptrs[b] = slot(cc);
+  }
+  LAT_TRY(check_chunks(c, ch, n));
+  LAT_TRY(enqueue_dit_interval(c, reinterpret_cast<bf16*>(kv), ptrs, ch, n, st));
+  for (int b = 0; b < n; ++b) ++steps[(fin + b) % S];
+  if (steps[fin % S] == S) {   // the oldest chunk has run its S steps
+    if (done) CUDA_TRY(cudaMemcpyAsync(done, slot(fin), (size_t)T * A * 4, cudaMemcpyDeviceToDevice, st));
+    *done_chunk = fin;
+    ++fin;
+  }
+  return LAT_OK;
+}
+
+lat_status lat_dit_pipeline_reset(lat_ctx* c, int sid) {
+  if (!c) return fail(LAT_ERR_ARG, "NULL argument");
+  LAT_TRY(check_latent_io(c));
+  if (sid < 0 || sid >= c->d.n_streams) return fail(LAT_ERR_ARG, "stream_id %d out of range", sid);
+  c->pipe_next[sid] = c->pipe_done[sid] = 0;
+  for (int s = 0; s < c->d.S; ++s) c->pipe_step[(size_t)sid * c->d.S + s] = 0;
   return LAT_OK;
 }
 

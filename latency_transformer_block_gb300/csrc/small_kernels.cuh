@@ -98,20 +98,22 @@ static __global__ void __launch_bounds__(256) head_euler_kernel(HeadArgs a) {
   }
   __syncthreads();
   // A outputs: thread (warp w, lane l) accumulates column l over rows n = w,
-  // w + 8, ...; 16 rows per pass with their weight loads in flight together
+  // w + 8, ...; 64 rows per pass with their weight loads in flight together
+  // (two L2 round trips for D = 1024)
+  constexpr int kPre = 64;
   for (int a0 = 0; a0 < a.A; a0 += 32) {
     const int col = a0 + lane;
     float acc = 0.f;
     if (col < a.A) {
-      for (int n0 = warp; n0 < a.D; n0 += 8 * 16) {
-        float wv[16];
+      for (int n0 = warp; n0 < a.D; n0 += 8 * kPre) {
+        float wv[kPre];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kPre; ++i) {
           const int n = n0 + 8 * i;
           wv[i] = n < a.D ? __ldg(a.wout + (size_t)n * a.A + col) : 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kPre; ++i) {
           const int n = n0 + 8 * i;
           if (n < a.D) acc = fmaf(sh[n], wv[i], acc);
         }
@@ -206,6 +208,23 @@ static __global__ void small_gemm_kernel(SmallGemmArgs a) {
   if (a.bias) acc += ld_any(a.bias, a.bias_bf16, n);
   if (a.act == 1) acc = silu(acc);
   a.C[(size_t)m * a.ldc + n] = acc;
+}
+
+// Euler step of the DiT latents of n chunks (T rows each): z[m][a] += dt[s_b] * v[m][a]
+// for row m of chunk b = m / T at its denoise step s_b.
+struct DitEulerArgs {
+  float* z;
+  const float* v;
+  const float* dt;
+  int step[16];
+  int T, A, n;
+};
+
+static __global__ void dit_euler_kernel(DitEulerArgs a) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)a.n * a.T * a.A) return;
+  const int b = (int)(i / ((size_t)a.T * a.A));
+  a.z[i] += a.dt[a.step[b]] * a.v[i];
 }
 
 // out[k][n] = g[k] * W[k][n] in fp32 (head fold; exact).

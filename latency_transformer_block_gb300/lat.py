@@ -85,6 +85,12 @@ def lib():
         L.lat_debug_step.restype = st
         L.lat_debug_trace.argtypes = [_P, _P, ctypes.c_longlong]
         L.lat_debug_trace.restype = st
+        L.lat_dit_interval.argtypes = [_P, _P, _P, ctypes.POINTER(ChunkDesc), ctypes.c_int, _P]
+        L.lat_dit_interval.restype = st
+        L.lat_dit_pipeline_push.argtypes = [_P, _P, ctypes.c_int, _P, _P, ctypes.POINTER(ctypes.c_int), _P]
+        L.lat_dit_pipeline_push.restype = st
+        L.lat_dit_pipeline_reset.argtypes = [_P, ctypes.c_int]
+        L.lat_dit_pipeline_reset.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -141,6 +147,20 @@ class Context:
             arr = (ChunkDesc * len(chunks))(*[ChunkDesc(*c) for c in chunks])
             check(lib().lat_block_forward(self.handle, layer, ptr(x), arr, len(chunks), ptr(kv),
                                           stream_ptr(stream)))
+
+    def dit_interval(self, kv, lat, chunks, stream=None):
+        arr = (ChunkDesc * len(chunks))(*[ChunkDesc(*c) for c in chunks])
+        check(lib().lat_dit_interval(self.handle, ptr(kv), ptr(lat), arr, len(chunks), stream_ptr(stream)))
+
+    def dit_pipeline_push(self, kv, stream_id, noise=None, done=None, stream=None):
+        """Admit `noise` (or drain when None); returns the index of the chunk completed (or -1)."""
+        out = ctypes.c_int(-1)
+        check(lib().lat_dit_pipeline_push(self.handle, ptr(kv), stream_id, ptr(noise), ptr(done),
+                                          ctypes.byref(out), stream_ptr(stream)))
+        return out.value
+
+    def dit_pipeline_reset(self, stream_id):
+        check(lib().lat_dit_pipeline_reset(self.handle, stream_id))
 
     def denoise_chunk(self, kv, state, x, stream=None):
         check(lib().lat_denoise_chunk(self.handle, ptr(kv), ptr(state), ptr(x), stream_ptr(stream)))

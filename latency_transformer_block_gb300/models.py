@@ -135,11 +135,25 @@ class DitStage:
         w.blocks = blocks
         for k in ("wt1", "bt1", "wt2", "bt2", "wmod", "bmod"):
             setattr(w, k, up(weight_bits[k]))
+        # latent in/out projections of the stage (interleaved schedule), when given
+        latent_io = "w_in" in weight_bits and cfg.get("lat_dim", 0) > 0
+        if latent_io:
+            for k in ("w_in", "b_in", "w_out", "b_out"):
+                setattr(w, k, up(weight_bits[k]))
         self._blocks = blocks
         cfg = dict(cfg, L=L)
         self.cfg = cfg
-        self.ctx = lat.Context(desc_from_config(cfg, lat.LAT_DIT, max_batch=max_batch, n_streams=n_streams), w)
+        desc = desc_from_config(cfg, lat.LAT_DIT, max_batch=max_batch, n_streams=n_streams)
+        desc.act_dim = cfg["lat_dim"] if latent_io else 0
+        self.ctx = lat.Context(desc, w)
         torch.cuda.synchronize()
+
+    def interval(self, ring: torch.Tensor, lat_z: torch.Tensor, chunks, stream=None):
+        """One interval of the interleaved schedule on latents lat_z [n][T][lat_dim] (in place)."""
+        self.ctx.dit_interval(ring, lat_z, chunks, stream=stream)
+
+    def push(self, ring: torch.Tensor, stream_id: int, noise=None, done=None, stream=None) -> int:
+        return self.ctx.dit_pipeline_push(ring, stream_id, noise, done, stream=stream)
 
     def block(self, layer, x: torch.Tensor, chunks, ring: torch.Tensor, stream=None):
         self.ctx.block_forward(layer, x, ring, chunks=chunks, stream=stream)
