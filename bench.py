@@ -72,6 +72,14 @@ def aggregate(elapsed_ms, units_per_rank, world, reduce_max):
     return t, units_per_rank * world
 
 
+def job_ms_per_chunk(elapsed_ms, steps, world, reduce_max):
+    """Replicas: every rank denoises `steps` chunks of its own; the job's time is
+    the slowest rank's, so the whole-job time per chunk is max_t / (steps * world).
+    Returns (ms per step on the slowest rank, whole-job ms per chunk)."""
+    t_max, chunks = aggregate(elapsed_ms, steps, world, reduce_max)
+    return t_max / steps, t_max / chunks
+
+
 def algorithmic_bytes(cfg):
     """Bytes per block-step and per chunk (weights read once + KV read once)."""
     D, F, Hq, Hkv, dh, L, S = cfg["D"], cfg["F"], cfg["Hq"], cfg["Hkv"], cfg["dh"], cfg["L"], cfg["S"]
@@ -266,9 +274,7 @@ def run_ours(args):
     clk = clocks.stop()
     m.ctx.sync()
     elapsed = e0.elapsed_time(e1)
-    t_max, chunks = aggregate(elapsed, args.steps, world, reduce_max)
-    ms_per_step = t_max / args.steps
-    value = ms_per_step / world if world > 1 else ms_per_step   # whole-job time per chunk
+    ms_per_step, value = job_ms_per_chunk(elapsed, args.steps, world, reduce_max)
 
     # --- end to end through the C ABI with host buffers (pinned), copies timed ---
     h_noise = torch.from_numpy(ib["noise"]).pin_memory()

@@ -26,9 +26,19 @@ struct NormArgs {
   __half* act2;            // [M][kActTerms * D]
 };
 
+// The row stays in registers (float4, up to kNormV per thread: D <= 8192) and
+// is read once; the planes are written 4 values (8 bytes) at a time.
+constexpr int kNormV = 8;
+
+__device__ __forceinline__ uint2 pack_half4(float a, float b, float c, float d) {
+  const __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+}
+
 static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
   const int m = blockIdx.x;
-  const float* xr = a.x + (size_t)m * a.D;
+  const int n4 = a.D / 4;
+  const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)m * a.D);
   __shared__ float red[8];
   __shared__ float stat[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -46,36 +56,57 @@ static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
     __syncthreads();
     return s;
   };
+  float4 v[kNormV];
+#pragma unroll
+  for (int u = 0; u < kNormV; ++u) {
+    const int c = threadIdx.x + 256 * u;
+    v[u] = c < n4 ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float mu = 0.f, rs;
   if (a.mode == NORM_LN_MOD) {
     float s = 0.f;
-    for (int c = threadIdx.x; c < a.D; c += 256) s += xr[c];
+#pragma unroll
+    for (int u = 0; u < kNormV; ++u) s += (v[u].x + v[u].y) + (v[u].z + v[u].w);
     mu = block_sum(s) / a.D;
-    float v = 0.f;
-    for (int c = threadIdx.x; c < a.D; c += 256) {
-      const float d = xr[c] - mu;
-      v += d * d;
-    }
-    rs = rsqrtf(block_sum(v) / a.D + a.eps);
+    float q = 0.f;
+#pragma unroll
+    for (int u = 0; u < kNormV; ++u)
+      if (threadIdx.x + 256 * u < n4) {
+        const float d0 = v[u].x - mu, d1 = v[u].y - mu, d2 = v[u].z - mu, d3 = v[u].w - mu;
+        q += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+      }
+    rs = rsqrtf(block_sum(q) / a.D + a.eps);
   } else {
-    float s = 0.f;
-    for (int c = threadIdx.x; c < a.D; c += 256) s += xr[c] * xr[c];
-    rs = rsqrtf(block_sum(s) / a.D + a.eps);
+    float q = 0.f;
+#pragma unroll
+    for (int u = 0; u < kNormV; ++u) q += (v[u].x * v[u].x + v[u].y * v[u].y) + (v[u].z * v[u].z + v[u].w * v[u].w);
+    rs = rsqrtf(block_sum(q) / a.D + a.eps);
   }
-  const float* sh = nullptr;
-  const float* sc = nullptr;
+  const float4* sh = nullptr;
+  const float4* sc = nullptr;
   if (a.mode == NORM_LN_MOD) {
     const int b = m / a.rows_per_chunk;
-    sh = a.table + a.shift_off[b];
-    sc = a.table + a.scale_off[b];
+    sh = reinterpret_cast<const float4*>(a.table + a.shift_off[b]);
+    sc = reinterpret_cast<const float4*>(a.table + a.scale_off[b]);
   }
   __half* hi = a.act2 + (size_t)m * kActTerms * a.D;
-  for (int c = threadIdx.x; c < a.D; c += 256) {
-    float u = (xr[c] - mu) * rs;
-    if (a.mode == NORM_LN_MOD) u = u * (1.f + sc[c]) + sh[c];
-    const __half h = __float2half_rn(u);
-    hi[c] = h;
-    hi[a.D + c] = __float2half_rn(u - __half2float(h));
+#pragma unroll
+  for (int u = 0; u < kNormV; ++u) {
+    const int c = threadIdx.x + 256 * u;
+    if (c >= n4) continue;
+    float w[4] = {(v[u].x - mu) * rs, (v[u].y - mu) * rs, (v[u].z - mu) * rs, (v[u].w - mu) * rs};
+    if (a.mode == NORM_LN_MOD) {
+      const float4 k = __ldg(sc + c), t = __ldg(sh + c);
+      w[0] = w[0] * (1.f + k.x) + t.x;
+      w[1] = w[1] * (1.f + k.y) + t.y;
+      w[2] = w[2] * (1.f + k.z) + t.z;
+      w[3] = w[3] * (1.f + k.w) + t.w;
+    }
+    const uint2 h = pack_half4(w[0], w[1], w[2], w[3]);
+    const __half2 h01 = *reinterpret_cast<const __half2*>(&h.x), h23 = *reinterpret_cast<const __half2*>(&h.y);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    *reinterpret_cast<uint2*>(hi + 4 * c) = h;
+    *reinterpret_cast<uint2*>(hi + a.D + 4 * c) = pack_half4(w[0] - f01.x, w[1] - f01.y, w[2] - f23.x, w[3] - f23.y);
   }
 }
 
@@ -131,45 +162,70 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
   const float* cj = a.cos_j + (size_t)j * half;
   const float* sj = a.sin_j + (size_t)j * half;
   const int nq = a.q_cols / a.dh, nk = a.kv_cols / a.dh;
-  for (int p = threadIdx.x; p < (nq + nk) * half; p += blockDim.x) {
-    const int head = p / half, i = p % half;
-    const float c = cj[i] * cb[i] - sj[i] * sb[i];
-    const float s = sj[i] * cb[i] + cj[i] * sb[i];
+  const int h4 = half / 4;
+  auto bf4 = [](const float (&y)[4]) {
+    const __nv_bfloat162 x = __floats2bfloat162_rn(y[0], y[1]), z = __floats2bfloat162_rn(y[2], y[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&z));
+  };
+  // 4 RoPE pairs (i .. i+3, i+half .. i+half+3) of one head per item: float4
+  // loads, 8- or 16-byte stores
+  for (int p = threadIdx.x; p < (nq + nk) * h4; p += blockDim.x) {
+    const int head = p / h4, i = (p % h4) * 4;
     const int col = head * a.dh + i;   // within q, or within k when head >= nq
-    const float x0 = row[col], x1 = row[col + half];
-    const float y0 = x0 * c - x1 * s, y1 = x1 * c + x0 * s;
+    const float4 cv = *reinterpret_cast<const float4*>(cj + i), sv = *reinterpret_cast<const float4*>(sj + i);
+    const float4 v0 = *reinterpret_cast<const float4*>(row + col);
+    const float4 v1 = *reinterpret_cast<const float4*>(row + col + half);
+    const float cjj[4] = {cv.x, cv.y, cv.z, cv.w}, sjj[4] = {sv.x, sv.y, sv.z, sv.w};
+    const float x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+    float y0[4], y1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float c = cjj[e] * cb[i + e] - sjj[e] * sb[i + e];
+      const float s = sjj[e] * cb[i + e] + cjj[e] * sb[i + e];
+      y0[e] = x0[e] * c - x1[e] * s;
+      y1[e] = x1[e] * c + x0[e] * s;
+    }
     if (head < nq) {
       float* qo = a.q_out + (size_t)m * a.q_cols + col;
-      qo[0] = y0;
-      qo[half] = y1;
+      *reinterpret_cast<float4*>(qo) = make_float4(y0[0], y0[1], y0[2], y0[3]);
+      *reinterpret_cast<float4*>(qo + half) = make_float4(y1[0], y1[1], y1[2], y1[3]);
     } else {
       __nv_bfloat16* kr = a.kdst[b] + (size_t)j * a.kv_ld + (col - a.q_cols);
-      kr[0] = __float2bfloat16_rn(y0);
-      kr[half] = __float2bfloat16_rn(y1);
+      *reinterpret_cast<uint2*>(kr) = bf4(y0);
+      *reinterpret_cast<uint2*>(kr + half) = bf4(y1);
       if (a.k16) {
         __half* k16 = a.k16 + (size_t)m * a.ld16 + (col - a.q_cols);
-        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
-        k16[0] = h0;
-        k16[half] = h1;
-        k16[a.kv_cols] = __float2half_rn(y0 - __half2float(h0));
-        k16[a.kv_cols + half] = __float2half_rn(y1 - __half2float(h1));
+        const uint2 h0 = pack_half4(y0[0], y0[1], y0[2], y0[3]), h1 = pack_half4(y1[0], y1[1], y1[2], y1[3]);
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&h0.x));
+        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&h0.y));
+        const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&h1.x));
+        const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&h1.y));
+        *reinterpret_cast<uint2*>(k16) = h0;
+        *reinterpret_cast<uint2*>(k16 + half) = h1;
+        *reinterpret_cast<uint2*>(k16 + a.kv_cols) = pack_half4(y0[0] - a0.x, y0[1] - a0.y, y0[2] - a1.x, y0[3] - a1.y);
+        *reinterpret_cast<uint2*>(k16 + a.kv_cols + half) =
+            pack_half4(y1[0] - b0.x, y1[1] - b0.y, y1[2] - b1.x, y1[3] - b1.y);
       } else {
         float* k32 = a.k32 + (size_t)m * a.kv_cols + (col - a.q_cols);
-        k32[0] = y0;
-        k32[half] = y1;
+        *reinterpret_cast<float4*>(k32) = make_float4(y0[0], y0[1], y0[2], y0[3]);
+        *reinterpret_cast<float4*>(k32 + half) = make_float4(y1[0], y1[1], y1[2], y1[3]);
       }
     }
   }
   const float* vr = row + a.q_cols + a.kv_cols;
-  for (int c = threadIdx.x; c < a.kv_cols; c += blockDim.x) {
-    a.vdst[b][(size_t)j * a.kv_ld + c] = __float2bfloat16_rn(vr[c]);
+  for (int c = 4 * threadIdx.x; c < a.kv_cols; c += 4 * blockDim.x) {
+    const float4 t = *reinterpret_cast<const float4*>(vr + c);
+    const float y[4] = {t.x, t.y, t.z, t.w};
+    *reinterpret_cast<uint2*>(a.vdst[b] + (size_t)j * a.kv_ld + c) = bf4(y);
     if (a.v16) {
       __half* v16 = a.v16 + (size_t)m * a.ld16 + c;
-      const __half h = __float2half_rn(vr[c]);
-      v16[0] = h;
-      v16[a.kv_cols] = __float2half_rn(vr[c] - __half2float(h));
+      const uint2 h = pack_half4(y[0], y[1], y[2], y[3]);
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+      *reinterpret_cast<uint2*>(v16) = h;
+      *reinterpret_cast<uint2*>(v16 + a.kv_cols) = pack_half4(y[0] - f0.x, y[1] - f0.y, y[2] - f1.x, y[3] - f1.y);
     } else {
-      a.v32[(size_t)m * a.kv_cols + c] = vr[c];
+      *reinterpret_cast<float4*>(a.v32 + (size_t)m * a.kv_cols + c) = t;
     }
   }
 }

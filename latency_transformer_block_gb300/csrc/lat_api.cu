@@ -161,6 +161,7 @@ struct lat_ctx {
   CUtensorMap map_up, map_down, map_patch;
   float *bpatch = nullptr, *adaln = nullptr, *cos_j = nullptr, *sin_j = nullptr, *qkvbuf = nullptr,
         *qbuf = nullptr;
+  float* adaln_tmp = nullptr;   // scratch of the adaLN table build: [S][t_dim], [S][D], [S][D]
   double* theta = nullptr;
   float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32; prefix prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
@@ -295,7 +296,7 @@ static lat_status check_desc(const lat_model_desc* d) {
   }
   // dense kinds: 128 x 256 x 64 tiles (every projection width a multiple of 256)
   if (d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 128 or 256 for the dense path");
-  if (d->D <= 0 || d->D % 256) return fail(LAT_ERR_SHAPE, "D must be a positive multiple of 256");
+  if (d->D <= 0 || d->D % 256 || d->D > 8192) return fail(LAT_ERR_SHAPE, "D must be a multiple of 256 in [256, 8192]");
   if ((d->Hq * d->dh) % 256) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 256");
   if (d->max_batch < 1 || d->max_batch > kMaxChunks) return fail(LAT_ERR_SHAPE, "max_batch must be in [1, 16]");
   if (d->kind == LAT_PI0_PREFIX) {
@@ -821,19 +822,16 @@ static lat_status build_adaln(lat_ctx* c, const std::vector<double>& t) {
     timestep_embedding_host(t[s], td, tmp);
     std::memcpy(&emb[(size_t)s * td], tmp.data(), td * sizeof(float));
   }
-  float *e0 = nullptr, *e1 = nullptr, *e2 = nullptr;
-  CUDA_TRY(cudaMalloc(&e0, (size_t)S * td * 4));
-  CUDA_TRY(cudaMalloc(&e1, (size_t)S * D * 4));
-  CUDA_TRY(cudaMalloc(&e2, (size_t)S * D * 4));
-  cudaMemcpy(e0, emb.data(), emb.size() * 4, cudaMemcpyHostToDevice);
+  // scratch owned by the context (allocated with it: a schedule change allocates nothing)
+  float* e0 = c->adaln_tmp;
+  float* e1 = e0 + (size_t)S * td;
+  float* e2 = e1 + (size_t)S * D;
+  CUDA_TRY(cudaMemcpy(e0, emb.data(), emb.size() * 4, cudaMemcpyHostToDevice));
   // e(t) = SiLU(temb Wt1 + bt1) Wt2 + bt2 ; A = SiLU(e) Wmod + bmod
   lat_status st = small_gemm(e0, false, td, c->wt1, true, D, c->bt1, true, e1, D, S, D, td, 1);
   if (st == LAT_OK) st = small_gemm(e1, false, D, c->wt2, true, D, c->bt2, true, e2, D, S, D, D, 1);
   if (st == LAT_OK) st = small_gemm(e2, false, D, c->wmod, true, 6 * D, c->bmod, true, c->adaln, 6 * D, S, 6 * D, D, 0);
   cudaError_t e = cudaDeviceSynchronize();
-  cudaFree(e0);
-  cudaFree(e1);
-  cudaFree(e2);
   if (st != LAT_OK) return st;
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "adaLN table: %s", cudaGetErrorString(e));
   std::vector<float> dts(S);   // Euler step sizes of the latent update
@@ -893,6 +891,7 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
   CUDA_TRY(cudaMemcpy(c->wmod, w->wmod, (size_t)D * 6 * D * 2, cudaMemcpyDeviceToDevice));
   CUDA_TRY(cudaMemcpy(c->bmod, w->bmod, (size_t)6 * D * 2, cudaMemcpyDeviceToDevice));
   LAT_TRY(c->alloc(&c->adaln, (size_t)d.S * 6 * D));
+  LAT_TRY(c->alloc(&c->adaln_tmp, (size_t)d.S * (td + 2 * D)));
   LAT_TRY(c->alloc(&c->dt, (size_t)d.S));
   std::vector<double> t(d.S + 1);
   for (int s = 0; s <= d.S; ++s) t[s] = (double)s / d.S;
