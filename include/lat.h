@@ -33,7 +33,7 @@
  *    Work is enqueued asynchronously; argument errors are detected on the host
  *    and returned before anything is enqueued.  A device-side wait that gives
  *    up (bounded spin) records LAT_ERR_TIMEOUT in the context; it is returned
- *    by lat_sync() and by the next call on that context.
+ *    by lat_sync(); lat_clear_error() makes the context usable again.
  *  - No call allocates device memory except lat_create (weights, tables,
  *    workspace) and the first lat_denoise_chunk on a new set of buffer
  *    addresses (graph instantiation).
@@ -351,6 +351,22 @@ lat_status lat_chunk_attention_noalloc(const float *q, const void *k, const void
 
 /* Wait for all work of the context and report a recorded device-side error. */
 lat_status lat_sync(lat_ctx *ctx);
+
+/*
+ * lat_clear_error -- after lat_sync has returned LAT_ERR_TIMEOUT: wait for the
+ * device, then clear the context's device error word so that its waits work
+ * again.  (While the word is set, every bounded wait of the context's kernels
+ * gives up at once and the results are meaningless.)  Synchronous.
+ */
+lat_status lat_clear_error(lat_ctx *ctx);
+
+/*
+ * lat_debug_timeout -- failure-detection check: enqueue one kernel whose
+ * bounded wait (on an mbarrier that nothing arrives on) gives up after the
+ * spin budget (~0.5 s) and records the error like any other wait of the path.
+ * The next lat_sync returns LAT_ERR_TIMEOUT; no GPU fault is involved.
+ */
+lat_status lat_debug_timeout(lat_ctx *ctx, void *stream);
 
 /* Human-readable name of a status; message of the last failure on this thread. */
 const char *lat_status_str(lat_status s);

@@ -1521,6 +1521,19 @@ lat_status lat_sync(lat_ctx* c) {
   return check_dev_err(c);
 }
 
+lat_status lat_clear_error(lat_ctx* c) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  CUDA_TRY(cudaDeviceSynchronize());
+  CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
+  return LAT_OK;
+}
+
+lat_status lat_debug_timeout(lat_ctx* c, void* stream) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  debug_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(c->err, 999);
+  return launch_check("debug_timeout");
+}
+
 void lat_destroy(lat_ctx* c) {
   if (!c) return;
   cudaDeviceSynchronize();

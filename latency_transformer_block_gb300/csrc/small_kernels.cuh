@@ -227,6 +227,19 @@ static __global__ void dit_euler_kernel(DitEulerArgs a) {
   a.z[i] += a.dt[a.step[b]] * a.v[i];
 }
 
+// Failure-detection check: one thread waits on an mbarrier that nothing
+// arrives on; the bounded wait gives up after the spin budget and records the
+// error in the context's error word (site `where`), as every wait of the path does.
+static __global__ void debug_timeout_kernel(DevErr* err, unsigned where) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, err, where);
+}
+
 // out[k][n] = g[k] * W[k][n] in fp32 (head fold; exact).
 static __global__ void scale_rows_f32_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, float* out, int K, int N) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;

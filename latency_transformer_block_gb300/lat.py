@@ -91,6 +91,10 @@ def lib():
         L.lat_dit_pipeline_push.restype = st
         L.lat_dit_pipeline_reset.argtypes = [_P, ctypes.c_int]
         L.lat_dit_pipeline_reset.restype = st
+        L.lat_clear_error.argtypes = [_P]
+        L.lat_clear_error.restype = st
+        L.lat_debug_timeout.argtypes = [_P, _P]
+        L.lat_debug_timeout.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -200,6 +204,12 @@ class Context:
 
     def sync(self):
         check(lib().lat_sync(self.handle))
+
+    def clear_error(self):
+        check(lib().lat_clear_error(self.handle))
+
+    def debug_timeout(self, stream=None):
+        check(lib().lat_debug_timeout(self.handle, stream_ptr(stream)))
 
     def close(self):
         if getattr(self, "handle", None):

@@ -42,3 +42,20 @@ def test_attention_kernel(name, T_q, T_kv):
     cfg, m = _ctx(name)
     got, ref = run_attention(m, cfg, T_q, T_kv, seed=T_q * 1000 + T_kv)
     assert_rel(got, ref, BLOCK_TOL, f"attention {name} {T_q}x{T_kv}")
+
+
+def test_device_wait_timeout_is_reported_and_cleared():
+    """Failure detection without a GPU fault: a bounded wait that nothing
+    completes gives up (~0.5 s), lat_sync reports LAT_ERR_TIMEOUT, and after
+    lat_clear_error the same context computes correct results again."""
+    from latency_transformer_block_gb300 import lat
+    cfg = synth.config("tiny")
+    m = Pi0ActionExpert(cfg, synth.pi0_weights(cfg, 0))
+    m.ctx.debug_timeout()
+    with pytest.raises(lat.LatError) as e:
+        m.ctx.sync()
+    assert e.value.code == 6                       # LAT_ERR_TIMEOUT
+    m.ctx.clear_error()
+    m.ctx.sync()
+    got, ref = run_attention(m, cfg, 64, 192, seed=5)
+    assert_rel(got, ref, BLOCK_TOL, "attention after a cleared timeout")
