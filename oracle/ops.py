@@ -54,8 +54,9 @@ def softmax(z: np.ndarray, axis: int = -1) -> np.ndarray:
     return e / np.sum(e, axis=axis, keepdims=True)
 
 
-def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
-    """softmax(q k^T * scale) v per head, no mask.
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, allow=None) -> np.ndarray:
+    """softmax(q k^T * scale) v per head; with `allow` (bool [Tq, Tk]) the
+    scores of disallowed (query, key) pairs are -inf before the softmax.
 
     q[Tq, Hq, dh], k/v[Tk, Hkv, dh]; query head h reads kv head h // (Hq/Hkv)
     (Hkv = 1 is multi-query attention, Hkv = Hq multi-head).
@@ -66,7 +67,10 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.n
     out = np.empty((Tq, Hq, v.shape[2]), dtype=np.float64)
     for h in range(Hq):
         j = h // group
-        p = softmax((q[:, h, :] @ k[:, j, :].T) * scale, axis=-1)
+        z = (q[:, h, :] @ k[:, j, :].T) * scale
+        if allow is not None:
+            z = np.where(allow, z, -np.inf)
+        p = softmax(z, axis=-1)
         out[:, h, :] = p @ v[:, j, :]
     return out
 

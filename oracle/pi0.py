@@ -72,6 +72,18 @@ def qkv(x, w, cfg):
     return q, k, v
 
 
+def chunk_mask(T, Tp, cfg):
+    """Which keys [prefix | own] each query token of the chunk sees: all of
+    them (default, bidirectional), or with cfg["prefix_lm"] the block mask of the
+    pi0 model, where the state token (query 0) sees the prefix and itself only
+    and the action tokens see everything.  None when nothing is masked."""
+    if not cfg.get("prefix_lm"):
+        return None
+    allow = np.ones((T, Tp + T), dtype=bool)
+    allow[0, Tp + 1:] = False
+    return allow
+
+
 def block(x, k_prefix, v_prefix, pos, w, cfg, kv_only=False):
     """One pre-norm block over [prefix KV | own tokens].
 
@@ -94,7 +106,7 @@ def block(x, k_prefix, v_prefix, pos, w, cfg, kv_only=False):
         return None, k_own, v_own
     K = np.concatenate([k_prefix, k]).reshape(-1, Hkv, dh)
     V = np.concatenate([v_prefix, v]).reshape(-1, Hkv, dh)
-    o = attention(q, K, V, 1.0 / np.sqrt(dh)).reshape(T, Hq * dh)
+    o = attention(q, K, V, 1.0 / np.sqrt(dh), allow=chunk_mask(T, k_prefix.shape[0], cfg)).reshape(T, Hq * dh)
     h = x + o @ w["wo"]
     hn = rmsnorm(h, cfg["eps"]) * w["g_ffn"]
     f = (gelu_tanh(hn @ w["wg"]) * (hn @ w["wu"])) @ w["wd"]

@@ -72,6 +72,14 @@ def _descs_step_off_by_one(i, n_chunks, S, stream=0):
     return sorted(((stream, c, min(S - 1, i - c + 1)) for c in chunks), key=lambda d: d[1] % S)
 
 
+def _mask_wrong_row(T, Tp, cfg):
+    if not cfg.get("prefix_lm"):
+        return None
+    allow = np.ones((T, Tp + T), dtype=bool)
+    allow[T - 1, Tp + 1:] = False
+    return allow
+
+
 _orig_attention = ops.attention
 
 MUTATIONS = [
@@ -85,6 +93,7 @@ MUTATIONS = [
     ((dit,), "history_chunks", _history_off_by_one, ["test_ring_slot_matches_fifo_simulation"]),
     ((fold, pi0), "fold_scale", _fold_no_round, ["test_rmsnorm_scale_fold_identity"]),
     ((pi0,), "times", _times_wrong, ["test_time_grid"]),
+    ((pi0,), "chunk_mask", _mask_wrong_row, ["test_pi0_prefix_lm_mask"]),
     ((dit,), "interval_descs", _descs_step_off_by_one,
      ["test_dit_interleaved_schedule", "test_dit_pipeline_equals_sequential"]),
 ]

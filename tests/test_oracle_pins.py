@@ -477,3 +477,38 @@ def test_dit_pipeline_linear_field_closed_form():
     for z0, z in zip(noises, out):
         ref = np.asarray(z0, np.float64) @ np.linalg.matrix_power(P, S) + dt * (k @ geo)
         assert np.allclose(z, ref, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# pi0 block mask variant (state token sees the prefix and itself only)
+# ---------------------------------------------------------------------------
+def test_masked_attention_is_attention_over_the_allowed_keys():
+    q = RNG.standard_normal((5, 2, 4))
+    k = RNG.standard_normal((7, 1, 4))
+    v = RNG.standard_normal((7, 1, 3))
+    allow = RNG.random((5, 7)) < 0.6
+    allow[:, 2] = True                              # every row sees at least one key
+    got = ops.attention(q, k, v, 0.5, allow=allow)
+    for t in range(5):
+        keys = np.flatnonzero(allow[t])
+        ref = _attention_loops(q[t:t + 1], k[keys], v[keys], 0.5)
+        assert np.allclose(got[t:t + 1], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_pi0_prefix_lm_mask():
+    """With the block mask the state token's row equals a block run on the state
+    token alone (it sees the prefix and itself), and the action rows equal the
+    unmasked block's (they see every key either way)."""
+    cfg, wb, ib = _tiny_pi0()
+    blk = pi0.decode_tree(wb["blocks"][0])
+    kv = bf16.decode(ib["kv"][0])
+    x = RNG.standard_normal((cfg["T_q"], cfg["D"]))
+    Tp = cfg["T_prefix"]
+    pos = Tp + np.arange(cfg["T_q"])
+    full, _, _ = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, blk, cfg)
+    cm = dict(cfg, prefix_lm=1)
+    masked, k_m, v_m = pi0.block(x, kv[0, :Tp], kv[1, :Tp], pos, blk, cm)
+    alone, _, _ = pi0.block(x[:1], kv[0, :Tp], kv[1, :Tp], pos[:1], blk, cm)
+    assert np.allclose(masked[0], alone[0], rtol=1e-12, atol=1e-13)
+    assert np.array_equal(masked[1:], full[1:])
+    assert not np.allclose(masked[0], full[0])
