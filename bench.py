@@ -41,7 +41,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD] + list(DENSE_WORKLOADS),
+    p.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "pi0_cycle"] + list(DENSE_WORKLOADS),
                    help="pi0_ae (default: the headline line) or one dense configuration")
     return p.parse_args()
 
@@ -496,10 +496,91 @@ def run_dense(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cycle(args):
+    """Control cycle of the pi0 pipeline: prefill of a new observation's prefix
+    KV (B = 1) and one denoised action chunk.  Sequential: both on one stream.
+    Concurrent (the reading note's two-stream scheme): the prefill writes the
+    next cache on one stream while the action expert works from the previous
+    cache on another; the two caches swap every cycle."""
+    import torch
+    rank, local_rank, world = dist_info()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from latency_transformer_block_gb300 import build as B
+    B.build()
+    from latency_transformer_block_gb300 import synth
+    from latency_transformer_block_gb300.models import Pi0ActionExpert, Pi0Prefix
+
+    cp, ca = synth.config("prefill"), synth.config(WORKLOAD)
+    pre = Pi0Prefix(cp, synth.prefill_weights(cp, 0), max_batch=1, device=dev)
+    ae = Pi0ActionExpert(ca, synth.pi0_weights(ca, 0), device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    pe = torch.randn(1, cp["T_prefix"], cp["patch_dim"], generator=gen, device=dev).to(torch.bfloat16)
+    kvs = [pre.new_kv(1)[:, 0] for _ in range(2)]       # [L][2][T_prefix + T_q][Hkv dh] each
+    ib = synth.pi0_inputs(ca, 0)
+    state = torch.from_numpy(ib["state"]).to(dev)
+    noise = torch.from_numpy(ib["noise"]).to(dev)
+    x = noise.clone()
+    sa, sb = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for k in kvs:
+        pre.prefill(pe, k.unsqueeze(1), sa)
+    sa.synchronize()
+
+    def cycle(i, concurrent):
+        s2 = sb if concurrent else sa
+        pre.prefill(pe, kvs[i % 2].unsqueeze(1), sa)
+        with torch.cuda.stream(s2):
+            x.copy_(noise, non_blocking=True)
+        ae.denoise(kvs[(i + 1) % 2], state, x, s2)
+        if concurrent:             # the cycle ends when both are done
+            ea, eb = torch.cuda.Event(), torch.cuda.Event()
+            ea.record(sa)
+            eb.record(sb)
+            sa.wait_event(eb)
+            sb.wait_event(ea)
+
+    def timed(concurrent):
+        for i in range(max(3, args.warmup)):
+            cycle(i, concurrent)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        for i in range(args.steps):
+            cycle(i, concurrent)
+        e1.record(sa)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    seq_ms = timed(False)
+    conc_ms = timed(True)
+    clk = clocks.stop()
+    ae.ctx.sync()
+    pre.ctx.sync()
+    line = {
+        "metric": "ms per control cycle (prefix prefill B=1 + one denoised action chunk)",
+        "value": round(conc_ms, 4), "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(conc_ms, 4), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) bf16 weights)",
+        "config": {"workload": "pi0_cycle", "sequential_ms": round(seq_ms, 4), "concurrent_ms": round(conc_ms, 4),
+                   "streams": 2, "caches": 2,
+                   "l2": "inputs larger than L2 (4.0 GB prefix weights + 623 MB expert weights per cycle)"},
+        "roofline": None, "clocks": clk, "e2e": None, "gpu_launches": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "pi0_cycle":
+        run_cycle(args)
     elif args.workload != WORKLOAD:
         run_dense(args)
     else:

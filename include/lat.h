@@ -87,6 +87,9 @@ typedef struct {
   int n_streams;   /* DiT: number of independent rings in the kv buffer           */
   float rope_base; /* RoPE base (10000)                                           */
   float eps;       /* norm epsilon (1e-6)                                         */
+  int prefix_lm;   /* action expert: 0 = the chunk's tokens all see each other;   */
+                   /* 1 = the pi0 model's block mask: the state token (token 0)   */
+                   /* sees the prefix and itself only, the action tokens every key */
 } lat_model_desc;
 
 /* One block's weights (device, bf16, [K_in][N_out] row-major; vectors [D]). */
@@ -195,7 +198,9 @@ lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_
  *  x:     device fp32 [T_q - 1][act_dim]: the initial noise in, the actions out
  *         (x <- x + dt * v after every step).
  * The first call for a given (kv, state, x, stream) captures the whole loop in
- * a CUDA graph; later calls replay it.  New addresses re-capture.
+ * a CUDA graph; later calls replay it.  The context keeps the graphs of up to 4
+ * such tuples (e.g. two caches used in turn while the next one is prefilled on
+ * another stream); a fifth replaces the least recently used one.
  */
 lat_status lat_denoise_chunk(lat_ctx *ctx, void *kv, const float *state, float *x, void *stream);
 

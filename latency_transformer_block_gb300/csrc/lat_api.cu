@@ -185,11 +185,24 @@ struct lat_ctx {
   std::vector<int> pipe_step;                  // [n_streams][S]: steps done by the chunk in each slot
 
   // captured denoise loop
-  cudaGraphExec_t gexec = nullptr;
-  void* g_kv = nullptr;
-  const float* g_state = nullptr;
-  float* g_x = nullptr;
-  void* g_stream = nullptr;
+  // captured denoise loops, one per (kv, state, x, stream), least recently used replaced
+  struct Graph {
+    cudaGraphExec_t exec = nullptr;
+    void* kv = nullptr;
+    const float* state = nullptr;
+    float* x = nullptr;
+    void* stream = nullptr;
+    unsigned long long used = 0;
+  };
+  static constexpr int kGraphs = 4;
+  Graph graphs[kGraphs];
+  unsigned long long graph_clock = 0;
+  void drop_graphs() {
+    for (Graph& g : graphs) {
+      if (g.exec) cudaGraphExecDestroy(g.exec);
+      g = Graph{};
+    }
+  }
 
   template <class T>
   lat_status alloc(T** p, size_t count) {
@@ -201,7 +214,7 @@ struct lat_ctx {
     return LAT_OK;
   }
   ~lat_ctx() {
-    if (gexec) cudaGraphExecDestroy(gexec);
+    drop_graphs();
     for (void* p : allocs) cudaFree(p);
   }
 };
@@ -292,14 +305,17 @@ static lat_status check_desc(const lat_model_desc* d) {
     if (d->T_q < 2 || d->T_q > 64) return fail(LAT_ERR_SHAPE, "T_q must be in [2, 64]");
     if (d->T_prefix < 0) return fail(LAT_ERR_SHAPE, "T_prefix must be >= 0");
     if (d->act_dim <= 0) return fail(LAT_ERR_SHAPE, "act_dim must be positive");
+    if (d->prefix_lm != 0 && d->prefix_lm != 1) return fail(LAT_ERR_ARG, "prefix_lm must be 0 or 1");
     return LAT_OK;
   }
   // dense kinds: 128 x 256 x 64 tiles (every projection width a multiple of 256)
   if (d->dh != 128 && d->dh != 256) return fail(LAT_ERR_SHAPE, "dh must be 128 or 256 for the dense path");
   if (d->D <= 0 || d->D % 256 || d->D > 8192) return fail(LAT_ERR_SHAPE, "D must be a multiple of 256 in [256, 8192]");
+  if (d->prefix_lm) return fail(LAT_ERR_ARG, "prefix_lm applies to the action expert only");
   if ((d->Hq * d->dh) % 256) return fail(LAT_ERR_SHAPE, "Hq dh must be a multiple of 256");
   if (d->max_batch < 1 || d->max_batch > kMaxChunks) return fail(LAT_ERR_SHAPE, "max_batch must be in [1, 16]");
   if (d->kind == LAT_PI0_PREFIX) {
+    if (d->dh != 256) return fail(LAT_ERR_SHAPE, "prefix model: dh must be 256");
     if (((d->Hq + 2 * d->Hkv) * d->dh) % 256 || (2 * d->Hkv * d->dh) % 256)
       return fail(LAT_ERR_SHAPE, "QKV and KV widths must be multiples of 256");
     if (d->F % 128) return fail(LAT_ERR_SHAPE, "F must be a multiple of 128");
@@ -587,6 +603,7 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     m.T_prefix = d.T_prefix;
     m.T_kv = T_kv;
     m.nqkv = c->nqkv;
+    m.prefix_lm = d.prefix_lm;
     m.eps = d.eps;
     m.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
     const GemmPlan* gp[4] = {&c->g_qkv, &c->g_o, &c->g_gu, &c->g_d};
@@ -1283,10 +1300,16 @@ lat_status lat_denoise_chunk(lat_ctx* c, void* kv, const float* state, float* x,
   if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "lat_denoise_chunk needs an action-expert context");
   if (!aligned16(kv) || !aligned16(state) || !aligned16(x)) return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (!c->gexec || c->g_kv != kv || c->g_state != state || c->g_x != x || c->g_stream != stream) {
-    if (c->gexec) {
-      cudaGraphExecDestroy(c->gexec);
-      c->gexec = nullptr;
+  lat_ctx::Graph* gr = nullptr;
+  for (lat_ctx::Graph& g : c->graphs)
+    if (g.exec && g.kv == kv && g.state == state && g.x == x && g.stream == stream) gr = &g;
+  if (!gr) {
+    gr = &c->graphs[0];   // a free slot, else the least recently used one
+    for (lat_ctx::Graph& g : c->graphs)
+      if (!g.exec || (gr->exec && g.used < gr->used)) gr = &g;
+    if (gr->exec) {
+      cudaGraphExecDestroy(gr->exec);
+      *gr = lat_ctx::Graph{};
     }
     cudaStream_t cap = st;
     bool own = false;
@@ -1304,15 +1327,19 @@ lat_status lat_denoise_chunk(lat_ctx* c, void* kv, const float* state, float* x,
       return s;
     }
     if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
-    e = cudaGraphInstantiate(&c->gexec, g, 0);
+    e = cudaGraphInstantiate(&gr->exec, g, 0);
     cudaGraphDestroy(g);
-    if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
-    c->g_kv = kv;
-    c->g_state = state;
-    c->g_x = x;
-    c->g_stream = stream;
+    if (e != cudaSuccess) {
+      gr->exec = nullptr;
+      return fail(LAT_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    }
+    gr->kv = kv;
+    gr->state = state;
+    gr->x = x;
+    gr->stream = stream;
   }
-  CUDA_TRY(cudaGraphLaunch(c->gexec, st));
+  gr->used = ++c->graph_clock;
+  CUDA_TRY(cudaGraphLaunch(gr->exec, st));
   return LAT_OK;
 }
 
@@ -1499,10 +1526,7 @@ lat_status lat_debug_trace(lat_ctx* c, unsigned long long* buf, long long n) {
   if (buf && n < (long long)c->num_sms * c->d.L * 64) return fail(LAT_ERR_SHAPE, "trace buffer too small");
   if (buf && (reinterpret_cast<uintptr_t>(buf) & 7u)) return fail(LAT_ERR_ALIGN, "trace buffer not 8-byte aligned");
   c->mk.trace = buf;
-  if (c->gexec) {   // the captured graph holds the old arguments
-    cudaGraphExecDestroy(c->gexec);
-    c->gexec = nullptr;
-  }
+  c->drop_graphs();   // the captured graphs hold the old arguments
   return LAT_OK;
 }
 

@@ -80,6 +80,7 @@ struct MkArgs {
   MkGemm g[4];              // 0 QKV, 1 O, 2 gate/up, 3 down
   int l0, l1;               // layers [l0, l1) of this launch
   int D, F, Hq, Hkv, T_q, T_prefix, T_kv, nqkv;
+  int prefix_lm;            // 1: the state token (query row 0) sees the prefix and itself only
   float eps, scale_log2;
   float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
   float* qkv;               // fp32 [64][nqkv] QKV sums (vector reductions of every K range; 0 at entry,
@@ -621,12 +622,15 @@ __device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc,
       s[j][3] = (sa[j][3] + sb[j][3]) + p1.y;
     }
     // ---- softmax of this key block (base 2) ----
+    // keys a row may see: all T_kv, or with the block mask the state token
+    // (row 0) only the prefix and itself (keys < T_prefix + 1)
+    const int lim0 = (a.prefix_lm && r0 == 0) ? a.T_prefix + 1 : a.T_kv;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int key = kb * KB + j * 8 + 2 * tq;
-      s[j][0] = (key < a.T_kv) ? s[j][0] * a.scale_log2 : -INFINITY;
-      s[j][1] = (key + 1 < a.T_kv) ? s[j][1] * a.scale_log2 : -INFINITY;
+      s[j][0] = (key < lim0) ? s[j][0] * a.scale_log2 : -INFINITY;
+      s[j][1] = (key + 1 < lim0) ? s[j][1] * a.scale_log2 : -INFINITY;
       s[j][2] = (key < a.T_kv) ? s[j][2] * a.scale_log2 : -INFINITY;
       s[j][3] = (key + 1 < a.T_kv) ? s[j][3] * a.scale_log2 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
@@ -636,13 +640,16 @@ __device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc,
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    // a row with every key of the block masked keeps max -inf (weight 0 in the
+    // combine); its exponentials are taken against 0 so that they are 0, not NaN
+    const float e0 = mx0 == -INFINITY ? 0.f : mx0, e1 = mx1 == -INFINITY ? 0.f : mx1;
     float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      s[j][0] = exp2f(s[j][0] - mx0);
-      s[j][1] = exp2f(s[j][1] - mx0);
-      s[j][2] = exp2f(s[j][2] - mx1);
-      s[j][3] = exp2f(s[j][3] - mx1);
+      s[j][0] = exp2f(s[j][0] - e0);
+      s[j][1] = exp2f(s[j][1] - e0);
+      s[j][2] = exp2f(s[j][2] - e1);
+      s[j][3] = exp2f(s[j][3] - e1);
       sum0 += s[j][0] + s[j][1];
       sum1 += s[j][2] + s[j][3];
     }

@@ -26,7 +26,7 @@ class ModelDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("kind", "D", "Hq", "Hkv", "dh", "F", "L", "S", "T_prefix", "T_q", "act_dim",
                  "n_hist", "t_dim", "patch_dim", "max_batch", "n_streams")] + \
-               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float)]
+               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float), ("prefix_lm", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

@@ -35,6 +35,7 @@ def desc_from_config(cfg: dict, kind: int, max_batch: int = 1, n_streams: int = 
     d.n_streams = n_streams
     d.rope_base = cfg["rope_base"]
     d.eps = cfg["eps"]
+    d.prefix_lm = int(cfg.get("prefix_lm", 0))
     return d
 
 

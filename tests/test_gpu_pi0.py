@@ -50,6 +50,8 @@ def _run_block(name, layer=0, seed=0, **over):
     ("tiny", {"T_q": 2, "T_prefix": 0}, 0),        # degenerate: state + 1 action, no prefix
     ("pi0_ae", {}, 0),
     ("pi0_ae", {}, 17),
+    ("tiny", {"prefix_lm": 1}, 0),                 # block mask: the state token sees prefix + itself
+    ("pi0_ae", {"prefix_lm": 1}, 0),
 ])
 def test_block_parity(name, over, layer):
     cfg, got_x, ref_x, got_kv, kv_in, k_own, v_own, Tp = _run_block(name, layer, **over)
@@ -60,7 +62,7 @@ def test_block_parity(name, over, layer):
 
 
 @pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"T_q": 33, "T_prefix": 70, "S": 3}),
-                                       ("pi0_ae", {})])
+                                       ("tiny", {"prefix_lm": 1}), ("pi0_ae", {})])
 def test_denoise_parity(name, over):
     cfg, wb, m = _model(name, **over)
     ib = synth.pi0_inputs(cfg, 1)
@@ -177,3 +179,40 @@ def _oracle_denoise_with_grid(ib, wb, cfg, t):
             kv[l, 1, Tp:] = v_own
         x = x + (t[s + 1] - t[s]) * pi0.head(h[1:], W, cfg["eps"])
     return x
+
+
+def test_two_streams_stale_cache():
+    """The two-stream scheme of the reading note: the prefix model fills the next
+    cache on one stream while the action expert denoises from the previous cache
+    on another.  The actions match the oracle on the cache they read, and the
+    new cache matches a prefill run alone (the prefill path is deterministic)."""
+    from latency_transformer_block_gb300.models import Pi0Prefix
+    ca = synth.config("tiny", Hq=2, Hkv=1, dh=256, L=2)
+    cp = synth.config("prefill", D=256, Hq=2, Hkv=1, dh=256, F=512, L=2, T_prefix=ca["T_prefix"],
+                      T_q=ca["T_q"], patch_dim=64)
+    wa = synth.pi0_weights(ca, 4)
+    pre = Pi0Prefix(cp, synth.prefill_weights(cp, 4), max_batch=1)
+    ae = Pi0ActionExpert(ca, wa)
+    pe0 = _dev_pe(synth.prefill_inputs(cp, 1, 5)["patch_emb"])
+    pe1 = _dev_pe(synth.prefill_inputs(cp, 1, 6)["patch_emb"])
+    kv0, kv1, kv1_alone = pre.new_kv(1), pre.new_kv(1), pre.new_kv(1)
+    pre.prefill(pe0, kv0)
+    pre.prefill(pe1, kv1_alone)
+    torch.cuda.synchronize()
+    ib = synth.pi0_inputs(ca, 4)
+    kv0_bits = bits_of(kv0)[:, 0]
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    state = torch.from_numpy(ib["state"]).cuda()
+    x = torch.from_numpy(ib["noise"]).cuda()
+    pre.prefill(pe1, kv1, sa)                       # next observation, stream A
+    ae.denoise(kv0[:, 0], state, x, sb)             # actions from the previous cache, stream B
+    torch.cuda.synchronize()
+    ae.ctx.sync()
+    pre.ctx.sync()
+    assert np.array_equal(bits_of(kv1), bits_of(kv1_alone))
+    ref, _ = pi0.denoise(ib["noise"], ib["state"], kv0_bits, wa, ca)
+    assert_rel(x.cpu().numpy(), ref, FINAL_TOL, "two-stream actions")
+
+
+def _dev_pe(bits):
+    return torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
