@@ -30,6 +30,11 @@ __device__ __forceinline__ void record_error(DevErr* e, unsigned code, unsigned 
 // this path normally completes in microseconds.
 constexpr long long kSpinBudget = 1000000000LL;
 
+// p[0..3] += (a, b, c, d): one vector reduction at L2 (p 16-byte aligned)
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -49,6 +49,8 @@ struct DenseArgs {
   float out_scale;       // acc *= out_scale before the epilogue (2^-s of weights held as 2^s W)
   int w_row0;            // first weight row of this matrix in the stacked tensor
   int epi;
+  int ksplit;            // K ranges per output tile (> 1 only for E_RESID / E_RESID_GATE: each
+                         // range adds its partial product into out with vector reductions)
   float* out;            // fp32 [M][ldo] (E_STORE / E_RESID / E_RESID_GATE)
   int ldo;
   const float* bias;     // E_STORE: fp32 [N] or null
@@ -122,7 +124,7 @@ __device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st
     for (int u = 0; u < 2; ++u) {
       const int row = row0 + i0 + 4 * u + rsub;
       x[u] = g[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (row < a.M && (a.epi == E_RESID || a.epi == E_RESID_GATE))
+      if (row < a.M && (a.epi == E_RESID || a.epi == E_RESID_GATE) && a.ksplit == 1)
         x[u] = *reinterpret_cast<const float4*>(a.out + (size_t)row * a.ldo + col);
       if (row < a.M && a.epi == E_RESID_GATE)
         g[u] = *reinterpret_cast<const float4*>(a.gate + a.gate_off[row / a.rows_per_chunk] + col);
@@ -142,6 +144,13 @@ __device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st
         __half* hp = a.act2 + (size_t)row * kActTerms * a.ldh + col;
         *reinterpret_cast<uint2*>(hp) = hv;
         *reinterpret_cast<uint2*>(hp + a.ldh) = lv;
+        continue;
+      }
+      if (a.ksplit > 1) {   // one K range of several: add the partial product
+        if (a.epi == E_RESID_GATE) {
+          r.x *= g[u].x; r.y *= g[u].y; r.z *= g[u].z; r.w *= g[u].w;
+        }
+        red_add_v4(a.out + (size_t)row * a.ldo + col, r.x, r.y, r.z, r.w);
         continue;
       }
       if (a.epi == E_STORE) {
@@ -201,11 +210,16 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = a.N / 256, m_tiles = (a.M + 127) / 128;
-  const int tiles = m_tiles * n_tiles;
+  const int n_tiles = a.N / 256, m_tiles = (a.M + 127) / 128, mn = m_tiles * n_tiles;
+  const int tiles = mn * a.ksplit;                            // tile t: K range t / mn of output tile t % mn
   const int nkb = a.K / 64;                                   // K-blocks of one plane
   const int chunk_kb = kChunkMMA / (4 * a.terms);             // K-blocks per accumulation chunk
-  const int nchunk = (nkb + chunk_kb - 1) / chunk_kb;
+  // K-blocks [kb0, kb1) of tile t and their accumulation chunks
+  auto krange = [&](int t, int& kb0, int& kb1) {
+    const int ks = t / mn;
+    kb0 = ks * nkb / a.ksplit;
+    kb1 = (ks + 1) * nkb / a.ksplit;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -241,8 +255,10 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         int tm, tn;
-        dense_tile(tile, m_tiles, n_tiles, tm, tn);
-        for (int i = 0; i < nkb; ++i, ++it) {
+        dense_tile(tile % mn, m_tiles, n_tiles, tm, tn);
+        int kb0, kb1;
+        krange(tile, kb0, kb1);
+        for (int i = kb0; i < kb1; ++i, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, a.err, 20)) { ok = false; break; }
@@ -262,13 +278,16 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
       bool ok = true;
       uint32_t it = 0, gch = 0;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        int kb0, kb1;
+        krange(tile, kb0, kb1);
+        const int nchunk = (kb1 - kb0 + chunk_kb - 1) / chunk_kb;
         for (int ch = 0; ch < nchunk && ok; ++ch, ++gch) {
           const int buf = gch & 1;
           // the epilogue has drained this accumulator (use gch - 2)
           if (!mbar_wait(&acc_empty[buf], ((gch >> 1) & 1) ^ 1, a.err, 24)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + (uint32_t)(buf * 256);
-          const int i0 = ch * chunk_kb, i1 = min(nkb, i0 + chunk_kb);
+          const int i0 = kb0 + ch * chunk_kb, i1 = min(kb1, i0 + chunk_kb);
           for (int i = i0; i < i1; ++i, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
@@ -297,7 +316,10 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       int tm, tn;
-      dense_tile(tile, m_tiles, n_tiles, tm, tn);
+      dense_tile(tile % mn, m_tiles, n_tiles, tm, tn);
+      int kb0, kb1;
+      krange(tile, kb0, kb1);
+      const int nchunk = (kb1 - kb0 + chunk_kb - 1) / chunk_kb;
       const int row0 = tm * 128 + quad * 32;
       float acc[128];
 #pragma unroll

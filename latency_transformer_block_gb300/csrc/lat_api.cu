@@ -717,7 +717,14 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
   a.f16 = wsel != W_PATCH;
   a.out_scale = wsel != W_PATCH ? c->wscale[wsel] : 1.f;
   if (a.N % 256 || a.K % 64 || a.terms < 1 || a.terms > kActTerms) return fail(LAT_ERR_SHAPE, "dense GEMM shape");
-  const int tiles = ((a.M + 127) / 128) * (a.N / 256);
+  const int mn = ((a.M + 127) / 128) * (a.N / 256);
+  // fewer output tiles than SMs (few tokens, narrow output): split K so that
+  // every SM gets work, keeping at least 8 K-blocks per range; only the
+  // residual epilogues, which add their product into x, can take partial sums
+  a.ksplit = 1;
+  if ((a.epi == E_RESID || a.epi == E_RESID_GATE) && mn < c->num_sms)
+    a.ksplit = std::max(1, std::min(c->num_sms / mn, (a.K / 64) / 8));
+  const int tiles = mn * a.ksplit;
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
   dense_gemm_kernel<kDStages, kActTerms>
       <<<grid, kDThreads, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel], a);

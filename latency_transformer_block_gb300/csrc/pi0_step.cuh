@@ -182,10 +182,7 @@ __device__ __forceinline__ void mk_zero_f4(float* p, int n4, int mt) {
   for (int i = blockIdx.x * 256 + mt; i < n4; i += gridDim.x * 256) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
 }
 
-// p[0..3] += (a, b, c, d): one vector reduction at L2 (p 16-byte aligned)
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
+
 
 // 8 fp32 values (registers) -> 8 bf16 hi and 8 bf16 lo (two-term split)
 __device__ __forceinline__ void split8_regs(const float (&v)[8], uint4& hi, uint4& lo) {

