@@ -398,13 +398,14 @@ constexpr int kMaxSeg = 5;
 struct AttnSeg {
   const __nv_bfloat16* k;    // bf16 keys (cache; tensor-core kernel: their fp16 copy kh / vh), or
   const __nv_bfloat16* v;
-  const float* k32;          // fp32 keys as computed (own chunk): split into hi + lo, or
-  const float* v32;
+  const __nv_bfloat16* kb2;  // keys as computed (own tokens) as two bf16 planes (hi, then lo
+  const __nv_bfloat16* vb2;  //   lo_off elements later; rows of kv_ld), or
   int n;
   const __half* k16;         // the same as two fp16 planes per key row (hi at column c,
   const __half* v16;         // lo at kv_ld + c; row stride 4 kv_ld): tensor-core kernel
   const __half* kh;          // cached keys / values converted to fp16 (rows of kv_ld),
   const __half* vh;          //   read by the tensor-core kernel
+  long long lo_off;          // kb2 / vb2: elements from the hi plane to the lo plane
 };
 
 struct SegGroup {
@@ -475,7 +476,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
 
   for (int si = 0; si < G.nseg; ++si) {
     const AttnSeg sg = G.seg[si];
-    const bool f32 = sg.k32 != nullptr;
+    const bool f32 = sg.kb2 != nullptr;   // own keys: hi and lo planes
     const int nkb = (sg.n + KB - 1) / KB;
     for (int kb = 0; kb < nkb; ++kb) {
       __syncthreads();
@@ -484,17 +485,11 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
         const int key = kb * KB + row;
         const bool in = key < sg.n;
         const size_t o = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
-        if (f32) {
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          uint4 kk = z, vv = z, kl = z, vl = z;
-          if (in) {
-            split8_to(sg.k32 + o, kk, kl);
-            split8_to(sg.v32 + o, vv, vl);
-          }
-          *reinterpret_cast<uint4*>(sK + row * LD + c8 * 8) = kk;
-          *reinterpret_cast<uint4*>(sV + row * LD + c8 * 8) = vv;
-          *reinterpret_cast<uint4*>(sK + KB * LD + row * LD + c8 * 8) = kl;
-          *reinterpret_cast<uint4*>(sV + KB * LD + row * LD + c8 * 8) = vl;
+        if (f32) {   // own keys: both planes by async copies (zero fill past the segment)
+          cp_async16(sK + row * LD + c8 * 8, sg.kb2 + o, in ? 16 : 0);
+          cp_async16(sV + row * LD + c8 * 8, sg.vb2 + o, in ? 16 : 0);
+          cp_async16(sK + KB * LD + row * LD + c8 * 8, sg.kb2 + sg.lo_off + o, in ? 16 : 0);
+          cp_async16(sV + KB * LD + row * LD + c8 * 8, sg.vb2 + sg.lo_off + o, in ? 16 : 0);
         } else {   // cache keys: async copies (zero fill past the segment)
           cp_async16(sK + row * LD + c8 * 8, sg.k + o, in ? 16 : 0);
           cp_async16(sV + row * LD + c8 * 8, sg.v + o, in ? 16 : 0);

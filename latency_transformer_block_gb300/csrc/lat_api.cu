@@ -163,7 +163,7 @@ struct lat_ctx {
         *qbuf = nullptr;
   float* adaln_tmp = nullptr;   // scratch of the adaLN table build: [S][t_dim], [S][D], [S][D]
   double* theta = nullptr;
-  float *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed (fp32; prefix prefill)
+  bf16 *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two bf16 planes [2][m_max][kvd] (prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
   __half* hist16 = nullptr;    // fp16 copy of one call's history K/V planes, [planes][T_q][D] (DiT)
   int hist_rows = 0;
@@ -324,6 +324,7 @@ static lat_status check_desc(const lat_model_desc* d) {
     return LAT_OK;
   }
   if (d->Hq != d->Hkv || d->Hq * d->dh != d->D) return fail(LAT_ERR_SHAPE, "DiT: Hq == Hkv and Hq dh == D");
+  if (d->dh != 128) return fail(LAT_ERR_SHAPE, "DiT: dh must be 128 (tensor-core attention)");
   if (d->F % 256) return fail(LAT_ERR_SHAPE, "F must be a multiple of 256");
   if (d->S <= 0 || d->T_q < 1 || d->n_hist < 0 || d->n_streams < 1 || d->t_dim <= 0 || d->t_dim % 2)
     return fail(LAT_ERR_SHAPE, "DiT: S, T_q, n_streams, t_dim must be positive (t_dim even), n_hist >= 0");
@@ -776,8 +777,8 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
     LAT_TRY(c->alloc(&c->hist16, (size_t)c->hist_rows * d.D));
     CUDA_TRY(cudaMemset(c->hist16, 0, (size_t)c->hist_rows * d.D * 2));   // rows never written stay finite
   } else {
-    LAT_TRY(c->alloc(&c->kown, (size_t)c->m_max * d.Hkv * d.dh));
-    LAT_TRY(c->alloc(&c->vown, (size_t)c->m_max * d.Hkv * d.dh));
+    LAT_TRY(c->alloc(&c->kown, (size_t)2 * c->m_max * d.Hkv * d.dh));
+    LAT_TRY(c->alloc(&c->vown, (size_t)2 * c->m_max * d.Hkv * d.dh));
   }
   LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, terms * d.D));
   LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, terms * qd));
@@ -993,7 +994,8 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     RopeKvArgs ra{};
     ra.qkv = c->qkvbuf; ra.ld_qkv = last ? 2 * kvd : c->nqkv; ra.q_cols = last ? 0 : qd; ra.kv_cols = kvd;
     ra.dh = d.dh; ra.T = T; ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta;
-    ra.q_out = c->qbuf; ra.kv_ld = kvd; ra.k32 = c->kown; ra.v32 = c->vown;
+    ra.q_out = c->qbuf; ra.kv_ld = kvd; ra.kb2 = c->kown; ra.vb2 = c->vown;
+    ra.lo_off = (long long)c->m_max * kvd;
     SegAttnArgs sa{};
     for (int b = 0; b < B; ++b) {
       bf16* kb = kv + (((size_t)l * B + b) * 2 + 0) * T_kv * kvd;
@@ -1001,7 +1003,9 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
       ra.kdst[b] = kb;
       ra.vdst[b] = kb + (size_t)T_kv * kvd;
       sa.grp[b].nseg = 1;   // the prefix tokens attend to their own K/V as computed
-      sa.grp[b].seg[0] = AttnSeg{nullptr, nullptr, c->kown + (size_t)b * T * kvd, c->vown + (size_t)b * T * kvd, T};
+      AttnSeg sg{nullptr, nullptr, c->kown + (size_t)b * T * kvd, c->vown + (size_t)b * T * kvd, T};
+      sg.lo_off = (long long)c->m_max * kvd;
+      sa.grp[b].seg[0] = sg;
     }
     rope_kv_kernel<<<M, 128, 0, st>>>(ra);
     LAT_TRY(launch_check("rope_kv"));
