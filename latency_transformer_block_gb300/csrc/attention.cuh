@@ -398,8 +398,8 @@ constexpr int kMaxSeg = 5;
 struct AttnSeg {
   const __nv_bfloat16* k;    // bf16 keys (cache; tensor-core kernel: their fp16 copy kh / vh), or
   const __nv_bfloat16* v;
-  const __nv_bfloat16* kb2;  // keys as computed (own tokens) as two bf16 planes (hi, then lo
-  const __nv_bfloat16* vb2;  //   lo_off elements later; rows of kv_ld), or
+  const __half* kb2;         // keys as computed (own tokens) as two fp16 planes (hi, then lo
+  const __half* vb2;         //   lo_off elements later; rows of kv_ld), or
   int n;
   const __half* k16;         // the same as two fp16 planes per key row (hi at column c,
   const __half* v16;         // lo at kv_ld + c; row stride 4 kv_ld): tensor-core kernel
@@ -428,14 +428,32 @@ struct SegAttnArgs {
   SegGroup grp[16];
 };
 
-template <int DH, int TERMS>
+// fp16 operands, fp32 accumulation
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Attention of the prefix tokens over their own K/V (prefix prefill; the
+// segments of a group must be own-key segments, kb2 / vb2 set), warp MMA
+// m16n8k16 with fp16 operands and fp32 accumulation.  Operands as two fp16
+// terms: q and P (hi = fp16(x), lo = fp16(x - hi)) and the own K / V as the
+// two fp16 planes the RoPE kernel wrote:
+//   S = q_hi K_hi + q_lo K_hi + q_hi K_lo,   O = P_hi V_hi + P_lo V_hi + P_hi V_lo
+// (the dropped lo x lo products are below 2^-22 of the kept ones).  One CTA =
+// one (head, 64-row query tile, group), 4 warps of 16 rows; keys in blocks of
+// 64, both planes of K and V by async copies.
+template <int DH>
 static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_constant__ SegAttnArgs a) {
   constexpr int KB = 64;
   constexpr int LD = DH + 8;
   constexpr int NT = DH / 8;
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(smem_raw);   // [2 planes][KB][LD]
-  __nv_bfloat16* sV = sK + 2 * KB * LD;
+  __half* sK = reinterpret_cast<__half*>(smem_raw);   // [2 planes][KB][LD]
+  __half* sV = sK + 2 * KB * LD;
   const uint32_t LO = (uint32_t)(KB * LD * 2);
   const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -447,26 +465,18 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   const float* q0 = a.q + row0 * a.q_ld + h * DH;
   const float* q1 = a.q + row1 * a.q_ld + h * DH;
 
-  // Q fragments as exact three-term splits: for dh <= 128 split once into
-  // registers [k-step][term][4]; for larger dh re-read per k-step
-  constexpr bool QREG = DH <= 128;
-  constexpr int KSQ = QREG ? DH / 16 : 1;
-  uint32_t qf[KSQ][3][4];
-  auto q_frag = [&](int ks, uint32_t (&af)[3][4]) {
+  // q fragments of k-step ks as two fp16 terms [term][4]
+  auto q_frag = [&](int ks, uint32_t (&af)[2][4]) {
     const int c = ks * 16 + 2 * tq;
     const float2 x00 = v0 ? *reinterpret_cast<const float2*>(q0 + c) : make_float2(0.f, 0.f);
     const float2 x10 = v1 ? *reinterpret_cast<const float2*>(q1 + c) : make_float2(0.f, 0.f);
     const float2 x01 = v0 ? *reinterpret_cast<const float2*>(q0 + c + 8) : make_float2(0.f, 0.f);
     const float2 x11 = v1 ? *reinterpret_cast<const float2*>(q1 + c + 8) : make_float2(0.f, 0.f);
-    split_pair_exact(x00.x, x00.y, af[0][0], af[1][0], af[2][0]);
-    split_pair_exact(x10.x, x10.y, af[0][1], af[1][1], af[2][1]);
-    split_pair_exact(x01.x, x01.y, af[0][2], af[1][2], af[2][2]);
-    split_pair_exact(x11.x, x11.y, af[0][3], af[1][3], af[2][3]);
+    split_pair_h2(x00.x, x00.y, af[0][0], af[1][0]);
+    split_pair_h2(x10.x, x10.y, af[0][1], af[1][1]);
+    split_pair_h2(x01.x, x01.y, af[0][2], af[1][2]);
+    split_pair_h2(x11.x, x11.y, af[0][3], af[1][3]);
   };
-  if constexpr (QREG) {
-#pragma unroll
-    for (int ks = 0; ks < KSQ; ++ks) q_frag(ks, qf[ks]);
-  }
   float o[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -476,7 +486,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
 
   for (int si = 0; si < G.nseg; ++si) {
     const AttnSeg sg = G.seg[si];
-    const bool f32 = sg.kb2 != nullptr;   // own keys: hi and lo planes
+    if (!sg.kb2) continue;   // own-key segments only (the host passes nothing else)
     const int nkb = (sg.n + KB - 1) / KB;
     for (int kb = 0; kb < nkb; ++kb) {
       __syncthreads();
@@ -485,26 +495,20 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
         const int key = kb * KB + row;
         const bool in = key < sg.n;
         const size_t o = (size_t)(in ? key : 0) * a.kv_ld + kvh * DH + c8 * 8;
-        if (f32) {   // own keys: both planes by async copies (zero fill past the segment)
-          cp_async16(sK + row * LD + c8 * 8, sg.kb2 + o, in ? 16 : 0);
-          cp_async16(sV + row * LD + c8 * 8, sg.vb2 + o, in ? 16 : 0);
-          cp_async16(sK + KB * LD + row * LD + c8 * 8, sg.kb2 + sg.lo_off + o, in ? 16 : 0);
-          cp_async16(sV + KB * LD + row * LD + c8 * 8, sg.vb2 + sg.lo_off + o, in ? 16 : 0);
-        } else {   // cache keys: async copies (zero fill past the segment)
-          cp_async16(sK + row * LD + c8 * 8, sg.k + o, in ? 16 : 0);
-          cp_async16(sV + row * LD + c8 * 8, sg.v + o, in ? 16 : 0);
-        }
+        cp_async16(sK + row * LD + c8 * 8, sg.kb2 + o, in ? 16 : 0);
+        cp_async16(sV + row * LD + c8 * 8, sg.vb2 + o, in ? 16 : 0);
+        cp_async16(sK + KB * LD + row * LD + c8 * 8, sg.kb2 + sg.lo_off + o, in ? 16 : 0);
+        cp_async16(sV + KB * LD + row * LD + c8 * 8, sg.vb2 + sg.lo_off + o, in ? 16 : 0);
       }
       cp_async_wait_all();
       __syncthreads();
       float s[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
+#pragma unroll 4
       for (int ks = 0; ks < DH / 16; ++ks) {
-        uint32_t afl[3][4];
-        if constexpr (!QREG) q_frag(ks, afl);
-        const uint32_t (&af)[3][4] = QREG ? qf[QREG ? ks : 0] : afl;
+        uint32_t af[2][4];
+        q_frag(ks, af);
 #pragma unroll
         for (int jp = 0; jp < 4; ++jp) {
           const int mi = lane >> 3, rr = lane & 7;
@@ -513,18 +517,13 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
           uint32_t b0, b1, b2, b3;
           ldsm_x4(sKa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
 #pragma unroll
-          for (int t = 0; t < TERMS; ++t) {
-            mma_16816(s[2 * jp], af[t], b0, b1);
-            mma_16816(s[2 * jp + 1], af[t], b2, b3);
+          for (int t = 0; t < 2; ++t) {
+            mma_16816_f16(s[2 * jp], af[t], b0, b1);
+            mma_16816_f16(s[2 * jp + 1], af[t], b2, b3);
           }
-          if (f32) {
-            ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-#pragma unroll
-            for (int t = 0; t < TERMS - 1; ++t) {
-              mma_16816(s[2 * jp], af[t], b0, b1);
-              mma_16816(s[2 * jp + 1], af[t], b2, b3);
-            }
-          }
+          ldsm_x4(sKa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+          mma_16816_f16(s[2 * jp], af[0], b0, b1);
+          mma_16816_f16(s[2 * jp + 1], af[0], b2, b3);
         }
       }
       float mx0 = m0, mx1 = m1;
@@ -570,11 +569,11 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pf[3][4];
-        split_pair_exact(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0], pf[2][0]);
-        split_pair_exact(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1], pf[2][1]);
-        split_pair_exact(s[2 * kk + 1][0], s[2 * kk + 1][1], pf[0][2], pf[1][2], pf[2][2]);
-        split_pair_exact(s[2 * kk + 1][2], s[2 * kk + 1][3], pf[0][3], pf[1][3], pf[2][3]);
+        uint32_t pf[2][4];
+        split_pair_h2(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0]);
+        split_pair_h2(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1]);
+        split_pair_h2(s[2 * kk + 1][0], s[2 * kk + 1][1], pf[0][2], pf[1][2]);
+        split_pair_h2(s[2 * kk + 1][2], s[2 * kk + 1][3], pf[0][3], pf[1][3]);
 #pragma unroll
         for (int jp = 0; jp < NT / 2; ++jp) {
           const int mi = lane >> 3, rr = lane & 7;
@@ -583,18 +582,13 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(sVa + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
 #pragma unroll
-          for (int t = 0; t < TERMS; ++t) {
-            mma_16816(o[2 * jp], pf[t], b0, b1);
-            mma_16816(o[2 * jp + 1], pf[t], b2, b3);
+          for (int t = 0; t < 2; ++t) {
+            mma_16816_f16(o[2 * jp], pf[t], b0, b1);
+            mma_16816_f16(o[2 * jp + 1], pf[t], b2, b3);
           }
-          if (f32) {
-            ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
-#pragma unroll
-            for (int t = 0; t < TERMS - 1; ++t) {
-              mma_16816(o[2 * jp], pf[t], b0, b1);
-              mma_16816(o[2 * jp + 1], pf[t], b2, b3);
-            }
-          }
+          ldsm_x4_t(sVa + LO + (uint32_t)(key * LD + col) * 2u, b0, b1, b2, b3);
+          mma_16816_f16(o[2 * jp], pf[0], b0, b1);
+          mma_16816_f16(o[2 * jp + 1], pf[0], b2, b3);
         }
       }
     }
@@ -630,7 +624,7 @@ static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2 + 64 * 
 static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
 static inline cudaError_t set_attention_smem_limits() {
-  cudaFuncSetAttribute(attention_seg_kernel<256, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
+  cudaFuncSetAttribute(attention_seg_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
   cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(64));
   cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(128));
   cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(256));

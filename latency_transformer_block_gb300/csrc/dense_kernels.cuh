@@ -134,8 +134,8 @@ struct RopeKvArgs {
   __nv_bfloat16* kdst[kMaxChunks];
   __nv_bfloat16* vdst[kMaxChunks];
   int kv_ld;                // row stride of kdst / vdst (elements)
-  __nv_bfloat16* kb2;       // K (after RoPE) and V as computed, as two bf16 planes
-  __nv_bfloat16* vb2;       //   [M][kv_cols] (hi), then lo lo_off elements later, or
+  __half* kb2;              // K (after RoPE) and V as computed, as two fp16 planes
+  __half* vb2;              //   [M][kv_cols] (hi), then lo lo_off elements later, or
   long long lo_off;
   __half* k16;              // the same as two fp16 planes (hi at column c, lo at kv_cols + c)
   __half* v16;              // of rows ld16 apart
@@ -207,14 +207,14 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
         *reinterpret_cast<uint2*>(k16 + a.kv_cols + half) =
             pack_half4(y1[0] - b0.x, y1[1] - b0.y, y1[2] - b1.x, y1[3] - b1.y);
       } else {
-        __nv_bfloat16* kp = a.kb2 + (size_t)m * a.kv_cols + (col - a.q_cols);
+        __half* kp = a.kb2 + (size_t)m * a.kv_cols + (col - a.q_cols);
         uint2 h, l;
-        split_pair2(y0[0], y0[1], h.x, l.x);
-        split_pair2(y0[2], y0[3], h.y, l.y);
+        split_pair_h2(y0[0], y0[1], h.x, l.x);
+        split_pair_h2(y0[2], y0[3], h.y, l.y);
         *reinterpret_cast<uint2*>(kp) = h;
         *reinterpret_cast<uint2*>(kp + a.lo_off) = l;
-        split_pair2(y1[0], y1[1], h.x, l.x);
-        split_pair2(y1[2], y1[3], h.y, l.y);
+        split_pair_h2(y1[0], y1[1], h.x, l.x);
+        split_pair_h2(y1[2], y1[3], h.y, l.y);
         *reinterpret_cast<uint2*>(kp + half) = h;
         *reinterpret_cast<uint2*>(kp + half + a.lo_off) = l;
       }
@@ -233,10 +233,10 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
       *reinterpret_cast<uint2*>(v16) = h;
       *reinterpret_cast<uint2*>(v16 + a.kv_cols) = pack_half4(y[0] - f0.x, y[1] - f0.y, y[2] - f1.x, y[3] - f1.y);
     } else {
-      __nv_bfloat16* vp = a.vb2 + (size_t)m * a.kv_cols + c;
+      __half* vp = a.vb2 + (size_t)m * a.kv_cols + c;
       uint2 h, l;
-      split_pair2(y[0], y[1], h.x, l.x);
-      split_pair2(y[2], y[3], h.y, l.y);
+      split_pair_h2(y[0], y[1], h.x, l.x);
+      split_pair_h2(y[2], y[3], h.y, l.y);
       *reinterpret_cast<uint2*>(vp) = h;
       *reinterpret_cast<uint2*>(vp + a.lo_off) = l;
     }

@@ -163,7 +163,7 @@ struct lat_ctx {
         *qbuf = nullptr;
   float* adaln_tmp = nullptr;   // scratch of the adaLN table build: [S][t_dim], [S][D], [S][D]
   double* theta = nullptr;
-  bf16 *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two bf16 planes [2][m_max][kvd] (prefill)
+  __half *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two fp16 planes [2][m_max][kvd] (prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
   __half* hist16 = nullptr;    // fp16 copy of one call's history K/V planes, [planes][T_q][D] (DiT)
   int hist_rows = 0;
@@ -962,7 +962,7 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
   }
   if (dh != 256) return fail(LAT_ERR_SHAPE, "dense-path attention: dh 128 or 256");
   dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups);
-  attention_seg_kernel<256, 3><<<grid, 128, attn_smem_bytes(dh), st>>>(a);
+  attention_seg_kernel<256><<<grid, 128, attn_smem_bytes(dh), st>>>(a);
   return launch_check("attention_seg");
 }
 
