@@ -425,6 +425,12 @@ struct SegAttnArgs {
   const __half* hist16;      // tensor-core kernel: base of the fp16 history copy (kh / vh are rows of it),
   int hist_rows;             //   its rows,
   const __half* own16;       //   and the base of the own fp16 planes
+  // prefix attention with kv_split > 1 key ranges per (head, query tile, group):
+  // blockIdx.z = group * kv_split + range; each range leaves its unnormalised
+  // output and row (max, sum) in part_o [z][Hq][T_rows][dh] / part_ml [z][Hq][T_rows][2]
+  int kv_split;
+  float* part_o;
+  float* part_ml;
   SegGroup grp[16];
 };
 
@@ -455,7 +461,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   __half* sK = reinterpret_cast<__half*>(smem_raw);   // [2 planes][KB][LD]
   __half* sV = sK + 2 * KB * LD;
   const uint32_t LO = (uint32_t)(KB * LD * 2);
-  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z / a.kv_split, kr = blockIdx.z % a.kv_split;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int kvh = h / (a.Hq / a.Hkv);
@@ -488,7 +494,8 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
     const AttnSeg sg = G.seg[si];
     if (!sg.kb2) continue;   // own-key segments only (the host passes nothing else)
     const int nkb = (sg.n + KB - 1) / KB;
-    for (int kb = 0; kb < nkb; ++kb) {
+    // this CTA's key blocks: range kr of kv_split
+    for (int kb = kr * nkb / a.kv_split; kb < (kr + 1) * nkb / a.kv_split; ++kb) {
       __syncthreads();
       for (int idx = threadIdx.x; idx < KB * (DH / 8); idx += 128) {
         const int row = idx / (DH / 8), c8 = idx % (DH / 8);
@@ -593,6 +600,20 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       }
     }
   }
+  if (a.kv_split > 1) {   // partial of one key range: unnormalised output, row max and sum
+    const size_t base = ((size_t)blockIdx.z * a.Hq + h) * a.T_rows;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int c = j * 8 + 2 * tq;
+      if (v0) *reinterpret_cast<float2*>(a.part_o + (base + rl0) * DH + c) = make_float2(o[j][0], o[j][1]);
+      if (v1) *reinterpret_cast<float2*>(a.part_o + (base + rl1) * DH + c) = make_float2(o[j][2], o[j][3]);
+    }
+    if (tq == 0) {
+      if (v0) *reinterpret_cast<float2*>(a.part_ml + (base + rl0) * 2) = make_float2(m0, l0);
+      if (v1) *reinterpret_cast<float2*>(a.part_ml + (base + rl1) * 2) = make_float2(m1, l1);
+    }
+    return;
+  }
   const float i0 = (l0 > 0.f) ? 1.f / l0 : 0.f, i1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -612,6 +633,32 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       *reinterpret_cast<uint32_t*>(p + a.ldh) = ll;
     }
   }
+}
+
+// Merge of the prefix attention's key ranges: per (row, head) of group b,
+// M = max_r m_r, o = sum_r 2^(m_r - M) O_r / sum_r 2^(m_r - M) l_r, written as
+// the two fp16 planes of the output projection's operand.  Grid (T_rows, Hq,
+// groups), one thread per head dimension.
+static __global__ void attention_seg_combine_kernel(const __grid_constant__ SegAttnArgs a, int dh) {
+  const int row = blockIdx.x, h = blockIdx.y, b = blockIdx.z, c = threadIdx.x;
+  float M = -INFINITY;
+  for (int r = 0; r < a.kv_split; ++r) {
+    const size_t z = (size_t)b * a.kv_split + r;
+    M = fmaxf(M, a.part_ml[((z * a.Hq + h) * a.T_rows + row) * 2]);
+  }
+  float num = 0.f, den = 0.f;
+  for (int r = 0; r < a.kv_split; ++r) {
+    const size_t z = (size_t)b * a.kv_split + r;
+    const size_t i = (z * a.Hq + h) * a.T_rows + row;
+    const float m = a.part_ml[i * 2], w = m == -INFINITY ? 0.f : exp2f(m - M);
+    num += w * a.part_o[i * dh + c];
+    den += w * a.part_ml[i * 2 + 1];
+  }
+  const float v = den > 0.f ? num / den : 0.f;
+  const __half hv = __float2half_rn(v);
+  __half* p = a.out + ((size_t)b * a.T_rows + row) * kActTerms * a.ldh + h * dh + c;
+  p[0] = hv;
+  p[a.ldh] = __float2half_rn(v - __half2float(hv));
 }
 
 // Launch the attention (and the combine when there are several key ranges).

@@ -162,6 +162,9 @@ struct lat_ctx {
   float *bpatch = nullptr, *adaln = nullptr, *cos_j = nullptr, *sin_j = nullptr, *qkvbuf = nullptr,
         *qbuf = nullptr;
   float* adaln_tmp = nullptr;   // scratch of the adaLN table build: [S][t_dim], [S][D], [S][D]
+  // prefix attention split over key ranges: partial outputs and (max, sum), at
+  // most num_sms CTAs x 64 rows
+  float *seg_part_o = nullptr, *seg_part_ml = nullptr;
   double* theta = nullptr;
   __half *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two fp16 planes [2][m_max][kvd] (prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
@@ -779,6 +782,8 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
   } else {
     LAT_TRY(c->alloc(&c->kown, (size_t)2 * c->m_max * d.Hkv * d.dh));
     LAT_TRY(c->alloc(&c->vown, (size_t)2 * c->m_max * d.Hkv * d.dh));
+    LAT_TRY(c->alloc(&c->seg_part_o, (size_t)c->num_sms * 64 * d.dh));
+    LAT_TRY(c->alloc(&c->seg_part_ml, (size_t)c->num_sms * 64 * 2));
   }
   LAT_TRY(make_act_map(&c->map_act_d, c->act2, c->m_max, terms * d.D));
   LAT_TRY(make_act_map(&c->map_act_o, c->act2, c->m_max, terms * qd));
@@ -961,9 +966,26 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
     return launch_check("attention_tc");
   }
   if (dh != 256) return fail(LAT_ERR_SHAPE, "dense-path attention: dh 128 or 256");
-  dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups);
-  attention_seg_kernel<256><<<grid, 128, attn_smem_bytes(dh), st>>>(a);
-  return launch_check("attention_seg");
+  // fewer CTAs than SMs (few groups): split the keys into ranges (at least two
+  // 64-key blocks each), merged by the combine kernel
+  SegAttnArgs b = a;
+  const int ctas = c->d.Hq * ((a.T_rows + 63) / 64) * groups;
+  int nkb_max = 1;
+  for (int g = 0; g < groups; ++g)
+    for (int s = 0; s < a.grp[g].nseg; ++s) nkb_max = std::max(nkb_max, (a.grp[g].seg[s].n + 63) / 64);
+  b.kv_split = 1;
+  if (ctas < c->num_sms && c->seg_part_o)
+    b.kv_split = std::max(1, std::min(std::min(4, c->num_sms / ctas), nkb_max / 2));
+  b.part_o = c->seg_part_o;
+  b.part_ml = c->seg_part_ml;
+  dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups * b.kv_split);
+  attention_seg_kernel<256><<<grid, 128, attn_smem_bytes(dh), st>>>(b);
+  LAT_TRY(launch_check("attention_seg"));
+  if (b.kv_split > 1) {
+    attention_seg_combine_kernel<<<dim3(a.T_rows, c->d.Hq, groups), dh, 0, st>>>(b, dh);
+    LAT_TRY(launch_check("attention_seg_combine"));
+  }
+  return LAT_OK;
 }
 
 static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, cudaStream_t st) {
