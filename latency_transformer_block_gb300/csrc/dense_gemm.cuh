@@ -49,8 +49,9 @@ struct DenseArgs {
   float out_scale;       // acc *= out_scale before the epilogue (2^-s of weights held as 2^s W)
   int w_row0;            // first weight row of this matrix in the stacked tensor
   int epi;
-  int ksplit;            // K ranges per output tile (> 1 only for E_RESID / E_RESID_GATE: each
-                         // range adds its partial product into out with vector reductions)
+  int ksplit;            // K ranges per output tile (> 1 only for E_STORE (out zeroed before, the
+                         // first range adds the bias), E_RESID and E_RESID_GATE: each range adds
+                         // its partial product into out with vector reductions)
   float* out;            // fp32 [M][ldo] (E_STORE / E_RESID / E_RESID_GATE)
   int ldo;
   const float* bias;     // E_STORE: fp32 [N] or null
@@ -112,11 +113,12 @@ __device__ __forceinline__ void stage_put(float4* st, int lane, const float* v, 
 // columns n0 .. n0 + 31 (feature columns of the split planes for the
 // E_*_SPLIT epilogues).  Lane l takes float4 chunk l & 7 of rows 4i + (l >> 3);
 // the loads of 8 rows are issued before their stores.
-__device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st, int row0, int n0, int lane) {
+__device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st, int row0, int n0, int lane,
+                                            bool first_range) {
   const int c = lane & 7, rsub = lane >> 3;
   const int col = n0 + 4 * c;
   float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.epi == E_STORE && a.bias) bias = *reinterpret_cast<const float4*>(a.bias + col);
+  if (a.epi == E_STORE && a.bias && first_range) bias = *reinterpret_cast<const float4*>(a.bias + col);
 #pragma unroll 1
   for (int i0 = 0; i0 < 32; i0 += 8) {
     float4 x[2], g[2];
@@ -149,6 +151,8 @@ __device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st
       if (a.ksplit > 1) {   // one K range of several: add the partial product
         if (a.epi == E_RESID_GATE) {
           r.x *= g[u].x; r.y *= g[u].y; r.z *= g[u].z; r.w *= g[u].w;
+        } else if (a.epi == E_STORE) {
+          r.x += bias.x; r.y += bias.y; r.z += bias.z; r.w += bias.w;
         }
         red_add_v4(a.out + (size_t)row * a.ldo + col, r.x, r.y, r.z, r.w);
         continue;
@@ -172,7 +176,7 @@ __device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st
 // f0 + 63) those features.  The accumulators are scaled by a.out_scale (a
 // power of two: exact) on the way.  All lanes take part.
 __device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[128], int row0, int n0, int f0,
-                                               float4* st, int lane) {
+                                               float4* st, int lane, bool first_range) {
   if (a.epi == E_GEGLU_SPLIT) {
 #pragma unroll
     for (int j = 0; j < 64; ++j) acc[j] = gelu_tanh(acc[j] * a.out_scale) * (acc[64 + j] * a.out_scale);
@@ -180,7 +184,7 @@ __device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[
     for (int q = 0; q < 2; ++q) {
       stage_put(st, lane, acc + 32 * q, 1.f);
       __syncwarp();
-      epi_quarter(a, st, row0, f0 + 32 * q, lane);
+      epi_quarter(a, st, row0, f0 + 32 * q, lane, true);
       __syncwarp();
     }
     return;
@@ -189,7 +193,7 @@ __device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[
   for (int q = 0; q < 4; ++q) {
     stage_put(st, lane, acc + 32 * q, a.out_scale);
     __syncwarp();
-    epi_quarter(a, st, row0, n0 + 32 * q, lane);
+    epi_quarter(a, st, row0, n0 + 32 * q, lane, first_range);
     __syncwarp();
   }
 }
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
-      if (ok) dense_epilogue(a, acc, row0, tn * 256 + hc * 128, tn * 128 + hc * 64, st, lane);
+      if (ok) dense_epilogue(a, acc, row0, tn * 256 + hc * 128, tn * 128 + hc * 64, st, lane, tile < mn);
     }
   }
   tc_fence_before();

@@ -723,11 +723,14 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
   if (a.N % 256 || a.K % 64 || a.terms < 1 || a.terms > kActTerms) return fail(LAT_ERR_SHAPE, "dense GEMM shape");
   const int mn = ((a.M + 127) / 128) * (a.N / 256);
   // fewer output tiles than SMs (few tokens, narrow output): split K so that
-  // every SM gets work, keeping at least 8 K-blocks per range; only the
-  // residual epilogues, which add their product into x, can take partial sums
+  // every SM gets work, keeping at least 8 K-blocks per range; only the linear
+  // epilogues can take partial sums (residual ones add into x, a plain store
+  // adds into a zeroed output)
   a.ksplit = 1;
-  if ((a.epi == E_RESID || a.epi == E_RESID_GATE) && mn < c->num_sms)
+  if ((a.epi == E_RESID || a.epi == E_RESID_GATE || a.epi == E_STORE) && mn < c->num_sms)
     a.ksplit = std::max(1, std::min(c->num_sms / mn, (a.K / 64) / 8));
+  if (a.ksplit > 1 && a.epi == E_STORE)
+    CUDA_TRY(cudaMemsetAsync(a.out, 0, (size_t)a.M * a.ldo * sizeof(float), st));
   const int tiles = mn * a.ksplit;
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
   dense_gemm_kernel<kDStages, kActTerms>
