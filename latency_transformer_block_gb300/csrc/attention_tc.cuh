@@ -105,6 +105,63 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 32 lanes x 32 bit, 64 consecutive columns per thread in one instruction,
+// then wait for the load.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bit, 64 consecutive columns per thread in one instruction,
+// then wait for the store.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
+      "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+      "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :
+      : "r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]),
+        "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]),
+        "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]),
+        "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]),
+        "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+      : "memory");
+}
+
+// 2^x by the special-function unit (ex2.approx; results below 2^-126 flush to
+// zero).  The softmax weights it produces lie in [0, 1], where a flushed value
+// is negligible against the row sum.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 8 bf16 (one uint4) -> 8 fp16
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   auto cv = [](uint32_t w) {
@@ -435,13 +492,10 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       const int bf = jb & 1;
       tc_wait(&o_full[bf], (uint32_t)(jb >> 1) & 1u, err, 68);
       tc_fence_after();
+      float t[64];
+      tmem_ld64(trow + 256u + (uint32_t)(bf * 128 + half * 64), t);
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        float t[32];
-        tmem_ld32(trow + 256u + (uint32_t)(bf * 128 + half * 64 + c2 * 32), t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = o[c2 * 32 + i] * alpha_prev + t[i];
-      }
+      for (int i = 0; i < 64; ++i) o[i] = o[i] * alpha_prev + t[i];
       tc_fence_before();
       mbar_arrive(&o_free[bf]);
     };
@@ -456,42 +510,52 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       if (st == 0) tc_mark(a.trace, 1, j, 0);
       tc_fence_after();
       const uint32_t sb = trow + (uint32_t)(bf * 128 + k0);   // S (then P) columns of my keys
-      float s[2][32];
-      tmem_ld32(sb, s[0]);
-      if (!own) tmem_ld32(sb + 32u, s[1]);
+      // raw scores of my keys (an own block has 32 per half: one 32-column load)
+      float s[64];
+      if (own) {
+        float t[32];
+        tmem_ld32(sb, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = t[i];
+      } else {
+        tmem_ld64(sb, s);
+      }
       float mloc = -INFINITY;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + ch * 32 + i;
-          s[ch][i] = (ch * 32 + i < nh && key < nv) ? s[ch][i] * a.scale_log2 : -INFINITY;
-          mloc = fmaxf(mloc, s[ch][i]);
-        }
+      for (int i = 0; i < 64; ++i) {
+        s[i] = (i < nh && k0 + i < nv) ? s[i] : -INFINITY;
+        mloc = fmaxf(mloc, s[i]);
+      }
+      mloc *= a.scale_log2;   // the scale is positive: the maximum commutes with it
       float* xb = sX + (j & 1) * 256;
       xb[half * 128 + r] = mloc;
       named_sync(4, 256);
+      // every block has a valid key, so mnew is finite from the first block on
       const float mnew = fmaxf(m, fmaxf(mloc, xb[(half ^ 1) * 128 + r]));
-      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - mnew);
+      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mnew);
       float lsum = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[ch][i] = exp2f(s[ch][i] - mnew);
-          lsum += s[ch][i];
-        }
+      for (int i = 0; i < 64; ++i) {
+        s[i] = ex2_approx(fmaf(s[i], a.scale_log2, -mnew));   // masked keys: 2^-inf = 0
+        lsum += s[i];
+      }
       l = l * alpha + lsum;
       m = mnew;
       if (st == 0) tc_mark(a.trace, 1, j, 1);
       // P over the S columns: per 32-key chunk 16 columns of P_hi, 16 of P_lo
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        if (ch == 1 && own) break;
+      if (own) {
         uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) split_pair_h2(s[ch][2 * e], s[ch][2 * e + 1], w[e], w[16 + e]);
-        tmem_st32(sb + (uint32_t)(ch * 32), w);
+        for (int e = 0; e < 16; ++e) split_pair_h2(s[2 * e], s[2 * e + 1], w[e], w[16 + e]);
+        tmem_st32(sb, w);
+      } else {
+        uint32_t w[64];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            split_pair_h2(s[32 * ch + 2 * e], s[32 * ch + 2 * e + 1], w[32 * ch + e], w[32 * ch + 16 + e]);
+        tmem_st64(sb, w);
       }
       tc_fence_before();
       mbar_arrive(&p_full[bf]);

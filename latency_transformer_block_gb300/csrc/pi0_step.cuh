@@ -315,14 +315,10 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool st
   const int q = mw & 3, ch = mw >> 2;
   const int f = r.m * 128 + q * 32 + lane;
   const uint32_t tb = acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
-  float v[32], w[32];
-  tmem_ld32(tb, v);
-  tmem_ld32(tb + 64, w);
+  float v[32], w[32], z[32];
+  tmem_ld32x3(tb, tb + 64, tb + 128, v, w, z);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += w[j];
-  tmem_ld32(tb + 128, w);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += w[j];
+  for (int j = 0; j < 32; ++j) v[j] = (v[j] + w[j]) + z[j];
   tc_fence_before();
   // each lane quad transposes 4 tokens x its 4 outputs, so a lane adds 4
   // consecutive outputs of one token: one vector reduction
