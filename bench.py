@@ -29,9 +29,9 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "pi0_ae"
 PAGES_AE_MS = 11.001   # pages' action-expert time, 2 views, RTX 4090 (context)
 # DRAM bytes (read + write) of one step-kernel launch from the ncu capture in
-# profiles/pi0_step_kernel_pi0_ae.md (639.82 MB read + 4.22 MB written); set to
+# profiles/pi0_step_kernel_pi0_ae.md (640.13 MB read + 4.30 MB written); set to
 # None whenever the kernel changes after that capture
-STEP_TRAFFIC = 644036864
+STEP_TRAFFIC = 644429056
 
 
 def parse():
