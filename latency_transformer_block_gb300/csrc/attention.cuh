@@ -431,6 +431,14 @@ struct SegAttnArgs {
   int kv_split;
   float* part_o;
   float* part_ml;
+  // tensor-core kernel: a 1-D grid of work items over the tiles (query tile
+  // fastest, then head, then group).  Tiles 0 .. tc_whole - 1 run whole; each
+  // later tile is cut into tc_pieces key ranges (one item each) that leave
+  // their unnormalised output and row (max, sum) in tc_part_o [piece][128][128]
+  // / tc_part_ml [piece][128][2], piece = item - tc_whole, for the combine.
+  int tc_whole, tc_pieces;
+  float* tc_part_o;
+  float* tc_part_ml;
   SegGroup grp[16];
 };
 

@@ -15,7 +15,9 @@
 //   O  = (P_hi + P_lo) V    (+ P_hi V_lo for own keys)
 //
 // The dropped cross terms (Q_lo K_lo, P_lo V_lo) are below 2^-22 of the kept
-// ones.  One CTA = one (128-row query tile, head, group).  Keys run in blocks:
+// ones.  One CTA = one (128-row query tile, head, group), or one key range of
+// such a tile when the launch splits the tiles of its last, partly filled
+// wave (attention_tc_combine_kernel merges the ranges).  Keys run in blocks:
 // 128 cached keys (history segments concatenated, N = 128 for S) or 64 own
 // keys (hi and lo planes in the same buffers).  On this hardware an M = 128
 // MMA costs the same ~152 cycles for N up to 256, so wide blocks matter.
@@ -47,6 +49,7 @@ namespace lat {
 constexpr int kTcThreads = 384;
 constexpr int kTcKB = 128;                      // cached keys per block
 constexpr int kTcKBO = 64;                      // own keys per block
+constexpr int kTcMinRangeBlocks = 2;            // key blocks of a split tile's key range, at least
 constexpr int kTcQT = 16384;                    // one [128 rows][64] 16-bit tile
 constexpr int kTcBuf = 32768;                   // one K or V buffer
 // shared memory: Q [2 planes][2 k-tiles], K [2 buffers], V [2 buffers], row
@@ -294,14 +297,22 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 22);
   TcSegTab* tab = reinterpret_cast<TcSegTab*>(sm + kTcOffTab);
 
-  // query tile fastest: the tiles of one head run together and share its K/V in L2
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // work item -> tile (and key range).  Query tile fastest: the tiles of one
+  // head run together and share its K/V in L2.
+  const int nqt = (a.T_rows + 127) / 128;
+  const int item = blockIdx.x;
+  const int tile = item < a.tc_whole ? item : a.tc_whole + (item - a.tc_whole) / a.tc_pieces;
+  const int piece = item < a.tc_whole ? -1 : (item - a.tc_whole) % a.tc_pieces;
+  const int qt = tile % nqt, h = (tile / nqt) % a.Hq, b = tile / (nqt * a.Hq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = h / (a.Hq / a.Hkv);
   const SegGroup& G = a.grp[b];
   TcKeys kk;
   kk.init(a, G, threadIdx.x == 0 ? tab : nullptr);
-  const int nblk = kk.nblk;
+  // key blocks j0 .. j0 + nblk - 1 of the group; below, j counts within the
+  // range (buffers and parities) and j0 + j names the block
+  const int j0 = piece < 0 ? 0 : piece * kk.nblk / a.tc_pieces;
+  const int nblk = (piece < 0 ? kk.nblk : (piece + 1) * kk.nblk / a.tc_pieces) - j0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 256);
@@ -341,7 +352,7 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc_wait(&k_full[bf], (j >> 1) & 1, err, 61)) return false;
           tc_mark(a.trace, 0, j, 0);
           tc_fence_after();
-          const bool own = kk.own(j);
+          const bool own = kk.own(j0 + j);
           const uint32_t kb = ka + (uint32_t)(bf * kTcBuf);
           const uint32_t kts = own ? 8192u : 16384u;   // k-tile stride: keys x 128 B
           const uint32_t idS = idesc_f16_f32(128, own ? kTcKBO : kTcKB);
@@ -367,7 +378,7 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
           if (j >= 2 && !tc_wait(&o_free[bf], par ^ 1u, err, 64)) return false;
           tc_mark(a.trace, 0, j, 1);
           tc_fence_after();
-          const bool own = kk.own(j);
+          const bool own = kk.own(j0 + j);
           const int nk = own ? kTcKBO : kTcKB;
           const uint32_t vb = va + (uint32_t)(bf * kTcBuf);
           const uint32_t lbo = own ? 8192u : 16384u;   // bytes between the two 64-dim halves of V
@@ -414,15 +425,15 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
           uint64_t* tb = isv ? &vt_full[bf] : &kt_full[bf];
           fence_proxy_async_smem();
           mbar_arrive_expect_tx(tb, kTcBuf);
-          if (!kk.own(j)) {
+          if (!kk.own(j0 + j)) {
             int sgi, k0, nv;
-            kk.cached(tab, j, sgi, k0, nv);
+            kk.cached(tab, j0 + j, sgi, k0, nv);
             const int row = (isv ? tab->vrow[sgi] : tab->krow[sgi]) + k0;
             tma_load_2d(dst, &ring_map, tb, kvh * DH, row, pol);
             tma_load_2d(dst + 16384, &ring_map, tb, kvh * DH + 64, row, pol);
           } else {
             // own-plane rows: [K hi | K lo | V hi | V lo], kv_ld columns each
-            const int row = tab->own_row + (j - kk.nb_c) * kTcKBO;
+            const int row = tab->own_row + (j0 + j - kk.nb_c) * kTcKBO;
             const int xh = (isv ? 2 * a.kv_ld : 0) + kvh * DH, xl = xh + a.kv_ld;
             tma_load_2d(dst, &own_map, tb, xh, row, pol);
             tma_load_2d(dst + 8192, &own_map, tb, xh + 64, row, pol);
@@ -467,8 +478,8 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       const int bf = j & 1;
       tc_wait(isv ? &vt_full[bf] : &kt_full[bf], (uint32_t)(j >> 1) & 1u, err, isv ? 70 : 69);
       uint8_t* dst = (isv ? sV : sK) + bf * kTcBuf;
-      const int nv = kk.valid(tab, j);
-      if (kk.own(j) && nv < kTcKBO) {
+      const int nv = kk.valid(tab, j0 + j);
+      if (kk.own(j0 + j) && nv < kTcKBO) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int it = st + 256 * u, r = it >> 4, c = it & 15;
@@ -502,10 +513,10 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     if (nblk > 0) prep(0, false);
     for (int j = 0; j < nblk; ++j) {
       const int bf = j & 1;
-      const bool own = kk.own(j);
+      const bool own = kk.own(j0 + j);
       if (j + 1 < nblk) prep(j + 1, false);   // K of the next block: its S overlaps this softmax
       const int nh = (own ? kTcKBO : kTcKB) / 2;     // keys of this thread's half
-      const int k0 = half * nh, nv = kk.valid(tab, j);
+      const int k0 = half * nh, nv = kk.valid(tab, j0 + j);
       tc_wait(&s_full[bf], (uint32_t)(j >> 1) & 1u, err, 67);
       if (st == 0) tc_mark(a.trace, 1, j, 0);
       tc_fence_after();
@@ -572,11 +583,19 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     named_sync(4, 256);
     const float lt = l + xl[(half ^ 1) * 128 + r];
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
-    if (rg < a.T_rows) {
+    if (rg < a.T_rows && piece < 0) {
 #pragma unroll
       for (int i = 0; i < 64; ++i) o[i] *= inv;
       // the two fp16 planes of the output projection's activation
       store_planes<64>(a.out + ((size_t)b * a.T_rows + rg) * kActTerms * a.ldh + h * DH + half * 64, a.ldh, o);
+    } else if (rg < a.T_rows) {
+      // one key range of a split tile: unnormalised output (relative to 2^m)
+      // and the row's (m, sum) for attention_tc_combine_kernel
+      const size_t pr = (size_t)(item - a.tc_whole) * 128 + r;
+      float4* po = reinterpret_cast<float4*>(a.tc_part_o + pr * DH + half * 64);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) po[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      if (half == 0) *reinterpret_cast<float2*>(a.tc_part_ml + pr * 2) = make_float2(m, lt);
     }
   }
   tc_fence_before();
@@ -585,6 +604,34 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Merge the key ranges of the split tiles: per row, the ranges' outputs
+// weighted by 2^(m_p - max m) over the weighted sums, written as the two fp16
+// planes a whole tile writes.  Grid (split tiles, 128 rows), one thread per
+// head dim.  A range without keys has m = -inf and weight 0.
+static __global__ void __launch_bounds__(128) attention_tc_combine_kernel(const __grid_constant__ SegAttnArgs a) {
+  constexpr int DH = 128;
+  const int nqt = (a.T_rows + 127) / 128;
+  const int tile = a.tc_whole + blockIdx.x, r = blockIdx.y, c = threadIdx.x;
+  const int qt = tile % nqt, h = (tile / nqt) % a.Hq, b = tile / (nqt * a.Hq);
+  const int rg = qt * 128 + r;
+  if (rg >= a.T_rows) return;
+  const size_t p0 = (size_t)blockIdx.x * a.tc_pieces;
+  float M = -INFINITY;
+  for (int p = 0; p < a.tc_pieces; ++p) M = fmaxf(M, a.tc_part_ml[((p0 + p) * 128 + r) * 2]);
+  float num = 0.f, den = 0.f;
+  for (int p = 0; p < a.tc_pieces; ++p) {
+    const size_t i = (p0 + p) * 128 + r;
+    const float m = a.tc_part_ml[i * 2], w = m == -INFINITY ? 0.f : exp2f(m - M);
+    num += w * a.tc_part_o[i * DH + c];
+    den += w * a.tc_part_ml[i * 2 + 1];
+  }
+  const float v = den > 0.f ? num / den : 0.f;
+  const __half hv = __float2half_rn(v);
+  __half* o = a.out + ((size_t)b * a.T_rows + rg) * kActTerms * a.ldh + h * DH + c;
+  o[0] = hv;
+  o[a.ldh] = __float2half_rn(v - __half2float(hv));
 }
 
 // The history K/V segments of one call (bf16 ring rows) -> their fp16 copy,

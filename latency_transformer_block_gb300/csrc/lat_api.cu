@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <utility>
 #include <cstdarg>
@@ -165,6 +166,7 @@ struct lat_ctx {
   // prefix attention split over key ranges: partial outputs and (max, sum), at
   // most num_sms CTAs x 64 rows
   float *seg_part_o = nullptr, *seg_part_ml = nullptr;
+  float *tc_part_o = nullptr, *tc_part_ml = nullptr;   // DiT attention: key ranges of the split tiles
   double* theta = nullptr;
   __half *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two fp16 planes [2][m_max][kvd] (prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
@@ -782,6 +784,9 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
     c->hist_rows = planes * d.T_q;
     LAT_TRY(c->alloc(&c->hist16, (size_t)c->hist_rows * d.D));
     CUDA_TRY(cudaMemset(c->hist16, 0, (size_t)c->hist_rows * d.D * 2));   // rows never written stay finite
+    // at most one key range per SM (enqueue_attention_seg), 128 rows x dh each
+    LAT_TRY(c->alloc(&c->tc_part_o, (size_t)c->num_sms * 128 * d.dh));
+    LAT_TRY(c->alloc(&c->tc_part_ml, (size_t)c->num_sms * 128 * 2));
   } else {
     LAT_TRY(c->alloc(&c->kown, (size_t)2 * c->m_max * d.Hkv * d.dh));
     LAT_TRY(c->alloc(&c->vown, (size_t)2 * c->m_max * d.Hkv * d.dh));
@@ -964,9 +969,42 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
     CUtensorMap ring_map, own_map;
     LAT_TRY(make_kmajor_map(&ring_map, a.hist16, a.hist_rows, a.kv_ld, 128));
     LAT_TRY(make_kmajor_map(&own_map, a.own16, c->m_max, 4 * a.kv_ld, 64));
-    dim3 grid((a.T_rows + 127) / 128, d.Hq, groups);
-    attention_tc_kernel<<<grid, kTcThreads, attn_tc_smem_bytes(), st>>>(a, ring_map, own_map, c->err);
-    return launch_check("attention_tc");
+    // One CTA per SM (TMEM), so the tiles run in waves of num_sms.  The tiles
+    // of a last, partly filled wave are cut into key ranges of at least
+    // kTcMinRangeBlocks blocks, as many per tile as fill the SMs once, and a
+    // combine kernel merges them: the tail takes a fraction of a whole tile's
+    // time instead of all of it.
+    const int nqt = (a.T_rows + 127) / 128, tiles = nqt * d.Hq * groups;
+    SegAttnArgs b = a;
+    b.tc_whole = tiles;
+    b.tc_pieces = 1;
+    b.tc_part_o = c->tc_part_o;
+    b.tc_part_ml = c->tc_part_ml;
+    const int tail = tiles % c->num_sms;
+    if (tail > 0 && c->tc_part_o) {
+      int nblk_min = INT_MAX;   // key blocks of each group, counted as the kernel does
+      for (int g = 0; g < groups; ++g) {
+        int nb = 0;
+        for (int s = 0; s < a.grp[g].nseg; ++s) {
+          const AttnSeg& sg = a.grp[g].seg[s];
+          nb += sg.k16 ? (sg.n + kTcKBO - 1) / kTcKBO : (sg.n + kTcKB - 1) / kTcKB;
+        }
+        nblk_min = std::min(nblk_min, nb);
+      }
+      const int pieces = std::min(c->num_sms / tail, nblk_min / kTcMinRangeBlocks);
+      if (pieces >= 2) {   // tail * pieces <= num_sms: fits the scratch
+        b.tc_whole = tiles - tail;
+        b.tc_pieces = pieces;
+      }
+    }
+    const int items = b.tc_whole + (tiles - b.tc_whole) * b.tc_pieces;
+    attention_tc_kernel<<<items, kTcThreads, attn_tc_smem_bytes(), st>>>(b, ring_map, own_map, c->err);
+    LAT_TRY(launch_check("attention_tc"));
+    if (b.tc_pieces > 1) {
+      attention_tc_combine_kernel<<<dim3(tiles - b.tc_whole, 128), 128, 0, st>>>(b);
+      LAT_TRY(launch_check("attention_tc_combine"));
+    }
+    return LAT_OK;
   }
   if (dh != 256) return fail(LAT_ERR_SHAPE, "dense-path attention: dh 128 or 256");
   // fewer CTAs than SMs (few groups): split the keys into ranges (at least two
