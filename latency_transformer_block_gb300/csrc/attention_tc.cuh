@@ -11,11 +11,13 @@
 //              query tile and head then reads by TMA
 //   own K/V    two fp16 planes of the fp32 values
 //
-//   S  = (Q_hi + Q_lo) K^T  (+ Q_hi K_lo^T for own keys)
+//   S  = (Q_hi + Q_lo) K^T  (own keys: (Q_hi + Q_lo) (K_hi + K_lo)^T, with
+//        K_hi and K_lo as the two 64-row halves of one N = 128 operand, so
+//        each 16-dim step is two MMAs as for cached keys; the row warps add
+//        the two 64-column halves of S)
 //   O  = (P_hi + P_lo) V    (+ P_hi V_lo for own keys)
 //
-// The dropped cross terms (Q_lo K_lo, P_lo V_lo) are below 2^-22 of the kept
-// ones.  One CTA = one (128-row query tile, head, group), or one key range of
+// The dropped cross term P_lo V_lo is below 2^-22 of the kept ones.  One CTA = one (128-row query tile, head, group), or one key range of
 // such a tile when the launch splits the tiles of its last, partly filled
 // wave (attention_tc_combine_kernel merges the ranges).  Keys run in blocks:
 // 128 cached keys (history segments concatenated, N = 128 for S) or 64 own
@@ -352,20 +354,18 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc_wait(&k_full[bf], (j >> 1) & 1, err, 61)) return false;
           tc_mark(a.trace, 0, j, 0);
           tc_fence_after();
-          const bool own = kk.own(j0 + j);
+          // 128 B-operand rows per k-tile: 128 cached keys, or the 64 own keys'
+          // hi plane then their lo plane (S columns 0..63: (Q_hi + Q_lo) K_hi,
+          // 64..127: (Q_hi + Q_lo) K_lo, summed by the row warps)
           const uint32_t kb = ka + (uint32_t)(bf * kTcBuf);
-          const uint32_t kts = own ? 8192u : 16384u;   // k-tile stride: keys x 128 B
-          const uint32_t idS = idesc_f16_f32(128, own ? kTcKBO : kTcKB);
+          const uint32_t idS = idesc_f16_f32(128, 128);
           const uint32_t d = tmem + (uint32_t)(bf * 128);
 #pragma unroll
           for (int s = 0; s < DH / 16; ++s) {   // dims 16 s .. 16 s + 15
             const uint32_t kt = (uint32_t)(s >> 2), off = (uint32_t)((s & 3) * 32);
-            const uint64_t bk = desc_k_sw128(kb + kt * kts + off);
+            const uint64_t bk = desc_k_sw128(kb + kt * 16384u + off);
             mma_bf16_ss(d, desc_k_sw128(qa + kt * kTcQT + off), bk, idS, s != 0 ? 1u : 0u);   // Q_hi K
             mma_bf16_ss(d, desc_k_sw128(qa + (2 + kt) * kTcQT + off), bk, idS, 1u);          // Q_lo K
-            if (own)                                                                          // Q_hi K_lo
-              mma_bf16_ss(d, desc_k_sw128(qa + kt * kTcQT + off), desc_k_sw128(kb + 16384u + kt * kts + off), idS,
-                          1u);
           }
           mma_commit(&k_free[bf]);
           mma_commit(&s_full[bf]);
@@ -433,12 +433,14 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_2d(dst + 16384, &ring_map, tb, kvh * DH + 64, row, pol);
           } else {
             // own-plane rows: [K hi | K lo | V hi | V lo], kv_ld columns each
+            // K: [k-tile][hi 64 rows | lo 64 rows]; V: [plane][64-dim half][64 keys]
             const int row = tab->own_row + (j0 + j - kk.nb_c) * kTcKBO;
             const int xh = (isv ? 2 * a.kv_ld : 0) + kvh * DH, xl = xh + a.kv_ld;
+            const int o1 = isv ? 8192 : 16384, ol = isv ? 16384 : 8192;   // second k-tile / half, lo plane
             tma_load_2d(dst, &own_map, tb, xh, row, pol);
-            tma_load_2d(dst + 8192, &own_map, tb, xh + 64, row, pol);
-            tma_load_2d(dst + 16384, &own_map, tb, xl, row, pol);
-            tma_load_2d(dst + 16384 + 8192, &own_map, tb, xl + 64, row, pol);
+            tma_load_2d(dst + o1, &own_map, tb, xh + 64, row, pol);
+            tma_load_2d(dst + ol, &own_map, tb, xl, row, pol);
+            tma_load_2d(dst + ol + o1, &own_map, tb, xl + 64, row, pol);
           }
         }
       }
@@ -484,9 +486,10 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
         for (int u = 0; u < 4; ++u) {
           const int it = st + 256 * u, r = it >> 4, c = it & 15;
           if (r < nv) continue;
-          const int off = (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          const int o1 = isv ? 8192 : 16384, ol = isv ? 16384 : 8192;   // as the TMA placed them
+          const int off = (c >> 3) * o1 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(dst + 16384 + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dst + ol + off) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
@@ -521,13 +524,14 @@ static __global__ void __launch_bounds__(kTcThreads, 1)
       if (st == 0) tc_mark(a.trace, 1, j, 0);
       tc_fence_after();
       const uint32_t sb = trow + (uint32_t)(bf * 128 + k0);   // S (then P) columns of my keys
-      // raw scores of my keys (an own block has 32 per half: one 32-column load)
+      // raw scores of my keys (an own block has 32 per half: the K_hi and K_lo
+      // parts, 64 columns apart)
       float s[64];
       if (own) {
-        float t[32];
-        tmem_ld32(sb, t);
+        float t[32], u[32];
+        tmem_ld32x2(sb, sb + 64u, t, u);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = t[i];
+        for (int i = 0; i < 32; ++i) s[i] = t[i] + u[i];
       } else {
         tmem_ld64(sb, s);
       }
