@@ -459,10 +459,13 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
 //   S = q_hi K_hi + q_lo K_hi + q_hi K_lo,   O = P_hi V_hi + P_lo V_hi + P_hi V_lo
 // (the dropped lo x lo products are below 2^-22 of the kept ones).  One CTA =
 // one (head, 64-row query tile, group), 4 warps of 16 rows; keys in blocks of
-// 64, both planes of K and V by async copies.
-template <int DH>
+// KB, both planes of K and V by async copies.  The K/V tiles are all of the
+// shared memory: with KB = 32 (67.6 KB for dh = 256) two CTAs share an SM (255
+// registers a thread: two CTAs fill the register file) and hide each other's
+// latency; KB = 64 (135 KB, one CTA per SM) syncs half as often, for grids
+// that have no more CTAs than SMs.
+template <int DH, int KB>
 static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_constant__ SegAttnArgs a) {
-  constexpr int KB = 64;
   constexpr int LD = DH + 8;
   constexpr int NT = DH / 8;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -517,15 +520,15 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       }
       cp_async_wait_all();
       __syncthreads();
-      float s[8][4];
+      float s[KB / 8][4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+      for (int j = 0; j < KB / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll 4
       for (int ks = 0; ks < DH / 16; ++ks) {
         uint32_t af[2][4];
         q_frag(ks, af);
 #pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
+        for (int jp = 0; jp < KB / 16; ++jp) {
           const int mi = lane >> 3, rr = lane & 7;
           const int key = jp * 16 + ((mi >> 1) << 3) + rr;
           const int col = ks * 16 + ((mi & 1) << 3);
@@ -543,7 +546,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       }
       float mx0 = m0, mx1 = m1;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < KB / 8; ++j) {
         const int key = kb * KB + j * 8 + 2 * tq;
         s[j][0] = (key < sg.n) ? s[j][0] * a.scale_log2 : -INFINITY;
         s[j][1] = (key + 1 < sg.n) ? s[j][1] * a.scale_log2 : -INFINITY;
@@ -561,7 +564,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
       m1 = mx1;
       float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < KB / 8; ++j) {
         s[j][0] = exp2f(s[j][0] - mx0);
         s[j][1] = exp2f(s[j][1] - mx0);
         s[j][2] = exp2f(s[j][2] - mx1);
@@ -583,7 +586,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
         o[j][3] *= al1;
       }
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int kk = 0; kk < KB / 16; ++kk) {
         uint32_t pf[2][4];
         split_pair_h2(s[2 * kk][0], s[2 * kk][1], pf[0][0], pf[1][0]);
         split_pair_h2(s[2 * kk][2], s[2 * kk][3], pf[0][1], pf[1][1]);
@@ -672,14 +675,16 @@ static __global__ void attention_seg_combine_kernel(const __grid_constant__ SegA
 // Launch the attention (and the combine when there are several key ranges).
 // The kernels need more than 48 KB of dynamic shared memory for dh = 256:
 // call set_attention_smem_limits() once per device first.
-// K and V tiles, two planes each, rows padded to dh + 8; plus the fp32 Q tile
-// of the chunk kernel (rows padded to dh + 4)
-static inline int attn_smem_bytes(int dh) { return 4 * 64 * (dh + 8) * 2 + 64 * (dh + 4) * 4; }
+// segment attention: K and V blocks of kb keys in two planes each, rows padded to dh + 8
+static inline int seg_attn_smem_bytes(int dh, int kb) { return 4 * kb * (dh + 8) * 2; }
 // chunk attention: K and V blocks in two planes each, plus the partial scores
 static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
 static inline cudaError_t set_attention_smem_limits() {
-  cudaFuncSetAttribute(attention_seg_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes(256));
+  cudaFuncSetAttribute(attention_seg_kernel<256, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       seg_attn_smem_bytes(256, 32));
+  cudaFuncSetAttribute(attention_seg_kernel<256, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       seg_attn_smem_bytes(256, 64));
   cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(64));
   cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(128));
   cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(256));
