@@ -17,9 +17,10 @@
 //        the two 64-column halves of S)
 //   O  = (P_hi + P_lo) V    (+ P_hi V_lo for own keys)
 //
-// The dropped cross term P_lo V_lo is below 2^-22 of the kept ones.  One CTA = one (128-row query tile, head, group), or one key range of
-// such a tile when the launch splits the tiles of its last, partly filled
-// wave (attention_tc_combine_kernel merges the ranges).  Keys run in blocks:
+// The dropped cross term P_lo V_lo is below 2^-22 of the kept ones.  One CTA =
+// one (128-row query tile, head, group), or one key range of such a tile when
+// the launch splits the tiles of its last, partly filled wave
+// (attention_tc_combine_kernel merges the ranges).  Keys run in blocks:
 // 128 cached keys (history segments concatenated, N = 128 for S) or 64 own
 // keys (hi and lo planes in the same buffers).  On this hardware an M = 128
 // MMA costs the same ~152 cycles for N up to 256, so wide blocks matter.
@@ -40,7 +41,7 @@
 // 32-key chunk: 16 columns of P_hi, then 16 of P_lo) and the PV MMA reads it
 // there as its A operand.  The product of one key block, P V, lands in
 // columns 256 + 128 (j % 2) .. and is added to the running output in fp32
-// registers, so no TMEM accumulation chain is longer than 24 MMAs.
+// registers, so no TMEM accumulation chain is longer than 16 MMAs.
 #pragma once
 #include "attention.cuh"
 #include "common.cuh"
