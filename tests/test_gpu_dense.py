@@ -121,6 +121,22 @@ def test_dit_1p3b_full_block_sampled_rows():
         assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 1.3B own KV chunk {c}")
 
 
+def test_dit_1p3b_mixed_history_sampled_rows():
+    # three chunks with 0, 2 and 4 history chunks (25, 51 and 77 key blocks):
+    # 468 attention tiles, so the 12 tiles past the third wave (query tiles
+    # 1..12 of the last head of the chunk with 4 history chunks) are cut into
+    # 12 key ranges each, a count bounded by the chunk with only its own keys;
+    # the sampled rows 1400.. and 1540.. lie in split tiles
+    cfg = synth.config("dit_1p3b", L=1)
+    descs = [(0, 0, 0), (0, 2, 1), (0, 9, 2)]
+    rows = np.r_[0:4, 1400:1404, 1540:1560]        # the last query tiles are the split ones
+    got_x, ref_x, got_ring, ref_ring, _ = _dit_case(cfg, descs, rows=rows)
+    assert_rel(got_x, ref_x, BLOCK_TOL, "dit 1.3B mixed-history block residual (sampled rows)")
+    for (st, c, s) in descs:
+        sl = c % 5
+        assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 1.3B own KV chunk {c}")
+
+
 def test_dit_14b_block_batch8_sampled_rows():
     cfg = synth.config("dit_14b")
     descs = synth.dit_chunk_descs(cfg, 8)
