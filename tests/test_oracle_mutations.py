@@ -8,6 +8,7 @@ pinned at that point.
 import numpy as np
 import pytest
 
+import oracle.bf16 as bf16
 import oracle.ops as ops
 import oracle.dit as dit
 import oracle.pi0 as pi0
@@ -80,6 +81,29 @@ def _mask_wrong_row(T, Tp, cfg):
     return allow
 
 
+def _layernorm_no_center(x, eps):
+    return x / np.sqrt(np.var(x, axis=-1, keepdims=True) + eps)
+
+
+def _silu_sigmoid_approx(x):
+    return x / (1.0 + np.exp(-1.702 * x))
+
+
+def _round_half_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    r = np.sign(m) * np.floor(np.abs(np.ldexp(m, 8)) + 0.5)
+    return np.ldexp(r, e - 8)
+
+
+def _ring_slot_mod_nhist(c, n_hist):
+    return c % n_hist
+
+
+def _positions_shifted(c, T):
+    return c * T + np.arange(T) + 1
+
+
 _orig_attention = ops.attention
 
 MUTATIONS = [
@@ -96,6 +120,11 @@ MUTATIONS = [
     ((pi0,), "chunk_mask", _mask_wrong_row, ["test_pi0_prefix_lm_mask"]),
     ((dit,), "interval_descs", _descs_step_off_by_one,
      ["test_dit_interleaved_schedule", "test_dit_pipeline_equals_sequential"]),
+    ((ops, dit), "layernorm", _layernorm_no_center, ["test_layernorm_closed_forms"]),
+    ((ops, pi0, dit), "silu", _silu_sigmoid_approx, ["test_silu_library"]),
+    ((bf16,), "round_rne", _round_half_away, ["test_bf16_ties_to_even_and_decode"]),
+    ((dit,), "ring_slot", _ring_slot_mod_nhist, ["test_ring_slot_matches_fifo_simulation"]),
+    ((dit,), "positions", _positions_shifted, ["test_ring_slot_matches_fifo_simulation"]),
 ]
 
 
