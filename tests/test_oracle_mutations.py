@@ -104,6 +104,24 @@ def _positions_shifted(c, T):
     return c * T + np.arange(T) + 1
 
 
+def _softmax_over_queries(z, axis=-1):
+    z = z - np.max(z, axis=-2, keepdims=True)
+    e = np.exp(z)
+    return e / np.sum(e, axis=-2, keepdims=True)
+
+
+def _rope_angles_half_rate(pos, dh, base):
+    i = np.arange(dh // 2, dtype=np.float64)
+    return np.asarray(pos, dtype=np.float64)[:, None] * (base ** (-i / dh))[None, :]
+
+
+def _embed_no_silu(x, t, W, D):
+    a = x @ W["w_in"] + W["b_in"]
+    te = np.broadcast_to(ops.timestep_embedding(t, D), a.shape)
+    z = np.concatenate([a, te], axis=1) @ W["w1"] + W["b1"]
+    return z @ W["w2"] + W["b2"]
+
+
 _orig_attention = ops.attention
 
 MUTATIONS = [
@@ -125,6 +143,9 @@ MUTATIONS = [
     ((bf16,), "round_rne", _round_half_away, ["test_bf16_ties_to_even_and_decode"]),
     ((dit,), "ring_slot", _ring_slot_mod_nhist, ["test_ring_slot_matches_fifo_simulation"]),
     ((dit,), "positions", _positions_shifted, ["test_ring_slot_matches_fifo_simulation"]),
+    ((ops,), "softmax", _softmax_over_queries, ["test_attention_brute_force"]),
+    ((ops,), "rope_angles", _rope_angles_half_rate, ["test_rope_hand_case", "test_rope_is_complex_rotation"]),
+    ((pi0,), "embed", _embed_no_silu, ["test_time_embedding_fold"]),
 ]
 
 
