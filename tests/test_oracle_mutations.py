@@ -122,6 +122,16 @@ def _embed_no_silu(x, t, W, D):
     return z @ W["w2"] + W["b2"]
 
 
+def _split6_swap_first(a, D):
+    sh1, sc1, g1, sh2, sc2, g2 = [a[i * D:(i + 1) * D] for i in range(6)]
+    return [sc1, sh1, g1, sh2, sc2, g2]
+
+
+def _split6_swap_second(a, D):
+    sh1, sc1, g1, sh2, sc2, g2 = [a[i * D:(i + 1) * D] for i in range(6)]
+    return [sh1, sc1, g1, sc2, sh2, g2]
+
+
 _orig_attention = ops.attention
 
 MUTATIONS = [
@@ -146,6 +156,8 @@ MUTATIONS = [
     ((ops,), "softmax", _softmax_over_queries, ["test_attention_brute_force"]),
     ((ops,), "rope_angles", _rope_angles_half_rate, ["test_rope_hand_case", "test_rope_is_complex_rotation"]),
     ((pi0,), "embed", _embed_no_silu, ["test_time_embedding_fold"]),
+    ((dit,), "_split6", _split6_swap_first, ["test_dit_zero_gates_is_identity_and_history_set"]),
+    ((dit,), "_split6", _split6_swap_second, ["test_dit_ffn_branch_closed_form"]),
 ]
 
 

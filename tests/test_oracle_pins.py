@@ -414,6 +414,25 @@ def test_dit_zero_gates_is_identity_and_history_set():
         assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
 
 
+def test_dit_ffn_branch_closed_form():
+    # gate1 = 0 leaves h = x; scale2 = -1 turns LN(h)(1 + scale2) + shift2 into
+    # the shift row for every token, so the block is
+    # x + gate2 * (GELU(shift2 W1) W2): the second modulation triple's order, its
+    # "1 +" and the FFN wiring, against matrix products and the pinned GELU
+    cfg, w, W, table, ring = _tiny_dit()
+    D = cfg["D"]
+    bm = RNG.standard_normal(6 * D) * 0.5
+    bm[2 * D:3 * D] = 0.0          # gate1
+    bm[4 * D:5 * D] = -1.0         # scale2
+    t = np.broadcast_to(bm, (cfg["S"], 6 * D)).copy()
+    xs = synth.dit_latents(cfg, 1, 9)
+    out = dit.block_batch(xs, [(0, 5, 2)], ring.copy(), t, w, cfg)
+    sh2, g2 = bm[3 * D:4 * D], bm[5 * D:6 * D]
+    f = ops.gelu_tanh(sh2[None, :] @ w["w1"]) @ w["w2"]
+    expect = xs[0].astype(np.float64) + g2 * f
+    assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------
 # Interleaved stage schedule of chunked AR diffusion (latent in/out + Euler)
 # ---------------------------------------------------------------------------
