@@ -1,0 +1,119 @@
+"""Phase table of the persistent step kernel (pi0 action expert) from its
+device timestamps (lat_debug_trace).
+
+  python -m latency_transformer_block_gb300.step_trace [--workload pi0_ae] [--chunks 3]
+
+Runs `--chunks` denoised chunks with the trace enabled (the last one is read)
+and prints, per phase of a block, the median over the blocks of one denoise
+step of
+  work    = last CTA finishing the phase - first CTA starting it,
+  barrier = first CTA starting the next phase - last CTA finishing this one,
+plus the sub-steps of the projection phases (median over the CTAs that take
+part): first activation tile, operand built, accumulator complete, epilogue
+done, each relative to the CTA's own phase start.
+
+Timestamps are the GPU's global timer (ns) written by thread 0 of each CTA's
+math warps; the trace changes nothing in the kernel's work but the writes.
+"""
+import argparse
+import sys
+
+import numpy as np
+
+# trace slots (the kernel's layout: 64 per CTA per block)
+PHASES = [  # (name, start slot, end slot)
+    ("QKV projection + head-group finalize", 1, 2),
+    ("attention", 5, 6),
+    ("combine", 7, 8),
+    ("O projection + residual", 9, 10),
+    ("gate/up projection + GeGLU tiles", 11, 12),
+    ("down projection + residual", 15, 16),
+]
+PROJ_SLOTS = {"QKV": (1, 20), "O": (9, 24), "gate/up": (11, 28), "down": (15, 32)}
+SUB = ["first tile", "operand built", "accumulator complete", "epilogue done"]
+
+
+def phase_table(tr: np.ndarray):
+    """tr: int64 [blocks][grid][64] timestamps (0 = not written)."""
+    L, G, _ = tr.shape
+    work = np.zeros((L, len(PHASES)))
+    bar = np.full((L, len(PHASES)), np.nan)
+    for l in range(L):
+        for i, (_, s, e) in enumerate(PHASES):
+            st = tr[l, :, s].astype(np.float64)
+            en = tr[l, :, e].astype(np.float64)
+            work[l, i] = (en.max() - st[st > 0].min()) / 1e3
+            if i + 1 < len(PHASES):
+                nxt = tr[l, :, PHASES[i + 1][1]].astype(np.float64)
+            elif l + 1 < L:
+                nxt = tr[l + 1, :, PHASES[0][1]].astype(np.float64)
+            else:
+                continue
+            bar[l, i] = (nxt[nxt > 0].min() - en.max()) / 1e3
+    sub = {}
+    for name, (s0, base) in PROJ_SLOTS.items():
+        vals = []
+        for l in range(L):
+            st = tr[l, :, s0].astype(np.float64)
+            rows = tr[l, :, base:base + 4].astype(np.float64)
+            ok = (rows > 0).all(axis=1)
+            if ok.any():
+                vals.append(np.median((rows[ok] - st[ok, None]) / 1e3, axis=0))
+        sub[name] = np.median(np.array(vals), axis=0) if vals else None
+    return work, bar, sub
+
+
+def report(tr: np.ndarray, out=sys.stdout):
+    work, bar, sub = phase_table(tr)
+    mw = np.median(work, axis=0)
+    mb = np.nanmedian(bar, axis=0)
+    print("| phase | work us | barrier us |", file=out)
+    print("|---|---|---|", file=out)
+    for i, (name, _, _) in enumerate(PHASES):
+        print(f"| {name} | {mw[i]:.2f} | {mb[i]:.2f} |", file=out)
+    per_block = np.median(work.sum(axis=1) + np.nan_to_num(bar).sum(axis=1))
+    print(f"| total | {mw.sum():.2f} | {np.nansum(mb):.2f} ({per_block:.1f} us per block) |", file=out)
+    print("", file=out)
+    print("| projection | " + " | ".join(SUB) + " |", file=out)
+    print("|---|" + "---|" * len(SUB), file=out)
+    for name, v in sub.items():
+        if v is not None:
+            print(f"| {name} | " + " | ".join(f"{x:.2f}" for x in v) + " |", file=out)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--workload", default="pi0_ae")
+    p.add_argument("--chunks", type=int, default=3)
+    args = p.parse_args()
+    import torch
+
+    from latency_transformer_block_gb300 import synth
+    from latency_transformer_block_gb300.models import Pi0ActionExpert
+
+    cfg = synth.config(args.workload)
+    wb = synth.pi0_weights(cfg, 0)
+    ib = synth.pi0_inputs(cfg, 0)
+    m = Pi0ActionExpert(cfg, wb, device="cuda:0")
+    kv = m.kv_from_bits(ib["kv"])
+    state = torch.from_numpy(ib["state"]).cuda()
+    noise = torch.from_numpy(ib["noise"]).cuda()
+    x = noise.clone()
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros(cfg["L"] * grid * 64, dtype=torch.int64, device="cuda")
+    m.ctx.debug_trace(buf)
+    for _ in range(args.chunks):
+        x.copy_(noise)
+        buf.zero_()
+        m.denoise(kv, state, x)
+    m.ctx.sync()
+    m.ctx.debug_trace(None)
+    # the buffer holds the last launch of the chunk (the last denoise step)
+    tr = buf.view(cfg["L"], grid, 64).cpu().numpy()
+    print(f"step kernel phases, workload {args.workload}: {cfg['L']} blocks of the last denoise step, "
+          f"grid {grid}")
+    report(tr)
+
+
+if __name__ == "__main__":
+    main()

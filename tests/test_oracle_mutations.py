@@ -132,7 +132,44 @@ def _split6_swap_second(a, D):
     return [sh1, sc1, g1, sc2, sh2, g2]
 
 
+def _head_no_gfinal(h, W, eps):
+    return ops.rmsnorm(h, eps) @ W["w_out"] + W["b_out"]
+
+
+def _head_no_norm(h, W, eps):
+    return (h * W["g_final"]) @ W["w_out"] + W["b_out"]
+
+
+def _adaln_no_inner_silu(W, cfg):
+    S, td = cfg["S"], cfg["t_dim"]
+    rows = []
+    for s in range(S):
+        e = (ops.timestep_embedding(s / S, td) @ W["wt1"] + W["bt1"]) @ W["wt2"] + W["bt2"]
+        rows.append(ops.silu(e) @ W["wmod"] + W["bmod"])
+    return np.stack(rows)
+
+
+def _adaln_grid_shifted(W, cfg):
+    S, td = cfg["S"], cfg["t_dim"]
+    rows = []
+    for s in range(S):
+        e = ops.silu(ops.timestep_embedding((s + 1) / S, td) @ W["wt1"] + W["bt1"]) @ W["wt2"] + W["bt2"]
+        rows.append(ops.silu(e) @ W["wmod"] + W["bmod"])
+    return np.stack(rows)
+
+
+def _state_token_no_bias(state, W):
+    return state @ W["w_state"]
+
+
+def _prefill_no_patch_bias(patch_emb_bits, weight_bits, cfg, skip_last=True, blocks=None):
+    wb = dict(weight_bits)
+    wb["b_patch"] = np.zeros_like(wb["b_patch"])
+    return _orig_prefill(patch_emb_bits, wb, cfg, skip_last=skip_last, blocks=blocks)
+
+
 _orig_attention = ops.attention
+_orig_prefill = pi0.prefill
 
 MUTATIONS = [
     # (module, attribute, replacement, pins that must catch it)
@@ -158,6 +195,12 @@ MUTATIONS = [
     ((pi0,), "embed", _embed_no_silu, ["test_time_embedding_fold"]),
     ((dit,), "_split6", _split6_swap_first, ["test_dit_zero_gates_is_identity_and_history_set"]),
     ((dit,), "_split6", _split6_swap_second, ["test_dit_ffn_branch_closed_form"]),
+    ((pi0,), "head", _head_no_gfinal, ["test_head_closed_form", "test_denoise_wiring_with_identity_blocks"]),
+    ((pi0,), "head", _head_no_norm, ["test_head_closed_form", "test_denoise_wiring_with_identity_blocks"]),
+    ((dit,), "adaln_table", _adaln_no_inner_silu, ["test_adaln_table_closed_form"]),
+    ((dit,), "adaln_table", _adaln_grid_shifted, ["test_adaln_table_closed_form"]),
+    ((pi0,), "state_token", _state_token_no_bias, ["test_state_token_closed_form"]),
+    ((pi0,), "prefill", _prefill_no_patch_bias, ["test_prefill_patch_projection"]),
 ]
 
 

@@ -531,3 +531,101 @@ def test_pi0_prefix_lm_mask():
     assert np.allclose(masked[0], alone[0], rtol=1e-12, atol=1e-13)
     assert np.array_equal(masked[1:], full[1:])
     assert not np.allclose(masked[0], full[0])
+
+
+# ----------------------------------------------------------------------------
+# action head, state token, adaLN table, prefix patch projection: closed forms
+# on hand-built weights (each would miss a dropped term with random weights
+# that the network-level pins zero out)
+# ----------------------------------------------------------------------------
+def test_head_closed_form():
+    """Rows h_r = a_r u with u a +-1 vector: mean(h_r^2) = a_r^2, so RMSNorm
+    gives a_r u / sqrt(a_r^2 + eps); W_out picks the first A dimensions, so the
+    velocity is that row times g_final on those dimensions, plus b_out."""
+    D, A, eps = 16, 4, 1e-6
+    u = np.where(RNG.standard_normal(D) > 0, 1.0, -1.0)
+    a = np.array([3.0, -0.5, 7.25])
+    h = a[:, None] * u[None, :]
+    g = 1.5 + 0.25 * np.arange(D)
+    w_out = np.zeros((D, A))
+    w_out[np.arange(A), np.arange(A)] = 1.0
+    b = np.array([0.5, -1.0, 2.0, 0.0])
+    v = pi0.head(h, {"g_final": g, "w_out": w_out, "b_out": b}, eps)
+    expect = (a / np.sqrt(a * a + eps))[:, None] * (u[:A] * g[:A])[None, :] + b[None, :]
+    assert np.allclose(v, expect, rtol=1e-14, atol=1e-15)
+
+
+def test_denoise_wiring_with_identity_blocks():
+    """Blocks with W_o = W_d = 0 are the identity, so each Euler step is
+    x <- x + dt head(embed(x, t_s)) on the action rows (the state row is not
+    integrated): the loop's order of embedding, head, rows and time grid."""
+    cfg, wb, ib = _tiny_pi0()
+    cfg = dict(cfg, S=3)
+    wb = dict(wb)
+    blocks = []
+    for b in wb["blocks"]:
+        b = dict(b)
+        b["wo"] = bf16.encode(np.zeros(b["wo"].shape))
+        b["wd"] = bf16.encode(np.zeros(b["wd"].shape))
+        blocks.append(b)
+    wb["blocks"] = blocks
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    x, _ = pi0.denoise(ib["noise"], ib["state"], ib["kv"], wb, cfg)
+    ref = np.asarray(ib["noise"], np.float64)
+    for s in range(cfg["S"]):
+        ref = ref + (1.0 / cfg["S"]) * pi0.head(pi0.embed(ref, s / cfg["S"], W, cfg["D"]), W, cfg["eps"])
+    assert np.allclose(x, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_state_token_closed_form():
+    state = np.array([1.0, -2.0, 0.5, 3.0])
+    w = np.zeros((4, 8))
+    w[0, 0], w[1, 3], w[3, 7] = 2.0, 1.0, -1.0
+    b = 0.5 * np.arange(8) + 0.25
+    got = pi0.state_token(state, {"w_state": w, "b_state": b})
+    expect = b.copy()
+    expect[0] += 2.0
+    expect[3] += -2.0
+    expect[7] += -3.0
+    assert np.array_equal(got, expect)
+
+
+def test_adaln_table_closed_form():
+    """Wt1 routes cos(1000 t) (the embedding's first cosine, frequency 1) to
+    every hidden unit, Wt2 is the identity and Wmod repeats its input six
+    times, so A[s][kD + j] = SiLU(SiLU(cos(1000 t_s) + bt1_j) + bt2_j) + bmod_{kD+j}
+    with t_s = s / S; SiLU from the library."""
+    D, td, S = 4, 16, 4
+    wt1 = np.zeros((td, D))
+    wt1[td // 2, :] = 1.0
+    bt1 = np.array([0.5, -1.0, 0.0, 2.0])
+    bt2 = np.array([0.0, 0.25, -0.5, 1.0])
+    bmod = np.linspace(-1.0, 1.0, 6 * D)
+    W = {"wt1": wt1, "bt1": bt1, "wt2": np.eye(D), "bt2": bt2, "wmod": np.tile(np.eye(D), (1, 6)), "bmod": bmod}
+    A = dit.adaln_table(W, {"S": S, "t_dim": td})
+    silu = torch.nn.functional.silu
+    for s in range(S):
+        z = torch.tensor(math.cos(1000.0 * s / S) + bt1, dtype=torch.float64)
+        e = silu(z) + torch.from_numpy(bt2)
+        expect = np.tile(silu(e).numpy(), 6) + bmod
+        assert np.allclose(A[s], expect, rtol=1e-13, atol=1e-14)
+
+
+def test_prefill_patch_projection():
+    """One-hot patch embeddings pick rows of W_patch, so layer 0's K/V are the
+    first block's K/V of h_i = W_patch[j_i] + b_patch at positions 0..Tp-1."""
+    cfg = synth.config("prefill", D=32, Hq=2, Hkv=1, dh=16, F=48, L=2, T_prefix=8, T_q=4, patch_dim=12)
+    wb = synth.prefill_weights(cfg, 7)
+    Tp, P = cfg["T_prefix"], cfg["patch_dim"]
+    idx = np.array([3, 0, 11, 5, 5, 7, 1, 2])
+    pe = np.zeros((1, Tp, P))
+    pe[0, np.arange(Tp), idx] = 1.0
+    kv = bf16.decode(pi0.prefill(bf16.encode(pe), wb, cfg))
+    wp, bp = bf16.decode(wb["w_patch"]), bf16.decode(wb["b_patch"])
+    assert np.count_nonzero(bp) > cfg["D"] // 2
+    h = wp[idx] + bp
+    w0 = pi0.method_block(pi0.decode_tree(wb["blocks"][0]))
+    empty = np.zeros((0, cfg["Hkv"] * cfg["dh"]))
+    _, k, v = pi0.block(h, empty, empty, np.arange(Tp), w0, cfg, kv_only=True)
+    assert np.array_equal(kv[0, 0, 0, :Tp], k)
+    assert np.array_equal(kv[0, 0, 1, :Tp], v)
