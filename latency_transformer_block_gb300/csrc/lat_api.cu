@@ -101,21 +101,6 @@ static lat_status make_kmajor_map(CUtensorMap* map, const void* base, int rows, 
   return LAT_OK;
 }
 
-// fp32 row-major activation [rows][cols] -> tiles of 64 rows x 64 columns, no swizzle.
-static lat_status make_f32_map(CUtensorMap* map, const void* base, int rows, int cols) {
-  EncodeTiledFn enc;
-  LAT_TRY(get_encode(&enc));
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  cuuint32_t box[2] = {64, 64};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(LAT_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
-  return LAT_OK;
-}
-
 // ---------------------------------------------------------------------------
 // context
 // ---------------------------------------------------------------------------
@@ -151,9 +136,8 @@ struct lat_ctx {
   int attn_split = 1;
   DevErr* err = nullptr;
 
-  // persistent step kernel: arguments, fp32 activation maps, zero-at-entry block
+  // persistent step kernel: arguments, zero-at-entry block
   MkArgs mk{};
-  CUtensorMap amap_x;
   void* mk_zero = nullptr;
   size_t mk_zero_bytes = 0;
 
@@ -565,7 +549,7 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   // --- persistent step kernel: [barrier counter, group counters | sums of squares |
   //     QKV sums], cleared before every launch; key-block partials; maps; plans ---
   {
-    const size_t bar_b = 128 + 4 * (size_t)kCntWords, ss_b = (size_t)L * 128 * 4, qkv_b = (size_t)64 * c->nqkv * 4;
+    const size_t bar_b = 128 + 4 * (size_t)kCntWords, ss_b = (size_t)kSsRows * 64 * 4, qkv_b = (size_t)64 * c->nqkv * 4;
     const size_t gu_b = (size_t)64 * 2 * F * 4;
     static_assert((128 + 4 * kCntWords) % 16 == 0, "counter block keeps the sums 16-byte aligned");
     if (c->nqkv / std::max(d.dh, 128) > 32) return fail(LAT_ERR_SHAPE, "at most 32 QKV head groups");
@@ -620,7 +604,6 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
       m.g[i].N = gp[i]->N_out;
       if (m.g[i].MT * m.g[i].splits > c->num_sms) return fail(LAT_ERR_SHAPE, "projection plan exceeds the grid");
     }
-    LAT_TRY(make_f32_map(&c->amap_x, c->xres, 64, D));
   }
 
   std::vector<double> t(d.S + 1);
@@ -672,13 +655,13 @@ static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long lo
   cfg.numAttrs = 1;
   cudaError_t e;
   if (c->d.dh == 64)
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
                            c->bmap_o, c->bmap_h, a);
   else if (c->d.dh == 128)
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<128>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<128>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
                            c->bmap_o, c->bmap_h, a);
   else
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<256>, c->map_qkv, c->map_o, c->map_gu, c->map_d, c->amap_x,
+    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<256>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
                            c->bmap_o, c->bmap_h, a);
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch pi0_step: %s", cudaGetErrorString(e));
   return LAT_OK;

@@ -14,13 +14,19 @@
 //  * warp 1 issues tcgen05 MMAs (M = 128 weight rows, N = 192 = three bf16
 //    planes x 64 tokens, fp32 accumulator in TMEM, two buffers).
 //  * warps 4..11 ("math") do everything that depends on activations: they
-//    split fp32 activation tiles (staged by warp 2's TMA) into three bf16
-//    planes in the MMA's swizzled layout, run the split-K epilogues (vector
-//    reductions into fp32 sums at L2), the attention and the combine of
-//    key-range partials.
+//    load the fp32 residual stream from global memory (several k-tiles in
+//    flight, in registers) and split it into three bf16 planes in the MMA's
+//    swizzled layout (warp 2 brings the other operands' planes by TMA), run
+//    the split-K epilogues (vector reductions into fp32 sums at L2), the
+//    attention and the combine of key-range partials.
+//  * Per weight tile the shared memory moves ~80 KB (MMA reads of the 24 KB
+//    operand and 16 KB weight tile, the operand's 24 KB of stores, the weight
+//    tile's 16 KB TMA write); at ~128 B per clock that, not the tensor core
+//    (96 cycles per M = 128, N = 192 MMA), paces a projection's k-tiles.
 //
 // Per block six phases, separated by a grid barrier (bounded spin):
-//   1 QKV projection of x (sums of squares of x on the side); the CTAs of
+//   1 QKV projection of x (sums of squares of x on the side, each head
+//     group from its own K ranges); the CTAs of
 //     each head group (its m-tiles, all K ranges) then wait for one another
 //     on a group counter and finalize the group's q / own k, v: RMS factor,
 //     RoPE, two-term bf16 planes, own k / v to the cache as bf16
@@ -45,13 +51,13 @@ namespace lat {
 
 constexpr int kMkThreads = 384;                 // 12 warps
 constexpr int kMkNW = 6;                        // weight ring slots
-constexpr int kMkNB = 2;                        // activation-plane ring slots
-constexpr int kMkNS = 4;                        // fp32 staging tiles (16 KB each)
+constexpr int kMkNB = 4;                        // activation-plane ring slots
+constexpr int kMkPre = 4;                       // k-tiles of x the math warps hold in flight (registers)
 constexpr int kMkWBytes = 128 * 64 * 2;         // one weight tile
 constexpr int kMkBBytes = 192 * 64 * 2;         // one activation tile, three planes
-constexpr int kMkTile32 = 64 * 64 * 4;          // one fp32 64 x 64 activation tile
-constexpr int kMkRegion = kMkNB * kMkBBytes + kMkNS * kMkTile32;   // also the attention's tiles
-constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 2 * kMkNS + 3;
+constexpr int kMkRegion = 99 * 1024;            // the operand slots, also the attention's tiles
+constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 3;
+static_assert(kMkNB * kMkBBytes <= kMkRegion, "operand slots must fit in the activation region");
 
 __host__ __device__ constexpr int mk_smem_bytes() { return 1024 + kMkNW * kMkWBytes + kMkRegion + 8 * kMkBars + 16; }
 
@@ -220,31 +226,45 @@ __device__ __forceinline__ void mk_grid_sync(unsigned* ctr, unsigned target, Dev
 // Shared state of the math warps.
 struct MkMath {
   uint8_t* sB;
-  uint8_t* sS;
   uint64_t* bfull;
   uint64_t* bempty;
-  uint64_t* sfull;
-  uint64_t* sempty;
   uint64_t* accfull;
   uint64_t* go;
   uint32_t tmem;
   uint32_t bt, gc;
-  uint32_t sph;    // bit i: parity of the next completion of sfull[i]
   int mt;
 };
 
-// Math side of one projection: fp32 activation tiles (staged by the loader) ->
-// exact bf16 planes for the MMA, or nothing when the loader brings the planes
-// themselves; then the split-K epilogue.  `stats` (CTAs of m-tile 0) receives
-// the per-token sums of squares of the activation.
-// Every K range adds its partial sums into `out` (vector reductions at L2).
-__device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool staged, float* stats, float* out,
-                                             int ld, int T_q, DevErr* err, unsigned long long* tr) {
+// Math side of one projection.  Projections of the residual stream x (QKV,
+// gate/up): the math warps load their rows of x straight from global memory,
+// kMkPre k-tiles in flight in registers, and write the exact bf16 planes into
+// the operand slots; for the others (act == nullptr) the loader brings the
+// planes by TMA.  Then the split-K epilogue: every K range adds its partial
+// sums into `out` (vector reductions at L2).  `stats`, when given, receives
+// this K range's per-token sums of squares of x (atomic adds).
+// 16 bytes from global memory through L2 (not L1: other SMs write x), issued
+// where it stands so that several k-tiles are in flight at once
+__device__ __forceinline__ float4 mk_ldcg4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void mk_load_tile(const float* act, int ld, int kt, const int (&rows)[2], int p,
+                                             float4 (&v)[4]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) v[2 * i + hh] = mk_ldcg4(act + (size_t)rows[i] * ld + kt * 64 + hh * 32 + 4 * p);
+}
+
+__device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const float* act, int act_ld, float* stats,
+                                             float* out, int ld, int T_q, DevErr* err, unsigned long long* tr) {
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
   const int nk = r.k1 - r.k0;
   const int mw = s.mt >> 5, lane = s.mt & 31;
-  if (!staged) {   // the loader brings this projection's operand planes by TMA
+  if (!act) {   // the loader brings this projection's operand planes by TMA
     s.bt += nk;
     if (tr) tr[0] = tr[1] = global_ns();
   }
@@ -259,42 +279,47 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool st
     rows[i] = mw * 8 + i + (rq & 1) * 4 + (rq >> 1) * 2;
     sq[i] = 0.f;
   }
-  const bool do_stats = stats != nullptr && r.m == 0;
-  for (int j = 0; j < (staged ? nk : 0); ++j) {
-    const int bi = j % kMkNS;
-    const uint32_t b = s.bt % kMkNB;
-    mk_wait(&s.sfull[bi], (s.sph >> bi) & 1u, err, 30);
-    s.sph ^= 1u << bi;
-    if (j == 0) mk_mark(tr, 0);
-    mk_wait(&s.bempty[b], ((s.bt / kMkNB) & 1) ^ 1, err, 31);
-    const float* src = reinterpret_cast<const float*>(s.sS + bi * kMkTile32);
-    uint8_t* dst = s.sB + b * kMkBBytes;
+  if (act) {
+    float4 xv[kMkPre][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int t = rows[i];
+    for (int u = 0; u < kMkPre; ++u)
+      if (u < nk) mk_load_tile(act, act_ld, r.k0 + u, rows, p, xv[u]);
+    mk_mark(tr, 0);
+    for (int j0 = 0; j0 < nk; j0 += kMkPre) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int col = hh * 32 + 4 * p;
-        const float4 v = *reinterpret_cast<const float4*>(src + t * 64 + col);
-        if (do_stats) sq[i] += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-        uint32_t h0, m0, l0, h1, m1, l1;
-        split_pair_exact(v.x, v.y, h0, m0, l0);
-        split_pair_exact(v.z, v.w, h1, m1, l1);
-        const uint32_t off = (uint32_t)(t * 128 + ((((col >> 3) ^ t) & 7) << 4) + ((p & 1) << 3));
-        *reinterpret_cast<uint2*>(dst + off) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(m0, m1);
-        *reinterpret_cast<uint2*>(dst + 16384 + off) = make_uint2(l0, l1);
+      for (int u = 0; u < kMkPre; ++u) {
+        const int j = j0 + u;
+        if (j < nk) {
+          const uint32_t b = s.bt % kMkNB;
+          mk_wait(&s.bempty[b], ((s.bt / kMkNB) & 1) ^ 1, err, 31);
+          uint8_t* dst = s.sB + b * kMkBBytes;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int t = rows[i];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int col = hh * 32 + 4 * p;
+              const float4 v = xv[u][2 * i + hh];
+              if (stats) sq[i] += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+              uint32_t h0, m0, l0, h1, m1, l1;
+              split_pair_exact(v.x, v.y, h0, m0, l0);
+              split_pair_exact(v.z, v.w, h1, m1, l1);
+              const uint32_t off = (uint32_t)(t * 128 + ((((col >> 3) ^ t) & 7) << 4) + ((p & 1) << 3));
+              *reinterpret_cast<uint2*>(dst + off) = make_uint2(h0, h1);
+              *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(m0, m1);
+              *reinterpret_cast<uint2*>(dst + 16384 + off) = make_uint2(l0, l1);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.bfull[b]);   // this warp's rows of the operand are written
+          ++s.bt;
+          if (j + kMkPre < nk) mk_load_tile(act, act_ld, r.k0 + j + kMkPre, rows, p, xv[u]);
+        }
       }
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&s.sempty[bi]);   // this warp is done with the staging tile
-      mbar_arrive(&s.bfull[b]);     // and its rows of the operand are written
-    }
-    ++s.bt;
   }
-  if (do_stats) {
+  if (stats) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float v = sq[i];
@@ -306,7 +331,7 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, bool st
   }
   // epilogue: warp (4 + mw) reads TMEM lanes 32 (mw % 4) .. +31 = output rows,
   // tokens 32 (mw / 4) .. +31 of each plane; the planes are summed hi + mid + lo
-  if (staged) mk_mark(tr, 1);
+  if (act) mk_mark(tr, 1);
   mk_wait(s.accfull, s.gc & 1, err, 32);
   mk_mark(tr, 2);
   tc_fence_after();
@@ -417,20 +442,24 @@ __device__ __forceinline__ void mk_qkv_finalize_group(const MkArgs& a, int h0, i
 constexpr int kCntQkvArr = 0;      // [32] QKV head groups: CTAs past their epilogue
 constexpr int kCntGuArr = 32;      // [192] gate/up tiles: CTAs past their epilogue
 constexpr int kCntWords = 224;
+// Per-token sums of squares of the projection input (MkArgs::ss), one row of
+// 64 per QKV head group, then one per gate/up tile: each group's own K ranges
+// add into its row, so a group needs no other group's statistics.
+constexpr int kSsQkv = 0;
+constexpr int kSsGu = 32;
+constexpr int kSsRows = 224;
 
 // Count this CTA into group counter `cnt`, then wait until the group has all
-// `target` arrivals and group counter `cnt0` too (the group whose CTAs add the
-// sums of squares of x).  Bounded: gives up (error recorded) after the spin
-// budget or when another CTA has failed.  The counters grow by one group's
-// arrivals per block and start at 0 with each launch.
-__device__ __forceinline__ void mk_group_wait(unsigned* cnt, const unsigned* cnt0, unsigned target, DevErr* err,
-                                              unsigned where, int mt) {
+// `target` arrivals.  Bounded: gives up (error recorded) after the spin budget
+// or when another CTA has failed.  The counters grow by one group's arrivals
+// per block and start at 0 with each launch.
+__device__ __forceinline__ void mk_group_wait(unsigned* cnt, unsigned target, DevErr* err, unsigned where, int mt) {
   __threadfence();   // this thread's reductions are performed before the arrival
   named_sync(2, 256);
   if (mt == 0) {
     atomicAdd(cnt, 1u);
     const long long t0 = clock64();
-    for (int i = 0; ld_acquire_u32(cnt) < target || ld_acquire_u32(cnt0) < target; ++i)
+    for (int i = 0; ld_acquire_u32(cnt) < target; ++i)
       if ((i & 15) == 15 && (mk_aborted(err) || clock64() - t0 > kSpinBudget)) {
         if (!mk_aborted(err)) record_error(err, 2u, where);
         break;
@@ -444,18 +473,23 @@ __device__ __forceinline__ void mk_group_wait(unsigned* cnt, const unsigned* cnt
 // heads, all K ranges) waits for the group, then finalizes its share of the
 // group's heads.  `lr` = block index within the launch.
 template <int DH>
-__device__ __forceinline__ void mk_qkv_arrive(const MkArgs& a, int lr, const float* ss1, __nv_bfloat16* kc,
-                                              __nv_bfloat16* vc, float invD, int mt) {
+struct MkQkvGroups {
+  static constexpr int MPG = DH >= 128 ? DH / 128 : 1;   // m-tiles per group
+  static constexpr int HPG = DH >= 128 ? 1 : 128 / DH;   // heads per group
+};
+
+template <int DH>
+__device__ __forceinline__ void mk_qkv_arrive(const MkArgs& a, int lr, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                                              float invD, int mt) {
   const MkGemm& g = a.g[0];
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
-  constexpr int MPG = DH >= 128 ? DH / 128 : 1;   // m-tiles per group
-  constexpr int HPG = DH >= 128 ? 1 : 128 / DH;   // heads per group
+  constexpr int MPG = MkQkvGroups<DH>::MPG, HPG = MkQkvGroups<DH>::HPG;
   const int grp = r.m / MPG;
   const int per = MPG * g.splits;
   const int part = (r.m % MPG) * g.splits + (int)blockIdx.x / g.MT;
-  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, a.grp_cnt + kCntQkvArr, (unsigned)((lr + 1) * per), a.err, 901, mt);
-  mk_qkv_finalize_group<DH>(a, grp * HPG, HPG, part, per, ss1, kc, vc, invD, mt);
+  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, (unsigned)((lr + 1) * per), a.err, 901, mt);
+  mk_qkv_finalize_group<DH>(a, grp * HPG, HPG, part, per, a.ss + (kSsQkv + grp) * 64, kc, vc, invD, mt);
 }
 
 // Phase 3: attention of the chunk over [cache | own], one (head, 32-key block)
@@ -858,36 +892,32 @@ __device__ __forceinline__ void mk_geglu_tile(const MkArgs& a, int m, int part, 
 
 // After the gate/up epilogue: every CTA of a tile (all K ranges) waits for
 // the tile, then writes its share of the tile's GeGLU planes.
-__device__ __forceinline__ void mk_gu_arrive(const MkArgs& a, int lr, const float* ss2, float invD, int mt) {
+__device__ __forceinline__ void mk_gu_arrive(const MkArgs& a, int lr, float invD, int mt) {
   const MkGemm& g = a.g[2];
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
-  unsigned* cnt = a.grp_cnt + kCntGuArr;
-  mk_group_wait(cnt + r.m, cnt, (unsigned)((lr + 1) * g.splits), a.err, 902, mt);
-  mk_geglu_tile(a, r.m, (int)blockIdx.x / g.MT, g.splits, ss2, invD, mt);
+  mk_group_wait(a.grp_cnt + kCntGuArr + r.m, (unsigned)((lr + 1) * g.splits), a.err, 902, mt);
+  mk_geglu_tile(a, r.m, (int)blockIdx.x / g.MT, g.splits, a.ss + (kSsGu + r.m) * 64, invD, mt);
 }
 
 template <int DH>
 __global__ void __launch_bounds__(kMkThreads, 1)
     pi0_step_kernel(const __grid_constant__ CUtensorMap w_qkv, const __grid_constant__ CUtensorMap w_o,
                     const __grid_constant__ CUtensorMap w_gu, const __grid_constant__ CUtensorMap w_d,
-                    const __grid_constant__ CUtensorMap act_x, const __grid_constant__ CUtensorMap act_op,
-                    const __grid_constant__ CUtensorMap act_hp, const MkArgs a) {
+                    const __grid_constant__ CUtensorMap act_op, const __grid_constant__ CUtensorMap act_hp,
+                    const MkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sW = smem;
   uint8_t* sR = smem + kMkNW * kMkWBytes;
   uint8_t* sB = sR;
-  uint8_t* sS = sR + kMkNB * kMkBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kMkRegion);
   uint64_t* wfull = bars;                  // weight tile landed
   uint64_t* wempty = wfull + kMkNW;        // weight slot free (MMA done)
   uint64_t* bfull = wempty + kMkNW;        // operand tile built by the math warps (8 arrivals)
   uint64_t* bfullt = bfull + kMkNB;        // operand tile landed by TMA (O and down projections)
   uint64_t* bempty = bfullt + kMkNB;       // operand slot free (MMA done)
-  uint64_t* sfull = bempty + kMkNB;        // staging tile landed
-  uint64_t* sempty = sfull + kMkNS;        // staging tile read by all math warps (8 arrivals)
-  uint64_t* accfull = sempty + kMkNS;      // accumulator complete
+  uint64_t* accfull = bempty + kMkNB;      // accumulator complete
   uint64_t* mdone = accfull + 1;           // every MMA complete (teardown)
   uint64_t* go = mdone + 1;                // grid barrier passed before a projection phase
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(go + 1);
@@ -902,10 +932,6 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       mbar_init(&bfull[i], 8);
       mbar_init(&bfullt[i], 1);
       mbar_init(&bempty[i], 1);
-    }
-    for (int i = 0; i < kMkNS; ++i) {
-      mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 8);
     }
     mbar_init(accfull, 1);
     mbar_init(mdone, 1);
@@ -992,16 +1018,13 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       mbar_wait(mdone, 0, nullptr, 0);
     } else if (warp == 2 && lane == 0) {
       // ---------------- activation loader ----------------
-      // after each grid barrier that opens a projection phase: fp32 activation
-      // tiles into the staging slots (refilled as the math warps release them),
-      // or, for the output projection, the operand planes straight into the
-      // operand slots
-      tma_prefetch_desc(&act_x);
+      // after each grid barrier that opens the output or the down projection:
+      // the operand planes straight into the operand slots (the math warps
+      // build the QKV and gate/up operands from x themselves)
       tma_prefetch_desc(&act_op);
       tma_prefetch_desc(&act_hp);
       const uint64_t pol = l2_policy_evict_last();
       uint32_t bt = 0, gop = 0;
-      uint32_t sfill[kMkNS] = {};   // copies issued into each staging tile so far
       uint32_t bout = 0;            // operand copies issued, by slot (bit)
       uint32_t pt = 0;              // per-slot parity of bfullt
       bool ok = true;
@@ -1032,25 +1055,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
               pt ^= 1u << b;
               ++bt;
             }
-          } else {                    // fp32 tiles of x into the staging slots
-            for (int j = 0; j < nk; ++j) {
-              const int bi = j % kMkNS;
-              if (sfill[bi] > 0 && !mk_wait(&sempty[bi], (sfill[bi] - 1) & 1, a.err, 42)) {
-                ok = false;
-                break;
-              }
-              fence_proxy_async_smem();   // the math warps' reads of the tile precede the copy
-              mbar_arrive_expect_tx(&sfull[bi], kMkTile32);
-              tma_load_2d(sS + bi * kMkTile32, &act_x, &sfull[bi], (r.k0 + j) * 64, 0, pol);
-              ++sfill[bi];
-            }
+          } else {                    // built by the math warps
             bt += nk;
           }
         }
-      // never leave a copy in flight: the last fill of every staging tile and
-      // every operand copy have landed
-      for (int i = 0; i < kMkNS; ++i)
-        if (sfill[i] > 0) mbar_wait(&sfull[i], (sfill[i] - 1) & 1, nullptr, 0);
+      // never leave a copy in flight: every operand copy has landed
       for (int i = 0; i < kMkNB; ++i)
         if ((bout >> i) & 1u) mbar_wait(&bfullt[i], ((pt >> i) & 1u) ^ 1u, nullptr, 0);
     }
@@ -1059,16 +1068,12 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     // ---------------- math warps ----------------
     MkMath s;
     s.sB = sB;
-    s.sS = sS;
     s.bfull = bfull;
     s.bempty = bempty;
-    s.sfull = sfull;
-    s.sempty = sempty;
     s.accfull = accfull;
     s.go = go;
     s.tmem = tmem;
     s.bt = s.gc = 0;
-    s.sph = 0;
     s.mt = threadIdx.x - 128;
     const int mt = s.mt;
     const unsigned G = gridDim.x;
@@ -1076,8 +1081,6 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     const float invD = 1.f / (float)a.D;
     const int kvd = a.Hkv * DH;
     for (int l = a.l0; l < a.l1; ++l) {
-      float* ss1 = a.ss + (size_t)l * 128;
-      float* ss2 = ss1 + 64;
       __nv_bfloat16* kc = a.kv + (size_t)(l - a.l0) * a.kv_stride;
       __nv_bfloat16* vc = kc + (size_t)a.T_kv * kvd;
       unsigned long long* tr =
@@ -1098,21 +1101,30 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           mk_attention<DH>(a, kc, vc, sR, mt, tr);
         } else if (ph == 3) {
           mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR), tr);
-          // the QKV sums of the next block start from zero (every finalizer of
-          // this block is done before the barrier that opened phase 2)
+          // the QKV sums and statistics of the next block start from zero
+          // (every finalizer of this block is done before the barrier that
+          // opened phase 2)
           mk_zero_f4(a.qkv, 16 * a.nqkv, mt);
+          mk_zero_f4(a.ss + kSsQkv * 64, 16 * (kSsGu - kSsQkv), mt);
         } else {
           const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
           float* out = ph == 0 ? a.qkv : ph == 5 ? a.gu : a.x;
           const int ld = ph == 0 ? a.nqkv : ph == 5 ? 2 * a.F : a.D;
-          float* stats = ph == 0 ? ss1 : ph == 5 ? ss2 : nullptr;
-          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5, stats, out, ld, a.T_q, a.err,
+          const MkRange r = mk_range(a.g[gi], blockIdx.x);
+          float* stats = nullptr;   // this K range's sums of squares of x, into its group's row
+          if (ph == 0 && r.m % MkQkvGroups<DH>::MPG == 0) stats = a.ss + (kSsQkv + r.m / MkQkvGroups<DH>::MPG) * 64;
+          if (ph == 5) stats = a.ss + (kSsGu + r.m) * 64;
+          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5 ? a.x : nullptr, a.D, stats, out, ld, a.T_q, a.err,
                        tr ? tr + 20 + 4 * gi : nullptr);
-          if (ph == 0) mk_qkv_arrive<DH>(a, lr, ss1, kc, vc, invD, mt);
-          if (ph == 5) mk_gu_arrive(a, lr, ss2, invD, mt);
-          // the gate/up sums of the next block start from zero (every GeGLU
-          // tile of this block was written before the barrier that opened phase 7)
-          if (ph == 7) mk_zero_f4(a.gu, 32 * a.F, mt);
+          if (ph == 0) mk_qkv_arrive<DH>(a, lr, kc, vc, invD, mt);
+          if (ph == 5) mk_gu_arrive(a, lr, invD, mt);
+          // the gate/up sums and statistics of the next block start from zero
+          // (every GeGLU tile of this block was written before the barrier that
+          // opened phase 7)
+          if (ph == 7) {
+            mk_zero_f4(a.gu, 32 * a.F, mt);
+            mk_zero_f4(a.ss + kSsGu * 64, 16 * (kSsRows - kSsGu), mt);
+          }
         }
         mk_mark(tr, 2 * ph + 2);
       }
