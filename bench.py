@@ -9,8 +9,14 @@ denoised chunk (lower is better); microseconds per block and tokens/s are
 reported alongside.  Every step streams all 623 MB of folded block weights
 from HBM (L2 is 129 MB), so no flush is needed between steps.
 
+The headline line also carries config.dense: every dense configuration
+(prefix prefill B = 1 / 8, the DiT 1.3B stage, its interleaved schedule, the
+DiT 14B block with 1 / 4 / 8 chunks) timed with CUDA events in the same run,
+with its useful TFLOP/s against the measured bf16 peak (--no-dense skips it).
+
 --impl reference times the CPU oracle (float64 numpy) on the same workload on
-the host cores; under torchrun only rank 0 runs it.
+the host cores, one whole denoise step per step; under torchrun only rank 0
+runs it.
 Multi-GPU: replicas only (one independent chunk per GPU per step, no
 collective on the data path); value = whole-job chunks per step time.
 """
@@ -28,10 +34,10 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD = "pi0_ae"
 PAGES_AE_MS = 11.001   # pages' action-expert time, 2 views, RTX 4090 (context)
-# DRAM bytes (read + write) of one step-kernel launch from the ncu capture in
-# profiles/pi0_step_kernel_pi0_ae.md (640.13 MB read + 4.30 MB written); set to
-# None whenever the kernel changes after that capture
-STEP_TRAFFIC = 644429056
+# DRAM bytes (read + write) of one step-kernel launch from the last ncu capture
+# of the kernel as it stands (dram__bytes_read.sum + dram__bytes_write.sum);
+# None when the kernel has changed since
+STEP_TRAFFIC = None
 
 
 def parse():
@@ -41,6 +47,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-dense", action="store_true",
+                   help="skip timing the dense configurations in the headline run")
     p.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "pi0_cycle"] + list(DENSE_WORKLOADS),
                    help="pi0_ae (default: the headline line) or one dense configuration")
     return p.parse_args()
@@ -162,51 +170,56 @@ def cpu_baseline(cfg, wb, ib):
 
 
 def run_reference(args):
+    """The oracle as it stands on the host cores: every step is one whole
+    denoise step of the chunk (state row + embedding, all 18 blocks, head and
+    Euler update), steps cycling through the chunk's 10 denoise steps and
+    starting a new chunk after the last; ms_per_step x steps is the timed time
+    and the value, ms per chunk, is ms_per_step x 10."""
     rank, _, world = dist_info()
     if rank != 0:
         return
     from latency_transformer_block_gb300 import synth
-    from oracle import pi0
+    from oracle import bf16, pi0
     cfg = synth.config(WORKLOAD)
     wb = synth.pi0_weights(cfg, 0)
     ib = synth.pi0_inputs(cfg, 0)
-    # one step = one block at one denoise step (a bounded sample); scaled to a chunk
-    blk = pi0.method_block(pi0.decode_tree(wb["blocks"][0]))
+    blocks = [pi0.method_block(pi0.decode_tree(b)) for b in wb["blocks"]]
     W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
-    from oracle import bf16
-    kv = bf16.decode(ib["kv"][0])
-    Tp, Tq = cfg["T_prefix"], cfg["T_q"]
+    kv = bf16.decode(ib["kv"])
+    Tp, Tq, S, L, D = cfg["T_prefix"], cfg["T_q"], cfg["S"], cfg["L"], cfg["D"]
     pos = Tp + np.arange(Tq)
-    x = ib["noise"].astype(np.float64)
+    times = pi0.times(cfg)
     st = pi0.state_token(ib["state"].astype(np.float64), W)
-    h = np.vstack([st[None, :], pi0.embed(x, 0.0, W, cfg["D"])])
+    state = {"x": ib["noise"].astype(np.float64), "s": 0}
 
     def one():
-        pi0.block(h, kv[0, :Tp], kv[1, :Tp], pos, blk, cfg)
+        s = state["s"]
+        x = state["x"] if s > 0 else ib["noise"].astype(np.float64)
+        h = np.vstack([st[None, :], pi0.embed(x, times[s], W, D)])
+        for l in range(L):
+            h, _, _ = pi0.block(h, kv[l, 0, :Tp], kv[l, 1, :Tp], pos, blocks[l], cfg)
+        state["x"] = x + (1.0 / S) * pi0.head(h[1:], W, cfg["eps"])
+        state["s"] = (s + 1) % S
 
     for _ in range(args.warmup):
         one()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one()
-    per_block = (time.perf_counter() - t0) * 1e3 / args.steps
-    t1 = time.perf_counter()
-    for _ in range(3):
-        pi0.embed(x, 0.0, W, cfg["D"])
-        pi0.head(h[1:], W, cfg["eps"])
-    per_embed_head = (time.perf_counter() - t1) * 1e3 / 3
-    value = per_block * cfg["L"] * cfg["S"] + per_embed_head * cfg["S"]
+    ms_step = (time.perf_counter() - t0) * 1e3 / args.steps
+    value = ms_step * S
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
     line = {
         "impl": "reference", "metric": "ms per denoised chunk", "value": round(value, 3), "unit": "ms",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value, 3),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) bf16 weights)",
-        "config": {"workload": WORKLOAD, "blocks": cfg["L"], "steps": cfg["S"], "tokens": cfg["T_q"],
-                   "prefix_kv": cfg["T_prefix"], "us_per_block": round(per_block * 1e3, 1)},
+        "config": {"workload": WORKLOAD, "blocks": L, "steps": S, "tokens": Tq, "prefix_kv": Tp,
+                   "step_unit": "one denoise step of the chunk (18 blocks + embedding + head); value = 10 steps",
+                   "us_per_block": round(ms_step * 1e3 / L, 1)},
         "cpu_baseline": {"value": round(value, 3), "unit": "ms", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} timed block-steps (block 0, step 0) + embedding/head, "
-                                   f"scaled x{cfg['L'] * cfg['S']} to one chunk"},
+                         "sample": f"{args.steps} timed denoise steps of pi0_ae chunks (each 18 blocks + "
+                                   f"embedding + head, float64 numpy), x{S} per chunk"},
         "e2e": {"value": round(value, 3), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -347,6 +360,16 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(h_out.numel() * 4)},
         "gpu_launches": launches_per_chunk * args.steps,
     }
+    if rank == 0 and not args.no_dense:
+        # the dense configurations, each timed with CUDA events in this same run
+        # (one model at a time; device memory freed in between)
+        del m, kv
+        torch.cuda.empty_cache()
+        line["config"]["dense"] = {}
+        for name in DENSE_WORKLOADS:
+            r = dense_measure(name, max(3, min(args.steps, 10)), 3, dev)
+            line["config"]["dense"][name] = r["summary"]
+            torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, wb, ib)
     if rank == 0:
@@ -375,25 +398,42 @@ def dense_flops(cfg, nb, descs=None):
     return 2 * macs * L
 
 
-def run_dense(args):
+def device_weights(make, cfg, dev, seed=0):
+    """Synthetic weights of the architecture for timing only, drawn on the
+    device with the generator's layout and distributions (N(0, 0.02) bf16,
+    norm scales 1 + N(0, 0.02)): the host generator would spend minutes on the
+    gigabytes of prefix and DiT weights.  Parity runs use the host generator."""
     import torch
-    rank, local_rank, world = dist_info()
-    if rank != 0:
-        return
-    name, nb, metric, unit = DENSE_WORKLOADS[args.workload]
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
+    tmpl = make(dict(cfg, L=1), seed)          # one block: names and shapes
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def draw(name, a):
+        t = torch.randn(a.shape, generator=g, device=dev) * 0.02
+        if name.startswith("g_"):
+            t += 1.0
+        return t.to(torch.bfloat16)
+    out = {k: draw(k, v) for k, v in tmpl.items() if k != "blocks"}
+    blk = tmpl["blocks"][0]
+    out["blocks"] = [{k: draw(k, v) for k, v in blk.items()} for _ in range(cfg["L"])]
+    return out
+
+
+def dense_measure(workload, steps, warmup, dev):
+    """Time one dense configuration (CUDA events on its stream) and the dense
+    GEMM alone on its FFN-in projection; returns the full line and a summary."""
+    import torch
     from latency_transformer_block_gb300 import build as B
     B.build()
     from latency_transformer_block_gb300 import synth
     from latency_transformer_block_gb300.models import DitStage, Pi0Prefix
-
+    name, nb, metric, unit = DENSE_WORKLOADS[workload]
     cfg = synth.config(name)
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     stream = torch.cuda.Stream(dev)
     if cfg["kind"] == "prefill":
-        m = Pi0Prefix(cfg, synth.prefill_weights(cfg, 0), max_batch=nb, device=dev)
+        m = Pi0Prefix(cfg, device_weights(synth.prefill_weights, cfg, dev), max_batch=nb, device=dev)
         pe = torch.randn(nb, cfg["T_prefix"], cfg["patch_dim"], generator=gen, device=dev).to(torch.bfloat16)
         kv = m.new_kv(nb)
         flops = dense_flops(cfg, nb)
@@ -403,8 +443,8 @@ def run_dense(args):
         def step():
             m.prefill(pe, kv, stream)
         blocks = cfg["L"]
-    elif args.workload.endswith("_pipeline"):
-        m = DitStage(cfg, synth.dit_weights(cfg, 0), max_batch=nb, n_streams=1, device=dev)
+    elif workload.endswith("_pipeline"):
+        m = DitStage(cfg, device_weights(synth.dit_weights, cfg, dev), max_batch=nb, n_streams=1, device=dev)
         ring = torch.randn(1, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
                            generator=gen, device=dev).to(torch.bfloat16)
         noise = torch.randn(cfg["T_chunk"], cfg["lat_dim"], generator=gen, device=dev)
@@ -424,7 +464,8 @@ def run_dense(args):
     else:
         descs = synth.dit_chunk_descs(cfg, nb)
         streams = (nb + cfg["S"] - 1) // cfg["S"]
-        m = DitStage(cfg, synth.dit_weights(cfg, 0), max_batch=nb, n_streams=streams, device=dev)
+        m = DitStage(cfg, device_weights(synth.dit_weights, cfg, dev), max_batch=nb, n_streams=streams,
+                     device=dev)
         ring = torch.randn(streams, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
                            generator=gen, device=dev).to(torch.bfloat16)
         x = torch.randn(nb, cfg["T_chunk"], cfg["D"], generator=gen, device=dev)
@@ -439,23 +480,23 @@ def run_dense(args):
                 m.block(l, x, descs, ring, stream)
         blocks = cfg["L"]
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
+        for _ in range(max(3, warmup)):
             step()
     stream.synchronize()
     m.ctx.sync()
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         e1.record(stream)
     stream.synchronize()
     clk = clocks.stop()
     m.ctx.sync()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     peak_gbs, peak_tf, peak_src = measured_peaks()
     tflops = flops / (ms * 1e-3) / 1e12
     # dominant kernel alone: the dense tcgen05 GEMM on the FFN-in projection with
@@ -478,11 +519,11 @@ def run_dense(args):
     g_useful = 2.0 * rows * ffn_n * ffn_k / (g_us * 1e-6) / 1e12
     value = ms if unit == "ms" else ms * 1e3 / blocks
     line = {
-        "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
+        "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) inputs and history, N(0,0.02) bf16 weights)",
-        "config": {"workload": args.workload, "batch": nb, "blocks": blocks,
+        "data": "synthetic (seeded N(0,1) inputs and history, N(0,0.02) bf16 weights drawn on the device)",
+        "config": {"workload": workload, "batch": nb, "blocks": blocks,
                    "us_per_block": round(ms * 1e3 / blocks, 2), "useful_tflop_per_step": round(flops / 1e12, 3),
                    "path_tflops": round(tflops, 1), "path_frac": round(tflops / peak_tf, 4),
                    "l2": "inputs larger than L2 (weights and KV streamed per step)"},
@@ -493,7 +534,25 @@ def run_dense(args):
                      "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS)"},
         "clocks": clk, "e2e": None, "gpu_launches": None,
     }
-    print(json.dumps(line), flush=True)
+    summary = {"metric": metric, "value": round(value, 4), "unit": unit, "ms_per_step": round(ms, 4),
+               "steps": steps, "us_per_block": round(ms * 1e3 / blocks, 2),
+               "useful_tflops": round(tflops, 1), "path_frac_of_bf16_peak": round(tflops / peak_tf, 4),
+               "ffn_in_gemm_useful_tflops": round(g_useful, 1),
+               "ffn_in_gemm_frac": round(g_useful / peak_tf, 4), "sm_mhz": clk.get("sm_mhz"),
+               "clock_reasons": clk.get("reasons")}
+    del m
+    return {"line": line, "summary": summary}
+
+
+def run_dense(args):
+    rank, local_rank, world = dist_info()
+    if rank != 0:
+        return
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    r = dense_measure(args.workload, args.steps, args.warmup, dev)
+    print(json.dumps(r["line"]), flush=True)
 
 
 def run_cycle(args):

@@ -174,6 +174,13 @@ lat_status lat_prefill_kv(lat_ctx *ctx, const void *patch_emb, int B, void *kv, 
 
 /*
  * lat_block_forward -- one block, in place on the residual stream.
+ * Defined by: for the pi0 models, the reading note's Fig. 4 (a pre-norm block
+ * of the action expert over [prefix KV | own tokens]) with the folds of its
+ * section 4; for LAT_DIT, the PhysisServe article's stage, "one transformer
+ * block at one denoise step", where a chunk reads the noisy KV that earlier
+ * chunks left at the same step and chunks of the same block at different
+ * steps are merged into one batch (its sections on the stage cut and on one
+ * GPU serving several stages).
  *  LAT_PI0_ACTION_EXPERT / LAT_PI0_PREFIX (chunks = NULL, n = 1):
  *    x:  device fp32 [T_q][D] (action expert) -- query tokens at positions
  *        T_prefix + j;
@@ -192,6 +199,11 @@ lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_
 
 /*
  * lat_denoise_chunk -- LAT_PI0_ACTION_EXPERT: the full S-step x L-block loop.
+ * Defined by: the reading note's section 2 (the expert reuses the prefix KV
+ * cache over 10 flow-matching steps of 18 blocks each, 63 action + 1 state
+ * token), section 4.2 (the time embedding folded into a per-step table) and
+ * section 3 (the loop replayed as one captured CUDA graph); each step ends in
+ * the Euler update x <- x + dt * v.
  *  kv:    device bf16 [L][2][T_prefix + T_q][Hkv*dh] (slots >= T_prefix are
  *         overwritten with the query tokens' K/V at every step);
  *  state: device fp32 [act_dim];
@@ -344,8 +356,14 @@ lat_status lat_debug_attention(lat_ctx *ctx, const float *q, const void *k, cons
  *  out: device fp32 [T_q][Hq*dh].  dh in {64, 128, 256}.
  * Limit: Hq * T_q * (dh + 2) <= 1048576 (one key range of partials), else
  * LAT_ERR_SHAPE; larger T_kv only means fewer, longer key ranges.
+ * Speed: the keys are split into as many ranges as the array holds partials
+ * for (at most 32, one per 32-key block at least), where a context's
+ * attention sizes its ranges by the SM count; at shapes where the array holds
+ * fewer ranges the call runs on fewer CTAs and is slower than the context's.
  * The first call on a device (with that device current) looks up the array's
- * device address and sets the kernels' shared-memory limit; make that first
+ * device address and sets the kernels' shared-memory limit, and so does the
+ * first call after the device's context changed (e.g. after cudaDeviceReset,
+ * which unloads the library's module); make that first
  * call before any stream capture.  Every call shares the one array: calls that
  * overlap on the GPU (different streams, or different host threads) race on
  * it and must be serialised by the caller.  Nothing in it needs clearing: a
@@ -372,6 +390,22 @@ lat_status lat_clear_error(lat_ctx *ctx);
  * The next lat_sync returns LAT_ERR_TIMEOUT; no GPU fault is involved.
  */
 lat_status lat_debug_timeout(lat_ctx *ctx, void *stream);
+
+/*
+ * lat_debug_wait_skew -- failure-detection check of the persistent step
+ * kernel's own bounded waits (action-expert contexts).  From the next launch
+ * on, one wait of the launch's first block expects `extra` more arrivals than
+ * will ever come: which = 1 the first grid barrier (between the QKV and the
+ * attention phase), 2 the first QKV head-group wait, 3 the first gate/up tile
+ * wait; which = 0 or extra = 0 switches it off.  The wait gives up after the
+ * spin budget (~0.5 s) and records LAT_ERR_TIMEOUT; every later wait of the
+ * launch sees the error and returns at once, the launch runs to its end with
+ * meaningless results and leaves no copy in flight.  The next lat_sync
+ * reports the timeout; after lat_clear_error (and the skew switched off) the
+ * context computes correct results again.  No GPU fault is involved.
+ * Captured denoise graphs are dropped (they hold the old arguments).
+ */
+lat_status lat_debug_wait_skew(lat_ctx *ctx, int which, int extra);
 
 /* Human-readable name of a status; message of the last failure on this thread. */
 const char *lat_status_str(lat_status s);

@@ -680,27 +680,36 @@ static inline int seg_attn_smem_bytes(int dh, int kb) { return 4 * kb * (dh + 8)
 // chunk attention: K and V blocks in two planes each, plus the partial scores
 static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
+// Each attribute call's own status (the first failure), so that an error an
+// earlier, unrelated launch left behind is neither reported here nor cleared.
 static inline cudaError_t set_attention_smem_limits() {
-  cudaFuncSetAttribute(attention_seg_kernel<256, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       seg_attn_smem_bytes(256, 32));
-  cudaFuncSetAttribute(attention_seg_kernel<256, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       seg_attn_smem_bytes(256, 64));
-  cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(64));
-  cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(128));
-  cudaFuncSetAttribute(attention_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_attn_smem_bytes(256));
-  return cudaGetLastError();
+  const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attention_seg_kernel<256, 32>, A, seg_attn_smem_bytes(256, 32))) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(attention_seg_kernel<256, 64>, A, seg_attn_smem_bytes(256, 64))) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(attention_kernel<64>, A, chunk_attn_smem_bytes(64))) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(attention_kernel<128>, A, chunk_attn_smem_bytes(128))) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attention_kernel<256>, A, chunk_attn_smem_bytes(256));
 }
 
+// Launches report their own status (cudaLaunchKernelEx), not the sticky last
+// error of the thread.
 static inline cudaError_t launch_chunk_attention(const AttnArgs& a, int dh, cudaStream_t st) {
-  dim3 grid(a.Hq, (a.T_q + 63) / 64, a.n_split);
-  const int smem = chunk_attn_smem_bytes(dh);
-  if (dh == 64) attention_kernel<64><<<grid, 256, smem, st>>>(a);
-  else if (dh == 128) attention_kernel<128><<<grid, 256, smem, st>>>(a);
-  else attention_kernel<256><<<grid, 256, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hq, (a.T_q + 63) / 64, a.n_split);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = chunk_attn_smem_bytes(dh);
+  cfg.stream = st;
+  cudaError_t e;
+  if (dh == 64) e = cudaLaunchKernelEx(&cfg, attention_kernel<64>, a);
+  else if (dh == 128) e = cudaLaunchKernelEx(&cfg, attention_kernel<128>, a);
+  else e = cudaLaunchKernelEx(&cfg, attention_kernel<256>, a);
   if (e != cudaSuccess || a.n_split == 1) return e;
-  attention_combine_kernel<<<dim3(a.T_q, a.Hq), dh, 0, st>>>(a, dh, nullptr);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3(a.T_q, a.Hq);
+  cc.blockDim = dim3(dh);
+  cc.stream = st;
+  return cudaLaunchKernelEx(&cc, attention_combine_kernel, a, dh, (__nv_bfloat16*)nullptr);
 }
 
 }  // namespace lat

@@ -1612,6 +1612,16 @@ lat_status lat_clear_error(lat_ctx* c) {
   return LAT_OK;
 }
 
+lat_status lat_debug_wait_skew(lat_ctx* c, int which, int extra) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  if (c->d.kind != LAT_PI0_ACTION_EXPERT) return fail(LAT_ERR_STATE, "wait skew: action-expert contexts only");
+  if (which < 0 || which > 3 || extra < 0) return fail(LAT_ERR_ARG, "which must be 0..3 and extra >= 0");
+  c->mk.skew_where = extra > 0 ? which : 0;
+  c->mk.skew = which > 0 ? (unsigned)extra : 0u;
+  c->drop_graphs();   // the captured graphs hold the old arguments
+  return LAT_OK;
+}
+
 lat_status lat_debug_timeout(lat_ctx* c, void* stream) {
   if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
   debug_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(c->err, 999);

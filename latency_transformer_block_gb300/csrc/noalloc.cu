@@ -12,6 +12,7 @@
 //
 // The array is part of the library image: every GPU that loads liblat.so holds
 // it (4 MiB) until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -30,15 +31,47 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-// Device address of g_noalloc_scratch, per device.  In host code the symbol
-// name is only a host-side stand-in; a kernel must be given the address that
-// cudaGetSymbolAddress returns with the device current.
+// Device address of g_noalloc_scratch, per device, and the id of the device
+// context it was looked up in.  In host code the symbol name is only a
+// host-side stand-in; a kernel must be given the address that
+// cudaGetSymbolAddress returns with the device current.  A new context on the
+// device (after cudaDeviceReset the module is loaded again, at a new address,
+// and the kernels' shared-memory limits are back at their defaults) repeats
+// the set-up.
 float* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};
 std::mutex g_setup_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// id of the current device context (0 if the driver cannot tell)
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    looked = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur && get_id && get_cur(&c) == CUDA_SUCCESS && c && get_id(c, &id) == CUDA_SUCCESS) return id;
+  return 0;
+}
 
 lat_status setup_device(int dev, float** out) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_addr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (!g_scratch_addr[dev] || id != g_ctx_id[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
@@ -46,6 +79,7 @@ lat_status setup_device(int dev, float** out) {
     e = lat::set_attention_smem_limits();
     if (e != cudaSuccess) return lat_internal_fail(LAT_ERR_CUDA, "cudaFuncSetAttribute(attention) failed");
     g_scratch_addr[dev] = static_cast<float*>(p);
+    g_ctx_id[dev] = id;
   }
   *out = g_scratch_addr[dev];
   return LAT_OK;
@@ -75,6 +109,9 @@ extern "C" lat_status lat_chunk_attention_noalloc(const float* q, const void* k,
   lat_status s = setup_device(dev, &scratch);
   if (s != LAT_OK) return s;
 
+  // as many key ranges as the array holds partials for (at most 32, at most
+  // one per 32-key block); a context sizes its ranges by the SM count instead,
+  // so at shapes where the array holds fewer ranges this call has fewer CTAs
   const int nkb = lat::attn_key_blocks(T_kv);
   int n_split = (int)(kNoAllocScratchFloats / per_split);
   if (n_split > nkb) n_split = nkb;

@@ -111,6 +111,10 @@ struct MkArgs {
   unsigned* bar;            // grid barrier counter (0 at entry)
   unsigned* grp_cnt;        // dataflow counters, kCntWords words (0 at entry)
   DevErr* err;
+  int skew_where;           // failure-detection hook: 0 off; 1 the first grid barrier, 2 the first QKV
+                            // head-group wait, 3 the first gate/up tile wait of the launch waits for
+  unsigned skew;            // this many arrivals more than will ever come (the wait runs out, the
+                            // error word records a timeout and every later wait returns at once)
   unsigned long long* trace;   // null, or [layers][grid][64] phase timestamps (ns): 0..14 block
                                // start and the ends of each phase / barrier, 16..18 attention,
                                // 20 + 4 g .. 23 + 4 g projection g
@@ -488,7 +492,8 @@ __device__ __forceinline__ void mk_qkv_arrive(const MkArgs& a, int lr, __nv_bflo
   const int grp = r.m / MPG;
   const int per = MPG * g.splits;
   const int part = (r.m % MPG) * g.splits + (int)blockIdx.x / g.MT;
-  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, (unsigned)((lr + 1) * per), a.err, 901, mt);
+  const unsigned extra = (lr == 0 && a.skew_where == 2) ? a.skew : 0u;
+  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, (unsigned)((lr + 1) * per) + extra, a.err, 901, mt);
   mk_qkv_finalize_group<DH>(a, grp * HPG, HPG, part, per, a.ss + (kSsQkv + grp) * 64, kc, vc, invD, mt);
 }
 
@@ -896,7 +901,8 @@ __device__ __forceinline__ void mk_gu_arrive(const MkArgs& a, int lr, float invD
   const MkGemm& g = a.g[2];
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
-  mk_group_wait(a.grp_cnt + kCntGuArr + r.m, (unsigned)((lr + 1) * g.splits), a.err, 902, mt);
+  const unsigned extra = (lr == 0 && a.skew_where == 3) ? a.skew : 0u;
+  mk_group_wait(a.grp_cnt + kCntGuArr + r.m, (unsigned)((lr + 1) * g.splits) + extra, a.err, 902, mt);
   mk_geglu_tile(a, r.m, (int)blockIdx.x / g.MT, g.splits, a.ss + (kSsGu + r.m) * 64, invD, mt);
 }
 
@@ -1093,7 +1099,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       const int lr = l - a.l0;
       for (int ph = 0; ph < 8; ++ph) {
         if (ph == 1 || ph == 6) continue;   // finalized inside the QKV and gate/up phases
-        if (ph > 0 || l > a.l0) mk_grid_sync(a.bar, ++nbar * G, a.err, mt);
+        if (ph > 0 || l > a.l0) {
+          ++nbar;
+          const unsigned extra = (nbar == 1 && a.skew_where == 1) ? a.skew : 0u;
+          mk_grid_sync(a.bar, nbar * G + extra, a.err, mt);
+        }
         const bool proj = ph == 0 || ph == 4 || ph == 5 || ph == 7;
         if (proj && mt == 0) mbar_arrive(go);   // the loader may fetch this phase's operand
         mk_mark(tr, 2 * ph + 1);

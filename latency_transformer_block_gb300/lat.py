@@ -95,6 +95,8 @@ def lib():
         L.lat_clear_error.restype = st
         L.lat_debug_timeout.argtypes = [_P, _P]
         L.lat_debug_timeout.restype = st
+        L.lat_debug_wait_skew.argtypes = [_P, ctypes.c_int, ctypes.c_int]
+        L.lat_debug_wait_skew.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -210,6 +212,10 @@ class Context:
 
     def debug_timeout(self, stream=None):
         check(lib().lat_debug_timeout(self.handle, stream_ptr(stream)))
+
+    def debug_wait_skew(self, which, extra):
+        """Make one bounded wait of the step kernel's first block expect `extra` arrivals too many."""
+        check(lib().lat_debug_wait_skew(self.handle, which, extra))
 
     def close(self):
         if getattr(self, "handle", None):

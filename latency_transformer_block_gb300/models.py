@@ -9,8 +9,12 @@ import torch
 from . import lat
 
 
-def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
-    """Upload bf16 bit patterns (uint16) as a torch bfloat16 tensor."""
+def _dev_bf16(bits, device) -> torch.Tensor:
+    """Upload bf16 bit patterns (uint16 array) as a torch bfloat16 tensor; a
+    bfloat16 torch tensor is taken as it is (moved to `device` if needed)."""
+    if isinstance(bits, torch.Tensor):
+        assert bits.dtype == torch.bfloat16, "weights must be bfloat16"
+        return bits.to(device).contiguous()
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
     return t.to(device).view(torch.bfloat16)
 

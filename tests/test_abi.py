@@ -57,4 +57,5 @@ def test_host_validation_without_gpu(L):
     assert L.lat_create(ctypes.byref(d), None, ctypes.byref(h)) == 2  # too many query tokens
     assert b"T_q" in L.lat_last_error()
     assert L.lat_sync(None) == 1
+    assert L.lat_debug_wait_skew(None, 1, 1) == 1                     # NULL ctx -> ARG
     L.lat_destroy(None)

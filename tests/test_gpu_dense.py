@@ -38,7 +38,11 @@ def test_prefill_small_parity():
     assert not np.any(got[:, :, :, Tp:]), "own-token slots must stay untouched"
 
 
-def test_prefill_full_b1_and_batch_independence():
+def test_prefill_full_b8_every_element_and_batch_independence():
+    """Full size, B = 8: every element's layer-0 K/V against the oracle (one
+    block from exact inputs: cache codes within one ulp), the whole 18-layer
+    cache of elements 0 and 5 against the oracle (final tolerance), and element
+    3 of the batch against a B = 1 run of the same input (GPU against GPU)."""
     cfg = synth.config("prefill")
     wb = synth.prefill_weights(cfg, 0)
     m = Pi0Prefix(cfg, wb, max_batch=8)
@@ -49,14 +53,24 @@ def test_prefill_full_b1_and_batch_independence():
     m.prefill(_dev_bf16(pe8[3:4], "cuda"), kv1)
     m.ctx.sync()
     got8, got1 = bits_of(kv8), bits_of(kv1)
-    # batch elements are independent: with one element the residual GEMMs split
-    # K (fp32 partial sums added in any order), so codes agree to rounding
-    Tp0 = cfg["T_prefix"]
-    assert_bf16_close(got8[:, 3:4, :, :Tp0], got1[:, :, :, :Tp0], "prefill batch independence", max_ulp=2)
-    ref = pi0.prefill(pe8[3:4], wb, cfg)
     Tp = cfg["T_prefix"]
-    assert_bf16_close(got1[0, :, :, :Tp], ref[0, :, :, :Tp], "prefill full layer 0 KV")
-    assert_rel(bf16.decode(got1[:, :, :, :Tp]), bf16.decode(ref[:, :, :, :Tp]), FINAL_TOL, "prefill full KV")
+    # layer 0 of every element: a one-layer prefill is the patch projection and
+    # the first block's K/V only
+    cfg1 = dict(cfg, L=1)
+    wb1 = dict(wb, blocks=wb["blocks"][:1])
+    blocks1 = [pi0.method_block(pi0.decode_tree(wb["blocks"][0]))]
+    for b in range(8):
+        ref0 = pi0.prefill(pe8[b:b + 1], wb1, cfg1, blocks=blocks1)
+        assert_bf16_close(got8[0, b:b + 1, :, :Tp], ref0[0, :, :, :Tp], f"prefill B=8 element {b} layer 0 KV")
+    blocks = [pi0.method_block(pi0.decode_tree(bl)) for bl in wb["blocks"]]
+    for b in (0, 5):
+        ref = pi0.prefill(pe8[b:b + 1], wb, cfg, blocks=blocks)
+        assert_rel(bf16.decode(got8[:, b:b + 1, :, :Tp]), bf16.decode(ref[:, :, :, :Tp]), FINAL_TOL,
+                   f"prefill B=8 element {b} KV, all 18 layers")
+    assert not np.any(got8[:, :, :, Tp:]), "own-token slots must stay untouched"
+    # batch elements are independent: with one element the residual GEMMs split
+    # K (fp32 partial sums added in another order), so codes agree to rounding
+    assert_bf16_close(got8[:, 3:4, :, :Tp], got1[:, :, :, :Tp], "prefill batch independence", max_ulp=2)
 
 
 # ----------------------------------------------------------------------------
@@ -146,6 +160,52 @@ def test_dit_14b_block_batch8_sampled_rows():
     for (st, c, s) in descs:
         sl = c % 5
         assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 14B own KV chunk {c}")
+
+
+@pytest.mark.parametrize("n", [1, 4])
+def test_dit_14b_block_sampled_rows(n):
+    """14B block with one chunk (its last wave's tail tiles split into key
+    ranges) and with four chunks at steps 0..3 (104 tail tiles, run whole)."""
+    cfg = synth.config("dit_14b")
+    descs = synth.dit_chunk_descs(cfg, n)
+    rows = np.r_[0:4, 640:644, 1400:1404, 1536:1560]   # the last query tiles: split / ragged
+    got_x, ref_x, got_ring, ref_ring, _ = _dit_case(cfg, descs, streams=1, rows=rows)
+    assert_rel(got_x, ref_x, BLOCK_TOL, f"dit 14B block n={n} residual (sampled rows)")
+    for (st, c, s) in descs:
+        sl = c % 5
+        assert_bf16_close(got_ring[st, s, sl], ref_ring[st, s, sl], f"dit 14B n={n} own KV chunk {c}")
+
+
+def test_dit_1p3b_whole_stage_interval():
+    """The full 1.3B stage: latent in-projection, all 30 blocks at each chunk's
+    own step, out-projection and Euler update for four chunks at steps 0..3
+    (chunks 3, 2, 1, 0: the interval that admits chunk 3), against the oracle's
+    stage interval at the final tolerance.  History slots the chunks read are
+    seeded; the others stay zero on both sides."""
+    cfg = synth.config("dit_1p3b")
+    wb = synth.dit_weights(cfg, 4)
+    m = DitStage(cfg, wb, max_batch=4, n_streams=1)
+    descs = synth.dit_chunk_descs(cfg, 4, first_chunk=3)
+    S, nh, L = cfg["S"], cfg["n_hist"], cfg["L"]
+    shape = (1, L, S, nh + 1, 2, cfg["T_chunk"], cfg["D"])
+    ring_bits = np.zeros(shape, np.uint16)
+    for (st, c, s) in descs:
+        for cc in dit.history_chunks(c, nh):
+            ring_bits[st, :, s, cc % (nh + 1)] = synth.normal_bf16(4, f"ring.{s}.{cc}", (L, 2, cfg["T_chunk"], cfg["D"]))
+    z0 = synth.dit_noise(cfg, 4, 4)
+    z = torch.from_numpy(z0).cuda()
+    ring = torch.from_numpy(ring_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    m.interval(ring, z, descs)
+    m.ctx.sync()
+    got = z.cpu().numpy()
+    del ring
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    W["blocks"] = [pi0.decode_tree(b) for b in wb["blocks"]]
+    table = dit.adaln_table(W, cfg)
+    # bf16 values are exact in float32; the oracle widens them to float64 as it reads
+    rings = synth.to_f32(ring_bits)
+    ref = dit.stage_interval(list(z0), descs, rings, table, W, cfg)
+    assert_rel(got, np.stack(ref), FINAL_TOL, "dit 1.3B whole-stage interval latents")
 
 
 def test_dit_indices_and_errors():

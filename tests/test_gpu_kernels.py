@@ -59,3 +59,34 @@ def test_device_wait_timeout_is_reported_and_cleared():
     m.ctx.sync()
     got, ref = run_attention(m, cfg, 64, 192, seed=5)
     assert_rel(got, ref, BLOCK_TOL, "attention after a cleared timeout")
+
+
+@pytest.mark.parametrize("which", [1, 2, 3], ids=["grid_barrier", "qkv_group_wait", "gate_up_tile_wait"])
+def test_step_kernel_wait_timeout_is_reported_and_cleared(which):
+    """Failure detection of the persistent step kernel's own waits, without a
+    GPU fault: one wait of the first block expects an arrival that never comes,
+    gives up (~0.5 s), every later wait of the launch returns at once, lat_sync
+    reports LAT_ERR_TIMEOUT; with the skew off and the error cleared the same
+    context denoises a chunk that matches the oracle."""
+    from latency_transformer_block_gb300 import lat
+    from oracle import pi0
+    from tests.parity import FINAL_TOL
+    cfg = synth.config("tiny")
+    wb = synth.pi0_weights(cfg, 0)
+    m = Pi0ActionExpert(cfg, wb)
+    ib = synth.pi0_inputs(cfg, 2)
+    kv = m.kv_from_bits(ib["kv"])
+    m.ctx.debug_wait_skew(which, 1)
+    m.ctx.debug_step(kv, 1)
+    with pytest.raises(lat.LatError) as e:
+        m.ctx.sync()
+    assert e.value.code == 6                       # LAT_ERR_TIMEOUT
+    m.ctx.debug_wait_skew(0, 0)
+    m.ctx.clear_error()
+    m.ctx.sync()
+    kv = m.kv_from_bits(ib["kv"])
+    x = torch.from_numpy(ib["noise"]).cuda()
+    m.denoise(kv, torch.from_numpy(ib["state"]).cuda(), x)
+    m.ctx.sync()
+    ref, _ = pi0.denoise(ib["noise"], ib["state"], ib["kv"], wb, cfg)
+    assert_rel(x.cpu().numpy(), ref, FINAL_TOL, "actions after a cleared step-kernel timeout")
