@@ -396,8 +396,10 @@ lat_status lat_debug_timeout(lat_ctx *ctx, void *stream);
  * kernel's own bounded waits (action-expert contexts).  From the next launch
  * on, one wait of the launch's first block expects `extra` more arrivals than
  * will ever come: which = 1 the first grid barrier (between the QKV and the
- * attention phase), 2 the first QKV head-group wait, 3 the first gate/up tile
- * wait; which = 0 or extra = 0 switches it off.  The wait gives up after the
+ * attention phase; `extra` arrivals too many), 2 the first QKV and 3 the
+ * first gate/up exchange of split-K partial sums inside a thread-block
+ * cluster (`extra` phases of the exchange barrier too many); which = 0 or
+ * extra = 0 switches it off.  The wait gives up after the
  * spin budget (~0.5 s) and records LAT_ERR_TIMEOUT; every later wait of the
  * launch sees the error and returns at once, the launch runs to its end with
  * meaningless results and leaves no copy in flight.  The next lat_sync

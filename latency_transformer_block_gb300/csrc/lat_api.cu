@@ -138,6 +138,7 @@ struct lat_ctx {
 
   // persistent step kernel: arguments, zero-at-entry block
   MkArgs mk{};
+  int step_grid = 0;   // CTAs of one step-kernel launch: co-resident clusters x 4
   void* mk_zero = nullptr;
   size_t mk_zero_bytes = 0;
 
@@ -402,6 +403,32 @@ static lat_status build_schedule(lat_ctx* c, const std::vector<double>& t) {
   return LAT_OK;
 }
 
+// Grid of the persistent step kernel: as many clusters of kMkCluster CTAs
+// (one CTA per SM) as can be resident at once, which its grid barriers need.
+static lat_status step_grid(lat_ctx* c) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMkCluster);
+  cfg.blockDim = dim3(kMkThreads);
+  cfg.dynamicSmemBytes = mk_smem_bytes();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kMkCluster;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e;
+  if (c->d.dh == 64) e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<64>, &cfg);
+  else if (c->d.dh == 128) e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<128>, &cfg);
+  else e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<256>, &cfg);
+  if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+  n = std::min(n, c->num_sms / kMkCluster);
+  if (n < 1) return fail(LAT_ERR_UNSUPPORTED, "no cluster of %d step-kernel CTAs fits on this device", kMkCluster);
+  c->step_grid = n * kMkCluster;
+  return LAT_OK;
+}
+
 static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   const lat_model_desc& d = c->d;
   const int D = d.D, F = d.F, L = d.L, A = d.act_dim;
@@ -424,12 +451,36 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(c->alloc(&c->wgu, (size_t)L * 2 * F * D));
   LAT_TRY(c->alloc(&c->wd, (size_t)L * D * F));
   LAT_TRY(c->alloc(&c->w2, (size_t)D * D));
+  // merged QKV rows permuted for the step kernel: in each 128-row tile, row
+  // 32 j + c holds the first element of rotary pair 16 j + c of the tile and
+  // row 32 j + 16 + c its partner dh / 2 further on, so that the quarter of a
+  // tile one CTA finalizes holds whole pairs (the pairs of the heads q.., k..,
+  // v.. in order; v rows are not rotated but move the same way)
+  if (c->nqkv % 128) return fail(LAT_ERR_SHAPE, "(Hq + 2 Hkv) * dh must be a multiple of 128");
+  std::vector<int> perm(c->nqkv);
+  {
+    const int pph = d.dh / 2;
+    for (int u = 0; u < c->nqkv / 128; ++u)
+      for (int j = 0; j < 4; ++j)
+        for (int h = 0; h < 2; ++h)
+          for (int cc = 0; cc < 16; ++cc) {
+            const int P = 64 * u + 16 * j + cc;
+            perm[128 * u + 32 * j + 16 * h + cc] = (P / pph) * d.dh + P % pph + h * pph;
+          }
+  }
+  int* dperm = nullptr;
+  bf16* qkv_tmp = nullptr;
+  LAT_TRY(c->alloc(&dperm, (size_t)c->nqkv));
+  LAT_TRY(c->alloc(&qkv_tmp, (size_t)c->nqkv * D));
+  CUDA_TRY(cudaMemcpy(dperm, perm.data(), perm.size() * sizeof(int), cudaMemcpyHostToDevice));
   for (int l = 0; l < L; ++l) {
     const lat_block_weights& b = w->blocks[l];
     bf16* q0 = c->wqkv + (size_t)l * c->nqkv * D;
-    LAT_TRY(fold_t(b.wq, b.g_attn, q0, D, qd));
-    LAT_TRY(fold_t(b.wk, b.g_attn, q0 + (size_t)qd * D, D, kvd));
-    LAT_TRY(fold_t(b.wv, b.g_attn, q0 + (size_t)(qd + kvd) * D, D, kvd));
+    LAT_TRY(fold_t(b.wq, b.g_attn, qkv_tmp, D, qd));
+    LAT_TRY(fold_t(b.wk, b.g_attn, qkv_tmp + (size_t)qd * D, D, kvd));
+    LAT_TRY(fold_t(b.wv, b.g_attn, qkv_tmp + (size_t)(qd + kvd) * D, D, kvd));
+    gather_rows_kernel<<<c->nqkv, 256>>>(qkv_tmp, dperm, q0, c->nqkv, D);
+    LAT_TRY(launch_check("gather_rows"));
     LAT_TRY(fold_t(b.wo, nullptr, c->wo + (size_t)l * D * qd, qd, D));
     // gate/up rows interleaved in 128-row tiles: 64 gate rows, then the 64 up
     // rows of the same FFN columns (one tile holds both inputs of its GeGLU)
@@ -546,25 +597,16 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
   CUDA_TRY(cudaMemset(c->xres, 0, (size_t)64 * D * 4));
 
-  // --- persistent step kernel: [barrier counter, group counters | sums of squares |
-  //     QKV sums], cleared before every launch; key-block partials; maps; plans ---
+  // --- persistent step kernel: barrier counter (cleared before every launch),
+  //     key-block partials, maps, cluster plans ---
   {
-    const size_t bar_b = 128 + 4 * (size_t)kCntWords, ss_b = (size_t)kSsRows * 64 * 4, qkv_b = (size_t)64 * c->nqkv * 4;
-    const size_t gu_b = (size_t)64 * 2 * F * 4;
-    static_assert((128 + 4 * kCntWords) % 16 == 0, "counter block keeps the sums 16-byte aligned");
-    if (c->nqkv / std::max(d.dh, 128) > 32) return fail(LAT_ERR_SHAPE, "at most 32 QKV head groups");
-    if (2 * F / 128 > 192) return fail(LAT_ERR_SHAPE, "F must be <= 12288");
-    c->mk_zero_bytes = bar_b + ss_b + qkv_b + gu_b;
+    c->mk_zero_bytes = 128;
     uint8_t* z = nullptr;
     LAT_TRY(c->alloc(&z, c->mk_zero_bytes));
     CUDA_TRY(cudaMemset(z, 0, c->mk_zero_bytes));
     c->mk_zero = z;
     MkArgs& m = c->mk;
     m.bar = reinterpret_cast<unsigned*>(z);
-    m.grp_cnt = m.bar + 32;
-    m.ss = reinterpret_cast<float*>(z + bar_b);
-    m.qkv = reinterpret_cast<float*>(z + bar_b + ss_b);
-    m.gu = reinterpret_cast<float*>(z + bar_b + ss_b + qkv_b);
     bf16 *qpl = nullptr, *kvo = nullptr;
     LAT_TRY(c->alloc(&qpl, (size_t)2 * 64 * qd));
     LAT_TRY(c->alloc(&kvo, (size_t)4 * 64 * kvd));
@@ -596,14 +638,28 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     m.prefix_lm = d.prefix_lm;
     m.eps = d.eps;
     m.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.dh));
-    const GemmPlan* gp[4] = {&c->g_qkv, &c->g_o, &c->g_gu, &c->g_d};
-    for (int i = 0; i < 4; ++i) {
-      m.g[i].MT = gp[i]->N_out / 128;
-      m.g[i].KT = gp[i]->K / 64;
-      m.g[i].splits = gp[i]->splits;
-      m.g[i].N = gp[i]->N_out;
-      if (m.g[i].MT * m.g[i].splits > c->num_sms) return fail(LAT_ERR_SHAPE, "projection plan exceeds the grid");
-    }
+    m.trace_stride = c->num_sms;
+    // grid: as many clusters of 4 as are co-resident with one CTA per SM
+    LAT_TRY(step_grid(c));
+    const int NC = c->step_grid / kMkCluster;
+    // QKV and gate/up: split-K partial sums meet in the cluster (distributed
+    // shared memory) and are finalized there; O and down: every CTA adds its
+    // K range's partial sums into the residual stream itself
+    MkGemm& gq = m.g[0];
+    gq = MkGemm{c->nqkv / 128, D / 64, c->nqkv, 0, 1, 0, 0};
+    MkGemm& go = m.g[1];
+    go = MkGemm{D / 128, qd / 64, D, 0, 0, 1, 0};
+    go.splits = std::min(c->step_grid / go.MT, go.KT);
+    MkGemm& gu = m.g[2];
+    gu = MkGemm{2 * F / 128, D / 64, 2 * F, 1, 0, 0, 0};
+    MkGemm& gd = m.g[3];
+    gd = MkGemm{D / 128, F / 64, D, 0, 0, 1, 0};
+    gd.splits = std::min(c->step_grid / gd.MT, gd.KT);
+    if (gq.MT > NC || gq.KT < kMkCluster) return fail(LAT_ERR_SHAPE, "QKV tiles exceed the co-resident clusters");
+    if (go.splits < 1 || gd.splits < 1) return fail(LAT_ERR_SHAPE, "O / down projections exceed the grid");
+    if (gu.MT % 2 || gu.MT / 2 > NC || gu.KT < 2)
+      return fail(LAT_ERR_SHAPE, "gate/up tiles (2F / 128 = %d) exceed twice the co-resident clusters (%d)",
+                  gu.MT, NC);
   }
 
   std::vector<double> t(d.S + 1);
@@ -633,8 +689,9 @@ static lat_status enqueue_attention(const lat_model_desc& d, const float* q, int
 }
 
 // ---------------------------------------------------------------------------
-// layers [l0, l1) of one denoise step on ctx->xres, one persistent launch
-// (cooperative: every CTA is resident, which the grid barriers need)
+// layers [l0, l1) of one denoise step on ctx->xres, one persistent launch in
+// clusters of 4 (cooperative: every CTA is resident, which the grid barriers
+// need)
 // ---------------------------------------------------------------------------
 static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long long kv_stride, cudaStream_t st) {
   CUDA_TRY(cudaMemsetAsync(c->mk_zero, 0, c->mk_zero_bytes, st));
@@ -644,15 +701,19 @@ static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long lo
   a.kv = kv;
   a.kv_stride = kv_stride;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(c->num_sms);
+  cfg.gridDim = dim3(c->step_grid);
   cfg.blockDim = dim3(kMkThreads);
   cfg.dynamicSmemBytes = mk_smem_bytes();
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kMkCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e;
   if (c->d.dh == 64)
     e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d,

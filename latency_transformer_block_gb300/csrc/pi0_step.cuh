@@ -50,14 +50,21 @@
 namespace lat {
 
 constexpr int kMkThreads = 384;                 // 12 warps
+constexpr int kMkCluster = 4;                   // CTAs per thread-block cluster
 constexpr int kMkNW = 6;                        // weight ring slots
-constexpr int kMkNB = 4;                        // activation-plane ring slots
+constexpr int kMkNB = 3;                        // activation-plane ring slots
 constexpr int kMkPre = 4;                       // k-tiles of x the math warps hold in flight (registers)
 constexpr int kMkWBytes = 128 * 64 * 2;         // one weight tile
 constexpr int kMkBBytes = 192 * 64 * 2;         // one activation tile, three planes
-constexpr int kMkRegion = 99 * 1024;            // the operand slots, also the attention's tiles
-constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 3;
-static_assert(kMkNB * kMkBBytes <= kMkRegion, "operand slots must fit in the activation region");
+// cluster exchange area (after the operand slots): 4 slots of split-K partial
+// sums [64 tokens][32 rows] fp32, written by the CTAs of the cluster into the
+// CTA that finalizes those rows, then 4 x 64 per-token sums of squares of x
+constexpr int kMkXSlot = 64 * 32 * 4;
+constexpr int kMkXOff = kMkNB * kMkBBytes;
+constexpr int kMkXBytes = 4 * kMkXSlot + 4 * 64 * 4;
+constexpr int kMkRegion = kMkXOff + kMkXBytes;  // also the attention's tiles (its own phase)
+constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 5;
+static_assert(kMkRegion % 1024 == 0, "the weight ring after the region stays 1024-byte aligned");
 
 __host__ __device__ constexpr int mk_smem_bytes() { return 1024 + kMkNW * kMkWBytes + kMkRegion + 8 * kMkBars + 16; }
 
@@ -75,11 +82,19 @@ __host__ __device__ constexpr int mk_attn_q_end() {
 static_assert(mk_attn_smem<256>() <= kMkRegion && mk_attn_q_end<256>() <= kMkRegion,
               "attention tiles must fit in the activation region");
 
-// One projection: MT tiles of 128 output rows, KT tiles of 64 inputs, K split
-// into `splits` ranges; CTA b < MT * splits takes m-tile b % MT and K range
-// b / MT.  N = rows of one layer's matrix in the stacked weight tensor.
+// One projection: MT tiles of 128 output rows (N rows of one layer's matrix
+// in the stacked weight tensor), KT tiles of 64 inputs.  CTA b is rank
+// b % 4 of cluster c = b / 4.
+//  pair = 0: cpm clusters per tile split its K into 4 cpm ranges (cluster c
+//            takes tile c / cpm; its ranks take 4 consecutive ranges); the 4
+//            partial sums of each row meet in the cluster: rank j finalizes
+//            rows 32 j .. 32 j + 31 of the tile.
+//  pair = 1: cluster c takes tiles 2 c and 2 c + 1, each split into 2 K
+//            ranges (ranks 2 i, 2 i + 1 of tile 2 c + i).
+//  direct = 1: no exchange; CTA b takes tile b % MT and K range b / MT of
+//            `splits` and adds its partial sums into the output itself.
 struct MkGemm {
-  int MT, KT, splits, N;
+  int MT, KT, N, pair, cpm, direct, splits;
 };
 
 struct MkArgs {
@@ -89,16 +104,10 @@ struct MkArgs {
   int prefix_lm;            // 1: the state token (query row 0) sees the prefix and itself only
   float eps, scale_log2;
   float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
-  float* qkv;               // fp32 [64][nqkv] QKV sums (vector reductions of every K range; 0 at entry,
-                            // cleared again in the GeGLU phase for the next block)
-  float* gu;                // fp32 [64][2F] gate/up sums in weight-row order (each 128-row tile = 64 gate
-                            // rows, then the 64 up rows of the same FFN columns); 0 at entry, cleared
-                            // again in the down phase for the next block
   __nv_bfloat16* o_planes;  // [3][64][Hq dh] attention output as exact bf16 planes (rows >= T_q stay 0)
   __nv_bfloat16* h_planes;  // [3][64][F] GeGLU output as exact bf16 planes (rows >= T_q stay 0)
   __nv_bfloat16* q_planes;  // [2][64][Hq dh] q after RoPE, two-term bf16 (hi, lo)
   __nv_bfloat16* kv_own;    // [k hi, k lo, v hi, v lo][64][Hkv dh] own keys / values, two-term bf16
-  float* ss;                // fp32 [L][2][64] sums of squares of x (0 at entry)
   float* part_m;            // [n_kb][Hq][T_q]
   float* part_l;
   float* part_o;            // [n_kb][Hq][8 warps][dh / 16 n-tiles][32 lanes] x float4
@@ -109,15 +118,15 @@ struct MkArgs {
   __nv_bfloat16* kv;        // cache of layer l0: [2][T_kv][Hkv dh]
   long long kv_stride;      // elements from one layer's cache to the next
   unsigned* bar;            // grid barrier counter (0 at entry)
-  unsigned* grp_cnt;        // dataflow counters, kCntWords words (0 at entry)
   DevErr* err;
   int skew_where;           // failure-detection hook: 0 off; 1 the first grid barrier, 2 the first QKV
-                            // head-group wait, 3 the first gate/up tile wait of the launch waits for
-  unsigned skew;            // this many arrivals more than will ever come (the wait runs out, the
+                            // exchange, 3 the first gate/up exchange of the launch waits for
+  unsigned skew;            // this many phases more than will ever complete (the wait runs out, the
                             // error word records a timeout and every later wait returns at once)
-  unsigned long long* trace;   // null, or [layers][grid][64] phase timestamps (ns): 0..14 block
+  unsigned long long* trace;   // null, or [layers][trace_stride][64] phase timestamps (ns): 0..14 block
                                // start and the ends of each phase / barrier, 16..18 attention,
-                               // 20 + 4 g .. 23 + 4 g projection g
+                               // 20 + 4 g .. 23 + 4 g projection g, 38 + g its cluster exchange received
+  int trace_stride;
 };
 
 struct MkRange {
@@ -127,11 +136,26 @@ struct MkRange {
 
 __device__ __forceinline__ MkRange mk_range(const MkGemm& g, int b) {
   MkRange r;
-  r.active = b < g.MT * g.splits;
-  r.m = b % g.MT;
-  const int s = b / g.MT;
-  r.k0 = s * g.KT / g.splits;
-  r.k1 = (s + 1) * g.KT / g.splits;
+  const int c = b / kMkCluster, q = b % kMkCluster;
+  int s, S;
+  if (g.direct) {
+    r.active = b < g.MT * g.splits;
+    r.m = b % g.MT;
+    s = b / g.MT;
+    S = g.splits;
+  } else if (g.pair) {
+    r.active = c < g.MT / 2;
+    r.m = 2 * c + (q >> 1);
+    s = q & 1;
+    S = 2;
+  } else {
+    r.active = c < g.MT * g.cpm;
+    r.m = c / g.cpm;
+    s = (c % g.cpm) * kMkCluster + q;
+    S = kMkCluster * g.cpm;
+  }
+  r.k0 = s * g.KT / S;
+  r.k1 = (s + 1) * g.KT / S;
   return r;
 }
 
@@ -155,6 +179,23 @@ __device__ __forceinline__ bool mk_wait(uint64_t* bar, uint32_t parity, DevErr* 
   }
 }
 
+// The same for an mbarrier completed by copies from other CTAs of the cluster
+// (acquire at cluster scope).  It does not give up early when another CTA has
+// failed: every CTA of an active cluster always sends its partial sums, so the
+// bytes always come, and no copy may still be on its way into this CTA when it
+// leaves; only the spin budget ends it.
+__device__ __forceinline__ bool mk_wait_cluster(uint64_t* bar, uint32_t parity, DevErr* err, unsigned where) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (int i = 0;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 63 && clock64() - t0 > kSpinBudget) {
+      record_error(err, 1u, where);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -169,38 +210,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 __device__ __forceinline__ void mk_mark(unsigned long long* tr, int ev) {
   if (tr) tr[ev] = global_ns();
-}
-
-__device__ __forceinline__ float2 ldcg2(const float* p) { return __ldcg(reinterpret_cast<const float2*>(p)); }
-
-// 4 x 4 transpose among the lanes k = lane % 4 of each lane quad: on entry
-// lane k holds row k (a0..a3), on exit it holds column k.  Two exchange rounds
-// (partner lane k ^ 1, then k ^ 2), two shuffles each.
-__device__ __forceinline__ void quad_transpose(float& a0, float& a1, float& a2, float& a3, int k) {
-  const bool c = k & 1, d = (k >> 1) & 1;
-  const float x0 = __shfl_xor_sync(0xffffffffu, c ? a0 : a1, 1);
-  const float x1 = __shfl_xor_sync(0xffffffffu, c ? a2 : a3, 1);
-  if (c) { a0 = x0; a2 = x1; } else { a1 = x0; a3 = x1; }
-  const float y0 = __shfl_xor_sync(0xffffffffu, d ? a0 : a2, 2);
-  const float y1 = __shfl_xor_sync(0xffffffffu, d ? a1 : a3, 2);
-  if (d) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
-}
-
-// n4 float4 of p = 0, spread over the grid's math threads
-__device__ __forceinline__ void mk_zero_f4(float* p, int n4, int mt) {
-  float4* z = reinterpret_cast<float4*>(p);
-  for (int i = blockIdx.x * 256 + mt; i < n4; i += gridDim.x * 256) __stcg(z + i, make_float4(0.f, 0.f, 0.f, 0.f));
-}
-
-
-
-// 8 fp32 values (registers) -> 8 bf16 hi and 8 bf16 lo (two-term split)
-__device__ __forceinline__ void split8_regs(const float (&v)[8], uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) split_pair2(v[2 * e], v[2 * e + 1], h[e], l[e]);
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Grid barrier among the math warps of all CTAs (barrier n waits for n * grid
@@ -230,24 +239,70 @@ __device__ __forceinline__ void mk_grid_sync(unsigned* ctr, unsigned target, Dev
 // Shared state of the math warps.
 struct MkMath {
   uint8_t* sB;
+  float* xbuf;        // cluster exchange slots [4][64 tokens][32 rows]
+  float* xss;         // [4][64] sums of squares of x, by source K range
   uint64_t* bfull;
   uint64_t* bempty;
   uint64_t* accfull;
+  uint64_t* xfull;    // exchange complete: armed by this CTA with the bytes it will receive
+  uint64_t* never;    // an mbarrier nothing arrives on (failure hook)
   uint64_t* go;
   uint32_t tmem;
-  uint32_t bt, gc;
+  uint32_t bt, gc, xuse;
+  bool xbroken;       // an exchange wait ran out: no further arming or waiting
   int mt;
 };
+
+// does cluster c take part in the exchange of this projection
+__device__ __forceinline__ bool mk_cluster_active(const MkGemm& g, int c) {
+  if (g.direct) return false;
+  return g.pair ? c < g.MT / 2 : c < g.MT * g.cpm;
+}
+
+// 4 x 4 transpose among the lanes k = lane % 4 of each lane quad: on entry
+// lane k holds row k (a0..a3), on exit it holds column k.  Two exchange rounds
+// (partner lane k ^ 1, then k ^ 2), two shuffles each.
+__device__ __forceinline__ void quad_transpose(float& a0, float& a1, float& a2, float& a3, int k) {
+  const bool c = k & 1, d = (k >> 1) & 1;
+  const float x0 = __shfl_xor_sync(0xffffffffu, c ? a0 : a1, 1);
+  const float x1 = __shfl_xor_sync(0xffffffffu, c ? a2 : a3, 1);
+  if (c) { a0 = x0; a2 = x1; } else { a1 = x0; a3 = x1; }
+  const float y0 = __shfl_xor_sync(0xffffffffu, d ? a0 : a2, 2);
+  const float y1 = __shfl_xor_sync(0xffffffffu, d ? a1 : a3, 2);
+  if (d) { a0 = y0; a1 = y1; } else { a2 = y0; a3 = y1; }
+}
+
+// bytes a CTA receives in the exchange of projection gi: the 4 slots of
+// partial sums, plus the sums of squares of x (QKV: 4 K ranges; gate/up: 2)
+__device__ __forceinline__ uint32_t mk_xbytes(int gi) {
+  return 4 * kMkXSlot + (gi == 0 ? 4 * 256 : gi == 2 ? 2 * 256 : 0);
+}
+
+// bytes of cluster c's next exchange after projection gi of layer l (gi = -1:
+// the first of layer l); 0 if it takes part in none before the launch ends
+__device__ __forceinline__ uint32_t mk_next_xbytes(const MkArgs& a, int l, int gi, int c) {
+  for (int k = 0; k < 8; ++k) {
+    if (++gi == 4) {
+      gi = 0;
+      ++l;
+    }
+    if (l >= a.l1) return 0;
+    if (mk_cluster_active(a.g[gi], c)) return mk_xbytes(gi);
+  }
+  return 0;
+}
 
 // Math side of one projection.  Projections of the residual stream x (QKV,
 // gate/up): the math warps load their rows of x straight from global memory,
 // kMkPre k-tiles in flight in registers, and write the exact bf16 planes into
 // the operand slots; for the others (act == nullptr) the loader brings the
-// planes by TMA.  Then the split-K epilogue: every K range adds its partial
-// sums into `out` (vector reductions at L2).  `stats`, when given, receives
-// this K range's per-token sums of squares of x (atomic adds).
+// planes by TMA.  Then the split-K epilogue: each warp sums the three planes
+// of its quarter of the tile's rows and stores them, through distributed
+// shared memory, into the exchange slot of the cluster rank that finalizes
+// those rows; with `stats` the per-token sums of squares of this K range go
+// to the ranks that need them.  Every warp then arrives on every rank's
+// exchange barrier.
 // 16 bytes from global memory through L2 (not L1: other SMs write x), issued
-// where it stands so that several k-tiles are in flight at once
 __device__ __forceinline__ float4 mk_ldcg4(const float* p) {
   float4 v;
   asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
@@ -262,12 +317,13 @@ __device__ __forceinline__ void mk_load_tile(const float* act, int ld, int kt, c
     for (int hh = 0; hh < 2; ++hh) v[2 * i + hh] = mk_ldcg4(act + (size_t)rows[i] * ld + kt * 64 + hh * 32 + 4 * p);
 }
 
-__device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const float* act, int act_ld, float* stats,
+__device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const float* act, int act_ld, bool stats,
                                              float* out, int ld, int T_q, DevErr* err, unsigned long long* tr) {
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
   const int nk = r.k1 - r.k0;
   const int mw = s.mt >> 5, lane = s.mt & 31;
+  const uint32_t rank = blockIdx.x % kMkCluster;
   if (!act) {   // the loader brings this projection's operand planes by TMA
     s.bt += nk;
     if (tr) tr[0] = tr[1] = global_ns();
@@ -323,18 +379,18 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
       }
     }
   }
-  if (stats) {
+  // this K range's per-token sums of squares of x (lanes p == 0 hold rows[i])
+  float ssq[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      float v = sq[i];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      if (p == 0) atomicAdd(stats + rows[i], v);
-    }
+  for (int i = 0; i < 2; ++i) {
+    float v = sq[i];
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    ssq[i] = v;
   }
-  // epilogue: warp (4 + mw) reads TMEM lanes 32 (mw % 4) .. +31 = output rows,
-  // tokens 32 (mw / 4) .. +31 of each plane; the planes are summed hi + mid + lo
+  // epilogue: warp (4 + mw) reads TMEM lanes 32 q .. +31 = rows of the tile,
+  // tokens 32 ch .. +31 of each plane, sums the planes hi + mid + lo
   if (act) mk_mark(tr, 1);
   mk_wait(s.accfull, s.gc & 1, err, 32);
   mk_mark(tr, 2);
@@ -342,159 +398,141 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
   const uint32_t acc = s.tmem + (s.gc & 1) * 256;
   ++s.gc;
   const int q = mw & 3, ch = mw >> 2;
-  const int f = r.m * 128 + q * 32 + lane;
   const uint32_t tb = acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
   float v[32], w[32], z[32];
   tmem_ld32x3(tb, tb + 64, tb + 128, v, w, z);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = (v[j] + w[j]) + z[j];
   tc_fence_before();
-  // each lane quad transposes 4 tokens x its 4 outputs, so a lane adds 4
-  // consecutive outputs of one token: one vector reduction
-  const int k4 = lane & 3;
-  const int fb = f - k4;
+  if (g.direct) {
+    // each lane quad transposes 4 tokens x its 4 rows, so a lane adds 4
+    // consecutive outputs of one token: one vector reduction into `out`
+    const int k4 = lane & 3;
+    const int fb = r.m * 128 + q * 32 + lane - k4;
 #pragma unroll
-  for (int j0 = 0; j0 < 32; j0 += 4) {
-    float a0 = v[j0], a1 = v[j0 + 1], a2 = v[j0 + 2], a3 = v[j0 + 3];
-    quad_transpose(a0, a1, a2, a3, k4);
-    const int t = ch * 32 + j0 + k4;
-    if (t < T_q) red_add_v4(out + (size_t)t * ld + fb, a0, a1, a2, a3);
+    for (int j0 = 0; j0 < 32; j0 += 4) {
+      float a0 = v[j0], a1 = v[j0 + 1], a2 = v[j0 + 2], a3 = v[j0 + 3];
+      quad_transpose(a0, a1, a2, a3, k4);
+      const int t = ch * 32 + j0 + k4;
+      if (t < T_q) red_add_v4(out + (size_t)t * ld + fb, a0, a1, a2, a3);
+    }
+    mk_mark(tr, 3);
+    return;
+  }
+  // every MMA of the projection is complete, so the operand slots are free:
+  // stage this warp's block, [token][row] (32 x 32 fp32), and the statistics
+  float* stg = reinterpret_cast<float*>(s.sB) + mw * 1024;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) stg[j * 32 + lane] = v[j];
+  float* sst = reinterpret_cast<float*>(s.sB) + 8 * 1024;
+  if (stats && p == 0) {
+    sst[rows[0]] = ssq[0];
+    sst[rows[1]] = ssq[1];
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  // the block goes to the rank that finalizes these rows, into the slot of
+  // this K range (tokens 32 ch ..): one bulk copy, completing on its barrier
+  uint32_t dest, slot;
+  if (g.pair) {
+    dest = (rank & 2) | (uint32_t)(q & 1);       // the K range (q & 1) of this tile finalizes its half
+    slot = (rank & 1) * 2 + (uint32_t)(q >> 1);  // [source K range][gate | up]
+  } else {
+    dest = (uint32_t)q;
+    slot = rank;
+  }
+  if (lane == 0)
+    bulk_copy_to_cluster(cluster_map(smem_u32(s.xbuf + slot * (kMkXSlot / 4) + ch * 1024), dest), smem_u32(stg),
+                         4096u, cluster_map(smem_u32(s.xfull), dest));
+  if (stats) {
+    // the sums of squares of this K range: to every rank (QKV) or to the two
+    // ranks of this tile (gate/up), in the row of this K range
+    named_sync(2, 256);
+    if (s.mt == 0) {
+      const uint32_t src = g.pair ? (rank & 1) : rank;
+      const uint32_t at = smem_u32(s.xss + src * 64);
+      for (uint32_t d = 0; d < kMkCluster; ++d)
+        if (!g.pair || (d & 2) == (rank & 2))
+          bulk_copy_to_cluster(cluster_map(at, d), smem_u32(sst), 256u, cluster_map(smem_u32(s.xfull), d));
+    }
   }
   mk_mark(tr, 3);
 }
 
-// q, own k and own v of one head group, from the finished QKV sums: every CTA
-// of the projection adds its K range into a.qkv (vector reductions); the CTA
-// that completes a group (all K ranges of its m-tiles) runs this for the
-// group's heads.  r = rsqrt(mean(x^2) + eps), RoPE (rotate-half pairs
-// (i, i + dh/2)) on q and k heads, two-term bf16 splits into q_planes /
-// kv_own, and the bf16 cache copy (nearest) of own k / v at slots T_prefix + t.
+// Wait until this CTA has received every byte of the exchange (its partial
+// sums and statistics from the cluster), then arm the barrier with the bytes
+// of its next exchange; with `skew` first a wait that nothing completes.
+__device__ __forceinline__ void mk_exchange_wait(MkMath& s, const MkArgs& a, int l, int gi, int c, bool skew,
+                                                 unsigned where) {
+  if (skew) mk_wait(s.never, 0, a.err, where + 100);
+  if (s.xbroken) return;
+  const bool ok = mk_wait_cluster(s.xfull, s.xuse & 1, a.err, where);
+  ++s.xuse;
+  if (!ok) {
+    s.xbroken = true;
+    return;
+  }
+  if (s.mt == 0) {
+    const uint32_t nb = mk_next_xbytes(a, l, gi, c);
+    if (nb) mbar_arrive_expect_tx(s.xfull, nb);
+  }
+}
+
+// QKV: rank j of the cluster of tile u finalizes the tile's rows 32 j .. +31,
+// which hold 16 rotary pairs (the weight rows are permuted at fold time: row
+// 32 j + c holds the first element of pair 16 j + c of the tile, row
+// 32 j + 16 + c its partner dh / 2 further on).  Per token: the sum of the 4 K
+// ranges times r = rsqrt(mean(x^2) + eps), RoPE on q and k heads, two-term
+// bf16 planes into q_planes / kv_own, and k, v (nearest bf16) into the cache
+// at slot T_prefix + t.
 template <int DH>
-__device__ __forceinline__ void mk_qkv_finalize_group(const MkArgs& a, int h0, int nhd, int part, int parts,
-                                                      const float* ss1, __nv_bfloat16* kc, __nv_bfloat16* vc,
-                                                      float invD, int mt) {
-  constexpr int HD = DH / 2;
-  const int nh = a.Hq + a.Hkv, kvd = a.Hkv * DH, qd = a.Hq * DH;
+__device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int u, int j, const float* xbuf, const float* xss,
+                                                __nv_bfloat16* kc, __nv_bfloat16* vc, float invD, int mt) {
+  constexpr int PPH = DH / 2;   // rotary pairs per head
+  const int qd = a.Hq * DH, kvd = a.Hkv * DH;
   const size_t qpl = (size_t)64 * qd, kpl = (size_t)64 * kvd;
-  for (int hd = h0; hd < h0 + nhd; ++hd) {
-    if (hd < nh) {   // q or k head: 4 RoPE pairs per item
-      const int n = a.T_q * (HD / 4);
-      for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
-        const int t = it / (HD / 4), i = (it % (HD / 4)) * 4;
-        const float* p0 = a.qkv + (size_t)t * a.nqkv + hd * DH + i;
-        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p0));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(p0 + HD));
-        const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
-        const float4 c = __ldg(reinterpret_cast<const float4*>(a.cos_t + (size_t)t * HD + i));
-        const float4 sn = __ldg(reinterpret_cast<const float4*>(a.sin_t + (size_t)t * HD + i));
-        const float a0[4] = {rv * x0.x, rv * x0.y, rv * x0.z, rv * x0.w};
-        const float a1[4] = {rv * x1.x, rv * x1.y, rv * x1.z, rv * x1.w};
-        const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
-        float y0[4], y1[4];
+  for (int it = mt; it < a.T_q * 16; it += 256) {
+    const int t = it >> 4, c = it & 15;
+    float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          y0[e] = a0[e] * cc[e] - a1[e] * ss[e];
-          y1[e] = a1[e] * cc[e] + a0[e] * ss[e];
-        }
-        uint32_t h0w[2], l0w[2], h1w[2], l1w[2];
-        split_pair2(y0[0], y0[1], h0w[0], l0w[0]);
-        split_pair2(y0[2], y0[3], h0w[1], l0w[1]);
-        split_pair2(y1[0], y1[1], h1w[0], l1w[0]);
-        split_pair2(y1[2], y1[3], h1w[1], l1w[1]);
-        if (hd < a.Hq) {
-          uint2* q = reinterpret_cast<uint2*>(a.q_planes + (size_t)t * qd + hd * DH + i);
-          q[0] = make_uint2(h0w[0], h0w[1]);
-          q[HD / 4] = make_uint2(h1w[0], h1w[1]);
-          q[qpl / 4] = make_uint2(l0w[0], l0w[1]);
-          q[qpl / 4 + HD / 4] = make_uint2(l1w[0], l1w[1]);
-        } else {
-          const int kh = hd - a.Hq;
-          uint2* k = reinterpret_cast<uint2*>(a.kv_own + (size_t)t * kvd + kh * DH + i);
-          k[0] = make_uint2(h0w[0], h0w[1]);
-          k[HD / 4] = make_uint2(h1w[0], h1w[1]);
-          k[kpl / 4] = make_uint2(l0w[0], l0w[1]);
-          k[kpl / 4 + HD / 4] = make_uint2(l1w[0], l1w[1]);
-          float tx, ty;
-          uint2* ck = reinterpret_cast<uint2*>(kc + (size_t)(a.T_prefix + t) * kvd + kh * DH + i);
-          ck[0] = make_uint2(rn_pair(y0[0], y0[1], tx, ty), rn_pair(y0[2], y0[3], tx, ty));
-          ck[HD / 4] = make_uint2(rn_pair(y1[0], y1[1], tx, ty), rn_pair(y1[2], y1[3], tx, ty));
-        }
-      }
-    } else {   // v head: 4 values per item
-      const int n = a.T_q * (DH / 4), j0 = (hd - nh) * DH;
-      for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
-        const int t = it / (DH / 4), j = j0 + (it % (DH / 4)) * 4;
-        float4 x = __ldcg(reinterpret_cast<const float4*>(a.qkv + (size_t)t * a.nqkv + nh * DH + j));
-        const float rv = rsqrtf(__ldcg(ss1 + t) * invD + a.eps);
-        x.x *= rv; x.y *= rv; x.z *= rv; x.w *= rv;
-        uint32_t hh[2], ll[2];
-        split_pair2(x.x, x.y, hh[0], ll[0]);
-        split_pair2(x.z, x.w, hh[1], ll[1]);
-        uint2* v = reinterpret_cast<uint2*>(a.kv_own + 2 * kpl + (size_t)t * kvd + j);
-        v[0] = make_uint2(hh[0], hh[1]);
-        v[kpl / 4] = make_uint2(ll[0], ll[1]);
-        float tx, ty;
-        *reinterpret_cast<uint2*>(vc + (size_t)(a.T_prefix + t) * kvd + j) =
-            make_uint2(rn_pair(x.x, x.y, tx, ty), rn_pair(x.z, x.w, tx, ty));
-      }
+    for (int src = 0; src < kMkCluster; ++src) {
+      x0 += xbuf[src * 2048 + t * 32 + c];
+      x1 += xbuf[src * 2048 + t * 32 + 16 + c];
+    }
+    const float ss = (xss[t] + xss[64 + t]) + (xss[128 + t] + xss[192 + t]);
+    const float rv = rsqrtf(ss * invD + a.eps);
+    x0 *= rv;
+    x1 *= rv;
+    const int P = 64 * u + 16 * j + c;
+    const int head = P / PPH, i = P % PPH;
+    float y0 = x0, y1 = x1;
+    if (head < a.Hq + a.Hkv) {   // q and k heads are rotated
+      const float cs = __ldg(a.cos_t + (size_t)t * PPH + i), sn = __ldg(a.sin_t + (size_t)t * PPH + i);
+      y0 = x0 * cs - x1 * sn;
+      y1 = x1 * cs + x0 * sn;
+    }
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+    const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
+    const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+    if (head < a.Hq) {
+      __nv_bfloat16* q = a.q_planes + (size_t)t * qd + head * DH + i;
+      q[0] = h0;
+      q[PPH] = h1;
+      q[qpl] = l0;
+      q[qpl + PPH] = l1;
+    } else {
+      const bool isk = head < a.Hq + a.Hkv;
+      const int kh = isk ? head - a.Hq : head - a.Hq - a.Hkv;
+      __nv_bfloat16* o = a.kv_own + (isk ? 0 : 2 * kpl) + (size_t)t * kvd + kh * DH + i;
+      o[0] = h0;
+      o[PPH] = h1;
+      o[kpl] = l0;
+      o[kpl + PPH] = l1;
+      __nv_bfloat16* cache = (isk ? kc : vc) + (size_t)(a.T_prefix + t) * kvd + kh * DH + i;
+      cache[0] = h0;   // the nearest bf16 of the value
+      cache[PPH] = h1;
     }
   }
-}
-
-// Counters after the grid barrier word (MkArgs::grp_cnt), 0 at launch entry;
-// each grows by one group's arrivals per block.
-constexpr int kCntQkvArr = 0;      // [32] QKV head groups: CTAs past their epilogue
-constexpr int kCntGuArr = 32;      // [192] gate/up tiles: CTAs past their epilogue
-constexpr int kCntWords = 224;
-// Per-token sums of squares of the projection input (MkArgs::ss), one row of
-// 64 per QKV head group, then one per gate/up tile: each group's own K ranges
-// add into its row, so a group needs no other group's statistics.
-constexpr int kSsQkv = 0;
-constexpr int kSsGu = 32;
-constexpr int kSsRows = 224;
-
-// Count this CTA into group counter `cnt`, then wait until the group has all
-// `target` arrivals.  Bounded: gives up (error recorded) after the spin budget
-// or when another CTA has failed.  The counters grow by one group's arrivals
-// per block and start at 0 with each launch.
-__device__ __forceinline__ void mk_group_wait(unsigned* cnt, unsigned target, DevErr* err, unsigned where, int mt) {
-  __threadfence();   // this thread's reductions are performed before the arrival
-  named_sync(2, 256);
-  if (mt == 0) {
-    atomicAdd(cnt, 1u);
-    const long long t0 = clock64();
-    for (int i = 0; ld_acquire_u32(cnt) < target; ++i)
-      if ((i & 15) == 15 && (mk_aborted(err) || clock64() - t0 > kSpinBudget)) {
-        if (!mk_aborted(err)) record_error(err, 2u, where);
-        break;
-      }
-    __threadfence();
-  }
-  named_sync(2, 256);
-}
-
-// After the QKV epilogue: every CTA of a head group (the m-tiles of whole
-// heads, all K ranges) waits for the group, then finalizes its share of the
-// group's heads.  `lr` = block index within the launch.
-template <int DH>
-struct MkQkvGroups {
-  static constexpr int MPG = DH >= 128 ? DH / 128 : 1;   // m-tiles per group
-  static constexpr int HPG = DH >= 128 ? 1 : 128 / DH;   // heads per group
-};
-
-template <int DH>
-__device__ __forceinline__ void mk_qkv_arrive(const MkArgs& a, int lr, __nv_bfloat16* kc, __nv_bfloat16* vc,
-                                              float invD, int mt) {
-  const MkGemm& g = a.g[0];
-  const MkRange r = mk_range(g, blockIdx.x);
-  if (!r.active) return;
-  constexpr int MPG = MkQkvGroups<DH>::MPG, HPG = MkQkvGroups<DH>::HPG;
-  const int grp = r.m / MPG;
-  const int per = MPG * g.splits;
-  const int part = (r.m % MPG) * g.splits + (int)blockIdx.x / g.MT;
-  const unsigned extra = (lr == 0 && a.skew_where == 2) ? a.skew : 0u;
-  mk_group_wait(a.grp_cnt + kCntQkvArr + grp, (unsigned)((lr + 1) * per) + extra, a.err, 901, mt);
-  mk_qkv_finalize_group<DH>(a, grp * HPG, HPG, part, per, a.ss + (kSsQkv + grp) * 64, kc, vc, invD, mt);
 }
 
 // Phase 3: attention of the chunk over [cache | own], one (head, 32-key block)
@@ -869,41 +907,54 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
   fence_proxy_async_smem();   // sw's bytes are reused by TMA in the next phase
 }
 
-// h = GELU(r g) * (r u) for the 64 FFN columns of gate/up tile m and every
-// token, as the exact bf16 planes of the down projection's operand; g and u
-// are the finished gate/up sums, r = rsqrt(mean(x^2) + eps) of the FFN input.
-__device__ __forceinline__ void mk_geglu_tile(const MkArgs& a, int m, int part, int parts, const float* ss2,
-                                              float invD, int mt) {
+// gate/up: rank (i, k) of the cluster (tile 2 c + i, K range k) finalizes the
+// FFN columns 64 m + 32 k .. +31 of its tile m: g and u are the sums of the
+// two K ranges' partials, r = rsqrt(mean(x^2) + eps) of the FFN input, and
+// h = GELU(r g) * (r u) goes out as the exact bf16 planes of the down
+// projection's operand.
+__device__ __forceinline__ void mk_gu_finalize(const MkArgs& a, int m, int k, const float* xbuf, const float* xss,
+                                               float invD, int mt) {
   const int F = a.F;
   const size_t pl = (size_t)64 * F;
-  const int n = a.T_q * 16;
-  for (int it = part * n / parts + mt; it < (part + 1) * n / parts; it += 256) {
-    const int t = it >> 4, i = (it & 15) * 4;
-    const float* gp = a.gu + (size_t)t * 2 * F + m * 128 + i;
-    const float4 g = __ldcg(reinterpret_cast<const float4*>(gp));
-    const float4 u = __ldcg(reinterpret_cast<const float4*>(gp + 64));
-    const float rv = rsqrtf(__ldcg(ss2 + t) * invD + a.eps);
-    const float h0 = gelu_tanh_fast(rv * g.x) * (rv * u.x), h1 = gelu_tanh_fast(rv * g.y) * (rv * u.y);
-    const float h2 = gelu_tanh_fast(rv * g.z) * (rv * u.z), h3 = gelu_tanh_fast(rv * g.w) * (rv * u.w);
+  for (int it = mt; it < a.T_q * 8; it += 256) {
+    const int t = it >> 3, c4 = (it & 7) * 4;
+    const float4 g0 = *reinterpret_cast<const float4*>(xbuf + 0 * 2048 + t * 32 + c4);
+    const float4 u0 = *reinterpret_cast<const float4*>(xbuf + 1 * 2048 + t * 32 + c4);
+    const float4 g1 = *reinterpret_cast<const float4*>(xbuf + 2 * 2048 + t * 32 + c4);
+    const float4 u1 = *reinterpret_cast<const float4*>(xbuf + 3 * 2048 + t * 32 + c4);
+    const float rv = rsqrtf((xss[t] + xss[64 + t]) * invD + a.eps);
+    const float h0 = gelu_tanh_fast(rv * (g0.x + g1.x)) * (rv * (u0.x + u1.x));
+    const float h1 = gelu_tanh_fast(rv * (g0.y + g1.y)) * (rv * (u0.y + u1.y));
+    const float h2 = gelu_tanh_fast(rv * (g0.z + g1.z)) * (rv * (u0.z + u1.z));
+    const float h3 = gelu_tanh_fast(rv * (g0.w + g1.w)) * (rv * (u0.w + u1.w));
     uint32_t a0, b0, c0, a1, b1, c1;
     split_pair_exact(h0, h1, a0, b0, c0);
     split_pair_exact(h2, h3, a1, b1, c1);
-    uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + m * 64 + i);
+    uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + m * 64 + k * 32 + c4);
     d[0] = make_uint2(a0, a1);
     d[pl / 4] = make_uint2(b0, b1);
     d[pl / 2] = make_uint2(c0, c1);
   }
 }
 
-// After the gate/up epilogue: every CTA of a tile (all K ranges) waits for
-// the tile, then writes its share of the tile's GeGLU planes.
-__device__ __forceinline__ void mk_gu_arrive(const MkArgs& a, int lr, float invD, int mt) {
-  const MkGemm& g = a.g[2];
-  const MkRange r = mk_range(g, blockIdx.x);
-  if (!r.active) return;
-  const unsigned extra = (lr == 0 && a.skew_where == 3) ? a.skew : 0u;
-  mk_group_wait(a.grp_cnt + kCntGuArr + r.m, (unsigned)((lr + 1) * g.splits) + extra, a.err, 902, mt);
-  mk_geglu_tile(a, r.m, (int)blockIdx.x / g.MT, g.splits, a.ss + (kSsGu + r.m) * 64, invD, mt);
+// O and down projections: rank j adds the sum of the cluster's 4 K ranges for
+// rows 32 j .. +31 of tile m (features 128 m + 32 j ..) into the residual
+// stream x, one vector reduction per 4 features (the other clusters of the
+// tile add their K ranges the same way).
+__device__ __forceinline__ void mk_x_finalize(const MkArgs& a, int m, int j, const float* xbuf, int mt) {
+  for (int it = mt; it < a.T_q * 8; it += 256) {
+    const int t = it >> 3, c4 = (it & 7) * 4;
+    float4 acc = *reinterpret_cast<const float4*>(xbuf + t * 32 + c4);
+#pragma unroll
+    for (int src = 1; src < kMkCluster; ++src) {
+      const float4 v = *reinterpret_cast<const float4*>(xbuf + src * 2048 + t * 32 + c4);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    red_add_v4(a.x + (size_t)t * a.D + m * 128 + j * 32 + c4, acc.x, acc.y, acc.z, acc.w);
+  }
 }
 
 template <int DH>
@@ -926,7 +977,9 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   uint64_t* accfull = bempty + kMkNB;      // accumulator complete
   uint64_t* mdone = accfull + 1;           // every MMA complete (teardown)
   uint64_t* go = mdone + 1;                // grid barrier passed before a projection phase
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(go + 1);
+  uint64_t* xfull = go + 1;                // cluster exchange received (bytes, armed by this CTA)
+  uint64_t* never = xfull + 1;             // nothing arrives (failure hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -942,7 +995,13 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     mbar_init(accfull, 1);
     mbar_init(mdone, 1);
     mbar_init(go, 1);
+    mbar_init(xfull, 1);
+    mbar_init(never, 1);
     fence_mbar_init();
+    // armed with the bytes of this CTA's first exchange before any peer can
+    // send (the cluster barrier below)
+    const uint32_t nb = mk_next_xbytes(a, a.l0, -1, (int)blockIdx.x / kMkCluster);
+    if (nb) mbar_arrive_expect_tx(xfull, nb);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -952,6 +1011,9 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the cluster's barriers are initialised before any CTA of it arrives on a
+  // peer's barrier or stores into a peer's exchange area
+  cluster_sync_all();
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
@@ -1074,12 +1136,17 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     // ---------------- math warps ----------------
     MkMath s;
     s.sB = sB;
+    s.xbuf = reinterpret_cast<float*>(sR + kMkXOff);
+    s.xss = s.xbuf + kMkCluster * (kMkXSlot / 4);
     s.bfull = bfull;
     s.bempty = bempty;
     s.accfull = accfull;
+    s.xfull = xfull;
+    s.never = never;
+    s.xbroken = false;
     s.go = go;
     s.tmem = tmem;
-    s.bt = s.gc = 0;
+    s.bt = s.gc = s.xuse = 0;
     s.mt = threadIdx.x - 128;
     const int mt = s.mt;
     const unsigned G = gridDim.x;
@@ -1090,13 +1157,14 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       __nv_bfloat16* kc = a.kv + (size_t)(l - a.l0) * a.kv_stride;
       __nv_bfloat16* vc = kc + (size_t)a.T_kv * kvd;
       unsigned long long* tr =
-          (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * gridDim.x + blockIdx.x) * 64 : nullptr;
+          (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * a.trace_stride + blockIdx.x) * 64 : nullptr;
       mk_mark(tr, 0);
       // phases: 0 QKV (+ q / own k, v), 2 attention, 3 combine, 4 O, 5 gate/up
       // (+ GeGLU planes), 7 down; a grid barrier before each (the first one of
       // a launch has none).  Indices 1 and 6 (former separate finalize phases)
       // are skipped so trace slots keep their meaning.
       const int lr = l - a.l0;
+      const int cl = (int)blockIdx.x / kMkCluster, rk = (int)blockIdx.x % kMkCluster;
       for (int ph = 0; ph < 8; ++ph) {
         if (ph == 1 || ph == 6) continue;   // finalized inside the QKV and gate/up phases
         if (ph > 0 || l > a.l0) {
@@ -1111,29 +1179,19 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           mk_attention<DH>(a, kc, vc, sR, mt, tr);
         } else if (ph == 3) {
           mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR), tr);
-          // the QKV sums and statistics of the next block start from zero
-          // (every finalizer of this block is done before the barrier that
-          // opened phase 2)
-          mk_zero_f4(a.qkv, 16 * a.nqkv, mt);
-          mk_zero_f4(a.ss + kSsQkv * 64, 16 * (kSsGu - kSsQkv), mt);
         } else {
           const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
-          float* out = ph == 0 ? a.qkv : ph == 5 ? a.gu : a.x;
-          const int ld = ph == 0 ? a.nqkv : ph == 5 ? 2 * a.F : a.D;
-          const MkRange r = mk_range(a.g[gi], blockIdx.x);
-          float* stats = nullptr;   // this K range's sums of squares of x, into its group's row
-          if (ph == 0 && r.m % MkQkvGroups<DH>::MPG == 0) stats = a.ss + (kSsQkv + r.m / MkQkvGroups<DH>::MPG) * 64;
-          if (ph == 5) stats = a.ss + (kSsGu + r.m) * 64;
-          mk_gemm_math(s, a.g[gi], ph == 0 || ph == 5 ? a.x : nullptr, a.D, stats, out, ld, a.T_q, a.err,
+          const MkGemm& g = a.g[gi];
+          const MkRange r = mk_range(g, blockIdx.x);
+          mk_gemm_math(s, g, ph == 0 || ph == 5 ? a.x : nullptr, a.D, ph == 0 || ph == 5, a.x, a.D, a.T_q, a.err,
                        tr ? tr + 20 + 4 * gi : nullptr);
-          if (ph == 0) mk_qkv_arrive<DH>(a, lr, kc, vc, invD, mt);
-          if (ph == 5) mk_gu_arrive(a, lr, invD, mt);
-          // the gate/up sums and statistics of the next block start from zero
-          // (every GeGLU tile of this block was written before the barrier that
-          // opened phase 7)
-          if (ph == 7) {
-            mk_zero_f4(a.gu, 32 * a.F, mt);
-            mk_zero_f4(a.ss + kSsGu * 64, 16 * (kSsRows - kSsGu), mt);
+          if (r.active && !g.direct) {   // the whole cluster is active or idle in a projection
+            const bool skew = a.skew > 0 && lr == 0 && ((a.skew_where == 2 && ph == 0) || (a.skew_where == 3 && ph == 5));
+            mk_exchange_wait(s, a, l, gi, cl, skew, 903 + gi);
+            mk_mark(tr, 38 + gi);   // exchange received
+            if (ph == 0) mk_qkv_finalize<DH>(a, cl, rk, s.xbuf, s.xss, kc, vc, invD, mt);
+            else if (ph == 5) mk_gu_finalize(a, r.m, rk & 1, s.xbuf, s.xss, invD, mt);
+            else mk_x_finalize(a, r.m, rk, s.xbuf, mt);
           }
         }
         mk_mark(tr, 2 * ph + 2);
@@ -1142,6 +1200,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer of its cluster may still store into it
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -162,6 +162,16 @@ static __global__ void fold_transpose_kernel(const __nv_bfloat16* W, const __nv_
   }
 }
 
+// out[r][k] = in[perm[r]][k]: a row permutation of a row-major [rows][K] bf16 matrix
+static __global__ void gather_rows_kernel(const __nv_bfloat16* in, const int* perm, __nv_bfloat16* out, int rows,
+                                          int K) {
+  const int r = blockIdx.x;
+  if (r >= rows) return;
+  const __nv_bfloat16* src = in + (size_t)perm[r] * K;
+  __nv_bfloat16* dst = out + (size_t)r * K;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) dst[k] = src[k];
+}
+
 // max |w| over n bf16 values into *out (as fp32 bits: non-negative floats
 // order like their bit patterns).  *out must start at 0.
 static __global__ void absmax_bf16_kernel(const __nv_bfloat16* w, size_t n, unsigned* out) {

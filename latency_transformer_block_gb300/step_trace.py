@@ -63,6 +63,30 @@ def phase_table(tr: np.ndarray):
     return work, bar, sub
 
 
+def spread(tr: np.ndarray):
+    """Per projection, percentiles over (block, CTA) of the sub-steps and of
+    the CTA's own end of the phase, relative to the first CTA starting it."""
+    res = {}
+    ends = {"QKV": 2, "O": 10, "gate/up": 12, "down": 16}
+    xrecv = {"QKV": 38, "O": 39, "gate/up": 40, "down": 41}
+    for name, (s0, base) in PROJ_SLOTS.items():
+        vals = []
+        for l in range(tr.shape[0]):
+            st = tr[l, :, s0].astype(np.float64)
+            t0 = st[st > 0].min()
+            rows = tr[l, :, base:base + 4].astype(np.float64)
+            ok = (rows > 0).all(axis=1)
+            if ok.any():
+                xr = tr[l, ok, xrecv[name]][:, None].astype(np.float64)
+                xr = np.where(xr > 0, xr, np.nan)
+                v = np.concatenate([rows[ok], xr, tr[l, ok, ends[name]][:, None].astype(np.float64)], axis=1)
+                vals.append((v - t0) / 1e3)
+        if vals:
+            v = np.concatenate(vals)
+            res[name] = np.nanpercentile(v, [10, 50, 90, 100], axis=0)
+    return res
+
+
 def report(tr: np.ndarray, out=sys.stdout):
     work, bar, sub = phase_table(tr)
     mw = np.median(work, axis=0)
@@ -79,6 +103,14 @@ def report(tr: np.ndarray, out=sys.stdout):
     for name, v in sub.items():
         if v is not None:
             print(f"| {name} | " + " | ".join(f"{x:.2f}" for x in v) + " |", file=out)
+    print("", file=out)
+    print("Spread over CTAs (us from the first CTA's phase start; p10 / p50 / p90 / max):", file=out)
+    print("", file=out)
+    print("| projection | " + " | ".join(SUB) + " | cluster exchange received | CTA's phase end |", file=out)
+    print("|---|" + "---|" * (len(SUB) + 2), file=out)
+    for name, q in spread(tr).items():
+        print(f"| {name} | " + " | ".join(" / ".join(f"{q[i, j]:.2f}" for i in range(4)) for j in range(q.shape[1]))
+              + " |", file=out)
 
 
 def main():

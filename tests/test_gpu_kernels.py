@@ -61,7 +61,7 @@ def test_device_wait_timeout_is_reported_and_cleared():
     assert_rel(got, ref, BLOCK_TOL, "attention after a cleared timeout")
 
 
-@pytest.mark.parametrize("which", [1, 2, 3], ids=["grid_barrier", "qkv_group_wait", "gate_up_tile_wait"])
+@pytest.mark.parametrize("which", [1, 2, 3], ids=["grid_barrier", "qkv_cluster_exchange", "gate_up_cluster_exchange"])
 def test_step_kernel_wait_timeout_is_reported_and_cleared(which):
     """Failure detection of the persistent step kernel's own waits, without a
     GPU fault: one wait of the first block expects an arrival that never comes,
