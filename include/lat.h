@@ -59,7 +59,10 @@ typedef enum {
   LAT_ERR_OOM = 5,        /* device allocation failed in lat_create              */
   LAT_ERR_TIMEOUT = 6,    /* a bounded device-side wait gave up                  */
   LAT_ERR_STATE = 7,      /* call not valid for this context kind / state        */
-  LAT_ERR_UNSUPPORTED = 8 /* no kernel for this device (needs sm_103)            */
+  LAT_ERR_UNSUPPORTED = 8, /* no kernel for this device (needs sm_103)           */
+  LAT_ERR_RANGE = 9       /* an activation reached |x| >= 65504 (or was not finite):
+                             the fp16 operand planes of the action expert's
+                             projections cannot hold it; results meaningless   */
 } lat_status;
 
 typedef enum {
@@ -274,7 +277,10 @@ lat_status lat_debug_indices(lat_ctx *ctx, const lat_chunk_desc *chunks, int n, 
  * 1 = attention output, 2 = gate/up, 3 = down) of blocks layer, layer+1, ...
  * (mod L, so successive launches stream different weights from HBM) on the
  * context's own workspace.  Used to time the weight-streaming kernel alone with
- * events on `stream`.  The workspace accumulators are left dirty: call
+ * events on `stream`.  The block projections are held in the layout of the
+ * persistent step kernel (fp16 = 2^s x the folded weight, QKV rows permuted),
+ * which this bf16 kernel streams as bytes: its outputs are not meaningful,
+ * only its time.  The workspace accumulators are left dirty: call
  * lat_debug_clear before the next lat_denoise_chunk / lat_block_forward.
  */
 lat_status lat_debug_gemm(lat_ctx *ctx, int which, int layer, int reps, void *stream);

@@ -13,12 +13,16 @@ namespace lat {
 // ---------------------------------------------------------------------------
 // Device error word.  Bounded waits that give up OR a code into it; the host
 // reads it in lat_sync.  Codes: 1 = mbarrier wait timeout, 2 = grid barrier
-// timeout.
+// timeout, 4 = activation out of fp16 range.
 // ---------------------------------------------------------------------------
 struct DevErr {
   unsigned int code;
   unsigned int where;  // call-site tag of the first failure
 };
+// error-word bit of an activation that left the range of the fp16 operand
+// planes (|x| >= kF16Max or not finite)
+constexpr unsigned kErrRange = 4u;
+constexpr float kF16Max = 65504.f;
 
 __device__ __forceinline__ void record_error(DevErr* e, unsigned code, unsigned where) {
   if (e) {

@@ -129,7 +129,7 @@ struct lat_ctx {
 
   // workspace
   bf16 *planes_x = nullptr, *planes_o = nullptr, *planes_h = nullptr;   // [3][64][K] activation planes
-  CUtensorMap bmap_x, bmap_o, bmap_h;
+  CUtensorMap bmap_x, bmap_o, bmap_h, pmap_o, pmap_h;
   float *xres = nullptr, *qkv_acc = nullptr, *gu_acc = nullptr, *q = nullptr, *o = nullptr, *r1 = nullptr,
         *r2 = nullptr, *z = nullptr, *pm = nullptr, *pl = nullptr, *po = nullptr, *state_emb = nullptr,
         *temb = nullptr;
@@ -490,6 +490,13 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     LAT_TRY(fold_t(b.wd, nullptr, c->wd + (size_t)l * D * F, F, D));
   }
   LAT_TRY(fold_t(w->w2, nullptr, c->w2, D, D));
+  // the step kernel multiplies the block projections with two fp16 planes of
+  // the activation: each family is held as fp16 = 2^s x the folded bf16 weight
+  // (exact), 2^-s applied in the epilogue
+  LAT_TRY(to_f16_scaled(c->wqkv, (size_t)L * c->nqkv * D, &c->mk.wsc[0]));
+  LAT_TRY(to_f16_scaled(c->wo, (size_t)L * D * qd, &c->mk.wsc[1]));
+  LAT_TRY(to_f16_scaled(c->wgu, (size_t)L * 2 * F * D, &c->mk.wsc[2]));
+  LAT_TRY(to_f16_scaled(c->wd, (size_t)L * D * F, &c->mk.wsc[3]));
   LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * c->nqkv, D, 128));
   LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, qd, 128));
   LAT_TRY(make_kmajor_map(&c->map_gu, c->wgu, L * 2 * F, D, 128));
@@ -591,6 +598,9 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(make_planes_map(&c->bmap_x, c->planes_x, D));
   LAT_TRY(make_planes_map(&c->bmap_o, c->planes_o, qd));
   LAT_TRY(make_planes_map(&c->bmap_h, c->planes_h, F));
+  // the step kernel's operands of the O / down projections: [2][64][K] fp16
+  LAT_TRY(make_kmajor_map(&c->pmap_o, c->planes_o, 128, qd, 128));
+  LAT_TRY(make_kmajor_map(&c->pmap_h, c->planes_h, 128, F, 128));
   LAT_TRY(c->alloc(&c->err, 1));
   CUDA_TRY(cudaMemset(c->qkv_acc, 0, (size_t)T * c->nqkv * 4));
   CUDA_TRY(cudaMemset(c->gu_acc, 0, (size_t)T * 2 * F * 4));
@@ -622,8 +632,8 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     m.part_l = pl;
     m.part_o = po;
     m.x = c->xres;
-    m.o_planes = c->planes_o;
-    m.h_planes = c->planes_h;
+    m.o_planes = reinterpret_cast<__half*>(c->planes_o);
+    m.h_planes = reinterpret_cast<__half*>(c->planes_h);
     m.cos_t = c->cos_t;
     m.sin_t = c->sin_t;
     m.err = c->err;
@@ -717,13 +727,13 @@ static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long lo
   cudaError_t e;
   if (c->d.dh == 64)
     e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->bmap_o, c->bmap_h, a);
+                           c->pmap_o, c->pmap_h, a);
   else if (c->d.dh == 128)
     e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<128>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->bmap_o, c->bmap_h, a);
+                           c->pmap_o, c->pmap_h, a);
   else
     e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<256>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->bmap_o, c->bmap_h, a);
+                           c->pmap_o, c->pmap_h, a);
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch pi0_step: %s", cudaGetErrorString(e));
   return LAT_OK;
 }
@@ -1299,6 +1309,7 @@ const char* lat_status_str(lat_status s) {
     case LAT_ERR_CUDA: return "LAT_ERR_CUDA";
     case LAT_ERR_OOM: return "LAT_ERR_OOM";
     case LAT_ERR_TIMEOUT: return "LAT_ERR_TIMEOUT";
+    case LAT_ERR_RANGE: return "LAT_ERR_RANGE";
     case LAT_ERR_STATE: return "LAT_ERR_STATE";
     case LAT_ERR_UNSUPPORTED: return "LAT_ERR_UNSUPPORTED";
   }
@@ -1376,6 +1387,8 @@ lat_status lat_prefill_kv(lat_ctx* c, const void* patch_emb, int B, void* kv, vo
 static lat_status check_dev_err(lat_ctx* c) {
   DevErr e{};
   CUDA_TRY(cudaMemcpy(&e, c->err, sizeof(e), cudaMemcpyDeviceToHost));
+  if (e.code & kErrRange)
+    return fail(LAT_ERR_RANGE, "an activation left the fp16 operand range (code %u, site %u)", e.code, e.where);
   if (e.code) return fail(LAT_ERR_TIMEOUT, "device wait gave up (code %u, site %u)", e.code, e.where);
   return LAT_OK;
 }

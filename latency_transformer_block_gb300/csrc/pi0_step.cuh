@@ -52,17 +52,18 @@ namespace lat {
 constexpr int kMkThreads = 384;                 // 12 warps
 constexpr int kMkCluster = 4;                   // CTAs per thread-block cluster
 constexpr int kMkNW = 6;                        // weight ring slots
-constexpr int kMkNB = 3;                        // activation-plane ring slots
-constexpr int kMkPre = 4;                       // k-tiles of x the math warps hold in flight (registers)
+constexpr int kMkNB = 4;                        // activation-plane ring slots
+constexpr int kMkPre = 5;                       // k-tiles of x the math warps hold in flight (registers)
 constexpr int kMkWBytes = 128 * 64 * 2;         // one weight tile
-constexpr int kMkBBytes = 192 * 64 * 2;         // one activation tile, three planes
+constexpr int kMkBBytes = 128 * 64 * 2;         // one activation tile, two fp16 planes
 // cluster exchange area (after the operand slots): 4 slots of split-K partial
 // sums [64 tokens][32 rows] fp32, written by the CTAs of the cluster into the
 // CTA that finalizes those rows, then 4 x 64 per-token sums of squares of x
 constexpr int kMkXSlot = 64 * 32 * 4;
 constexpr int kMkXOff = kMkNB * kMkBBytes;
 constexpr int kMkXBytes = 4 * kMkXSlot + 4 * 64 * 4;
-constexpr int kMkRegion = kMkXOff + kMkXBytes;  // also the attention's tiles (its own phase)
+constexpr int kMkRegion = 99 * 1024;            // also the attention's tiles (its own phase)
+static_assert(kMkXOff + kMkXBytes <= kMkRegion, "operand slots and exchange area fit in the region");
 constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 5;
 static_assert(kMkRegion % 1024 == 0, "the weight ring after the region stays 1024-byte aligned");
 
@@ -104,8 +105,9 @@ struct MkArgs {
   int prefix_lm;            // 1: the state token (query row 0) sees the prefix and itself only
   float eps, scale_log2;
   float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
-  __nv_bfloat16* o_planes;  // [3][64][Hq dh] attention output as exact bf16 planes (rows >= T_q stay 0)
-  __nv_bfloat16* h_planes;  // [3][64][F] GeGLU output as exact bf16 planes (rows >= T_q stay 0)
+  __half* o_planes;         // [2][64][Hq dh] attention output as two fp16 planes (rows >= T_q stay 0)
+  __half* h_planes;         // [2][64][F] GeGLU output as two fp16 planes (rows >= T_q stay 0)
+  float wsc[4];             // 2^-s of each projection's weights (held as fp16 = 2^s w, exact)
   __nv_bfloat16* q_planes;  // [2][64][Hq dh] q after RoPE, two-term bf16 (hi, lo)
   __nv_bfloat16* kv_own;    // [k hi, k lo, v hi, v lo][64][Hkv dh] own keys / values, two-term bf16
   float* part_m;            // [n_kb][Hq][T_q]
@@ -318,7 +320,8 @@ __device__ __forceinline__ void mk_load_tile(const float* act, int ld, int kt, c
 }
 
 __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const float* act, int act_ld, bool stats,
-                                             float* out, int ld, int T_q, DevErr* err, unsigned long long* tr) {
+                                             float wsc, float* out, int ld, int T_q, DevErr* err,
+                                             unsigned long long* tr) {
   const MkRange r = mk_range(g, blockIdx.x);
   if (!r.active) return;
   const int nk = r.k1 - r.k0;
@@ -340,6 +343,7 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
     sq[i] = 0.f;
   }
   if (act) {
+    float amax = 0.f;   // largest |x| converted (fp16 planes hold |x| < 65504)
     float4 xv[kMkPre][4];
 #pragma unroll
     for (int u = 0; u < kMkPre; ++u)
@@ -361,13 +365,13 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
               const int col = hh * 32 + 4 * p;
               const float4 v = xv[u][2 * i + hh];
               if (stats) sq[i] += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-              uint32_t h0, m0, l0, h1, m1, l1;
-              split_pair_exact(v.x, v.y, h0, m0, l0);
-              split_pair_exact(v.z, v.w, h1, m1, l1);
+              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+              uint32_t h0, l0, h1, l1;
+              split_pair_h2(v.x, v.y, h0, l0);
+              split_pair_h2(v.z, v.w, h1, l1);
               const uint32_t off = (uint32_t)(t * 128 + ((((col >> 3) ^ t) & 7) << 4) + ((p & 1) << 3));
               *reinterpret_cast<uint2*>(dst + off) = make_uint2(h0, h1);
-              *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(m0, m1);
-              *reinterpret_cast<uint2*>(dst + 16384 + off) = make_uint2(l0, l1);
+              *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(l0, l1);
             }
           }
           fence_proxy_async_smem();
@@ -378,6 +382,7 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
         }
       }
     }
+    if (!(amax < kF16Max)) record_error(err, kErrRange, 33);
   }
   // this K range's per-token sums of squares of x (lanes p == 0 hold rows[i])
   float ssq[2];
@@ -390,7 +395,8 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
     ssq[i] = v;
   }
   // epilogue: warp (4 + mw) reads TMEM lanes 32 q .. +31 = rows of the tile,
-  // tokens 32 ch .. +31 of each plane, sums the planes hi + mid + lo
+  // tokens 32 ch .. +31 of each plane, sums the planes hi + lo and undoes the
+  // weights' power-of-two scale
   if (act) mk_mark(tr, 1);
   mk_wait(s.accfull, s.gc & 1, err, 32);
   mk_mark(tr, 2);
@@ -399,10 +405,10 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
   ++s.gc;
   const int q = mw & 3, ch = mw >> 2;
   const uint32_t tb = acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32);
-  float v[32], w[32], z[32];
-  tmem_ld32x3(tb, tb + 64, tb + 128, v, w, z);
+  float v[32], w[32];
+  tmem_ld32x2(tb, tb + 64, v, w);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = (v[j] + w[j]) + z[j];
+  for (int j = 0; j < 32; ++j) v[j] = (v[j] + w[j]) * wsc;
   tc_fence_before();
   if (g.direct) {
     // each lane quad transposes 4 tokens x its 4 rows, so a lane adds 4
@@ -782,7 +788,8 @@ __device__ __forceinline__ void mk_attention(const MkArgs& a, __nv_bfloat16* kc,
 }
 
 // Phase 4: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s per (token,
-// head), written as the exact bf16 planes of the output projection's operand.  Work comes in
+// head), written as the two fp16 planes of the output projection's operand
+// (o is a weighted mean of cached values, far inside fp16's range).  Work comes in
 // chunks of 256 fragments (the attention's output order); for the <= 2 (head,
 // warp) groups of a chunk the per-row weights 2^(m_s - M) / L go to shared
 // memory first, then each thread merges one fragment over all key blocks.
@@ -884,21 +891,19 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
         acc.z += a1 * z.z;
         acc.w += a1 * z.w;
       }
-      uint32_t hi, mid, lo;
+      uint32_t hi, lo;
       const size_t col = (size_t)h * DH + c;
       if (r0 < a.T_q) {
-        split_pair_exact(acc.x, acc.y, hi, mid, lo);
+        split_pair_h2(acc.x, acc.y, hi, lo);
         uint32_t* d = reinterpret_cast<uint32_t*>(a.o_planes + (size_t)r0 * qd + col);
         d[0] = hi;
-        d[pl / 2] = mid;
-        d[pl] = lo;
+        d[pl / 2] = lo;
       }
       if (r1 < a.T_q) {
-        split_pair_exact(acc.z, acc.w, hi, mid, lo);
+        split_pair_h2(acc.z, acc.w, hi, lo);
         uint32_t* d = reinterpret_cast<uint32_t*>(a.o_planes + (size_t)r1 * qd + col);
         d[0] = hi;
-        d[pl / 2] = mid;
-        d[pl] = lo;
+        d[pl / 2] = lo;
       }
     }
     named_sync(3, 256);   // sw is reused by the next chunk
@@ -910,7 +915,7 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
 // gate/up: rank (i, k) of the cluster (tile 2 c + i, K range k) finalizes the
 // FFN columns 64 m + 32 k .. +31 of its tile m: g and u are the sums of the
 // two K ranges' partials, r = rsqrt(mean(x^2) + eps) of the FFN input, and
-// h = GELU(r g) * (r u) goes out as the exact bf16 planes of the down
+// h = GELU(r g) * (r u) goes out as the two fp16 planes of the down
 // projection's operand.
 __device__ __forceinline__ void mk_gu_finalize(const MkArgs& a, int m, int k, const float* xbuf, const float* xss,
                                                float invD, int mt) {
@@ -927,13 +932,13 @@ __device__ __forceinline__ void mk_gu_finalize(const MkArgs& a, int m, int k, co
     const float h1 = gelu_tanh_fast(rv * (g0.y + g1.y)) * (rv * (u0.y + u1.y));
     const float h2 = gelu_tanh_fast(rv * (g0.z + g1.z)) * (rv * (u0.z + u1.z));
     const float h3 = gelu_tanh_fast(rv * (g0.w + g1.w)) * (rv * (u0.w + u1.w));
-    uint32_t a0, b0, c0, a1, b1, c1;
-    split_pair_exact(h0, h1, a0, b0, c0);
-    split_pair_exact(h2, h3, a1, b1, c1);
+    if (!(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))) < kF16Max)) record_error(a.err, kErrRange, 34);
+    uint32_t a0, b0, a1, b1;
+    split_pair_h2(h0, h1, a0, b0);
+    split_pair_h2(h2, h3, a1, b1);
     uint2* d = reinterpret_cast<uint2*>(a.h_planes + (size_t)t * F + m * 64 + k * 32 + c4);
     d[0] = make_uint2(a0, a1);
     d[pl / 4] = make_uint2(b0, b1);
-    d[pl / 2] = make_uint2(c0, c1);
   }
 }
 
@@ -1048,7 +1053,7 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         mbar_wait(&wfull[i % kMkNW], (i / kMkNW) & 1, nullptr, 0);
     } else if (warp == 1 && lane == 0) {
       // ---------------- MMA issue ----------------
-      const uint32_t idesc = idesc_bf16_f32(128, 192);
+      const uint32_t idesc = idesc_f16_f32(128, 128);   // M = 128 weight rows, N = 2 fp16 planes x 64 tokens
       uint32_t wt = 0, bt = 0, gc = 0, pf = 0, pt = 0;   // pf / pt: per-slot parities of bfull / bfullt
       bool ok = true;
       for (int l = a.l0; l < a.l1 && ok; ++l)
@@ -1183,8 +1188,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
           const MkGemm& g = a.g[gi];
           const MkRange r = mk_range(g, blockIdx.x);
-          mk_gemm_math(s, g, ph == 0 || ph == 5 ? a.x : nullptr, a.D, ph == 0 || ph == 5, a.x, a.D, a.T_q, a.err,
-                       tr ? tr + 20 + 4 * gi : nullptr);
+          mk_gemm_math(s, g, ph == 0 || ph == 5 ? a.x : nullptr, a.D, ph == 0 || ph == 5, a.wsc[gi], a.x, a.D,
+                       a.T_q, a.err, tr ? tr + 20 + 4 * gi : nullptr);
           if (r.active && !g.direct) {   // the whole cluster is active or idle in a projection
             const bool skew = a.skew > 0 && lr == 0 && ((a.skew_where == 2 && ph == 0) || (a.skew_where == 3 && ph == 5));
             mk_exchange_wait(s, a, l, gi, cl, skew, 903 + gi);

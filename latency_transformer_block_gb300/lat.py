@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(HERE, "liblat.so")
 
 LAT_PI0_ACTION_EXPERT, LAT_PI0_PREFIX, LAT_DIT = 0, 1, 2
 STATUS = ["LAT_OK", "LAT_ERR_ARG", "LAT_ERR_SHAPE", "LAT_ERR_ALIGN", "LAT_ERR_CUDA", "LAT_ERR_OOM",
-          "LAT_ERR_TIMEOUT", "LAT_ERR_STATE", "LAT_ERR_UNSUPPORTED"]
+          "LAT_ERR_TIMEOUT", "LAT_ERR_STATE", "LAT_ERR_UNSUPPORTED", "LAT_ERR_RANGE"]
 
 
 class LatError(RuntimeError):
