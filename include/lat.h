@@ -415,6 +415,15 @@ lat_status lat_debug_timeout(lat_ctx *ctx, void *stream);
  */
 lat_status lat_debug_wait_skew(lat_ctx *ctx, int which, int extra);
 
+/*
+ * lat_debug_act_terms -- precision study of the dense path (LAT_PI0_PREFIX,
+ * LAT_DIT): the block projections multiply `terms` fp16 planes of their
+ * activation (2, the default: hi + lo, 22 significant bits; 1: hi only, 11
+ * bits, half the tensor work).  For measuring the error of one plane against
+ * the oracle; not meant for production use.
+ */
+lat_status lat_debug_act_terms(lat_ctx *ctx, int terms);
+
 /* Human-readable name of a status; message of the last failure on this thread. */
 const char *lat_status_str(lat_status s);
 const char *lat_last_error(void);

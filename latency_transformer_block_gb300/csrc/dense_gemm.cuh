@@ -65,16 +65,20 @@ struct DenseArgs {
   DevErr* err;
 };
 
-// Tile order: groups of kDGroupM m-tiles, m fastest within a group and the
+// Tile order: groups of `group` m-tiles, m fastest within a group and the
 // group's n-tiles in turn.  A wave of CTAs then covers a block of about
-// kDGroupM m-tiles x (grid / kDGroupM) n-tiles: each weight tile crosses from
-// HBM once per group (its kDGroupM readers run together) and the group's
-// activation rows stay in L2 while the group sweeps the n-tiles.
+// `group` m-tiles x (grid / group) n-tiles: each weight tile crosses from HBM
+// once per group (its readers run together) and the group's activation rows
+// stay in L2 while the group sweeps the n-tiles.  With at most kDGroupAll
+// m-tiles (activation planes of ~42 MB) one group takes them all, so every
+// weight tile crosses from HBM once; more m-tiles go in groups of kDGroupM.
 constexpr int kDGroupM = 8;
+constexpr int kDGroupAll = 16;
 __device__ __forceinline__ void dense_tile(int t, int m_tiles, int n_tiles, int& tm, int& tn) {
-  const int grp = t / (kDGroupM * n_tiles);
-  const int m0 = grp * kDGroupM, gm = min(kDGroupM, m_tiles - m0);
-  const int r = t - grp * kDGroupM * n_tiles;
+  const int group = m_tiles <= kDGroupAll ? m_tiles : kDGroupM;
+  const int grp = t / (group * n_tiles);
+  const int m0 = grp * group, gm = min(group, m_tiles - m0);
+  const int r = t - grp * group * n_tiles;
   tm = m0 + r % gm;
   tn = r / gm;
 }

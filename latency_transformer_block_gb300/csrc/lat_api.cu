@@ -158,6 +158,7 @@ struct lat_ctx {
   __half* hist16 = nullptr;    // fp16 copy of one call's history K/V planes, [planes][T_q][D] (DiT)
   int hist_rows = 0;
   __half *act2 = nullptr, *act2f = nullptr;   // fp16 activation planes [M][kActTerms * K]
+  int act_terms = kActTerms;   // planes of the activation the block projections multiply (1: hi only)
   // the four block projections (merged QKV, output, FFN in, FFN out) of the dense
   // path are held as fp16 = 2^s x folded bf16 weight; wscale = 2^-s per matrix
   float wscale[4] = {1.f, 1.f, 1.f, 1.f};
@@ -1106,7 +1107,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     LAT_TRY(launch_check("norm_split"));
     {
       DenseArgs a{};
-      a.M = M; a.K = D; a.terms = kActTerms; a.epi = E_STORE; a.out = c->qkvbuf;
+      a.M = M; a.K = D; a.terms = c->act_terms; a.epi = E_STORE; a.out = c->qkvbuf;
       if (last) { a.N = 2 * kvd; a.w_row0 = l * c->nqkv + qd; a.ldo = 2 * kvd; }
       else { a.N = c->nqkv; a.w_row0 = l * c->nqkv; a.ldo = c->nqkv; }
       LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, a, st));
@@ -1136,20 +1137,20 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     LAT_TRY(enqueue_attention_seg(c, sa, B, st));
     {
       DenseArgs a{};
-      a.M = M; a.N = D; a.K = qd; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
+      a.M = M; a.N = D; a.K = qd; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
       LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
     }
     norm_split_kernel<<<M, 256, 0, st>>>(na);
     LAT_TRY(launch_check("norm_split"));
     {
       DenseArgs a{};
-      a.M = M; a.N = 2 * F; a.K = D; a.terms = kActTerms; a.w_row0 = l * 2 * F; a.epi = E_GEGLU_SPLIT;
+      a.M = M; a.N = 2 * F; a.K = D; a.terms = c->act_terms; a.w_row0 = l * 2 * F; a.epi = E_GEGLU_SPLIT;
       a.act2 = c->act2f; a.ldh = F;
       LAT_TRY(enqueue_dense(c, c->map_act_d, W_UP, a, st));
     }
     {
       DenseArgs a{};
-      a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
+      a.M = M; a.N = D; a.K = F; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
       LAT_TRY(enqueue_dense(c, c->map_act_f, W_DOWN, a, st));
     }
   }
@@ -1178,7 +1179,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   LAT_TRY(launch_check("norm_split"));
   {
     DenseArgs a{};
-    a.M = M; a.N = 3 * D; a.K = D; a.terms = kActTerms; a.w_row0 = l * 3 * D; a.epi = E_STORE; a.out = c->qkvbuf;
+    a.M = M; a.N = 3 * D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * 3 * D; a.epi = E_STORE; a.out = c->qkvbuf;
     a.ldo = 3 * D;
     LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, a, st));
   }
@@ -1237,7 +1238,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   LAT_TRY(enqueue_attention_seg(c, sa, n, st));
   {
     DenseArgs a{};
-    a.M = M; a.N = D; a.K = D; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
+    a.M = M; a.N = D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
     a.gate = c->adaln; a.rows_per_chunk = T;
     for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 2 * D;
     LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
@@ -1250,12 +1251,12 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   LAT_TRY(launch_check("norm_split"));
   {
     DenseArgs a{};
-    a.M = M; a.N = F; a.K = D; a.terms = kActTerms; a.w_row0 = l * F; a.epi = E_GELU_SPLIT; a.act2 = c->act2f; a.ldh = F;
+    a.M = M; a.N = F; a.K = D; a.terms = c->act_terms; a.w_row0 = l * F; a.epi = E_GELU_SPLIT; a.act2 = c->act2f; a.ldh = F;
     LAT_TRY(enqueue_dense(c, c->map_act_d, W_UP, a, st));
   }
   {
     DenseArgs a{};
-    a.M = M; a.N = D; a.K = F; a.terms = kActTerms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
+    a.M = M; a.N = D; a.K = F; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID_GATE; a.out = x; a.ldo = D;
     a.gate = c->adaln; a.rows_per_chunk = T;
     for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 5 * D;
     LAT_TRY(enqueue_dense(c, c->map_act_f, W_DOWN, a, st));
@@ -1683,6 +1684,14 @@ lat_status lat_clear_error(lat_ctx* c) {
   if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemset(c->err, 0, sizeof(DevErr)));
+  return LAT_OK;
+}
+
+lat_status lat_debug_act_terms(lat_ctx* c, int terms) {
+  if (!c) return fail(LAT_ERR_ARG, "ctx is NULL");
+  if (c->d.kind != LAT_PI0_PREFIX && c->d.kind != LAT_DIT) return fail(LAT_ERR_STATE, "dense contexts only");
+  if (terms < 1 || terms > kActTerms) return fail(LAT_ERR_ARG, "terms must be 1 or 2");
+  c->act_terms = terms;
   return LAT_OK;
 }
 

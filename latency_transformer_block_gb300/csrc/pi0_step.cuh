@@ -491,13 +491,44 @@ __device__ __forceinline__ void mk_exchange_wait(MkMath& s, const MkArgs& a, int
 // ranges times r = rsqrt(mean(x^2) + eps), RoPE on q and k heads, two-term
 // bf16 planes into q_planes / kv_own, and k, v (nearest bf16) into the cache
 // at slot T_prefix + t.
+// The rotation angles of a thread's (at most 4) items, loaded before the
+// exchange wait so that their latency overlaps it.
+struct MkRot {
+  float c[4], s[4];
+};
+
+template <int DH>
+__device__ __forceinline__ MkRot mk_qkv_angles(const MkArgs& a, int u, int j, int mt) {
+  constexpr int PPH = DH / 2;
+  MkRot rot;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    const int it = mt + 256 * n;
+    rot.c[n] = 1.f;
+    rot.s[n] = 0.f;
+    if (it < a.T_q * 16) {
+      const int t = it >> 4, c = it & 15;
+      const int P = 64 * u + 16 * j + c;
+      if (P / PPH < a.Hq + a.Hkv) {
+        rot.c[n] = __ldg(a.cos_t + (size_t)t * PPH + P % PPH);
+        rot.s[n] = __ldg(a.sin_t + (size_t)t * PPH + P % PPH);
+      }
+    }
+  }
+  return rot;
+}
+
 template <int DH>
 __device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int u, int j, const float* xbuf, const float* xss,
-                                                __nv_bfloat16* kc, __nv_bfloat16* vc, float invD, int mt) {
+                                                __nv_bfloat16* kc, __nv_bfloat16* vc, float invD, const MkRot& rot,
+                                                int mt) {
   constexpr int PPH = DH / 2;   // rotary pairs per head
   const int qd = a.Hq * DH, kvd = a.Hkv * DH;
   const size_t qpl = (size_t)64 * qd, kpl = (size_t)64 * kvd;
-  for (int it = mt; it < a.T_q * 16; it += 256) {
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {   // T_q <= 64: at most 4 items of 16 pairs x T_q tokens per thread
+    const int it = mt + 256 * n;
+    if (it >= a.T_q * 16) break;
     const int t = it >> 4, c = it & 15;
     float x0 = 0.f, x1 = 0.f;
 #pragma unroll
@@ -511,12 +542,9 @@ __device__ __forceinline__ void mk_qkv_finalize(const MkArgs& a, int u, int j, c
     x1 *= rv;
     const int P = 64 * u + 16 * j + c;
     const int head = P / PPH, i = P % PPH;
-    float y0 = x0, y1 = x1;
-    if (head < a.Hq + a.Hkv) {   // q and k heads are rotated
-      const float cs = __ldg(a.cos_t + (size_t)t * PPH + i), sn = __ldg(a.sin_t + (size_t)t * PPH + i);
-      y0 = x0 * cs - x1 * sn;
-      y1 = x1 * cs + x0 * sn;
-    }
+    // q and k heads are rotated (v heads carry cos 1, sin 0)
+    const float y0 = x0 * rot.c[n] - x1 * rot.s[n];
+    const float y1 = x1 * rot.c[n] + x0 * rot.s[n];
     const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
     const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
     const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
@@ -1192,9 +1220,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
                        a.T_q, a.err, tr ? tr + 20 + 4 * gi : nullptr);
           if (r.active && !g.direct) {   // the whole cluster is active or idle in a projection
             const bool skew = a.skew > 0 && lr == 0 && ((a.skew_where == 2 && ph == 0) || (a.skew_where == 3 && ph == 5));
+            MkRot rot;
+            if (ph == 0) rot = mk_qkv_angles<DH>(a, cl, rk, mt);
             mk_exchange_wait(s, a, l, gi, cl, skew, 903 + gi);
             mk_mark(tr, 38 + gi);   // exchange received
-            if (ph == 0) mk_qkv_finalize<DH>(a, cl, rk, s.xbuf, s.xss, kc, vc, invD, mt);
+            if (ph == 0) mk_qkv_finalize<DH>(a, cl, rk, s.xbuf, s.xss, kc, vc, invD, rot, mt);
             else if (ph == 5) mk_gu_finalize(a, r.m, rk & 1, s.xbuf, s.xss, invD, mt);
             else mk_x_finalize(a, r.m, rk, s.xbuf, mt);
           }

@@ -97,6 +97,8 @@ def lib():
         L.lat_debug_timeout.restype = st
         L.lat_debug_wait_skew.argtypes = [_P, ctypes.c_int, ctypes.c_int]
         L.lat_debug_wait_skew.restype = st
+        L.lat_debug_act_terms.argtypes = [_P, ctypes.c_int]
+        L.lat_debug_act_terms.restype = st
         L.lat_sync.argtypes = [_P]
         L.lat_sync.restype = st
         L.lat_status_str.argtypes = [ctypes.c_int]
@@ -212,6 +214,10 @@ class Context:
 
     def debug_timeout(self, stream=None):
         check(lib().lat_debug_timeout(self.handle, stream_ptr(stream)))
+
+    def debug_act_terms(self, terms):
+        """Dense path: multiply 1 or 2 fp16 planes of the activation (precision study)."""
+        check(lib().lat_debug_act_terms(self.handle, terms))
 
     def debug_wait_skew(self, which, extra):
         """Make one bounded wait of the step kernel's first block expect `extra` arrivals too many."""
