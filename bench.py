@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-dense", action="store_true",
                    help="skip timing the dense configurations in the headline run")
+    p.add_argument("--layers", type=int, default=0,
+                   help="dense workloads: run this many blocks instead of the configuration's "
+                        "(same per-block shapes; for small profiler captures)")
     p.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "pi0_cycle"] + list(DENSE_WORKLOADS),
                    help="pi0_ae (default: the headline line) or one dense configuration")
     return p.parse_args()
@@ -419,16 +422,17 @@ def device_weights(make, cfg, dev, seed=0):
     return out
 
 
-def dense_measure(workload, steps, warmup, dev):
+def dense_measure(workload, steps, warmup, dev, layers=0):
     """Time one dense configuration (CUDA events on its stream) and the dense
-    GEMM alone on its FFN-in projection; returns the full line and a summary."""
+    GEMM alone on its FFN-in projection; returns the full line and a summary.
+    layers > 0 runs that many blocks instead of the configuration's."""
     import torch
     from latency_transformer_block_gb300 import build as B
     B.build()
     from latency_transformer_block_gb300 import synth
     from latency_transformer_block_gb300.models import DitStage, Pi0Prefix
     name, nb, metric, unit = DENSE_WORKLOADS[workload]
-    cfg = synth.config(name)
+    cfg = synth.config(name, **({"L": layers} if layers > 0 else {}))
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     stream = torch.cuda.Stream(dev)
@@ -551,7 +555,10 @@ def run_dense(args):
     import torch
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    r = dense_measure(args.workload, args.steps, args.warmup, dev)
+    r = dense_measure(args.workload, args.steps, args.warmup, dev, args.layers)
+    if args.layers > 0:
+        r["line"]["config"]["blocks_run"] = args.layers
+        r["line"]["config"]["note"] = "fewer blocks than the configuration (profiling run)"
     print(json.dumps(r["line"]), flush=True)
 
 
