@@ -13,7 +13,7 @@ namespace lat {
 // ---------------------------------------------------------------------------
 // Device error word.  Bounded waits that give up OR a code into it; the host
 // reads it in lat_sync.  Codes: 1 = mbarrier wait timeout, 2 = grid barrier
-// timeout, 4 = activation out of fp16 range.
+// timeout, 4 = activation out of fp16 range, 8 = launched without its clusters.
 // ---------------------------------------------------------------------------
 struct DevErr {
   unsigned int code;
@@ -22,6 +22,9 @@ struct DevErr {
 // error-word bit of an activation that left the range of the fp16 operand
 // planes (|x| >= kF16Max or not finite)
 constexpr unsigned kErrRange = 4u;
+// error-word bit of a kernel launched without the thread-block clusters it
+// exchanges data in (it then returns before touching another CTA's memory)
+constexpr unsigned kErrLaunch = 8u;
 constexpr float kF16Max = 65504.f;
 
 __device__ __forceinline__ void record_error(DevErr* e, unsigned code, unsigned where) {
@@ -92,6 +95,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevErr
 // ---------------------------------------------------------------------------
 // thread-block clusters (distributed shared memory)
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

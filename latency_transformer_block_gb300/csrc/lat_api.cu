@@ -1388,6 +1388,8 @@ lat_status lat_prefill_kv(lat_ctx* c, const void* patch_emb, int B, void* kv, vo
 static lat_status check_dev_err(lat_ctx* c) {
   DevErr e{};
   CUDA_TRY(cudaMemcpy(&e, c->err, sizeof(e), cudaMemcpyDeviceToHost));
+  if (e.code & kErrLaunch)
+    return fail(LAT_ERR_CUDA, "the step kernel ran without its clusters of %d CTAs (site %u)", kMkCluster, e.where);
   if (e.code & kErrRange)
     return fail(LAT_ERR_RANGE, "an activation left the fp16 operand range (code %u, site %u)", e.code, e.where);
   if (e.code) return fail(LAT_ERR_TIMEOUT, "device wait gave up (code %u, site %u)", e.code, e.where);

@@ -996,6 +996,14 @@ __global__ void __launch_bounds__(kMkThreads, 1)
                     const __grid_constant__ CUtensorMap w_gu, const __grid_constant__ CUtensorMap w_d,
                     const __grid_constant__ CUtensorMap act_op, const __grid_constant__ CUtensorMap act_hp,
                     const MkArgs a) {
+  // the CTAs exchange partial sums with the other CTAs of their cluster of 4:
+  // launched any other way (a replay by a tool that drops the cluster shape)
+  // every CTA records the error and returns before any barrier, TMEM or
+  // distributed shared-memory access
+  if (cluster_size() != (uint32_t)kMkCluster || gridDim.x % kMkCluster != 0) {
+    if (threadIdx.x == 0) record_error(a.err, kErrLaunch, 950);
+    return;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sW = smem;

@@ -87,6 +87,28 @@ def spread(tr: np.ndarray):
     return res
 
 
+ATTN = [("q and key tiles loaded", 17), ("own-key lo planes loaded", 18), ("P V done", 19), ("partials stored", 6)]
+COMB = [("weights of the rows", 36), ("merged, planes stored", 37)]
+
+
+def attention_spread(tr: np.ndarray):
+    """Attention and combine sub-steps: percentiles over (block, CTA) of each
+    mark, us from the first CTA's phase start."""
+    res = {}
+    for name, s0, marks in (("attention", 5, ATTN), ("combine", 7, COMB)):
+        vals = []
+        for l in range(tr.shape[0]):
+            st = tr[l, :, s0].astype(np.float64)
+            t0 = st[st > 0].min()
+            cols = tr[l, :, [m for _, m in marks]].T.astype(np.float64)
+            ok = (cols > 0).all(axis=1)
+            if ok.any():
+                vals.append((cols[ok] - t0) / 1e3)
+        if vals:
+            res[name] = (marks, np.percentile(np.concatenate(vals), [10, 50, 90, 100], axis=0))
+    return res
+
+
 def report(tr: np.ndarray, out=sys.stdout):
     work, bar, sub = phase_table(tr)
     mw = np.median(work, axis=0)
@@ -111,6 +133,11 @@ def report(tr: np.ndarray, out=sys.stdout):
     for name, q in spread(tr).items():
         print(f"| {name} | " + " | ".join(" / ".join(f"{q[i, j]:.2f}" for i in range(4)) for j in range(q.shape[1]))
               + " |", file=out)
+    print("", file=out)
+    for name, (marks, q) in attention_spread(tr).items():
+        print(f"{name} (us from the first CTA's phase start; p10 / p50 / p90 / max):", file=out)
+        for j, (label, _) in enumerate(marks):
+            print(f"  {label}: " + " / ".join(f"{q[i, j]:.2f}" for i in range(4)), file=out)
 
 
 def main():
