@@ -205,15 +205,19 @@ lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_
  * Defined by: the reading note's section 2 (the expert reuses the prefix KV
  * cache over 10 flow-matching steps of 18 blocks each, 63 action + 1 state
  * token), section 4.2 (the time embedding folded into a per-step table) and
- * section 3 (the loop replayed as one captured CUDA graph); each step ends in
- * the Euler update x <- x + dt * v.
+ * section 3 (launch gaps are what the expert's time is lost to); each step
+ * ends in the Euler update x <- x + dt * v.  The whole chunk -- state token,
+ * then per step the embedding, W2, the L blocks and the head with its Euler
+ * update -- is ONE launch of the persistent step kernel (grid barriers between
+ * its phases), preceded by a 128-byte clear of its barrier counter.
  *  kv:    device bf16 [L][2][T_prefix + T_q][Hkv*dh] (slots >= T_prefix are
  *         overwritten with the query tokens' K/V at every step);
  *  state: device fp32 [act_dim];
  *  x:     device fp32 [T_q - 1][act_dim]: the initial noise in, the actions out
- *         (x <- x + dt * v after every step).
- * The first call for a given (kv, state, x, stream) captures the whole loop in
- * a CUDA graph; later calls replay it.  The context keeps the graphs of up to 4
+ *         (written once, after the last step; the steps in between keep the
+ *         actions in the context's own buffers).
+ * The first call for a given (kv, state, x, stream) captures the clear and the
+ * launch in a CUDA graph; later calls replay it.  The context keeps the graphs of up to 4
  * such tuples (e.g. two caches used in turn while the next one is prefilled on
  * another stream); a fifth replaces the least recently used one.
  */

@@ -146,6 +146,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // Asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte
 // aligned) from this CTA's shared memory into shared memory of a CTA of the
 // cluster; the bytes complete a transaction on that CTA's mbarrier `mbar`.
+// global -> this CTA's shared memory, completing on an mbarrier of this CTA
+// (addresses 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "r"(src), "r"(bytes), "r"(mbar)

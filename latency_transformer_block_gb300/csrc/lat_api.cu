@@ -118,18 +118,18 @@ struct lat_ctx {
   bf16 *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr, *w2 = nullptr;
   CUtensorMap map_qkv, map_o, map_gu, map_d, map_w2;
   int nqkv = 0;
-  GemmPlan g_qkv{}, g_o{}, g_gu{}, g_d{}, g_w2{};
+  GemmPlan g_qkv{}, g_o{}, g_gu{}, g_d{};
 
   // action-expert tables (fp32)
-  float *wfold = nullptr, *ttab = nullptr, *b2 = nullptr, *wout = nullptr, *bout = nullptr, *dt = nullptr;
+  float *wfold = nullptr, *ttab = nullptr, *b2 = nullptr, *gfin = nullptr, *bout = nullptr, *dt = nullptr;
   bf16 *w_state = nullptr, *b_state = nullptr, *w1_keep = nullptr, *b1_keep = nullptr, *w_in_keep = nullptr,
-       *b_in_keep = nullptr;
+       *b_in_keep = nullptr, *w_out = nullptr;
   float* cos_t = nullptr;
   float* sin_t = nullptr;
 
   // workspace
   bf16 *planes_x = nullptr, *planes_o = nullptr, *planes_h = nullptr;   // [3][64][K] activation planes
-  CUtensorMap bmap_x, bmap_o, bmap_h, pmap_o, pmap_h;
+  CUtensorMap bmap_x, bmap_o, bmap_h, pmap_o, pmap_h, pmap_e;
   float *xres = nullptr, *qkv_acc = nullptr, *gu_acc = nullptr, *q = nullptr, *o = nullptr, *r1 = nullptr,
         *r2 = nullptr, *z = nullptr, *pm = nullptr, *pl = nullptr, *po = nullptr, *state_emb = nullptr,
         *temb = nullptr;
@@ -404,6 +404,13 @@ static lat_status build_schedule(lat_ctx* c, const std::vector<double>& t) {
   return LAT_OK;
 }
 
+// the step kernel for a head dimension: the blocks of one step, or a whole chunk
+static const void* step_kernel(int dh, bool chunk) {
+  if (dh == 64) return chunk ? (const void*)pi0_step_kernel<64, true> : (const void*)pi0_step_kernel<64, false>;
+  if (dh == 128) return chunk ? (const void*)pi0_step_kernel<128, true> : (const void*)pi0_step_kernel<128, false>;
+  return chunk ? (const void*)pi0_step_kernel<256, true> : (const void*)pi0_step_kernel<256, false>;
+}
+
 // Grid of the persistent step kernel: as many clusters of kMkCluster CTAs
 // (one CTA per SM) as can be resident at once, which its grid barriers need.
 static lat_status step_grid(lat_ctx* c) {
@@ -420,9 +427,7 @@ static lat_status step_grid(lat_ctx* c) {
   cfg.numAttrs = 1;
   int n = 0;
   cudaError_t e;
-  if (c->d.dh == 64) e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<64>, &cfg);
-  else if (c->d.dh == 128) e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<128>, &cfg);
-  else e = cudaOccupancyMaxActiveClusters(&n, pi0_step_kernel<256>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, step_kernel(c->d.dh, true), &cfg);
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
   n = std::min(n, c->num_sms / kMkCluster);
   if (n < 1) return fail(LAT_ERR_UNSUPPORTED, "no cluster of %d step-kernel CTAs fits on this device", kMkCluster);
@@ -498,6 +503,7 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(to_f16_scaled(c->wo, (size_t)L * D * qd, &c->mk.wsc[1]));
   LAT_TRY(to_f16_scaled(c->wgu, (size_t)L * 2 * F * D, &c->mk.wsc[2]));
   LAT_TRY(to_f16_scaled(c->wd, (size_t)L * D * F, &c->mk.wsc[3]));
+  LAT_TRY(to_f16_scaled(c->w2, (size_t)D * D, &c->mk.wsc[4]));
   LAT_TRY(make_kmajor_map(&c->map_qkv, c->wqkv, L * c->nqkv, D, 128));
   LAT_TRY(make_kmajor_map(&c->map_o, c->wo, L * D, qd, 128));
   LAT_TRY(make_kmajor_map(&c->map_gu, c->wgu, L * 2 * F, D, 128));
@@ -507,7 +513,6 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   c->g_o = plan_gemm(D, qd, c->num_sms);
   c->g_gu = plan_gemm(2 * F, D, c->num_sms);
   c->g_d = plan_gemm(D, F, c->num_sms);
-  c->g_w2 = plan_gemm(D, D, c->num_sms);
 
   // --- embedding / head (fp32 folds) ---
   LAT_TRY(c->alloc(&c->w_in_keep, (size_t)A * D));
@@ -527,7 +532,8 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(c->alloc(&c->temb, (size_t)d.S * D));
   LAT_TRY(c->alloc(&c->dt, (size_t)d.S));
   LAT_TRY(c->alloc(&c->b2, (size_t)D));
-  LAT_TRY(c->alloc(&c->wout, (size_t)D * A));
+  LAT_TRY(c->alloc(&c->gfin, (size_t)D));
+  LAT_TRY(c->alloc(&c->w_out, (size_t)D * A));
   LAT_TRY(c->alloc(&c->bout, (size_t)A));
   // W' = W_in W1[0:D]
   LAT_TRY(small_gemm(w->w_in, true, D, w->w1, true, D, nullptr, false, c->wfold, D, A, D, D, 0));
@@ -535,9 +541,9 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
   LAT_TRY(launch_check("b2"));
   bf16_to_f32_kernel<<<(A + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->b_out), c->bout, A);
   LAT_TRY(launch_check("bout"));
-  scale_rows_f32_kernel<<<(D * A + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->w_out),
-                                                       reinterpret_cast<const bf16*>(w->g_final), c->wout, D, A);
-  LAT_TRY(launch_check("wout"));
+  bf16_to_f32_kernel<<<(D + 255) / 256, 256>>>(reinterpret_cast<const bf16*>(w->g_final), c->gfin, D);
+  LAT_TRY(launch_check("g_final"));
+  CUDA_TRY(cudaMemcpy(c->w_out, w->w_out, (size_t)D * A * 2, cudaMemcpyDeviceToDevice));
 
   // --- RoPE tables for the query positions (float64 -> fp32) ---
   const int half = d.dh / 2;
@@ -671,6 +677,39 @@ static lat_status create_pi0(lat_ctx* c, const lat_weights* w) {
     if (gu.MT % 2 || gu.MT / 2 > NC || gu.KT < 2)
       return fail(LAT_ERR_SHAPE, "gate/up tiles (2F / 128 = %d) exceed twice the co-resident clusters (%d)",
                   gu.MT, NC);
+    // a whole chunk in one launch: W2 (the embedding's second projection) adds
+    // its K ranges into the residual rows like O and down; the head and the
+    // embedding take one CTA per action row
+    MkGemm& g2 = m.g[4];
+    g2 = MkGemm{D / 128, D / 64, D, 0, 0, 1, 0};
+    g2.splits = std::min(c->step_grid / g2.MT, g2.KT);
+    if (g2.splits < 1) return fail(LAT_ERR_SHAPE, "W2 projection exceeds the grid");
+    // the head and embedding: a pair of CTAs per action row, one for the state row
+    if (2 * (T - 1) + 1 > c->step_grid)
+      return fail(LAT_ERR_SHAPE, "%d action rows need %d step-kernel CTAs (%d)", T - 1, 2 * (T - 1) + 1, c->step_grid);
+    if (A % 4 || 1024 % A || A > 256)
+      return fail(LAT_ERR_SHAPE, "act_dim %d: the fused head needs a multiple of 4 dividing 1024", A);
+    if ((size_t)D * A * 2 > (size_t)kMkXOff || (size_t)(D + 1024 + D / 2 + A + 16) * 4 > (size_t)(kMkRegion - kMkXOff))
+      return fail(LAT_ERR_SHAPE, "width %d x act_dim %d: the fused head exceeds the step kernel's shared memory", D, A);
+    float* ab = nullptr;
+    LAT_TRY(c->alloc(&ab, (size_t)2 * (T - 1) * A));
+    m.act_buf = ab;
+    bf16* ep = nullptr;   // [2][64][D] fp16 planes of the embedding
+    LAT_TRY(c->alloc(&ep, (size_t)2 * 64 * D));
+    CUDA_TRY(cudaMemset(ep, 0, (size_t)2 * 64 * D * 2));   // row 0 (the state token) and rows >= T_q stay 0
+    LAT_TRY(make_kmajor_map(&c->pmap_e, ep, 128, D, 128));
+    m.e_planes = reinterpret_cast<__half*>(ep);
+    m.A = A;
+    m.w_state = c->w_state;
+    m.b_state = c->b_state;
+    m.state_emb = c->state_emb;
+    m.wfold = c->wfold;
+    m.ttab = c->ttab;
+    m.b2 = c->b2;
+    m.w_out = reinterpret_cast<const __nv_bfloat16*>(c->w_out);
+    m.g_final = c->gfin;
+    m.bout = c->bout;
+    m.dt = c->dt;
   }
 
   std::vector<double> t(d.S + 1);
@@ -700,17 +739,22 @@ static lat_status enqueue_attention(const lat_model_desc& d, const float* q, int
 }
 
 // ---------------------------------------------------------------------------
-// layers [l0, l1) of one denoise step on ctx->xres, one persistent launch in
-// clusters of 4 (cooperative: every CTA is resident, which the grid barriers
-// need)
+// Persistent step kernel, one launch in clusters of 4 (cooperative: every CTA
+// is resident, which the grid barriers need).  steps == 0: layers [l0, l1) of
+// one denoise step on ctx->xres.  steps > 0: the whole chunk of `steps`
+// denoise steps on the actions x (noise in, actions out) with the robot state.
 // ---------------------------------------------------------------------------
-static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long long kv_stride, cudaStream_t st) {
+static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long long kv_stride, cudaStream_t st,
+                                   int steps = 0, float* x = nullptr, const float* state = nullptr) {
   CUDA_TRY(cudaMemsetAsync(c->mk_zero, 0, c->mk_zero_bytes, st));
   MkArgs a = c->mk;
   a.l0 = l0;
   a.l1 = l1;
   a.kv = kv;
   a.kv_stride = kv_stride;
+  a.steps = steps;
+  a.act = x;
+  a.state = state;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c->step_grid);
   cfg.blockDim = dim3(kMkThreads);
@@ -725,40 +769,18 @@ static lat_status enqueue_pi0_step(lat_ctx* c, int l0, int l1, bf16* kv, long lo
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e;
-  if (c->d.dh == 64)
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<64>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->pmap_o, c->pmap_h, a);
-  else if (c->d.dh == 128)
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<128>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->pmap_o, c->pmap_h, a);
-  else
-    e = cudaLaunchKernelEx(&cfg, pi0_step_kernel<256>, c->map_qkv, c->map_o, c->map_gu, c->map_d,
-                           c->pmap_o, c->pmap_h, a);
+  void* args[] = {&c->map_qkv, &c->map_o, &c->map_gu, &c->map_d, &c->pmap_o, &c->pmap_h, &c->map_w2, &c->pmap_e, &a};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, step_kernel(c->d.dh, steps > 0), args);
   if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "launch pi0_step: %s", cudaGetErrorString(e));
   return LAT_OK;
 }
 
+// one denoised chunk: state token, then per step the embedding, W2, every
+// block and the head + Euler update, all inside one step-kernel launch
 static lat_status enqueue_denoise(lat_ctx* c, bf16* kv, const float* state, float* x, cudaStream_t st) {
   const lat_model_desc& d = c->d;
-  const int D = d.D, T = d.T_q, A = d.act_dim;
-  const int T_kv = d.T_prefix + d.T_q;
-  const size_t layer_elems = (size_t)2 * T_kv * d.Hkv * d.dh;
-  // state token (once per chunk)
-  LAT_TRY(small_gemm(state, false, A, c->w_state, true, D, c->b_state, true, c->state_emb, D, 1, D, A, 0, st));
-  for (int s = 0; s < d.S; ++s) {
-    EmbedArgs e{x, c->wfold, c->ttab, c->b2, c->state_emb, c->planes_x, c->xres, D, A, T, s};
-    PDL_TRY("embed_prologue", launch_pdl(embed_prologue_kernel, dim3((D + 255) / 256, T), dim3(256), 0, st, e));
-    {
-      SkinnyArgs a{};
-      a.n_tok = T - 1; a.out = c->xres + D; a.out_ld = D;
-      LAT_TRY(enqueue_skinny(c, c->map_w2, c->bmap_x, c->g_w2, 0, a, st));
-    }
-    LAT_TRY(enqueue_pi0_step(c, 0, d.L, kv, (long long)layer_elems, st));
-    HeadArgs h{c->xres, c->wout, c->bout, x, c->dt, s, D, A, d.eps};
-    PDL_TRY("head_euler", launch_pdl(head_euler_kernel, dim3(T - 1), dim3(256), (size_t)D * 4, st, h));
-  }
-  return LAT_OK;
+  const size_t layer_elems = (size_t)2 * (d.T_prefix + d.T_q) * d.Hkv * d.dh;
+  return enqueue_pi0_step(c, 0, d.L, kv, (long long)layer_elems, st, d.S, x, state);
 }
 
 
@@ -1340,9 +1362,9 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     cudaFuncSetAttribute(dense_gemm_kernel<kDStages, kActTerms>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          dense_smem_bytes(kDStages, kActTerms));
     cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_tc_smem_bytes());
-    cudaFuncSetAttribute(pi0_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
-    cudaFuncSetAttribute(pi0_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
-    cudaFuncSetAttribute(pi0_step_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
+    for (int dh : {64, 128, 256})
+      for (bool chunk : {false, true})
+        cudaFuncSetAttribute(step_kernel(dh, chunk), cudaFuncAttributeMaxDynamicSharedMemorySize, mk_smem_bytes());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       delete c;

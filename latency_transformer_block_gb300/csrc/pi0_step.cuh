@@ -1,44 +1,44 @@
-// Persistent kernel for the pi0 action expert: all blocks of one denoise step
-// in one launch.
+// Persistent kernel for the pi0 action expert: the blocks of one denoise step,
+// or (chunk kernel) a whole denoised chunk -- every step's embedding, W2
+// projection, blocks and head -- in one launch.
 //
 // "Running VLAs at Real-time Speed" (reading note, sections 3 and 6) puts the
 // action expert's time into launch gaps and into streaming every block's
 // weights once per step; the TileRT page describes a persistent engine that
 // keeps weight loads running while compute waits on its dependencies.  Here one
-// CTA per SM lives for the whole step:
+// CTA per SM lives for the whole launch, in thread-block clusters of 4
+// (cooperative launch: every CTA is resident, which the grid barriers need):
 //
-//  * warp 0 streams this CTA's share of every block's weights (128 x 64 bf16
-//    tiles, TMA, 128-byte swizzle) through a ring of shared-memory slots.  The
-//    weights do not depend on activations, so the stream runs ahead across
-//    phase boundaries and is throttled only by the ring.
-//  * warp 1 issues tcgen05 MMAs (M = 128 weight rows, N = 192 = three bf16
+//  * warp 0 streams this CTA's share of every projection's weights (128 x 64
+//    fp16 tiles, TMA, 128-byte swizzle) through a ring of shared-memory slots.
+//    The weights do not depend on activations, so the stream runs ahead
+//    across phase (and step) boundaries and is throttled only by the ring.
+//  * warp 1 issues tcgen05 MMAs (M = 128 weight rows, N = 128 = two fp16
 //    planes x 64 tokens, fp32 accumulator in TMEM, two buffers).
+//  * warp 2 brings the operand planes of the O, down and W2 projections by
+//    TMA once the grid barrier before them has passed.
 //  * warps 4..11 ("math") do everything that depends on activations: they
-//    load the fp32 residual stream from global memory (several k-tiles in
-//    flight, in registers) and split it into three bf16 planes in the MMA's
-//    swizzled layout (warp 2 brings the other operands' planes by TMA), run
-//    the split-K epilogues (vector reductions into fp32 sums at L2), the
-//    attention and the combine of key-range partials.
-//  * Per weight tile the shared memory moves ~80 KB (MMA reads of the 24 KB
-//    operand and 16 KB weight tile, the operand's 24 KB of stores, the weight
-//    tile's 16 KB TMA write); at ~128 B per clock that, not the tensor core
-//    (96 cycles per M = 128, N = 192 MMA), paces a projection's k-tiles.
+//    load the fp32 residual stream (several k-tiles in flight, in registers)
+//    and split it into two fp16 planes (hi = fp16(x), lo = fp16(x - hi)) in
+//    the MMA's swizzled layout, run the split-K epilogues, the attention, the
+//    combine of key-range partials and (chunk kernel) the head and embedding.
+//  * Weights are held as fp16 = 2^s x the folded bf16 weight (exact); the
+//    epilogue multiplies by 2^-s.
 //
 // Per block six phases, separated by a grid barrier (bounded spin):
-//   1 QKV projection of x (sums of squares of x on the side, each head
-//     group from its own K ranges); the CTAs of
-//     each head group (its m-tiles, all K ranges) then wait for one another
-//     on a group counter and finalize the group's q / own k, v: RMS factor,
-//     RoPE, two-term bf16 planes, own k / v to the cache as bf16
-//   2 attention: per (head, 32-key block), partial (max, sum, output)
-//   3 combine of the key-block partials into the exact bf16 planes of o;
-//     clears the QKV sums for the next block
-//   4 x += o Wo (operand planes by TMA)
-//   5 gate/up projection of x (gate and up rows of the same 64 FFN columns
-//     in one 128-row tile; sums of squares on the side); the CTAs of each
-//     tile wait for one another and write h = GELU(r g) * (r u) as exact
-//     bf16 planes
-//   6 x += h Wd (operand planes by TMA); clears the gate/up sums
+//   QKV projection of x: the 4 CTAs of a cluster take the 4 K ranges of one
+//     128-row tile; their partial sums (and the per-token sums of squares of
+//     x) meet in the cluster by bulk copies into the finalizing CTA's shared
+//     memory; each CTA finalizes a quarter of the tile's rows (whole rotary
+//     pairs: RMS factor, RoPE, q planes, own k / v into the cache)
+//   attention: per (head, 32-key block), partial (max, sum, output)
+//   combine of the key-block partials into the fp16 planes of o
+//   x += o Wo: every CTA adds its K range's partial sums into x (vector
+//     reductions at L2)
+//   gate/up projection of x (gate and up rows of the same 64 FFN columns in
+//     one 128-row tile; two tiles x two K ranges per cluster, exchanged like
+//     QKV); h = GELU(r g) * (r u) as fp16 planes
+//   x += h Wd, like O
 // The RMSNorm scales are folded into the weights; the per-token factor
 // r = rsqrt(mean(x^2) + eps) multiplies the projection sums (the projection is
 // linear in its input), as in the pages' fold (section 4.1).
@@ -53,7 +53,7 @@ constexpr int kMkThreads = 384;                 // 12 warps
 constexpr int kMkCluster = 4;                   // CTAs per thread-block cluster
 constexpr int kMkNW = 6;                        // weight ring slots
 constexpr int kMkNB = 4;                        // activation-plane ring slots
-constexpr int kMkPre = 5;                       // k-tiles of x the math warps hold in flight (registers)
+constexpr int kMkPre = 5;   // k-tiles of x the math warps hold in flight (registers)
 constexpr int kMkWBytes = 128 * 64 * 2;         // one weight tile
 constexpr int kMkBBytes = 128 * 64 * 2;         // one activation tile, two fp16 planes
 // cluster exchange area (after the operand slots): 4 slots of split-K partial
@@ -64,7 +64,7 @@ constexpr int kMkXOff = kMkNB * kMkBBytes;
 constexpr int kMkXBytes = 4 * kMkXSlot + 4 * 64 * 4;
 constexpr int kMkRegion = 99 * 1024;            // also the attention's tiles (its own phase)
 static_assert(kMkXOff + kMkXBytes <= kMkRegion, "operand slots and exchange area fit in the region");
-constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 5;
+constexpr int kMkBars = 2 * kMkNW + 3 * kMkNB + 6;
 static_assert(kMkRegion % 1024 == 0, "the weight ring after the region stays 1024-byte aligned");
 
 __host__ __device__ constexpr int mk_smem_bytes() { return 1024 + kMkNW * kMkWBytes + kMkRegion + 8 * kMkBars + 16; }
@@ -99,15 +99,34 @@ struct MkGemm {
 };
 
 struct MkArgs {
-  MkGemm g[4];              // 0 QKV, 1 O, 2 gate/up, 3 down
+  MkGemm g[5];              // 0 QKV, 1 O, 2 gate/up, 3 down, 4 W2 (the embedding's second projection)
   int l0, l1;               // layers [l0, l1) of this launch
+  int steps;                // 0: the blocks once (one denoise step, or one block); > 0: a whole chunk of
+                            // `steps` denoise steps, each embedding + W2 + every block, then the head
   int D, F, Hq, Hkv, T_q, T_prefix, T_kv, nqkv;
   int prefix_lm;            // 1: the state token (query row 0) sees the prefix and itself only
   float eps, scale_log2;
   float* x;                 // fp32 [64][D] residual stream (rows >= T_q stay 0)
   __half* o_planes;         // [2][64][Hq dh] attention output as two fp16 planes (rows >= T_q stay 0)
   __half* h_planes;         // [2][64][F] GeGLU output as two fp16 planes (rows >= T_q stay 0)
-  float wsc[4];             // 2^-s of each projection's weights (held as fp16 = 2^s w, exact)
+  float wsc[5];             // 2^-s of each projection's weights (held as fp16 = 2^s w, exact)
+  // chunk mode: the embedding and head around the blocks (all fp32 unless noted)
+  float* act;               // [T_q - 1][A] actions: the noise in, the actions out (x <- x + dt v)
+  float* act_buf;           // [2][T_q - 1][A] the actions between steps (step s writes buffer s mod 2)
+  const float* state;       // [A]
+  const __nv_bfloat16* w_state;   // bf16 [A][D]
+  const __nv_bfloat16* b_state;   // bf16 [D]
+  float* state_emb;         // [D] state row, written at step 0
+  const float* wfold;       // [A][D] W' = W_in W1_a
+  const float* ttab;        // [S][D] T[s]
+  const float* b2;          // [D]
+  __half* e_planes;         // [2][64][D] SiLU(x W' + T[s]) of the action rows (row 1 + t) as two fp16
+                            // planes, the W2 operand (row 0 and rows >= T_q stay 0)
+  const __nv_bfloat16* w_out;   // bf16 [D][A] (the head's weight; copied whole into shared memory)
+  const float* g_final;     // [D] the final RMSNorm scale
+  const float* bout;        // [A]
+  const float* dt;          // [S]
+  int A;
   __nv_bfloat16* q_planes;  // [2][64][Hq dh] q after RoPE, two-term bf16 (hi, lo)
   __nv_bfloat16* kv_own;    // [k hi, k lo, v hi, v lo][64][Hkv dh] own keys / values, two-term bf16
   float* part_m;            // [n_kb][Hq][T_q]
@@ -159,6 +178,38 @@ __device__ __forceinline__ MkRange mk_range(const MkGemm& g, int b) {
   r.k0 = s * g.KT / S;
   r.k1 = (s + 1) * g.KT / S;
   return r;
+}
+
+// Position in a launch's order of projections: per denoise step (chunk mode)
+// W2, then per block QKV, O, gate/up, down.
+struct MkPos {
+  int s, l, gi;
+  bool valid;
+};
+
+__device__ __forceinline__ MkPos mk_seq_first(const MkArgs& a) {
+  MkPos p;
+  p.s = 0;
+  p.l = a.l0;
+  p.gi = a.steps > 0 ? 4 : 0;
+  p.valid = a.l1 > a.l0;
+  return p;
+}
+
+__device__ __forceinline__ void mk_seq_next(const MkArgs& a, MkPos& p) {
+  if (p.gi == 4) {
+    p.gi = 0;
+    p.l = a.l0;
+    return;
+  }
+  if (++p.gi < 4) return;
+  p.gi = 0;
+  if (++p.l < a.l1) return;
+  if (a.steps > 0 && ++p.s < a.steps) {
+    p.gi = 4;
+    return;
+  }
+  p.valid = false;
 }
 
 __device__ __forceinline__ bool mk_aborted(DevErr* e) { return *reinterpret_cast<volatile unsigned*>(&e->code) != 0; }
@@ -238,21 +289,36 @@ __device__ __forceinline__ void mk_grid_sync(unsigned* ctr, unsigned target, Dev
   named_sync(1, 256);
 }
 
-// Shared state of the math warps.
+// Shared state of the math warps.  Every shared-memory address is a fixed
+// offset from the (1024-byte aligned) base, so only the base is kept:
+//   [weight slots kMkNW x kMkWBytes][region kMkRegion: operand slots, exchange
+//   slots and statistics][mbarriers: wfull[NW] wempty[NW] bfull[NB] bfullt[NB]
+//   bempty[NB] accfull mdone go xfull never hfull][TMEM address, re-arm table]
 struct MkMath {
-  uint8_t* sB;
-  float* xbuf;        // cluster exchange slots [4][64 tokens][32 rows]
-  float* xss;         // [4][64] sums of squares of x, by source K range
-  uint64_t* bfull;
-  uint64_t* bempty;
-  uint64_t* accfull;
-  uint64_t* xfull;    // exchange complete: armed by this CTA with the bytes it will receive
-  uint64_t* never;    // an mbarrier nothing arrives on (failure hook)
-  uint64_t* go;
+  uint8_t* base;
   uint32_t tmem;
   uint32_t bt, gc, xuse;
   bool xbroken;       // an exchange wait ran out: no further arming or waiting
   int mt;
+  __device__ __forceinline__ uint8_t* sB() const { return base + kMkNW * kMkWBytes; }   // operand slots
+  // cluster exchange slots [4][64 tokens][32 rows] and [4][64] sums of squares of x, by source K range
+  __device__ __forceinline__ float* xbuf() const { return reinterpret_cast<float*>(sB() + kMkXOff); }
+  __device__ __forceinline__ float* xss() const { return xbuf() + kMkCluster * (kMkXSlot / 4); }
+  __device__ __forceinline__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(sB() + kMkRegion); }
+  __device__ __forceinline__ uint64_t* bfull() const { return bars() + 2 * kMkNW; }
+  __device__ __forceinline__ uint64_t* bempty() const { return bars() + 2 * kMkNW + 2 * kMkNB; }
+  __device__ __forceinline__ uint64_t* accfull() const { return bars() + 2 * kMkNW + 3 * kMkNB; }
+  __device__ __forceinline__ uint64_t* go() const { return accfull() + 2; }
+  // exchange complete: armed by this CTA with the bytes it will receive
+  __device__ __forceinline__ uint64_t* xfull() const { return accfull() + 3; }
+  // an mbarrier nothing arrives on (failure hook)
+  __device__ __forceinline__ uint64_t* never() const { return accfull() + 4; }
+  // the head's weight landed in the operand slots (chunk mode)
+  __device__ __forceinline__ uint64_t* hfull() const { return accfull() + 5; }
+  // after the barriers: the TMEM address, then the re-arm table (mk_xtable)
+  __device__ __forceinline__ const uint32_t* xtable() const {
+    return reinterpret_cast<const uint32_t*>(bars() + kMkBars) + 1;
+  }
 };
 
 // does cluster c take part in the exchange of this projection
@@ -280,23 +346,27 @@ __device__ __forceinline__ uint32_t mk_xbytes(int gi) {
   return 4 * kMkXSlot + (gi == 0 ? 4 * 256 : gi == 2 ? 2 * 256 : 0);
 }
 
-// bytes of cluster c's next exchange after projection gi of layer l (gi = -1:
-// the first of layer l); 0 if it takes part in none before the launch ends
-__device__ __forceinline__ uint32_t mk_next_xbytes(const MkArgs& a, int l, int gi, int c) {
-  for (int k = 0; k < 8; ++k) {
-    if (++gi == 4) {
-      gi = 0;
-      ++l;
-    }
-    if (l >= a.l1) return 0;
-    if (mk_cluster_active(a.g[gi], c)) return mk_xbytes(gi);
-  }
-  return 0;
+// The exchanges of cluster c: QKV (gi 0) and gate/up (gi 2) of every block,
+// where the cluster holds tiles of them (O, down and W2 add their partial sums
+// into x directly).  Bytes of the cluster's first exchange of the launch, and
+// of the one after its exchange in projection gi at position p (0 after the
+// last one).
+__device__ __forceinline__ uint32_t mk_first_xbytes(const MkArgs& a, int c) {
+  if (a.l1 <= a.l0) return 0;
+  return mk_cluster_active(a.g[0], c) ? mk_xbytes(0) : mk_cluster_active(a.g[2], c) ? mk_xbytes(2) : 0;
+}
+
+// The table the math warps re-arm from (set up once per launch, in shared
+// memory): [0] bytes after a QKV exchange, [1] after a gate/up exchange.
+__device__ __forceinline__ void mk_xtable(const MkArgs& a, int c, uint32_t* t) {
+  const bool q_on = mk_cluster_active(a.g[0], c), u_on = mk_cluster_active(a.g[2], c);
+  t[0] = mk_xbytes(u_on ? 2 : 0);
+  t[1] = mk_xbytes(q_on ? 0 : 2);
 }
 
 // Math side of one projection.  Projections of the residual stream x (QKV,
 // gate/up): the math warps load their rows of x straight from global memory,
-// kMkPre k-tiles in flight in registers, and write the exact bf16 planes into
+// PRE k-tiles in flight in registers, and write the exact bf16 planes into
 // the operand slots; for the others (act == nullptr) the loader brings the
 // planes by TMA.  Then the split-K epilogue: each warp sums the three planes
 // of its quarter of the tile's rows and stores them, through distributed
@@ -319,6 +389,7 @@ __device__ __forceinline__ void mk_load_tile(const float* act, int ld, int kt, c
     for (int hh = 0; hh < 2; ++hh) v[2 * i + hh] = mk_ldcg4(act + (size_t)rows[i] * ld + kt * 64 + hh * 32 + 4 * p);
 }
 
+template <int PRE>
 __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const float* act, int act_ld, bool stats,
                                              float wsc, float* out, int ld, int T_q, DevErr* err,
                                              unsigned long long* tr) {
@@ -344,19 +415,19 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
   }
   if (act) {
     float amax = 0.f;   // largest |x| converted (fp16 planes hold |x| < 65504)
-    float4 xv[kMkPre][4];
+    float4 xv[PRE][4];
 #pragma unroll
-    for (int u = 0; u < kMkPre; ++u)
+    for (int u = 0; u < PRE; ++u)
       if (u < nk) mk_load_tile(act, act_ld, r.k0 + u, rows, p, xv[u]);
     mk_mark(tr, 0);
-    for (int j0 = 0; j0 < nk; j0 += kMkPre) {
+    for (int j0 = 0; j0 < nk; j0 += PRE) {
 #pragma unroll
-      for (int u = 0; u < kMkPre; ++u) {
+      for (int u = 0; u < PRE; ++u) {
         const int j = j0 + u;
         if (j < nk) {
           const uint32_t b = s.bt % kMkNB;
-          mk_wait(&s.bempty[b], ((s.bt / kMkNB) & 1) ^ 1, err, 31);
-          uint8_t* dst = s.sB + b * kMkBBytes;
+          mk_wait(&s.bempty()[b], ((s.bt / kMkNB) & 1) ^ 1, err, 31);
+          uint8_t* dst = s.sB() + b * kMkBBytes;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const int t = rows[i];
@@ -376,9 +447,9 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&s.bfull[b]);   // this warp's rows of the operand are written
+          if (lane == 0) mbar_arrive(&s.bfull()[b]);   // this warp's rows of the operand are written
           ++s.bt;
-          if (j + kMkPre < nk) mk_load_tile(act, act_ld, r.k0 + j + kMkPre, rows, p, xv[u]);
+          if (j + PRE < nk) mk_load_tile(act, act_ld, r.k0 + j + PRE, rows, p, xv[u]);
         }
       }
     }
@@ -398,7 +469,7 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
   // tokens 32 ch .. +31 of each plane, sums the planes hi + lo and undoes the
   // weights' power-of-two scale
   if (act) mk_mark(tr, 1);
-  mk_wait(s.accfull, s.gc & 1, err, 32);
+  mk_wait(s.accfull(), s.gc & 1, err, 32);
   mk_mark(tr, 2);
   tc_fence_after();
   const uint32_t acc = s.tmem + (s.gc & 1) * 256;
@@ -427,10 +498,10 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
   }
   // every MMA of the projection is complete, so the operand slots are free:
   // stage this warp's block, [token][row] (32 x 32 fp32), and the statistics
-  float* stg = reinterpret_cast<float*>(s.sB) + mw * 1024;
+  float* stg = reinterpret_cast<float*>(s.sB()) + mw * 1024;
 #pragma unroll
   for (int j = 0; j < 32; ++j) stg[j * 32 + lane] = v[j];
-  float* sst = reinterpret_cast<float*>(s.sB) + 8 * 1024;
+  float* sst = reinterpret_cast<float*>(s.sB()) + 8 * 1024;
   if (stats && p == 0) {
     sst[rows[0]] = ssq[0];
     sst[rows[1]] = ssq[1];
@@ -448,40 +519,39 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
     slot = rank;
   }
   if (lane == 0)
-    bulk_copy_to_cluster(cluster_map(smem_u32(s.xbuf + slot * (kMkXSlot / 4) + ch * 1024), dest), smem_u32(stg),
-                         4096u, cluster_map(smem_u32(s.xfull), dest));
+    bulk_copy_to_cluster(cluster_map(smem_u32(s.xbuf() + slot * (kMkXSlot / 4) + ch * 1024), dest), smem_u32(stg),
+                         4096u, cluster_map(smem_u32(s.xfull()), dest));
   if (stats) {
     // the sums of squares of this K range: to every rank (QKV) or to the two
     // ranks of this tile (gate/up), in the row of this K range
     named_sync(2, 256);
     if (s.mt == 0) {
       const uint32_t src = g.pair ? (rank & 1) : rank;
-      const uint32_t at = smem_u32(s.xss + src * 64);
+      const uint32_t at = smem_u32(s.xss() + src * 64);
       for (uint32_t d = 0; d < kMkCluster; ++d)
         if (!g.pair || (d & 2) == (rank & 2))
-          bulk_copy_to_cluster(cluster_map(at, d), smem_u32(sst), 256u, cluster_map(smem_u32(s.xfull), d));
+          bulk_copy_to_cluster(cluster_map(at, d), smem_u32(sst), 256u, cluster_map(smem_u32(s.xfull()), d));
     }
   }
   mk_mark(tr, 3);
 }
 
-// Wait until this CTA has received every byte of the exchange (its partial
-// sums and statistics from the cluster), then arm the barrier with the bytes
-// of its next exchange; with `skew` first a wait that nothing completes.
-__device__ __forceinline__ void mk_exchange_wait(MkMath& s, const MkArgs& a, int l, int gi, int c, bool skew,
-                                                 unsigned where) {
-  if (skew) mk_wait(s.never, 0, a.err, where + 100);
+// Wait until this CTA has received every byte of the exchange of projection
+// gi (its partial sums and statistics from the cluster), then arm the barrier
+// with the bytes of its next exchange; with `skew` first a wait that nothing
+// completes.
+__device__ __forceinline__ void mk_exchange_wait(MkMath& s, const MkArgs& a, int gi, bool skew, unsigned where) {
+  if (skew) mk_wait(s.never(), 0, a.err, where + 100);
   if (s.xbroken) return;
-  const bool ok = mk_wait_cluster(s.xfull, s.xuse & 1, a.err, where);
+  const bool ok = mk_wait_cluster(s.xfull(), s.xuse & 1, a.err, where);
   ++s.xuse;
   if (!ok) {
     s.xbroken = true;
     return;
   }
-  if (s.mt == 0) {
-    const uint32_t nb = mk_next_xbytes(a, l, gi, c);
-    if (nb) mbar_arrive_expect_tx(s.xfull, nb);
-  }
+  // armed for the next exchange even after the last one: a barrier left
+  // expecting bytes at exit is harmless (nothing is in flight to this CTA)
+  if (s.mt == 0) mbar_arrive_expect_tx(s.xfull(), s.xtable()[gi >> 1]);
 }
 
 // QKV: rank j of the cluster of tile u finalizes the tile's rows 32 j .. +31,
@@ -970,31 +1040,189 @@ __device__ __forceinline__ void mk_gu_finalize(const MkArgs& a, int m, int k, co
   }
 }
 
-// O and down projections: rank j adds the sum of the cluster's 4 K ranges for
-// rows 32 j .. +31 of tile m (features 128 m + 32 j ..) into the residual
-// stream x, one vector reduction per 4 features (the other clusters of the
-// tile add their K ranges the same way).
-__device__ __forceinline__ void mk_x_finalize(const MkArgs& a, int m, int j, const float* xbuf, int mt) {
-  for (int it = mt; it < a.T_q * 8; it += 256) {
-    const int t = it >> 3, c4 = (it & 7) * 4;
-    float4 acc = *reinterpret_cast<const float4*>(xbuf + t * 32 + c4);
-#pragma unroll
-    for (int src = 1; src < kMkCluster; ++src) {
-      const float4 v = *reinterpret_cast<const float4*>(xbuf + src * 2048 + t * 32 + c4);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+// Chunk mode: the action rows' head of the previous denoise step and the
+// embedding of this one ("Running VLAs at Real-time Speed", the action
+// expert's input and output projections, in the folded form of its
+// section 4.2).  Action row t has the pair of CTAs 2t, 2t + 1; each computes
+// the row's head (the same values) and half of its embedding columns:
+//   head (step s - 1):  v[a] = r(h) sum_n g[n] h[n] W_out[n][a] + b_out[a],
+//                       h = x[1 + t], r(h) = 1 / sqrt(mean(h^2) + eps),
+//                       act_s[t][a] = act_{s-1}[t][a] + dt[s - 1] v[a]
+//                       (written by CTA 2t: into act_buf[s mod 2], after the
+//                       last step into the caller's actions; act_0, the
+//                       noise, is first copied to act_buf[0], so no phase
+//                       reads what it writes)
+//   embedding (step s): emb[1 + t][n] = SiLU(sum_a act[t][a] W'[a][n] + T[s][n])
+//                       x[1 + t][n] = b2[n]   (the W2 projection adds onto it)
+// and CTA 2 (T_q - 1) the state row: x[0] = state_emb = state W_state +
+// b_state (computed at step 0).  The embedding goes out as the two fp16
+// planes the W2 projection's loader brings by TMA (an activation outside
+// fp16's range records LAT_ERR_RANGE).  W_out was copied into the operand
+// slots before the grid barrier (mk_head_prefetch, barrier `hfull`); the
+// scratch lives in the exchange area.  Every read of the residual stream
+// bypasses L1 (other SMs wrote it).
+__device__ __forceinline__ void mk_head_embed(const MkArgs& a, int s, bool head, bool embed, uint8_t* sB,
+                                              uint64_t* hfull, int mt, unsigned long long* tr) {
+  const int D = a.D, A = a.A, T1 = a.T_q - 1;
+  const int b = blockIdx.x;
+  if (b == 2 * T1 && embed) {
+    float* x0 = a.x;
+    for (int n = mt; n < D; n += 256) {
+      float v;
+      if (s == 0) {
+        v = __bfloat162float(a.b_state[n]);
+        for (int j = 0; j < A; ++j) v = fmaf(a.state[j], __bfloat162float(a.w_state[(size_t)j * D + n]), v);
+        a.state_emb[n] = v;
+      } else {
+        v = a.state_emb[n];   // written by this CTA at step 0
+      }
+      x0[n] = v;
     }
-    red_add_v4(a.x + (size_t)t * a.D + m * 128 + j * 32 + c4, acc.x, acc.y, acc.z, acc.w);
+    return;
+  }
+  if (b >= 2 * T1) return;
+  const int t = b >> 1, half = b & 1;
+  float* sh = reinterpret_cast<float*>(sB + kMkXOff);   // [D] g (.) h
+  float* part = sh + D;                                 // [256] partial sums
+  float* zp = part + 256 * 4;                           // [D / 2] embedding partials
+  float* xa = zp + D / 2;                               // [A] this row's actions
+  float* red = xa + A;                                  // [8] + 1
+  float* hrow = a.x + (size_t)(1 + t) * D;
+  const size_t ra = (size_t)t * A + mt, nb = (size_t)T1 * A;
+  if (mt < A) xa[mt] = __ldcg((s == 0 ? a.act : a.act_buf + ((s - 1) & 1) * nb) + ra);   // CTA 2t wrote it
+  if (s == 0 && half == 0 && mt < A) a.act_buf[ra] = xa[mt];
+  mk_mark(tr, 0);
+  // loads that wait on nothing, issued before the ones the steps depend on
+  const float bo = head && mt < A ? a.bout[mt] : 0.f;
+  const float dts = head ? a.dt[s - 1] : 0.f;
+  if (head) {
+    float ss = 0.f;
+    for (int n = 4 * mt; n < D; n += 1024) {
+      const float4 v = mk_ldcg4(hrow + n);
+      const float4 g = *reinterpret_cast<const float4*>(a.g_final + n);
+      *reinterpret_cast<float4*>(sh + n) = make_float4(g.x * v.x, g.y * v.y, g.z * v.z, g.w * v.w);
+      ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+    }
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((mt & 31) == 0) red[mt >> 5] = ss;
+    mk_mark(tr, 1);
+    mk_wait(hfull, (uint32_t)(s - 1) & 1u, a.err, 36);   // W_out in the operand slots
+    mk_mark(tr, 2);
+    named_sync(4, 256);
+    if (mt == 0) {
+      float tot = 0.f;
+      for (int w = 0; w < 8; ++w) tot += red[w];
+      red[8] = rsqrtf(tot / (float)D + a.eps);
+    }
+    // thread mt: column pair cp (columns 2 cp, 2 cp + 1), rows n = rp mod RP
+    const int A2 = A >> 1, RP = 256 / A2;
+    const int cp = mt % A2, rp = mt / A2;
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(sB);
+    float2 acc = make_float2(0.f, 0.f);
+    const int n_it = D / RP;
+    for (int i0 = 0; i0 < n_it; i0 += 8) {   // 8 rows' loads in flight, then their FMAs
+      __nv_bfloat162 w[8];
+      float hv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int n = rp + (i0 + u < n_it ? i0 + u : 0) * RP;
+        w[u] = w2[n * A2 + cp];
+        hv[u] = i0 + u < n_it ? sh[n] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float2 wf = __bfloat1622float2(w[u]);
+        acc.x = fmaf(hv[u], wf.x, acc.x);
+        acc.y = fmaf(hv[u], wf.y, acc.y);
+      }
+    }
+    part[rp * A + 2 * cp] = acc.x;
+    part[rp * A + 2 * cp + 1] = acc.y;
+    named_sync(4, 256);
+    mk_mark(tr, 3);
+    if (mt < A) {
+      float v = 0.f;
+      for (int i = 0; i < RP; ++i) v += part[i * A + mt];
+      v = red[8] * v + bo;
+      const float nx = xa[mt] + dts * v;
+      xa[mt] = nx;
+      if (half == 0) (s == a.steps ? a.act : a.act_buf + (s & 1) * nb)[ra] = nx;
+    }
+  }
+  named_sync(4, 256);   // xa complete; every read of the row h is done
+  mk_mark(tr, 4);
+  if (!embed) return;
+  // this CTA's half of the columns, n0 .. n0 + D / 2: thread (jh, q) sums the
+  // actions jh A / 2 .. of column quad q; the second half of the actions
+  // meets the first in shared memory
+  const int n0 = half * (D >> 1), jh = mt >> 7, q = mt & 127;
+  const int A_h = A >> 1;
+  const float* tt = a.ttab + (size_t)s * D;
+  __half* ehi = a.e_planes + (size_t)(1 + t) * D;
+  __half* elo = ehi + (size_t)64 * D;
+  for (int c0 = 0; c0 < (D >> 1); c0 += 512) {   // the same trip count in every thread (named barrier)
+    const int c = c0 + 4 * q;
+    const bool on = c < (D >> 1);
+    const int n = n0 + (on ? c : 0);
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 tv = z, bv = z;
+    if (jh == 0 && on) {
+      tv = *reinterpret_cast<const float4*>(tt + n);
+      bv = *reinterpret_cast<const float4*>(a.b2 + n);
+    }
+    const float* wf = a.wfold + (size_t)(jh * A_h) * D + n;
+#pragma unroll 16
+    for (int j = 0; j < (on ? A_h : 0); ++j) {
+      const float4 w = *reinterpret_cast<const float4*>(wf + (size_t)j * D);
+      const float xj = xa[jh * A_h + j];
+      z.x = fmaf(xj, w.x, z.x);
+      z.y = fmaf(xj, w.y, z.y);
+      z.z = fmaf(xj, w.z, z.z);
+      z.w = fmaf(xj, w.w, z.w);
+    }
+    if (jh == 1 && on) *reinterpret_cast<float4*>(zp + c) = z;
+    named_sync(4, 256);
+    if (jh == 0 && on) {
+      const float4 z1 = *reinterpret_cast<const float4*>(zp + c);
+      const float e0 = silu(z.x + z1.x + tv.x), e1 = silu(z.y + z1.y + tv.y);
+      const float e2 = silu(z.z + z1.z + tv.z), e3 = silu(z.w + z1.w + tv.w);
+      if (!(fmaxf(fmaxf(fabsf(e0), fabsf(e1)), fmaxf(fabsf(e2), fabsf(e3))) < kF16Max))
+        record_error(a.err, kErrRange, 35);
+      uint32_t h0, l0, h1, l1;
+      split_pair_h2(e0, e1, h0, l0);
+      split_pair_h2(e2, e3, h1, l1);
+      *reinterpret_cast<uint2*>(ehi + n) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(elo + n) = make_uint2(l0, l1);
+      *reinterpret_cast<float4*>(hrow + n) = bv;
+    }
+    named_sync(4, 256);   // zp is reused by the next columns
+  }
+  // the scratch (generic writes) is next written by peers' bulk copies
+  fence_proxy_async_smem();
+  mk_mark(tr, 5);
+}
+
+// Chunk mode, after the last block's down projection of a step: the CTAs of
+// the action rows copy W_out (bf16 [D][A]) whole into their operand slots,
+// which no projection uses until W2 of the next step, so that the head after
+// the grid barrier reads it from shared memory.
+__device__ __forceinline__ void mk_head_prefetch(const MkArgs& a, uint8_t* sB, uint64_t* hfull, int mt) {
+  if ((int)blockIdx.x >= 2 * (a.T_q - 1)) return;
+  named_sync(4, 256);   // every math warp is past its reads of the slots
+  if (mt == 0) {
+    fence_proxy_async_smem();
+    const uint32_t bytes = (uint32_t)(a.D * a.A * 2);
+    mbar_arrive_expect_tx(hfull, bytes);
+    bulk_copy_g2s(smem_u32(sB), a.w_out, bytes, smem_u32(hfull));
   }
 }
 
-template <int DH>
+template <int DH, bool CHUNK>
 __global__ void __launch_bounds__(kMkThreads, 1)
     pi0_step_kernel(const __grid_constant__ CUtensorMap w_qkv, const __grid_constant__ CUtensorMap w_o,
                     const __grid_constant__ CUtensorMap w_gu, const __grid_constant__ CUtensorMap w_d,
                     const __grid_constant__ CUtensorMap act_op, const __grid_constant__ CUtensorMap act_hp,
+                    const __grid_constant__ CUtensorMap w_w2, const __grid_constant__ CUtensorMap act_ep,
                     const MkArgs a) {
   // the CTAs exchange partial sums with the other CTAs of their cluster of 4:
   // launched any other way (a replay by a tool that drops the cluster shape)
@@ -1020,7 +1248,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   uint64_t* go = mdone + 1;                // grid barrier passed before a projection phase
   uint64_t* xfull = go + 1;                // cluster exchange received (bytes, armed by this CTA)
   uint64_t* never = xfull + 1;             // nothing arrives (failure hook)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* hfull = never + 1;             // the head's weight landed (chunk mode)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(hfull + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -1038,11 +1267,13 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     mbar_init(go, 1);
     mbar_init(xfull, 1);
     mbar_init(never, 1);
+    mbar_init(hfull, 1);
     fence_mbar_init();
     // armed with the bytes of this CTA's first exchange before any peer can
     // send (the cluster barrier below)
-    const uint32_t nb = mk_next_xbytes(a, a.l0, -1, (int)blockIdx.x / kMkCluster);
+    const uint32_t nb = mk_first_xbytes(a, (int)blockIdx.x / kMkCluster);
     if (nb) mbar_arrive_expect_tx(xfull, nb);
+    mk_xtable(a, (int)blockIdx.x / kMkCluster, tmem_slot + 1);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -1056,23 +1287,27 @@ __global__ void __launch_bounds__(kMkThreads, 1)
   // peer's barrier or stores into a peer's exchange area
   cluster_sync_all();
 
+  // register split of the launch's 384 x 168 = 64512 registers: the four
+  // producer warps keep 40 each (128 x 40 = 5120), the eight math warps take
+  // 232 (256 x 232 = 59392); 5120 + 59392 = 64512
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
     if (warp == 0 && lane == 0) {
       // ---------------- weight stream ----------------
       tma_prefetch_desc(&w_qkv);
       tma_prefetch_desc(&w_o);
       tma_prefetch_desc(&w_gu);
       tma_prefetch_desc(&w_d);
+      if (a.steps > 0) tma_prefetch_desc(&w_w2);
       const uint64_t pol = l2_policy_evict_first();
       uint32_t wt = 0;
       bool ok = true;
-      for (int l = a.l0; l < a.l1 && ok; ++l)
-        for (int gi = 0; gi < 4 && ok; ++gi) {
+      for (MkPos ps = mk_seq_first(a); ps.valid && ok; mk_seq_next(a, ps)) {
+          const int gi = ps.gi;
           const MkRange r = mk_range(a.g[gi], blockIdx.x);
           if (!r.active) continue;
-          const CUtensorMap* map = gi == 0 ? &w_qkv : gi == 1 ? &w_o : gi == 2 ? &w_gu : &w_d;
-          const int row = l * a.g[gi].N + r.m * 128;
+          const CUtensorMap* map = gi == 0 ? &w_qkv : gi == 1 ? &w_o : gi == 2 ? &w_gu : gi == 3 ? &w_d : &w_w2;
+          const int row = (gi == 4 ? 0 : ps.l * a.g[gi].N) + r.m * 128;
           for (int k = r.k0; k < r.k1; ++k) {
             const uint32_t s = wt % kMkNW;
             if (!mk_wait(&wempty[s], ((wt / kMkNW) & 1) ^ 1, a.err, 20)) {
@@ -1092,14 +1327,14 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       const uint32_t idesc = idesc_f16_f32(128, 128);   // M = 128 weight rows, N = 2 fp16 planes x 64 tokens
       uint32_t wt = 0, bt = 0, gc = 0, pf = 0, pt = 0;   // pf / pt: per-slot parities of bfull / bfullt
       bool ok = true;
-      for (int l = a.l0; l < a.l1 && ok; ++l)
-        for (int gi = 0; gi < 4 && ok; ++gi) {
+      for (MkPos ps = mk_seq_first(a); ps.valid && ok; mk_seq_next(a, ps)) {
+          const int gi = ps.gi;
           const MkRange r = mk_range(a.g[gi], blockIdx.x);
           if (!r.active) continue;
           const uint32_t acc = tmem + (gc & 1) * 256;
           for (int k = r.k0; k < r.k1; ++k) {
             const uint32_t b = bt % kMkNB, s = wt % kMkNW;
-            const bool tma_b = gi == 1 || gi == 3;
+            const bool tma_b = gi == 1 || gi == 3 || gi == 4;
             uint64_t* bf = tma_b ? &bfullt[b] : &bfull[b];
             const uint32_t par = ((tma_b ? pt : pf) >> b) & 1u;
             if (!mk_wait(bf, par, a.err, 21) || !mk_wait(&wfull[s], (wt / kMkNW) & 1, a.err, 22)) {
@@ -1127,18 +1362,19 @@ __global__ void __launch_bounds__(kMkThreads, 1)
       mbar_wait(mdone, 0, nullptr, 0);
     } else if (warp == 2 && lane == 0) {
       // ---------------- activation loader ----------------
-      // after each grid barrier that opens the output or the down projection:
-      // the operand planes straight into the operand slots (the math warps
-      // build the QKV and gate/up operands from x themselves)
+      // after each grid barrier that opens the output, the down or the W2
+      // projection: the operand planes straight into the operand slots (the
+      // math warps build the QKV and gate/up operands from x themselves)
       tma_prefetch_desc(&act_op);
       tma_prefetch_desc(&act_hp);
+      if (a.steps > 0) tma_prefetch_desc(&act_ep);
       const uint64_t pol = l2_policy_evict_last();
       uint32_t bt = 0, gop = 0;
       uint32_t bout = 0;            // operand copies issued, by slot (bit)
       uint32_t pt = 0;              // per-slot parity of bfullt
       bool ok = true;
-      for (int l = a.l0; l < a.l1 && ok; ++l)
-        for (int gi = 0; gi < 4 && ok; ++gi) {
+      for (MkPos ps = mk_seq_first(a); ps.valid && ok; mk_seq_next(a, ps)) {
+          const int gi = ps.gi;
           if (!mk_wait(go, gop & 1, a.err, 40)) {
             ok = false;
             break;
@@ -1149,8 +1385,8 @@ __global__ void __launch_bounds__(kMkThreads, 1)
           const MkRange r = mk_range(a.g[gi], blockIdx.x);
           if (!r.active) continue;
           const int nk = r.k1 - r.k0;
-          if (gi == 1 || gi == 3) {   // operand planes straight into the operand slots
-            const CUtensorMap* map = gi == 1 ? &act_op : &act_hp;
+          if (gi == 1 || gi == 3 || gi == 4) {   // operand planes straight into the operand slots
+            const CUtensorMap* map = gi == 1 ? &act_op : gi == 3 ? &act_hp : &act_ep;
             for (int j = 0; j < nk; ++j) {
               const uint32_t b = bt % kMkNB;
               if (!mk_wait(&bempty[b], ((bt / kMkNB) & 1) ^ 1, a.err, 41)) {
@@ -1173,19 +1409,11 @@ __global__ void __launch_bounds__(kMkThreads, 1)
         if ((bout >> i) & 1u) mbar_wait(&bfullt[i], ((pt >> i) & 1u) ^ 1u, nullptr, 0);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
     // ---------------- math warps ----------------
     MkMath s;
-    s.sB = sB;
-    s.xbuf = reinterpret_cast<float*>(sR + kMkXOff);
-    s.xss = s.xbuf + kMkCluster * (kMkXSlot / 4);
-    s.bfull = bfull;
-    s.bempty = bempty;
-    s.accfull = accfull;
-    s.xfull = xfull;
-    s.never = never;
+    s.base = smem;
     s.xbroken = false;
-    s.go = go;
     s.tmem = tmem;
     s.bt = s.gc = s.xuse = 0;
     s.mt = threadIdx.x - 128;
@@ -1194,51 +1422,83 @@ __global__ void __launch_bounds__(kMkThreads, 1)
     unsigned nbar = 0;
     const float invD = 1.f / (float)a.D;
     const int kvd = a.Hkv * DH;
-    for (int l = a.l0; l < a.l1; ++l) {
-      __nv_bfloat16* kc = a.kv + (size_t)(l - a.l0) * a.kv_stride;
-      __nv_bfloat16* vc = kc + (size_t)a.T_kv * kvd;
-      unsigned long long* tr =
-          (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * a.trace_stride + blockIdx.x) * 64 : nullptr;
-      mk_mark(tr, 0);
-      // phases: 0 QKV (+ q / own k, v), 2 attention, 3 combine, 4 O, 5 gate/up
-      // (+ GeGLU planes), 7 down; a grid barrier before each (the first one of
-      // a launch has none).  Indices 1 and 6 (former separate finalize phases)
-      // are skipped so trace slots keep their meaning.
-      const int lr = l - a.l0;
-      const int cl = (int)blockIdx.x / kMkCluster, rk = (int)blockIdx.x % kMkCluster;
-      for (int ph = 0; ph < 8; ++ph) {
-        if (ph == 1 || ph == 6) continue;   // finalized inside the QKV and gate/up phases
-        if (ph > 0 || l > a.l0) {
+    constexpr bool chunk = CHUNK;   // a whole chunk (a.steps > 0) or the blocks once
+    const int cl = (int)blockIdx.x / kMkCluster, rk = (int)blockIdx.x % kMkCluster;
+    for (int st = 0; st < (chunk ? a.steps : 1); ++st) {
+      if constexpr (chunk) {
+        // before the first block of each step, after a grid barrier (none
+        // before the launch's first phase): the head of the previous step and
+        // the embedding (trace slots 42, 43, sub-steps 52..), then W2 (44..49)
+        unsigned long long* tr0 = (a.trace && mt == 0) ? a.trace + (size_t)blockIdx.x * 64 : nullptr;
+        if (st > 0) {
           ++nbar;
-          const unsigned extra = (nbar == 1 && a.skew_where == 1) ? a.skew : 0u;
-          mk_grid_sync(a.bar, nbar * G + extra, a.err, mt);
+          mk_grid_sync(a.bar, nbar * G, a.err, mt);
         }
-        const bool proj = ph == 0 || ph == 4 || ph == 5 || ph == 7;
-        if (proj && mt == 0) mbar_arrive(go);   // the loader may fetch this phase's operand
-        mk_mark(tr, 2 * ph + 1);
-        if (ph == 2) {
-          mk_attention<DH>(a, kc, vc, sR, mt, tr);
-        } else if (ph == 3) {
-          mk_combine<DH>(a, mt, reinterpret_cast<float*>(sR), tr);
-        } else {
-          const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
-          const MkGemm& g = a.g[gi];
-          const MkRange r = mk_range(g, blockIdx.x);
-          mk_gemm_math(s, g, ph == 0 || ph == 5 ? a.x : nullptr, a.D, ph == 0 || ph == 5, a.wsc[gi], a.x, a.D,
-                       a.T_q, a.err, tr ? tr + 20 + 4 * gi : nullptr);
-          if (r.active && !g.direct) {   // the whole cluster is active or idle in a projection
-            const bool skew = a.skew > 0 && lr == 0 && ((a.skew_where == 2 && ph == 0) || (a.skew_where == 3 && ph == 5));
-            MkRot rot;
-            if (ph == 0) rot = mk_qkv_angles<DH>(a, cl, rk, mt);
-            mk_exchange_wait(s, a, l, gi, cl, skew, 903 + gi);
-            mk_mark(tr, 38 + gi);   // exchange received
-            if (ph == 0) mk_qkv_finalize<DH>(a, cl, rk, s.xbuf, s.xss, kc, vc, invD, rot, mt);
-            else if (ph == 5) mk_gu_finalize(a, r.m, rk & 1, s.xbuf, s.xss, invD, mt);
-            else mk_x_finalize(a, r.m, rk, s.xbuf, mt);
-          }
-        }
-        mk_mark(tr, 2 * ph + 2);
+        mk_mark(tr0, 42);
+        mk_head_embed(a, st, st > 0, true, s.sB(), s.hfull(), mt, tr0 ? tr0 + 52 : nullptr);
+        mk_mark(tr0, 43);
+        ++nbar;
+        mk_grid_sync(a.bar, nbar * G + ((nbar == 1 && a.skew_where == 1) ? a.skew : 0u), a.err, mt);
+        if (mt == 0) mbar_arrive(s.go());   // the loader may fetch the embedding planes
+        mk_mark(tr0, 44);
+        mk_gemm_math<kMkPre>(s, a.g[4], nullptr, a.D, false, a.wsc[4], a.x, a.D, a.T_q, a.err,
+                             tr0 ? tr0 + 45 : nullptr);
+        mk_mark(tr0, 49);
       }
+      for (int l = a.l0; l < a.l1; ++l) {
+        __nv_bfloat16* kc = a.kv + (size_t)(l - a.l0) * a.kv_stride;
+        __nv_bfloat16* vc = kc + (size_t)a.T_kv * kvd;
+        unsigned long long* tr =
+            (a.trace && mt == 0) ? a.trace + ((size_t)(l - a.l0) * a.trace_stride + blockIdx.x) * 64 : nullptr;
+        mk_mark(tr, 0);
+        // phases: 0 QKV (+ q / own k, v), 2 attention, 3 combine, 4 O, 5 gate/up
+        // (+ GeGLU planes), 7 down; a grid barrier before each (the first one of
+        // a launch has none).  Indices 1 and 6 (former separate finalize phases)
+        // are skipped so trace slots keep their meaning.
+        for (int ph = 0; ph < 8; ++ph) {
+          if (ph == 1 || ph == 6) continue;   // finalized inside the QKV and gate/up phases
+          if (ph > 0 || l > a.l0 || chunk) {
+            ++nbar;
+            const unsigned extra = (nbar == 1 && a.skew_where == 1) ? a.skew : 0u;
+            mk_grid_sync(a.bar, nbar * G + extra, a.err, mt);
+          }
+          const bool proj = ph == 0 || ph == 4 || ph == 5 || ph == 7;
+          if (proj && mt == 0) mbar_arrive(s.go());   // the loader may fetch this phase's operand
+          mk_mark(tr, 2 * ph + 1);
+          if (ph == 2) {
+            mk_attention<DH>(a, kc, vc, s.sB(), mt, tr);
+          } else if (ph == 3) {
+            mk_combine<DH>(a, mt, reinterpret_cast<float*>(s.sB()), tr);
+          } else {
+            const int gi = ph == 0 ? 0 : ph == 4 ? 1 : ph == 5 ? 2 : 3;
+            const MkGemm& g = a.g[gi];
+            const MkRange r = mk_range(g, blockIdx.x);
+            mk_gemm_math<kMkPre>(s, g, ph == 0 || ph == 5 ? a.x : nullptr, a.D, ph == 0 || ph == 5, a.wsc[gi], a.x,
+                                 a.D, a.T_q, a.err, tr ? tr + 20 + 4 * gi : nullptr);
+            if (r.active && !g.direct) {   // QKV and gate/up: the whole cluster is active or idle
+              const bool skew = a.skew > 0 && st == 0 && l == a.l0 &&
+                                ((a.skew_where == 2 && ph == 0) || (a.skew_where == 3 && ph == 5));
+              MkRot rot;
+              if (ph == 0) rot = mk_qkv_angles<DH>(a, cl, rk, mt);
+              mk_exchange_wait(s, a, gi, skew, 903 + gi);
+              mk_mark(tr, 38 + gi);   // exchange received
+              if (ph == 0) mk_qkv_finalize<DH>(a, cl, rk, s.xbuf(), s.xss(), kc, vc, invD, rot, mt);
+              else mk_gu_finalize(a, r.m, rk & 1, s.xbuf(), s.xss(), invD, mt);
+            }
+          }
+          if (chunk && ph == 7 && l == a.l1 - 1) mk_head_prefetch(a, s.sB(), s.hfull(), mt);
+          mk_mark(tr, 2 * ph + 2);
+        }
+      }
+    }
+    if constexpr (chunk) {   // the last step's head
+      unsigned long long* trl =
+          (a.trace && mt == 0) ? a.trace + ((size_t)(a.l1 - 1 - a.l0) * a.trace_stride + blockIdx.x) * 64 : nullptr;
+      ++nbar;
+      mk_grid_sync(a.bar, nbar * G, a.err, mt);
+      mk_mark(trl, 50);
+      mk_head_embed(a, a.steps, true, false, s.sB(), s.hfull(), mt, trl ? trl + 52 : nullptr);
+      mk_mark(trl, 51);
     }
   }
   tc_fence_before();

@@ -17,121 +17,6 @@ __host__ __device__ __forceinline__ long long chunk_pos0(int chunk, int T) { ret
 
 
 // ---------------------------------------------------------------------------
-// Embedding prologue of one denoise step (folded form, section 4.2 of the note):
-//   z[t][n]      = sum_a x[t][a] W'[a][n] + T[s][n]      (t < T_q - 1)
-//   planes       = three bf16 planes of SiLU(z) (the W2 GEMM's activation)
-//   xres[0][n]   = state token (precomputed for the chunk)
-//   xres[1+t][n] = b2[n]   (the W2 GEMM accumulates SiLU(z) W2 on top)
-// Grid (ceil(D/256), T_q), blockDim 256; row blockIdx.y == T_q - 1 writes the state row.
-// ---------------------------------------------------------------------------
-struct EmbedArgs {
-  const float* x;        // actions fp32 [T_q-1][A]
-  const float* wfold;    // fp32 [A][D]
-  const float* ttab;     // fp32 [S][D]
-  const float* b2;       // fp32 [D]
-  const float* state_emb;  // fp32 [D]
-  __nv_bfloat16* planes; // [3][64][D]
-  float* xres;           // fp32 [T_q][D]
-  int D, A, T_q, step;
-};
-
-static __global__ void embed_prologue_kernel(EmbedArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  const int t = blockIdx.y;
-  if (n >= a.D) return;
-  if (t == a.T_q - 1) {
-    a.xres[n] = a.state_emb[n];
-    return;
-  }
-  float acc = a.ttab[(size_t)a.step * a.D + n];
-  const float* xr = a.x + (size_t)t * a.A;
-  for (int j = 0; j < a.A; ++j) acc = fmaf(xr[j], a.wfold[(size_t)j * a.D + n], acc);
-  const Split3 s3 = split3(silu(acc));
-  a.planes[(size_t)t * a.D + n] = s3.hi;
-  a.planes[(size_t)(64 + t) * a.D + n] = s3.mid;
-  a.planes[(size_t)(128 + t) * a.D + n] = s3.lo;
-  a.xres[(size_t)(1 + t) * a.D + n] = a.b2[n];
-}
-
-// ---------------------------------------------------------------------------
-// Head + Euler update: for action row t (residual row 1 + t)
-//   v[t][a] = r * sum_n h[1+t][n] W'out[n][a] + b_out[a],  r = RMS factor
-//   x[t][a] += dt * v[t][a]
-// W'out = diag(g_final) W_out in fp32.  Grid T_q - 1, blockDim 256, dynamic
-// shared memory D floats (the row).
-// ---------------------------------------------------------------------------
-struct HeadArgs {
-  const float* xres;     // [T_q][D]
-  const float* wout;     // fp32 [D][A]
-  const float* bout;     // fp32 [A]
-  float* x;              // [T_q-1][A]
-  const float* dt;       // device scalar table [S]
-  int step, D, A;
-  float eps;
-};
-
-static __global__ void __launch_bounds__(256) head_euler_kernel(HeadArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int t = blockIdx.x;
-  const float* h = a.xres + (size_t)(1 + t) * a.D;
-  extern __shared__ float sh[];   // the row h [D]
-  __shared__ float red[8][33];
-  __shared__ float rs;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // RMS factor (and the row into shared memory)
-  float ss = 0.f;
-  for (int n = threadIdx.x; n < a.D; n += 256) {
-    const float v = h[n];
-    sh[n] = v;
-    ss += v * v;
-  }
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp][32] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w][32];
-    rs = rsqrtf(s / a.D + a.eps);
-  }
-  __syncthreads();
-  // A outputs: thread (warp w, lane l) accumulates column l over rows n = w,
-  // w + 8, ...; 64 rows per pass with their weight loads in flight together
-  // (two L2 round trips for D = 1024)
-  constexpr int kPre = 64;
-  for (int a0 = 0; a0 < a.A; a0 += 32) {
-    const int col = a0 + lane;
-    float acc = 0.f;
-    if (col < a.A) {
-      for (int n0 = warp; n0 < a.D; n0 += 8 * kPre) {
-        float wv[kPre];
-#pragma unroll
-        for (int i = 0; i < kPre; ++i) {
-          const int n = n0 + 8 * i;
-          wv[i] = n < a.D ? __ldg(a.wout + (size_t)n * a.A + col) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < kPre; ++i) {
-          const int n = n0 + 8 * i;
-          if (n < a.D) acc = fmaf(sh[n], wv[i], acc);
-        }
-      }
-    }
-    red[warp][lane] = acc;
-    __syncthreads();
-    if (warp == 0 && col < a.A) {
-      float s = 0.f;
-      for (int w = 0; w < 8; ++w) s += red[w][lane];
-      const float v = rs * s + a.bout[col];
-      a.x[(size_t)t * a.A + col] += a.dt[a.step] * v;
-    }
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Offline folds
 // ---------------------------------------------------------------------------
 // out[orow(n)][k] = bf16( g[k] * W[k][n] )  -- transpose to K-major with the
@@ -248,14 +133,6 @@ static __global__ void debug_timeout_kernel(DevErr* err, unsigned where) {
   }
   __syncthreads();
   if (threadIdx.x == 0) mbar_wait(&bar, 0, err, where);
-}
-
-// out[k][n] = g[k] * W[k][n] in fp32 (head fold; exact).
-static __global__ void scale_rows_f32_kernel(const __nv_bfloat16* W, const __nv_bfloat16* g, float* out, int K, int N) {
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (size_t)K * N) return;
-  const int k = (int)(i / N);
-  out[i] = __bfloat162float(W[i]) * __bfloat162float(g[k]);
 }
 
 static __global__ void bf16_to_f32_kernel(const __nv_bfloat16* in, float* out, int n) {

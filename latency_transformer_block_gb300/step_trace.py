@@ -3,9 +3,10 @@ device timestamps (lat_debug_trace).
 
   python -m latency_transformer_block_gb300.step_trace [--workload pi0_ae] [--chunks 3]
 
-Runs `--chunks` denoised chunks with the trace enabled (the last one is read)
-and prints, per phase of a block, the median over the blocks of one denoise
-step of
+Runs `--chunks` denoised chunks with the trace enabled (one launch each; every
+denoise step writes the same slots, so the buffer holds the last step of the
+last chunk) and prints, per phase of a block, the median over the blocks of
+one denoise step of
   work    = last CTA finishing the phase - first CTA starting it,
   barrier = first CTA starting the next phase - last CTA finishing this one,
 plus the sub-steps of the projection phases (median over the CTAs that take
@@ -87,6 +88,56 @@ def spread(tr: np.ndarray):
     return res
 
 
+STEP_EDGES = [  # (name, trace row: 0 = first block, -1 = last block, start slot, end slot)
+    ("head of the previous step + embedding", 0, 42, 43),
+    ("W2 projection (embedding)", 0, 44, 49),
+    ("head of the last step", -1, 50, 51),
+]
+
+
+def step_edges(tr: np.ndarray):
+    """The chunk's per-step phases around the blocks: work (last CTA end -
+    first CTA start) and the barrier to the next phase, us."""
+    res = []
+    nxt_slot = {42: (0, 44), 44: (0, 1)}
+    for name, row, s0, s1 in STEP_EDGES:
+        st = tr[row, :, s0].astype(np.float64)
+        en = tr[row, :, s1].astype(np.float64)
+        if not (st > 0).any():
+            continue
+        work = (en[en > 0].max() - st[st > 0].min()) / 1e3
+        bar = float("nan")
+        if s0 in nxt_slot:
+            r, ns = nxt_slot[s0]
+            nx = tr[r, :, ns].astype(np.float64)
+            if (nx > 0).any():
+                bar = (nx[nx > 0].min() - en[en > 0].max()) / 1e3
+        res.append((name, work, bar))
+    return res
+
+
+HEAD = [("actions loaded", 52), ("row loaded, sum of squares", 53), ("W_out in shared memory", 54),
+        ("head dot products", 55), ("actions updated", 56), ("embedding stored", 57)]
+
+
+def head_spread(tr: np.ndarray):
+    """Sub-steps of the head + embedding phase (first block's row) and of the
+    last head (last block's row): percentiles over the CTAs that run them, us
+    from the first CTA's phase start."""
+    res = {}
+    for name, row, s0, marks in (("head of the previous step + embedding", 0, 42, HEAD),
+                                 ("head of the last step", -1, 50, HEAD[:5])):
+        st = tr[row, :, s0].astype(np.float64)
+        if not (st > 0).any():
+            continue
+        t0 = st[st > 0].min()
+        cols = tr[row, :, [m for _, m in marks]].T.astype(np.float64)
+        ok = (cols > 0).all(axis=1)
+        if ok.any():
+            res[name] = (marks, np.percentile((cols[ok] - t0) / 1e3, [10, 50, 90, 100], axis=0))
+    return res
+
+
 ATTN = [("q and key tiles loaded", 17), ("own-key lo planes loaded", 18), ("P V done", 19), ("partials stored", 6)]
 COMB = [("weights of the rows", 36), ("merged, planes stored", 37)]
 
@@ -119,6 +170,13 @@ def report(tr: np.ndarray, out=sys.stdout):
         print(f"| {name} | {mw[i]:.2f} | {mb[i]:.2f} |", file=out)
     per_block = np.median(work.sum(axis=1) + np.nan_to_num(bar).sum(axis=1))
     print(f"| total | {mw.sum():.2f} | {np.nansum(mb):.2f} ({per_block:.1f} us per block) |", file=out)
+    edges = step_edges(tr)
+    if edges:
+        print("", file=out)
+        print("| per-step phase | work us | barrier us |", file=out)
+        print("|---|---|---|", file=out)
+        for name, w, b in edges:
+            print(f"| {name} | {w:.2f} | {b:.2f} |", file=out)
     print("", file=out)
     print("| projection | " + " | ".join(SUB) + " |", file=out)
     print("|---|" + "---|" * len(SUB), file=out)
@@ -134,7 +192,7 @@ def report(tr: np.ndarray, out=sys.stdout):
         print(f"| {name} | " + " | ".join(" / ".join(f"{q[i, j]:.2f}" for i in range(4)) for j in range(q.shape[1]))
               + " |", file=out)
     print("", file=out)
-    for name, (marks, q) in attention_spread(tr).items():
+    for name, (marks, q) in list(attention_spread(tr).items()) + list(head_spread(tr).items()):
         print(f"{name} (us from the first CTA's phase start; p10 / p50 / p90 / max):", file=out)
         for j, (label, _) in enumerate(marks):
             print(f"  {label}: " + " / ".join(f"{q[i, j]:.2f}" for i in range(4)), file=out)
@@ -167,7 +225,7 @@ def main():
         m.denoise(kv, state, x)
     m.ctx.sync()
     m.ctx.debug_trace(None)
-    # the buffer holds the last launch of the chunk (the last denoise step)
+    # every step of the chunk's launch writes the same slots: the last one stays
     tr = buf.view(cfg["L"], grid, 64).cpu().numpy()
     print(f"step kernel phases, workload {args.workload}: {cfg['L']} blocks of the last denoise step, "
           f"grid {grid}")

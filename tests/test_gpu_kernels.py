@@ -61,13 +61,16 @@ def test_device_wait_timeout_is_reported_and_cleared():
     assert_rel(got, ref, BLOCK_TOL, "attention after a cleared timeout")
 
 
+@pytest.mark.parametrize("mode", ["one_step", "whole_chunk"])
 @pytest.mark.parametrize("which", [1, 2, 3], ids=["grid_barrier", "qkv_cluster_exchange", "gate_up_cluster_exchange"])
-def test_step_kernel_wait_timeout_is_reported_and_cleared(which):
+def test_step_kernel_wait_timeout_is_reported_and_cleared(which, mode):
     """Failure detection of the persistent step kernel's own waits, without a
     GPU fault: one wait of the first block expects an arrival that never comes,
     gives up (~0.5 s), every later wait of the launch returns at once, lat_sync
     reports LAT_ERR_TIMEOUT; with the skew off and the error cleared the same
-    context denoises a chunk that matches the oracle."""
+    context denoises a chunk that matches the oracle.  `one_step`: the blocks
+    of one denoise step; `whole_chunk`: the launch that runs every step of a
+    chunk with its embedding and head."""
     from latency_transformer_block_gb300 import lat
     from oracle import pi0
     from tests.parity import FINAL_TOL
@@ -77,7 +80,11 @@ def test_step_kernel_wait_timeout_is_reported_and_cleared(which):
     ib = synth.pi0_inputs(cfg, 2)
     kv = m.kv_from_bits(ib["kv"])
     m.ctx.debug_wait_skew(which, 1)
-    m.ctx.debug_step(kv, 1)
+    if mode == "one_step":
+        m.ctx.debug_step(kv, 1)
+    else:
+        x = torch.from_numpy(ib["noise"]).cuda()
+        m.denoise(kv, torch.from_numpy(ib["state"]).cuda(), x)
     with pytest.raises(lat.LatError) as e:
         m.ctx.sync()
     assert e.value.code == 6                       # LAT_ERR_TIMEOUT
