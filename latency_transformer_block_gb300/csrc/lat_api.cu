@@ -1412,9 +1412,11 @@ static lat_status check_dev_err(lat_ctx* c) {
   CUDA_TRY(cudaMemcpy(&e, c->err, sizeof(e), cudaMemcpyDeviceToHost));
   if (e.code & kErrLaunch)
     return fail(LAT_ERR_CUDA, "the step kernel ran without its clusters of %d CTAs (site %u)", kMkCluster, e.where);
+  // a wait that gave up comes first: the values computed after it are not
+  // meaningful, so a range error recorded with it is a consequence
+  if (e.code & ~kErrRange) return fail(LAT_ERR_TIMEOUT, "device wait gave up (code %u, site %u)", e.code, e.where);
   if (e.code & kErrRange)
     return fail(LAT_ERR_RANGE, "an activation left the fp16 operand range (code %u, site %u)", e.code, e.where);
-  if (e.code) return fail(LAT_ERR_TIMEOUT, "device wait gave up (code %u, site %u)", e.code, e.where);
   return LAT_OK;
 }
 

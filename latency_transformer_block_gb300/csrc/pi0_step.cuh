@@ -214,6 +214,13 @@ __device__ __forceinline__ void mk_seq_next(const MkArgs& a, MkPos& p) {
 
 __device__ __forceinline__ bool mk_aborted(DevErr* e) { return *reinterpret_cast<volatile unsigned*>(&e->code) != 0; }
 
+// An activation outside the fp16 operand planes' range.  Not recorded once
+// the launch has given up on a wait: the math warps then run on to the end
+// over values that no longer mean anything.
+__device__ __forceinline__ void mk_range_error(DevErr* e, unsigned where) {
+  if (!mk_aborted(e)) record_error(e, kErrRange, where);
+}
+
 // Bounded mbarrier wait that also gives up as soon as any CTA has recorded an
 // error: after a failure every wait returns at once and the kernel runs to its
 // end with meaningless results (the host reports the error).
@@ -453,7 +460,7 @@ __device__ __forceinline__ void mk_gemm_math(MkMath& s, const MkGemm& g, const f
         }
       }
     }
-    if (!(amax < kF16Max)) record_error(err, kErrRange, 33);
+    if (!(amax < kF16Max)) mk_range_error(err, 33);
   }
   // this K range's per-token sums of squares of x (lanes p == 0 hold rows[i])
   float ssq[2];
@@ -991,6 +998,9 @@ __device__ __forceinline__ void mk_combine(const MkArgs& a, int mt, float* sw, u
       }
       uint32_t hi, lo;
       const size_t col = (size_t)h * DH + c;
+      if (!(fmaxf(r0 < a.T_q ? fmaxf(fabsf(acc.x), fabsf(acc.y)) : 0.f,
+                  r1 < a.T_q ? fmaxf(fabsf(acc.z), fabsf(acc.w)) : 0.f) < kF16Max))
+        mk_range_error(a.err, 37);
       if (r0 < a.T_q) {
         split_pair_h2(acc.x, acc.y, hi, lo);
         uint32_t* d = reinterpret_cast<uint32_t*>(a.o_planes + (size_t)r0 * qd + col);
@@ -1030,7 +1040,7 @@ __device__ __forceinline__ void mk_gu_finalize(const MkArgs& a, int m, int k, co
     const float h1 = gelu_tanh_fast(rv * (g0.y + g1.y)) * (rv * (u0.y + u1.y));
     const float h2 = gelu_tanh_fast(rv * (g0.z + g1.z)) * (rv * (u0.z + u1.z));
     const float h3 = gelu_tanh_fast(rv * (g0.w + g1.w)) * (rv * (u0.w + u1.w));
-    if (!(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))) < kF16Max)) record_error(a.err, kErrRange, 34);
+    if (!(fmaxf(fmaxf(fabsf(h0), fabsf(h1)), fmaxf(fabsf(h2), fabsf(h3))) < kF16Max)) mk_range_error(a.err, 34);
     uint32_t a0, b0, a1, b1;
     split_pair_h2(h0, h1, a0, b0);
     split_pair_h2(h2, h3, a1, b1);
@@ -1187,7 +1197,7 @@ __device__ __forceinline__ void mk_head_embed(const MkArgs& a, int s, bool head,
       const float e0 = silu(z.x + z1.x + tv.x), e1 = silu(z.y + z1.y + tv.y);
       const float e2 = silu(z.z + z1.z + tv.z), e3 = silu(z.w + z1.w + tv.w);
       if (!(fmaxf(fmaxf(fabsf(e0), fabsf(e1)), fmaxf(fabsf(e2), fabsf(e3))) < kF16Max))
-        record_error(a.err, kErrRange, 35);
+        mk_range_error(a.err, 35);
       uint32_t h0, l0, h1, l1;
       split_pair_h2(e0, e1, h0, l0);
       split_pair_h2(e2, e3, h1, l1);
