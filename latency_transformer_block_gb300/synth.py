@@ -56,11 +56,13 @@ CONFIGS = {
     # projections (lat_dim; the interleaved-schedule interval).
     "dit_1p3b": dict(kind="dit", D=1536, H=12, dh=128, F=8960, L=30, S=4,
                      T_chunk=1560, n_hist=4, t_dim=256, rope_base=10000.0,
-                     eps=1e-6, batches=(4,), lat_dim=64),
+                     eps=1e-6, batches=(4,), lat_dim=64,
+                     grid_h=0, grid_w=0, text_len=0, page_tokens=0),
     # one 14B-class DiT block: width 5120, 40 heads x 128, FFN 13824.
     "dit_14b": dict(kind="dit", D=5120, H=40, dh=128, F=13824, L=1, S=4,
                     T_chunk=1560, n_hist=4, t_dim=256, rope_base=10000.0,
-                    eps=1e-6, batches=(1, 4, 8), lat_dim=64),
+                    eps=1e-6, batches=(1, 4, 8), lat_dim=64,
+                    grid_h=0, grid_w=0, text_len=0, page_tokens=0),
 }
 
 WEIGHT_STD = 0.02
@@ -248,6 +250,15 @@ def dit_weights(cfg: dict, seed: int = 0, layers=None) -> dict:
             "w1": normal_bf16(seed, p + "w1", (D, F), w),
             "w2": normal_bf16(seed, p + "w2", (F, D), w),
         })
+        if cfg.get("text_len", 0):   # text cross-attention: LayerNorm affine, q / k / v / o
+            blocks[-1].update({
+                "g_c": normal_bf16(seed, p + "g_c", (D,), SCALE_STD, 1.0),
+                "b_c": normal_bf16(seed, p + "b_c", (D,), w),
+                "cq": normal_bf16(seed, p + "cq", (D, D), w),
+                "ck": normal_bf16(seed, p + "ck", (D, D), w),
+                "cv": normal_bf16(seed, p + "cv", (D, D), w),
+                "co": normal_bf16(seed, p + "co", (D, D), w),
+            })
     return {
         "blocks": blocks,
         # timestep MLP: sinusoid(t_dim) -> D -> SiLU -> D, then SiLU -> 6D
@@ -275,6 +286,26 @@ def dit_ring(cfg: dict, seed: int = 0, streams: int = 1, layers: int = 1,
     """
     shape = (streams, layers, cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"])
     return normal_bf16(seed, tag, shape)
+
+
+def dit_text(cfg: dict, streams: int = 1, seed: int = 0, tag: str = "text") -> np.ndarray:
+    """Text contexts of the streams (already in the model width), N(0,1) bf16:
+    [streams][text_len][D]."""
+    return normal_bf16(seed, tag, (streams, cfg["text_len"], cfg["D"]))
+
+
+def dit_page_table(cfg: dict, streams: int = 1, layers: int = 1, seed: int = 0,
+                   spare: int = 3) -> tuple:
+    """A page table for rings kept in pages of cfg["page_tokens"] tokens: every
+    (stream, block, step) ring of (n_hist + 1) * T_chunk tokens gets
+    ceil(.../page_tokens) pages, drawn as a seeded permutation of a pool with
+    ``spare`` pages more than needed.  Returns (table int32 [streams][layers][S]
+    [pages], pool size)."""
+    S = cfg["S"]
+    per = -(-(cfg["n_hist"] + 1) * cfg["T_chunk"] // cfg["page_tokens"])
+    n = streams * layers * S * per
+    perm = np.random.Generator(np.random.Philox(key=_key(seed, "page_table", 0))).permutation(n + spare)
+    return perm[:n].astype(np.int32).reshape(streams, layers, S, per), n + spare
 
 
 def dit_latents(cfg: dict, n: int, seed: int = 0, tag: str = "x") -> np.ndarray:

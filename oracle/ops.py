@@ -4,7 +4,9 @@ Readings where the pages are silent (each listed in the design notes):
 * RMSNorm / LayerNorm epsilon 1e-6; LayerNorm has no affine part (the adaLN
   modulation supplies it).
 * RoPE is the rotate-half form: dimension i pairs with i + dh/2,
-  theta_i = base**(-2i/dh), angle = position * theta_i.
+  theta_i = base**(-2i/dh), angle = position * theta_i.  3-D RoPE (video
+  tokens at (frame, y, x)): three bands of the head, each such a RoPE of its own
+  width at its own coordinate.
 * Attention scale 1/sqrt(dh); no mask (every query sees every key given).
 * GELU is the tanh form of Hendrycks & Gimpel.
 * Timestep embedding: [sin(1000 t w_i), cos(1000 t w_i)], w_i = 10000**(-i/(d/2)).
@@ -46,6 +48,23 @@ def rope(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
     s = np.sin(ang)[:, None, :]
     a, b = x[..., :half], x[..., half:]
     return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def rope_bands(dh: int) -> list:
+    """3-D RoPE bands of a head (frame, height, width): (offset, width) each.
+    Frame d_f = dh - 4 floor(dh/6), height and width 2 floor(dh/6) each."""
+    dhw = 2 * (dh // 6)
+    df = dh - 2 * dhw
+    return [(0, df), (df, dhw), (df + dhw, dhw)]
+
+
+def rope3d(x: np.ndarray, pos3: np.ndarray, base: float) -> np.ndarray:
+    """3-D RoPE of x[T, H, dh] at positions pos3[T, 3] = (frame, y, x): band b
+    (rope_bands) is a rotate-half RoPE of its own width at coordinate pos3[:, b]."""
+    out = np.array(x, dtype=np.float64, copy=True)
+    for b, (o, d) in enumerate(rope_bands(x.shape[2])):
+        out[..., o:o + d] = rope(x[..., o:o + d], pos3[:, b], base)
+    return out
 
 
 def softmax(z: np.ndarray, axis: int = -1) -> np.ndarray:

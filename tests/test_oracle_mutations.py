@@ -168,7 +168,50 @@ def _prefill_no_patch_bias(patch_emb_bits, weight_bits, cfg, skip_last=True, blo
     return _orig_prefill(patch_emb_bits, wb, cfg, skip_last=skip_last, blocks=blocks)
 
 
+def _bands_equal_thirds(dh):
+    w = 2 * (dh // 6)
+    return [(0, w), (w, w), (2 * w, dh - 2 * w)]
+
+
+def _positions3_yx_swapped(c, cfg):
+    T, gh, gw = cfg["T_chunk"], cfg["grid_h"], cfg["grid_w"]
+    j = np.arange(T)
+    return np.stack([c * (T // (gh * gw)) + j // (gh * gw), j % gw, (j // gw) % gh], axis=1)
+
+
+def _rope3d_one_band(x, pos3, base):
+    return ops.rope(x, pos3[:, 0], base)
+
+
+def _cross_no_affine(h, w, ctx, cfg):
+    return _orig_cross(h, dict(w, g_c=np.ones_like(w["g_c"]), b_c=np.zeros_like(w["b_c"])), ctx, cfg)
+
+
+def _cross_k_from_h(h, w, ctx, cfg):
+    H, dh, eps = cfg["H"], cfg["dh"], cfg["eps"]
+    u = ops.layernorm(h, eps) * w["g_c"] + w["b_c"]
+    q = (u @ w["cq"]).reshape(len(h), H, dh)
+    k = (u @ w["ck"]).reshape(len(h), H, dh)
+    v = (ctx @ w["cv"]).reshape(len(ctx), H, dh)[:len(h)] if len(ctx) >= len(h) else (u @ w["cv"]).reshape(len(h), H, dh)
+    o = ops.attention(q, k, v, 1.0 / np.sqrt(dh)).reshape(len(h), H * dh)
+    return h + o @ w["co"]
+
+
+def _pool_row_off_by_one(ring, table, cfg, n_pool):
+    st, L, S, R, _, T, D = ring.shape
+    P = cfg["page_tokens"]
+    pool = np.zeros((n_pool, 2, P, D), dtype=ring.dtype)
+    for a in range(st):
+        for l in range(L):
+            for s in range(S):
+                flat = ring[a, l, s].transpose(1, 0, 2, 3).reshape(2, R * T, D)
+                for r in range(R * T):
+                    pool[table[a, l, s, r // P], :, (r + 1) % P] = flat[:, r]
+    return pool
+
+
 _orig_attention = ops.attention
+_orig_cross = dit._cross
 _orig_prefill = pi0.prefill
 
 MUTATIONS = [
@@ -201,6 +244,13 @@ MUTATIONS = [
     ((dit,), "adaln_table", _adaln_grid_shifted, ["test_adaln_table_closed_form"]),
     ((pi0,), "state_token", _state_token_no_bias, ["test_state_token_closed_form"]),
     ((pi0,), "prefill", _prefill_no_patch_bias, ["test_prefill_patch_projection"]),
+    ((ops,), "rope_bands", _bands_equal_thirds, ["test_rope_bands_split"]),
+    ((dit,), "positions3", _positions3_yx_swapped, ["test_positions3_hand_cases"]),
+    ((ops, dit), "rope3d", _rope3d_one_band,
+     ["test_rope3d_reduces_to_rope_per_band", "test_dit_wan_block_rows_and_batch"]),
+    ((dit,), "_cross", _cross_no_affine, ["test_dit_cross_attention_closed_forms"]),
+    ((dit,), "_cross", _cross_k_from_h, ["test_dit_cross_attention_closed_forms"]),
+    ((dit,), "ring_to_pool", _pool_row_off_by_one, ["test_page_pool_round_trip_and_hand_case"]),
 ]
 
 

@@ -629,3 +629,154 @@ def test_prefill_patch_projection():
     _, k, v = pi0.block(h, empty, empty, np.arange(Tp), w0, cfg, kv_only=True)
     assert np.array_equal(kv[0, 0, 0, :Tp], k)
     assert np.array_equal(kv[0, 0, 1, :Tp], v)
+
+
+# ---------------------------------------------------------------------------
+# Wan-class options of the DiT block: 3-D RoPE, text cross-attention, pages
+# ---------------------------------------------------------------------------
+def test_rope_bands_split():
+    # frame d - 4 floor(d/6), height and width 2 floor(d/6): contiguous, even widths
+    assert ops.rope_bands(128) == [(0, 44), (44, 42), (86, 42)]
+    assert ops.rope_bands(64) == [(0, 24), (24, 20), (44, 20)]
+    for dh in (16, 32, 96, 128, 256):
+        b = ops.rope_bands(dh)
+        assert b[0][0] == 0 and b[1][0] == b[0][1] and b[2][0] == b[1][0] + b[1][1]
+        assert sum(w for _, w in b) == dh and all(w % 2 == 0 for _, w in b)
+
+
+def test_positions3_hand_cases():
+    cfg = synth.config("dit_1p3b", T_chunk=24, grid_h=4, grid_w=3)   # 2 frames of 4 x 3
+    p = dit.positions3(5, cfg)
+    assert p.shape == (24, 3)
+    assert list(p[0]) == [10, 0, 0] and list(p[2]) == [10, 0, 2] and list(p[3]) == [10, 1, 0]
+    assert list(p[11]) == [10, 3, 2] and list(p[12]) == [11, 0, 0] and list(p[23]) == [11, 3, 2]
+    # one frame's (y, x) are all distinct; the configs' chunk is one 30 x 52 frame
+    assert len({(y, x) for _, y, x in p[:12]}) == 12
+    big = synth.config("dit_1p3b", grid_h=30, grid_w=52)
+    q = dit.positions3(3, big)
+    assert q[0].tolist() == [3, 0, 0] and q[-1].tolist() == [3, 29, 51] and q[52].tolist() == [3, 1, 0]
+
+
+def test_rope3d_reduces_to_rope_per_band():
+    dh, base = 32, 10000.0
+    x = RNG.standard_normal((7, 2, dh))
+    pos = RNG.integers(0, 500, (7, 3))
+    y = ops.rope3d(x, pos, base)
+    for b, (o, w) in enumerate(ops.rope_bands(dh)):
+        assert np.allclose(y[..., o:o + w], ops.rope(x[..., o:o + w], pos[:, b], base), rtol=1e-13, atol=1e-13)
+        # a vector living on band b turns with coordinate b only
+        xb = np.zeros_like(x)
+        xb[..., o:o + w] = x[..., o:o + w]
+        moved = pos.copy()
+        moved[:, [i for i in range(3) if i != b]] += 17
+        assert np.allclose(ops.rope3d(xb, pos, base), ops.rope3d(xb, moved, base), rtol=1e-13, atol=1e-13)
+
+
+def test_rope3d_scores_depend_on_relative_position_only():
+    dh, base = 48, 10000.0
+    q = RNG.standard_normal((1, 1, dh))
+    k = RNG.standard_normal((1, 1, dh))
+
+    def dot(a, b):
+        return float(np.sum(ops.rope3d(q, np.array([a]), base) * ops.rope3d(k, np.array([b]), base)))
+
+    a, b, shift = np.array([3, 1, 4]), np.array([1, 5, 9]), np.array([40, 7, 11])
+    assert np.isclose(dot(a, b), dot(a + shift, b + shift), rtol=1e-11)
+    assert not np.isclose(dot(a, b), dot(a, b + np.array([0, 1, 0])), rtol=1e-6)
+
+
+def _tiny_wan(seed=4, **over):
+    cfg = synth.config("dit_1p3b", D=32, H=2, dh=16, F=40, L=1, T_chunk=12, t_dim=16,
+                       grid_h=2, grid_w=3, text_len=5, **over)
+    wb = synth.dit_weights(cfg, seed)
+    W = pi0.decode_tree({k: v for k, v in wb.items() if k != "blocks"})
+    w = pi0.decode_tree(wb["blocks"][0])
+    table = dit.adaln_table(W, cfg)
+    ring = bf16.decode(synth.dit_ring(cfg, seed, streams=2))[:, 0]
+    text = bf16.decode(synth.dit_text(cfg, 2, seed))
+    return cfg, w, table, ring, text
+
+
+def test_dit_cross_attention_closed_forms():
+    cfg, w, table, ring, text = _tiny_wan()
+    D, eps = cfg["D"], cfg["eps"]
+    xs = synth.dit_latents(cfg, 1, 5)
+    desc = [(1, 6, 2)]
+    # W_o^c = 0: the block without its cross-attention sublayer
+    off = dit.block_batch(xs, desc, ring.copy(), table, dict(w, co=np.zeros_like(w["co"])), dict(cfg, text_len=0))
+    on0 = dit.block_batch(xs, desc, ring.copy(), table, dict(w, co=np.zeros_like(w["co"])), cfg, text)
+    assert np.array_equal(off, on0)
+    # gate1 = gate2 = 0 isolates the sublayer: x' = x + cross(x)
+    tz = table.copy()
+    tz[:, 2 * D:3 * D] = 0.0
+    tz[:, 5 * D:6 * D] = 0.0
+    x0 = xs[0].astype(np.float64)
+    # one text token: softmax = 1, every row gets (ctx W_v^c) W_o^c
+    one = dict(cfg, text_len=1)
+    ctx1 = text[:, :1]
+    out = dit.block_batch(xs, desc, ring.copy(), tz, w, one, ctx1)
+    expect = x0 + (ctx1[1] @ w["cv"]) @ w["co"]
+    assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
+    # g_c = b_c = 0: q = 0, uniform weights, every row gets mean(ctx W_v^c) W_o^c;
+    # LN affine pinned with b_c alone (g_c = 0): q = b_c W_q^c for every row
+    wz = dict(w, g_c=np.zeros(D), b_c=np.zeros(D))
+    out = dit.block_batch(xs, desc, ring.copy(), tz, wz, cfg, text)
+    expect = x0 + (text[1] @ w["cv"]).mean(axis=0) @ w["co"]
+    assert np.allclose(out[0], expect, rtol=1e-12, atol=1e-12)
+    wb_ = dict(w, g_c=np.zeros(D))
+    out = dit.block_batch(xs, desc, ring.copy(), tz, wb_, cfg, text)
+    H, dh = cfg["H"], cfg["dh"]
+    q = (w["b_c"] @ w["cq"]).reshape(H, dh)
+    k = (text[1] @ w["ck"]).reshape(-1, H, dh)
+    v = (text[1] @ w["cv"]).reshape(-1, H, dh)
+    o = np.empty(D)
+    for h in range(H):
+        z = k[:, h] @ q[h] / math.sqrt(dh)
+        p = np.exp(z - z.max())
+        o[h * dh:(h + 1) * dh] = (p / p.sum()) @ v[:, h]
+    assert np.allclose(out[0], x0 + o @ w["co"], rtol=1e-12, atol=1e-12)
+    # with the affine: rows see LN(h) g_c + b_c (brute force on one row)
+    out = dit.block_batch(xs, desc, ring.copy(), tz, w, cfg, text)
+    r = 4
+    u = ops.layernorm(x0[r:r + 1], eps)[0] * w["g_c"] + w["b_c"]
+    qr = (u @ w["cq"]).reshape(H, dh)
+    for h in range(H):
+        z = k[:, h] @ qr[h] / math.sqrt(dh)
+        p = np.exp(z - z.max())
+        o[h * dh:(h + 1) * dh] = (p / p.sum()) @ v[:, h]
+    assert np.allclose(out[0, r], x0[r] + o @ w["co"], rtol=1e-12, atol=1e-12)
+
+
+def test_dit_wan_block_rows_and_batch():
+    cfg, w, table, ring, text = _tiny_wan()
+    descs = [(0, 9, 0), (1, 3, 2)]
+    xs = synth.dit_latents(cfg, 2, 6)
+    r_batch = ring.copy()
+    out = dit.block_batch(xs, descs, r_batch, table, w, cfg, text)
+    rows = [0, 5, 11]
+    r_rows = ring.copy()
+    part = dit.block_batch_rows(xs, descs, r_rows, table, w, cfg, rows, text)
+    assert np.allclose(part, out[:, rows], rtol=1e-12, atol=1e-12)
+    assert np.array_equal(r_rows, r_batch)
+    # 3-D RoPE in the block: k written to the ring is the 3-D rotation of u W_k
+    D, T = cfg["D"], cfg["T_chunk"]
+    sh1, sc1 = table[0, :D], table[0, D:2 * D]
+    u = ops.layernorm(xs[0].astype(np.float64), cfg["eps"]) * (1 + sc1) + sh1
+    k = ops.rope3d((u @ w["wk"]).reshape(T, cfg["H"], cfg["dh"]), dit.positions3(9, cfg), cfg["rope_base"])
+    assert np.array_equal(r_batch[0, 0, 9 % 5, 0], bf16.round_rne(k.reshape(T, D)))
+
+
+def test_page_pool_round_trip_and_hand_case():
+    cfg = synth.config("dit_1p3b", D=8, T_chunk=24, page_tokens=10)
+    assert dit.pages_per_ring(cfg) == 12            # 5 slots x 24 tokens = 120 = 12 pages
+    table, n_pool = synth.dit_page_table(cfg, streams=2, layers=3)
+    assert table.shape == (2, 3, cfg["S"], 12) and n_pool == 2 * 3 * cfg["S"] * 12 + 3
+    assert len(np.unique(table)) == table.size and table.min() >= 0 and table.max() < n_pool
+    ring = RNG.standard_normal((2, 3, cfg["S"], 5, 2, 24, 8))
+    pool = dit.ring_to_pool(ring, table, cfg, n_pool)
+    # ring row r = slot * T + j lives at page table[r // P], offset r % P:
+    # slot 1, token 23 is row 47 -> page table[4], offset 7 (a chunk boundary inside a page)
+    assert np.array_equal(pool[table[1, 2, 3, 4], :, 7], ring[1, 2, 3, 1, :, 23])
+    assert np.array_equal(pool[table[0, 1, 0, 2], :, 3], ring[0, 1, 0, 0, :, 23])
+    assert np.array_equal(pool[table[0, 1, 0, 2], :, 4], ring[0, 1, 0, 1, :, 0])
+    assert np.array_equal(dit.pool_to_ring(pool, table, cfg, 2, 3), ring)
