@@ -70,6 +70,10 @@ DENSE_WORKLOADS = {
     "dit_14b_n1": ("dit_14b", 1, "us per block", "us"),
     "dit_14b_n4": ("dit_14b", 4, "us per block", "us"),
     "dit_14b_n8": ("dit_14b", 8, "us per block", "us"),
+    # the 1.3B chunk with the Wan-class options: 3-D RoPE over one 30 x 52 frame
+    # per chunk, cross-attention to 512 text tokens, rings in pages of 256 tokens
+    "dit_1p3b_wan": ("dit_1p3b", 4, "ms per denoised chunk", "ms",
+                     dict(grid_h=30, grid_w=52, text_len=512, page_tokens=256)),
 }
 
 
@@ -400,9 +404,11 @@ def dense_flops(cfg, nb, descs=None):
         return 2 * macs
     T, nh = cfg["T_chunk"], cfg["n_hist"]
     per_chunk_proj = T * (D * 3 * D + D * D + D * F + F * D)
+    tl = cfg.get("text_len", 0)
+    per_chunk_cross = T * 2 * D * D + 2 * T * tl * D if tl else 0   # q, o projections; scores and P V
     macs = 0
     for (_, c, _) in descs:
-        macs += per_chunk_proj + 2 * T * T * (1 + min(c, nh)) * D
+        macs += per_chunk_proj + 2 * T * T * (1 + min(c, nh)) * D + per_chunk_cross
     return 2 * macs * L
 
 
@@ -436,8 +442,11 @@ def dense_measure(workload, steps, warmup, dev, layers=0):
     B.build()
     from latency_transformer_block_gb300 import synth
     from latency_transformer_block_gb300.models import DitStage, Pi0Prefix
-    name, nb, metric, unit = DENSE_WORKLOADS[workload]
-    cfg = synth.config(name, **({"L": layers} if layers > 0 else {}))
+    name, nb, metric, unit = DENSE_WORKLOADS[workload][:4]
+    over = dict(DENSE_WORKLOADS[workload][4]) if len(DENSE_WORKLOADS[workload]) > 4 else {}
+    if layers > 0:
+        over["L"] = layers
+    cfg = synth.config(name, **over)
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     stream = torch.cuda.Stream(dev)
@@ -475,8 +484,15 @@ def dense_measure(workload, steps, warmup, dev, layers=0):
         streams = (nb + cfg["S"] - 1) // cfg["S"]
         m = DitStage(cfg, device_weights(synth.dit_weights, cfg, dev), max_batch=nb, n_streams=streams,
                      device=dev)
-        ring = torch.randn(streams, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
-                           generator=gen, device=dev).to(torch.bfloat16)
+        if cfg.get("page_tokens", 0):   # the rings in a pool of pages, a seeded permutation of it
+            table, n_pool = synth.dit_page_table(cfg, streams, cfg["L"])
+            ring = torch.randn(n_pool, 2, cfg["page_tokens"], cfg["D"], generator=gen, device=dev).to(torch.bfloat16)
+            m.bind_pages(table)
+        else:
+            ring = torch.randn(streams, cfg["L"], cfg["S"], cfg["n_hist"] + 1, 2, cfg["T_chunk"], cfg["D"],
+                               generator=gen, device=dev).to(torch.bfloat16)
+        for st in range(streams if cfg.get("text_len", 0) else 0):   # each stream's text context
+            m.set_text(st, torch.randn(cfg["text_len"], cfg["D"], generator=gen, device=dev).to(torch.bfloat16))
         x = torch.randn(nb, cfg["T_chunk"], cfg["D"], generator=gen, device=dev)
         cfg["Hkv"] = cfg["H"]
         cfg["Hq"] = cfg["H"]
@@ -532,7 +548,7 @@ def dense_measure(workload, steps, warmup, dev, layers=0):
         "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) inputs and history, N(0,0.02) bf16 weights drawn on the device)",
-        "config": {"workload": workload, "batch": nb, "blocks": blocks,
+        "config": {"workload": workload, "batch": nb, "blocks": blocks, **over,
                    "us_per_block": round(ms * 1e3 / blocks, 2), "useful_tflop_per_step": round(flops / 1e12, 3),
                    "path_tflops": round(tflops, 1), "path_frac": round(tflops / peak_tf, 4),
                    "l2": "inputs larger than L2 (weights and KV streamed per step)"},

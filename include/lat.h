@@ -93,6 +93,11 @@ typedef struct {
   int prefix_lm;   /* action expert: 0 = the chunk's tokens all see each other;   */
                    /* 1 = the pi0 model's block mask: the state token (token 0)   */
                    /* sees the prefix and itself only, the action tokens every key */
+  /* DiT, Wan-class options (0 = off; see lat_dit_set_text / lat_dit_bind_pages): */
+  int grid_h, grid_w; /* 3-D RoPE: a chunk is T_q / (grid_h grid_w) latent frames  */
+                   /* of grid_h x grid_w patches                                  */
+  int text_len;    /* text cross-attention over a context of text_len tokens      */
+  int page_tokens; /* rings kept in pages of page_tokens tokens of a page pool    */
 } lat_model_desc;
 
 /* One block's weights (device, bf16, [K_in][N_out] row-major; vectors [D]). */
@@ -108,6 +113,9 @@ typedef struct {
   const void *wd;      /* pi0: down projection [F][D]                            */
   const void *w1;      /* DiT: FFN in [D][F]                                     */
   const void *w2;      /* DiT: FFN out [F][D]                                    */
+  /* DiT with text_len > 0: the cross-attention sublayer                         */
+  const void *g_cross, *b_cross; /* LayerNorm affine [D], [D]                     */
+  const void *cq, *ck, *cv, *co; /* [D][D] each                                    */
 } lat_block_weights;
 
 typedef struct {
@@ -132,7 +140,9 @@ typedef struct {
 /* One chunk of a DiT batch. */
 typedef struct {
   int stream;  /* ring index, 0 <= stream < n_streams                             */
-  int chunk;   /* chunk index c >= 0 (RoPE position of token j: c*T_q + j)        */
+  int chunk;   /* chunk index c >= 0 (RoPE position of token j: c*T_q + j; with   */
+               /* grid_h > 0: frame c*T_q/(grid_h grid_w) + j/(grid_h grid_w),   */
+               /* row (j/grid_w) mod grid_h, column j mod grid_w)                 */
   int step;    /* denoise step 0 <= step < S                                      */
 } lat_chunk_desc;
 
@@ -195,7 +205,11 @@ lat_status lat_prefill_kv(lat_ctx *ctx, const void *patch_emb, int B, void *kv, 
  *        step s writes its K/V into slot c mod (n_hist+1) of ring
  *        (stream, layer, s), then attends to that slot and to the slots of
  *        chunks c-1..c-n_hist (those >= 0).  Two chunks of one call may not
- *        share (stream, step, slot): LAT_ERR_ARG.
+ *        share (stream, step, slot): LAT_ERR_ARG.  With grid_h > 0 (3-D RoPE)
+ *        each head's K in the ring has its dh dims in band-pair order: the
+ *        first halves of the frame, height and width bands, then their second
+ *        halves (every score is unchanged: q uses the same order).  With
+ *        page_tokens > 0, kv is the page pool (lat_dit_bind_pages).
  */
 lat_status lat_block_forward(lat_ctx *ctx, int layer, float *x, const lat_chunk_desc *chunks,
                              int n, void *kv, void *stream);
@@ -260,6 +274,38 @@ lat_status lat_dit_interval(lat_ctx *ctx, void *kv, float *lat, const lat_chunk_
  */
 lat_status lat_dit_pipeline_push(lat_ctx *ctx, void *kv, int stream_id, const float *noise, float *done,
                                  int *done_chunk, void *stream);
+
+/*
+ * lat_dit_set_text -- LAT_DIT with text_len > 0: the text context of one stream
+ * ring (its chunks' cross-attention keys and values).
+ * Defined by: none of the pages (the PhysisServe article names Wan-class
+ * backbones, which attend to a text context; the reading): a sublayer between
+ * self-attention and the FFN, x += Attn(LN(x) g_cross + b_cross, ctx) co with
+ * q = (..) cq, k = ctx ck, v = ctx cv per head, no RoPE, no mask, no gate.
+ *  text: device bf16 [text_len][D], already in the model width; read during the
+ *        call (stream-ordered).
+ * Computes every block's K/V of the context once, into the context's own
+ * buffer (fp32 values kept as two fp16 planes), used by every later chunk of
+ * that stream until the next call.  A chunk of a stream without a context
+ * fails with LAT_ERR_STATE.
+ */
+lat_status lat_dit_set_text(lat_ctx *ctx, int stream_id, const void *text, void *stream);
+
+/*
+ * lat_dit_bind_pages -- LAT_DIT with page_tokens > 0: the page table of the
+ * rings.  Defined by: none of the pages (M*'s serving layer integrates paged
+ * attention; the reading): the (n_hist+1) * T_q tokens of each (stream, block,
+ * step) ring -- chunk c's token j at ring row (c mod (n_hist+1)) * T_q + j --
+ * live in pages of page_tokens tokens (a page size need not divide T_q).
+ *  table: device int32 [n_streams][L][S][ceil((n_hist+1) T_q / page_tokens)],
+ *         page indices into the pool; borrowed until the next call.
+ * With pages bound, the kv argument of lat_block_forward / lat_dit_interval /
+ * lat_dit_pipeline_push is the pool, device bf16 [pages][2][page_tokens][D]
+ * (plane 0 K, plane 1 V); every value written and read is the one the
+ * contiguous ring would hold at that row.  The caller keeps every page index
+ * below the pool's size (not checked on the device).
+ */
+lat_status lat_dit_bind_pages(lat_ctx *ctx, const int *table);
 
 /* lat_dit_pipeline_reset -- forget the chunks in flight of one stream and start
  * its chunk count at 0 again (host state only). */

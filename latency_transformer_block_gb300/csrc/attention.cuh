@@ -425,6 +425,7 @@ struct SegAttnArgs {
   const __half* hist16;      // tensor-core kernel: base of the fp16 history copy (kh / vh are rows of it),
   int hist_rows;             //   its rows,
   const __half* own16;       //   and the base of the own fp16 planes
+  int own_rows;              //   its rows (0: the context's dense-path workspace rows)
   // prefix attention with kv_split > 1 key ranges per (head, query tile, group):
   // blockIdx.z = group * kv_split + range; each range leaves its unnormalised
   // output and row (max, sum) in part_o [z][Hq][T_rows][dh] / part_ml [z][Hq][T_rows][2]

@@ -646,6 +646,13 @@ struct HistCvtArgs {
   const __nv_bfloat16* src[kMaxHistPlanes];
   __half* dst[kMaxHistPlanes];
   int planes, rows, cols;
+  // page_tokens > 0: planes 2q (K) and 2q + 1 (V) are ring rows row0[q] ..
+  // + rows - 1 of one ring, kept in the pool [pages][2][page_tokens][cols]
+  // through its page list ptab[q] (src unused)
+  int page_tokens;
+  const int* ptab[kMaxHistPlanes / 2];
+  int row0[kMaxHistPlanes / 2];
+  const __nv_bfloat16* pool;
 };
 
 static __global__ void __launch_bounds__(256) hist_to_f16_kernel(const __grid_constant__ HistCvtArgs a) {
@@ -654,7 +661,17 @@ static __global__ void __launch_bounds__(256) hist_to_f16_kernel(const __grid_co
   for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
     const int p = (int)(i / per);
     const size_t j = i - (size_t)p * per;
-    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(a.src[p]) + j);
+    const uint4* src;
+    if (a.page_tokens > 0) {   // 8 values never cross a row (cols is a multiple of 8)
+      const size_t e = 8 * j;
+      const int row = (int)(e / a.cols), P = a.page_tokens;
+      const int r = a.row0[p >> 1] + row;
+      const size_t off = (((size_t)a.ptab[p >> 1][r / P] * 2 + (p & 1)) * P + r % P) * a.cols + e % a.cols;
+      src = reinterpret_cast<const uint4*>(a.pool + off);
+    } else {
+      src = reinterpret_cast<const uint4*>(a.src[p]) + j;
+    }
+    const uint4 v = __ldcs(src);
     reinterpret_cast<uint4*>(a.dst[p])[j] = bf16x8_to_f16x8(v);
   }
 }

@@ -8,11 +8,13 @@ namespace lat {
 // ---------------------------------------------------------------------------
 // Norm prologue with the split of the next GEMM's activation into two fp16 planes:
 //   RMS:    u = x * rsqrt(mean(x^2) + eps)              (scale g folded into W)
-//   LN_MOD: u = LN(x) * (1 + scale_b) + shift_b          (adaLN of chunk b)
+//   LN_MOD: u = LN(x) * (1 + scale_b) + shift_b          (adaLN of chunk b, or a
+//           LayerNorm affine: scale = g - 1, shift = b, the same for every b)
+//   NONE:   u = x                                        (the planes alone)
 //   act[m][c] = fp16(u), act[m][D + c] = fp16(u - act[m][c])
 // One CTA of 256 threads per row.
 // ---------------------------------------------------------------------------
-enum NormMode : int { NORM_RMS = 0, NORM_LN_MOD = 1 };
+enum NormMode : int { NORM_RMS = 0, NORM_LN_MOD = 1, NORM_NONE = 2 };
 
 struct NormArgs {
   const float* x;
@@ -76,11 +78,13 @@ static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
         q += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
       }
     rs = rsqrtf(block_sum(q) / a.D + a.eps);
-  } else {
+  } else if (a.mode == NORM_RMS) {
     float q = 0.f;
 #pragma unroll
     for (int u = 0; u < kNormV; ++u) q += (v[u].x * v[u].x + v[u].y * v[u].y) + (v[u].z * v[u].z + v[u].w * v[u].w);
     rs = rsqrtf(block_sum(q) / a.D + a.eps);
+  } else {
+    rs = 1.f;
   }
   const float4* sh = nullptr;
   const float4* sc = nullptr;
@@ -140,6 +144,13 @@ struct RopeKvArgs {
   __half* k16;              // the same as two fp16 planes (hi at column c, lo at kv_cols + c)
   __half* v16;              // of rows ld16 apart
   int ld16;
+  // page_tokens > 0: kdst / vdst unused; group b's token j is ring row
+  // row0[b] + j, which lives in page ptab[b][row / page_tokens] of the pool
+  // [pages][2][page_tokens][kv_ld] (plane 0 K, 1 V) at row % page_tokens
+  int page_tokens;
+  const int* ptab[kMaxChunks];
+  int row0[kMaxChunks];
+  __nv_bfloat16* pool;
 };
 
 static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
@@ -160,6 +171,17 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
   }
   __syncthreads();
   const float* row = a.qkv + (size_t)m * a.ld_qkv;
+  __nv_bfloat16* krow;   // this token's K and V rows in the ring (or its page)
+  __nv_bfloat16* vrow;
+  if (a.page_tokens > 0) {
+    const int r = a.row0[b] + j, P = a.page_tokens;
+    const size_t k0 = ((size_t)a.ptab[b][r / P] * 2 * P + r % P) * a.kv_ld;
+    krow = a.pool + k0;
+    vrow = a.pool + k0 + (size_t)P * a.kv_ld;
+  } else {
+    krow = a.kdst[b] + (size_t)j * a.kv_ld;
+    vrow = a.vdst[b] + (size_t)j * a.kv_ld;
+  }
   const float* cj = a.cos_j + (size_t)j * half;
   const float* sj = a.sin_j + (size_t)j * half;
   const int nq = a.q_cols / a.dh, nk = a.kv_cols / a.dh;
@@ -191,7 +213,7 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
       *reinterpret_cast<float4*>(qo) = make_float4(y0[0], y0[1], y0[2], y0[3]);
       *reinterpret_cast<float4*>(qo + half) = make_float4(y1[0], y1[1], y1[2], y1[3]);
     } else {
-      __nv_bfloat16* kr = a.kdst[b] + (size_t)j * a.kv_ld + (col - a.q_cols);
+      __nv_bfloat16* kr = krow + (col - a.q_cols);
       *reinterpret_cast<uint2*>(kr) = bf4(y0);
       *reinterpret_cast<uint2*>(kr + half) = bf4(y1);
       if (a.k16) {
@@ -224,7 +246,7 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
   for (int c = 4 * threadIdx.x; c < a.kv_cols; c += 4 * blockDim.x) {
     const float4 t = *reinterpret_cast<const float4*>(vr + c);
     const float y[4] = {t.x, t.y, t.z, t.w};
-    *reinterpret_cast<uint2*>(a.vdst[b] + (size_t)j * a.kv_ld + c) = bf4(y);
+    *reinterpret_cast<uint2*>(vrow + c) = bf4(y);
     if (a.v16) {
       __half* v16 = a.v16 + (size_t)m * a.ld16 + c;
       const uint2 h = pack_half4(y[0], y[1], y[2], y[3]);
@@ -240,6 +262,23 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
       *reinterpret_cast<uint2*>(vp) = h;
       *reinterpret_cast<uint2*>(vp + a.lo_off) = l;
     }
+  }
+}
+
+// K | V rows as computed (fp32 [rows][2 cols]) -> [rows][K hi | K lo | V hi | V lo]
+// fp16 planes, the layout the tensor-core attention reads its non-cached keys in
+// (the text context's keys and values of a cross-attention).
+static __global__ void __launch_bounds__(256) kv_planes_kernel(const float* kv, int rows, int cols, __half* out) {
+  const size_t n4 = (size_t)rows * 2 * cols / 4;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (size_t)gridDim.x * 256) {
+    const size_t e = 4 * i, r = e / (2 * cols), c = e % (2 * cols);
+    const float4 v = *reinterpret_cast<const float4*>(kv + e);
+    const uint2 h = pack_half4(v.x, v.y, v.z, v.w);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+    const size_t o = r * 4 * cols + (c < (size_t)cols ? c : cols + c);   // K at 0.., V at 2 cols..
+    *reinterpret_cast<uint2*>(out + o) = h;
+    *reinterpret_cast<uint2*>(out + o + cols) = pack_half4(v.x - f0.x, v.y - f0.y, v.z - f1.x, v.w - f1.y);
   }
 }
 

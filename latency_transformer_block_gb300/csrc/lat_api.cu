@@ -161,12 +161,22 @@ struct lat_ctx {
   int act_terms = kActTerms;   // planes of the activation the block projections multiply (1: hi only)
   // the four block projections (merged QKV, output, FFN in, FFN out) of the dense
   // path are held as fp16 = 2^s x folded bf16 weight; wscale = 2^-s per matrix
-  float wscale[4] = {1.f, 1.f, 1.f, 1.f};
+  float wscale[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};   // indexed by WSel
   CUtensorMap map_act_d, map_act_o, map_act_f;
   int m_max = 0;
   bf16 *wt1 = nullptr, *bt1 = nullptr, *wt2 = nullptr, *bt2 = nullptr, *wmod = nullptr, *bmod = nullptr;
 
   unsigned long long* attn_trace = nullptr;   // DiT: timestamps of the attention (measurement hook)
+
+  // DiT, Wan-class options
+  int frames_per_chunk = 0;        // 3-D RoPE: T_q / (grid_h grid_w)
+  bf16 *wcq = nullptr, *wco = nullptr, *wckv = nullptr;   // cross-attention, K-major fp16 (2^s): [L][D][D],
+  CUtensorMap map_cq, map_co, map_ckv;                      //   [L][D][D], [L][2D][D] (K rows, then V rows)
+  float* cross_ln = nullptr;       // [L][2][D]: b_cross (shift), g_cross - 1 (scale)
+  __half* text_kv = nullptr;       // [n_streams][L][text_len][K hi | K lo | V hi | V lo]
+  std::vector<char> text_set;      // per stream: lat_dit_set_text was called
+  const int* page_table = nullptr; // [n_streams][L][S][pages_per_ring] (lat_dit_bind_pages)
+  int pages_per_ring = 0;
 
   // DiT latent I/O (act_dim > 0) and the interleaved schedule
   bf16 *wlin = nullptr, *blin = nullptr, *wlout = nullptr, *blout = nullptr;   // [A][D], [D], [D][A], [A]
@@ -321,12 +331,31 @@ static lat_status check_desc(const lat_model_desc* d) {
     return fail(LAT_ERR_SHAPE, "DiT: S, T_q, n_streams, t_dim must be positive (t_dim even), n_hist >= 0");
   if (d->n_hist + 1 > kMaxSeg) return fail(LAT_ERR_SHAPE, "n_hist must be <= 4");
   if (d->act_dim < 0) return fail(LAT_ERR_SHAPE, "DiT: act_dim (latent channels) must be >= 0");
+  if (d->grid_h < 0 || d->grid_w < 0 || (d->grid_h > 0) != (d->grid_w > 0))
+    return fail(LAT_ERR_SHAPE, "DiT: grid_h and grid_w both positive (3-D RoPE) or both 0");
+  if (d->grid_h > 0 && d->T_q % (d->grid_h * d->grid_w))
+    return fail(LAT_ERR_SHAPE, "DiT: T_q must be whole frames of grid_h x grid_w tokens");
+  if (d->text_len < 0 || d->text_len > d->max_batch * d->T_q)
+    return fail(LAT_ERR_SHAPE, "DiT: text_len must be in [0, max_batch * T_q]");
+  if (d->page_tokens < 0 || (d->page_tokens > 0 && d->page_tokens > (d->n_hist + 1) * d->T_q))
+    return fail(LAT_ERR_SHAPE, "DiT: page_tokens must be in [0, (n_hist + 1) T_q]");
   return LAT_OK;
+}
+// ring rows of one (stream, block, step) and pages per ring
+static int ring_pages(const lat_model_desc& d) {
+  return d.page_tokens > 0 ? ((d.n_hist + 1) * d.T_q + d.page_tokens - 1) / d.page_tokens : 0;
 }
 
 // ---------------------------------------------------------------------------
 // offline folds
 // ---------------------------------------------------------------------------
+static float bf16_bits_to_float(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
 static lat_status fold_t(const void* W, const void* g, bf16* out, int K, int N, int il = 0, int il_off = 0) {
   if (!W || !aligned16(W)) return fail(LAT_ERR_ALIGN, "weight pointer NULL or not 16-byte aligned");
   dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
@@ -792,10 +821,11 @@ static constexpr int kDStages = 3;
 
 // weight of a dense projection: the four fp16 block projections, or the bf16
 // patch embedding (prefix prefill, one plain bf16 activation plane)
-enum WSel : int { W_QKV = 0, W_O = 1, W_UP = 2, W_DOWN = 3, W_PATCH = 4 };
+enum WSel : int { W_QKV = 0, W_O = 1, W_UP = 2, W_DOWN = 3, W_PATCH = 4, W_CQ = 5, W_CO = 6, W_CKV = 7 };
 
 static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int wsel, DenseArgs a, cudaStream_t st) {
-  const CUtensorMap* wm[5] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down, &c->map_patch};
+  const CUtensorMap* wm[8] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down, &c->map_patch,
+                              &c->map_cq, &c->map_co, &c->map_ckv};
   a.err = c->err;
   a.f16 = wsel != W_PATCH;
   a.out_scale = wsel != W_PATCH ? c->wscale[wsel] : 1.f;
@@ -840,6 +870,63 @@ static lat_status build_rope_tables(lat_ctx* c, int T) {
   CUDA_TRY(cudaMemcpy(c->cos_j, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice));
   CUDA_TRY(cudaMemcpy(c->sin_j, stt.data(), stt.size() * 4, cudaMemcpyHostToDevice));
   CUDA_TRY(cudaMemcpy(c->theta, th.data(), th.size() * 8, cudaMemcpyHostToDevice));
+  return LAT_OK;
+}
+
+// 3-D RoPE ("frame, height, width" bands of each head; the DiT context's
+// reading of Wan-class video tokens).  The kernel rotates pair (p, p + dh/2)
+// of a head; the bands' own pairs (o_b + i, o_b + i + d_b/2) are put there by
+// a permutation of the q and k dims (rows of the folded Wq, Wk): kernel pair p
+// is band b's pair i = p - P_b, P_b = the pairs of the bands before it.
+struct Rope3d {
+  int off[3], width[3], pair0[4];
+  explicit Rope3d(int dh) {
+    const int hw = 2 * (dh / 6);
+    width[0] = dh - 2 * hw;
+    width[1] = width[2] = hw;
+    off[0] = 0;
+    off[1] = width[0];
+    off[2] = width[0] + hw;
+    pair0[0] = 0;
+    for (int b = 0; b < 3; ++b) pair0[b + 1] = pair0[b] + width[b] / 2;
+  }
+  int band(int p) const { return p < pair0[1] ? 0 : p < pair0[2] ? 1 : 2; }
+  // model dim of kernel dim k (< dh)
+  int model_dim(int k, int dh) const {
+    const int p = k < dh / 2 ? k : k - dh / 2, b = band(p), i = p - pair0[b];
+    return off[b] + i + (k < dh / 2 ? 0 : width[b] / 2);
+  }
+};
+
+// cos / sin of each token's angles within its chunk (frame within the chunk,
+// row, column) and the per-pair frequency the chunk's frame offset turns by
+// (frame band only); the kernel composes them as for 1-D RoPE
+static lat_status build_rope_tables_3d(lat_ctx* c) {
+  const lat_model_desc& d = c->d;
+  const int half = d.dh / 2, T = d.T_q, gh = d.grid_h, gw = d.grid_w;
+  const Rope3d r(d.dh);
+  std::vector<float> ct((size_t)T * half), stt((size_t)T * half);
+  std::vector<double> th(half), thp(half);
+  for (int p = 0; p < half; ++p) {
+    const int b = r.band(p), i = p - r.pair0[b];
+    th[p] = std::pow((double)d.rope_base, -2.0 * i / r.width[b]);
+    thp[p] = b == 0 ? th[p] : 0.0;
+  }
+  for (int j = 0; j < T; ++j) {
+    const int coord[3] = {j / (gh * gw), (j / gw) % gh, j % gw};
+    for (int p = 0; p < half; ++p) {
+      const double ang = (double)coord[r.band(p)] * th[p];
+      ct[(size_t)j * half + p] = (float)std::cos(ang);
+      stt[(size_t)j * half + p] = (float)std::sin(ang);
+    }
+  }
+  LAT_TRY(c->alloc(&c->cos_j, ct.size()));
+  LAT_TRY(c->alloc(&c->sin_j, stt.size()));
+  LAT_TRY(c->alloc(&c->theta, thp.size()));
+  CUDA_TRY(cudaMemcpy(c->cos_j, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->sin_j, stt.data(), stt.size() * 4, cudaMemcpyHostToDevice));
+  CUDA_TRY(cudaMemcpy(c->theta, thp.data(), thp.size() * 8, cudaMemcpyHostToDevice));
+  c->frames_per_chunk = T / (gh * gw);
   return LAT_OK;
 }
 
@@ -983,6 +1070,65 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
     LAT_TRY(fold_t(b.w1, nullptr, c->wup + (size_t)l * F * D, D, F));
     LAT_TRY(fold_t(b.w2, nullptr, c->wdown + (size_t)l * D * F, F, D));
   }
+  if (d.grid_h > 0) {   // 3-D RoPE: each head's q and k dims in band-pair order (rows of Wq, Wk)
+    const Rope3d r(d.dh);
+    std::vector<int> perm((size_t)3 * D);
+    for (int row = 0; row < 3 * D; ++row) {
+      const int part = row / D, h = (row % D) / d.dh, k = row % d.dh;
+      perm[row] = part < 2 ? part * D + h * d.dh + r.model_dim(k, d.dh) : row;
+    }
+    int* dperm = nullptr;
+    bf16* tmp = nullptr;
+    CUDA_TRY(cudaMalloc(&dperm, perm.size() * sizeof(int)));
+    cudaError_t e = cudaMalloc(&tmp, (size_t)3 * D * D * sizeof(bf16));
+    if (e == cudaSuccess) e = cudaMemcpy(dperm, perm.data(), perm.size() * sizeof(int), cudaMemcpyHostToDevice);
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+      bf16* q0 = c->wqkv + (size_t)l * 3 * D * D;
+      e = cudaMemcpy(tmp, q0, (size_t)3 * D * D * sizeof(bf16), cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess) {
+        gather_rows_kernel<<<3 * D, 256>>>(tmp, dperm, q0, 3 * D, D);
+        e = cudaGetLastError();
+      }
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    cudaFree(dperm);
+    cudaFree(tmp);
+    if (e != cudaSuccess) return fail(LAT_ERR_CUDA, "3-D RoPE weight permutation: %s", cudaGetErrorString(e));
+  }
+  if (d.text_len > 0) {   // cross-attention: q, o and the context's k | v, folded like the block's
+    LAT_TRY(c->alloc(&c->wcq, (size_t)L * D * D));
+    LAT_TRY(c->alloc(&c->wco, (size_t)L * D * D));
+    LAT_TRY(c->alloc(&c->wckv, (size_t)L * 2 * D * D));
+    LAT_TRY(c->alloc(&c->cross_ln, (size_t)L * 2 * D));
+    std::vector<uint16_t> gb(2 * (size_t)D);
+    std::vector<float> ln((size_t)L * 2 * D);
+    for (int l = 0; l < L; ++l) {
+      const lat_block_weights& b = w->blocks[l];
+      const void* cp[] = {b.g_cross, b.b_cross, b.cq, b.ck, b.cv, b.co};
+      for (const void* p : cp)
+        if (!p || !aligned16(p)) return fail(LAT_ERR_ALIGN, "block %d cross-attention weight NULL or not 16-byte aligned", l);
+      LAT_TRY(fold_t(b.cq, nullptr, c->wcq + (size_t)l * D * D, D, D));
+      LAT_TRY(fold_t(b.co, nullptr, c->wco + (size_t)l * D * D, D, D));
+      LAT_TRY(fold_t(b.ck, nullptr, c->wckv + (size_t)l * 2 * D * D, D, D));
+      LAT_TRY(fold_t(b.cv, nullptr, c->wckv + (size_t)l * 2 * D * D + (size_t)D * D, D, D));
+      CUDA_TRY(cudaMemcpy(gb.data(), b.b_cross, (size_t)D * 2, cudaMemcpyDeviceToHost));
+      CUDA_TRY(cudaMemcpy(gb.data() + D, b.g_cross, (size_t)D * 2, cudaMemcpyDeviceToHost));
+      for (int i = 0; i < D; ++i) {
+        ln[(size_t)l * 2 * D + i] = bf16_bits_to_float(gb[i]);                 // shift = b
+        ln[(size_t)l * 2 * D + D + i] = bf16_bits_to_float(gb[D + i]) - 1.f;   // scale = g - 1 (exact)
+      }
+    }
+    CUDA_TRY(cudaMemcpy(c->cross_ln, ln.data(), ln.size() * 4, cudaMemcpyHostToDevice));
+    LAT_TRY(to_f16_scaled(c->wcq, (size_t)L * D * D, &c->wscale[W_CQ]));
+    LAT_TRY(to_f16_scaled(c->wco, (size_t)L * D * D, &c->wscale[W_CO]));
+    LAT_TRY(to_f16_scaled(c->wckv, (size_t)L * 2 * D * D, &c->wscale[W_CKV]));
+    LAT_TRY(make_kmajor_map(&c->map_cq, c->wcq, L * D, D, 128));
+    LAT_TRY(make_kmajor_map(&c->map_co, c->wco, L * D, D, 128));
+    LAT_TRY(make_kmajor_map(&c->map_ckv, c->wckv, L * 2 * D, D, 128));
+    LAT_TRY(c->alloc(&c->text_kv, (size_t)d.n_streams * L * d.text_len * 4 * D));
+    c->text_set.assign(d.n_streams, 0);
+  }
+  c->pages_per_ring = ring_pages(d);
   LAT_TRY(to_f16_scaled(c->wqkv, (size_t)L * 3 * D * D, &c->wscale[W_QKV]));
   LAT_TRY(to_f16_scaled(c->wo, (size_t)L * D * D, &c->wscale[W_O]));
   LAT_TRY(to_f16_scaled(c->wup, (size_t)L * F * D, &c->wscale[W_UP]));
@@ -1033,7 +1179,8 @@ static lat_status create_dit(lat_ctx* c, const lat_weights* w) {
     c->pipe_done.assign(d.n_streams, 0);
     c->pipe_step.assign((size_t)d.n_streams * d.S, 0);
   }
-  LAT_TRY(build_rope_tables(c, d.T_q));
+  if (d.grid_h > 0) LAT_TRY(build_rope_tables_3d(c));
+  else LAT_TRY(build_rope_tables(c, d.T_q));
   CUDA_TRY(cudaDeviceSynchronize());
   return LAT_OK;
 }
@@ -1045,7 +1192,7 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
     if (!a.hist16 || !a.own16) return fail(LAT_ERR_STATE, "tensor-core attention needs the fp16 history copy");
     CUtensorMap ring_map, own_map;
     LAT_TRY(make_kmajor_map(&ring_map, a.hist16, a.hist_rows, a.kv_ld, 128));
-    LAT_TRY(make_kmajor_map(&own_map, a.own16, c->m_max, 4 * a.kv_ld, 64));
+    LAT_TRY(make_kmajor_map(&own_map, a.own16, a.own_rows > 0 ? a.own_rows : c->m_max, 4 * a.kv_ld, 64));
     // One CTA per SM (TMEM), so the tiles run in waves of num_sms.  The tiles
     // of a last, partly filled wave are cut into key ranges of at least
     // kTcMinRangeBlocks blocks, as many per tile as fill the SMs once, and a
@@ -1186,10 +1333,14 @@ static bf16* ring_ptr(const lat_ctx* c, bf16* kv, int stream, int layer, int ste
   return kv + idx * d.T_q * d.D;
 }
 
+// One DiT block on a batch of chunks: adaLN norm, QKV, RoPE (1-D or 3-D) with
+// the own K/V into the ring (or its pages), the history's fp16 copy, attention,
+// O (x gate); with text_len > 0 the text cross-attention sublayer; the FFN.
 static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk_desc* ch, int n, bf16* kv,
                                     cudaStream_t st) {
   const lat_model_desc& d = c->d;
   const int D = d.D, F = d.F, T = d.T_q, M = n * T;
+  const int R = d.n_hist + 1, P = d.page_tokens;
   NormArgs na{};
   na.x = x; na.D = D; na.mode = NORM_LN_MOD; na.eps = d.eps; na.table = c->adaln; na.rows_per_chunk = T;
   na.act2 = c->act2;
@@ -1209,34 +1360,59 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   ra.qkv = c->qkvbuf; ra.ld_qkv = 3 * D; ra.q_cols = D; ra.kv_cols = D; ra.dh = d.dh; ra.T = T;
   ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta; ra.q_out = c->qbuf; ra.kv_ld = D;
   ra.k16 = c->kvown16; ra.v16 = c->kvown16 + 2 * D; ra.ld16 = 4 * D;
+  if (P > 0) {
+    ra.page_tokens = P;
+    ra.pool = kv;
+  }
+  // the page list of ring (stream, layer, step)
+  auto pages = [&](int stream, int step) {
+    return c->page_table + (((size_t)stream * d.L + l) * d.S + step) * c->pages_per_ring;
+  };
   SegAttnArgs sa{};
   HistCvtArgs hc{};   // every distinct history segment of the call, once, into the fp16 copy
   hc.rows = T;
   hc.cols = D;
+  if (P > 0) {
+    hc.page_tokens = P;
+    hc.pool = kv;
+  }
+  long long hkey[kMaxHistPlanes / 2];   // (stream, step, slot) of each copied segment
   for (int b = 0; b < n; ++b) {
     const int cb = ch[b].chunk, sb = ch[b].step, stb = ch[b].stream;
-    ra.pos0[b] = chunk_pos0(cb, T);
-    ra.kdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 0);
-    ra.vdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 1);
+    ra.pos0[b] = d.grid_h > 0 ? (long long)cb * c->frames_per_chunk : chunk_pos0(cb, T);
+    if (P > 0) {
+      ra.ptab[b] = pages(stb, sb);
+      ra.row0[b] = ring_slot_of(cb, d.n_hist) * T;
+    } else {
+      ra.kdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 0);
+      ra.vdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 1);
+    }
     int ns = 0;
     for (int k = d.n_hist; k >= 1; --k) {       // history, oldest first
       const int cc = cb - k;
       if (cc < 0) continue;
-      const bf16* hk = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 0);
-      const bf16* hv = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cc, d.n_hist), 1);
-      int p = 0;
-      while (p < hc.planes && hc.src[p] != hk) p += 2;
-      if (p == hc.planes) {
-        if (p + 2 > kMaxHistPlanes || (p + 2) * T > c->hist_rows) return fail(LAT_ERR_SHAPE, "history copy overflow");
-        hc.src[p] = hk;
-        hc.src[p + 1] = hv;
-        hc.dst[p] = c->hist16 + (size_t)p * T * D;
-        hc.dst[p + 1] = c->hist16 + (size_t)(p + 1) * T * D;
-        hc.planes = p + 2;
+      const int slot = ring_slot_of(cc, d.n_hist);
+      const long long key = ((long long)stb * d.S + sb) * R + slot;
+      int q = 0;
+      while (2 * q < hc.planes && hkey[q] != key) ++q;
+      if (2 * q == hc.planes) {
+        if (2 * q + 2 > kMaxHistPlanes || (2 * q + 2) * T > c->hist_rows)
+          return fail(LAT_ERR_SHAPE, "history copy overflow");
+        hkey[q] = key;
+        if (P > 0) {
+          hc.ptab[q] = pages(stb, sb);
+          hc.row0[q] = slot * T;
+        } else {
+          hc.src[2 * q] = ring_ptr(c, kv, stb, l, sb, slot, 0);
+          hc.src[2 * q + 1] = ring_ptr(c, kv, stb, l, sb, slot, 1);
+        }
+        hc.dst[2 * q] = c->hist16 + (size_t)(2 * q) * T * D;
+        hc.dst[2 * q + 1] = c->hist16 + (size_t)(2 * q + 1) * T * D;
+        hc.planes = 2 * q + 2;
       }
-      AttnSeg sg{hk, hv, nullptr, nullptr, T};
-      sg.kh = hc.dst[p];
-      sg.vh = hc.dst[p + 1];
+      AttnSeg sg{nullptr, nullptr, nullptr, nullptr, T};
+      sg.kh = hc.dst[2 * q];
+      sg.vh = hc.dst[2 * q + 1];
       sa.grp[b].seg[ns++] = sg;
     }
     // own keys as computed (fp16 hi/lo planes of the fp32 values); the ring slot holds their bf16 copy
@@ -1264,6 +1440,35 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     a.gate = c->adaln; a.rows_per_chunk = T;
     for (int b = 0; b < n; ++b) a.gate_off[b] = ch[b].step * 6 * D + 2 * D;
     LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
+  }
+  if (d.text_len > 0) {   // x += Attn(LN(x) g + b, text) Wo^c: q from x, the stream's K/V of the text
+    NormArgs nc = na;
+    for (int b = 0; b < n; ++b) {
+      nc.shift_off[b] = l * 2 * D;
+      nc.scale_off[b] = l * 2 * D + D;
+    }
+    nc.table = c->cross_ln;
+    norm_split_kernel<<<M, 256, 0, st>>>(nc);
+    LAT_TRY(launch_check("norm_split"));
+    {
+      DenseArgs a{};
+      a.M = M; a.N = D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_STORE; a.out = c->qbuf;
+      a.ldo = D;
+      LAT_TRY(enqueue_dense(c, c->map_act_d, W_CQ, a, st));
+    }
+    SegAttnArgs ca = sa;
+    for (int b = 0; b < n; ++b) {
+      const __half* tk = c->text_kv + ((size_t)ch[b].stream * d.L + l) * d.text_len * 4 * D;
+      ca.grp[b].nseg = 1;
+      ca.grp[b].seg[0] = AttnSeg{nullptr, nullptr, nullptr, nullptr, d.text_len, tk, tk + 2 * D};
+    }
+    ca.own16 = c->text_kv;
+    ca.own_rows = d.n_streams * d.L * d.text_len;
+    ca.trace = nullptr;
+    LAT_TRY(enqueue_attention_seg(c, ca, n, st));
+    DenseArgs a{};
+    a.M = M; a.N = D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID; a.out = x; a.ldo = D;
+    LAT_TRY(enqueue_dense(c, c->map_act_o, W_CO, a, st));
   }
   for (int b = 0; b < n; ++b) {
     na.shift_off[b] = ch[b].step * 6 * D + 3 * D;
@@ -1422,6 +1627,14 @@ static lat_status check_dev_err(lat_ctx* c) {
 
 // A DiT batch: 1 <= n <= max_batch chunks with indices in range, no two
 // sharing (stream, step, ring slot).
+// the Wan-class options a DiT stream needs before its chunks run
+static lat_status check_stream_ready(const lat_ctx* c, int stream) {
+  if (c->d.text_len > 0 && !c->text_set[stream])
+    return fail(LAT_ERR_STATE, "stream %d has no text context (lat_dit_set_text)", stream);
+  if (c->d.page_tokens > 0 && !c->page_table) return fail(LAT_ERR_STATE, "no page table bound (lat_dit_bind_pages)");
+  return LAT_OK;
+}
+
 static lat_status check_chunks(const lat_ctx* c, const lat_chunk_desc* chunks, int n) {
   if (!chunks || n < 1 || n > c->d.max_batch) return fail(LAT_ERR_ARG, "DiT: need 1 <= n <= max_batch chunks");
   for (int i = 0; i < n; ++i) {
@@ -1433,6 +1646,7 @@ static lat_status check_chunks(const lat_ctx* c, const lat_chunk_desc* chunks, i
       if (chunks[j].stream == a.stream && chunks[j].step == a.step &&
           ring_slot_of(chunks[j].chunk, c->d.n_hist) == ring_slot_of(a.chunk, c->d.n_hist))
         return fail(LAT_ERR_ARG, "chunks %d and %d share a ring slot", j, i);
+    LAT_TRY(check_stream_ready(c, a.stream));
   }
   return LAT_OK;
 }
@@ -1528,6 +1742,7 @@ lat_status lat_dit_pipeline_push(lat_ctx* c, void* kv, int sid, const float* noi
   const lat_model_desc& d = c->d;
   if (sid < 0 || sid >= d.n_streams) return fail(LAT_ERR_ARG, "stream_id %d out of range", sid);
   if (d.S > d.max_batch) return fail(LAT_ERR_SHAPE, "the schedule needs S <= max_batch");
+  LAT_TRY(check_stream_ready(c, sid));
   if (!aligned16(kv) || (noise && !aligned16(noise)) || (done && !aligned16(done)))
     return fail(LAT_ERR_ALIGN, "pointer not 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1559,6 +1774,44 @@ lat_status lat_dit_pipeline_push(lat_ctx* c, void* kv, int sid, const float* noi
     *done_chunk = fin;
     ++fin;
   }
+  return LAT_OK;
+}
+
+lat_status lat_dit_set_text(lat_ctx* c, int sid, const void* text, void* stream) {
+  if (!c || !text) return fail(LAT_ERR_ARG, "NULL argument");
+  const lat_model_desc& d = c->d;
+  if (d.kind != LAT_DIT || d.text_len <= 0) return fail(LAT_ERR_STATE, "needs a DiT context with text_len > 0");
+  if (sid < 0 || sid >= d.n_streams) return fail(LAT_ERR_ARG, "stream_id %d out of range", sid);
+  if (!aligned16(text)) return fail(LAT_ERR_ALIGN, "text not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int D = d.D, Tt = d.text_len;
+  // the context as fp32 rows, then as the two fp16 planes the projections multiply
+  bf16_to_f32_kernel<<<(Tt * D + 255) / 256, 256, 0, st>>>(reinterpret_cast<const bf16*>(text), c->qkvbuf, Tt * D);
+  LAT_TRY(launch_check("text bf16 -> fp32"));
+  NormArgs na{};
+  na.x = c->qkvbuf; na.D = D; na.mode = NORM_NONE; na.eps = d.eps; na.rows_per_chunk = Tt; na.act2 = c->act2;
+  norm_split_kernel<<<Tt, 256, 0, st>>>(na);
+  LAT_TRY(launch_check("norm_split"));
+  for (int l = 0; l < d.L; ++l) {   // k | v of every block, fp32, then their fp16 planes
+    DenseArgs a{};
+    a.M = Tt; a.N = 2 * D; a.K = D; a.terms = kActTerms; a.w_row0 = l * 2 * D; a.epi = E_STORE; a.out = c->qkvbuf;
+    a.ldo = 2 * D;
+    LAT_TRY(enqueue_dense(c, c->map_act_d, W_CKV, a, st));
+    __half* out = c->text_kv + ((size_t)sid * d.L + l) * Tt * 4 * D;
+    const size_t n4 = (size_t)Tt * 2 * D / 4;
+    kv_planes_kernel<<<(unsigned)std::min<size_t>((n4 + 255) / 256, (size_t)c->num_sms * 8), 256, 0, st>>>(
+        c->qkvbuf, Tt, D, out);
+    LAT_TRY(launch_check("kv_planes"));
+  }
+  c->text_set[sid] = 1;
+  return LAT_OK;
+}
+
+lat_status lat_dit_bind_pages(lat_ctx* c, const int* table) {
+  if (!c || !table) return fail(LAT_ERR_ARG, "NULL argument");
+  if (c->d.kind != LAT_DIT || c->d.page_tokens <= 0) return fail(LAT_ERR_STATE, "needs a DiT context with page_tokens > 0");
+  if (!aligned16(table)) return fail(LAT_ERR_ALIGN, "page table not 16-byte aligned");
+  c->page_table = table;
   return LAT_OK;
 }
 

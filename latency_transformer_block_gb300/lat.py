@@ -26,14 +26,17 @@ class ModelDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("kind", "D", "Hq", "Hkv", "dh", "F", "L", "S", "T_prefix", "T_q", "act_dim",
                  "n_hist", "t_dim", "patch_dim", "max_batch", "n_streams")] + \
-               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float), ("prefix_lm", ctypes.c_int)]
+               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float), ("prefix_lm", ctypes.c_int),
+                ("grid_h", ctypes.c_int), ("grid_w", ctypes.c_int), ("text_len", ctypes.c_int),
+                ("page_tokens", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
 
 
 class BlockWeights(ctypes.Structure):
-    _fields_ = [(n, _P) for n in ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "wg", "wu", "wd", "w1", "w2")]
+    _fields_ = [(n, _P) for n in ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "wg", "wu", "wd", "w1", "w2",
+                                  "g_cross", "b_cross", "cq", "ck", "cv", "co")]
 
 
 class Weights(ctypes.Structure):
@@ -91,6 +94,10 @@ def lib():
         L.lat_dit_pipeline_push.restype = st
         L.lat_dit_pipeline_reset.argtypes = [_P, ctypes.c_int]
         L.lat_dit_pipeline_reset.restype = st
+        L.lat_dit_set_text.argtypes = [_P, ctypes.c_int, _P, _P]
+        L.lat_dit_set_text.restype = st
+        L.lat_dit_bind_pages.argtypes = [_P, _P]
+        L.lat_dit_bind_pages.restype = st
         L.lat_clear_error.argtypes = [_P]
         L.lat_clear_error.restype = st
         L.lat_debug_timeout.argtypes = [_P, _P]
@@ -169,6 +176,12 @@ class Context:
 
     def dit_pipeline_reset(self, stream_id):
         check(lib().lat_dit_pipeline_reset(self.handle, stream_id))
+
+    def dit_set_text(self, stream_id, text, stream=None):
+        check(lib().lat_dit_set_text(self.handle, stream_id, ptr(text), stream_ptr(stream)))
+
+    def dit_bind_pages(self, table):
+        check(lib().lat_dit_bind_pages(self.handle, ptr(table)))
 
     def denoise_chunk(self, kv, state, x, stream=None):
         check(lib().lat_denoise_chunk(self.handle, ptr(kv), ptr(state), ptr(x), stream_ptr(stream)))

@@ -40,6 +40,10 @@ def desc_from_config(cfg: dict, kind: int, max_batch: int = 1, n_streams: int = 
     d.rope_base = cfg["rope_base"]
     d.eps = cfg["eps"]
     d.prefix_lm = int(cfg.get("prefix_lm", 0))
+    d.grid_h = cfg.get("grid_h", 0)
+    d.grid_w = cfg.get("grid_w", 0)
+    d.text_len = cfg.get("text_len", 0)
+    d.page_tokens = cfg.get("page_tokens", 0)
     return d
 
 
@@ -136,6 +140,10 @@ class DitStage:
         for l, b in enumerate(weight_bits["blocks"]):
             for k in ("wq", "wk", "wv", "wo", "w1", "w2"):
                 setattr(blocks[l], k, up(b[k]))
+            if cfg.get("text_len", 0):
+                for k, f in (("g_c", "g_cross"), ("b_c", "b_cross"), ("cq", "cq"), ("ck", "ck"), ("cv", "cv"),
+                             ("co", "co")):
+                    setattr(blocks[l], f, up(b[k]))
         w = lat.Weights()
         w.blocks = blocks
         for k in ("wt1", "bt1", "wt2", "bt2", "wmod", "bmod"):
@@ -162,3 +170,18 @@ class DitStage:
 
     def block(self, layer, x: torch.Tensor, chunks, ring: torch.Tensor, stream=None):
         self.ctx.block_forward(layer, x, ring, chunks=chunks, stream=stream)
+
+    def set_text(self, stream_id: int, text_bits, stream=None):
+        """The text context of one stream: bf16 bits [text_len][D] (host numpy) or a
+        bf16 device tensor."""
+        t = _dev_bf16(text_bits, self.device)
+        self.ctx.dit_set_text(stream_id, t, stream=stream)
+        self._text_keep = getattr(self, "_text_keep", {})
+        self._text_keep[stream_id] = t   # read by the enqueued work
+
+    def bind_pages(self, table):
+        """The page table (int32 [n_streams][L][S][pages], host numpy or device tensor)."""
+        t = table if isinstance(table, torch.Tensor) else torch.from_numpy(table)
+        t = t.to(self.device, dtype=torch.int32).contiguous()
+        self._pages = t
+        self.ctx.dit_bind_pages(t)
