@@ -472,6 +472,7 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __half* sK = reinterpret_cast<__half*>(smem_raw);   // [2 planes][KB][LD]
   __half* sV = sK + 2 * KB * LD;
+  __half* sQ = sV + 2 * KB * LD;                      // the CTA's 64 q rows as [2 planes][64][LD]
   const uint32_t LO = (uint32_t)(KB * LD * 2);
   const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z / a.kv_split, kr = blockIdx.z % a.kv_split;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -480,20 +481,25 @@ static __global__ void __launch_bounds__(128) attention_seg_kernel(const __grid_
   const int rl0 = qt * 64 + warp * 16 + g, rl1 = rl0 + 8;     // rows within the group
   const bool v0 = rl0 < a.T_rows, v1 = rl1 < a.T_rows;
   const size_t row0 = (size_t)b * a.T_rows + (v0 ? rl0 : 0), row1 = (size_t)b * a.T_rows + (v1 ? rl1 : 0);
-  const float* q0 = a.q + row0 * a.q_ld + h * DH;
-  const float* q1 = a.q + row1 * a.q_ld + h * DH;
 
-  // q fragments of k-step ks as two fp16 terms [term][4]
+  // the q rows of this CTA, once: two fp16 planes (hi = fp16(q), lo = fp16(q - hi))
+  for (int idx = threadIdx.x; idx < 64 * (DH / 4); idx += 128) {
+    const int row = idx / (DH / 4), c4 = (idx % (DH / 4)) * 4;
+    const int rl = qt * 64 + row;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (rl < a.T_rows) v = *reinterpret_cast<const float4*>(a.q + ((size_t)b * a.T_rows + rl) * a.q_ld + h * DH + c4);
+    uint32_t h0, l0, h1, l1;
+    split_pair_h2(v.x, v.y, h0, l0);
+    split_pair_h2(v.z, v.w, h1, l1);
+    *reinterpret_cast<uint2*>(sQ + row * LD + c4) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(sQ + 64 * LD + row * LD + c4) = make_uint2(l0, l1);
+  }
+  const uint32_t sQa = smem_u32(sQ);
+  // q fragments of k-step ks as two fp16 terms [term][4], by ldmatrix
   auto q_frag = [&](int ks, uint32_t (&af)[2][4]) {
-    const int c = ks * 16 + 2 * tq;
-    const float2 x00 = v0 ? *reinterpret_cast<const float2*>(q0 + c) : make_float2(0.f, 0.f);
-    const float2 x10 = v1 ? *reinterpret_cast<const float2*>(q1 + c) : make_float2(0.f, 0.f);
-    const float2 x01 = v0 ? *reinterpret_cast<const float2*>(q0 + c + 8) : make_float2(0.f, 0.f);
-    const float2 x11 = v1 ? *reinterpret_cast<const float2*>(q1 + c + 8) : make_float2(0.f, 0.f);
-    split_pair_h2(x00.x, x00.y, af[0][0], af[1][0]);
-    split_pair_h2(x10.x, x10.y, af[0][1], af[1][1]);
-    split_pair_h2(x01.x, x01.y, af[0][2], af[1][2]);
-    split_pair_h2(x11.x, x11.y, af[0][3], af[1][3]);
+    const uint32_t ad = sQa + (uint32_t)((warp * 16 + (lane & 15)) * LD + ks * 16 + ((lane >> 4) << 3)) * 2u;
+    ldsm_x4(ad, af[0][0], af[0][1], af[0][2], af[0][3]);
+    ldsm_x4(ad + (uint32_t)(64 * LD * 2), af[1][0], af[1][1], af[1][2], af[1][3]);
   };
   float o[NT][4];
 #pragma unroll
@@ -677,7 +683,7 @@ static __global__ void attention_seg_combine_kernel(const __grid_constant__ SegA
 // The kernels need more than 48 KB of dynamic shared memory for dh = 256:
 // call set_attention_smem_limits() once per device first.
 // segment attention: K and V blocks of kb keys in two planes each, rows padded to dh + 8
-static inline int seg_attn_smem_bytes(int dh, int kb) { return 4 * kb * (dh + 8) * 2; }
+static inline int seg_attn_smem_bytes(int dh, int kb) { return (4 * kb + 2 * 64) * (dh + 8) * 2; }
 // chunk attention: K and V blocks in two planes each, plus the partial scores
 static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) * 2 + 8 * 16 * (kAttnKB + 2) * 4; }
 
@@ -686,8 +692,8 @@ static inline int chunk_attn_smem_bytes(int dh) { return 4 * kAttnKB * (dh + 8) 
 static inline cudaError_t set_attention_smem_limits() {
   const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attention_seg_kernel<256, 16>, A, seg_attn_smem_bytes(256, 16))) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(attention_seg_kernel<256, 32>, A, seg_attn_smem_bytes(256, 32))) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(attention_seg_kernel<256, 64>, A, seg_attn_smem_bytes(256, 64))) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(attention_kernel<64>, A, chunk_attn_smem_bytes(64))) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(attention_kernel<128>, A, chunk_attn_smem_bytes(128))) != cudaSuccess) return e;
   return cudaFuncSetAttribute(attention_kernel<256>, A, chunk_attn_smem_bytes(256));

@@ -1244,10 +1244,10 @@ static lat_status enqueue_attention_seg(const lat_ctx* c, const SegAttnArgs& a, 
   b.part_o = c->seg_part_o;
   b.part_ml = c->seg_part_ml;
   dim3 grid(c->d.Hq, (a.T_rows + 63) / 64, groups * b.kv_split);
-  if ((long long)grid.x * grid.y * grid.z > c->num_sms)   // two CTAs a SM
-    attention_seg_kernel<256, 32><<<grid, 128, seg_attn_smem_bytes(dh, 32), st>>>(b);
+  if ((long long)grid.x * grid.y * grid.z > c->num_sms)   // two CTAs a SM: 16-key blocks
+    attention_seg_kernel<256, 16><<<grid, 128, seg_attn_smem_bytes(dh, 16), st>>>(b);
   else
-    attention_seg_kernel<256, 64><<<grid, 128, seg_attn_smem_bytes(dh, 64), st>>>(b);
+    attention_seg_kernel<256, 32><<<grid, 128, seg_attn_smem_bytes(dh, 32), st>>>(b);
   LAT_TRY(launch_check("attention_seg"));
   if (b.kv_split > 1) {
     attention_seg_combine_kernel<<<dim3(a.T_rows, c->d.Hq, groups), dh, 0, st>>>(b, dh);
