@@ -20,12 +20,19 @@
 // GEMM's activation).
 //
 // Accumulation in two levels: the tensor core sums one chunk of at most 32
-// MMAs (8 / terms K-blocks of all planes) into a TMEM accumulator; the
-// epilogue warps add each finished chunk into fp32 registers (round to
-// nearest) while the tensor core fills the other TMEM accumulator.  Measured
-// on this hardware, an fp32 TMEM accumulator run over thousands of MMAs drifts
-// by about one unit of its last place per MMA in one direction (K = 13824 x 2
-// terms gave 2e-4 relative error); chunks of 32 MMAs bound that drift to ~4e-6.
+// (or 64) MMAs into a TMEM accumulator; the epilogue warps add each finished
+// chunk into fp32 registers (round to nearest) while the tensor core fills the
+// other TMEM accumulator.  Measured on this hardware, an fp32 TMEM accumulator
+// run over thousands of MMAs drifts by about one unit of its last place per
+// MMA in one direction (K = 13824 x 2 terms gave 2e-4 relative error); chunks
+// of 32 MMAs bound that drift to ~4e-6, chunks of 64 to ~8e-6.  The chunk
+// length also sets how far the tensor core runs into the next tile (two
+// accumulators of one chunk each) while the epilogue warps finish the last
+// one: the DiT block's QKV and FFN-in projections take chunks of 64, so that
+// their MMAs do not wait on the longer epilogues (RoPE and the cache stores,
+// GELU and the plane split).  The residual projections (short epilogues, the
+// longest K) and the prefix prefill (whose K/V error compounds over its 18
+// blocks) keep chunks of 32.
 #pragma once
 #include "common.cuh"
 
@@ -37,10 +44,48 @@ enum DenseEpi : int {
   E_RESID_GATE = 2,   // out[m][n] += gate[chunk(m)][n] * acc
   E_GELU_SPLIT = 3,   // act planes <- split of GELU_tanh(acc)
   E_GEGLU_SPLIT = 4,  // tile = [64 gate | 64 up] -> act planes <- split of GELU(g) * u
+  E_ROPE_KV = 5,      // [q | k | v] heads of 128: rotary on q and k; q -> fp32, k and v -> ring + fp16 planes
 };
 
 constexpr int kMaxChunks = 16;
-constexpr int kChunkMMA = 32;   // MMAs (of K = 16) per TMEM accumulation chunk, at most
+constexpr int kChunkMMA = 32;       // MMAs (of K = 16) per TMEM accumulation chunk, at most (default)
+constexpr int kChunkMMALong = 64;   // the same for the DiT QKV and FFN-in projections
+
+// The K / V ring rows of the chunks of a call: chunk b's token j is row j of
+// kdst[b] / vdst[b] (rows ld elements apart), or with page_tokens > 0 ring row
+// row0[b] + j, which lives in page ptab[b][row / page_tokens] of the pool
+// [pages][2][page_tokens][ld] (plane 0 K, 1 V) at row % page_tokens.
+struct RingRows {
+  __nv_bfloat16* kdst[kMaxChunks];
+  __nv_bfloat16* vdst[kMaxChunks];
+  int ld;
+  int page_tokens;
+  const int* ptab[kMaxChunks];
+  int row0[kMaxChunks];
+  __nv_bfloat16* pool;
+};
+
+__device__ __forceinline__ __nv_bfloat16* ring_row(const RingRows& g, int b, int j, int plane) {
+  if (g.page_tokens > 0) {
+    const int r = g.row0[b] + j, P = g.page_tokens;
+    return g.pool + ((size_t)g.ptab[b][r / P] * 2 * P + (size_t)plane * P + r % P) * g.ld;
+  }
+  return (plane ? g.vdst[b] : g.kdst[b]) + (size_t)j * g.ld;
+}
+
+// E_ROPE_KV: the QKV projection of a DiT block (dh = 128, as many k and v
+// heads as q heads).  Output column n is part n / D (q, k, v) of head
+// (n % D) / 128; row m is token m % T of chunk m / T.  Pair (i, i + 64) of a
+// q or k head turns by the row's rotation rot (rope_rows_kernel: the chunk's
+// base position composed with the token's angles).
+struct RopeEpi {
+  const float4* rot;   // per 32-row group g: [2][16][32] float4, (cos | sin) of pairs 4i .. 4i + 3 of row 32 g + r
+  int heads;           // heads per part (D = 128 heads)
+  int T;
+  float* q_out;        // fp32 [M][D]
+  __half* own16;       // [M][4 D]: K hi | K lo | V hi | V lo (fp16 planes of the values as computed)
+  RingRows ring;       // the bf16 K / V rows of the cache
+};
 
 struct DenseArgs {
   int M, N, K;           // K = reduction length of one term
@@ -49,6 +94,7 @@ struct DenseArgs {
   float out_scale;       // acc *= out_scale before the epilogue (2^-s of weights held as 2^s W)
   int w_row0;            // first weight row of this matrix in the stacked tensor
   int epi;
+  int chunk_mma;         // MMAs per TMEM accumulation chunk: kChunkMMA or kChunkMMALong
   int ksplit;            // K ranges per output tile (> 1 only for E_STORE (out zeroed before, the
                          // first range adds the bias), E_RESID and E_RESID_GATE: each range adds
                          // its partial product into out with vector reductions)
@@ -62,6 +108,7 @@ struct DenseArgs {
   // E_*_SPLIT: fp16 planes [M][kActTerms * ldh] (hi of column c at c, lo at ldh + c)
   __half* act2;
   int ldh;
+  RopeEpi rope;          // E_ROPE_KV
   DevErr* err;
 };
 
@@ -90,7 +137,8 @@ __host__ __device__ constexpr int dense_slot_bytes(int planes) { return planes *
 
 // Epilogue: eight warps; warp 4 + e reads TMEM lanes 32 (e % 4) .. + 31 (the
 // rows of its quadrant) and columns 128 (e / 4) .. + 127 of the 256-wide
-// accumulator.  Each passes its 32 rows x 128 columns through a 4 KB buffer
+// accumulator (E_ROPE_KV: pairs 32 (e / 4) .. + 31 of the tile's two heads,
+// see rope_rot_load).  Each passes its 32 rows x 128 columns through a 4 KB buffer
 // [32 rows][8 float4] in four 32-column quarters, float4 chunk c of row r at
 // position c ^ (r & 7) (conflict-free both for a lane writing its own row and
 // for 8 lanes reading one row), so that global reads and writes run along rows
@@ -174,6 +222,103 @@ __device__ __forceinline__ void epi_quarter(const DenseArgs& a, const float4* st
   }
 }
 
+// One staged 32-column quarter (columns col0 .. col0 + 31 of part `part`) of
+// the E_ROPE_KV epilogue: q rows as fp32, k / v rows as bf16 into the ring and
+// as two fp16 planes.  Lane l takes float4 chunk l & 7 of rows 4i + (l >> 3).
+__device__ __forceinline__ void rope_quarter(const DenseArgs& a, const float4* st, int row0, int part, int col0,
+                                             int lane, int b0) {
+  const RopeEpi& r = a.rope;
+  const int c = lane & 7, rsub = lane >> 3, col = col0 + 4 * c, D = r.heads * 128;
+#pragma unroll 2
+  for (int i = 0; i < 32; i += 4) {
+    const int r0 = i + rsub, row = row0 + r0;
+    if (row >= a.M) continue;
+    const float4 v = st[r0 * 8 + (c ^ (r0 & 7))];
+    if (part == 0) {
+      *reinterpret_cast<float4*>(r.q_out + (size_t)row * D + col) = v;
+      continue;
+    }
+    int b = b0, j = row - b0 * r.T;   // b0 = row0 / T: chunks of at least 32 rows step once at most
+    while (j >= r.T) {
+      j -= r.T;
+      ++b;
+    }
+    const __nv_bfloat162 x = __floats2bfloat162_rn(v.x, v.y), z = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(ring_row(r.ring, b, j, part - 1) + col) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&z));
+    uint2 h, l;
+    split_pair_h2(v.x, v.y, h.x, l.x);
+    split_pair_h2(v.z, v.w, h.y, l.y);
+    __half* p = r.own16 + (size_t)row * 4 * D + (size_t)(part - 1) * 2 * D + col;
+    *reinterpret_cast<uint2*>(p) = h;
+    *reinterpret_cast<uint2*>(p + D) = l;
+  }
+}
+
+// E_ROPE_KV: the 256 columns of a tile are two heads of one part (q, k or
+// v); epilogue warp hc takes pairs 32 hc .. 32 hc + 31 of both, so lane l
+// holds acc[32 k + t] = tile column 32 hc + 64 k + t of row row0 + l (k = 0, 1:
+// the pair's first and second members in head 0, k = 2, 3 in head 1) and
+// needs the rotation of 32 pairs of its row only.  rope_rot_load fetches that
+// of 16 pairs (cos and sin of pairs 32 hc + 16 h .. + 15: 8 float4, coalesced
+// over the warp's 32 rows); the first half is issued before the last
+// accumulation chunk lands, so that its L2 latency overlaps the MMAs.
+__device__ __forceinline__ void rope_rot_load(const DenseArgs& a, int row0, int hc, int h, int lane,
+                                              float4 (&rv)[8]) {
+  const float4* rc = a.rope.rot + (size_t)(row0 >> 5) * 1024 + (hc * 8 + h * 4) * 32 + lane;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    rv[u] = __ldg(rc + u * 32);            // cos of pairs 32 hc + 16 h + 4u .. + 3
+    rv[4 + u] = __ldg(rc + 512 + u * 32);  // sin
+  }
+}
+
+// Turn pairs t = 16 h .. 16 h + 15 (of the warp's 32) of both heads by rv,
+// the weight scale sc folded into cos and sin (a power of two: exact).
+__device__ __forceinline__ void rope_turn(float (&acc)[128], const float4 (&rv)[8], int h, float sc) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float cc[4] = {rv[u].x * sc, rv[u].y * sc, rv[u].z * sc, rv[u].w * sc};
+    const float ss[4] = {rv[4 + u].x * sc, rv[4 + u].y * sc, rv[4 + u].z * sc, rv[4 + u].w * sc};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int t = 64 * g + 16 * h + 4 * u + e;
+        const float x0 = acc[t], x1 = acc[32 + t];
+        acc[t] = x0 * cc[e] - x1 * ss[e];
+        acc[32 + t] = x1 * cc[e] + x0 * ss[e];
+      }
+    }
+  }
+}
+
+// E_ROPE_KV epilogue of one tile for the warp's 32 rows (layout above): q and
+// k heads turn each pair by the row's rotation (rv0: pairs 0 .. 15 of the
+// warp's, loaded during the last chunk), then every quarter passes through
+// the staging buffer to its stores.
+__device__ __forceinline__ void rope_epilogue(const DenseArgs& a, float (&acc)[128], int row0, int n0, float4* st,
+                                              int lane, const float4 (&rv0)[8]) {
+  const RopeEpi& r = a.rope;
+  const int D = r.heads * 128, hc = (n0 >> 7) & 1, t0 = n0 - hc * 128;
+  const int part = t0 / D, col0 = t0 - part * D + hc * 32, b0 = row0 / r.T;
+  float sc = a.out_scale;
+  if (part < 2) {
+    rope_turn(acc, rv0, 0, sc);
+    float4 rv1[8];
+    if (row0 < a.M) rope_rot_load(a, row0, hc, 1, lane, rv1);
+    rope_turn(acc, rv1, 1, sc);
+    sc = 1.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    stage_put(st, lane, acc + 32 * k, sc);
+    __syncwarp();
+    rope_quarter(a, st, row0, part, col0 + (k >> 1) * 128 + (k & 1) * 64, lane, b0);
+    __syncwarp();
+  }
+}
+
 // Epilogue of one tile for the warp's 32 rows (lane l holds the 128
 // accumulated columns of row row0 + l): output columns n0 .. n0 + 127, or for
 // the gate/up tile of E_GEGLU_SPLIT ([64 gate | 64 up] of features f0 ..
@@ -202,7 +347,9 @@ __device__ __forceinline__ void dense_epilogue(const DenseArgs& a, float (&acc)[
   }
 }
 
-template <int STAGES, int PLANES>
+// ROPE: the E_ROPE_KV instantiation (its own column assignment and epilogue;
+// the other epilogues run in the instantiation without them).
+template <int STAGES, int PLANES, bool ROPE>
 __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_constant__ CUtensorMap amap,
                                                                   const __grid_constant__ CUtensorMap wmap,
                                                                   const __grid_constant__ DenseArgs a) {
@@ -221,7 +368,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
   const int n_tiles = a.N / 256, m_tiles = (a.M + 127) / 128, mn = m_tiles * n_tiles;
   const int tiles = mn * a.ksplit;                            // tile t: K range t / mn of output tile t % mn
   const int nkb = a.K / 64;                                   // K-blocks of one plane
-  const int chunk_kb = kChunkMMA / (4 * a.terms);             // K-blocks per accumulation chunk
+  const int chunk_kb = a.chunk_mma / (4 * a.terms);           // K-blocks per accumulation chunk
   // K-blocks [kb0, kb1) of tile t and their accumulation chunks
   auto krange = [&](int t, int& kb0, int& kb1) {
     const int ks = t / mn;
@@ -319,6 +466,7 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDRegsEpi));
     const int ew = warp - 4;
     const int quad = warp & 3, hc = ew >> 2;   // TMEM lane quadrant, column half
+    constexpr bool rope = ROPE;
     float4* st = stage + ew * 32 * 8;
     uint32_t gch = 0;
     bool ok = true;
@@ -332,23 +480,33 @@ __global__ void __launch_bounds__(kDThreads, 1) dense_gemm_kernel(const __grid_c
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      // the warp's 128 accumulator columns: 16-column pieces c at col(c) =
+      // base + (c / 2) pstride + (c % 2) 16 (E_ROPE_KV: pairs 32 hc .. of both heads)
+      const int cbase = rope ? hc * 32 : hc * 128;
+      constexpr int pstride = rope ? 64 : 32;
+      float4 rv[8];   // E_ROPE_KV: the rotation of the first 16 pairs
       for (int ch = 0; ch < nchunk; ++ch, ++gch) {
         const int buf = gch & 1;
+        if constexpr (rope) {
+          if (ch == nchunk - 1 && row0 < a.M) rope_rot_load(a, row0, hc, 0, lane, rv);
+        }
         // warp-uniform outcome: the TMEM loads below are warp-collective
         if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (gch >> 1) & 1, a.err, 23))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + hc * 128);
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * 256 + cbase);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           float v[16];
-          tmem_ld16(tb + c * 16, v);
+          tmem_ld16(tb + (c >> 1) * pstride + (c & 1) * 16, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[c * 16 + j] += v[j];
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
       }
-      if (ok) dense_epilogue(a, acc, row0, tn * 256 + hc * 128, tn * 128 + hc * 64, st, lane, tile < mn);
+      if (!ok) break;
+      if constexpr (rope) rope_epilogue(a, acc, row0, tn * 256 + hc * 128, st, lane, rv);
+      else dense_epilogue(a, acc, row0, tn * 256 + hc * 128, tn * 128 + hc * 64, st, lane, tile < mn);
     }
   }
   tc_fence_before();

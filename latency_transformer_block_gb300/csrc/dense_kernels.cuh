@@ -115,12 +115,13 @@ static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// RoPE + K/V into the cache.  Input qkv fp32 [M][ld_qkv] = [q (Hq*dh) | k | v]
-// (or [k | v] when q_cols == 0).  Row m belongs to group b = m / T (a chunk or a
-// batch element) at token j = m % T, position pos0[b] + j.
+// RoPE + K/V into the cache (prefix prefill).  Input qkv fp32 [M][ld_qkv] =
+// [q (Hq*dh) | k | v] (or [k | v] when q_cols == 0).  Row m belongs to batch
+// element b = m / T at token j = m % T, position pos0[b] + j.
 //   cos/sin(pos * theta_i) = rotation of j (fp32 table built from float64)
 //   composed with the rotation of pos0[b] (float64 on the device, per CTA).
-// q -> fp32 q_out [M][Hq*dh]; k, v -> bf16 rows j of kdst[b], vdst[b].
+// q -> fp32 q_out [M][Hq*dh]; k, v -> bf16 rows j of kdst[b], vdst[b] and the
+// two fp16 planes of the values as computed.
 // Grid M, blockDim 128.
 // ---------------------------------------------------------------------------
 struct RopeKvArgs {
@@ -139,49 +140,33 @@ struct RopeKvArgs {
   __nv_bfloat16* vdst[kMaxChunks];
   int kv_ld;                // row stride of kdst / vdst (elements)
   __half* kb2;              // K (after RoPE) and V as computed, as two fp16 planes
-  __half* vb2;              //   [M][kv_cols] (hi), then lo lo_off elements later, or
+  __half* vb2;              //   [M][kv_cols] (hi), then lo lo_off elements later
   long long lo_off;
-  __half* k16;              // the same as two fp16 planes (hi at column c, lo at kv_cols + c)
-  __half* v16;              // of rows ld16 apart
-  int ld16;
-  // page_tokens > 0: kdst / vdst unused; group b's token j is ring row
-  // row0[b] + j, which lives in page ptab[b][row / page_tokens] of the pool
-  // [pages][2][page_tokens][kv_ld] (plane 0 K, 1 V) at row % page_tokens
-  int page_tokens;
-  const int* ptab[kMaxChunks];
-  int row0[kMaxChunks];
-  __nv_bfloat16* pool;
 };
+
+// cos / sin of pos0 * theta_i in float64, rounded to fp32 (1, 0 at pos0 = 0)
+__device__ __forceinline__ void base_rotation(long long pos0, double theta, float& c, float& s) {
+  if (pos0 == 0) {
+    c = 1.f;
+    s = 0.f;
+  } else {
+    double sd, cd;
+    sincos((double)pos0 * theta, &sd, &cd);
+    c = (float)cd;
+    s = (float)sd;
+  }
+}
 
 static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
   const int m = blockIdx.x;
   const int b = m / a.T, j = m % a.T;
   const int half = a.dh / 2;
   __shared__ float cb[128], sb[128];   // rotation of pos0[b], dh/2 <= 128
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    if (a.pos0[b] == 0) {
-      cb[i] = 1.f;
-      sb[i] = 0.f;
-    } else {
-      double s, c;
-      sincos((double)a.pos0[b] * a.theta[i], &s, &c);
-      cb[i] = (float)c;
-      sb[i] = (float)s;
-    }
-  }
+  for (int i = threadIdx.x; i < half; i += blockDim.x) base_rotation(a.pos0[b], a.theta[i], cb[i], sb[i]);
   __syncthreads();
   const float* row = a.qkv + (size_t)m * a.ld_qkv;
-  __nv_bfloat16* krow;   // this token's K and V rows in the ring (or its page)
-  __nv_bfloat16* vrow;
-  if (a.page_tokens > 0) {
-    const int r = a.row0[b] + j, P = a.page_tokens;
-    const size_t k0 = ((size_t)a.ptab[b][r / P] * 2 * P + r % P) * a.kv_ld;
-    krow = a.pool + k0;
-    vrow = a.pool + k0 + (size_t)P * a.kv_ld;
-  } else {
-    krow = a.kdst[b] + (size_t)j * a.kv_ld;
-    vrow = a.vdst[b] + (size_t)j * a.kv_ld;
-  }
+  __nv_bfloat16* krow = a.kdst[b] + (size_t)j * a.kv_ld;   // this token's K and V rows in the cache
+  __nv_bfloat16* vrow = a.vdst[b] + (size_t)j * a.kv_ld;
   const float* cj = a.cos_j + (size_t)j * half;
   const float* sj = a.sin_j + (size_t)j * half;
   const int nq = a.q_cols / a.dh, nk = a.kv_cols / a.dh;
@@ -216,30 +201,16 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
       __nv_bfloat16* kr = krow + (col - a.q_cols);
       *reinterpret_cast<uint2*>(kr) = bf4(y0);
       *reinterpret_cast<uint2*>(kr + half) = bf4(y1);
-      if (a.k16) {
-        __half* k16 = a.k16 + (size_t)m * a.ld16 + (col - a.q_cols);
-        const uint2 h0 = pack_half4(y0[0], y0[1], y0[2], y0[3]), h1 = pack_half4(y1[0], y1[1], y1[2], y1[3]);
-        const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&h0.x));
-        const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&h0.y));
-        const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&h1.x));
-        const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&h1.y));
-        *reinterpret_cast<uint2*>(k16) = h0;
-        *reinterpret_cast<uint2*>(k16 + half) = h1;
-        *reinterpret_cast<uint2*>(k16 + a.kv_cols) = pack_half4(y0[0] - a0.x, y0[1] - a0.y, y0[2] - a1.x, y0[3] - a1.y);
-        *reinterpret_cast<uint2*>(k16 + a.kv_cols + half) =
-            pack_half4(y1[0] - b0.x, y1[1] - b0.y, y1[2] - b1.x, y1[3] - b1.y);
-      } else {
-        __half* kp = a.kb2 + (size_t)m * a.kv_cols + (col - a.q_cols);
-        uint2 h, l;
-        split_pair_h2(y0[0], y0[1], h.x, l.x);
-        split_pair_h2(y0[2], y0[3], h.y, l.y);
-        *reinterpret_cast<uint2*>(kp) = h;
-        *reinterpret_cast<uint2*>(kp + a.lo_off) = l;
-        split_pair_h2(y1[0], y1[1], h.x, l.x);
-        split_pair_h2(y1[2], y1[3], h.y, l.y);
-        *reinterpret_cast<uint2*>(kp + half) = h;
-        *reinterpret_cast<uint2*>(kp + half + a.lo_off) = l;
-      }
+      __half* kp = a.kb2 + (size_t)m * a.kv_cols + (col - a.q_cols);
+      uint2 h, l;
+      split_pair_h2(y0[0], y0[1], h.x, l.x);
+      split_pair_h2(y0[2], y0[3], h.y, l.y);
+      *reinterpret_cast<uint2*>(kp) = h;
+      *reinterpret_cast<uint2*>(kp + a.lo_off) = l;
+      split_pair_h2(y1[0], y1[1], h.x, l.x);
+      split_pair_h2(y1[2], y1[3], h.y, l.y);
+      *reinterpret_cast<uint2*>(kp + half) = h;
+      *reinterpret_cast<uint2*>(kp + half + a.lo_off) = l;
     }
   }
   const float* vr = row + a.q_cols + a.kv_cols;
@@ -247,21 +218,64 @@ static __global__ void __launch_bounds__(128) rope_kv_kernel(RopeKvArgs a) {
     const float4 t = *reinterpret_cast<const float4*>(vr + c);
     const float y[4] = {t.x, t.y, t.z, t.w};
     *reinterpret_cast<uint2*>(vrow + c) = bf4(y);
-    if (a.v16) {
-      __half* v16 = a.v16 + (size_t)m * a.ld16 + c;
-      const uint2 h = pack_half4(y[0], y[1], y[2], y[3]);
-      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-      *reinterpret_cast<uint2*>(v16) = h;
-      *reinterpret_cast<uint2*>(v16 + a.kv_cols) = pack_half4(y[0] - f0.x, y[1] - f0.y, y[2] - f1.x, y[3] - f1.y);
-    } else {
-      __half* vp = a.vb2 + (size_t)m * a.kv_cols + c;
-      uint2 h, l;
-      split_pair_h2(y[0], y[1], h.x, l.x);
-      split_pair_h2(y[2], y[3], h.y, l.y);
-      *reinterpret_cast<uint2*>(vp) = h;
-      *reinterpret_cast<uint2*>(vp + a.lo_off) = l;
+    __half* vp = a.vb2 + (size_t)m * a.kv_cols + c;
+    uint2 h, l;
+    split_pair_h2(y[0], y[1], h.x, l.x);
+    split_pair_h2(y[2], y[3], h.y, l.y);
+    *reinterpret_cast<uint2*>(vp) = h;
+    *reinterpret_cast<uint2*>(vp + a.lo_off) = l;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rotation of every row of a DiT call (dh = 128), the table the E_ROPE_KV
+// epilogue of the QKV projection reads: row m (token j = m % T of chunk
+// b = m / T) turns pair i by cos/sin(pos0[b] theta_i) (float64 on the device)
+// composed with the token's own cos_j / sin_j (the 1-D position j, or the
+// frame-within-chunk, row and column of a video token).  Output per 32-row
+// group g: [2][16][32] float4, (cos | sin) of pairs 4i .. 4i + 3 of row 32g + r,
+// so that a warp holding rows 32g .. 32g + 31 reads each float4 row coalesced.
+// Rows m >= M of the last group repeat row M - 1.  Grid ceil(M / 32), blockDim 256.
+// ---------------------------------------------------------------------------
+struct RopeRowsArgs {
+  int M, T, n;              // rows, rows per chunk, chunks
+  const float* cos_j;       // [T][64]
+  const float* sin_j;
+  const double* theta;      // [64] the per-pair frequency the chunk's base position turns by
+  long long pos0[kMaxChunks];
+  float4* rot;
+};
+
+static __global__ void __launch_bounds__(256) rope_rows_kernel(RopeRowsArgs a) {
+  const int m0 = blockIdx.x * 32, b0 = m0 / a.T;
+  __shared__ float cb[2][64], sb[2][64];   // base rotations of chunks b0, b0 + 1
+  if (threadIdx.x < 128) {
+    const int k = threadIdx.x >> 6, i = threadIdx.x & 63, b = min(b0 + k, a.n - 1);
+    base_rotation(a.pos0[b], a.theta[i], cb[k][i], sb[k][i]);
+  }
+  __syncthreads();
+  float4* out = a.rot + (size_t)blockIdx.x * 1024;
+  for (int it = threadIdx.x; it < 512; it += blockDim.x) {
+    const int r = it & 31, i = 4 * (it >> 5);
+    const int m = min(m0 + r, a.M - 1), b = m / a.T, j = m - b * a.T;
+    const float4 cv = *reinterpret_cast<const float4*>(a.cos_j + (size_t)j * 64 + i);
+    const float4 sv = *reinterpret_cast<const float4*>(a.sin_j + (size_t)j * 64 + i);
+    const float cjj[4] = {cv.x, cv.y, cv.z, cv.w}, sjj[4] = {sv.x, sv.y, sv.z, sv.w};
+    float c[4], s[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float bc, bs;
+      if (b - b0 < 2) {
+        bc = cb[b - b0][i + e];
+        bs = sb[b - b0][i + e];
+      } else {   // chunks shorter than 32 rows: a group spans more than two
+        base_rotation(a.pos0[b], a.theta[i + e], bc, bs);
+      }
+      c[e] = cjj[e] * bc - sjj[e] * bs;
+      s[e] = sjj[e] * bc + cjj[e] * bs;
     }
+    out[(it >> 5) * 32 + r] = make_float4(c[0], c[1], c[2], c[3]);
+    out[512 + (it >> 5) * 32 + r] = make_float4(s[0], s[1], s[2], s[3]);
   }
 }
 

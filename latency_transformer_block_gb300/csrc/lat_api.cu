@@ -155,6 +155,7 @@ struct lat_ctx {
   double* theta = nullptr;
   __half *kown = nullptr, *vown = nullptr;   // own tokens' K/V as computed, two fp16 planes [2][m_max][kvd] (prefill)
   __half* kvown16 = nullptr;   // the same as fp16 planes [M][K hi | K lo | V hi | V lo] (DiT)
+  float4* rope_rot = nullptr;  // DiT: each row's rotation, [m_max / 32][2][16][32] float4 (rope_rows_kernel)
   __half* hist16 = nullptr;    // fp16 copy of one call's history K/V planes, [planes][T_q][D] (DiT)
   int hist_rows = 0;
   __half *act2 = nullptr, *act2f = nullptr;   // fp16 activation planes [M][kActTerms * K]
@@ -827,6 +828,9 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
   const CUtensorMap* wm[8] = {&c->map_qkv, &c->map_o, &c->map_up, &c->map_down, &c->map_patch,
                               &c->map_cq, &c->map_co, &c->map_ckv};
   a.err = c->err;
+  // DiT projections with a long epilogue (RoPE + cache stores, GELU + plane
+  // split): longer chunks, so that the MMAs run on through it
+  a.chunk_mma = c->d.kind == LAT_DIT && (a.epi == E_ROPE_KV || a.epi == E_GELU_SPLIT) ? kChunkMMALong : kChunkMMA;
   a.f16 = wsel != W_PATCH;
   a.out_scale = wsel != W_PATCH ? c->wscale[wsel] : 1.f;
   if (a.N % 256 || a.K % 64 || a.terms < 1 || a.terms > kActTerms) return fail(LAT_ERR_SHAPE, "dense GEMM shape");
@@ -842,8 +846,12 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
     CUDA_TRY(cudaMemsetAsync(a.out, 0, (size_t)a.M * a.ldo * sizeof(float), st));
   const int tiles = mn * a.ksplit;
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;   // persistent over the tiles
-  dense_gemm_kernel<kDStages, kActTerms>
-      <<<grid, kDThreads, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel], a);
+  if (a.epi == E_ROPE_KV)
+    dense_gemm_kernel<kDStages, kActTerms, true>
+        <<<grid, kDThreads, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel], a);
+  else
+    dense_gemm_kernel<kDStages, kActTerms, false>
+        <<<grid, kDThreads, dense_smem_bytes(kDStages, kActTerms), st>>>(amap, *wm[wsel], a);
   return launch_check("dense_gemm");
 }
 
@@ -938,10 +946,14 @@ static lat_status alloc_dense_workspace(lat_ctx* c, int rows_per_group) {
   const int wact = d.D > qd ? d.D : qd;
   LAT_TRY(c->alloc(&c->act2, (size_t)c->m_max * terms * wact));
   LAT_TRY(c->alloc(&c->act2f, (size_t)c->m_max * terms * d.F));
-  LAT_TRY(c->alloc(&c->qkvbuf, (size_t)c->m_max * c->nqkv));
+  // fp32 [q | k | v] of the prefill's QKV projection; a DiT block rotates and
+  // stores in the projection's epilogue, and uses it only to encode the text
+  if (d.kind != LAT_DIT) LAT_TRY(c->alloc(&c->qkvbuf, (size_t)c->m_max * c->nqkv));
+  else if (d.text_len > 0) LAT_TRY(c->alloc(&c->qkvbuf, (size_t)d.text_len * 2 * d.D));
   LAT_TRY(c->alloc(&c->qbuf, (size_t)c->m_max * qd));
   if (d.kind == LAT_DIT) {
     LAT_TRY(c->alloc(&c->kvown16, (size_t)c->m_max * 4 * d.Hkv * d.dh));
+    LAT_TRY(c->alloc(&c->rope_rot, (size_t)(c->m_max + 31) / 32 * 1024));
     const int planes = std::max(1, 2 * d.max_batch * d.n_hist);
     if (planes > kMaxHistPlanes) return fail(LAT_ERR_SHAPE, "max_batch x n_hist must be <= %d", kMaxHistPlanes / 2);
     if ((size_t)planes * d.T_q > 0x7fffffffu) return fail(LAT_ERR_SHAPE, "history copy too large for one tensor map");
@@ -1350,19 +1362,18 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   }
   norm_split_kernel<<<M, 256, 0, st>>>(na);
   LAT_TRY(launch_check("norm_split"));
-  {
-    DenseArgs a{};
-    a.M = M; a.N = 3 * D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * 3 * D; a.epi = E_STORE; a.out = c->qkvbuf;
-    a.ldo = 3 * D;
-    LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, a, st));
-  }
-  RopeKvArgs ra{};
-  ra.qkv = c->qkvbuf; ra.ld_qkv = 3 * D; ra.q_cols = D; ra.kv_cols = D; ra.dh = d.dh; ra.T = T;
-  ra.cos_j = c->cos_j; ra.sin_j = c->sin_j; ra.theta = c->theta; ra.q_out = c->qbuf; ra.kv_ld = D;
-  ra.k16 = c->kvown16; ra.v16 = c->kvown16 + 2 * D; ra.ld16 = 4 * D;
+  // the QKV projection turns q and k and stores q, the ring rows and the fp16
+  // planes of the own K / V in its epilogue, from each row's rotation
+  RopeRowsArgs rr{};
+  rr.M = M; rr.T = T; rr.n = n; rr.cos_j = c->cos_j; rr.sin_j = c->sin_j; rr.theta = c->theta; rr.rot = c->rope_rot;
+  DenseArgs qa{};
+  qa.M = M; qa.N = 3 * D; qa.K = D; qa.terms = c->act_terms; qa.w_row0 = l * 3 * D; qa.epi = E_ROPE_KV;
+  RopeEpi& ra = qa.rope;
+  ra.rot = c->rope_rot; ra.heads = d.Hq; ra.T = T; ra.q_out = c->qbuf; ra.own16 = c->kvown16;
+  ra.ring.ld = D;
   if (P > 0) {
-    ra.page_tokens = P;
-    ra.pool = kv;
+    ra.ring.page_tokens = P;
+    ra.ring.pool = kv;
   }
   // the page list of ring (stream, layer, step)
   auto pages = [&](int stream, int step) {
@@ -1379,13 +1390,13 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   long long hkey[kMaxHistPlanes / 2];   // (stream, step, slot) of each copied segment
   for (int b = 0; b < n; ++b) {
     const int cb = ch[b].chunk, sb = ch[b].step, stb = ch[b].stream;
-    ra.pos0[b] = d.grid_h > 0 ? (long long)cb * c->frames_per_chunk : chunk_pos0(cb, T);
+    rr.pos0[b] = d.grid_h > 0 ? (long long)cb * c->frames_per_chunk : chunk_pos0(cb, T);
     if (P > 0) {
-      ra.ptab[b] = pages(stb, sb);
-      ra.row0[b] = ring_slot_of(cb, d.n_hist) * T;
+      ra.ring.ptab[b] = pages(stb, sb);
+      ra.ring.row0[b] = ring_slot_of(cb, d.n_hist) * T;
     } else {
-      ra.kdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 0);
-      ra.vdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 1);
+      ra.ring.kdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 0);
+      ra.ring.vdst[b] = ring_ptr(c, kv, stb, l, sb, ring_slot_of(cb, d.n_hist), 1);
     }
     int ns = 0;
     for (int k = d.n_hist; k >= 1; --k) {       // history, oldest first
@@ -1420,9 +1431,10 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     sa.grp[b].seg[ns++] = AttnSeg{nullptr, nullptr, nullptr, nullptr, T, own, own + 2 * D};
     sa.grp[b].nseg = ns;
   }
-  rope_kv_kernel<<<M, 128, 0, st>>>(ra);
-  LAT_TRY(launch_check("rope_kv"));
-  if (hc.planes > 0) {   // after rope_kv: a chunk of this call may be another's history
+  rope_rows_kernel<<<(M + 31) / 32, 256, 0, st>>>(rr);
+  LAT_TRY(launch_check("rope_rows"));
+  LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, qa, st));
+  if (hc.planes > 0) {   // after the ring rows are written: a chunk of this call may be another's history
     const size_t chunks = (size_t)hc.planes * T * D / 8;
     const unsigned grid = (unsigned)std::min<size_t>((chunks + 255) / 256, (size_t)c->num_sms * 8);
     hist_to_f16_kernel<<<grid, 256, 0, st>>>(hc);
@@ -1564,8 +1576,8 @@ lat_status lat_create(const lat_model_desc* desc, const lat_weights* w, lat_ctx*
     cudaFuncSetAttribute(skinny_gemm_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          skinny_smem_bytes(kStages));
     set_attention_smem_limits();
-    cudaFuncSetAttribute(dense_gemm_kernel<kDStages, kActTerms>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         dense_smem_bytes(kDStages, kActTerms));
+    for (auto k : {dense_gemm_kernel<kDStages, kActTerms, false>, dense_gemm_kernel<kDStages, kActTerms, true>})
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes(kDStages, kActTerms));
     cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_tc_smem_bytes());
     for (int dh : {64, 128, 256})
       for (bool chunk : {false, true})
