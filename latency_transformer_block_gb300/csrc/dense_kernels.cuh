@@ -12,7 +12,8 @@ namespace lat {
 //           LayerNorm affine: scale = g - 1, shift = b, the same for every b)
 //   NONE:   u = x                                        (the planes alone)
 //   act[m][c] = fp16(u), act[m][D + c] = fp16(u - act[m][c])
-// One CTA of 256 threads per row.
+// One CTA of 256 threads per row (norm_split_kernel), or one warp per row for
+// D <= 2048 (norm_split_warp_kernel).
 // ---------------------------------------------------------------------------
 enum NormMode : int { NORM_RMS = 0, NORM_LN_MOD = 1, NORM_NONE = 2 };
 
@@ -35,6 +36,25 @@ constexpr int kNormV = 8;
 __device__ __forceinline__ uint2 pack_half4(float a, float b, float c, float d) {
   const __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
   return make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+}
+
+// Columns 4c .. 4c + 3 of a row: normalised (mean mu, factor rs), the adaLN /
+// affine rows applied (LN_MOD), stored as the two fp16 planes.
+__device__ __forceinline__ void norm_store4(const NormArgs& a, __half* hi, int c, float4 x, float mu, float rs,
+                                            const float4* sh, const float4* sc) {
+  float w[4] = {(x.x - mu) * rs, (x.y - mu) * rs, (x.z - mu) * rs, (x.w - mu) * rs};
+  if (a.mode == NORM_LN_MOD) {
+    const float4 k = __ldg(sc + c), t = __ldg(sh + c);
+    w[0] = w[0] * (1.f + k.x) + t.x;
+    w[1] = w[1] * (1.f + k.y) + t.y;
+    w[2] = w[2] * (1.f + k.z) + t.z;
+    w[3] = w[3] * (1.f + k.w) + t.w;
+  }
+  const uint2 h = pack_half4(w[0], w[1], w[2], w[3]);
+  const __half2 h01 = *reinterpret_cast<const __half2*>(&h.x), h23 = *reinterpret_cast<const __half2*>(&h.y);
+  const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+  *reinterpret_cast<uint2*>(hi + 4 * c) = h;
+  *reinterpret_cast<uint2*>(hi + a.D + 4 * c) = pack_half4(w[0] - f01.x, w[1] - f01.y, w[2] - f23.x, w[3] - f23.y);
 }
 
 static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
@@ -97,20 +117,60 @@ static __global__ void __launch_bounds__(256) norm_split_kernel(NormArgs a) {
 #pragma unroll
   for (int u = 0; u < kNormV; ++u) {
     const int c = threadIdx.x + 256 * u;
-    if (c >= n4) continue;
-    float w[4] = {(v[u].x - mu) * rs, (v[u].y - mu) * rs, (v[u].z - mu) * rs, (v[u].w - mu) * rs};
-    if (a.mode == NORM_LN_MOD) {
-      const float4 k = __ldg(sc + c), t = __ldg(sh + c);
-      w[0] = w[0] * (1.f + k.x) + t.x;
-      w[1] = w[1] * (1.f + k.y) + t.y;
-      w[2] = w[2] * (1.f + k.z) + t.z;
-      w[3] = w[3] * (1.f + k.w) + t.w;
-    }
-    const uint2 h = pack_half4(w[0], w[1], w[2], w[3]);
-    const __half2 h01 = *reinterpret_cast<const __half2*>(&h.x), h23 = *reinterpret_cast<const __half2*>(&h.y);
-    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-    *reinterpret_cast<uint2*>(hi + 4 * c) = h;
-    *reinterpret_cast<uint2*>(hi + a.D + 4 * c) = pack_half4(w[0] - f01.x, w[1] - f01.y, w[2] - f23.x, w[3] - f23.y);
+    if (c < n4) norm_store4(a, hi, c, v[u], mu, rs, sh, sc);
+  }
+}
+
+// The same for rows of D <= 32 * 4 * NV: one warp per row (eight a CTA), the
+// row in registers, the sums by warp shuffles alone.  Grid ceil(M / 8).
+template <int NV>
+static __global__ void __launch_bounds__(256) norm_split_warp_kernel(NormArgs a, int M) {
+  const int m = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (m >= M) return;   // whole warps; nothing below synchronises the CTA
+  const int n4 = a.D / 4;
+  const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)m * a.D);
+  auto warp_sum = [](float v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
+  float4 v[NV];
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    const int c = lane + 32 * u;
+    v[u] = c < n4 ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float mu = 0.f, rs = 1.f;
+  if (a.mode == NORM_LN_MOD) {
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) s += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+    mu = warp_sum(s) / a.D;
+    float q = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u)
+      if (lane + 32 * u < n4) {
+        const float d0 = v[u].x - mu, d1 = v[u].y - mu, d2 = v[u].z - mu, d3 = v[u].w - mu;
+        q += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+      }
+    rs = rsqrtf(warp_sum(q) / a.D + a.eps);
+  } else if (a.mode == NORM_RMS) {
+    float q = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) q += (v[u].x * v[u].x + v[u].y * v[u].y) + (v[u].z * v[u].z + v[u].w * v[u].w);
+    rs = rsqrtf(warp_sum(q) / a.D + a.eps);
+  }
+  const float4* sh = nullptr;
+  const float4* sc = nullptr;
+  if (a.mode == NORM_LN_MOD) {
+    const int b = m / a.rows_per_chunk;
+    sh = reinterpret_cast<const float4*>(a.table + a.shift_off[b]);
+    sc = reinterpret_cast<const float4*>(a.table + a.scale_off[b]);
+  }
+  __half* hi = a.act2 + (size_t)m * kActTerms * a.D;
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    const int c = lane + 32 * u;
+    if (c < n4) norm_store4(a, hi, c, v[u], mu, rs, sh, sc);
   }
 }
 

@@ -855,6 +855,18 @@ static lat_status enqueue_dense(const lat_ctx* c, const CUtensorMap& amap, int w
   return launch_check("dense_gemm");
 }
 
+// norm prologue of M rows: one warp per row up to D = 2048, else one CTA per row
+static lat_status enqueue_norm(const NormArgs& na, int M, cudaStream_t st) {
+  const unsigned g = (unsigned)((M + 7) / 8);
+  const int nv = (na.D + 127) / 128;   // float4 per lane
+  if (nv <= 4) norm_split_warp_kernel<4><<<g, 256, 0, st>>>(na, M);
+  else if (nv <= 8) norm_split_warp_kernel<8><<<g, 256, 0, st>>>(na, M);
+  else if (nv <= 12) norm_split_warp_kernel<12><<<g, 256, 0, st>>>(na, M);
+  else if (nv <= 16) norm_split_warp_kernel<16><<<g, 256, 0, st>>>(na, M);
+  else norm_split_kernel<<<M, 256, 0, st>>>(na);
+  return launch_check("norm_split");
+}
+
 // tensor map of a row-major bf16 activation [rows][cols] read in 128 x 64 tiles
 static lat_status make_act_map(CUtensorMap* map, const void* base, int rows, int cols) {
   return make_kmajor_map(map, base, rows, cols, 128);
@@ -1284,8 +1296,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
     const bool last = (l == L - 1);
     NormArgs na{};
     na.x = c->xres; na.D = D; na.mode = NORM_RMS; na.eps = d.eps; na.act2 = c->act2;
-    norm_split_kernel<<<M, 256, 0, st>>>(na);
-    LAT_TRY(launch_check("norm_split"));
+    LAT_TRY(enqueue_norm(na, M, st));
     {
       DenseArgs a{};
       a.M = M; a.K = D; a.terms = c->act_terms; a.epi = E_STORE; a.out = c->qkvbuf;
@@ -1321,8 +1332,7 @@ static lat_status enqueue_prefill(lat_ctx* c, const bf16* pe, int B, bf16* kv, c
       a.M = M; a.N = D; a.K = qd; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_RESID; a.out = c->xres; a.ldo = D;
       LAT_TRY(enqueue_dense(c, c->map_act_o, W_O, a, st));
     }
-    norm_split_kernel<<<M, 256, 0, st>>>(na);
-    LAT_TRY(launch_check("norm_split"));
+    LAT_TRY(enqueue_norm(na, M, st));
     {
       DenseArgs a{};
       a.M = M; a.N = 2 * F; a.K = D; a.terms = c->act_terms; a.w_row0 = l * 2 * F; a.epi = E_GEGLU_SPLIT;
@@ -1360,8 +1370,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     na.shift_off[b] = ch[b].step * 6 * D + 0 * D;
     na.scale_off[b] = ch[b].step * 6 * D + 1 * D;
   }
-  norm_split_kernel<<<M, 256, 0, st>>>(na);
-  LAT_TRY(launch_check("norm_split"));
+  LAT_TRY(enqueue_norm(na, M, st));
   // the QKV projection turns q and k and stores q, the ring rows and the fp16
   // planes of the own K / V in its epilogue, from each row's rotation
   RopeRowsArgs rr{};
@@ -1460,8 +1469,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
       nc.scale_off[b] = l * 2 * D + D;
     }
     nc.table = c->cross_ln;
-    norm_split_kernel<<<M, 256, 0, st>>>(nc);
-    LAT_TRY(launch_check("norm_split"));
+    LAT_TRY(enqueue_norm(nc, M, st));
     {
       DenseArgs a{};
       a.M = M; a.N = D; a.K = D; a.terms = c->act_terms; a.w_row0 = l * D; a.epi = E_STORE; a.out = c->qbuf;
@@ -1486,8 +1494,7 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
     na.shift_off[b] = ch[b].step * 6 * D + 3 * D;
     na.scale_off[b] = ch[b].step * 6 * D + 4 * D;
   }
-  norm_split_kernel<<<M, 256, 0, st>>>(na);
-  LAT_TRY(launch_check("norm_split"));
+  LAT_TRY(enqueue_norm(na, M, st));
   {
     DenseArgs a{};
     a.M = M; a.N = F; a.K = D; a.terms = c->act_terms; a.w_row0 = l * F; a.epi = E_GELU_SPLIT; a.act2 = c->act2f; a.ldh = F;
@@ -1802,8 +1809,7 @@ lat_status lat_dit_set_text(lat_ctx* c, int sid, const void* text, void* stream)
   LAT_TRY(launch_check("text bf16 -> fp32"));
   NormArgs na{};
   na.x = c->qkvbuf; na.D = D; na.mode = NORM_NONE; na.eps = d.eps; na.rows_per_chunk = Tt; na.act2 = c->act2;
-  norm_split_kernel<<<Tt, 256, 0, st>>>(na);
-  LAT_TRY(launch_check("norm_split"));
+  LAT_TRY(enqueue_norm(na, Tt, st));
   for (int l = 0; l < d.L; ++l) {   // k | v of every block, fp32, then their fp16 planes
     DenseArgs a{};
     a.M = Tt; a.N = 2 * D; a.K = D; a.terms = kActTerms; a.w_row0 = l * 2 * D; a.epi = E_STORE; a.out = c->qkvbuf;
