@@ -144,6 +144,23 @@ def test_dit_pages_equal_contiguous_ring(wan):
     assert np.array_equal(out[False][2], out[True][2]), "paged ring contents differ from the contiguous ring's"
 
 
+@pytest.mark.parametrize("grid,paged", [(None, False), (None, True), ((2, 5), True)],
+                         ids=["1d", "1d_pages8", "3d_pages8"])
+def test_dit_short_chunks_parity(grid, paged):
+    """Chunks of 20 tokens: a 32-row group of the QKV epilogue spans two or three
+    chunks (the per-row rotation table's fallback for a third chunk, the chunk walk
+    of the cache stores), and pages of 8 tokens put several page boundaries inside
+    one warp's rows; 3-D RoPE over two 2 x 5 frames per chunk."""
+    base = dict(D=256, H=2, dh=128, F=512, L=2, T_chunk=20, t_dim=64)
+    if grid:
+        base.update(grid_h=grid[0], grid_w=grid[1], text_len=16, lat_dim=16)
+    cfg = synth.config("dit_1p3b", **base, page_tokens=8 if paged else 0)
+    descs = [(0, 7, 0), (0, 6, 1), (0, 5, 2), (0, 4, 3), (1, 2, 0)]   # 100 rows, 5 chunks
+    got_x, ref_x, got_ring, ref_ring, ring_in = _wan_case(cfg, descs, streams=2, layer=1, paged=paged)
+    assert_rel(got_x, ref_x, BLOCK_TOL, "dit short chunks block residual")
+    _check_ring(cfg, descs, 2, got_ring, ref_ring, ring_in, "dit short chunks")
+
+
 def test_dit_wan_1p3b_sampled_rows():
     """The 1.3B block with one 30 x 52 frame per chunk, 512 text tokens and
     pages of 256 tokens: the steady-state batch of four chunks on sampled rows
