@@ -163,7 +163,8 @@ def attention_spread(tr: np.ndarray):
 def report(tr: np.ndarray, out=sys.stdout):
     work, bar, sub = phase_table(tr)
     mw = np.median(work, axis=0)
-    mb = np.nanmedian(bar, axis=0)
+    # the last phase of the last block has no next phase: its column may be all NaN
+    mb = np.array([np.nanmedian(c) if np.isfinite(c).any() else np.nan for c in bar.T])
     print("| phase | work us | barrier us |", file=out)
     print("|---|---|---|", file=out)
     for i, (name, _, _) in enumerate(PHASES):
@@ -227,8 +228,9 @@ def main():
     m.ctx.debug_trace(None)
     # every step of the chunk's launch writes the same slots: the last one stays
     tr = buf.view(cfg["L"], grid, 64).cpu().numpy()
+    ctas = int((tr[0] != 0).any(axis=1).sum())   # the buffer has a row per SM; the launch uses fewer CTAs
     print(f"step kernel phases, workload {args.workload}: {cfg['L']} blocks of the last denoise step, "
-          f"grid {grid}")
+          f"{ctas} CTAs")
     report(tr)
 
 
