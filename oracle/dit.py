@@ -24,7 +24,7 @@ Readings where the pages are silent (listed in the design notes):
   ring's format), then runs attention for every chunk.  A chunk's history keys
   are the ring's bf16 values; its own keys enter its attention as computed.
   Two chunks of one call may not share a (stream, step, slot).
-* Latent in/out and the denoise step (silent on the pages; the survey's
+* Latent in/out and the denoise step (the pages are silent; the plainest
   reading): a chunk's latent z [T, A] enters the stage as x = z W_in + b_in, the
   L blocks run at its step s, v = x W_out + b_out, and z <- z + dt v with
   dt = 1 / S (the same grid t_s = s / S as the adaLN table).
