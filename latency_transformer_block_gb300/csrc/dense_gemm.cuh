@@ -303,10 +303,10 @@ __device__ __forceinline__ void rope_epilogue(const DenseArgs& a, float (&acc)[1
   const int D = r.heads * 128, hc = (n0 >> 7) & 1, t0 = n0 - hc * 128;
   const int part = t0 / D, col0 = t0 - part * D + hc * 32, b0 = row0 / r.T;
   float sc = a.out_scale;
-  if (part < 2) {
+  if (part < 2 && row0 < a.M) {   // warp-uniform: a warp wholly past M stores nothing
     rope_turn(acc, rv0, 0, sc);
     float4 rv1[8];
-    if (row0 < a.M) rope_rot_load(a, row0, hc, 1, lane, rv1);
+    rope_rot_load(a, row0, hc, 1, lane, rv1);
     rope_turn(acc, rv1, 1, sc);
     sc = 1.f;
   }
