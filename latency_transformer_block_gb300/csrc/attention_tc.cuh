@@ -655,24 +655,31 @@ struct HistCvtArgs {
   const __nv_bfloat16* pool;
 };
 
+// Contiguous rings: a grid-stride loop over 8-value chunks.  Pages: one warp
+// per (plane, row), the row's pool address resolved once through the page
+// table and its cols / 8 chunks taken by the lanes in turn (grid-stride over
+// planes x rows, 8 warps a CTA).
 static __global__ void __launch_bounds__(256) hist_to_f16_kernel(const __grid_constant__ HistCvtArgs a) {
-  const size_t per = (size_t)a.rows * a.cols / 8;   // 8-value chunks per plane
-  const size_t n = per * a.planes;
-  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
-    const int p = (int)(i / per);
-    const size_t j = i - (size_t)p * per;
-    const uint4* src;
-    if (a.page_tokens > 0) {   // 8 values never cross a row (cols is a multiple of 8)
-      const size_t e = 8 * j;
-      const int row = (int)(e / a.cols), P = a.page_tokens;
-      const int r = a.row0[p >> 1] + row;
-      const size_t off = (((size_t)a.ptab[p >> 1][r / P] * 2 + (p & 1)) * P + r % P) * a.cols + e % a.cols;
-      src = reinterpret_cast<const uint4*>(a.pool + off);
-    } else {
-      src = reinterpret_cast<const uint4*>(a.src[p]) + j;
+  if (a.page_tokens == 0) {
+    const size_t per = (size_t)a.rows * a.cols / 8;   // 8-value chunks per plane
+    const size_t n = per * a.planes;
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+      const int p = (int)(i / per);
+      const size_t j = i - (size_t)p * per;
+      reinterpret_cast<uint4*>(a.dst[p])[j] = bf16x8_to_f16x8(__ldcs(reinterpret_cast<const uint4*>(a.src[p]) + j));
     }
-    const uint4 v = __ldcs(src);
-    reinterpret_cast<uint4*>(a.dst[p])[j] = bf16x8_to_f16x8(v);
+    return;
+  }
+  const int lane = threadIdx.x & 31, c8 = a.cols / 8;   // cols is a multiple of 8
+  const long long tasks = (long long)a.planes * a.rows;
+  for (long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); t < tasks; t += (long long)gridDim.x * 8) {
+    const int p = (int)(t / a.rows), row = (int)(t - (long long)p * a.rows);
+    const int r = a.row0[p >> 1] + row, P = a.page_tokens;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.pool + (((size_t)a.ptab[p >> 1][r / P] * 2 + (p & 1)) * P + r % P) * (size_t)a.cols);
+    uint4* dst = reinterpret_cast<uint4*>(a.dst[p] + (size_t)row * a.cols);
+#pragma unroll 4
+    for (int c = lane; c < c8; c += 32) dst[c] = bf16x8_to_f16x8(__ldcs(src + c));
   }
 }
 

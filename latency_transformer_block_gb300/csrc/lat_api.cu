@@ -1444,8 +1444,9 @@ static lat_status enqueue_dit_block(lat_ctx* c, int l, float* x, const lat_chunk
   LAT_TRY(launch_check("rope_rows"));
   LAT_TRY(enqueue_dense(c, c->map_act_d, W_QKV, qa, st));
   if (hc.planes > 0) {   // after the ring rows are written: a chunk of this call may be another's history
-    const size_t chunks = (size_t)hc.planes * T * D / 8;
-    const unsigned grid = (unsigned)std::min<size_t>((chunks + 255) / 256, (size_t)c->num_sms * 8);
+    // contiguous: 256 chunks of 8 values a CTA; pages: one warp per (plane, row), 8 a CTA
+    const size_t work = P > 0 ? ((size_t)hc.planes * T + 7) / 8 : ((size_t)hc.planes * T * D / 8 + 255) / 256;
+    const unsigned grid = (unsigned)std::min<size_t>(work, (size_t)c->num_sms * 8);
     hist_to_f16_kernel<<<grid, 256, 0, st>>>(hc);
     LAT_TRY(launch_check("hist_to_f16"));
   }
